@@ -1,0 +1,60 @@
+"""Plant plausible mistakes in copies of the oracle and check the pins catch them.
+
+Each mutant is the oracle's C source with one textual change (a dropped term, a
+wrong sign, a wrong index, a transposed operand, an off-by-one), compiled to a
+temporary library on the CPU. The pins of oracle_pins must fail on every one.
+"""
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle
+import oracle_pins
+
+SRC = open(oracle._SRC).read()
+
+# (name, original text, replacement). Each original must occur exactly once.
+MUTANTS = [
+    ("group_index_modulo", "int g = h / (Hq / Hkv);", "int g = h % Hkv;"),
+    ("group_index_modulo_batch", "g = h / G;\n                const int L",
+     "g = h % Hkv;\n                const int L"),
+    ("no_max_subtraction", "w[t] = exp(w[t] - mx);", "w[t] = exp(w[t]);"),
+    ("flipped_exponent_sign", "w[t] = exp(w[t] - mx);", "w[t] = exp(mx - w[t]);"),
+    ("scale_dropped", "w[t] = scale * dot;", "w[t] = dot;"),
+    ("softmax_not_normalised", "for (int t = 0; t < L; ++t) w[t] /= sum;", ""),
+    ("cache_index_transposed",
+     "return c + (((size_t)b * (size_t)S_max + (size_t)t) * (size_t)Hkv + (size_t)g) * (size_t)D;",
+     "return c + (((size_t)b * (size_t)Hkv + (size_t)g) * (size_t)S_max + (size_t)t) * (size_t)D;"),
+    ("last_token_dropped", "for (int t = 0; t < L; ++t) {\n                    const uint16_t* vr",
+     "for (int t = 0; t < L - 1; ++t) {\n                    const uint16_t* vr"),
+    ("merge_rescale_dropped", "const double a = exp(m[j] - M);", "const double a = 1.0;"),
+    ("merge_denominator_unscaled", "denom += a * l[j];", "denom += l[j];"),
+    ("lse_missing_max", "return mx + log(sum);", "return log(sum);"),
+    ("append_wrong_row", "const size_t dst = (((size_t)b * S_max + (size_t)t) * Hkv + h) * (size_t)D;",
+     "const size_t dst = (((size_t)b * S_max + (size_t)(t > 0 ? t - 1 : t)) * Hkv + h) * (size_t)D;"),
+]
+
+
+@pytest.fixture(scope="module")
+def workdir():
+    with tempfile.TemporaryDirectory() as d:
+        yield d
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(name, old, new, workdir):
+    assert SRC.count(old) == 1, f"mutation site for {name} not unique/absent"
+    src = os.path.join(workdir, f"{name}.c")
+    with open(src, "w") as f:
+        f.write(SRC.replace(old, new))
+    lib_path = oracle.build(force=True, src=src, out=os.path.join(workdir, f"{name}.so"))
+    lib = oracle._load(lib_path)
+    failed = []
+    for check in oracle_pins.ALL_CHECKS:
+        try:
+            check(lib)
+        except (AssertionError, ValueError, FloatingPointError):
+            failed.append(check.__name__)
+    assert failed, f"no pin caught the planted mistake {name}"
