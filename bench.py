@@ -1,0 +1,435 @@
+#!/usr/bin/env python3
+"""Decode-step benchmark: KV append + split-KV decode attention + merge.
+
+One step = one pass of the whole hot path over one batch: append the new
+token's K/V to the cache, then decode attention over every sequence's cache.
+Default workload: the PaLM-540B-style multiquery decode step (batch 64, 48
+query heads over 1 KV head of 256, context 2048), one layer.
+
+Prints ONE JSON line (rank 0). `value` is KV GB/s (algorithmic bytes of the
+attention step: valid K/V rows + q + output, over the device time of the
+step). Throughput in tokens/s (batch / step time) is reported beside it.
+
+  python bench.py [--config palm] [--steps 50] [--warmup 5] [--impl ours|reference]
+
+Under torchrun (--gpus N > 1) every rank runs its own replica of the
+workload on its own GPU (the (sequence, KV head) units are independent, so
+no data-path collective exists); timing is bracketed by a barrier and the
+maximum over ranks is taken.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads  # noqa: E402
+from kv_cache_decode_gb300 import roofline  # noqa: E402
+
+METRIC = "decode-attention KV GB/s and % of GB300 HBM peak; decode tokens/s per shape"
+UNIT = "GB/s"
+CHUNK_SOURCES = ["split_kv_chunk.cuh", "split_kv_chunk_variants.cuh", "common.cuh", "schedule.cuh"]
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="palm", help="tiny|palm|mha|gqa|long|long_trialN")
+    ap.add_argument("--n-split", type=int, default=0, help="0 = heuristic")
+    ap.add_argument("--out-dtype", default="bf16", choices=["bf16", "f32"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")), ws
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def chunk_source_hash() -> str:
+    h = hashlib.sha256()
+    for name in CHUNK_SOURCES:
+        with open(os.path.join(ROOT, "kv_cache_decode_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(config: str):
+    """DRAM bytes per chunk-kernel launch from the committed ncu summary, or
+    None when that summary was taken on a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    want = chunk_source_hash()
+    for line in open(path):
+        if line.startswith("#") or not line.strip():
+            continue
+        kv = dict(x.split("=", 1) for x in line.split())
+        if kv.get("config") == config and kv.get("src_sha") == want:
+            return int(float(kv["dram_bytes_per_launch"]))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        self.t0 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        # nvidia-smi needs at least one sample period
+        while time.time() - self.t0 < 0.5:
+            time.sleep(0.05)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.file.flush()
+        self.file.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.file.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.file.name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline leg and the reference arm)
+# ---------------------------------------------------------------------------
+
+def oracle_rate(w, inp, budget_s: float, repeats: int = 1):
+    """Time the oracle on a bounded sample of sequences. Returns
+    (GB/s of algorithmic bytes, seconds per sample pass, rows, cores)."""
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
+    B = inp.q.shape[0]
+    kc, vc, _ = oracle.kv_append(inp.k_cache[:1], inp.v_cache[:1], inp.k_new[:1], inp.v_new[:1], inp.pos[:1])
+    t = time.perf_counter()
+    oracle.decode_attention(inp.q[:1], kc, vc, inp.seq_lens[:1], w.scale)
+    t1 = max(time.perf_counter() - t, 1e-4)
+    n = int(max(1, min(B, budget_s / t1)))
+    rows = np.arange(n)
+    kc, vc, _ = oracle.kv_append(inp.k_cache[rows], inp.v_cache[rows], inp.k_new[rows],
+                                 inp.v_new[rows], inp.pos[rows])
+    times = []
+    for _ in range(repeats):
+        t = time.perf_counter()
+        oracle.decode_attention(inp.q[rows], kc, vc, inp.seq_lens[rows], w.scale)
+        times.append(time.perf_counter() - t)
+    sec = statistics.median(times)
+    nbytes = roofline.attention_step_bytes(inp.seq_lens[rows], w.Hq, w.Hkv, w.D)
+    return nbytes / sec / 1e9, sec, n, cores
+
+
+def run_reference(args):
+    rank, _, _ = dist_env()
+    if rank != 0:
+        return
+    w = workloads.get(args.config)
+    # the oracle only needs the sampled rows; generate a handful of sequences
+    B_sample = min(w.B, 8)
+    inp = workloads.step_inputs(w, batch_index=range(B_sample), pad_bits=0)
+    per_step = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+    gbs_list = []
+    n_rows = cores = 0
+    for i in range(args.warmup + args.steps):
+        gbs, sec, n_rows, cores = oracle_rate(w, inp, per_step)
+        if i >= args.warmup:
+            gbs_list.append(gbs)
+    value = statistics.median(gbs_list)
+    step_bytes_full = roofline.attention_step_bytes(workloads.seq_lens(w), w.Hq, w.Hkv, w.D)
+    ms = step_bytes_full / (value * 1e9) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "batch": w.B,
+                   "n_heads_q": w.Hq, "n_heads_kv": w.Hkv, "head_dim": w.D},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"{n_rows} of {w.B} sequences per step (all heads), float64 C oracle"},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# Our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args):
+    import torch
+
+    import kv_cache_decode_gb300 as kvd
+
+    rank, local_rank, world = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    from kv_cache_decode_gb300 import _build
+    _build.build()
+    kvd.load()
+
+    w = workloads.get(args.config)
+    inp = workloads.step_inputs(w, pad_bits=0)
+    B, Hq, D = inp.q.shape
+    S, Hkv = inp.k_cache.shape[1], inp.k_cache.shape[2]
+    lens_np = inp.seq_lens
+    max_len = int(w.S_max)
+    step_bytes = roofline.attention_step_bytes(lens_np, Hq, Hkv, D)
+    kv_bytes = roofline.attention_kv_bytes(lens_np, Hkv, D)
+    append_bytes = roofline.append_bytes(B, Hkv, D)
+    flops = roofline.attention_step_flops(lens_np, Hq, D)
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
+    cache_bytes = 2 * inp.k_cache.nbytes
+    # Rotate cache copies so that each step's K/V rows are not L2-resident.
+    R = max(1, math.ceil(3 * l2 / max(kv_bytes, 1)))
+    R = max(1, min(R, int(40e9 // max(cache_bytes, 1)), 16))
+    kc0, vc0 = up(inp.k_cache), up(inp.v_cache)
+    kcs, vcs = [kc0], [vc0]
+    for _ in range(R - 1):
+        kcs.append(kc0.clone())
+        vcs.append(vc0.clone())
+    q, kn, vn = up(inp.q), up(inp.k_new), up(inp.v_new)
+    pos = torch.from_numpy(inp.pos).to(dev)
+    lens = torch.from_numpy(lens_np).to(dev)
+    out_t = torch.bfloat16 if args.out_dtype == "bf16" else torch.float32
+    out = torch.empty((B, Hq, D), dtype=out_t, device=dev)
+    n_split, ws_bytes = kvd.decode_plan(B, Hq, Hkv, D, max_len, 0, args.n_split, args.out_dtype)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    launches_per_step = 2 + (1 if n_split > 1 else 0)
+
+    def step(r, stream=None):
+        kvd.kv_append(kcs[r], vcs[r], kn, vn, pos, stream=stream)
+        kvd.decode_attention(q, kcs[r], vcs[r], lens, max_len, w.scale, out, workspace=ws,
+                             n_split=args.n_split, stream=stream)
+
+    for i in range(max(args.warmup, 3)):
+        step(i % R)
+    torch.cuda.synchronize()
+
+    # CUDA graphs: one per cache copy, replayed round-robin in the timed region.
+    graphs = []
+    cap_stream = torch.cuda.Stream(device=dev)
+    for r in range(R):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap_stream):
+            step(r)
+        graphs.append(g)
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    # ---- timed region: K whole steps ----
+    sampler = ClockSampler(local_rank)
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    for i in range(args.warmup):
+        graphs[i % R].replay()
+    barrier()
+    torch.cuda.synchronize()
+    ev0.record()
+    for i in range(args.steps):
+        graphs[i % R].replay()
+    ev1.record()
+    ev1.synchronize()
+    torch.cuda.synchronize()
+    barrier()
+    total_ms = ev0.elapsed_time(ev1)
+
+    # ---- chunk-kernel durations: events around each launch on its stream ----
+    stream = torch.cuda.current_stream()
+    ea = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    eb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda._sleep(int(2e6 + 2e5 * args.steps))  # let the host queue ahead of the GPU
+    for i in range(args.steps):
+        r = i % R
+        kvd.kv_append(kcs[r], vcs[r], kn, vn, pos)
+        ea[i].record(stream)
+        kvd.split_kv_chunk(q, kcs[r], vcs[r], lens, max_len, w.scale, out, workspace=ws,
+                           n_split=args.n_split)
+        eb[i].record(stream)
+        kvd.split_kv_merge(q, kcs[r], vcs[r], lens, max_len, w.scale, out, workspace=ws,
+                           n_split=args.n_split)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    chunk_ms = [a.elapsed_time(b) for a, b in zip(ea, eb)]
+    chunk_avg_ms = statistics.mean(chunk_ms)
+
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms, chunk_avg_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms, chunk_avg_ms = float(t[0]), float(t[1])
+
+    ms_per_step = total_ms / args.steps
+    value = world * step_bytes / (ms_per_step * 1e-3) / 1e9
+    tokens_per_s = world * B / (ms_per_step * 1e-3)
+
+    # ---- end to end through the public API with host buffers ----
+    e2e = None
+    if not args.no_e2e:
+        pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+        q_h = pin(inp.q.view(np.int16))
+        kn_h, vn_h = pin(inp.k_new.view(np.int16)), pin(inp.v_new.view(np.int16))
+        pos_h, lens_h = pin(inp.pos), pin(lens_np)
+        out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        h2d = q_h.nbytes + kn_h.nbytes + vn_h.nbytes + pos_h.nbytes + lens_h.nbytes
+        d2h = out_h.nbytes
+
+        def e2e_step(r):
+            q.view(torch.int16).copy_(q_h, non_blocking=True)
+            kn.view(torch.int16).copy_(kn_h, non_blocking=True)
+            vn.view(torch.int16).copy_(vn_h, non_blocking=True)
+            pos.copy_(pos_h, non_blocking=True)
+            lens.copy_(lens_h, non_blocking=True)
+            step(r)
+            out_h.copy_(out, non_blocking=True)
+
+        for i in range(args.warmup):
+            e2e_step(i % R)
+        torch.cuda.synchronize()
+        barrier()
+        t0 = time.perf_counter()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for i in range(args.steps):
+            e2e_step(i % R)
+        e1.record()
+        e1.synchronize()
+        wall_ms = (time.perf_counter() - t0) * 1e3
+        e2e_ms = max(e0.elapsed_time(e1), wall_ms) / args.steps
+        if world > 1:
+            import torch.distributed as dist
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            dist.all_reduce(t, op=dist.ReduceOp.MAX)
+            e2e_ms = float(t[0])
+        e2e = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e2e_ms, 4), "tokens_per_s": round(world * B / (e2e_ms * 1e-3), 1)}
+
+    if rank != 0:
+        return
+
+    peak, peak_kind = measured_peaks()
+    achieved = step_bytes / (chunk_avg_ms * 1e-3) / 1e9
+    traffic = ncu_traffic(w.name)
+    cpu = None
+    if not args.no_cpu_baseline:
+        gbs, sec, n_rows, cores = oracle_rate(w, inp, budget_s=10.0, repeats=1)
+        cpu = {"value": round(gbs, 5), "unit": UNIT, "cores": cores, "kind": "oracle",
+               "sample": f"{n_rows} of {B} sequences (all heads), float64 C oracle, {sec:.2f} s"}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": w.name, "description": w.description, "batch": B, "n_heads_q": Hq,
+                   "n_heads_kv": Hkv, "head_dim": D, "context": [int(lens_np.min()), int(lens_np.max())],
+                   "out_dtype": args.out_dtype, "n_split": n_split, "parallelism": f"replicas x{world}",
+                   "l2_flush": f"{R} rotating KV-cache copies ({R * kv_bytes / 1e6:.0f} MB of K/V rows "
+                               f"vs {l2 / 1e6:.0f} MB L2)",
+                   "timing": "CUDA graph per step, CUDA events on the replay stream"},
+        "tokens_per_s": round(tokens_per_s, 1),
+        "hbm_frac_of_step": round(value / world / peak, 4),
+        "step_bytes": int(step_bytes), "append_bytes": int(append_bytes), "flops": int(flops),
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "split_kv_chunk", "peak_source": f"{peak_kind} copy bandwidth",
+                     "kernel_ms": round(chunk_avg_ms, 5)},
+        "gpu_launches": int(launches_per_step * args.steps),
+        "clocks": clocks,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "impl": "ours",
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+    rank, _, world = dist_env()
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

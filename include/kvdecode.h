@@ -1,0 +1,216 @@
+/*
+ * kvdecode: one generation step of attention over a KV cache on one GB300.
+ *
+ * C ABI. Every pointer is plain memory owned by the caller (device memory
+ * unless stated otherwise); the library allocates nothing and keeps no state
+ * between calls, so it is reentrant. All GPU work is queued asynchronously on
+ * the caller's stream; no call synchronises with the host.
+ *
+ * Problem statement (page titles and sections of the sources):
+ *   - During generation each sequence produces one new token: its key and
+ *     value projections are appended to the KV cache, and its query attends
+ *     over every cached token (All About Transformer Inference, "Transformer
+ *     inference basics", the Generation bullet; "Implementation: JetStream",
+ *     the generate method).
+ *   - Cache layout K[B, S, K, H], V likewise: batch, sequence position, KV
+ *     head, head dimension (All About Transformer Inference, "Sharding the KV
+ *     cache"). Here: bf16 [batch, s_max, n_heads_kv, head_dim], contiguous.
+ *   - Query heads are grouped onto KV heads by the reshape [N] -> [K, M],
+ *     M = N / K: query head n reads KV head n / M (same section, attention
+ *     algorithm; multiquery attention is K = 1: Efficiently Scaling
+ *     Transformer Inference, section 3.3).
+ *   - Reads are ragged: only the first seq_lens[b] cached tokens of sequence b
+ *     are read (All About Transformer Inference, "Tricks for improving
+ *     generation throughput and latency", ragged HBM reads).
+ *
+ * Status handling: host-checkable faults are reported synchronously by the
+ * return value, before anything is launched. Values that live on the device
+ * (seq_lens, pos) cannot be checked on the host: out-of-range values are
+ * clamped or skipped by the kernels, which then set a bit in the optional
+ * device status word (never a trap).
+ */
+#ifndef KVDECODE_H
+#define KVDECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum kvd_status {
+    KVD_OK = 0,
+    KVD_ERR_INVALID_ARG = 1,          /* null/misaligned pointer, bad size or value */
+    KVD_ERR_UNSUPPORTED = 2,          /* valid but not implemented (head_dim, group size) */
+    KVD_ERR_WORKSPACE_TOO_SMALL = 3,  /* workspace_bytes below kvd_decode_plan's figure */
+    KVD_ERR_CUDA = 4                  /* a CUDA runtime call or launch failed */
+} kvd_status;
+
+typedef enum kvd_out_dtype {
+    KVD_OUT_BF16 = 0,  /* bf16 output, round-to-nearest-even from fp32 */
+    KVD_OUT_F32 = 1    /* fp32 output, with softmax weights carried to ~2^-17 */
+} kvd_out_dtype;
+
+/* cudaStream_t, passed as an opaque pointer (0 = the legacy default stream). */
+typedef void* kvd_stream_t;
+
+/* Bits of the optional device status word (int32, caller-owned, OR-ed in). */
+#define KVD_STATUS_SEQ_LEN_CLAMPED 0x1  /* some seq_lens[b] outside [0, min(s_max, max_seq_len)] */
+#define KVD_STATUS_POS_OUT_OF_RANGE 0x2 /* some pos[b] outside [0, s_max): that row not written */
+
+/* Supported shapes: head_dim in {64, 128, 256}; n_heads_q a multiple of
+ * n_heads_kv with group size n_heads_q / n_heads_kv <= 64. */
+#define KVD_MAX_GROUP 64
+
+/*
+ * kvd_decode_plan: split count and workspace size for kvd_decode_attention.
+ *
+ * The context of all (sequence, KV head) pairs is laid end to end and cut into
+ * n_split contiguous, equal runs of tokens, one per CTA; each run's partial
+ * softmax results are merged afterwards (All About Transformer Inference,
+ * "Sharding the KV cache", sequence sharding accumulated like Flash Attention;
+ * the split count adapts to shape and hardware as in the heuristic dataflow of
+ * FlashDecoding++). n_split_request = 0 picks the heuristic (one CTA per
+ * resident slot on num_sms SMs, capped by the work); > 0 forces that count.
+ * num_sms = 0 queries the current CUDA device (needs a GPU); > 0 uses it as
+ * given (host-only planning). max_seq_len is the largest seq_lens value the
+ * call may see (<= s_max).
+ * Outputs: *n_split_out (>= 1) and *workspace_bytes_out (0 when n_split is 1).
+ * Errors: KVD_ERR_INVALID_ARG for null outputs, non-positive sizes, a group
+ * that does not divide, max_seq_len < 0 or out_dtype unknown;
+ * KVD_ERR_UNSUPPORTED for head_dim / group size outside the list above;
+ * KVD_ERR_CUDA if num_sms = 0 and the device query fails.
+ */
+kvd_status kvd_decode_plan(int batch, int n_heads_q, int n_heads_kv, int head_dim,
+                           int max_seq_len, int num_sms, int n_split_request,
+                           kvd_out_dtype out_dtype,
+                           int* n_split_out, size_t* workspace_bytes_out);
+
+/*
+ * kvd_kv_append: write the new token's key and value rows into the cache.
+ *   k_cache[b, pos[b], h, :] = k_new[b, h, :]; v_cache likewise.
+ * (All About Transformer Inference, "Transformer inference basics": the new
+ * token's KV is appended to the KV cache.) A bit copy: no arithmetic.
+ *   k_cache, v_cache : bf16 [batch, s_max, n_heads_kv, head_dim], 16-byte aligned
+ *   k_new, v_new     : bf16 [batch, n_heads_kv, head_dim], 16-byte aligned
+ *   pos              : device int32 [batch], the pre-append length of each
+ *                      sequence; not modified. Rows with pos[b] outside
+ *                      [0, s_max) are skipped and flag KVD_STATUS_POS_OUT_OF_RANGE.
+ *   status_word      : optional device int32 (may be NULL).
+ * batch = 0 is a no-op. Errors: KVD_ERR_INVALID_ARG for null or misaligned
+ * pointers, negative sizes, head_dim not a multiple of 8; KVD_ERR_CUDA if the
+ * launch fails.
+ */
+kvd_status kvd_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                         const int32_t* pos, int batch, int s_max, int n_heads_kv,
+                         int head_dim, int32_t* status_word, kvd_stream_t stream);
+
+/*
+ * kvd_decode_attention: attention of one new token per sequence over its cache.
+ *   out[b, h, :] = sum_{t < L_b} softmax_t(scale * q[b, h, :] . K[b, t, g, :]) V[b, t, g, :]
+ *   with g = h / (n_heads_q / n_heads_kv) and L_b = seq_lens[b] (clamped),
+ * computed as the pages describe the fused attention: read q, read the K and
+ * V cache once, q.K, softmax over the sequence, weights times V, write the
+ * output, never writing the score matrix (All About Transformer Inference,
+ * "What about attention?"; the softmax is evaluated in base 2 with log2(e)
+ * folded into the scale, Efficiently Scaling Transformer Inference, section
+ * 3.5). The context is split into n_split runs whose partial softmax results
+ * (run maximum, sum of exponentials, unnormalised weighted sum of V) are
+ * merged by log-sum-exp.
+ *   q               : bf16 [batch, n_heads_q, head_dim], 16-byte aligned
+ *   k_cache/v_cache : bf16 [batch, s_max, n_heads_kv, head_dim], 16-byte aligned;
+ *                     only rows t < L_b are read
+ *   seq_lens        : device int32 [batch]; clamped to [0, min(s_max, max_seq_len)]
+ *                     (KVD_STATUS_SEQ_LEN_CLAMPED). L_b = 0 gives a zero row and
+ *                     lse = -inf.
+ *   scale           : finite softmax scale (typically 1/sqrt(head_dim))
+ *   n_split         : 0 = heuristic, else the count to use (see kvd_decode_plan)
+ *   workspace       : device scratch of at least kvd_decode_plan's bytes for the
+ *                     same (batch, heads, head_dim, max_seq_len, n_split,
+ *                     out_dtype), 256-byte aligned; may be NULL when that is 0.
+ *                     Contents need no initialisation and are not preserved.
+ *   out             : [batch, n_heads_q, head_dim], bf16 or fp32 per out_dtype,
+ *                     16-byte aligned
+ *   lse_out         : optional fp32 [batch, n_heads_q], natural-log
+ *                     log(sum_t exp(scale * q.k_t))
+ *   status_word     : optional device int32
+ * batch = 0 is a no-op. Call order for a generation step: kvd_kv_append with
+ * pos = old length, then this with seq_lens = old length + 1, same stream.
+ * Errors (nothing launched): KVD_ERR_INVALID_ARG for null or misaligned
+ * pointers, non-positive sizes, max_seq_len outside [0, s_max], a group that
+ * does not divide, a non-finite scale, n_split < 0 or an unknown out_dtype;
+ * KVD_ERR_UNSUPPORTED as for kvd_decode_plan; KVD_ERR_WORKSPACE_TOO_SMALL;
+ * KVD_ERR_CUDA if a launch fails.
+ */
+kvd_status kvd_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* seq_lens, int batch, int s_max, int max_seq_len,
+                                int n_heads_q, int n_heads_kv, int head_dim, float scale,
+                                int n_split, void* workspace, size_t workspace_bytes,
+                                void* out, kvd_out_dtype out_dtype, float* lse_out,
+                                int32_t* status_word, kvd_stream_t stream);
+
+/*
+ * The two launches of kvd_decode_attention, exposed separately so that each
+ * can be timed on its own. Arguments and errors are those of
+ * kvd_decode_attention; calling kvd_split_kv_chunk then kvd_split_kv_merge on
+ * one stream with the same arguments is exactly kvd_decode_attention.
+ *  - kvd_split_kv_chunk: every CTA streams its run of K/V rows and either
+ *    writes final rows (pairs it covers entirely) or partial (m, l, o) states
+ *    into the workspace.
+ *  - kvd_split_kv_merge: merges the partial states of every split pair by
+ *    log-sum-exp: M = max_j m_j, w_j = 2^(m_j - M), out = sum_j w_j o_j /
+ *    sum_j w_j l_j, skipping empty partials. A no-op when n_split is 1.
+ */
+kvd_status kvd_split_kv_chunk(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* seq_lens, int batch, int s_max, int max_seq_len,
+                              int n_heads_q, int n_heads_kv, int head_dim, float scale,
+                              int n_split, void* workspace, size_t workspace_bytes,
+                              void* out, kvd_out_dtype out_dtype, float* lse_out,
+                              int32_t* status_word, kvd_stream_t stream);
+kvd_status kvd_split_kv_merge(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* seq_lens, int batch, int s_max, int max_seq_len,
+                              int n_heads_q, int n_heads_kv, int head_dim, float scale,
+                              int n_split, void* workspace, size_t workspace_bytes,
+                              void* out, kvd_out_dtype out_dtype, float* lse_out,
+                              int32_t* status_word, kvd_stream_t stream);
+
+/*
+ * kvd_schedule_describe: host-only replica of the device work schedule, for
+ * inspection and tests (no GPU needed). seq_lens_host is HOST int32 [batch].
+ * Writes up to max_rows rows of 8 int32 each to rows_out:
+ *   {cta, b, h, tok_lo, tok_hi, kind, slot, c_last}
+ * one row per segment (a CTA's tokens [tok_lo, tok_hi) of pair (b, h)) and one
+ * per empty pair, where kind is 0 = final (the CTA owns and covers the pair),
+ * 1 = partial written by the pair's owner, 2 = partial written by another CTA,
+ * 3 = empty pair (zero output). slot is the partial's workspace slot (-1 if
+ * none); c_last is the last CTA contributing to the pair (owner rows of kind 1).
+ * *n_rows_out receives the total number of rows (even if > max_rows) and
+ * *n_split_eff_out the number of CTAs that do work. Errors as kvd_decode_plan.
+ */
+kvd_status kvd_schedule_describe(const int32_t* seq_lens_host, int batch, int s_max,
+                                 int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim,
+                                 int n_split, kvd_out_dtype out_dtype,
+                                 int32_t* rows_out, int max_rows, int* n_rows_out,
+                                 int* n_split_eff_out);
+
+/*
+ * kvd_kernel_info: launch shape of the attention kernel chosen for a shape:
+ * threads per CTA, dynamic shared memory bytes, tokens per pipeline tile and
+ * the CTAs per SM the heuristic assumes. Host only. Errors as kvd_decode_plan.
+ */
+kvd_status kvd_kernel_info(int n_heads_q, int n_heads_kv, int head_dim, kvd_out_dtype out_dtype,
+                           int* threads_out, int* smem_bytes_out, int* tile_tokens_out,
+                           int* ctas_per_sm_out);
+
+/* Human-readable name of a status code (static string). */
+const char* kvd_status_string(kvd_status s);
+
+/* Library version string (static). */
+const char* kvd_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVDECODE_H */

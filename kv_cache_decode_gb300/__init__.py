@@ -1,1 +1,264 @@
-"""Single-token decode attention over a KV cache for GB300 (sm_103a)."""
+"""Single-token decode attention over a KV cache on GB300 (sm_103a).
+
+Thin ctypes binding over ``libkvdecode.so`` (C ABI declared in
+``include/kvdecode.h``). Every step of the path runs in the library's CUDA
+kernels; this module only checks tensor metadata and marshals pointers and
+sizes. PyTorch supplies device memory and streams. There is no CPU fallback:
+if the library is missing or stale, loading fails with an error.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional, Tuple
+
+import numpy as np
+
+from . import roofline  # noqa: F401  (host-side byte model)
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libkvdecode.so")
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA = range(5)
+OUT_BF16, OUT_F32 = 0, 1
+STATUS_SEQ_LEN_CLAMPED = 0x1
+STATUS_POS_OUT_OF_RANGE = 0x2
+
+# Every symbol include/kvdecode.h declares.
+EXPORTED = (
+    "kvd_decode_plan", "kvd_kv_append", "kvd_decode_attention", "kvd_split_kv_chunk",
+    "kvd_split_kv_merge", "kvd_schedule_describe", "kvd_kernel_info", "kvd_status_string",
+    "kvd_version",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KvdError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+def load(path: str = LIB_PATH):
+    """Load libkvdecode.so. Raises if it has not been built (no fallback)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"{path} is missing: build it with `python -m kv_cache_decode_gb300._build` "
+                "(or __graft_entry__.build()); there is no CPU fallback")
+        from . import _build
+        if path == LIB_PATH and not _build.up_to_date():
+            raise RuntimeError(f"{path} is older than its sources: rebuild it")
+        _lib = _declare(ctypes.CDLL(path))
+        return _lib
+
+
+def _declare(lib):
+    P, I, F, SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+    PI, PSZ = ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_size_t)
+    lib.kvd_decode_plan.argtypes = [I, I, I, I, I, I, I, I, PI, PSZ]
+    lib.kvd_kv_append.argtypes = [P, P, P, P, P, I, I, I, I, P, P]
+    dec = [P, P, P, P, I, I, I, I, I, I, F, I, P, SZ, P, I, P, P, P]
+    for name in ("kvd_decode_attention", "kvd_split_kv_chunk", "kvd_split_kv_merge"):
+        getattr(lib, name).argtypes = dec
+    lib.kvd_schedule_describe.argtypes = [P, I, I, I, I, I, I, I, I, P, I, PI, PI]
+    lib.kvd_kernel_info.argtypes = [I, I, I, I, PI, PI, PI, PI]
+    lib.kvd_status_string.argtypes = [I]
+    lib.kvd_status_string.restype = ctypes.c_char_p
+    lib.kvd_version.argtypes = []
+    lib.kvd_version.restype = ctypes.c_char_p
+    for name in EXPORTED[:7]:
+        getattr(lib, name).restype = I
+    return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load().kvd_status_string(int(status)).decode()
+    except Exception:  # pragma: no cover - library missing
+        return "status"
+
+
+def version() -> str:
+    return load().kvd_version().decode()
+
+
+def _out_code(out_dtype) -> int:
+    if out_dtype in (OUT_BF16, "bf16", "bfloat16"):
+        return OUT_BF16
+    if out_dtype in (OUT_F32, "f32", "float32", "fp32"):
+        return OUT_F32
+    import torch
+    if out_dtype is torch.bfloat16:
+        return OUT_BF16
+    if out_dtype is torch.float32:
+        return OUT_F32
+    raise ValueError(f"unknown out_dtype {out_dtype!r}")
+
+
+def _check(rc: int, what: str):
+    if rc != OK:
+        raise KvdError(rc, what)
+
+
+def _ptr(t) -> Optional[int]:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    h = stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+    return h or None
+
+
+# ---------------------------------------------------------------------------
+# Host-only queries
+# ---------------------------------------------------------------------------
+
+def decode_plan(batch: int, n_heads_q: int, n_heads_kv: int, head_dim: int, max_seq_len: int,
+                num_sms: int = 0, n_split: int = 0, out_dtype="bf16") -> Tuple[int, int]:
+    """(n_split, workspace_bytes) for a decode_attention call of this shape."""
+    lib = load()
+    n = ctypes.c_int(0)
+    ws = ctypes.c_size_t(0)
+    _check(lib.kvd_decode_plan(batch, n_heads_q, n_heads_kv, head_dim, max_seq_len, num_sms,
+                               n_split, _out_code(out_dtype), ctypes.byref(n), ctypes.byref(ws)),
+           "kvd_decode_plan")
+    return n.value, ws.value
+
+
+def kernel_info(n_heads_q: int, n_heads_kv: int, head_dim: int, out_dtype="bf16") -> dict:
+    lib = load()
+    th, sm, tt, cps = (ctypes.c_int(0) for _ in range(4))
+    _check(lib.kvd_kernel_info(n_heads_q, n_heads_kv, head_dim, _out_code(out_dtype),
+                               ctypes.byref(th), ctypes.byref(sm), ctypes.byref(tt),
+                               ctypes.byref(cps)), "kvd_kernel_info")
+    return {"threads": th.value, "smem_bytes": sm.value, "tile_tokens": tt.value,
+            "ctas_per_sm": cps.value}
+
+
+def schedule_describe(seq_lens, s_max: int, max_seq_len: int, n_heads_q: int, n_heads_kv: int,
+                      head_dim: int, n_split: int, out_dtype="bf16"):
+    """Host replica of the device schedule: (rows [n, 8] int32, n_split_eff).
+
+    Row = (cta, b, h, tok_lo, tok_hi, kind, slot, c_last); kind 0 final,
+    1 partial by owner, 2 partial by another CTA, 3 empty pair.
+    """
+    lib = load()
+    lens = np.ascontiguousarray(seq_lens, dtype=np.int32)
+    n_rows = ctypes.c_int(0)
+    eff = ctypes.c_int(0)
+    args = [lens.ctypes.data_as(ctypes.c_void_p), int(lens.size), s_max, max_seq_len, n_heads_q,
+            n_heads_kv, head_dim, n_split, _out_code(out_dtype)]
+    _check(lib.kvd_schedule_describe(*args, None, 0, ctypes.byref(n_rows), ctypes.byref(eff)),
+           "kvd_schedule_describe")
+    rows = np.zeros((max(n_rows.value, 1), 8), dtype=np.int32)
+    _check(lib.kvd_schedule_describe(*args, rows.ctypes.data_as(ctypes.c_void_p), n_rows.value,
+                                     ctypes.byref(n_rows), ctypes.byref(eff)),
+           "kvd_schedule_describe")
+    return rows[:n_rows.value], eff.value
+
+
+# ---------------------------------------------------------------------------
+# GPU entry points (torch CUDA tensors in, results written in place)
+# ---------------------------------------------------------------------------
+
+def _require(t, name, dtype=None, ndim=None):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be on a CUDA device")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if ndim is not None and t.dim() != ndim:
+        raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
+
+
+def kv_append(k_cache, v_cache, k_new, v_new, pos, status=None, stream=None):
+    """k_cache[b, pos[b], h, :] = k_new[b, h, :] (and V), on the GPU."""
+    import torch
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _require(t, n, torch.bfloat16, 4)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _require(t, n, torch.bfloat16, 3)
+    _require(pos, "pos", torch.int32, 1)
+    B, S, Hkv, D = k_cache.shape
+    if v_cache.shape != k_cache.shape or k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) \
+            or pos.shape != (B,):
+        raise ValueError("kv_append: inconsistent shapes")
+    _check(load().kvd_kv_append(k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(),
+                                v_new.data_ptr(), pos.data_ptr(), B, S, Hkv, D, _ptr(status),
+                                _stream_handle(stream)), "kvd_kv_append")
+
+
+def _decode_args(q, k_cache, v_cache, seq_lens, max_seq_len, scale, n_split, workspace, out,
+                 lse, status, stream):
+    import torch
+    _require(q, "q", torch.bfloat16, 3)
+    _require(k_cache, "k_cache", torch.bfloat16, 4)
+    _require(v_cache, "v_cache", torch.bfloat16, 4)
+    _require(seq_lens, "seq_lens", torch.int32, 1)
+    _require(out, "out", None, 3)
+    B, Hq, D = q.shape
+    _, S, Hkv, Dk = k_cache.shape
+    if k_cache.shape[0] != B or Dk != D or v_cache.shape != k_cache.shape or \
+            seq_lens.shape != (B,) or out.shape != (B, Hq, D):
+        raise ValueError("decode_attention: inconsistent shapes")
+    if out.dtype == torch.bfloat16:
+        code = OUT_BF16
+    elif out.dtype == torch.float32:
+        code = OUT_F32
+    else:
+        raise TypeError("out must be bfloat16 or float32")
+    if lse is not None:
+        _require(lse, "lse", torch.float32, 2)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(),
+                                                           workspace.numel() * workspace.element_size())
+    return [q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), seq_lens.data_ptr(), B, S,
+            int(max_seq_len), Hq, Hkv, D, float(scale), int(n_split), ws_ptr, ws_bytes,
+            out.data_ptr(), code, _ptr(lse), _ptr(status), _stream_handle(stream)]
+
+
+def alloc_workspace(q, k_cache, max_seq_len: int, n_split: int = 0, out_dtype="bf16"):
+    """A device workspace big enough for decode_attention with these arguments."""
+    import torch
+    B, Hq, D = q.shape
+    Hkv = k_cache.shape[2]
+    with torch.cuda.device(q.device):
+        _, nbytes = decode_plan(B, Hq, Hkv, D, max_seq_len, 0, n_split, out_dtype)
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=q.device)
+
+
+def decode_attention(q, k_cache, v_cache, seq_lens, max_seq_len: int, scale: float, out,
+                     workspace=None, n_split: int = 0, lse=None, status=None, stream=None):
+    """out[b, h] = softmax(scale * q[b, h] . K[b, :L_b, h // G]) V[b, :L_b, h // G]."""
+    args = _decode_args(q, k_cache, v_cache, seq_lens, max_seq_len, scale, n_split, workspace,
+                        out, lse, status, stream)
+    _check(load().kvd_decode_attention(*args), "kvd_decode_attention")
+
+
+def split_kv_chunk(q, k_cache, v_cache, seq_lens, max_seq_len: int, scale: float, out,
+                   workspace=None, n_split: int = 0, lse=None, status=None, stream=None):
+    """First launch of decode_attention only (the split-KV chunk kernel)."""
+    args = _decode_args(q, k_cache, v_cache, seq_lens, max_seq_len, scale, n_split, workspace,
+                        out, lse, status, stream)
+    _check(load().kvd_split_kv_chunk(*args), "kvd_split_kv_chunk")
+
+
+def split_kv_merge(q, k_cache, v_cache, seq_lens, max_seq_len: int, scale: float, out,
+                   workspace=None, n_split: int = 0, lse=None, status=None, stream=None):
+    """Second launch of decode_attention only (the log-sum-exp merge kernel)."""
+    args = _decode_args(q, k_cache, v_cache, seq_lens, max_seq_len, scale, n_split, workspace,
+                        out, lse, status, stream)
+    _check(load().kvd_split_kv_merge(*args), "kvd_split_kv_merge")

@@ -1,0 +1,351 @@
+// C ABI of libkvdecode: argument validation, planning and launches.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+#include "../../include/kvdecode.h"
+#include "params.h"
+#include "schedule.cuh"
+
+namespace kvd {
+
+const ChunkKernel* chunk_table_d64(int ht, bool f32);
+const ChunkKernel* chunk_table_d128(int ht, bool f32);
+const ChunkKernel* chunk_table_d256(int ht, bool f32);
+
+const ChunkKernel* find_chunk_kernel(int head_dim, int head_tiles, bool f32_out) {
+    switch (head_dim) {
+        case 64: return chunk_table_d64(head_tiles, f32_out);
+        case 128: return chunk_table_d128(head_tiles, f32_out);
+        case 256: return chunk_table_d256(head_tiles, f32_out);
+        default: return nullptr;
+    }
+}
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_num_sms[kMaxDevices];
+// Bit i of g_smem_ready[dev] is set once kernel variant i may use its
+// dynamic shared memory size on device dev.
+std::atomic<uint64_t> g_smem_ready[kMaxDevices];
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+kvd_status check_shape(int batch, int Hq, int Hkv, int D, kvd_out_dtype dt) {
+    if (batch < 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return KVD_ERR_INVALID_ARG;
+    if (Hq % Hkv != 0) return KVD_ERR_INVALID_ARG;
+    if (dt != KVD_OUT_BF16 && dt != KVD_OUT_F32) return KVD_ERR_INVALID_ARG;
+    if (D != 64 && D != 128 && D != 256) return KVD_ERR_UNSUPPORTED;
+    if (Hq / Hkv > KVD_MAX_GROUP) return KVD_ERR_UNSUPPORTED;
+    return KVD_OK;
+}
+
+const ChunkKernel* pick_kernel(int Hq, int Hkv, int D, kvd_out_dtype dt) {
+    const int G = Hq / Hkv;
+    return find_chunk_kernel(D, (G + 15) / 16, dt == KVD_OUT_F32);
+}
+
+int kernel_index(const ChunkKernel* k) {
+    const int d = (k->head_dim == 64) ? 0 : (k->head_dim == 128 ? 1 : 2);
+    return (d * 4 + (k->head_tiles - 1)) * 2 + (k->f32_out ? 1 : 0);
+}
+
+kvd_status device_sms(int* sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KVD_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return KVD_ERR_CUDA;
+    int v = g_num_sms[dev].load(std::memory_order_relaxed);
+    if (v <= 0) {
+        if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+            return KVD_ERR_CUDA;
+        g_num_sms[dev].store(v, std::memory_order_relaxed);
+    }
+    *sms = v;
+    return KVD_OK;
+}
+
+// Split count: one CTA per resident slot, but no fewer than two pipeline tiles
+// of work per CTA for short or small batches.
+int heuristic_split(const ChunkKernel* k, int batch, int Hkv, int max_len, int num_sms) {
+    const long long upper = (long long)batch * Hkv * max_len;  // tokens, an upper bound
+    const long long slots = (long long)num_sms * k->ctas_per_sm;
+    const long long min_tokens = 2LL * k->tile_tokens;
+    const long long by_work = std::max(1LL, (upper + min_tokens - 1) / min_tokens);
+    return (int)std::max(1LL, std::min(slots, by_work));
+}
+
+size_t workspace_for(int n_split, int batch, int Hq, int Hkv, int D) {
+    if (n_split <= 1 || batch == 0) return 0;
+    const size_t P = (size_t)batch * Hkv, G = (size_t)(Hq / Hkv);
+    const size_t slots = (size_t)n_split + P - 1;
+    return align256(P * sizeof(int2)) + align256(slots * G * D * sizeof(float)) +
+           align256(slots * G * sizeof(float2));
+}
+
+kvd_status plan(int batch, int Hq, int Hkv, int D, int max_len, int num_sms, int n_split_req,
+                kvd_out_dtype dt, int* n_split, size_t* ws, const ChunkKernel** kern) {
+    kvd_status st = check_shape(batch, Hq, Hkv, D, dt);
+    if (st != KVD_OK) return st;
+    if (max_len < 0 || n_split_req < 0 || num_sms < 0) return KVD_ERR_INVALID_ARG;
+    const ChunkKernel* k = pick_kernel(Hq, Hkv, D, dt);
+    if (!k) return KVD_ERR_UNSUPPORTED;
+    int n = n_split_req;
+    if (n == 0) {
+        int sms = num_sms;
+        if (sms == 0) {
+            st = device_sms(&sms);
+            if (st != KVD_OK) return st;
+        }
+        n = heuristic_split(k, batch, Hkv, max_len, sms);
+    }
+    *n_split = n;
+    *ws = workspace_for(n, batch, Hq, Hkv, D);
+    if (kern) *kern = k;
+    return KVD_OK;
+}
+
+enum Phase { kBoth = 3, kChunk = 1, kMerge = 2 };
+
+kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_cache,
+                  const int32_t* seq_lens, int batch, int s_max, int max_seq_len, int Hq, int Hkv,
+                  int D, float scale, int n_split_req, void* workspace, size_t workspace_bytes,
+                  void* out, kvd_out_dtype dt, float* lse, int32_t* status, kvd_stream_t stream) {
+    kvd_status st = check_shape(batch, Hq, Hkv, D, dt);
+    if (st != KVD_OK) return st;
+    if (s_max <= 0 || max_seq_len < 0 || max_seq_len > s_max) return KVD_ERR_INVALID_ARG;
+    if (!std::isfinite(scale) || n_split_req < 0) return KVD_ERR_INVALID_ARG;
+    if (!q || !k_cache || !v_cache || !seq_lens || !out) return KVD_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
+        !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)) || (status && !aligned(status, 4)))
+        return KVD_ERR_INVALID_ARG;
+    if ((size_t)batch * s_max * Hkv * D > ((size_t)1 << 62)) return KVD_ERR_INVALID_ARG;
+
+    int n_split = 0;
+    size_t need = 0;
+    const ChunkKernel* k = nullptr;
+    st = plan(batch, Hq, Hkv, D, max_seq_len, 0 /* query device if heuristic */, n_split_req, dt,
+              &n_split, &need, &k);
+    if (st != KVD_OK) return st;
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need) return KVD_ERR_WORKSPACE_TOO_SMALL;
+        if (!aligned(workspace, 256)) return KVD_ERR_INVALID_ARG;
+    }
+    if (batch == 0) return KVD_OK;
+
+    DecodeParams p;
+    std::memset(&p, 0, sizeof p);
+    p.q = q;
+    p.k = k_cache;
+    p.v = v_cache;
+    p.seq_lens = seq_lens;
+    p.B = batch;
+    p.S_max = s_max;
+    p.len_cap = std::min(s_max, max_seq_len);
+    p.Hq = Hq;
+    p.Hkv = Hkv;
+    p.G = Hq / Hkv;
+    p.scale_log2 = scale * 1.4426950408889634f;
+    p.n_split = n_split;
+    p.out = out;
+    p.lse = lse;
+    p.status = status;
+    if (need > 0) {
+        const size_t P = (size_t)batch * Hkv, G = (size_t)p.G, slots = (size_t)n_split + P - 1;
+        uint8_t* w = static_cast<uint8_t*>(workspace);
+        p.ws_rec = reinterpret_cast<int2*>(w);
+        w += align256(P * sizeof(int2));
+        p.ws_o = reinterpret_cast<float*>(w);
+        w += align256(slots * G * D * sizeof(float));
+        p.ws_ml = reinterpret_cast<float2*>(w);
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+    if (phase & kChunk) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVD_ERR_CUDA;
+        const uint64_t bit = 1ull << kernel_index(k);
+        if (!(g_smem_ready[dev].load(std::memory_order_acquire) & bit)) {
+            if (cudaFuncSetAttribute(reinterpret_cast<const void*>(k->fn),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     k->smem_bytes) != cudaSuccess)
+                return KVD_ERR_CUDA;
+            g_smem_ready[dev].fetch_or(bit, std::memory_order_acq_rel);
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)n_split, 1, 1);
+        cfg.blockDim = dim3((unsigned)k->threads, 1, 1);
+        cfg.dynamicSmemBytes = (size_t)k->smem_bytes;
+        cfg.stream = s;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, k->fn, p) != cudaSuccess) return KVD_ERR_CUDA;
+    }
+    if ((phase & kMerge) && n_split > 1) {
+        if (launch_merge(p, D, dt == KVD_OUT_F32, s) != cudaSuccess) return KVD_ERR_CUDA;
+    }
+    return KVD_OK;
+}
+
+}  // namespace
+}  // namespace kvd
+
+using namespace kvd;
+
+extern "C" {
+
+kvd_status kvd_decode_plan(int batch, int n_heads_q, int n_heads_kv, int head_dim, int max_seq_len,
+                           int num_sms, int n_split_request, kvd_out_dtype out_dtype,
+                           int* n_split_out, size_t* workspace_bytes_out) {
+    if (!n_split_out || !workspace_bytes_out) return KVD_ERR_INVALID_ARG;
+    return plan(batch, n_heads_q, n_heads_kv, head_dim, max_seq_len, num_sms, n_split_request,
+                out_dtype, n_split_out, workspace_bytes_out, nullptr);
+}
+
+kvd_status kvd_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                         const int32_t* pos, int batch, int s_max, int n_heads_kv, int head_dim,
+                         int32_t* status_word, kvd_stream_t stream) {
+    if (batch < 0 || s_max < 0 || n_heads_kv <= 0 || head_dim <= 0 || head_dim % 8 != 0)
+        return KVD_ERR_INVALID_ARG;
+    if (!k_cache || !v_cache || !k_new || !v_new || !pos) return KVD_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_new, 16) ||
+        !aligned(v_new, 16) || !aligned(pos, 4) || (status_word && !aligned(status_word, 4)))
+        return KVD_ERR_INVALID_ARG;
+    if (batch == 0) return KVD_OK;
+    return launch_append(k_cache, v_cache, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim,
+                         status_word, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KVD_OK
+               : KVD_ERR_CUDA;
+}
+
+kvd_status kvd_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* seq_lens, int batch, int s_max, int max_seq_len,
+                                int n_heads_q, int n_heads_kv, int head_dim, float scale,
+                                int n_split, void* workspace, size_t workspace_bytes, void* out,
+                                kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                                kvd_stream_t stream) {
+    return decode(kBoth, q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q,
+                  n_heads_kv, head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype,
+                  lse_out, status_word, stream);
+}
+
+kvd_status kvd_split_kv_chunk(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* seq_lens, int batch, int s_max, int max_seq_len,
+                              int n_heads_q, int n_heads_kv, int head_dim, float scale, int n_split,
+                              void* workspace, size_t workspace_bytes, void* out,
+                              kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                              kvd_stream_t stream) {
+    return decode(kChunk, q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q,
+                  n_heads_kv, head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype,
+                  lse_out, status_word, stream);
+}
+
+kvd_status kvd_split_kv_merge(const void* q, const void* k_cache, const void* v_cache,
+                              const int32_t* seq_lens, int batch, int s_max, int max_seq_len,
+                              int n_heads_q, int n_heads_kv, int head_dim, float scale, int n_split,
+                              void* workspace, size_t workspace_bytes, void* out,
+                              kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                              kvd_stream_t stream) {
+    return decode(kMerge, q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q,
+                  n_heads_kv, head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype,
+                  lse_out, status_word, stream);
+}
+
+kvd_status kvd_schedule_describe(const int32_t* seq_lens_host, int batch, int s_max,
+                                 int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim,
+                                 int n_split, kvd_out_dtype out_dtype, int32_t* rows_out,
+                                 int max_rows, int* n_rows_out, int* n_split_eff_out) {
+    kvd_status st = check_shape(batch, n_heads_q, n_heads_kv, head_dim, out_dtype);
+    if (st != KVD_OK) return st;
+    if (s_max <= 0 || max_seq_len < 0 || max_seq_len > s_max || n_split <= 0 || max_rows < 0)
+        return KVD_ERR_INVALID_ARG;
+    if ((batch > 0 && !seq_lens_host) || !n_rows_out || (max_rows > 0 && !rows_out))
+        return KVD_ERR_INVALID_ARG;
+    const ChunkKernel* k = pick_kernel(n_heads_q, n_heads_kv, head_dim, out_dtype);
+    if (!k) return KVD_ERR_UNSUPPORTED;
+
+    struct HostLen {
+        const int32_t* lens;
+        int cap;
+        int operator()(int b) const { return clamp_len(lens[b], cap); }
+    };
+    const HostLen len{seq_lens_host, std::min(s_max, max_seq_len)};
+    long long total = 0;
+    for (int b = 0; b < batch; ++b) total += len(b);
+    total *= n_heads_kv;
+    const int C_eff = effective_ctas(n_split, total);
+    int rows = 0;
+    auto emit = [&](int c, int b, int h, int lo, int hi, int kind, int slot, int c_last) {
+        if (rows < max_rows) {
+            int32_t* r = rows_out + 8 * (size_t)rows;
+            r[0] = c; r[1] = b; r[2] = h; r[3] = lo; r[4] = hi; r[5] = kind; r[6] = slot; r[7] = c_last;
+        }
+        ++rows;
+    };
+    for (int c = 0; c < C_eff; ++c) {
+        Walker<HostLen> w(len, batch, n_heads_kv, k->tile_tokens, c, C_eff, total);
+        int b0 = batch;
+        long long cum = 0, cum0 = total;
+        for (int b = 0; b < batch; ++b) {
+            const int L = len(b);
+            if (is_first_seq_candidate(cum, L, n_heads_kv, w.S)) {
+                b0 = b;
+                cum0 = cum;
+                break;
+            }
+            cum += (long long)n_heads_kv * L;
+        }
+        w.start(b0, cum0);
+        auto on_empty = [&](int b, int h) { emit(c, b, h, 0, 0, 3, -1, c); };
+        Tile t;
+        int seg_lo = 0;
+        while (w.next(t, on_empty)) {
+            if (t.seg_start) seg_lo = t.tok_lo;
+            if (t.seg_end) {
+                const int pair = t.b * n_heads_kv + t.h;
+                if (t.full)
+                    emit(c, t.b, t.h, seg_lo, t.tok_hi, 0, -1, c);
+                else
+                    emit(c, t.b, t.h, seg_lo, t.tok_hi, t.owned ? 1 : 2, c + pair, t.c_last);
+            }
+        }
+        w.finish(on_empty);
+    }
+    *n_rows_out = rows;
+    if (n_split_eff_out) *n_split_eff_out = C_eff;
+    return KVD_OK;
+}
+
+kvd_status kvd_kernel_info(int n_heads_q, int n_heads_kv, int head_dim, kvd_out_dtype out_dtype,
+                           int* threads_out, int* smem_bytes_out, int* tile_tokens_out,
+                           int* ctas_per_sm_out) {
+    kvd_status st = check_shape(1, n_heads_q, n_heads_kv, head_dim, out_dtype);
+    if (st != KVD_OK) return st;
+    const ChunkKernel* k = pick_kernel(n_heads_q, n_heads_kv, head_dim, out_dtype);
+    if (!k) return KVD_ERR_UNSUPPORTED;
+    if (threads_out) *threads_out = k->threads;
+    if (smem_bytes_out) *smem_bytes_out = k->smem_bytes;
+    if (tile_tokens_out) *tile_tokens_out = k->tile_tokens;
+    if (ctas_per_sm_out) *ctas_per_sm_out = k->ctas_per_sm;
+    return KVD_OK;
+}
+
+const char* kvd_status_string(kvd_status s) {
+    switch (s) {
+        case KVD_OK: return "ok";
+        case KVD_ERR_INVALID_ARG: return "invalid argument";
+        case KVD_ERR_UNSUPPORTED: return "unsupported shape";
+        case KVD_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+        case KVD_ERR_CUDA: return "CUDA error";
+        default: return "unknown status";
+    }
+}
+
+const char* kvd_version(void) { return "kvdecode 0.1.0 (sm_103a)"; }
+
+}  // extern "C"

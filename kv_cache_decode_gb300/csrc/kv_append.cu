@@ -1,0 +1,56 @@
+// KV append: the new token's key and value rows are copied into the cache at
+// each sequence's current length (All About Transformer Inference,
+// "Transformer inference basics", Generation: the new token's KV is appended
+// to the KV cache). A bit copy in 16-byte vectors; no arithmetic.
+#include "../../include/kvdecode.h"
+#include "common.cuh"
+#include "params.h"
+
+namespace kvd {
+
+__global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_cache, uint4* __restrict__ v_cache,
+                                                       const uint4* __restrict__ k_new,
+                                                       const uint4* __restrict__ v_new,
+                                                       const int32_t* __restrict__ pos, int B,
+                                                       int S_max, int Hkv, int vec_per_row,
+                                                       int32_t* status) {
+    // Let the attention kernel that follows start its launch; it waits for
+    // this grid's writes before reading the cache.
+    pdl_launch_dependents();
+    const long long rows = (long long)B * Hkv;
+    const long long per_tensor = rows * vec_per_row;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < 2 * per_tensor;
+         i += (long long)gridDim.x * blockDim.x) {
+        const int which = (int)(i / per_tensor);
+        const long long r = i - which * per_tensor;
+        const long long row = r / vec_per_row;  // b * Hkv + h
+        const int ch = (int)(r - row * vec_per_row);
+        const int b = (int)(row / Hkv), h = (int)(row - (long long)b * Hkv);
+        const int t = __ldg(pos + b);
+        if (t < 0 || t >= S_max) {
+            if (status && which == 0 && h == 0 && ch == 0) atomicOr(status, KVD_STATUS_POS_OUT_OF_RANGE);
+            continue;
+        }
+        const long long dst = (((long long)b * S_max + t) * Hkv + h) * vec_per_row + ch;
+        if (which == 0)
+            k_cache[dst] = __ldg(k_new + r);
+        else
+            v_cache[dst] = __ldg(v_new + r);
+    }
+}
+
+cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                          const int32_t* pos, int B, int S_max, int Hkv, int D,
+                          int32_t* status, cudaStream_t stream) {
+    const int vec_per_row = D / 8;
+    const long long work = 2LL * B * Hkv * vec_per_row;
+    long long blocks = (work + 255) / 256;
+    if (blocks > 4096) blocks = 4096;
+    if (blocks < 1) blocks = 1;
+    kv_append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), static_cast<const uint4*>(k_new),
+        static_cast<const uint4*>(v_new), pos, B, S_max, Hkv, vec_per_row, status);
+    return cudaGetLastError();
+}
+
+}  // namespace kvd

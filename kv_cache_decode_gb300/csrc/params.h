@@ -1,0 +1,41 @@
+// Kernel parameter blocks and the host-side table of attention kernel variants.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace kvd {
+
+struct DecodeParams {
+    const void* q;        // bf16 [B, Hq, D]
+    const void* k;        // bf16 [B, S_max, Hkv, D]
+    const void* v;
+    const int32_t* seq_lens;
+    int B, S_max, len_cap, Hq, Hkv, G;
+    float scale_log2;     // scale * log2(e): scores are kept in base-2 units
+    int n_split;          // CTAs launched for the chunk kernel
+    void* out;            // bf16 or fp32 [B, Hq, D]
+    float* lse;           // optional fp32 [B, Hq]
+    int32_t* status;      // optional
+    int2* ws_rec;         // [B*Hkv] merge records; null when n_split == 1
+    float* ws_o;          // [slots, G, D] partial unnormalised outputs
+    float2* ws_ml;        // [slots, G] partial (max, sum), base-2 max
+};
+
+// One compiled variant of the split-KV chunk kernel.
+struct ChunkKernel {
+    void (*fn)(DecodeParams);
+    int head_dim, head_tiles, threads, smem_bytes, tile_tokens, ctas_per_sm;
+    bool f32_out;
+};
+
+// Lookup by head dimension, number of 16-row head tiles (1..4) and output type.
+const ChunkKernel* find_chunk_kernel(int head_dim, int head_tiles, bool f32_out);
+
+cudaError_t launch_merge(const DecodeParams& p, int head_dim, bool f32_out, cudaStream_t stream);
+cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                          const int32_t* pos, int B, int S_max, int Hkv, int D,
+                          int32_t* status, cudaStream_t stream);
+
+}  // namespace kvd

@@ -1,0 +1,479 @@
+// Split-KV chunk kernel: each CTA streams its run of the KV cache once and
+// computes, for the whole query-head group of every pair it touches, the
+// partial softmax state (running max m, sum of exponentials l, unnormalised
+// weighted sum of V rows o), writing either the final output (pairs it covers
+// entirely) or the partial state for the merge kernel.
+//
+// The fused attention follows All About Transformer Inference, "What about
+// attention?": read q, read the K and V rows once, q.K, softmax over the
+// sequence, weights times V, write the output, with the score matrix never
+// leaving the chip. The softmax is taken in base 2 with log2(e) folded into
+// the scale (Efficiently Scaling Transformer Inference, section 3.5). The
+// running-max update is the online form of the log-sum-exp merge used to
+// accumulate sequence-sharded KV (All About Transformer Inference, "Sharding
+// the KV cache"). K/V tiles are staged through a multi-buffered shared-memory
+// pipeline so loads of later tiles overlap compute on the current one (the
+// double-buffering idea of FlashDecoding++'s flat GEMM, here STAGES deep).
+//
+// Warp layout: HT head tiles of 16 query heads x TS token slices. Warp
+// (ht, ts) keeps q rows [16 ht, 16 ht + 16) of the group as mma A fragments in
+// registers, computes S = q K^T for tokens [ts*TW, (ts+1)*TW) of every tile
+// with m16n8k16 bf16 MMAs (fp32 accumulate), takes the online softmax in
+// registers and reuses P directly as the A operand of O += P V. At the end of
+// a segment the TS token slices are merged through shared memory.
+#pragma once
+
+#include <math_constants.h>
+
+#include "../../include/kvdecode.h"
+#include "common.cuh"
+#include "params.h"
+#include "schedule.cuh"
+
+namespace kvd {
+
+struct DevLen {
+    const int32_t* lens;
+    int cap;
+    KVD_HD int operator()(int b) const {
+#ifdef __CUDA_ARCH__
+        return clamp_len(__ldg(lens + b), cap);
+#else
+        return clamp_len(lens[b], cap);
+#endif
+    }
+};
+
+struct NoOp {
+    KVD_HD void operator()(int, int) const {}
+};
+
+template <int NW>
+__device__ __forceinline__ long long block_sum_ll(long long v, long long* sh) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) sh[warp] = v;
+    __syncthreads();
+    long long t = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) t += sh[w];
+    __syncthreads();
+    return t;
+}
+
+// Inclusive scan over the block; *total receives the block sum.
+template <int NW>
+__device__ __forceinline__ long long block_incl_scan_ll(long long v, long long* sh,
+                                                        long long* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        long long n = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += n;
+    }
+    if (lane == 31) sh[warp] = v;
+    __syncthreads();
+    long long pre = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        if (w < warp) pre += sh[w];
+        tot += sh[w];
+    }
+    __syncthreads();
+    *total = tot;
+    return v + pre;
+}
+
+template <int NW>
+__device__ __forceinline__ int block_min_int(int v, int* sh) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, off));
+    if (lane == 0) sh[warp] = v;
+    __syncthreads();
+    int m = sh[0];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) m = min(m, sh[w]);
+    __syncthreads();
+    return m;
+}
+
+template <int D, int HT, int TS, int TT, int STAGES>
+struct ChunkShape {
+    static constexpr int NW = HT * TS;
+    static constexpr int NT = NW * 32;
+    static constexpr int TW = TT / TS;  // tokens per warp per tile
+    static constexpr int NS = TW / 8;   // score n-tiles per warp
+    static constexpr int KS = D / 16;   // k-steps over the head dimension
+    static constexpr int ND = D / 8;    // output n-tiles (8 columns each)
+    static constexpr int CH = D / 8;    // 16-byte chunks per K/V row
+    static constexpr int TILE_ELEMS = TT * D;
+    static constexpr int STAGE_BYTES = 2 * TILE_ELEMS * 2;
+    static constexpr int MB_FLOATS_PER_WARP = (ND * 4 + 4) * 32;
+    static constexpr int MB_BYTES = (TS - 1) * HT * MB_FLOATS_PER_WARP * 4;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + MB_BYTES;
+    static_assert(TW % 16 == 0, "each warp needs whole 16-token k-steps");
+    static_assert(D % 16 == 0 && D >= 64, "head_dim");
+};
+
+template <int D, int HT, int TS, int TT, int STAGES, bool F32OUT, int MINB>
+__global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const DecodeParams p) {
+    using Sh = ChunkShape<D, HT, TS, TT, STAGES>;
+    constexpr int NW = Sh::NW, NT = Sh::NT, TW = Sh::TW, NS = Sh::NS, KS = Sh::KS,
+                  ND = Sh::ND, CH = Sh::CH, TILE_ELEMS = Sh::TILE_ELEMS;
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ long long s_red[NW];
+    __shared__ int s_redi[NW];
+    __shared__ long long s_cum0;
+
+    __nv_bfloat16* stages = reinterpret_cast<__nv_bfloat16*>(smem);
+    float* mbuf = reinterpret_cast<float*>(smem + STAGES * Sh::STAGE_BYTES);
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int ht = warp / TS, ts = warp % TS;
+    const int c = blockIdx.x;
+    const int G = p.G;
+
+    // Inputs may be produced by the previous kernel on the stream (the append).
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const DevLen len{p.seq_lens, p.len_cap};
+
+    // ---- total work and this CTA's token run ----
+    long long mine = 0;
+    bool clamped = false;
+    for (int b = tid; b < p.B; b += NT) {
+        const int raw = __ldg(p.seq_lens + b);
+        const int L = clamp_len(raw, p.len_cap);
+        clamped |= (raw != L);
+        mine += L;
+    }
+    if (clamped && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
+    const long long total = block_sum_ll<NW>(mine, s_red) * p.Hkv;
+    const int C_eff = effective_ctas(p.n_split, total);
+    if (c >= C_eff) return;
+    const long long S = run_begin(c, C_eff, total);
+
+    // ---- first sequence touching the run ----
+    int b0 = p.B;
+    long long cum0 = total;
+    {
+        long long base = 0;
+        for (int chunk = 0; chunk < p.B; chunk += NT) {
+            const int b = chunk + tid;
+            const int L = (b < p.B) ? len(b) : 0;
+            const long long v = (long long)L * p.Hkv;
+            long long ctot;
+            const long long cs = base + block_incl_scan_ll<NW>(v, s_red, &ctot) - v;
+            const bool cand = (b < p.B) && is_first_seq_candidate(cs, L, p.Hkv, S);
+            const int bmin = block_min_int<NW>(cand ? b : 0x7fffffff, s_redi);
+            if (bmin != 0x7fffffff) {
+                if (b == bmin) s_cum0 = cs;
+                __syncthreads();
+                b0 = bmin;
+                cum0 = s_cum0;
+                break;
+            }
+            base += ctot;
+        }
+    }
+
+    Walker<DevLen> lw(len, p.B, p.Hkv, TT, c, C_eff, total);
+    lw.start(b0, cum0);
+    Walker<DevLen> cw = lw;
+
+    const uint64_t policy = l2_evict_first_policy();
+    const __nv_bfloat16* Kg = reinterpret_cast<const __nv_bfloat16*>(p.k);
+    const __nv_bfloat16* Vg = reinterpret_cast<const __nv_bfloat16*>(p.v);
+    const size_t row_stride = (size_t)p.Hkv * D;  // elements between consecutive tokens
+
+    // Issue the cp.async copies of one tile's K and V rows into a stage.
+    // Row r of the stage holds token tok_lo + r; its 16-byte chunk ch is
+    // stored at chunk position ch ^ (r & 7), so that ldmatrix reads of 8
+    // consecutive rows hit 8 distinct bank groups.
+    auto issue = [&](const Tile& t, int stage) {
+        const int nvalid = t.tok_hi - t.tok_lo;
+        const size_t row0 = ((size_t)t.b * p.S_max + t.tok_lo) * p.Hkv + t.h;
+        const __nv_bfloat16* kb = Kg + row0 * D;
+        const __nv_bfloat16* vb = Vg + row0 * D;
+        const uint32_t sbase = smem_u32(stages) + stage * Sh::STAGE_BYTES;
+#pragma unroll 4
+        for (int i = tid; i < 2 * TT * CH; i += NT) {
+            const int kv = i / (TT * CH);
+            const int r = (i / CH) % TT;
+            const int ch = i % CH;
+            const __nv_bfloat16* base = kv ? vb : kb;
+            const bool ok = r < nvalid;
+            const __nv_bfloat16* src = ok ? base + (size_t)r * row_stride + ch * 8 : base;
+            const uint32_t dst = sbase + (uint32_t)((kv * TILE_ELEMS + r * D + ((ch ^ (r & 7)) * 8)) * 2);
+            cp_async_16(dst, src, ok ? 16 : 0, policy);
+        }
+    };
+
+    // Zero output for an empty pair this CTA owns.
+    auto write_empty = [&](int b, int h) {
+        const size_t row = (size_t)b * p.Hq + (size_t)h * G;
+        if constexpr (F32OUT) {
+            float* o = reinterpret_cast<float*>(p.out) + row * D;
+            for (int i = tid; i < G * D; i += NT) o[i] = 0.f;
+        } else {
+            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + row * D;
+            for (int i = tid; i < G * D; i += NT) o[i] = __float2bfloat16_rn(0.f);
+        }
+        if (p.lse)
+            for (int i = tid; i < G; i += NT) p.lse[row + i] = -CUDART_INF_F;
+        if (tid == 0 && p.ws_rec) p.ws_rec[(size_t)b * p.Hkv + h] = make_int2(-1, -1);
+    };
+
+    // ---- per-warp state ----
+    uint32_t qf[KS][4];
+    float o[ND][4];
+    float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+#pragma unroll
+    for (int n = 0; n < ND; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+#pragma unroll
+    for (int kk = 0; kk < KS; ++kk) qf[kk][0] = qf[kk][1] = qf[kk][2] = qf[kk][3] = 0u;
+
+    const int r0 = ht * 16 + (lane >> 2);  // group-local query heads of this thread's rows
+    const int r1 = r0 + 8;
+    const float scale_log2 = p.scale_log2;
+
+    // ---- prologue ----
+#pragma unroll
+    for (int s = 0; s < STAGES - 1; ++s) {
+        Tile t;
+        if (lw.next(t, NoOp{})) issue(t, s);
+        cp_async_commit();
+    }
+
+    int it = 0;
+    Tile ct;
+    while (cw.next(ct, write_empty)) {
+        cp_async_wait<STAGES - 2>();
+        __syncthreads();
+        {
+            Tile t;
+            if (lw.next(t, NoOp{})) issue(t, (it + STAGES - 1) % STAGES);
+            cp_async_commit();
+        }
+        const int stage = it % STAGES;
+        ++it;
+
+        if (ct.seg_start) {
+            const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(p.q) +
+                                      ((size_t)ct.b * p.Hq + (size_t)ct.h * G) * D;
+            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qb + (size_t)r0 * D);
+            const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qb + (size_t)r1 * D);
+            const bool v0 = r0 < G, v1 = r1 < G;
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                const int w = kk * 8 + (lane & 3);  // 32-bit word index of column kk*16 + 2*(lane&3)
+                qf[kk][0] = v0 ? __ldg(q0 + w) : 0u;
+                qf[kk][1] = v1 ? __ldg(q1 + w) : 0u;
+                qf[kk][2] = v0 ? __ldg(q0 + w + 4) : 0u;
+                qf[kk][3] = v1 ? __ldg(q1 + w + 4) : 0u;
+            }
+            m0 = m1 = -CUDART_INF_F;
+            l0 = l1 = 0.f;
+#pragma unroll
+            for (int n = 0; n < ND; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+        }
+
+        const int nvalid = ct.tok_hi - ct.tok_lo;
+        const int wbase = ts * TW;
+        if (wbase < nvalid) {
+            const uint32_t kbase = smem_u32(stages) + stage * Sh::STAGE_BYTES;
+            const uint32_t vbase = kbase + TILE_ELEMS * 2;
+
+            // S = q K^T over this warp's TW tokens.
+            float s[NS][4];
+#pragma unroll
+            for (int j = 0; j < NS; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+                for (int n2 = 0; n2 < NS / 2; ++n2) {
+                    const int row = wbase + n2 * 16 + ((lane >> 4) & 1) * 8 + (lane & 7);
+                    const int ch = kk * 2 + ((lane >> 3) & 1);
+                    uint32_t b0, b1, b2, b3;
+                    ldmatrix_x4(kbase + (uint32_t)((row * D + ((ch ^ (row & 7)) * 8)) * 2), b0, b1, b2, b3);
+                    mma_bf16_16816(s[2 * n2], qf[kk], b0, b1);
+                    mma_bf16_16816(s[2 * n2 + 1], qf[kk], b2, b3);
+                }
+            }
+
+            // Scale to base-2 units, mask tokens past the tile's end, row maxima.
+            float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
+#pragma unroll
+            for (int j = 0; j < NS; ++j) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int tok = wbase + j * 8 + (lane & 3) * 2 + (e & 1);
+                    s[j][e] = (tok < nvalid) ? s[j][e] * scale_log2 : -CUDART_INF_F;
+                }
+                mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
+                mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
+            }
+#pragma unroll
+            for (int off = 1; off <= 2; off <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+            }
+            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+            const float mu0 = (mn0 == -CUDART_INF_F) ? 0.f : mn0;
+            const float mu1 = (mn1 == -CUDART_INF_F) ? 0.f : mn1;
+            const float a0 = exp2f(m0 - mu0), a1 = exp2f(m1 - mu1);
+            m0 = mn0;
+            m1 = mn1;
+
+            // P = 2^(s - m) as bf16 A fragments (hi part; lo part for fp32 output).
+            uint32_t pa[NS / 2][4];
+            uint32_t pl[F32OUT ? NS / 2 : 1][4];
+            float ls0 = 0.f, ls1 = 0.f;
+#pragma unroll
+            for (int j = 0; j < NS; ++j) {
+                const float e0 = exp2f(s[j][0] - mu0), e1 = exp2f(s[j][1] - mu0);
+                const float e2 = exp2f(s[j][2] - mu1), e3 = exp2f(s[j][3] - mu1);
+                const uint32_t h01 = pack_bf16x2(e0, e1), h23 = pack_bf16x2(e2, e3);
+                pa[j >> 1][(j & 1) * 2 + 0] = h01;
+                pa[j >> 1][(j & 1) * 2 + 1] = h23;
+                if constexpr (F32OUT) {
+                    pl[j >> 1][(j & 1) * 2 + 0] = pack_bf16x2(e0 - bf16_lo(h01), e1 - bf16_hi(h01));
+                    pl[j >> 1][(j & 1) * 2 + 1] = pack_bf16x2(e2 - bf16_lo(h23), e3 - bf16_hi(h23));
+                    ls0 += e0 + e1;
+                    ls1 += e2 + e3;
+                } else {
+                    // The weights actually multiplied into V are the rounded ones;
+                    // summing those keeps the output an exact convex combination.
+                    ls0 += bf16_lo(h01) + bf16_hi(h01);
+                    ls1 += bf16_lo(h23) + bf16_hi(h23);
+                }
+            }
+            l0 = l0 * a0 + ls0;
+            l1 = l1 * a1 + ls1;
+            if (__any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f)) {
+#pragma unroll
+                for (int n = 0; n < ND; ++n) {
+                    o[n][0] *= a0;
+                    o[n][1] *= a0;
+                    o[n][2] *= a1;
+                    o[n][3] *= a1;
+                }
+            }
+
+            // O += P V.
+#pragma unroll
+            for (int k2 = 0; k2 < NS / 2; ++k2) {
+#pragma unroll
+                for (int n2 = 0; n2 < ND / 2; ++n2) {
+                    const int row = wbase + k2 * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                    const int ch = n2 * 2 + ((lane >> 4) & 1);
+                    uint32_t v0, v1, v2, v3;
+                    ldmatrix_x4_trans(vbase + (uint32_t)((row * D + ((ch ^ (row & 7)) * 8)) * 2), v0, v1, v2, v3);
+                    mma_bf16_16816(o[2 * n2], pa[k2], v0, v1);
+                    mma_bf16_16816(o[2 * n2 + 1], pa[k2], v2, v3);
+                    if constexpr (F32OUT) {
+                        mma_bf16_16816(o[2 * n2], pl[k2], v0, v1);
+                        mma_bf16_16816(o[2 * n2 + 1], pl[k2], v2, v3);
+                    }
+                }
+            }
+        }
+
+        if (ct.seg_end) {
+            // Row sums are spread over the 4 lanes of a quad.
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+            l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+            l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+            if constexpr (TS > 1) {
+                if (ts > 0) {
+                    float* mb = mbuf + ((ts - 1) * HT + ht) * Sh::MB_FLOATS_PER_WARP;
+#pragma unroll
+                    for (int n = 0; n < ND; ++n)
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) mb[(n * 4 + e) * 32 + lane] = o[n][e];
+                    mb[(ND * 4 + 0) * 32 + lane] = m0;
+                    mb[(ND * 4 + 1) * 32 + lane] = m1;
+                    mb[(ND * 4 + 2) * 32 + lane] = l0;
+                    mb[(ND * 4 + 3) * 32 + lane] = l1;
+                }
+                __syncthreads();
+                if (ts == 0) {
+#pragma unroll
+                    for (int t2 = 1; t2 < TS; ++t2) {
+                        const float* mb = mbuf + ((t2 - 1) * HT + ht) * Sh::MB_FLOATS_PER_WARP;
+                        const float om0 = mb[(ND * 4 + 0) * 32 + lane];
+                        const float om1 = mb[(ND * 4 + 1) * 32 + lane];
+                        const float ol0 = mb[(ND * 4 + 2) * 32 + lane];
+                        const float ol1 = mb[(ND * 4 + 3) * 32 + lane];
+                        const float M0 = fmaxf(m0, om0), M1 = fmaxf(m1, om1);
+                        const float A0 = exp2f(m0 - M0), B0 = exp2f(om0 - M0);
+                        const float A1 = exp2f(m1 - M1), B1 = exp2f(om1 - M1);
+                        l0 = A0 * l0 + B0 * ol0;
+                        l1 = A1 * l1 + B1 * ol1;
+                        m0 = M0;
+                        m1 = M1;
+#pragma unroll
+                        for (int n = 0; n < ND; ++n) {
+                            o[n][0] = A0 * o[n][0] + B0 * mb[(n * 4 + 0) * 32 + lane];
+                            o[n][1] = A0 * o[n][1] + B0 * mb[(n * 4 + 1) * 32 + lane];
+                            o[n][2] = A1 * o[n][2] + B1 * mb[(n * 4 + 2) * 32 + lane];
+                            o[n][3] = A1 * o[n][3] + B1 * mb[(n * 4 + 3) * 32 + lane];
+                        }
+                    }
+                }
+            }
+
+            if (ts == 0) {
+                const size_t pair = (size_t)ct.b * p.Hkv + ct.h;
+                const size_t qrow = (size_t)ct.b * p.Hq + (size_t)ct.h * G;
+                const bool v0 = r0 < G, v1 = r1 < G;
+                if (ct.full) {
+                    const float i0 = 1.f / l0, i1 = 1.f / l1;
+#pragma unroll
+                    for (int n = 0; n < ND; ++n) {
+                        const int d = n * 8 + (lane & 3) * 2;
+                        if constexpr (F32OUT) {
+                            float* out = reinterpret_cast<float*>(p.out);
+                            if (v0) *reinterpret_cast<float2*>(out + (qrow + r0) * D + d) = make_float2(o[n][0] * i0, o[n][1] * i0);
+                            if (v1) *reinterpret_cast<float2*>(out + (qrow + r1) * D + d) = make_float2(o[n][2] * i1, o[n][3] * i1);
+                        } else {
+                            __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+                            if (v0) *reinterpret_cast<uint32_t*>(out + (qrow + r0) * D + d) = pack_bf16x2(o[n][0] * i0, o[n][1] * i0);
+                            if (v1) *reinterpret_cast<uint32_t*>(out + (qrow + r1) * D + d) = pack_bf16x2(o[n][2] * i1, o[n][3] * i1);
+                        }
+                    }
+                    if (p.lse && (lane & 3) == 0) {
+                        if (v0) p.lse[qrow + r0] = (m0 + log2f(l0)) * 0.69314718055994531f;
+                        if (v1) p.lse[qrow + r1] = (m1 + log2f(l1)) * 0.69314718055994531f;
+                    }
+                    if (tid == 0 && p.ws_rec) p.ws_rec[pair] = make_int2(-1, -1);
+                } else {
+                    const size_t slot = (size_t)c + pair;
+                    float* wo = p.ws_o + slot * G * D;
+#pragma unroll
+                    for (int n = 0; n < ND; ++n) {
+                        const int d = n * 8 + (lane & 3) * 2;
+                        if (v0) *reinterpret_cast<float2*>(wo + (size_t)r0 * D + d) = make_float2(o[n][0], o[n][1]);
+                        if (v1) *reinterpret_cast<float2*>(wo + (size_t)r1 * D + d) = make_float2(o[n][2], o[n][3]);
+                    }
+                    if ((lane & 3) == 0) {
+                        if (v0) p.ws_ml[slot * G + r0] = make_float2(m0, l0);
+                        if (v1) p.ws_ml[slot * G + r1] = make_float2(m1, l1);
+                    }
+                    if (tid == 0 && ct.owned) p.ws_rec[pair] = make_int2(c, ct.c_last);
+                }
+            }
+            if constexpr (TS > 1) __syncthreads();
+        }
+    }
+    cw.finish(write_empty);
+    cp_async_wait<0>();
+}
+
+}  // namespace kvd

@@ -1,0 +1,149 @@
+"""The C ABI on the CPU: the library loads, exports every declared symbol, plans
+on the host, and rejects bad arguments with the documented status before any
+launch.
+
+Calls that pass fake (never dereferenced) device pointers are written so that
+argument validation fails first; no call here reaches a CUDA launch.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import kv_cache_decode_gb300 as kvd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kvdecode.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from kv_cache_decode_gb300 import _build
+    _build.build()
+    return kvd.load()
+
+
+def test_exports_every_declared_symbol(lib):
+    text = open(HEADER).read()
+    declared = set(re.findall(r"^\s*(?:kvd_status|const char\*)\s+(kvd_\w+)\s*\(", text, re.M))
+    assert declared == set(kvd.EXPORTED)
+    for name in declared:
+        assert hasattr(lib, name), name
+    assert kvd.version().startswith("kvdecode")
+
+
+def test_status_strings(lib):
+    for code in range(5):
+        assert kvd.status_string(code)
+    assert kvd.status_string(99) == "unknown status"
+
+
+@pytest.mark.parametrize("shape,expect", [
+    ((1, 8, 1, 128, 256), kvd.OK),
+    ((0, 8, 1, 128, 256), kvd.OK),
+    ((1, 8, 3, 128, 256), kvd.ERR_INVALID_ARG),    # group does not divide
+    ((1, 8, 1, 96, 256), kvd.ERR_UNSUPPORTED),     # head_dim
+    ((1, 130, 2, 128, 256), kvd.ERR_UNSUPPORTED),  # group 65 > 64
+    ((1, 0, 1, 128, 256), kvd.ERR_INVALID_ARG),
+    ((1, 8, 1, 128, -1), kvd.ERR_INVALID_ARG),
+    ((-1, 8, 1, 128, 256), kvd.ERR_INVALID_ARG),
+])
+def test_plan_validation(lib, shape, expect):
+    n = ctypes.c_int(0)
+    ws = ctypes.c_size_t(0)
+    rc = lib.kvd_decode_plan(*shape, 152, 0, 0, ctypes.byref(n), ctypes.byref(ws))
+    assert rc == expect
+
+
+def test_plan_null_outputs(lib):
+    assert lib.kvd_decode_plan(1, 8, 1, 128, 256, 152, 0, 0, None, None) == kvd.ERR_INVALID_ARG
+
+
+def test_plan_heuristic_and_workspace(lib):
+    # One CTA per resident slot, capped by the work; workspace formula.
+    for name, B, Hq, Hkv, D, L in [("palm", 64, 48, 1, 256, 2048), ("mha", 32, 40, 40, 128, 4096),
+                                    ("gqa", 128, 32, 8, 128, 8192), ("long", 4, 48, 1, 256, 65536)]:
+        info = kvd.kernel_info(Hq, Hkv, D)
+        n, ws = kvd.decode_plan(B, Hq, Hkv, D, L, num_sms=152)
+        assert n == 152 * info["ctas_per_sm"], name
+        G, P = Hq // Hkv, B * Hkv
+        slots = n + P - 1
+        r = lambda x: (x + 255) // 256 * 256
+        assert ws == r(P * 8) + r(slots * G * D * 4) + r(slots * G * 8), name
+    # tiny: capped by work (256 tokens, two tiles per CTA minimum)
+    info = kvd.kernel_info(8, 1, 128)
+    n, ws = kvd.decode_plan(1, 8, 1, 128, 256, num_sms=152)
+    assert n == 256 // (2 * info["tile_tokens"])
+    assert kvd.decode_plan(1, 8, 1, 128, 256, num_sms=152, n_split=1) == (1, 0)
+    assert kvd.decode_plan(2, 8, 1, 128, 256, num_sms=152, n_split=5)[0] == 5
+
+
+def test_kernel_info_fits_smem(lib):
+    for D in (64, 128, 256):
+        for G in (1, 4, 8, 16, 17, 32, 48, 64):
+            for dt in ("bf16", "f32"):
+                info = kvd.kernel_info(G, 1, D, dt)
+                assert info["smem_bytes"] <= 227 * 1024
+                assert info["smem_bytes"] * info["ctas_per_sm"] <= 228 * 1024
+                assert info["threads"] % 32 == 0
+
+
+FAKE = 0x100000  # aligned, never dereferenced: every call below fails validation first
+
+
+def _dec_args(**over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, lens=FAKE, B=2, S=64, maxlen=64, Hq=8, Hkv=2, D=128,
+             scale=0.088, n_split=4, ws=FAKE, ws_bytes=0, out=FAKE, dt=0, lse=None, status=None,
+             stream=None)
+    a.update(over)
+    return [a[k] for k in ("q", "k", "v", "lens", "B", "S", "maxlen", "Hq", "Hkv", "D", "scale",
+                           "n_split", "ws", "ws_bytes", "out", "dt", "lse", "status", "stream")]
+
+
+@pytest.mark.parametrize("fn", ["kvd_decode_attention", "kvd_split_kv_chunk", "kvd_split_kv_merge"])
+@pytest.mark.parametrize("over,expect", [
+    (dict(q=None), kvd.ERR_INVALID_ARG),
+    (dict(k=None), kvd.ERR_INVALID_ARG),
+    (dict(v=None), kvd.ERR_INVALID_ARG),
+    (dict(lens=None), kvd.ERR_INVALID_ARG),
+    (dict(out=None), kvd.ERR_INVALID_ARG),
+    (dict(q=FAKE + 8), kvd.ERR_INVALID_ARG),        # not 16-byte aligned
+    (dict(k=FAKE + 2), kvd.ERR_INVALID_ARG),
+    (dict(out=FAKE + 4), kvd.ERR_INVALID_ARG),
+    (dict(lens=FAKE + 2), kvd.ERR_INVALID_ARG),
+    (dict(B=-1), kvd.ERR_INVALID_ARG),
+    (dict(S=0), kvd.ERR_INVALID_ARG),
+    (dict(maxlen=65), kvd.ERR_INVALID_ARG),         # max_seq_len > s_max
+    (dict(maxlen=-1), kvd.ERR_INVALID_ARG),
+    (dict(Hq=7), kvd.ERR_INVALID_ARG),              # group does not divide
+    (dict(D=100), kvd.ERR_UNSUPPORTED),
+    (dict(Hq=130, Hkv=2), kvd.ERR_UNSUPPORTED),
+    (dict(scale=float("nan")), kvd.ERR_INVALID_ARG),
+    (dict(scale=float("inf")), kvd.ERR_INVALID_ARG),
+    (dict(n_split=-2), kvd.ERR_INVALID_ARG),
+    (dict(dt=7), kvd.ERR_INVALID_ARG),
+    (dict(ws_bytes=16), kvd.ERR_WORKSPACE_TOO_SMALL),
+    (dict(ws=None, ws_bytes=1 << 30), kvd.ERR_WORKSPACE_TOO_SMALL),
+    (dict(ws=FAKE + 16, ws_bytes=1 << 30), kvd.ERR_INVALID_ARG),  # workspace not 256-aligned
+])
+def test_decode_rejects(lib, fn, over, expect):
+    assert getattr(lib, fn)(*_dec_args(**over)) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((None, FAKE, FAKE, FAKE, FAKE, 2, 8, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE + 8, FAKE, 2, 8, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, None, 2, 8, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 1, 100, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, -1, 8, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 0, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, 0, 8, 1, 128, None, None), kvd.OK),  # batch 0: no-op
+])
+def test_append_rejects(lib, args, expect):
+    assert lib.kvd_kv_append(*args) == expect
+
+
+def test_decode_batch_zero_is_noop(lib):
+    assert lib.kvd_decode_attention(*_dec_args(B=0, n_split=3, ws=None)) == kvd.OK
