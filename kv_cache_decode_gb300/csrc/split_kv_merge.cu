@@ -23,8 +23,10 @@ __global__ void __launch_bounds__(128) split_kv_merge_kernel(const DecodeParams 
     const int lane = threadIdx.x & 31;
     const int G = p.G;
     if (g >= G) return;
-    const int2 rec = p.ws_rec[pair];
-    if (rec.x < 0) return;  // written in full by the chunk kernel
+    const int2 rec = __ldcg(p.ws_rec + pair);
+    // rec.x < 0: the chunk kernel wrote this pair in full. The range check
+    // keeps every slot read inside the workspace whatever its contents.
+    if (rec.x < 0 || rec.y < rec.x || rec.y >= p.n_split) return;
 
     float M = -CUDART_INF_F, L = 0.f;
     float acc[PER_LANE];
