@@ -11,7 +11,10 @@
   output), guard bands around the outputs and the workspace, and bitwise
   determinism across runs.
 Tolerances: bf16 output within 1e-2 (one bf16 step where that step exceeds
-1e-2); fp32 output within 1e-4.
+1e-2); fp32 output within 1e-4. The natural-log normaliser lse within 1e-4 in
+fp32 mode; in bf16 mode the normaliser sums the bf16-rounded weights (the ones
+multiplied into V, so that the output stays an exact convex combination of V
+rows), which carry up to 2^-9 relative rounding each, so lse is held to 2^-8.
 """
 import numpy as np
 import pytest
@@ -34,7 +37,8 @@ def _check(inp, r, out_dtype, rows=None, what=""):
     err = assert_close(got, ref, out_dtype, what)
     fin = np.isfinite(ref_lse)
     assert np.array_equal(np.isfinite(lse), fin), what
-    assert np.max(np.abs(lse[fin] - ref_lse[fin]), initial=0.0) < 1e-4, what
+    lse_tol = 1e-4 if out_dtype == "f32" else 2.0 ** -8
+    assert np.max(np.abs(lse[fin] - ref_lse[fin]), initial=0.0) < lse_tol, what
     assert np.all(lse[~fin] == -np.inf), what
     assert r.guards_ok, f"{what}: output guard band overwritten"
     assert r.ws_guards_ok, f"{what}: workspace guard band overwritten"
