@@ -58,6 +58,7 @@ typedef void* kvd_stream_t;
 /* Bits of the optional device status word (int32, caller-owned, OR-ed in). */
 #define KVD_STATUS_SEQ_LEN_CLAMPED 0x1  /* some seq_lens[b] outside [0, min(s_max, max_seq_len)] */
 #define KVD_STATUS_POS_OUT_OF_RANGE 0x2 /* some pos[b] outside [0, s_max): that row not written */
+#define KVD_STATUS_TIMEOUT 0x4          /* an internal pipeline wait gave up (~2 s): outputs invalid */
 
 /* Supported shapes: head_dim in {64, 128, 256}; n_heads_q a multiple of
  * n_heads_kv with group size n_heads_q / n_heads_kv <= 64. */

@@ -10,17 +10,22 @@
 
 namespace kvd {
 
-const ChunkKernel* chunk_table_d64(int ht, bool f32);
-const ChunkKernel* chunk_table_d128(int ht, bool f32);
-const ChunkKernel* chunk_table_d256(int ht, bool f32);
+const ChunkKernel* mma_table_d64(bool f32);
+const ChunkKernel* mma_table_d128(bool f32);
+const ChunkKernel* mma_table_d256(bool f32);
 
-const ChunkKernel* find_chunk_kernel(int head_dim, int head_tiles, bool f32_out) {
+const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out) {
     switch (head_dim) {
-        case 64: return chunk_table_d64(head_tiles, f32_out);
-        case 128: return chunk_table_d128(head_tiles, f32_out);
-        case 256: return chunk_table_d256(head_tiles, f32_out);
+        case 64: return mma_table_d64(f32_out);
+        case 128: return mma_table_d128(f32_out);
+        case 256: return mma_table_d256(f32_out);
         default: return nullptr;
     }
+}
+
+const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out) {
+    if (group < 1 || group > KVD_MAX_GROUP) return nullptr;
+    return group <= 16 ? mma_chunk_kernel(head_dim, f32_out) : tc_chunk_kernel(head_dim, f32_out);
 }
 
 namespace {
@@ -44,13 +49,7 @@ kvd_status check_shape(int batch, int Hq, int Hkv, int D, kvd_out_dtype dt) {
 }
 
 const ChunkKernel* pick_kernel(int Hq, int Hkv, int D, kvd_out_dtype dt) {
-    const int G = Hq / Hkv;
-    return find_chunk_kernel(D, (G + 15) / 16, dt == KVD_OUT_F32);
-}
-
-int kernel_index(const ChunkKernel* k) {
-    const int d = (k->head_dim == 64) ? 0 : (k->head_dim == 128 ? 1 : 2);
-    return (d * 4 + (k->head_tiles - 1)) * 2 + (k->f32_out ? 1 : 0);
+    return find_chunk_kernel(D, Hq / Hkv, dt == KVD_OUT_F32);
 }
 
 kvd_status device_sms(int* sms) {
@@ -122,6 +121,9 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
         !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)) || (status && !aligned(status, 4)))
         return KVD_ERR_INVALID_ARG;
     if ((size_t)batch * s_max * Hkv * D > ((size_t)1 << 62)) return KVD_ERR_INVALID_ARG;
+    // The tensor-core path addresses cache rows and query rows with 32-bit TMA coordinates.
+    if (Hq / Hkv > 16 && ((long long)batch * s_max > 0x7fffffffLL || (long long)batch * Hq > 0x7fffffffLL))
+        return KVD_ERR_UNSUPPORTED;
 
     int n_split = 0;
     size_t need = 0;
@@ -166,25 +168,14 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     if (phase & kChunk) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVD_ERR_CUDA;
-        const uint64_t bit = 1ull << kernel_index(k);
+        const uint64_t bit = 1ull << k->index;
         if (!(g_smem_ready[dev].load(std::memory_order_acquire) & bit)) {
-            if (cudaFuncSetAttribute(reinterpret_cast<const void*>(k->fn),
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     k->smem_bytes) != cudaSuccess)
+            if (cudaFuncSetAttribute(k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k->smem_bytes) !=
+                cudaSuccess)
                 return KVD_ERR_CUDA;
             g_smem_ready[dev].fetch_or(bit, std::memory_order_acq_rel);
         }
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)n_split, 1, 1);
-        cfg.blockDim = dim3((unsigned)k->threads, 1, 1);
-        cfg.dynamicSmemBytes = (size_t)k->smem_bytes;
-        cfg.stream = s;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        attr[0].val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, k->fn, p) != cudaSuccess) return KVD_ERR_CUDA;
+        if (k->launch(*k, p, s) != cudaSuccess) return KVD_ERR_CUDA;
     }
     if ((phase & kMerge) && n_split > 1) {
         if (launch_merge(p, D, dt == KVD_OUT_F32, s) != cudaSuccess) return KVD_ERR_CUDA;

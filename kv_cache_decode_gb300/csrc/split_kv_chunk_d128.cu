@@ -1,6 +1,6 @@
-// Split-KV chunk kernel variants for head_dim 128.
+// Split-KV chunk kernel (mma.sync engine) for head_dim 128.
 #include "split_kv_chunk_variants.cuh"
 
 namespace kvd {
-KVD_CHUNK_TABLE(128)
+KVD_MMA_TABLE(128, 2)
 }  // namespace kvd

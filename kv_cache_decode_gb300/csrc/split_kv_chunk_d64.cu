@@ -1,6 +1,6 @@
-// Split-KV chunk kernel variants for head_dim 64.
+// Split-KV chunk kernel (mma.sync engine) for head_dim 64.
 #include "split_kv_chunk_variants.cuh"
 
 namespace kvd {
-KVD_CHUNK_TABLE(64)
+KVD_MMA_TABLE(64, 0)
 }  // namespace kvd

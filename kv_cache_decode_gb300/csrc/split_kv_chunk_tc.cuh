@@ -1,0 +1,497 @@
+// Split-KV chunk kernel on the 5th-generation tensor cores (tcgen05), for wide
+// query-head groups (17..64 query heads per KV head: multiquery and wide
+// grouped-query attention).
+//
+// Same schedule, same outputs and same partial-state format as the mma.sync
+// chunk kernel (split_kv_chunk.cuh); only the engine differs. Per 64-token
+// tile of one (sequence, KV head) pair:
+//   S  = Q K^T      tcgen05.mma, M = 64 query heads (group padded to 64),
+//                   N = 64 tokens, K = head_dim; fp32 accumulator in TMEM
+//   P  = 2^(S*scale*log2e - m)   four softmax warps, one query head per thread
+//   O += P V        tcgen05.mma, M = 64, N = head_dim, K = 64 tokens; O in TMEM
+// Operands never pass through registers: TMA writes K, V and Q tiles into
+// 128-byte-swizzled shared memory, and the MMAs read them there, so each K/V
+// byte crosses shared memory once (the mma.sync kernel re-reads it once per
+// 16-head tile). The online softmax follows the log-sum-exp accumulation of
+// sequence-sharded KV (All About Transformer Inference, "Sharding the KV
+// cache") in base 2 (Efficiently Scaling Transformer Inference, section 3.5).
+// The running maximum m used for the exponentials is only raised when a tile's
+// maximum exceeds it by more than 2^8 (weights stay <= 256, exact in fp32), so
+// rescaling O in TMEM is rare; the result is identical in exact arithmetic
+// because O and l always share the same m.
+//
+// Warp roles (7 warps): 0 = TMA producer for K (and Q at each new pair),
+// 1 = MMA issuer (one thread) and TMEM owner, 2 = TMA producer for V,
+// 3..6 = softmax / rescale / epilogue (warp w serves TMEM lane quarter w % 4).
+// Pipelines: K ring of KST stages, V ring of VST stages, two S buffers in
+// TMEM, two P buffers in shared memory, one Q buffer, O in TMEM. Every wait is
+// bounded; a timeout flags KVD_STATUS_TIMEOUT and all roles wind down.
+#pragma once
+
+#include <math_constants.h>
+
+#include "../../include/kvdecode.h"
+#include "common.cuh"
+#include "params.h"
+#include "schedule.cuh"
+#include "split_kv_chunk.cuh"  // DevLen, NoOp, block scans
+#include "tc_common.cuh"
+
+namespace kvd {
+
+template <int D, bool F32OUT>
+struct TcShape {
+    static constexpr int T = 64;                 // tokens per tile
+    static constexpr int KB = D / 64;            // 128-byte swizzle atoms across head_dim
+    static constexpr int TILE_BYTES = T * D * 2; // one K (or V) tile
+    static constexpr int KB_BYTES = T * 128;     // one 64-column block of a tile
+    static constexpr int Q_BYTES = 64 * D * 2;   // 64 rows (group padded)
+    static constexpr int KST = D == 256 ? 3 : (D == 128 ? 5 : 8);
+    static constexpr int VST = D == 256 ? 2 : (D == 128 ? 4 : 6);
+    static constexpr int P_BYTES = 64 * T * 2;   // one P buffer (64 rows x 64 tokens)
+    static constexpr int NP = F32OUT ? 2 : 1;    // hi (and lo) parts of P
+    static constexpr int OFF_Q = 0;
+    static constexpr int OFF_K = OFF_Q + Q_BYTES;
+    static constexpr int OFF_V = OFF_K + KST * TILE_BYTES;
+    static constexpr int OFF_P = OFF_V + VST * TILE_BYTES;
+    static constexpr int OFF_BAR = OFF_P + 2 * NP * P_BYTES;
+    // barriers: k_full, k_empty [KST]; v_full, v_empty [VST]; q_full, q_empty;
+    // s_full, s_free, p_full, p_free [2]; o_done; mma_done
+    static constexpr int NBAR = 2 * KST + 2 * VST + 2 + 8 + 2;
+    static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
+    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+    static constexpr int TMEM_S = 0;             // S buffers at columns 0 and T
+    static constexpr int TMEM_O = 2 * T;         // O at columns [2T, 2T + D)
+    static constexpr int TMEM_COLS = (2 * T + D) <= 256 ? 256 : 512;
+    static constexpr int NWARPS = 7;
+    static constexpr int THREADS = NWARPS * 32;
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+struct TcMaps {
+    CUtensorMap q;  // 2D: [B*Hq rows, D] box (64, G)
+    CUtensorMap k;  // 3D: [B*S_max, Hkv, D] box (64, 1, 64)
+    CUtensorMap v;
+};
+
+template <int D, bool F32OUT>
+__global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
+    split_kv_chunk_tc_kernel(const DecodeParams p, const __grid_constant__ TcMaps maps) {
+    using Sh = TcShape<D, F32OUT>;
+    constexpr int T = Sh::T, KB = Sh::KB, KST = Sh::KST, VST = Sh::VST, NW = Sh::NWARPS;
+    constexpr long long kBudget = 4000000000LL;  // ~2 s of clock cycles per wait
+
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ long long s_red[NW];
+    __shared__ int s_redi[NW];
+    __shared__ long long s_cum0;
+
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    const uint32_t sbase = smem_u32(smem);
+    const uint32_t sQ = sbase + Sh::OFF_Q, sK = sbase + Sh::OFF_K, sV = sbase + Sh::OFF_V,
+                   sP = sbase + Sh::OFF_P, sBar = sbase + Sh::OFF_BAR;
+    auto k_full = [&](int s) { return sBar + 8u * s; };
+    auto k_empty = [&](int s) { return sBar + 8u * (KST + s); };
+    auto v_full = [&](int s) { return sBar + 8u * (2 * KST + s); };
+    auto v_empty = [&](int s) { return sBar + 8u * (2 * KST + VST + s); };
+    const uint32_t q_full = sBar + 8u * (2 * KST + 2 * VST);
+    const uint32_t q_empty = q_full + 8;
+    auto s_full = [&](int b) { return q_empty + 8u * (1 + b); };
+    auto s_free = [&](int b) { return q_empty + 8u * (3 + b); };
+    auto p_full = [&](int b) { return q_empty + 8u * (5 + b); };
+    auto p_free = [&](int b) { return q_empty + 8u * (7 + b); };
+    const uint32_t o_done = q_empty + 8u * 9;
+    const uint32_t mma_done = q_empty + 8u * 10;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::OFF_MISC);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Sh::OFF_MISC + 8);
+    // P buffer b, part (0 = hi, 1 = lo)
+    auto p_buf = [&](int b, int part) { return sP + (uint32_t)((b * Sh::NP + part) * Sh::P_BYTES); };
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = blockIdx.x;
+    const int G = p.G;
+
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const DevLen len{p.seq_lens, p.len_cap};
+    // ---- total work, this CTA's run, first sequence (as in the mma.sync kernel) ----
+    long long mine = 0;
+    bool clamped = false;
+    for (int b = tid; b < p.B; b += Sh::THREADS) {
+        const int raw = __ldg(p.seq_lens + b);
+        const int L = clamp_len(raw, p.len_cap);
+        clamped |= (raw != L);
+        mine += L;
+    }
+    if (clamped && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
+    const long long total = block_sum_ll<NW>(mine, s_red) * p.Hkv;
+    const int C_eff = effective_ctas(p.n_split, total);
+    if (c >= C_eff) return;
+    const long long S = run_begin(c, C_eff, total);
+    int b0 = p.B;
+    long long cum0 = total;
+    {
+        long long base = 0;
+        for (int chunk = 0; chunk < p.B; chunk += Sh::THREADS) {
+            const int b = chunk + tid;
+            const int L = (b < p.B) ? len(b) : 0;
+            const long long v = (long long)L * p.Hkv;
+            long long ctot;
+            const long long cs = base + block_incl_scan_ll<NW>(v, s_red, &ctot) - v;
+            const bool cand = (b < p.B) && is_first_seq_candidate(cs, L, p.Hkv, S);
+            const int bmin = block_min_int<NW>(cand ? b : 0x7fffffff, s_redi);
+            if (bmin != 0x7fffffff) {
+                if (b == bmin) s_cum0 = cs;
+                __syncthreads();
+                b0 = bmin;
+                cum0 = s_cum0;
+                break;
+            }
+            base += ctot;
+        }
+    }
+
+    // ---- set-up: barriers, zeroed Q and P buffers, TMEM ----
+    if (tid == 0) {
+        for (int s = 0; s < KST; ++s) {
+            tc::mbar_init(k_full(s), 1);
+            tc::mbar_init(k_empty(s), 1);
+        }
+        for (int s = 0; s < VST; ++s) {
+            tc::mbar_init(v_full(s), 1);
+            tc::mbar_init(v_empty(s), 1);
+        }
+        tc::mbar_init(q_full, 1);
+        tc::mbar_init(q_empty, 1);
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(s_full(b), 1);
+            tc::mbar_init(s_free(b), 4);
+            tc::mbar_init(p_full(b), 4);
+            tc::mbar_init(p_free(b), 1);
+        }
+        tc::mbar_init(o_done, 1);
+        tc::mbar_init(mma_done, 1);
+        *abort_flag = 0;
+        tc::mbar_fence_init();
+    }
+    // Rows of Q past the group, and P rows of padded heads, stay zero.
+    for (int i = tid; i < Sh::Q_BYTES / 16; i += Sh::THREADS)
+        reinterpret_cast<uint4*>(smem + Sh::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = tid; i < 2 * Sh::NP * Sh::P_BYTES / 16; i += Sh::THREADS)
+        reinterpret_cast<uint4*>(smem + Sh::OFF_P)[i] = make_uint4(0, 0, 0, 0);
+    tc::fence_proxy_async_smem();
+    if (warp == 1) tc::tmem_alloc(smem_u32(tmem_slot), Sh::TMEM_COLS);
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    Walker<DevLen> walker(len, p.B, p.Hkv, T, c, C_eff, total);
+    walker.start(b0, cum0);
+
+    if (warp == 0 || warp == 2) {
+        // ===================== TMA producers =====================
+        if (lane == 0) {
+            const bool is_k = (warp == 0);
+            const uint64_t pol_kv = l2_evict_first_policy();
+            const uint64_t pol_q = tc::l2_evict_last_policy();
+            Tile t;
+            int j = 0, qn = 0;
+            const int NS = is_k ? KST : VST;
+            while (walker.next(t, NoOp{})) {
+                if (is_k && t.seg_start) {
+                    if (!tc::mbar_wait(q_empty, (qn & 1) ^ 1, abort_flag, kBudget)) break;
+                    tc::mbar_arrive_expect_tx(q_full, (uint32_t)(KB * 128 * G));
+                    const int qrow = t.b * p.Hq + t.h * G;
+#pragma unroll
+                    for (int kb = 0; kb < KB; ++kb)
+                        tc::tma_load_2d(sQ + kb * 8192, &maps.q, kb * 64, qrow, q_full, pol_q);
+                    ++qn;
+                }
+                const int s = j % NS;
+                const uint32_t full = is_k ? k_full(s) : v_full(s);
+                const uint32_t empty = is_k ? k_empty(s) : v_empty(s);
+                if (!tc::mbar_wait(empty, ((j / NS) & 1) ^ 1, abort_flag, kBudget)) break;
+                tc::mbar_arrive_expect_tx(full, (uint32_t)Sh::TILE_BYTES);
+                const uint32_t dst = (is_k ? sK : sV) + (uint32_t)(s * Sh::TILE_BYTES);
+                const int row = t.b * p.S_max + t.tok_lo;
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb)
+                    tc::tma_load_3d(dst + kb * Sh::KB_BYTES, is_k ? &maps.k : &maps.v, kb * 64, t.h, row,
+                                    full, pol_kv);
+                ++j;
+            }
+            // Do not leave with copies in flight: wait for the last loads to land.
+            for (int jj = (j > NS ? j - NS : 0); jj < j; ++jj) {
+                const int s = jj % NS;
+                tc::mbar_wait(is_k ? k_full(s) : v_full(s), (jj / NS) & 1, abort_flag, kBudget / 4);
+            }
+            if (is_k && qn > 0) tc::mbar_wait(q_full, (qn - 1) & 1, abort_flag, kBudget / 4);
+        }
+    } else if (warp == 1) {
+        // ===================== MMA issuer =====================
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = tc::idesc_bf16_f32(64, T, false, false);
+            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(64, D, false, true);
+            int qn = 0;
+            bool ok = true;
+            auto mma_s = [&](const Tile& t, int i) {
+                const int sk = i % KST, sb = i & 1;
+                ok = ok && tc::mbar_wait(k_full(sk), (i / KST) & 1, abort_flag, kBudget);
+                ok = ok && tc::mbar_wait(s_free(sb), ((i >> 1) & 1) ^ 1, abort_flag, kBudget);
+                if (t.seg_start) {
+                    ok = ok && tc::mbar_wait(q_full, qn & 1, abort_flag, kBudget);
+                    ++qn;
+                }
+                if (!ok) return;
+                tc::fence_after_sync();
+                const uint32_t kt = sK + (uint32_t)(sk * Sh::TILE_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint64_t a = tc::sdesc_sw128(sQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+                    const uint64_t b = tc::sdesc_sw128(kt + (kk >> 2) * Sh::KB_BYTES + (kk & 3) * 32, 16, 1024);
+                    tc::mma_bf16(tmem + Sh::TMEM_S + sb * T, a, b, idesc_s, kk > 0);
+                }
+                tc::mma_commit(s_full(sb));
+                tc::mma_commit(k_empty(sk));
+                if (t.seg_end) tc::mma_commit(q_empty);
+            };
+            auto mma_o = [&](const Tile& t, int i) {
+                const int sv = i % VST, sb = i & 1;
+                ok = ok && tc::mbar_wait(v_full(sv), (i / VST) & 1, abort_flag, kBudget);
+                ok = ok && tc::mbar_wait(p_full(sb), (i >> 1) & 1, abort_flag, kBudget);
+                if (!ok) return;
+                tc::fence_after_sync();
+                const uint32_t vt = sV + (uint32_t)(sv * Sh::TILE_BYTES);
+#pragma unroll
+                for (int k2 = 0; k2 < T / 16; ++k2) {
+                    const uint64_t b = tc::sdesc_sw128(vt + k2 * 2048, Sh::KB_BYTES, 1024);
+#pragma unroll
+                    for (int part = 0; part < Sh::NP; ++part) {
+                        const uint64_t a = tc::sdesc_sw128(p_buf(sb, part) + k2 * 32, 16, 1024);
+                        tc::mma_bf16(tmem + Sh::TMEM_O, a, b, idesc_o,
+                                     (t.seg_start && k2 == 0 && part == 0) ? 0u : 1u);
+                    }
+                }
+                tc::mma_commit(v_empty(sv));
+                tc::mma_commit(p_free(sb));
+                tc::mma_commit(o_done);
+            };
+            Tile cur, nxt;
+            bool has_cur = walker.next(cur, NoOp{});
+            int i = 0;
+            if (has_cur) mma_s(cur, 0);
+            while (has_cur && ok) {
+                const bool has_nxt = walker.next(nxt, NoOp{});
+                const bool new_seg = has_nxt && nxt.seg_start;
+                if (has_nxt && !new_seg) mma_s(nxt, i + 1);  // S of the next tile overlaps softmax
+                mma_o(cur, i);
+                if (has_nxt && new_seg) mma_s(nxt, i + 1);   // a new pair's Q arrives after this
+                cur = nxt;
+                has_cur = has_nxt;
+                ++i;
+            }
+            // All tensor-core work of this CTA done before TMEM is released.
+            tc::mma_commit(mma_done);
+            tc::mbar_wait(mma_done, 0, abort_flag, kBudget);
+        }
+    } else {
+        // ===================== softmax / epilogue (warps 3..6) =====================
+        const int quarter = warp & 3;                 // TMEM lanes [32*quarter, +32)
+        const int row = quarter * 16 + lane;          // group-local query head of this thread
+        const bool has_row = lane < 16;
+        const bool active = has_row && row < G;
+        const int st = tid - 3 * 32;                  // 0..127 among the softmax threads
+        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const float scale_log2 = p.scale_log2;
+
+        auto write_empty = [&](int b, int h) {
+            const size_t r0 = (size_t)b * p.Hq + (size_t)h * G;
+            if constexpr (F32OUT) {
+                float* o = reinterpret_cast<float*>(p.out) + r0 * D;
+                for (int i2 = st; i2 < G * D; i2 += 128) o[i2] = 0.f;
+            } else {
+                __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + r0 * D;
+                for (int i2 = st; i2 < G * D; i2 += 128) o[i2] = __float2bfloat16_rn(0.f);
+            }
+            if (p.lse)
+                for (int i2 = st; i2 < G; i2 += 128) p.lse[r0 + i2] = -CUDART_INF_F;
+            if (st == 0 && p.ws_rec) p.ws_rec[(size_t)b * p.Hkv + h] = make_int2(-1, -1);
+        };
+
+        float m_used = 0.f, l = 0.f;
+        Tile t;
+        int i = 0;
+        bool ok = true;
+        while (ok && walker.next(t, write_empty)) {
+            const int sb = i & 1;
+            ok = __all_sync(0xffffffffu, tc::mbar_wait(s_full(sb), (i >> 1) & 1, abort_flag, kBudget));
+            if (!ok) break;
+            tc::fence_after_sync();
+            __syncwarp();
+            uint32_t sr[T];
+            tc::tmem_ld32(tmem + lane_base + Sh::TMEM_S + sb * T, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
+            tc::tmem_ld32(tmem + lane_base + Sh::TMEM_S + sb * T + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            tc::tmem_wait_ld();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(s_free(sb));
+
+            const int nvalid = t.tok_hi - t.tok_lo;
+            float s[T];
+            float mt = -CUDART_INF_F;
+#pragma unroll
+            for (int k = 0; k < T; ++k) {
+                s[k] = (k < nvalid) ? __uint_as_float(sr[k]) * scale_log2 : -CUDART_INF_F;
+                mt = fmaxf(mt, s[k]);
+            }
+            bool need = false;
+            float alpha = 1.f;
+            if (t.seg_start) {
+                m_used = mt;
+                l = 0.f;
+            } else if (mt > m_used + 8.f) {
+                need = true;
+                alpha = exp2f(m_used - mt);
+            }
+            if (__any_sync(0xffffffffu, need && has_row)) {
+                // O must hold the previous tile's P V before it is rescaled.
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(o_done, (i - 1) & 1, abort_flag, kBudget));
+                if (!ok) break;
+                tc::fence_after_sync();
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t r[32];
+                    const uint32_t ta = tmem + lane_base + Sh::TMEM_O + cc * 32;
+                    __syncwarp();
+                    tc::tmem_ld32(ta, r);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
+                    tc::tmem_st32(ta, r);
+                }
+                tc::tmem_wait_st();
+                if (need) {
+                    l *= alpha;
+                    m_used = mt;
+                }
+            }
+
+            // P buffer sb is free once the P V of tile i - 2 has completed.
+            ok = __all_sync(0xffffffffu, tc::mbar_wait(p_free(sb), ((i >> 1) & 1) ^ 1, abort_flag, kBudget));
+            if (!ok) break;
+            if (has_row) {
+                const uint32_t prow = p_buf(sb, 0) + (uint32_t)row * 128;
+                const uint32_t prow_lo = p_buf(sb, Sh::NP - 1) + (uint32_t)row * 128;
+                float ls = 0.f;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint32_t hi[4], lo[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int k = ch * 8 + e * 2;
+                        const float e0 = active ? exp2f(s[k] - m_used) : 0.f;
+                        const float e1 = active ? exp2f(s[k + 1] - m_used) : 0.f;
+                        hi[e] = pack_bf16x2(e0, e1);
+                        if constexpr (F32OUT) {
+                            lo[e] = pack_bf16x2(e0 - bf16_lo(hi[e]), e1 - bf16_hi(hi[e]));
+                            ls += e0 + e1;
+                        } else {
+                            ls += bf16_lo(hi[e]) + bf16_hi(hi[e]);
+                        }
+                    }
+                    const uint32_t off = (uint32_t)((ch ^ (row & 7)) * 16);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(prow + off), "r"(hi[0]),
+                                 "r"(hi[1]), "r"(hi[2]), "r"(hi[3]) : "memory");
+                    if constexpr (F32OUT)
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(prow_lo + off), "r"(lo[0]),
+                                     "r"(lo[1]), "r"(lo[2]), "r"(lo[3]) : "memory");
+                }
+                l += ls;
+            }
+            if (nvalid < T) {
+                // Rows past the sequence's end came from the cache's padding (or the
+                // next sequence): zero them so that 0-weights never meet NaN.
+                const int sv = i % VST;
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(v_full(sv), (i / VST) & 1, abort_flag, kBudget));
+                if (!ok) break;
+                uint8_t* vt = smem + Sh::OFF_V + sv * Sh::TILE_BYTES;
+                const int n16 = (T - nvalid) * KB * 8;
+                for (int idx = st; idx < n16; idx += 128) {
+                    const int r = nvalid + idx / (KB * 8);
+                    const int rem = idx % (KB * 8);
+                    *reinterpret_cast<uint4*>(vt + (rem >> 3) * Sh::KB_BYTES + r * 128 + (rem & 7) * 16) =
+                        make_uint4(0, 0, 0, 0);
+                }
+            }
+            tc::fence_proxy_async_smem();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(p_full(sb));
+
+            if (t.seg_end) {
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(o_done, i & 1, abort_flag, kBudget));
+                if (!ok) break;
+                tc::fence_after_sync();
+                const size_t pair = (size_t)t.b * p.Hkv + t.h;
+                const size_t qrow = (size_t)t.b * p.Hq + (size_t)t.h * G + row;
+                const size_t slot = (size_t)c + pair;
+                const float inv = (l > 0.f) ? 1.f / l : 0.f;
+#pragma unroll 1
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t r[32];
+                    __syncwarp();
+                    tc::tmem_ld32(tmem + lane_base + Sh::TMEM_O + cc * 32, r);
+                    tc::tmem_wait_ld();
+                    if (!active) {
+                    } else if (t.full) {
+                        if constexpr (F32OUT) {
+                            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + qrow * D + cc * 32);
+#pragma unroll
+                            for (int k = 0; k < 8; ++k)
+                                o[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
+                                                   __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
+                        } else {
+                            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + qrow * D + cc * 32);
+#pragma unroll
+                            for (int k = 0; k < 4; ++k)
+                                o[k] = make_uint4(
+                                    pack_bf16x2(__uint_as_float(r[8 * k]) * inv, __uint_as_float(r[8 * k + 1]) * inv),
+                                    pack_bf16x2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv),
+                                    pack_bf16x2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv),
+                                    pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv));
+                        }
+                    } else {
+                        float4* o = reinterpret_cast<float4*>(p.ws_o + (slot * G + row) * D + cc * 32);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            o[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                               __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+                    }
+                }
+                tc::fence_before_sync();
+                if (active) {
+                    if (t.full) {
+                        if (p.lse) p.lse[qrow] = (m_used + log2f(l)) * 0.69314718055994531f;
+                    } else {
+                        p.ws_ml[slot * G + row] = make_float2(m_used, l);
+                    }
+                }
+                // Only the pair's owner writes its merge record.
+                if (st == 0 && p.ws_rec && t.owned)
+                    p.ws_rec[pair] = t.full ? make_int2(-1, -1) : make_int2(c, t.c_last);
+            }
+            ++i;
+        }
+        if (ok) walker.finish(write_empty);
+    }
+
+    __syncthreads();
+    if (*abort_flag && tid == 0 && p.status) atomicOr(p.status, KVD_STATUS_TIMEOUT);
+    if (warp == 1) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, Sh::TMEM_COLS);
+    }
+}
+
+}  // namespace kvd

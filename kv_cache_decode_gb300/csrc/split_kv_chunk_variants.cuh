@@ -20,32 +20,45 @@ struct ChunkConfig {
     static constexpr int MINB = (2 * (SMEM + 1024) <= 228 * 1024) ? 2 : 1;
 };
 
-template <int D, int HT, bool F32>
-inline ChunkKernel make_chunk_kernel() {
-    using C = ChunkConfig<D, HT>;
-    using Sh = ChunkShape<D, HT, C::TS, C::TT, C::STAGES>;
+template <int D, bool F32>
+cudaError_t launch_mma_chunk(const ChunkKernel& k, const DecodeParams& p, cudaStream_t stream) {
+    using C = ChunkConfig<D, 1>;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.n_split, 1, 1);
+    cfg.blockDim = dim3((unsigned)k.threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)k.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_kv_chunk_kernel<D, 1, C::TS, C::TT, C::STAGES, F32, C::MINB>, p);
+}
+
+template <int D, bool F32>
+inline ChunkKernel make_mma_chunk_kernel(int index) {
+    using C = ChunkConfig<D, 1>;
+    using Sh = ChunkShape<D, 1, C::TS, C::TT, C::STAGES>;
     ChunkKernel k;
-    k.fn = split_kv_chunk_kernel<D, HT, C::TS, C::TT, C::STAGES, F32, C::MINB>;
+    k.fn = reinterpret_cast<const void*>(split_kv_chunk_kernel<D, 1, C::TS, C::TT, C::STAGES, F32, C::MINB>);
+    k.launch = launch_mma_chunk<D, F32>;
     k.head_dim = D;
-    k.head_tiles = HT;
     k.threads = Sh::NT;
     k.smem_bytes = Sh::SMEM_BYTES;
     k.tile_tokens = C::TT;
     k.ctas_per_sm = C::MINB;
     k.f32_out = F32;
+    k.tensor_core = false;
+    k.index = index;
     return k;
 }
 
-#define KVD_CHUNK_TABLE(D)                                                                   \
-    const ChunkKernel* chunk_table_d##D(int ht, bool f32) {                                 \
-        static const ChunkKernel table[4][2] = {                                            \
-            {make_chunk_kernel<D, 1, false>(), make_chunk_kernel<D, 1, true>()},            \
-            {make_chunk_kernel<D, 2, false>(), make_chunk_kernel<D, 2, true>()},            \
-            {make_chunk_kernel<D, 3, false>(), make_chunk_kernel<D, 3, true>()},            \
-            {make_chunk_kernel<D, 4, false>(), make_chunk_kernel<D, 4, true>()},            \
-        };                                                                                  \
-        if (ht < 1 || ht > 4) return nullptr;                                               \
-        return &table[ht - 1][f32 ? 1 : 0];                                                 \
+#define KVD_MMA_TABLE(D, IDX)                                                                     \
+    const ChunkKernel* mma_table_d##D(bool f32) {                                                \
+        static const ChunkKernel table[2] = {make_mma_chunk_kernel<D, false>(IDX),              \
+                                             make_mma_chunk_kernel<D, true>(IDX + 1)};           \
+        return &table[f32 ? 1 : 0];                                                              \
     }
 
 }  // namespace kvd
