@@ -56,8 +56,8 @@ struct TcShape {
     static constexpr int OFF_P = OFF_V + VST * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_P + 2 * NP * P_BYTES;
     // barriers: k_full, k_empty [KST]; v_full, v_empty [VST]; q_full, q_empty;
-    // s_full, s_free, p_full, p_free [2]; o_done; mma_done
-    static constexpr int NBAR = 2 * KST + 2 * VST + 2 + 8 + 2;
+    // s_full, s_free, p_full, o_fin [2]; mma_done
+    static constexpr int NBAR = 2 * KST + 2 * VST + 2 + 8 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
     static constexpr int TMEM_S = 0;             // S buffers at columns 0 and T
@@ -99,9 +99,11 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
     auto s_full = [&](int b) { return q_empty + 8u * (1 + b); };
     auto s_free = [&](int b) { return q_empty + 8u * (3 + b); };
     auto p_full = [&](int b) { return q_empty + 8u * (5 + b); };
-    auto p_free = [&](int b) { return q_empty + 8u * (7 + b); };
-    const uint32_t o_done = q_empty + 8u * 9;
-    const uint32_t mma_done = q_empty + 8u * 10;
+    // o_fin[i & 1] completes when O += P(i) V(i) has finished. One barrier per
+    // P buffer (rather than one for all tiles) keeps every waiter within one
+    // phase of the completion it waits for, so parity waits are unambiguous.
+    auto o_fin = [&](int b) { return q_empty + 8u * (7 + b); };
+    const uint32_t mma_done = q_empty + 8u * 9;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Sh::OFF_MISC + 8);
     // P buffer b, part (0 = hi, 1 = lo)
@@ -111,48 +113,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
     const int c = blockIdx.x;
     const int G = p.G;
 
-    pdl_wait();
-    pdl_launch_dependents();
-
-    const DevLen len{p.seq_lens, p.len_cap};
-    // ---- total work, this CTA's run, first sequence (as in the mma.sync kernel) ----
-    long long mine = 0;
-    bool clamped = false;
-    for (int b = tid; b < p.B; b += Sh::THREADS) {
-        const int raw = __ldg(p.seq_lens + b);
-        const int L = clamp_len(raw, p.len_cap);
-        clamped |= (raw != L);
-        mine += L;
-    }
-    if (clamped && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
-    const long long total = block_sum_ll<NW>(mine, s_red) * p.Hkv;
-    const int C_eff = effective_ctas(p.n_split, total);
-    if (c >= C_eff) return;
-    const long long S = run_begin(c, C_eff, total);
-    int b0 = p.B;
-    long long cum0 = total;
-    {
-        long long base = 0;
-        for (int chunk = 0; chunk < p.B; chunk += Sh::THREADS) {
-            const int b = chunk + tid;
-            const int L = (b < p.B) ? len(b) : 0;
-            const long long v = (long long)L * p.Hkv;
-            long long ctot;
-            const long long cs = base + block_incl_scan_ll<NW>(v, s_red, &ctot) - v;
-            const bool cand = (b < p.B) && is_first_seq_candidate(cs, L, p.Hkv, S);
-            const int bmin = block_min_int<NW>(cand ? b : 0x7fffffff, s_redi);
-            if (bmin != 0x7fffffff) {
-                if (b == bmin) s_cum0 = cs;
-                __syncthreads();
-                b0 = bmin;
-                cum0 = s_cum0;
-                break;
-            }
-            base += ctot;
-        }
-    }
-
-    // ---- set-up: barriers, zeroed Q and P buffers, TMEM ----
+    // ---- set-up (reads no inputs, so it overlaps the previous kernel's tail) ----
     if (tid == 0) {
         for (int s = 0; s < KST; ++s) {
             tc::mbar_init(k_full(s), 1);
@@ -168,9 +129,8 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
             tc::mbar_init(s_full(b), 1);
             tc::mbar_init(s_free(b), 4);
             tc::mbar_init(p_full(b), 4);
-            tc::mbar_init(p_free(b), 1);
+            tc::mbar_init(o_fin(b), 1);
         }
-        tc::mbar_init(o_done, 1);
         tc::mbar_init(mma_done, 1);
         *abort_flag = 0;
         tc::mbar_fence_init();
@@ -182,23 +142,76 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
         reinterpret_cast<uint4*>(smem + Sh::OFF_P)[i] = make_uint4(0, 0, 0, 0);
     tc::fence_proxy_async_smem();
     if (warp == 1) tc::tmem_alloc(smem_u32(tmem_slot), Sh::TMEM_COLS);
-    __syncthreads();
+
+    // Inputs may be produced by the previous kernel on the stream (the append).
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const DevLen len{p.seq_lens, p.len_cap};
+    // ---- total work, this CTA's run, first sequence (as in the mma.sync kernel) ----
+    long long mine = 0;
+    bool clamped = false;
+    for (int b = tid; b < p.B; b += Sh::THREADS) {
+        const int raw = __ldg(p.seq_lens + b);
+        const int L = clamp_len(raw, p.len_cap);
+        clamped |= (raw != L);
+        mine += L;
+    }
+    if (clamped && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
+    const long long total = block_sum_ll<NW>(mine, s_red) * p.Hkv;  // also orders the set-up
+    const int C_eff = effective_ctas(p.n_split, total);
+    const bool has_work = c < C_eff;
+    const long long S = has_work ? run_begin(c, C_eff, total) : total;
+    int b0 = p.B;
+    long long cum0 = total;
+    for (long long base = 0, chunk = 0; has_work && chunk < p.B; chunk += Sh::THREADS) {
+        const int b = (int)chunk + tid;
+        const int L = (b < p.B) ? len(b) : 0;
+        const long long v = (long long)L * p.Hkv;
+        long long ctot;
+        const long long cs = base + block_incl_scan_ll<NW>(v, s_red, &ctot) - v;
+        const bool cand = (b < p.B) && is_first_seq_candidate(cs, L, p.Hkv, S);
+        const int bmin = block_min_int<NW>(cand ? b : 0x7fffffff, s_redi);
+        if (bmin != 0x7fffffff) {
+            if (b == bmin) s_cum0 = cs;
+            __syncthreads();
+            b0 = bmin;
+            cum0 = s_cum0;
+            break;
+        }
+        base += ctot;
+    }
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    Walker<DevLen> walker(len, p.B, p.Hkv, T, c, C_eff, total);
+    Walker<DevLen> walker(len, p.B, p.Hkv, T, c, has_work ? C_eff : c + 1, has_work ? total : 0);
     walker.start(b0, cum0);
 
-    if (warp == 0 || warp == 2) {
+    if (!has_work) {
+        // no tokens for this CTA: fall through to the common exit (TMEM release)
+    } else if (warp == 0 || warp == 2) {
         // ===================== TMA producers =====================
         if (lane == 0) {
             const bool is_k = (warp == 0);
             const uint64_t pol_kv = l2_evict_first_policy();
             const uint64_t pol_q = tc::l2_evict_last_policy();
-            Tile t;
+            Tile t, pt;
             int j = 0, qn = 0;
             const int NS = is_k ? KST : VST;
+            const CUtensorMap* map = is_k ? &maps.k : &maps.v;
+            // A second walker runs kPrefetch tiles ahead and warms L2 with them, so the
+            // HBM latency is paid before a shared-memory stage frees up.
+            constexpr int kPrefetch = 3;
+            Walker<DevLen> ahead = walker;
+            auto prefetch = [&](const Tile& x) {
+                const int r = x.b * p.S_max + x.tok_lo;
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb) tc::tma_prefetch_3d(map, kb * 64, x.h, r);
+            };
+            for (int a = 0; a < kPrefetch; ++a)
+                if (ahead.next(pt, NoOp{})) prefetch(pt);
             while (walker.next(t, NoOp{})) {
+                if (ahead.next(pt, NoOp{})) prefetch(pt);
                 if (is_k && t.seg_start) {
                     if (!tc::mbar_wait(q_empty, (qn & 1) ^ 1, abort_flag, kBudget)) break;
                     tc::mbar_arrive_expect_tx(q_full, (uint32_t)(KB * 128 * G));
@@ -217,8 +230,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
                 const int row = t.b * p.S_max + t.tok_lo;
 #pragma unroll
                 for (int kb = 0; kb < KB; ++kb)
-                    tc::tma_load_3d(dst + kb * Sh::KB_BYTES, is_k ? &maps.k : &maps.v, kb * 64, t.h, row,
-                                    full, pol_kv);
+                    tc::tma_load_3d(dst + kb * Sh::KB_BYTES, map, kb * 64, t.h, row, full, pol_kv);
                 ++j;
             }
             // Do not leave with copies in flight: wait for the last loads to land.
@@ -234,16 +246,8 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
             constexpr uint32_t idesc_s = tc::idesc_bf16_f32(64, T, false, false);
             constexpr uint32_t idesc_o = tc::idesc_bf16_f32(64, D, false, true);
             int qn = 0;
-            bool ok = true;
             auto mma_s = [&](const Tile& t, int i) {
                 const int sk = i % KST, sb = i & 1;
-                ok = ok && tc::mbar_wait(k_full(sk), (i / KST) & 1, abort_flag, kBudget);
-                ok = ok && tc::mbar_wait(s_free(sb), ((i >> 1) & 1) ^ 1, abort_flag, kBudget);
-                if (t.seg_start) {
-                    ok = ok && tc::mbar_wait(q_full, qn & 1, abort_flag, kBudget);
-                    ++qn;
-                }
-                if (!ok) return;
                 tc::fence_after_sync();
                 const uint32_t kt = sK + (uint32_t)(sk * Sh::TILE_BYTES);
 #pragma unroll
@@ -258,9 +262,6 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
             };
             auto mma_o = [&](const Tile& t, int i) {
                 const int sv = i % VST, sb = i & 1;
-                ok = ok && tc::mbar_wait(v_full(sv), (i / VST) & 1, abort_flag, kBudget);
-                ok = ok && tc::mbar_wait(p_full(sb), (i >> 1) & 1, abort_flag, kBudget);
-                if (!ok) return;
                 tc::fence_after_sync();
                 const uint32_t vt = sV + (uint32_t)(sv * Sh::TILE_BYTES);
 #pragma unroll
@@ -274,22 +275,49 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
                     }
                 }
                 tc::mma_commit(v_empty(sv));
-                tc::mma_commit(p_free(sb));
-                tc::mma_commit(o_done);
+                tc::mma_commit(o_fin(sb));
             };
-            Tile cur, nxt;
-            bool has_cur = walker.next(cur, NoOp{});
-            int i = 0;
-            if (has_cur) mma_s(cur, 0);
-            while (has_cur && ok) {
-                const bool has_nxt = walker.next(nxt, NoOp{});
-                const bool new_seg = has_nxt && nxt.seg_start;
-                if (has_nxt && !new_seg) mma_s(nxt, i + 1);  // S of the next tile overlaps softmax
-                mma_o(cur, i);
-                if (has_nxt && new_seg) mma_s(nxt, i + 1);   // a new pair's Q arrives after this
-                cur = nxt;
-                has_cur = has_nxt;
-                ++i;
+            // Issue whichever of S(i) = Q K^T and O += P(j) V(j) is ready first, so that
+            // S of upcoming tiles is never queued behind a wait for P or V.
+            Tile tq[4];
+            int n_fetched = 0, s_idx = 0, o_idx = 0;
+            bool walker_done = false;
+            long long idle_since = clock64();
+            while (true) {
+                while (!walker_done && n_fetched < o_idx + 4) {
+                    if (walker.next(tq[n_fetched & 3], NoOp{}))
+                        ++n_fetched;
+                    else
+                        walker_done = true;
+                }
+                if (walker_done && o_idx == n_fetched) break;
+                bool progress = false;
+                if (s_idx < n_fetched && s_idx < o_idx + 3) {
+                    const Tile& t = tq[s_idx & 3];
+                    if (tc::mbar_try_wait(k_full(s_idx % KST), (s_idx / KST) & 1) &&
+                        tc::mbar_try_wait(s_free(s_idx & 1), ((s_idx >> 1) & 1) ^ 1) &&
+                        (!t.seg_start || tc::mbar_try_wait(q_full, qn & 1))) {
+                        if (t.seg_start) ++qn;
+                        mma_s(t, s_idx);
+                        ++s_idx;
+                        progress = true;
+                    }
+                }
+                if (o_idx < s_idx) {
+                    const Tile& t = tq[o_idx & 3];
+                    if (tc::mbar_try_wait(v_full(o_idx % VST), (o_idx / VST) & 1) &&
+                        tc::mbar_try_wait(p_full(o_idx & 1), (o_idx >> 1) & 1)) {
+                        mma_o(t, o_idx);
+                        ++o_idx;
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    idle_since = clock64();
+                } else if (*abort_flag || clock64() - idle_since > kBudget) {
+                    *abort_flag = 1;
+                    break;
+                }
             }
             // All tensor-core work of this CTA done before TMEM is released.
             tc::mma_commit(mma_done);
@@ -356,7 +384,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
             }
             if (__any_sync(0xffffffffu, need && has_row)) {
                 // O must hold the previous tile's P V before it is rescaled.
-                ok = __all_sync(0xffffffffu, tc::mbar_wait(o_done, (i - 1) & 1, abort_flag, kBudget));
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(o_fin((i - 1) & 1), ((i - 1) >> 1) & 1, abort_flag, kBudget));
                 if (!ok) break;
                 tc::fence_after_sync();
 #pragma unroll 1
@@ -378,7 +406,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
             }
 
             // P buffer sb is free once the P V of tile i - 2 has completed.
-            ok = __all_sync(0xffffffffu, tc::mbar_wait(p_free(sb), ((i >> 1) & 1) ^ 1, abort_flag, kBudget));
+            ok = __all_sync(0xffffffffu, tc::mbar_wait(o_fin(sb), ((i >> 1) & 1) ^ 1, abort_flag, kBudget));
             if (!ok) break;
             if (has_row) {
                 const uint32_t prow = p_buf(sb, 0) + (uint32_t)row * 128;
@@ -430,7 +458,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
             if (lane == 0) tc::mbar_arrive(p_full(sb));
 
             if (t.seg_end) {
-                ok = __all_sync(0xffffffffu, tc::mbar_wait(o_done, i & 1, abort_flag, kBudget));
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(o_fin(sb), (i >> 1) & 1, abort_flag, kBudget));
                 if (!ok) break;
                 tc::fence_after_sync();
                 const size_t pair = (size_t)t.b * p.Hkv + t.h;
