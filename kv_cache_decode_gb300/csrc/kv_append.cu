@@ -47,10 +47,14 @@ cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const
     long long blocks = (work + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     if (blocks < 1) blocks = 1;
-    kv_append_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
-        static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), static_cast<const uint4*>(k_new),
-        static_cast<const uint4*>(v_new), pos, B, S_max, Hkv, vec_per_row, status);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
+    cfg.blockDim = dim3(256, 1, 1);
+    cfg.stream = stream;
+    // The launch's own status (a stale error from earlier work is not picked up).
+    return cudaLaunchKernelEx(&cfg, kv_append_kernel, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
+                              static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), pos, B, S_max,
+                              Hkv, vec_per_row, status);
 }
 
 }  // namespace kvd

@@ -26,13 +26,13 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 // bf16 tensor map with 128-byte swizzle; dims/strides innermost first (strides in bytes).
 bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, const cuuint64_t* strides,
-            const cuuint32_t* box) {
+            const cuuint32_t* box, bool swizzle = true) {
     auto enc = encode_fn();
     if (!enc) return false;
     const cuuint32_t es[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, es,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -53,6 +53,9 @@ cudaError_t launch_tc_chunk(const ChunkKernel& k, const DecodeParams& p, cudaStr
         const cuuint32_t box[3] = {64, 1, (cuuint32_t)TcShape<D, F32>::T};
         if (!encode(&maps.k, p.k, 3, dims, strides, box)) return cudaErrorInvalidValue;
         if (!encode(&maps.v, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
+        const cuuint32_t pf_box[3] = {(cuuint32_t)D, 1, (cuuint32_t)TcShape<D, F32>::T};
+        if (!encode(&maps.k_pf, p.k, 3, dims, strides, pf_box, false)) return cudaErrorInvalidValue;
+        if (!encode(&maps.v_pf, p.v, 3, dims, strides, pf_box, false)) return cudaErrorInvalidValue;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.n_split, 1, 1);

@@ -20,9 +20,10 @@
 // rescaling O in TMEM is rare; the result is identical in exact arithmetic
 // because O and l always share the same m.
 //
-// Warp roles (7 warps): 0 = TMA producer for K (and Q at each new pair),
+// Warp roles (11 warps): 0 = TMA producer for K (and Q at each new pair),
 // 1 = MMA issuer (one thread) and TMEM owner, 2 = TMA producer for V,
-// 3..6 = softmax / rescale / epilogue (warp w serves TMEM lane quarter w % 4).
+// 3..10 = softmax / rescale / epilogue (two warps per TMEM lane quarter w % 4,
+// splitting the token columns of S and the output columns of O).
 // Pipelines: K ring of KST stages, V ring of VST stages, two S buffers in
 // TMEM, two P buffers in shared memory, one Q buffer, O in TMEM. Every wait is
 // bounded; a timeout flags KVD_STATUS_TIMEOUT and all roles wind down.
@@ -46,7 +47,8 @@ struct TcShape {
     static constexpr int TILE_BYTES = T * D * 2; // one K (or V) tile
     static constexpr int KB_BYTES = T * 128;     // one 64-column block of a tile
     static constexpr int Q_BYTES = 64 * D * 2;   // 64 rows (group padded)
-    static constexpr int KST = D == 256 ? 3 : (D == 128 ? 5 : 8);
+    // fp32-output mode carries a second (low) P buffer, so it keeps one K stage fewer.
+    static constexpr int KST = D == 256 ? (F32OUT ? 2 : 3) : (D == 128 ? 5 : 8);
     static constexpr int VST = D == 256 ? 2 : (D == 128 ? 4 : 6);
     static constexpr int P_BYTES = 64 * T * 2;   // one P buffer (64 rows x 64 tokens)
     static constexpr int NP = F32OUT ? 2 : 1;    // hi (and lo) parts of P
@@ -56,22 +58,25 @@ struct TcShape {
     static constexpr int OFF_P = OFF_V + VST * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_P + 2 * NP * P_BYTES;
     // barriers: k_full, k_empty [KST]; v_full, v_empty [VST]; q_full, q_empty;
-    // s_full, s_free, p_full, o_fin [2]; mma_done
-    static constexpr int NBAR = 2 * KST + 2 * VST + 2 + 8 + 1;
+    // s_full, s_free, p_full, o_fin [2]; mma_done; xbar [4]
+    static constexpr int NBAR = 2 * KST + 2 * VST + 2 + 8 + 1 + 4;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+    static constexpr int STATIC_SMEM = 2048;  // block scans and the exchange buffer (checked by ptxas -v)
     static constexpr int TMEM_S = 0;             // S buffers at columns 0 and T
     static constexpr int TMEM_O = 2 * T;         // O at columns [2T, 2T + D)
     static constexpr int TMEM_COLS = (2 * T + D) <= 256 ? 256 : 512;
-    static constexpr int NWARPS = 7;
+    static constexpr int NWARPS = 11;  // producers 0 and 2, MMA 1, softmax 3..10
     static constexpr int THREADS = NWARPS * 32;
-    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+    static_assert(SMEM_BYTES + STATIC_SMEM <= 227 * 1024, "shared memory budget");
 };
 
 struct TcMaps {
-    CUtensorMap q;  // 2D: [B*Hq rows, D] box (64, G)
-    CUtensorMap k;  // 3D: [B*S_max, Hkv, D] box (64, 1, 64)
+    CUtensorMap q;     // 2D: [B*Hq rows, D] box (64, G), 128-byte swizzle
+    CUtensorMap k;     // 3D: [B*S_max, Hkv, D] box (64, 1, 64), 128-byte swizzle
     CUtensorMap v;
+    CUtensorMap k_pf;  // same tensors, box (D, 1, 64) unswizzled: one L2 prefetch per tile
+    CUtensorMap v_pf;
 };
 
 template <int D, bool F32OUT>
@@ -85,6 +90,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
     __shared__ long long s_red[NW];
     __shared__ int s_redi[NW];
     __shared__ long long s_cum0;
+    __shared__ float xbuf[2 * 4 * 32];  // [exchange parity][quarter][half][16 rows]
 
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sbase = smem_u32(smem);
@@ -104,6 +110,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
     // phase of the completion it waits for, so parity waits are unambiguous.
     auto o_fin = [&](int b) { return q_empty + 8u * (7 + b); };
     const uint32_t mma_done = q_empty + 8u * 9;
+    auto xbar = [&](int q) { return q_empty + 8u * (10 + q); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Sh::OFF_MISC + 8);
     // P buffer b, part (0 = hi, 1 = lo)
@@ -127,11 +134,12 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
         tc::mbar_init(q_empty, 1);
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(s_full(b), 1);
-            tc::mbar_init(s_free(b), 4);
-            tc::mbar_init(p_full(b), 4);
+            tc::mbar_init(s_free(b), 8);
+            tc::mbar_init(p_full(b), 8);
             tc::mbar_init(o_fin(b), 1);
         }
         tc::mbar_init(mma_done, 1);
+        for (int q = 0; q < 4; ++q) tc::mbar_init(xbar(q), 2);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
@@ -199,19 +207,21 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
             int j = 0, qn = 0;
             const int NS = is_k ? KST : VST;
             const CUtensorMap* map = is_k ? &maps.k : &maps.v;
+            const CUtensorMap* pf_map = is_k ? &maps.k_pf : &maps.v_pf;
             // A second walker runs kPrefetch tiles ahead and warms L2 with them, so the
-            // HBM latency is paid before a shared-memory stage frees up.
+            // HBM latency is paid before a shared-memory stage frees up. The first
+            // tile's own loads go out before any prefetch.
             constexpr int kPrefetch = 3;
             Walker<DevLen> ahead = walker;
-            auto prefetch = [&](const Tile& x) {
-                const int r = x.b * p.S_max + x.tok_lo;
-#pragma unroll
-                for (int kb = 0; kb < KB; ++kb) tc::tma_prefetch_3d(map, kb * 64, x.h, r);
+            int n_ahead = 0;
+            auto prefetch_next = [&]() {
+                if (ahead.next(pt, NoOp{})) {
+                    if (n_ahead > 0) tc::tma_prefetch_3d(pf_map, 0, pt.h, pt.b * p.S_max + pt.tok_lo);
+                    ++n_ahead;
+                }
             };
-            for (int a = 0; a < kPrefetch; ++a)
-                if (ahead.next(pt, NoOp{})) prefetch(pt);
+            prefetch_next();  // the first tile itself is loaded below, not prefetched
             while (walker.next(t, NoOp{})) {
-                if (ahead.next(pt, NoOp{})) prefetch(pt);
                 if (is_k && t.seg_start) {
                     if (!tc::mbar_wait(q_empty, (qn & 1) ^ 1, abort_flag, kBudget)) break;
                     tc::mbar_arrive_expect_tx(q_full, (uint32_t)(KB * 128 * G));
@@ -232,6 +242,10 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
                 for (int kb = 0; kb < KB; ++kb)
                     tc::tma_load_3d(dst + kb * Sh::KB_BYTES, map, kb * 64, t.h, row, full, pol_kv);
                 ++j;
+                if (j == 1)
+                    for (int a = 0; a < kPrefetch; ++a) prefetch_next();
+                else
+                    prefetch_next();
             }
             // Do not leave with copies in flight: wait for the last loads to land.
             for (int jj = (j > NS ? j - NS : 0); jj < j; ++jj) {
@@ -324,30 +338,53 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
             tc::mbar_wait(mma_done, 0, abort_flag, kBudget);
         }
     } else {
-        // ===================== softmax / epilogue (warps 3..6) =====================
-        const int quarter = warp & 3;                 // TMEM lanes [32*quarter, +32)
-        const int row = quarter * 16 + lane;          // group-local query head of this thread
+        // ===================== softmax / epilogue (warps 3..10) =====================
+        // Two warps serve each TMEM lane quarter (a warp reaches the 32 lanes
+        // 32 * (warp % 4) ...): the warp of half 0 takes token columns [0, 32)
+        // of every S tile and output columns [0, D/2), the other the upper
+        // halves. Row maxima and row sums are exchanged between the two through
+        // shared memory, synchronised by a two-arrival mbarrier per quarter
+        // (bounded waits, so an abort cannot strand the partner warp).
+        constexpr int HT = T / 2;   // token columns per half
+        constexpr int HD = D / 2;   // output columns per half
+        const int sw = warp - 3;    // 0..7
+        const int quarter = warp & 3;
+        const int half = sw >> 2;
+        const int row = quarter * 16 + lane;   // group-local query head of this thread
         const bool has_row = lane < 16;
         const bool active = has_row && row < G;
-        const int st = tid - 3 * 32;                  // 0..127 among the softmax threads
+        const int st = tid - 3 * 32;           // 0..255 among the softmax threads
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const float scale_log2 = p.scale_log2;
+        int nx = 0;  // exchanges done with the partner warp
+
+        // Exchange one float per row with the partner warp; returns the partner's.
+        auto exchange = [&](float v, bool& ok_) -> float {
+            float* buf = xbuf + ((nx & 1) * 4 + quarter) * 32;
+            if (has_row) buf[half * 16 + lane] = v;
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(xbar(quarter));
+            ok_ = __all_sync(0xffffffffu, tc::mbar_wait(xbar(quarter), nx & 1, abort_flag, kBudget));
+            const float other = buf[(half ^ 1) * 16 + (lane & 15)];
+            ++nx;
+            return other;
+        };
 
         auto write_empty = [&](int b, int h) {
             const size_t r0 = (size_t)b * p.Hq + (size_t)h * G;
             if constexpr (F32OUT) {
                 float* o = reinterpret_cast<float*>(p.out) + r0 * D;
-                for (int i2 = st; i2 < G * D; i2 += 128) o[i2] = 0.f;
+                for (int i2 = st; i2 < G * D; i2 += 256) o[i2] = 0.f;
             } else {
                 __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + r0 * D;
-                for (int i2 = st; i2 < G * D; i2 += 128) o[i2] = __float2bfloat16_rn(0.f);
+                for (int i2 = st; i2 < G * D; i2 += 256) o[i2] = __float2bfloat16_rn(0.f);
             }
             if (p.lse)
-                for (int i2 = st; i2 < G; i2 += 128) p.lse[r0 + i2] = -CUDART_INF_F;
+                for (int i2 = st; i2 < G; i2 += 256) p.lse[r0 + i2] = -CUDART_INF_F;
             if (st == 0 && p.ws_rec) p.ws_rec[(size_t)b * p.Hkv + h] = make_int2(-1, -1);
         };
 
-        float m_used = 0.f, l = 0.f;
+        float m_used = 0.f, l = 0.f;  // l: this half's share of the row sum
         Tile t;
         int i = 0;
         bool ok = true;
@@ -357,22 +394,29 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
             if (!ok) break;
             tc::fence_after_sync();
             __syncwarp();
-            uint32_t sr[T];
-            tc::tmem_ld32(tmem + lane_base + Sh::TMEM_S + sb * T, *reinterpret_cast<uint32_t(*)[32]>(&sr[0]));
-            tc::tmem_ld32(tmem + lane_base + Sh::TMEM_S + sb * T + 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[32]));
+            uint32_t sr[HT];
+            tc::tmem_ld32(tmem + lane_base + Sh::TMEM_S + sb * T + half * HT, sr);
             tc::tmem_wait_ld();
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(s_free(sb));
 
+            // Scores in base-2 units; columns past the tile's last token masked.
             const int nvalid = t.tok_hi - t.tok_lo;
-            float s[T];
-            float mt = -CUDART_INF_F;
+            const int nv = nvalid - half * HT;  // valid columns of this half (may be <= 0)
+            float s[HT];
 #pragma unroll
-            for (int k = 0; k < T; ++k) {
-                s[k] = (k < nvalid) ? __uint_as_float(sr[k]) * scale_log2 : -CUDART_INF_F;
-                mt = fmaxf(mt, s[k]);
-            }
+            for (int k = 0; k < HT; ++k)
+                s[k] = (k < nv) ? __uint_as_float(sr[k]) * scale_log2 : -CUDART_INF_F;
+            float mx[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) mx[k] = fmaxf(fmaxf(s[k], s[k + 8]), fmaxf(s[k + 16], s[k + 24]));
+#pragma unroll
+            for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], mx[k + 4]);
+            const float mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+            const float mt = fmaxf(mh, exchange(mh, ok));
+            if (!ok) break;
+
             bool need = false;
             float alpha = 1.f;
             if (t.seg_start) {
@@ -388,9 +432,9 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
                 if (!ok) break;
                 tc::fence_after_sync();
 #pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
+                for (int cc = 0; cc < HD / 32; ++cc) {
                     uint32_t r[32];
-                    const uint32_t ta = tmem + lane_base + Sh::TMEM_O + cc * 32;
+                    const uint32_t ta = tmem + lane_base + Sh::TMEM_O + half * HD + cc * 32;
                     __syncwarp();
                     tc::tmem_ld32(ta, r);
                     tc::tmem_wait_ld();
@@ -399,10 +443,10 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
                     tc::tmem_st32(ta, r);
                 }
                 tc::tmem_wait_st();
-                if (need) {
-                    l *= alpha;
-                    m_used = mt;
-                }
+            }
+            if (need) {
+                l *= alpha;
+                m_used = mt;
             }
 
             // P buffer sb is free once the P V of tile i - 2 has completed.
@@ -413,13 +457,13 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
                 const uint32_t prow_lo = p_buf(sb, Sh::NP - 1) + (uint32_t)row * 128;
                 float ls = 0.f;
 #pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
+                for (int ch = 0; ch < 4; ++ch) {
                     uint32_t hi[4], lo[4];
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
                         const int k = ch * 8 + e * 2;
-                        const float e0 = active ? exp2f(s[k] - m_used) : 0.f;
-                        const float e1 = active ? exp2f(s[k + 1] - m_used) : 0.f;
+                        const float e0 = active ? tc::ex2_approx(s[k] - m_used) : 0.f;
+                        const float e1 = active ? tc::ex2_approx(s[k + 1] - m_used) : 0.f;
                         hi[e] = pack_bf16x2(e0, e1);
                         if constexpr (F32OUT) {
                             lo[e] = pack_bf16x2(e0 - bf16_lo(hi[e]), e1 - bf16_hi(hi[e]));
@@ -428,7 +472,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
                             ls += bf16_lo(hi[e]) + bf16_hi(hi[e]);
                         }
                     }
-                    const uint32_t off = (uint32_t)((ch ^ (row & 7)) * 16);
+                    const uint32_t off = (uint32_t)(((half * 4 + ch) ^ (row & 7)) * 16);
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(prow + off), "r"(hi[0]),
                                  "r"(hi[1]), "r"(hi[2]), "r"(hi[3]) : "memory");
                     if constexpr (F32OUT)
@@ -445,7 +489,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
                 if (!ok) break;
                 uint8_t* vt = smem + Sh::OFF_V + sv * Sh::TILE_BYTES;
                 const int n16 = (T - nvalid) * KB * 8;
-                for (int idx = st; idx < n16; idx += 128) {
+                for (int idx = st; idx < n16; idx += 256) {
                     const int r = nvalid + idx / (KB * 8);
                     const int rem = idx % (KB * 8);
                     *reinterpret_cast<uint4*>(vt + (rem >> 3) * Sh::KB_BYTES + r * 128 + (rem & 7) * 16) =
@@ -458,29 +502,32 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
             if (lane == 0) tc::mbar_arrive(p_full(sb));
 
             if (t.seg_end) {
+                const float ltot = l + exchange(l, ok);
+                if (!ok) break;
                 ok = __all_sync(0xffffffffu, tc::mbar_wait(o_fin(sb), (i >> 1) & 1, abort_flag, kBudget));
                 if (!ok) break;
                 tc::fence_after_sync();
                 const size_t pair = (size_t)t.b * p.Hkv + t.h;
                 const size_t qrow = (size_t)t.b * p.Hq + (size_t)t.h * G + row;
                 const size_t slot = (size_t)c + pair;
-                const float inv = (l > 0.f) ? 1.f / l : 0.f;
+                const float inv = (ltot > 0.f) ? 1.f / ltot : 0.f;
 #pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
+                for (int cc = 0; cc < HD / 32; ++cc) {
                     uint32_t r[32];
+                    const int col = half * HD + cc * 32;
                     __syncwarp();
-                    tc::tmem_ld32(tmem + lane_base + Sh::TMEM_O + cc * 32, r);
+                    tc::tmem_ld32(tmem + lane_base + Sh::TMEM_O + col, r);
                     tc::tmem_wait_ld();
                     if (!active) {
                     } else if (t.full) {
                         if constexpr (F32OUT) {
-                            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + qrow * D + cc * 32);
+                            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + qrow * D + col);
 #pragma unroll
                             for (int k = 0; k < 8; ++k)
                                 o[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
                                                    __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
                         } else {
-                            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + qrow * D + cc * 32);
+                            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + qrow * D + col);
 #pragma unroll
                             for (int k = 0; k < 4; ++k)
                                 o[k] = make_uint4(
@@ -490,7 +537,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
                                     pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv));
                         }
                     } else {
-                        float4* o = reinterpret_cast<float4*>(p.ws_o + (slot * G + row) * D + cc * 32);
+                        float4* o = reinterpret_cast<float4*>(p.ws_o + (slot * G + row) * D + col);
 #pragma unroll
                         for (int k = 0; k < 8; ++k)
                             o[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
@@ -498,11 +545,11 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
                     }
                 }
                 tc::fence_before_sync();
-                if (active) {
+                if (active && half == 0) {
                     if (t.full) {
-                        if (p.lse) p.lse[qrow] = (m_used + log2f(l)) * 0.69314718055994531f;
+                        if (p.lse) p.lse[qrow] = (m_used + log2f(ltot)) * 0.69314718055994531f;
                     } else {
-                        p.ws_ml[slot * G + row] = make_float2(m_used, l);
+                        p.ws_ml[slot * G + row] = make_float2(m_used, ltot);
                     }
                 }
                 // Only the pair's owner writes its merge record.
