@@ -25,7 +25,7 @@ const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out) {
 
 const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out) {
     if (group < 1 || group > KVD_MAX_GROUP) return nullptr;
-    return group <= 16 ? mma_chunk_kernel(head_dim, f32_out) : tc_chunk_kernel(head_dim, f32_out);
+    return group <= 16 ? mma_chunk_kernel(head_dim, f32_out) : tc_chunk_kernel(head_dim, f32_out, group);
 }
 
 namespace {

@@ -29,14 +29,14 @@ struct ChunkKernel {
     cudaError_t (*launch)(const struct ChunkKernel& k, const DecodeParams& p, cudaStream_t s);
     int head_dim, threads, smem_bytes, tile_tokens, ctas_per_sm;
     bool f32_out, tensor_core;
-    int index;  // position in the variant table (0..11)
+    int index;  // position in the variant table (0..17)
 };
 
 // The kernel for a shape: groups of up to 16 query heads per KV head run on the
 // mma.sync kernel, wider groups (17..64) on the tcgen05 kernel.
 const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out);
 const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out);
-const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out);
+const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out, int group);
 
 cudaError_t launch_merge(const DecodeParams& p, int head_dim, bool f32_out, cudaStream_t stream);
 cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,

@@ -37,7 +37,7 @@ bool encode(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims, 
 
 }  // namespace
 
-template <int D, bool F32>
+template <int D, bool F32, int QR>
 cudaError_t launch_tc_chunk(const ChunkKernel& k, const DecodeParams& p, cudaStream_t stream) {
     TcMaps maps;
     std::memset(&maps, 0, sizeof maps);
@@ -50,12 +50,9 @@ cudaError_t launch_tc_chunk(const ChunkKernel& k, const DecodeParams& p, cudaStr
     {
         const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hkv, (cuuint64_t)p.B * p.S_max};
         const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.Hkv * D * 2};
-        const cuuint32_t box[3] = {64, 1, (cuuint32_t)TcShape<D, F32>::T};
+        const cuuint32_t box[3] = {64, 1, (cuuint32_t)TcShape<D, F32, QR>::T};
         if (!encode(&maps.k, p.k, 3, dims, strides, box)) return cudaErrorInvalidValue;
         if (!encode(&maps.v, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
-        const cuuint32_t pf_box[3] = {(cuuint32_t)D, 1, (cuuint32_t)TcShape<D, F32>::T};
-        if (!encode(&maps.k_pf, p.k, 3, dims, strides, pf_box, false)) return cudaErrorInvalidValue;
-        if (!encode(&maps.v_pf, p.v, 3, dims, strides, pf_box, false)) return cudaErrorInvalidValue;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.n_split, 1, 1);
@@ -67,15 +64,15 @@ cudaError_t launch_tc_chunk(const ChunkKernel& k, const DecodeParams& p, cudaStr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kv_chunk_tc_kernel<D, F32>, p, maps);
+    return cudaLaunchKernelEx(&cfg, split_kv_chunk_tc_kernel<D, F32, QR>, p, maps);
 }
 
-template <int D, bool F32>
+template <int D, bool F32, int QR>
 static ChunkKernel make_tc(int index) {
-    using Sh = TcShape<D, F32>;
+    using Sh = TcShape<D, F32, QR>;
     ChunkKernel k;
-    k.fn = reinterpret_cast<const void*>(split_kv_chunk_tc_kernel<D, F32>);
-    k.launch = launch_tc_chunk<D, F32>;
+    k.fn = reinterpret_cast<const void*>(split_kv_chunk_tc_kernel<D, F32, QR>);
+    k.launch = launch_tc_chunk<D, F32, QR>;
     k.head_dim = D;
     k.threads = Sh::THREADS;
     k.smem_bytes = Sh::SMEM_BYTES;
@@ -87,14 +84,19 @@ static ChunkKernel make_tc(int index) {
     return k;
 }
 
-const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out) {
-    static const ChunkKernel table[3][2] = {
-        {make_tc<64, false>(6), make_tc<64, true>(7)},
-        {make_tc<128, false>(8), make_tc<128, true>(9)},
-        {make_tc<256, false>(10), make_tc<256, true>(11)},
+// Groups of up to 48 query heads store Q in 48-row blocks (saving shared
+// memory for a third K stage); wider groups in 64-row blocks.
+const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out, int group) {
+    static const ChunkKernel table[3][2][2] = {
+        {{make_tc<64, false, 48>(6), make_tc<64, true, 48>(7)}, {make_tc<64, false, 64>(8), make_tc<64, true, 64>(9)}},
+        {{make_tc<128, false, 48>(10), make_tc<128, true, 48>(11)},
+         {make_tc<128, false, 64>(12), make_tc<128, true, 64>(13)}},
+        {{make_tc<256, false, 48>(14), make_tc<256, true, 48>(15)},
+         {make_tc<256, false, 64>(16), make_tc<256, true, 64>(17)}},
     };
     const int d = head_dim == 64 ? 0 : (head_dim == 128 ? 1 : (head_dim == 256 ? 2 : -1));
-    return d < 0 ? nullptr : &table[d][f32_out ? 1 : 0];
+    if (d < 0 || group < 1 || group > 64) return nullptr;
+    return &table[d][group <= 48 ? 0 : 1][f32_out ? 1 : 0];
 }
 
 }  // namespace kvd

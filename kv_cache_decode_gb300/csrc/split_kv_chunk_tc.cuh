@@ -40,49 +40,57 @@
 
 namespace kvd {
 
-template <int D, bool F32OUT>
+template <int D, bool F32OUT, int QR>
 struct TcShape {
     static constexpr int T = 64;                 // tokens per tile
     static constexpr int KB = D / 64;            // 128-byte swizzle atoms across head_dim
     static constexpr int TILE_BYTES = T * D * 2; // one K (or V) tile
     static constexpr int KB_BYTES = T * 128;     // one 64-column block of a tile
-    static constexpr int Q_BYTES = 64 * D * 2;   // 64 rows (group padded)
-    // fp32-output mode carries a second (low) P buffer, so it keeps one K stage fewer.
-    static constexpr int KST = D == 256 ? (F32OUT ? 2 : 3) : (D == 128 ? 5 : 8);
-    static constexpr int VST = D == 256 ? 2 : (D == 128 ? 4 : 6);
+    // Q is stored as KB blocks of QR rows (the group rounded up to 8, capped at
+    // 64). The M = 64 MMA reads 64 rows from each block start; for QR < 64 the
+    // extra rows alias the next block (or the K ring after Q): they only feed
+    // accumulator rows of padded heads, which are never used.
+    static constexpr int QB_BYTES = QR * 128;
+    static constexpr int Q_BYTES = KB * QB_BYTES;
     static constexpr int P_BYTES = 64 * T * 2;   // one P buffer (64 rows x 64 tokens)
     static constexpr int NP = F32OUT ? 2 : 1;    // hi (and lo) parts of P
+    // Stage counts: three V stages (a V stage is held until P V of its tile is
+    // done, so the V ring needs the depth), K stages as the budget allows.
+    static constexpr int VST = D == 256 ? 3 : (D == 128 ? 5 : 8);
+    static constexpr int BUDGET = 224 * 1024 - Q_BYTES - NP * P_BYTES - VST * TILE_BYTES;
+    static constexpr int KST_FIT = BUDGET / TILE_BYTES;
+    static constexpr int KST = KST_FIT > 8 ? 8 : KST_FIT;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
     static constexpr int OFF_V = OFF_K + KST * TILE_BYTES;
     static constexpr int OFF_P = OFF_V + VST * TILE_BYTES;
-    static constexpr int OFF_BAR = OFF_P + 2 * NP * P_BYTES;
+    static constexpr int OFF_BAR = OFF_P + NP * P_BYTES;
     // barriers: k_full, k_empty [KST]; v_full, v_empty [VST]; q_full, q_empty;
     // s_full, s_free, p_full, o_fin [2]; mma_done; xbar [4]
     static constexpr int NBAR = 2 * KST + 2 * VST + 2 + 8 + 1 + 4;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
-    static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + alignment slack
+    static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int STATIC_SMEM = 2048;  // block scans and the exchange buffer (checked by ptxas -v)
     static constexpr int TMEM_S = 0;             // S buffers at columns 0 and T
     static constexpr int TMEM_O = 2 * T;         // O at columns [2T, 2T + D)
     static constexpr int TMEM_COLS = (2 * T + D) <= 256 ? 256 : 512;
     static constexpr int NWARPS = 11;  // producers 0 and 2, MMA 1, softmax 3..10
     static constexpr int THREADS = NWARPS * 32;
+    static_assert(KST >= 2, "need at least two K stages");
     static_assert(SMEM_BYTES + STATIC_SMEM <= 227 * 1024, "shared memory budget");
+    static_assert(QR % 8 == 0 && QR <= 64, "Q rows per block");
 };
 
 struct TcMaps {
-    CUtensorMap q;     // 2D: [B*Hq rows, D] box (64, G), 128-byte swizzle
-    CUtensorMap k;     // 3D: [B*S_max, Hkv, D] box (64, 1, 64), 128-byte swizzle
+    CUtensorMap q;  // 2D: [B*Hq rows, D] box (64, G), 128-byte swizzle
+    CUtensorMap k;  // 3D: [B*S_max, Hkv, D] box (64, 1, 64), 128-byte swizzle
     CUtensorMap v;
-    CUtensorMap k_pf;  // same tensors, box (D, 1, 64) unswizzled: one L2 prefetch per tile
-    CUtensorMap v_pf;
 };
 
-template <int D, bool F32OUT>
-__global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
+template <int D, bool F32OUT, int QR>
+__global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     split_kv_chunk_tc_kernel(const DecodeParams p, const __grid_constant__ TcMaps maps) {
-    using Sh = TcShape<D, F32OUT>;
+    using Sh = TcShape<D, F32OUT, QR>;
     constexpr int T = Sh::T, KB = Sh::KB, KST = Sh::KST, VST = Sh::VST, NW = Sh::NWARPS;
     constexpr long long kBudget = 4000000000LL;  // ~2 s of clock cycles per wait
 
@@ -92,7 +100,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
     __shared__ long long s_cum0;
     __shared__ float xbuf[2 * 4 * 32];  // [exchange parity][quarter][half][16 rows]
 
-    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* smem = smem_raw;  // 1024-byte aligned (128-byte swizzle atoms need it)
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + Sh::OFF_Q, sK = sbase + Sh::OFF_K, sV = sbase + Sh::OFF_V,
                    sP = sbase + Sh::OFF_P, sBar = sbase + Sh::OFF_BAR;
@@ -113,14 +121,20 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
     auto xbar = [&](int q) { return q_empty + 8u * (10 + q); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Sh::OFF_MISC + 8);
-    // P buffer b, part (0 = hi, 1 = lo)
-    auto p_buf = [&](int b, int part) { return sP + (uint32_t)((b * Sh::NP + part) * Sh::P_BYTES); };
+    // The P buffer, part 0 = hi, 1 = lo. One buffer: P(i) is written only once
+    // P(i-1) V(i-1) has completed.
+    auto p_buf = [&](int /*tile parity*/, int part) { return sP + (uint32_t)(part * Sh::P_BYTES); };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = blockIdx.x;
     const int G = p.G;
 
     // ---- set-up (reads no inputs, so it overlaps the previous kernel's tail) ----
+    if (tid == 32) {
+        asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&maps.q)) : "memory");
+        asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&maps.k)) : "memory");
+        asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&maps.v)) : "memory");
+    }
     if (tid == 0) {
         for (int s = 0; s < KST; ++s) {
             tc::mbar_init(k_full(s), 1);
@@ -146,7 +160,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
     // Rows of Q past the group, and P rows of padded heads, stay zero.
     for (int i = tid; i < Sh::Q_BYTES / 16; i += Sh::THREADS)
         reinterpret_cast<uint4*>(smem + Sh::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
-    for (int i = tid; i < 2 * Sh::NP * Sh::P_BYTES / 16; i += Sh::THREADS)
+    for (int i = tid; i < Sh::NP * Sh::P_BYTES / 16; i += Sh::THREADS)
         reinterpret_cast<uint4*>(smem + Sh::OFF_P)[i] = make_uint4(0, 0, 0, 0);
     tc::fence_proxy_async_smem();
     if (warp == 1) tc::tmem_alloc(smem_u32(tmem_slot), Sh::TMEM_COLS);
@@ -203,24 +217,10 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
             const bool is_k = (warp == 0);
             const uint64_t pol_kv = l2_evict_first_policy();
             const uint64_t pol_q = tc::l2_evict_last_policy();
-            Tile t, pt;
+            Tile t;
             int j = 0, qn = 0;
             const int NS = is_k ? KST : VST;
             const CUtensorMap* map = is_k ? &maps.k : &maps.v;
-            const CUtensorMap* pf_map = is_k ? &maps.k_pf : &maps.v_pf;
-            // A second walker runs kPrefetch tiles ahead and warms L2 with them, so the
-            // HBM latency is paid before a shared-memory stage frees up. The first
-            // tile's own loads go out before any prefetch.
-            constexpr int kPrefetch = 3;
-            Walker<DevLen> ahead = walker;
-            int n_ahead = 0;
-            auto prefetch_next = [&]() {
-                if (ahead.next(pt, NoOp{})) {
-                    if (n_ahead > 0) tc::tma_prefetch_3d(pf_map, 0, pt.h, pt.b * p.S_max + pt.tok_lo);
-                    ++n_ahead;
-                }
-            };
-            prefetch_next();  // the first tile itself is loaded below, not prefetched
             while (walker.next(t, NoOp{})) {
                 if (is_k && t.seg_start) {
                     if (!tc::mbar_wait(q_empty, (qn & 1) ^ 1, abort_flag, kBudget)) break;
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
                     const int qrow = t.b * p.Hq + t.h * G;
 #pragma unroll
                     for (int kb = 0; kb < KB; ++kb)
-                        tc::tma_load_2d(sQ + kb * 8192, &maps.q, kb * 64, qrow, q_full, pol_q);
+                        tc::tma_load_2d(sQ + kb * Sh::QB_BYTES, &maps.q, kb * 64, qrow, q_full, pol_q);
                     ++qn;
                 }
                 const int s = j % NS;
@@ -242,10 +242,6 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
                 for (int kb = 0; kb < KB; ++kb)
                     tc::tma_load_3d(dst + kb * Sh::KB_BYTES, map, kb * 64, t.h, row, full, pol_kv);
                 ++j;
-                if (j == 1)
-                    for (int a = 0; a < kPrefetch; ++a) prefetch_next();
-                else
-                    prefetch_next();
             }
             // Do not leave with copies in flight: wait for the last loads to land.
             for (int jj = (j > NS ? j - NS : 0); jj < j; ++jj) {
@@ -266,7 +262,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
                 const uint32_t kt = sK + (uint32_t)(sk * Sh::TILE_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = tc::sdesc_sw128(sQ + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+                    const uint64_t a = tc::sdesc_sw128(sQ + (kk >> 2) * Sh::QB_BYTES + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = tc::sdesc_sw128(kt + (kk >> 2) * Sh::KB_BYTES + (kk & 3) * 32, 16, 1024);
                     tc::mma_bf16(tmem + Sh::TMEM_S + sb * T, a, b, idesc_s, kk > 0);
                 }
@@ -425,12 +421,34 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
             } else if (mt > m_used + 8.f) {
                 need = true;
                 alpha = exp2f(m_used - mt);
+                m_used = mt;
             }
-            if (__any_sync(0xffffffffu, need && has_row)) {
-                // O must hold the previous tile's P V before it is rescaled.
+            // P = 2^(s - m) into registers (bf16 hi part; lo part for fp32 output).
+            uint32_t hi[HT / 2], lo[F32OUT ? HT / 2 : 1];
+            float ls = 0.f;
+#pragma unroll
+            for (int k2 = 0; k2 < HT / 2; ++k2) {
+                const float e0 = active ? tc::ex2_approx(s[2 * k2] - m_used) : 0.f;
+                const float e1 = active ? tc::ex2_approx(s[2 * k2 + 1] - m_used) : 0.f;
+                hi[k2] = pack_bf16x2(e0, e1);
+                if constexpr (F32OUT) {
+                    lo[k2] = pack_bf16x2(e0 - bf16_lo(hi[k2]), e1 - bf16_hi(hi[k2]));
+                    ls += e0 + e1;
+                } else {
+                    // The weights actually multiplied into V are the rounded ones;
+                    // summing those keeps the output an exact convex combination.
+                    ls += bf16_lo(hi[k2]) + bf16_hi(hi[k2]);
+                }
+            }
+
+            // O += P(i-1) V(i-1) must have completed: it reads the P buffer, and O
+            // is rescaled below if the running maximum moved.
+            if (i > 0) {
                 ok = __all_sync(0xffffffffu, tc::mbar_wait(o_fin((i - 1) & 1), ((i - 1) >> 1) & 1, abort_flag, kBudget));
                 if (!ok) break;
                 tc::fence_after_sync();
+            }
+            if (__any_sync(0xffffffffu, need && has_row)) {
 #pragma unroll 1
                 for (int cc = 0; cc < HD / 32; ++cc) {
                     uint32_t r[32];
@@ -444,42 +462,19 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT>::THREADS, 1)
                 }
                 tc::tmem_wait_st();
             }
-            if (need) {
-                l *= alpha;
-                m_used = mt;
-            }
-
-            // P buffer sb is free once the P V of tile i - 2 has completed.
-            ok = __all_sync(0xffffffffu, tc::mbar_wait(o_fin(sb), ((i >> 1) & 1) ^ 1, abort_flag, kBudget));
-            if (!ok) break;
+            l = l * alpha + ls;
             if (has_row) {
                 const uint32_t prow = p_buf(sb, 0) + (uint32_t)row * 128;
                 const uint32_t prow_lo = p_buf(sb, Sh::NP - 1) + (uint32_t)row * 128;
-                float ls = 0.f;
 #pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t hi[4], lo[4];
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int k = ch * 8 + e * 2;
-                        const float e0 = active ? tc::ex2_approx(s[k] - m_used) : 0.f;
-                        const float e1 = active ? tc::ex2_approx(s[k + 1] - m_used) : 0.f;
-                        hi[e] = pack_bf16x2(e0, e1);
-                        if constexpr (F32OUT) {
-                            lo[e] = pack_bf16x2(e0 - bf16_lo(hi[e]), e1 - bf16_hi(hi[e]));
-                            ls += e0 + e1;
-                        } else {
-                            ls += bf16_lo(hi[e]) + bf16_hi(hi[e]);
-                        }
-                    }
                     const uint32_t off = (uint32_t)(((half * 4 + ch) ^ (row & 7)) * 16);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(prow + off), "r"(hi[0]),
-                                 "r"(hi[1]), "r"(hi[2]), "r"(hi[3]) : "memory");
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(prow + off), "r"(hi[4 * ch]),
+                                 "r"(hi[4 * ch + 1]), "r"(hi[4 * ch + 2]), "r"(hi[4 * ch + 3]) : "memory");
                     if constexpr (F32OUT)
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(prow_lo + off), "r"(lo[0]),
-                                     "r"(lo[1]), "r"(lo[2]), "r"(lo[3]) : "memory");
+                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(prow_lo + off), "r"(lo[4 * ch]),
+                                     "r"(lo[4 * ch + 1]), "r"(lo[4 * ch + 2]), "r"(lo[4 * ch + 3]) : "memory");
                 }
-                l += ls;
             }
             if (nvalid < T) {
                 // Rows past the sequence's end came from the cache's padding (or the
