@@ -304,9 +304,9 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                 bool progress = false;
                 if (s_idx < n_fetched && s_idx < o_idx + 3) {
                     const Tile& t = tq[s_idx & 3];
-                    if (tc::mbar_try_wait(k_full(s_idx % KST), (s_idx / KST) & 1) &&
-                        tc::mbar_try_wait(s_free(s_idx & 1), ((s_idx >> 1) & 1) ^ 1) &&
-                        (!t.seg_start || tc::mbar_try_wait(q_full, qn & 1))) {
+                    if (tc::mbar_test(k_full(s_idx % KST), (s_idx / KST) & 1) &&
+                        tc::mbar_test(s_free(s_idx & 1), ((s_idx >> 1) & 1) ^ 1) &&
+                        (!t.seg_start || tc::mbar_test(q_full, qn & 1))) {
                         if (t.seg_start) ++qn;
                         mma_s(t, s_idx);
                         ++s_idx;
@@ -315,8 +315,8 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                 }
                 if (o_idx < s_idx) {
                     const Tile& t = tq[o_idx & 3];
-                    if (tc::mbar_try_wait(v_full(o_idx % VST), (o_idx / VST) & 1) &&
-                        tc::mbar_try_wait(p_full(o_idx & 1), (o_idx >> 1) & 1)) {
+                    if (tc::mbar_test(v_full(o_idx % VST), (o_idx / VST) & 1) &&
+                        tc::mbar_test(p_full(o_idx & 1), (o_idx >> 1) & 1)) {
                         mma_o(t, o_idx);
                         ++o_idx;
                         progress = true;
