@@ -204,6 +204,38 @@ kvd_status kvd_kernel_info(int n_heads_q, int n_heads_kv, int head_dim, kvd_out_
                            int* threads_out, int* smem_bytes_out, int* tile_tokens_out,
                            int* ctas_per_sm_out);
 
+/*
+ * kvd_decode_attention_static: kvd_decode_attention for callers that cannot
+ * allocate device memory. (The sources have no counterpart: this is a
+ * deployment convenience, not part of the method.)
+ *
+ * Some callers may not allocate at decode time: a serving loop whose device
+ * memory is budgeted and frozen at start-up, a plugin handed only the tensors
+ * it works on, or a path that must not risk the device-wide synchronisation
+ * that cudaMalloc/cudaFree can cause. This entry point takes the same
+ * arguments as kvd_decode_attention without workspace/workspace_bytes and
+ * uses instead a scratch array inside the library: a __device__ array of
+ * KVD_STATIC_WORKSPACE_BYTES that every GPU loading the library holds until
+ * the process exits. It allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library call); inputs and outputs stay the caller's.
+ *   - Limit: if kvd_decode_plan's workspace for the call exceeds
+ *     KVD_STATIC_WORKSPACE_BYTES, the call returns KVD_ERR_WORKSPACE_TOO_SMALL
+ *     and launches nothing (a smaller n_split lowers the need).
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents.
+ *     Nothing in it needs to start at zero, but calls that overlap on the GPU
+ *     (e.g. on two streams) race on it: serialise them.
+ * Other arguments, errors and results as kvd_decode_attention.
+ */
+#define KVD_STATIC_WORKSPACE_BYTES ((size_t)16 << 20)
+kvd_status kvd_decode_attention_static(const void* q, const void* k_cache, const void* v_cache,
+                                       const int32_t* seq_lens, int batch, int s_max, int max_seq_len,
+                                       int n_heads_q, int n_heads_kv, int head_dim, float scale,
+                                       int n_split, void* out, kvd_out_dtype out_dtype, float* lse_out,
+                                       int32_t* status_word, kvd_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* kvd_status_string(kvd_status s);
 

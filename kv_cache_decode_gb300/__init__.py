@@ -29,8 +29,9 @@ STATUS_POS_OUT_OF_RANGE = 0x2
 EXPORTED = (
     "kvd_decode_plan", "kvd_kv_append", "kvd_decode_attention", "kvd_split_kv_chunk",
     "kvd_split_kv_merge", "kvd_schedule_describe", "kvd_kernel_info", "kvd_status_string",
-    "kvd_version",
+    "kvd_version", "kvd_decode_attention_static",
 )
+STATIC_WORKSPACE_BYTES = 16 << 20  # KVD_STATIC_WORKSPACE_BYTES
 
 _lock = threading.Lock()
 _lib = None
@@ -67,6 +68,8 @@ def _declare(lib):
     dec = [P, P, P, P, I, I, I, I, I, I, F, I, P, SZ, P, I, P, P, P]
     for name in ("kvd_decode_attention", "kvd_split_kv_chunk", "kvd_split_kv_merge"):
         getattr(lib, name).argtypes = dec
+    lib.kvd_decode_attention_static.argtypes = [P, P, P, P, I, I, I, I, I, I, F, I, P, I, P, P, P]
+    lib.kvd_decode_attention_static.restype = I
     lib.kvd_schedule_describe.argtypes = [P, I, I, I, I, I, I, I, I, P, I, PI, PI]
     lib.kvd_kernel_info.argtypes = [I, I, I, I, PI, PI, PI, PI]
     lib.kvd_status_string.argtypes = [I]
@@ -246,6 +249,16 @@ def decode_attention(q, k_cache, v_cache, seq_lens, max_seq_len: int, scale: flo
     args = _decode_args(q, k_cache, v_cache, seq_lens, max_seq_len, scale, n_split, workspace,
                         out, lse, status, stream)
     _check(load().kvd_decode_attention(*args), "kvd_decode_attention")
+
+
+def decode_attention_static(q, k_cache, v_cache, seq_lens, max_seq_len: int, scale: float, out,
+                            n_split: int = 0, lse=None, status=None, stream=None):
+    """decode_attention using the library's own static scratch array (no workspace
+    argument, nothing allocated). Calls that overlap on the GPU share that array."""
+    a = _decode_args(q, k_cache, v_cache, seq_lens, max_seq_len, scale, n_split, None, out, lse,
+                     status, stream)
+    args = a[:12] + a[14:]  # drop workspace pointer and size
+    _check(load().kvd_decode_attention_static(*args), "kvd_decode_attention_static")
 
 
 def split_kv_chunk(q, k_cache, v_cache, seq_lens, max_seq_len: int, scale: float, out,
