@@ -40,7 +40,9 @@ from kv_cache_decode_gb300 import roofline  # noqa: E402
 
 METRIC = "decode-attention KV GB/s and % of GB300 HBM peak; decode tokens/s per shape"
 UNIT = "GB/s"
-CHUNK_SOURCES = ["split_kv_chunk.cuh", "split_kv_chunk_variants.cuh", "common.cuh", "schedule.cuh"]
+# Every source of the attention kernels: a profile taken on other sources is stale.
+CHUNK_SOURCES = ["split_kv_chunk.cuh", "split_kv_chunk_variants.cuh", "split_kv_chunk_tc.cuh",
+                 "split_kv_chunk_tc_launch.cuh", "tc_common.cuh", "common.cuh", "schedule.cuh"]
 
 
 def parse_args():
@@ -51,6 +53,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="palm", help="tiny|palm|mha|gqa|long|long_trialN")
     ap.add_argument("--n-split", type=int, default=0, help="0 = heuristic")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="use only the first N sequences (smaller profiling captures); 0 = the workload's")
     ap.add_argument("--out-dtype", default="bf16", choices=["bf16", "f32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
@@ -231,6 +235,8 @@ def run_ours(args):
     kvd.load()
 
     w = workloads.get(args.config)
+    if args.batch:
+        w = w.with_batch(min(args.batch, w.B))
     inp = workloads.step_inputs(w, pad_bits=0)
     B, Hq, D = inp.q.shape
     S, Hkv = inp.k_cache.shape[1], inp.k_cache.shape[2]

@@ -29,7 +29,7 @@ struct ChunkKernel {
     cudaError_t (*launch)(const struct ChunkKernel& k, const DecodeParams& p, cudaStream_t s);
     int head_dim, threads, smem_bytes, tile_tokens, ctas_per_sm;
     bool f32_out, tensor_core;
-    int index;  // position in the variant table (0..17)
+    int index;  // position in the variant table (0..29), for the per-device attribute bitmask
 };
 
 // The kernel for a shape: groups of up to 16 query heads per KV head run on the

@@ -111,8 +111,11 @@ struct ChunkShape {
     static constexpr int TILE_ELEMS = TT * D;
     static constexpr int STAGE_BYTES = 2 * TILE_ELEMS * 2;
     static constexpr int MB_FLOATS_PER_WARP = (ND * 4 + 4) * 32;
+    // The token slices are merged at the end of a segment through the stage of
+    // the segment's last tile, which every warp has finished reading by then.
     static constexpr int MB_BYTES = (TS - 1) * HT * MB_FLOATS_PER_WARP * 4;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + MB_BYTES;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES;
+    static_assert(MB_BYTES <= STAGE_BYTES, "warp-merge data must fit in one stage");
     static_assert(TW % 16 == 0, "each warp needs whole 16-token k-steps");
     static_assert(D % 16 == 0 && D >= 64, "head_dim");
 };
@@ -129,7 +132,6 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
     __shared__ long long s_cum0;
 
     __nv_bfloat16* stages = reinterpret_cast<__nv_bfloat16*>(smem);
-    float* mbuf = reinterpret_cast<float*>(smem + STAGES * Sh::STAGE_BYTES);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ht = warp / TS, ts = warp % TS;
@@ -288,10 +290,12 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
             const uint32_t kbase = smem_u32(stages) + stage * Sh::STAGE_BYTES;
             const uint32_t vbase = kbase + TILE_ELEMS * 2;
 
-            // S = q K^T over this warp's TW tokens.
-            float s[NS][4];
+            // S = q K^T over this warp's TW tokens, as two independent accumulation
+            // chains (even and odd k-steps) to halve the MMA dependency chain.
+            float s[NS][4], s2[NS][4];
 #pragma unroll
-            for (int j = 0; j < NS; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+            for (int j = 0; j < NS; ++j)
+                s[j][0] = s[j][1] = s[j][2] = s[j][3] = s2[j][0] = s2[j][1] = s2[j][2] = s2[j][3] = 0.f;
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
 #pragma unroll
@@ -300,10 +304,19 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                     const int ch = kk * 2 + ((lane >> 3) & 1);
                     uint32_t b0, b1, b2, b3;
                     ldmatrix_x4(kbase + (uint32_t)((row * D + ((ch ^ (row & 7)) * 8)) * 2), b0, b1, b2, b3);
-                    mma_bf16_16816(s[2 * n2], qf[kk], b0, b1);
-                    mma_bf16_16816(s[2 * n2 + 1], qf[kk], b2, b3);
+                    if (kk & 1) {
+                        mma_bf16_16816(s2[2 * n2], qf[kk], b0, b1);
+                        mma_bf16_16816(s2[2 * n2 + 1], qf[kk], b2, b3);
+                    } else {
+                        mma_bf16_16816(s[2 * n2], qf[kk], b0, b1);
+                        mma_bf16_16816(s[2 * n2 + 1], qf[kk], b2, b3);
+                    }
                 }
             }
+#pragma unroll
+            for (int j = 0; j < NS; ++j)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[j][e] += s2[j][e];
 
             // Scale to base-2 units, mask tokens past the tile's end, row maxima.
             float mx0 = -CUDART_INF_F, mx1 = -CUDART_INF_F;
@@ -391,6 +404,8 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
             l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
             if constexpr (TS > 1) {
+                float* mbuf = reinterpret_cast<float*>(smem + stage * Sh::STAGE_BYTES);
+                __syncthreads();  // every warp is done with this stage's K/V rows
                 if (ts > 0) {
                     float* mb = mbuf + ((ts - 1) * HT + ht) * Sh::MB_FLOATS_PER_WARP;
 #pragma unroll

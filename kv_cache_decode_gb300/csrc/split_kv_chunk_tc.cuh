@@ -51,12 +51,16 @@ struct TcShape {
     // extra rows alias the next block (or the K ring after Q): they only feed
     // accumulator rows of padded heads, which are never used.
     static constexpr int QB_BYTES = QR * 128;
-    static constexpr int Q_BYTES = KB * QB_BYTES;
+    // Q slots: narrow groups keep a ring of four (a few KB each), so the
+    // producer loads the next pairs' Q ahead of time; wide groups keep one.
+    static constexpr int NQ = QR <= 16 ? 4 : 1;
+    static constexpr int QS_BYTES = KB * QB_BYTES;  // one slot
+    static constexpr int Q_BYTES = NQ * QS_BYTES;
     static constexpr int P_BYTES = 64 * T * 2;   // one P buffer (64 rows x 64 tokens)
     static constexpr int NP = F32OUT ? 2 : 1;    // hi (and lo) parts of P
     // Stage counts: three V stages (a V stage is held until P V of its tile is
     // done, so the V ring needs the depth), K stages as the budget allows.
-    static constexpr int VST = D == 256 ? 3 : (D == 128 ? 5 : 8);
+    static constexpr int VST = D == 256 ? 3 : (D == 128 ? 6 : 8);
     static constexpr int BUDGET = 224 * 1024 - Q_BYTES - NP * P_BYTES - VST * TILE_BYTES;
     static constexpr int KST_FIT = BUDGET / TILE_BYTES;
     static constexpr int KST = KST_FIT > 8 ? 8 : KST_FIT;
@@ -65,9 +69,9 @@ struct TcShape {
     static constexpr int OFF_V = OFF_K + KST * TILE_BYTES;
     static constexpr int OFF_P = OFF_V + VST * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_P + NP * P_BYTES;
-    // barriers: k_full, k_empty [KST]; v_full, v_empty [VST]; q_full, q_empty;
+    // barriers: k_full, k_empty [KST]; v_full, v_empty [VST]; q_full, q_empty [NQ];
     // s_full, s_free, p_full, o_fin [2]; mma_done; xbar [4]
-    static constexpr int NBAR = 2 * KST + 2 * VST + 2 + 8 + 1 + 4;
+    static constexpr int NBAR = 2 * KST + 2 * VST + 2 * NQ + 8 + 1 + 4;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int STATIC_SMEM = 2048;  // block scans and the exchange buffer (checked by ptxas -v)
@@ -108,17 +112,19 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     auto k_empty = [&](int s) { return sBar + 8u * (KST + s); };
     auto v_full = [&](int s) { return sBar + 8u * (2 * KST + s); };
     auto v_empty = [&](int s) { return sBar + 8u * (2 * KST + VST + s); };
-    const uint32_t q_full = sBar + 8u * (2 * KST + 2 * VST);
-    const uint32_t q_empty = q_full + 8;
-    auto s_full = [&](int b) { return q_empty + 8u * (1 + b); };
-    auto s_free = [&](int b) { return q_empty + 8u * (3 + b); };
-    auto p_full = [&](int b) { return q_empty + 8u * (5 + b); };
+    constexpr int NQ = Sh::NQ;
+    auto q_full = [&](int s) { return sBar + 8u * (2 * KST + 2 * VST + s); };
+    auto q_empty = [&](int s) { return sBar + 8u * (2 * KST + 2 * VST + NQ + s); };
+    const uint32_t sBar2 = sBar + 8u * (2 * KST + 2 * VST + 2 * NQ - 1);  // base of the rest
+    auto s_full = [&](int b) { return sBar2 + 8u * (1 + b); };
+    auto s_free = [&](int b) { return sBar2 + 8u * (3 + b); };
+    auto p_full = [&](int b) { return sBar2 + 8u * (5 + b); };
     // o_fin[i & 1] completes when O += P(i) V(i) has finished. One barrier per
     // P buffer (rather than one for all tiles) keeps every waiter within one
     // phase of the completion it waits for, so parity waits are unambiguous.
-    auto o_fin = [&](int b) { return q_empty + 8u * (7 + b); };
-    const uint32_t mma_done = q_empty + 8u * 9;
-    auto xbar = [&](int q) { return q_empty + 8u * (10 + q); };
+    auto o_fin = [&](int b) { return sBar2 + 8u * (7 + b); };
+    const uint32_t mma_done = sBar2 + 8u * 9;
+    auto xbar = [&](int q) { return sBar2 + 8u * (10 + q); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Sh::OFF_MISC + 8);
     // The P buffer, part 0 = hi, 1 = lo. One buffer: P(i) is written only once
@@ -144,8 +150,10 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             tc::mbar_init(v_full(s), 1);
             tc::mbar_init(v_empty(s), 1);
         }
-        tc::mbar_init(q_full, 1);
-        tc::mbar_init(q_empty, 1);
+        for (int s = 0; s < NQ; ++s) {
+            tc::mbar_init(q_full(s), 1);
+            tc::mbar_init(q_empty(s), 1);
+        }
         for (int b = 0; b < 2; ++b) {
             tc::mbar_init(s_full(b), 1);
             tc::mbar_init(s_free(b), 8);
@@ -223,12 +231,14 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             const CUtensorMap* map = is_k ? &maps.k : &maps.v;
             while (walker.next(t, NoOp{})) {
                 if (is_k && t.seg_start) {
-                    if (!tc::mbar_wait(q_empty, (qn & 1) ^ 1, abort_flag, kBudget)) break;
-                    tc::mbar_arrive_expect_tx(q_full, (uint32_t)(KB * 128 * G));
+                    const int qs = qn % NQ;
+                    if (!tc::mbar_wait(q_empty(qs), ((qn / NQ) & 1) ^ 1, abort_flag, kBudget)) break;
+                    tc::mbar_arrive_expect_tx(q_full(qs), (uint32_t)(KB * 128 * G));
                     const int qrow = t.b * p.Hq + t.h * G;
 #pragma unroll
                     for (int kb = 0; kb < KB; ++kb)
-                        tc::tma_load_2d(sQ + kb * Sh::QB_BYTES, &maps.q, kb * 64, qrow, q_full, pol_q);
+                        tc::tma_load_2d(sQ + qs * Sh::QS_BYTES + kb * Sh::QB_BYTES, &maps.q, kb * 64, qrow,
+                                        q_full(qs), pol_q);
                     ++qn;
                 }
                 const int s = j % NS;
@@ -248,7 +258,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                 const int s = jj % NS;
                 tc::mbar_wait(is_k ? k_full(s) : v_full(s), (jj / NS) & 1, abort_flag, kBudget / 4);
             }
-            if (is_k && qn > 0) tc::mbar_wait(q_full, (qn - 1) & 1, abort_flag, kBudget / 4);
+            if (is_k && qn > 0) tc::mbar_wait(q_full((qn - 1) % NQ), ((qn - 1) / NQ) & 1, abort_flag, kBudget / 4);
         }
     } else if (warp == 1) {
         // ===================== MMA issuer =====================
@@ -256,21 +266,22 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             constexpr uint32_t idesc_s = tc::idesc_bf16_f32(64, T, false, false);
             constexpr uint32_t idesc_o = tc::idesc_bf16_f32(64, D, false, true);
             int qn = 0;
-            auto mma_s = [&](const Tile& t, int i) {
+            auto mma_s = [&](bool seg_end, int i, int qs) {
                 const int sk = i % KST, sb = i & 1;
+                const uint32_t qt = sQ + (uint32_t)(qs * Sh::QS_BYTES);
                 tc::fence_after_sync();
                 const uint32_t kt = sK + (uint32_t)(sk * Sh::TILE_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint64_t a = tc::sdesc_sw128(sQ + (kk >> 2) * Sh::QB_BYTES + (kk & 3) * 32, 16, 1024);
+                    const uint64_t a = tc::sdesc_sw128(qt + (kk >> 2) * Sh::QB_BYTES + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = tc::sdesc_sw128(kt + (kk >> 2) * Sh::KB_BYTES + (kk & 3) * 32, 16, 1024);
                     tc::mma_bf16(tmem + Sh::TMEM_S + sb * T, a, b, idesc_s, kk > 0);
                 }
                 tc::mma_commit(s_full(sb));
                 tc::mma_commit(k_empty(sk));
-                if (t.seg_end) tc::mma_commit(q_empty);
+                if (seg_end) tc::mma_commit(q_empty(qs));
             };
-            auto mma_o = [&](const Tile& t, int i) {
+            auto mma_o = [&](bool seg_start, int i) {
                 const int sv = i % VST, sb = i & 1;
                 tc::fence_after_sync();
                 const uint32_t vt = sV + (uint32_t)(sv * Sh::TILE_BYTES);
@@ -281,7 +292,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                     for (int part = 0; part < Sh::NP; ++part) {
                         const uint64_t a = tc::sdesc_sw128(p_buf(sb, part) + k2 * 32, 16, 1024);
                         tc::mma_bf16(tmem + Sh::TMEM_O, a, b, idesc_o,
-                                     (t.seg_start && k2 == 0 && part == 0) ? 0u : 1u);
+                                     (seg_start && k2 == 0 && part == 0) ? 0u : 1u);
                     }
                 }
                 tc::mma_commit(v_empty(sv));
@@ -289,35 +300,41 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             };
             // Issue whichever of S(i) = Q K^T and O += P(j) V(j) is ready first, so that
             // S of upcoming tiles is never queued behind a wait for P or V.
-            Tile tq[4];
+            // Tiles between o_idx and the walker's position: only their segment
+            // start/end flags are needed, kept as 2 bits per tile in a register.
+            uint32_t flags = 0;
+            auto flag = [&](int idx) { return (flags >> (2 * (idx & 15))) & 3u; };
             int n_fetched = 0, s_idx = 0, o_idx = 0;
             bool walker_done = false;
             long long idle_since = clock64();
             while (true) {
                 while (!walker_done && n_fetched < o_idx + 4) {
-                    if (walker.next(tq[n_fetched & 3], NoOp{}))
+                    Tile t;
+                    if (walker.next(t, NoOp{})) {
+                        const int sh2 = 2 * (n_fetched & 15);
+                        flags = (flags & ~(3u << sh2)) | ((t.seg_start ? 1u : 0u) << sh2) | ((t.seg_end ? 2u : 0u) << sh2);
                         ++n_fetched;
-                    else
+                    } else {
                         walker_done = true;
+                    }
                 }
                 if (walker_done && o_idx == n_fetched) break;
                 bool progress = false;
                 if (s_idx < n_fetched && s_idx < o_idx + 3) {
-                    const Tile& t = tq[s_idx & 3];
+                    const uint32_t f = flag(s_idx);
                     if (tc::mbar_test(k_full(s_idx % KST), (s_idx / KST) & 1) &&
                         tc::mbar_test(s_free(s_idx & 1), ((s_idx >> 1) & 1) ^ 1) &&
-                        (!t.seg_start || tc::mbar_test(q_full, qn & 1))) {
-                        if (t.seg_start) ++qn;
-                        mma_s(t, s_idx);
+                        (!(f & 1u) || tc::mbar_test(q_full(qn % NQ), (qn / NQ) & 1))) {
+                        if (f & 1u) ++qn;
+                        mma_s((f & 2u) != 0, s_idx, (qn - 1) % NQ);
                         ++s_idx;
                         progress = true;
                     }
                 }
                 if (o_idx < s_idx) {
-                    const Tile& t = tq[o_idx & 3];
                     if (tc::mbar_test(v_full(o_idx % VST), (o_idx / VST) & 1) &&
                         tc::mbar_test(p_full(o_idx & 1), (o_idx >> 1) & 1)) {
-                        mma_o(t, o_idx);
+                        mma_o((flag(o_idx) & 1u) != 0, o_idx);
                         ++o_idx;
                         progress = true;
                     }

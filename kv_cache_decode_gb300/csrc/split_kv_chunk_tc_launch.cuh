@@ -1,0 +1,65 @@
+// tcgen05 split-KV chunk kernel: TMA tensor maps and launch (included by the
+// per-head-dim instantiation files).
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include <cstring>
+
+#include "split_kv_chunk_tc.cuh"
+
+namespace kvd {
+
+// bf16 tensor map with 128-byte swizzle; dims/strides innermost first (strides in bytes).
+bool tc_encode_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                   const cuuint64_t* strides, const cuuint32_t* box);
+
+template <int D, bool F32, int QR>
+cudaError_t launch_tc_chunk(const ChunkKernel& k, const DecodeParams& p, cudaStream_t stream) {
+    TcMaps maps;
+    std::memset(&maps, 0, sizeof maps);
+    {
+        const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)p.B * p.Hq};
+        const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
+        const cuuint32_t box[2] = {64, (cuuint32_t)p.G};
+        if (!tc_encode_map(&maps.q, p.q, 2, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hkv, (cuuint64_t)p.B * p.S_max};
+        const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.Hkv * D * 2};
+        const cuuint32_t box[3] = {64, 1, (cuuint32_t)TcShape<D, F32, QR>::T};
+        if (!tc_encode_map(&maps.k, p.k, 3, dims, strides, box)) return cudaErrorInvalidValue;
+        if (!tc_encode_map(&maps.v, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)p.n_split, 1, 1);
+    cfg.blockDim = dim3((unsigned)k.threads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)k.smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, split_kv_chunk_tc_kernel<D, F32, QR>, p, maps);
+}
+
+template <int D, bool F32, int QR>
+static ChunkKernel make_tc(int index) {
+    using Sh = TcShape<D, F32, QR>;
+    ChunkKernel k;
+    k.fn = reinterpret_cast<const void*>(split_kv_chunk_tc_kernel<D, F32, QR>);
+    k.launch = launch_tc_chunk<D, F32, QR>;
+    k.head_dim = D;
+    k.threads = Sh::THREADS;
+    k.smem_bytes = Sh::SMEM_BYTES;
+    k.tile_tokens = Sh::T;
+    k.ctas_per_sm = 1;
+    k.f32_out = F32;
+    k.tensor_core = true;
+    k.index = index;
+    return k;
+}
+
+
+}  // namespace kvd

@@ -13,7 +13,9 @@ template <int D, int HT>
 struct ChunkConfig {
     static constexpr int TS = (HT == 1) ? 4 : 2;
     static constexpr int TT = (HT == 1) ? 64 : 32;
-    static constexpr int STAGES = (HT == 1 && D == 256) ? 2 : 4;
+    // Three stages at head_dim 128 (two CTAs, eight warps per SM), three at 256
+    // (one CTA), four at 64.
+    static constexpr int STAGES = (D == 64) ? 4 : 3;
     // Two CTAs per SM when two fit in the SM's 228 KB of shared memory (1 KB
     // of it is reserved per CTA); __launch_bounds__ then caps registers to match.
     static constexpr int SMEM = ChunkShape<D, HT, TS, TT, STAGES>::SMEM_BYTES;
