@@ -197,12 +197,17 @@ kvd_status kvd_schedule_describe(const int32_t* seq_lens_host, int batch, int s_
 
 /*
  * kvd_kernel_info: launch shape of the attention kernel chosen for a shape:
- * threads per CTA, dynamic shared memory bytes, tokens per pipeline tile and
- * the CTAs per SM the heuristic assumes. Host only. Errors as kvd_decode_plan.
+ * threads per CTA, dynamic shared memory bytes, tokens per pipeline tile, the
+ * CTAs per SM the heuristic assumes, and the unit and start-up charge of its
+ * work schedule. The schedule lays the (sequence, KV head) pairs on a line of
+ * positions of seg_unit tokens each (1, or tile_tokens when the kernel's time
+ * is set by its tile count): a non-empty pair occupies
+ * seg_cost + ceil(len / seg_unit) positions, and the CTAs get balanced runs of
+ * positions. Any out pointer may be NULL. Host only. Errors as kvd_decode_plan.
  */
 kvd_status kvd_kernel_info(int n_heads_q, int n_heads_kv, int head_dim, kvd_out_dtype out_dtype,
                            int* threads_out, int* smem_bytes_out, int* tile_tokens_out,
-                           int* ctas_per_sm_out);
+                           int* ctas_per_sm_out, int* seg_unit_out, int* seg_cost_out);
 
 /*
  * kvd_decode_attention_static: kvd_decode_attention for callers that cannot

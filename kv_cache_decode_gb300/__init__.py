@@ -71,7 +71,7 @@ def _declare(lib):
     lib.kvd_decode_attention_static.argtypes = [P, P, P, P, I, I, I, I, I, I, F, I, P, I, P, P, P]
     lib.kvd_decode_attention_static.restype = I
     lib.kvd_schedule_describe.argtypes = [P, I, I, I, I, I, I, I, I, P, I, PI, PI]
-    lib.kvd_kernel_info.argtypes = [I, I, I, I, PI, PI, PI, PI]
+    lib.kvd_kernel_info.argtypes = [I, I, I, I, PI, PI, PI, PI, PI, PI]
     lib.kvd_status_string.argtypes = [I]
     lib.kvd_status_string.restype = ctypes.c_char_p
     lib.kvd_version.argtypes = []
@@ -140,12 +140,13 @@ def decode_plan(batch: int, n_heads_q: int, n_heads_kv: int, head_dim: int, max_
 
 def kernel_info(n_heads_q: int, n_heads_kv: int, head_dim: int, out_dtype="bf16") -> dict:
     lib = load()
-    th, sm, tt, cps = (ctypes.c_int(0) for _ in range(4))
+    th, sm, tt, cps, su, sc = (ctypes.c_int(0) for _ in range(6))
     _check(lib.kvd_kernel_info(n_heads_q, n_heads_kv, head_dim, _out_code(out_dtype),
                                ctypes.byref(th), ctypes.byref(sm), ctypes.byref(tt),
-                               ctypes.byref(cps)), "kvd_kernel_info")
+                               ctypes.byref(cps), ctypes.byref(su), ctypes.byref(sc)),
+           "kvd_kernel_info")
     return {"threads": th.value, "smem_bytes": sm.value, "tile_tokens": tt.value,
-            "ctas_per_sm": cps.value}
+            "ctas_per_sm": cps.value, "seg_unit": su.value, "seg_cost": sc.value}
 
 
 def schedule_describe(seq_lens, s_max: int, max_seq_len: int, n_heads_q: int, n_heads_kv: int,

@@ -266,8 +266,9 @@ kvd_status kvd_schedule_describe(const int32_t* seq_lens_host, int batch, int s_
         int operator()(int b) const { return clamp_len(lens[b], cap); }
     };
     const HostLen len{seq_lens_host, std::min(s_max, max_seq_len)};
+    const RuntimeGeom geo{k->tile_tokens, k->seg_unit, k->seg_cost};
     long long total = 0;
-    for (int b = 0; b < batch; ++b) total += len(b);
+    for (int b = 0; b < batch; ++b) total += pair_extent(len(b), geo);
     total *= n_heads_kv;
     const int C_eff = effective_ctas(n_split, total);
     int rows = 0;
@@ -279,17 +280,17 @@ kvd_status kvd_schedule_describe(const int32_t* seq_lens_host, int batch, int s_
         ++rows;
     };
     for (int c = 0; c < C_eff; ++c) {
-        Walker<HostLen> w(len, batch, n_heads_kv, k->tile_tokens, c, C_eff, total);
+        Walker<HostLen, RuntimeGeom> w(len, geo, batch, n_heads_kv, c, C_eff, total);
         int b0 = batch;
         long long cum = 0, cum0 = total;
         for (int b = 0; b < batch; ++b) {
-            const int L = len(b);
-            if (is_first_seq_candidate(cum, L, n_heads_kv, w.S)) {
+            const long long e = pair_extent(len(b), geo);
+            if (is_first_seq_candidate(cum, e, n_heads_kv, w.S)) {
                 b0 = b;
                 cum0 = cum;
                 break;
             }
-            cum += (long long)n_heads_kv * L;
+            cum += (long long)n_heads_kv * e;
         }
         w.start(b0, cum0);
         auto on_empty = [&](int b, int h) { emit(c, b, h, 0, 0, 3, -1, c); };
@@ -314,7 +315,7 @@ kvd_status kvd_schedule_describe(const int32_t* seq_lens_host, int batch, int s_
 
 kvd_status kvd_kernel_info(int n_heads_q, int n_heads_kv, int head_dim, kvd_out_dtype out_dtype,
                            int* threads_out, int* smem_bytes_out, int* tile_tokens_out,
-                           int* ctas_per_sm_out) {
+                           int* ctas_per_sm_out, int* seg_unit_out, int* seg_cost_out) {
     kvd_status st = check_shape(1, n_heads_q, n_heads_kv, head_dim, out_dtype);
     if (st != KVD_OK) return st;
     const ChunkKernel* k = pick_kernel(n_heads_q, n_heads_kv, head_dim, out_dtype);
@@ -323,6 +324,8 @@ kvd_status kvd_kernel_info(int n_heads_q, int n_heads_kv, int head_dim, kvd_out_
     if (smem_bytes_out) *smem_bytes_out = k->smem_bytes;
     if (tile_tokens_out) *tile_tokens_out = k->tile_tokens;
     if (ctas_per_sm_out) *ctas_per_sm_out = k->ctas_per_sm;
+    if (seg_unit_out) *seg_unit_out = k->seg_unit;
+    if (seg_cost_out) *seg_cost_out = k->seg_cost;
     return KVD_OK;
 }
 

@@ -28,6 +28,8 @@ struct ChunkKernel {
     const void* fn;  // the __global__ function (for attributes)
     cudaError_t (*launch)(const struct ChunkKernel& k, const DecodeParams& p, cudaStream_t s);
     int head_dim, threads, smem_bytes, tile_tokens, ctas_per_sm;
+    int seg_unit;    // tokens per schedule position (1 or tile_tokens, see schedule.cuh)
+    int seg_cost;    // positions charged per pair by the schedule
     bool f32_out, tensor_core;
     int index;  // position in the variant table (0..29), for the per-device attribute bitmask
 };

@@ -1,17 +1,25 @@
 // Work schedule of the split-KV decode: shared by the device kernels and by the
 // host-side replica used for planning and tests, so both walk the same path.
 //
-// The (sequence b, KV head h) pairs are laid end to end in b-major order, pair
-// p = b * Hkv + h holding L_b tokens; total = Hkv * sum_b L_b. CTA c of the
-// C_eff working CTAs gets the contiguous token run [c*total/C_eff,
-// (c+1)*total/C_eff). Within a run the CTA walks pairs and cuts each pair's
-// part (a "segment") into pipeline tiles of at most TT tokens.
+// The (sequence b, KV head h) pairs are laid end to end in b-major order on a
+// line of positions, each position standing for U consecutive tokens of a pair
+// (U = 1, or U = TT, the kernel's pipeline tile). A pair of L_b > 0 tokens
+// occupies X + ceil(L_b / U) positions: a prefix of X positions that stands
+// for the fixed cost of starting a pair inside a CTA's run (loading its
+// queries, filling the pipeline), then its tokens. Empty pairs occupy nothing.
+// CTA c of the C_eff working CTAs gets the contiguous run
+// [c*total/C_eff, (c+1)*total/C_eff) of positions, so runs are balanced to one
+// position of estimated time. Within a run a CTA walks pairs and cuts each
+// pair's tokens inside the run (a "segment") into tiles of at most TT tokens.
+// A kernel whose time per tile is fixed (latency-bound) takes U = TT, so that
+// its runs are balanced in tiles; a bandwidth-bound one takes U = 1.
 //
-// Every pair has one owner: the CTA whose run contains the pair's first token
-// (or the last CTA for empty pairs at the very end). If the owner covers the
-// pair entirely it writes the final output; otherwise each contributing CTA c
-// writes a partial (m, l, o) into slot c + p, and the owner records the range
-// of contributing CTAs for the merge kernel. Slots are unique because walking
+// Every pair has one owner: for a non-empty pair, the CTA whose run contains
+// its first token; for an empty pair, the CTA whose run contains its position
+// (the last CTA for empty pairs at the very end). If the owner covers the pair
+// entirely it writes the final output; otherwise each contributing CTA c writes
+// a partial (m, l, o) into slot c + p, and the owner records the range of
+// contributing CTAs for the merge kernel. Slots are unique because walking
 // segments in order, each step increments c, p or both.
 #pragma once
 
@@ -31,8 +39,33 @@ namespace kvd {
 
 KVD_HD int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
 
-// Number of CTAs that receive work: at most one per token, at least one (the
-// last CTA also owns trailing empty pairs, so one is needed even for no work).
+// Geometry of the walk: tokens per tile TT, tokens per position U (1 or TT)
+// and start-up cost X (positions). Compile-time constants in kernels, so that
+// the divisions become shifts and a zero cost compiles away; run-time values
+// in the host replica.
+template <int TT_, int U_, int X_>
+struct FixedGeom {
+    static_assert(U_ == 1 || U_ == TT_, "a position is one token or one tile");
+    KVD_HD constexpr int tt() const { return TT_; }
+    KVD_HD constexpr int unit() const { return U_; }
+    KVD_HD constexpr int x() const { return X_; }
+};
+struct RuntimeGeom {
+    int tt_, unit_, x_;
+    KVD_HD int tt() const { return tt_; }
+    KVD_HD int unit() const { return unit_; }
+    KVD_HD int x() const { return x_; }
+};
+
+// Positions occupied by a pair of L >= 0 tokens.
+template <class Geom>
+KVD_HD long long pair_extent(int L, Geom g) {
+    const int n = (L + g.unit() - 1) / g.unit();
+    return (long long)n + (n > 0 ? g.x() : 0);
+}
+
+// Number of CTAs that receive work: at most one per position, at least one
+// (the last CTA also owns trailing empty pairs, so one is needed even for no work).
 KVD_HD int effective_ctas(int n_split, long long total) {
     if (total <= 0) return 1;
     return (long long)n_split < total ? n_split : (int)total;
@@ -42,7 +75,7 @@ KVD_HD long long run_begin(int c, int C_eff, long long total) {
     return (long long)c * total / C_eff;
 }
 
-// The CTA whose run [run_begin(c), run_begin(c + 1)) contains token t < total.
+// The CTA whose run [run_begin(c), run_begin(c + 1)) contains position t < total.
 KVD_HD int cta_of_token(long long t, int C_eff, long long total) {
     return (int)(((t + 1) * (long long)C_eff - 1) / total);
 }
@@ -57,27 +90,31 @@ struct Tile {
     int c_last;        // last contributing CTA (owned && !full)
 };
 
-// Walks one CTA's token run. LenFn: int(int b) returning the clamped length.
-template <class LenFn>
+// Walks one CTA's run. LenFn: int(int b) returning the clamped length;
+// Geom: FixedGeom<TT, U, X> or RuntimeGeom.
+template <class LenFn, class Geom>
 struct Walker {
     LenFn len;
-    int B, Hkv, TT;
+    Geom g;
+    int B, Hkv;
     int c, C_eff;
-    long long total, S, E;  // this CTA's run [S, E)
+    long long total, S, E;  // this CTA's run [S, E) of positions
     // state
     int b, h, L;
-    long long pstart, pos;
+    long long pstart, pos;  // position of the current pair, position reached
 
     KVD_HD_TEMPLATE
-    KVD_HD Walker(LenFn f, int B_, int Hkv_, int TT_, int c_, int C_eff_, long long total_)
-        : len(f), B(B_), Hkv(Hkv_), TT(TT_), c(c_), C_eff(C_eff_), total(total_) {
+    KVD_HD Walker(LenFn f, Geom g_, int B_, int Hkv_, int c_, int C_eff_, long long total_)
+        : len(f), g(g_), B(B_), Hkv(Hkv_), c(c_), C_eff(C_eff_), total(total_) {
         S = run_begin(c, C_eff, total);
         E = run_begin(c + 1, C_eff, total);
         b = B; h = 0; L = 0; pstart = total; pos = S;
     }
 
+    KVD_HD long long ext() const { return pair_extent(L, g); }
+
     // b0 = first sequence whose pairs end after S or start at or after S;
-    // cum0 = token offset of pair (b0, 0).
+    // cum0 = position of pair (b0, 0).
     KVD_HD_TEMPLATE
     KVD_HD void start(int b0, long long cum0) {
         b = b0;
@@ -85,15 +122,15 @@ struct Walker {
         pstart = cum0;
         L = (b < B) ? len(b) : 0;
         if (b < B && L > 0 && pstart < S) {
-            h = (int)((S - pstart) / L);
-            pstart += (long long)h * L;
+            h = (int)((S - pstart) / ext());
+            pstart += (long long)h * ext();
         }
         pos = S;
     }
 
     KVD_HD_TEMPLATE
     KVD_HD void advance_pair() {
-        pstart += L;
+        pstart += ext();
         if (++h == Hkv) {
             h = 0;
             ++b;
@@ -102,52 +139,59 @@ struct Walker {
     }
 
     // Next tile of the run; calls on_empty(b, h) for each empty pair passed
-    // on the way (those pairs start inside this run, so this CTA owns them).
+    // on the way (those pairs lie inside this run, so this CTA owns them).
     KVD_HD_TEMPLATE
     template <class F>
     KVD_HD bool next(Tile& t, F&& on_empty) {
         if (pos >= E) return false;
-        while (pos >= pstart + L) {
+        while (pos >= pstart + ext()) {
             if (L == 0) on_empty(b, h);
             advance_pair();
         }
-        const long long pend = pstart + L;
-        const long long seg_lo = pstart > S ? pstart : S;
+        const long long real0 = pstart + g.x();  // position of the pair's first token
+        if (g.x() > 0 && pos < real0) {
+            pos = real0;                         // skip the pair's start-up prefix
+            if (pos >= E) return false;
+        }
+        const long long pend = pstart + ext();
+        const long long seg_lo = real0 > S ? real0 : S;
         const long long seg_hi = pend < E ? pend : E;
-        long long te = pos + TT;
+        long long te = pos + g.tt() / g.unit();
         if (te > seg_hi) te = seg_hi;
         t.b = b;
         t.h = h;
         t.L = L;
-        t.tok_lo = (int)(pos - pstart);
-        t.tok_hi = (int)(te - pstart);
+        t.tok_lo = (int)(pos - real0) * g.unit();
+        t.tok_hi = (int)(te - real0) * g.unit();
+        if (t.tok_hi > L) t.tok_hi = L;
         t.seg_start = (pos == seg_lo);
         t.seg_end = (te == seg_hi);
-        t.owned = (pstart >= S);
+        t.owned = (real0 >= S);
         t.full = t.owned && (pend <= E);
         t.c_last = (t.owned && !t.full) ? cta_of_token(pend - 1, C_eff, total) : c;
         pos = te;
         return true;
     }
 
-    // After the last tile: the last CTA also owns the empty pairs that start at
-    // the very end of the token order.
+    // After the last tile: the last CTA also owns the empty pairs that sit at
+    // the very end of the line.
     KVD_HD_TEMPLATE
     template <class F>
     KVD_HD void finish(F&& on_empty) {
         if (c != C_eff - 1) return;
+        if (pos < E) pos = E;  // the run may end inside a prefix
         while (b < B) {
-            if (pos < pstart + L) break;  // cannot happen once pos == total
+            if (pos < pstart + ext()) break;  // cannot happen once pos == total
             if (L == 0) on_empty(b, h);
             advance_pair();
         }
     }
 };
 
-// Condition selecting b0 in Walker::start, given sequence b's cumulative start
-// (in tokens, counting all its Hkv pairs) and its clamped length.
-KVD_HD bool is_first_seq_candidate(long long cum_start_b, int L_b, int Hkv, long long S) {
-    return (cum_start_b + (long long)Hkv * L_b > S) || (cum_start_b >= S);
+// Condition selecting b0 in Walker::start, given sequence b's cumulative
+// position (counting all its Hkv pairs) and the extent of one of its pairs.
+KVD_HD bool is_first_seq_candidate(long long cum_start_b, long long ext_b, int Hkv, long long S) {
+    return (cum_start_b + (long long)Hkv * ext_b > S) || (cum_start_b >= S);
 }
 
 }  // namespace kvd

@@ -115,6 +115,11 @@ struct ChunkShape {
     // the segment's last tile, which every warp has finished reading by then.
     static constexpr int MB_BYTES = (TS - 1) * HT * MB_FLOATS_PER_WARP * 4;
     static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES;
+    // Schedule: runs balanced in tokens (the kernel is bandwidth-bound, so a
+    // short tile costs less than a full one), no charge per pair (a new pair's
+    // queries come from L2 while the previous tiles are still in flight).
+    static constexpr int SEG_UNIT = 1;
+    static constexpr int SEG_COST = 0;
     static_assert(MB_BYTES <= STAGE_BYTES, "warp-merge data must fit in one stage");
     static_assert(TW % 16 == 0, "each warp needs whole 16-token k-steps");
     static_assert(D % 16 == 0 && D >= 64, "head_dim");
@@ -124,7 +129,7 @@ template <int D, int HT, int TS, int TT, int STAGES, bool F32OUT, int MINB>
 __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const DecodeParams p) {
     using Sh = ChunkShape<D, HT, TS, TT, STAGES>;
     constexpr int NW = Sh::NW, NT = Sh::NT, TW = Sh::TW, NS = Sh::NS, KS = Sh::KS,
-                  ND = Sh::ND, CH = Sh::CH, TILE_ELEMS = Sh::TILE_ELEMS;
+                  ND = Sh::ND, CH = Sh::CH, TILE_ELEMS = Sh::TILE_ELEMS, SEG_COST = Sh::SEG_COST;
 
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ long long s_red[NW];
@@ -143,6 +148,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
     pdl_launch_dependents();
 
     const DevLen len{p.seq_lens, p.len_cap};
+    using Geo = FixedGeom<TT, Sh::SEG_UNIT, SEG_COST>;
 
     // ---- total work and this CTA's token run ----
     long long mine = 0;
@@ -151,7 +157,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
         const int raw = __ldg(p.seq_lens + b);
         const int L = clamp_len(raw, p.len_cap);
         clamped |= (raw != L);
-        mine += L;
+        mine += pair_extent(L, Geo{});
     }
     if (clamped && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
     const long long total = block_sum_ll<NW>(mine, s_red) * p.Hkv;
@@ -167,10 +173,11 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
         for (int chunk = 0; chunk < p.B; chunk += NT) {
             const int b = chunk + tid;
             const int L = (b < p.B) ? len(b) : 0;
-            const long long v = (long long)L * p.Hkv;
+            const long long e = pair_extent(L, Geo{});
+            const long long v = e * p.Hkv;
             long long ctot;
             const long long cs = base + block_incl_scan_ll<NW>(v, s_red, &ctot) - v;
-            const bool cand = (b < p.B) && is_first_seq_candidate(cs, L, p.Hkv, S);
+            const bool cand = (b < p.B) && is_first_seq_candidate(cs, e, p.Hkv, S);
             const int bmin = block_min_int<NW>(cand ? b : 0x7fffffff, s_redi);
             if (bmin != 0x7fffffff) {
                 if (b == bmin) s_cum0 = cs;
@@ -183,9 +190,9 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
         }
     }
 
-    Walker<DevLen> lw(len, p.B, p.Hkv, TT, c, C_eff, total);
+    Walker<DevLen, Geo> lw(len, Geo{}, p.B, p.Hkv, c, C_eff, total);
     lw.start(b0, cum0);
-    Walker<DevLen> cw = lw;
+    Walker<DevLen, Geo> cw = lw;
 
     const uint64_t policy = l2_evict_first_policy();
     const __nv_bfloat16* Kg = reinterpret_cast<const __nv_bfloat16*>(p.k);

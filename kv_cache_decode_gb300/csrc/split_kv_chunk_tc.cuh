@@ -43,6 +43,11 @@ namespace kvd {
 template <int D, bool F32OUT, int QR>
 struct TcShape {
     static constexpr int T = 64;                 // tokens per tile
+    // Schedule: runs balanced in whole tiles (a tile's time is set by the
+    // pipeline's latency, whatever its length), plus one tile's charge for
+    // starting a pair inside a run (its Q load and first K tile).
+    static constexpr int SEG_UNIT = T;
+    static constexpr int SEG_COST = 1;
     static constexpr int KB = D / 64;            // 128-byte swizzle atoms across head_dim
     static constexpr int TILE_BYTES = T * D * 2; // one K (or V) tile
     static constexpr int KB_BYTES = T * 128;     // one 64-column block of a tile
@@ -95,7 +100,8 @@ template <int D, bool F32OUT, int QR>
 __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     split_kv_chunk_tc_kernel(const DecodeParams p, const __grid_constant__ TcMaps maps) {
     using Sh = TcShape<D, F32OUT, QR>;
-    constexpr int T = Sh::T, KB = Sh::KB, KST = Sh::KST, VST = Sh::VST, NW = Sh::NWARPS;
+    constexpr int T = Sh::T, KB = Sh::KB, KST = Sh::KST, VST = Sh::VST, NW = Sh::NWARPS,
+                  SEG_COST = Sh::SEG_COST;
     constexpr long long kBudget = 4000000000LL;  // ~2 s of clock cycles per wait
 
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -178,6 +184,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     pdl_launch_dependents();
 
     const DevLen len{p.seq_lens, p.len_cap};
+    using Geo = FixedGeom<T, Sh::SEG_UNIT, SEG_COST>;
     // ---- total work, this CTA's run, first sequence (as in the mma.sync kernel) ----
     long long mine = 0;
     bool clamped = false;
@@ -185,7 +192,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
         const int raw = __ldg(p.seq_lens + b);
         const int L = clamp_len(raw, p.len_cap);
         clamped |= (raw != L);
-        mine += L;
+        mine += pair_extent(L, Geo{});
     }
     if (clamped && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
     const long long total = block_sum_ll<NW>(mine, s_red) * p.Hkv;  // also orders the set-up
@@ -197,10 +204,11 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     for (long long base = 0, chunk = 0; has_work && chunk < p.B; chunk += Sh::THREADS) {
         const int b = (int)chunk + tid;
         const int L = (b < p.B) ? len(b) : 0;
-        const long long v = (long long)L * p.Hkv;
+        const long long e = pair_extent(L, Geo{});
+        const long long v = e * p.Hkv;
         long long ctot;
         const long long cs = base + block_incl_scan_ll<NW>(v, s_red, &ctot) - v;
-        const bool cand = (b < p.B) && is_first_seq_candidate(cs, L, p.Hkv, S);
+        const bool cand = (b < p.B) && is_first_seq_candidate(cs, e, p.Hkv, S);
         const int bmin = block_min_int<NW>(cand ? b : 0x7fffffff, s_redi);
         if (bmin != 0x7fffffff) {
             if (b == bmin) s_cum0 = cs;
@@ -214,7 +222,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    Walker<DevLen> walker(len, p.B, p.Hkv, T, c, has_work ? C_eff : c + 1, has_work ? total : 0);
+    Walker<DevLen, Geo> walker(len, Geo{}, p.B, p.Hkv, c, has_work ? C_eff : c + 1, has_work ? total : 0);
     walker.start(b0, cum0);
 
     if (!has_work) {

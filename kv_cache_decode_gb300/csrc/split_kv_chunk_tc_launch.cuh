@@ -55,6 +55,8 @@ static ChunkKernel make_tc(int index) {
     k.smem_bytes = Sh::SMEM_BYTES;
     k.tile_tokens = Sh::T;
     k.ctas_per_sm = 1;
+    k.seg_unit = Sh::SEG_UNIT;
+    k.seg_cost = Sh::SEG_COST;
     k.f32_out = F32;
     k.tensor_core = true;
     k.index = index;

@@ -50,6 +50,8 @@ inline ChunkKernel make_mma_chunk_kernel(int index) {
     k.smem_bytes = Sh::SMEM_BYTES;
     k.tile_tokens = C::TT;
     k.ctas_per_sm = C::MINB;
+    k.seg_unit = Sh::SEG_UNIT;
+    k.seg_cost = Sh::SEG_COST;
     k.f32_out = F32;
     k.tensor_core = false;
     k.index = index;

@@ -1,10 +1,14 @@
 """The split schedule (host replica of the device walk) on the CPU.
 
 Checks, for random ragged batches and every split count: each token of each
-(sequence, KV head) pair is covered by exactly one CTA; runs are balanced to
-one token; every pair has exactly one owner record; partial slots are unique
-and inside the workspace; and the CTAs contributing partials to a split pair
-form the contiguous range the owner records.
+(sequence, KV head) pair is covered by exactly one CTA, in whole positions of
+the kernel's seg_unit tokens (only a pair's last may be short); each CTA's
+tokens lie in its run of a line on which a non-empty pair occupies seg_cost
+start-up positions and then one position per seg_unit tokens, with runs
+balanced to one position and filled exactly; every pair has exactly one owner
+record; partial slots are unique and inside the workspace; and the CTAs
+contributing partials to a split pair form the contiguous range the owner
+records.
 """
 from collections import defaultdict
 
@@ -28,10 +32,18 @@ def _check(lens, Hq, Hkv, D, n_split, s_max=None, max_len=None):
     rows, eff = kvd.schedule_describe(lens, s_max, max_len, Hq, Hkv, D, n_split)
     B = len(lens)
     P = B * Hkv
-    tt = kvd.kernel_info(Hq, Hkv, D)["tile_tokens"]
+    info = kvd.kernel_info(Hq, Hkv, D)
+    X, U = info["seg_cost"], info["seg_unit"]
+    assert U in (1, info["tile_tokens"])
     Lc = np.clip(lens, 0, min(s_max, max_len))
-    total = int(Lc.sum()) * Hkv
+    ext = np.where(Lc > 0, -(-Lc // U) + X, 0).astype(np.int64)
+    total = int(ext.sum()) * Hkv
     assert eff == (1 if total == 0 else min(n_split, total))
+    # independent restatement of the runs: CTA c covers positions
+    # [c*total//eff, (c+1)*total//eff); tokens [i*U, (i+1)*U) of pair p sit at
+    # position start_p + X + i
+    bounds = [c * total // eff for c in range(eff + 1)]
+    pstart = np.concatenate([[0], np.cumsum(np.repeat(ext, Hkv))])
 
     covered = defaultdict(list)
     owner = defaultdict(list)
@@ -46,6 +58,10 @@ def _check(lens, Hq, Hkv, D, n_split, s_max=None, max_len=None):
             owner[p].append((c, kind, c))
             continue
         assert 0 <= lo < hi <= Lc[b]
+        assert lo % U == 0 and (hi % U == 0 or hi == Lc[b]), "segments are whole positions"
+        v0 = pstart[p] + X
+        assert bounds[c] <= v0 + lo // U and v0 + -(-hi // U) <= bounds[c + 1], \
+            "segment outside the CTA's run"
         covered[p].append((lo, hi))
         per_cta[c] += hi - lo
         if kind in (0, 1):
@@ -65,14 +81,31 @@ def _check(lens, Hq, Hkv, D, n_split, s_max=None, max_len=None):
             pos = hi
         assert pos == Lc[b]
         c0, kind, c_last = owner[p][0]
+        # the owner's run holds the pair's first tile (its position, if empty)
+        at = pstart[p] + X if Lc[b] > 0 else pstart[p]
+        if at == total:
+            assert c0 == eff - 1
+        else:
+            assert bounds[c0] <= at < bounds[c0 + 1]
         if kind == 1:
             assert contributors[p] == set(range(c0, c_last + 1))
         elif kind == 0:
             assert len(iv) == 1 and not contributors[p]
     if total:
-        sizes = [per_cta[c] for c in range(eff)]
-        assert max(sizes) - min(sizes) <= 1 and sum(sizes) == total
-        assert min(sizes) >= 1
+        assert sum(per_cta.values()) == int(Lc.sum()) * Hkv
+        runs = np.diff(bounds)
+        assert runs.max() - runs.min() <= 1 and runs.min() >= 1
+        # a CTA's positions plus the prefixes inside its run fill the run exactly
+        tiles = defaultdict(int)
+        for c, b, h, lo, hi, kind, slot, c_last in rows.tolist():
+            if kind != 3:
+                tiles[c] += -(-hi // U) - lo // U
+        pre = defaultdict(int)
+        for p in range(P):
+            if Lc[p // Hkv] > 0:
+                for v in range(pstart[p], pstart[p] + X):
+                    pre[int(np.searchsorted(bounds, v, side="right")) - 1] += 1
+        assert all(tiles[c] + pre[c] == runs[c] for c in range(eff))
     return rows, eff
 
 
