@@ -151,6 +151,9 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     p.G = Hq / Hkv;
     p.scale_log2 = scale * 1.4426950408889634f;
     p.n_split = n_split;
+    p.tile_tokens = k->tile_tokens;
+    p.seg_unit = k->seg_unit;
+    p.seg_cost = k->seg_cost;
     p.out = out;
     p.lse = lse;
     p.status = status;
@@ -178,7 +181,9 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
         if (k->launch(*k, p, s) != cudaSuccess) return KVD_ERR_CUDA;
     }
     if ((phase & kMerge) && n_split > 1) {
-        if (launch_merge(p, D, dt == KVD_OUT_F32, s) != cudaSuccess) return KVD_ERR_CUDA;
+        int sms = 0;
+        if (device_sms(&sms) != KVD_OK) return KVD_ERR_CUDA;
+        if (launch_merge(p, D, dt == KVD_OUT_F32, sms, s) != cudaSuccess) return KVD_ERR_CUDA;
     }
     return KVD_OK;
 }

@@ -15,6 +15,7 @@ struct DecodeParams {
     int B, S_max, len_cap, Hq, Hkv, G;
     float scale_log2;     // scale * log2(e): scores are kept in base-2 units
     int n_split;          // CTAs launched for the chunk kernel
+    int tile_tokens, seg_unit, seg_cost;  // its schedule geometry (see schedule.cuh)
     void* out;            // bf16 or fp32 [B, Hq, D]
     float* lse;           // optional fp32 [B, Hq]
     int32_t* status;      // optional
@@ -40,7 +41,7 @@ const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out);
 const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out);
 const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out, int group);
 
-cudaError_t launch_merge(const DecodeParams& p, int head_dim, bool f32_out, cudaStream_t stream);
+cudaError_t launch_merge(const DecodeParams& p, int head_dim, bool f32_out, int num_sms, cudaStream_t stream);
 cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                           const int32_t* pos, int B, int S_max, int Hkv, int D,
                           int32_t* status, cudaStream_t stream);

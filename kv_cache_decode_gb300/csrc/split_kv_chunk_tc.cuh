@@ -531,6 +531,34 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                 const size_t qrow = (size_t)t.b * p.Hq + (size_t)t.h * G + row;
                 const size_t slot = (size_t)c + pair;
                 const float inv = (ltot > 0.f) ? 1.f / ltot : 0.f;
+                // Rows go out through a 1 KB staging area per warp, so that each
+                // global store instruction writes whole row pieces instead of 16
+                // bytes of 16 different rows. The staging area is the part of the P
+                // buffer this warp itself writes (its 16 rows, its half of the
+                // columns): the last O MMA has read it (o_fin), and only this warp
+                // writes it again, for the next tile, after this epilogue.
+                const bool f32_row = F32OUT || !t.full;       // 32-bit words out
+                const int words = f32_row ? 32 : 16;           // per row per 32 columns
+                const int rpr = 1024 / (words * 4);            // rows per staging round
+                const int cpr = words / 4;                     // 16-byte chunks per row piece
+                // 16-byte unit u (0..63) of the staging area -> its place in P.
+                auto stg = [&](int u) -> uint32_t {
+                    const int prow = quarter * 16 + (u >> 2);
+                    return p_buf(0, 0) + (uint32_t)(prow * 128 + (((half * 4 + (u & 3)) ^ (prow & 7)) * 16));
+                };
+                uint8_t* gbase;
+                size_t gstride;                                // bytes between rows
+                if (t.full && !F32OUT) {
+                    gbase = reinterpret_cast<uint8_t*>(p.out) + (size_t)(t.b * p.Hq + t.h * G + quarter * 16) * D * 2;
+                    gstride = (size_t)D * 2;
+                } else if (t.full) {
+                    gbase = reinterpret_cast<uint8_t*>(p.out) + (size_t)(t.b * p.Hq + t.h * G + quarter * 16) * D * 4;
+                    gstride = (size_t)D * 4;
+                } else {
+                    gbase = reinterpret_cast<uint8_t*>(p.ws_o + (slot * G + quarter * 16) * D);
+                    gstride = (size_t)D * 4;
+                }
+                const int rows_here = min(16, G - quarter * 16);  // active rows of this warp's quarter
 #pragma unroll 1
                 for (int cc = 0; cc < HD / 32; ++cc) {
                     uint32_t r[32];
@@ -538,30 +566,45 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                     __syncwarp();
                     tc::tmem_ld32(tmem + lane_base + Sh::TMEM_O + col, r);
                     tc::tmem_wait_ld();
-                    if (!active) {
-                    } else if (t.full) {
-                        if constexpr (F32OUT) {
-                            float4* o = reinterpret_cast<float4*>(reinterpret_cast<float*>(p.out) + qrow * D + col);
+                    if (rows_here <= 0) continue;
+                    // Output words in place: w[k] reads only r[k] (fp32) or r[2k], r[2k+1] (bf16).
+                    uint32_t* w = r;
+                    if (f32_row) {
+                        const float sc = t.full ? inv : 1.f;
 #pragma unroll
-                            for (int k = 0; k < 8; ++k)
-                                o[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
-                                                   __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
-                        } else {
-                            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + qrow * D + col);
-#pragma unroll
-                            for (int k = 0; k < 4; ++k)
-                                o[k] = make_uint4(
-                                    pack_bf16x2(__uint_as_float(r[8 * k]) * inv, __uint_as_float(r[8 * k + 1]) * inv),
-                                    pack_bf16x2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv),
-                                    pack_bf16x2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv),
-                                    pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv));
-                        }
+                        for (int k = 0; k < 32; ++k) w[k] = __float_as_uint(__uint_as_float(r[k]) * sc);
                     } else {
-                        float4* o = reinterpret_cast<float4*>(p.ws_o + (slot * G + row) * D + col);
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            o[k] = make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                               __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3]));
+                        for (int k = 0; k < 16; ++k)
+                            w[k] = pack_bf16x2(__uint_as_float(r[2 * k]) * inv, __uint_as_float(r[2 * k + 1]) * inv);
+                    }
+                    const size_t gcol = (size_t)col * (f32_row ? 4 : 2);
+                    for (int r0 = 0; r0 < rows_here; r0 += rpr) {
+                        __syncwarp();
+                        const int rl = lane - r0;  // this lane's row within the round
+                        if (has_row && rl >= 0 && rl < rpr) {
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                if (q < cpr) {
+                                    const uint32_t a = stg(rl * cpr + q);
+                                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a), "r"(w[4 * q]),
+                                                 "r"(w[4 * q + 1]), "r"(w[4 * q + 2]), "r"(w[4 * q + 3]) : "memory");
+                                }
+                            }
+                        }
+                        __syncwarp();
+#pragma unroll
+                        for (int it = 0; it < 2; ++it) {
+                            const int idx = it * 32 + lane;      // 16-byte chunk of the round
+                            const int rr = idx / cpr, q = idx % cpr;
+                            if (r0 + rr < rows_here) {
+                                const uint32_t a = stg(rr * cpr + q);
+                                uint4 v;
+                                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
+                                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
+                                *reinterpret_cast<uint4*>(gbase + (size_t)(r0 + rr) * gstride + gcol + q * 16) = v;
+                            }
+                        }
                     }
                 }
                 tc::fence_before_sync();
