@@ -161,7 +161,10 @@ kvd_status kvd_decode_attention(const void* q, const void* k_cache, const void* 
  *    into the workspace.
  *  - kvd_split_kv_merge: merges the partial states of every split pair by
  *    log-sum-exp: M = max_j m_j, w_j = 2^(m_j - M), out = sum_j w_j o_j /
- *    sum_j w_j l_j, skipping empty partials. A no-op when n_split is 1.
+ *    sum_j w_j l_j, skipping empty partials. A no-op when n_split is 1. It
+ *    recomputes from seq_lens which CTAs wrote partials for each pair (and
+ *    reads seq_lens before waiting for the chunk launch), so seq_lens must hold
+ *    the values the chunk call used and must not be written in between.
  */
 kvd_status kvd_split_kv_chunk(const void* q, const void* k_cache, const void* v_cache,
                               const int32_t* seq_lens, int batch, int s_max, int max_seq_len,

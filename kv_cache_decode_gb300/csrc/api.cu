@@ -80,8 +80,7 @@ size_t workspace_for(int n_split, int batch, int Hq, int Hkv, int D) {
     if (n_split <= 1 || batch == 0) return 0;
     const size_t P = (size_t)batch * Hkv, G = (size_t)(Hq / Hkv);
     const size_t slots = (size_t)n_split + P - 1;
-    return align256(P * sizeof(int2)) + align256(slots * G * D * sizeof(float)) +
-           align256(slots * G * sizeof(float2));
+    return align256(slots * G * D * sizeof(float)) + align256(slots * G * sizeof(float2));
 }
 
 kvd_status plan(int batch, int Hq, int Hkv, int D, int max_len, int num_sms, int n_split_req,
@@ -160,8 +159,6 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     if (need > 0) {
         const size_t P = (size_t)batch * Hkv, G = (size_t)p.G, slots = (size_t)n_split + P - 1;
         uint8_t* w = static_cast<uint8_t*>(workspace);
-        p.ws_rec = reinterpret_cast<int2*>(w);
-        w += align256(P * sizeof(int2));
         p.ws_o = reinterpret_cast<float*>(w);
         w += align256(slots * G * D * sizeof(float));
         p.ws_ml = reinterpret_cast<float2*>(w);

@@ -19,7 +19,6 @@ struct DecodeParams {
     void* out;            // bf16 or fp32 [B, Hq, D]
     float* lse;           // optional fp32 [B, Hq]
     int32_t* status;      // optional
-    int2* ws_rec;         // [B*Hkv] merge records; null when n_split == 1
     float* ws_o;          // [slots, G, D] partial unnormalised outputs
     float2* ws_ml;        // [slots, G] partial (max, sum), base-2 max
 };

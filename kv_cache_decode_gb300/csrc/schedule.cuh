@@ -18,9 +18,9 @@
 // its first token; for an empty pair, the CTA whose run contains its position
 // (the last CTA for empty pairs at the very end). If the owner covers the pair
 // entirely it writes the final output; otherwise each contributing CTA c writes
-// a partial (m, l, o) into slot c + p, and the owner records the range of
-// contributing CTAs for the merge kernel. Slots are unique because walking
-// segments in order, each step increments c, p or both.
+// a partial (m, l, o) into slot c + p, and the merge kernel, which recomputes
+// the range of contributing CTAs from the same walk, combines them. Slots are
+// unique because walking segments in order, each step increments c, p or both.
 #pragma once
 
 #include <stdint.h>

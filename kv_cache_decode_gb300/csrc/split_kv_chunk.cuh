@@ -234,7 +234,6 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
         }
         if (p.lse)
             for (int i = tid; i < G; i += NT) p.lse[row + i] = -CUDART_INF_F;
-        if (tid == 0 && p.ws_rec) p.ws_rec[(size_t)b * p.Hkv + h] = make_int2(-1, -1);
     };
 
     // ---- per-warp state ----
@@ -474,7 +473,6 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                         if (v0) p.lse[qrow + r0] = (m0 + log2f(l0)) * 0.69314718055994531f;
                         if (v1) p.lse[qrow + r1] = (m1 + log2f(l1)) * 0.69314718055994531f;
                     }
-                    if (tid == 0 && p.ws_rec) p.ws_rec[pair] = make_int2(-1, -1);
                 } else {
                     const size_t slot = (size_t)c + pair;
                     float* wo = p.ws_o + slot * G * D;
@@ -488,7 +486,6 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                         if (v0) p.ws_ml[slot * G + r0] = make_float2(m0, l0);
                         if (v1) p.ws_ml[slot * G + r1] = make_float2(m1, l1);
                     }
-                    if (tid == 0 && ct.owned) p.ws_rec[pair] = make_int2(c, ct.c_last);
                 }
             }
             if constexpr (TS > 1) __syncthreads();

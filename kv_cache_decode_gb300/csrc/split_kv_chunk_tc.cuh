@@ -402,7 +402,6 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             }
             if (p.lse)
                 for (int i2 = st; i2 < G; i2 += 256) p.lse[r0 + i2] = -CUDART_INF_F;
-            if (st == 0 && p.ws_rec) p.ws_rec[(size_t)b * p.Hkv + h] = make_int2(-1, -1);
         };
 
         float m_used = 0.f, l = 0.f;  // l: this half's share of the row sum
@@ -615,9 +614,6 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                         p.ws_ml[slot * G + row] = make_float2(m_used, ltot);
                     }
                 }
-                // Only the pair's owner writes its merge record.
-                if (st == 0 && p.ws_rec && t.owned)
-                    p.ws_rec[pair] = t.full ? make_int2(-1, -1) : make_int2(c, t.c_last);
             }
             ++i;
         }

@@ -11,8 +11,8 @@
 // s + 2S, ... The work is latency-bound (a few KB per row, read from L2), so:
 //  * the contributing CTAs of each pair are recomputed from the lengths with
 //    the chunk kernel's own schedule code, before the dependency wait (the
-//    lengths are an input, not a chunk-kernel output), instead of being read
-//    from a record the chunk kernel wrote, which would cost a round trip;
+//    lengths are an input, not a chunk-kernel output), so no round trip is
+//    spent reading it from the workspace;
 //  * each thread issues the loads of a whole batch of its partials before
 //    using any of them, one round trip per batch of kBatch partials. Batches
 //    after the first are folded in with the running maximum (rescaling the

@@ -56,7 +56,7 @@ extern "C" kvd_status kvd_decode_attention_static(const void* q, const void* k_c
         if (st != KVD_OK) return st;
     }
     // Nothing in the workspace needs to start at zero: every call writes the
-    // merge records and partial states it reads.
+    // partial states it reads.
     return kvd_decode_attention(q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q,
                                 n_heads_kv, head_dim, scale, n_split, ws, need > 0 ? KVD_STATIC_WORKSPACE_BYTES : 0,
                                 out, out_dtype, lse_out, status_word, stream);
