@@ -20,10 +20,11 @@
 // rescaling O in TMEM is rare; the result is identical in exact arithmetic
 // because O and l always share the same m.
 //
-// Warp roles (11 warps): 0 = TMA producer for K (and Q at each new pair),
-// 1 = MMA issuer (one thread) and TMEM owner, 2 = TMA producer for V,
-// 3..10 = softmax / rescale / epilogue (two warps per TMEM lane quarter w % 4,
-// splitting the token columns of S and the output columns of O).
+// Warp roles (13 warps): 0 = TMA producer for K (and Q at each new pair),
+// 2 = TMA producer for V, 1 and 11 = S issuers (one thread each, one half of
+// head_dim each; warp 1 also owns TMEM), 12 = O issuer, 3..10 = softmax /
+// rescale / epilogue (two warps per TMEM lane quarter w % 4, splitting the
+// token columns of S and the output columns of O).
 // Pipelines: K ring of KST stages, V ring of VST stages, two S buffers in
 // TMEM, two P buffers in shared memory, one Q buffer, O in TMEM. Every wait is
 // bounded; a timeout flags KVD_STATUS_TIMEOUT and all roles wind down.
@@ -80,14 +81,17 @@ struct TcShape {
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int STATIC_SMEM = 2048;  // block scans and the exchange buffer (checked by ptxas -v)
-    static constexpr int TMEM_S = 0;             // S buffers at columns 0 and T
-    static constexpr int TMEM_O = 2 * T;         // O at columns [2T, 2T + D)
-    static constexpr int TMEM_COLS = (2 * T + D) <= 256 ? 256 : 512;
-    static constexpr int NWARPS = 11;  // producers 0 and 2, MMA 1, softmax 3..10
+    static constexpr int TMEM_S = 0;             // S, first head_dim half: columns 0 and T
+    static constexpr int TMEM_S2 = 2 * T;        // S, second half: columns 2T and 3T
+    static constexpr int TMEM_O = 4 * T;         // O at columns [4T, 4T + D)
+    static constexpr int TMEM_COLS = (4 * T + D) <= 256 ? 256 : 512;
+    // producers 0 and 2, S issuers 1 and 11, O issuer 12, softmax 3..10
+    static constexpr int NWARPS = 13;
     static constexpr int THREADS = NWARPS * 32;
     static_assert(KST >= 2, "need at least two K stages");
     static_assert(SMEM_BYTES + STATIC_SMEM <= 227 * 1024, "shared memory budget");
     static_assert(QR % 8 == 0 && QR <= 64, "Q rows per block");
+    static_assert(4 * T + D <= 512, "TMEM columns");
 };
 
 struct TcMaps {
@@ -150,7 +154,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     if (tid == 0) {
         for (int s = 0; s < KST; ++s) {
             tc::mbar_init(k_full(s), 1);
-            tc::mbar_init(k_empty(s), 1);
+            tc::mbar_init(k_empty(s), 2);  // both S issuers
         }
         for (int s = 0; s < VST; ++s) {
             tc::mbar_init(v_full(s), 1);
@@ -158,15 +162,15 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
         }
         for (int s = 0; s < NQ; ++s) {
             tc::mbar_init(q_full(s), 1);
-            tc::mbar_init(q_empty(s), 1);
+            tc::mbar_init(q_empty(s), 2);
         }
         for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(s_full(b), 1);
+            tc::mbar_init(s_full(b), 2);
             tc::mbar_init(s_free(b), 8);
             tc::mbar_init(p_full(b), 8);
             tc::mbar_init(o_fin(b), 1);
         }
-        tc::mbar_init(mma_done, 1);
+        tc::mbar_init(mma_done, 3);  // S issuers and O issuer
         for (int q = 0; q < 4; ++q) tc::mbar_init(xbar(q), 2);
         *abort_flag = 0;
         tc::mbar_fence_init();
@@ -268,29 +272,59 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             }
             if (is_k && qn > 0) tc::mbar_wait(q_full((qn - 1) % NQ), ((qn - 1) / NQ) & 1, abort_flag, kBudget / 4);
         }
-    } else if (warp == 1) {
-        // ===================== MMA issuer =====================
+    } else if (warp == 1 || warp == 11) {
+        // ===================== S issuers (one thread each) =====================
+        // S = Q K^T is issued as two independent accumulations over the two
+        // halves of head_dim, by two threads into two TMEM buffers that the
+        // softmax adds: a tcgen05.mma of this shape costs its issuing thread
+        // about as long as the tensor core needs for two of them, so two
+        // issuers finish a tile's S in half the time and release its K stage
+        // sooner.
         if (lane == 0) {
+            const int kh = (warp == 11) ? 1 : 0;
+            constexpr int KH = D / 32;  // k-steps per half
             constexpr uint32_t idesc_s = tc::idesc_bf16_f32(64, T, false, false);
-            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(64, D, false, true);
-            int qn = 0;
-            auto mma_s = [&](bool seg_end, int i, int qs) {
+            const uint32_t s_base = tmem + (kh ? Sh::TMEM_S2 : Sh::TMEM_S);
+            Tile t;
+            int i = 0, qn = 0;
+            while (walker.next(t, NoOp{})) {
                 const int sk = i % KST, sb = i & 1;
-                const uint32_t qt = sQ + (uint32_t)(qs * Sh::QS_BYTES);
+                if (t.seg_start) {
+                    if (!tc::mbar_wait(q_full(qn % NQ), (qn / NQ) & 1, abort_flag, kBudget)) break;
+                    ++qn;
+                }
+                const int qs = (qn - 1) % NQ;
+                if (!tc::mbar_wait(k_full(sk), (i / KST) & 1, abort_flag, kBudget)) break;
+                if (!tc::mbar_wait(s_free(sb), ((i >> 1) & 1) ^ 1, abort_flag, kBudget)) break;
                 tc::fence_after_sync();
+                const uint32_t qt = sQ + (uint32_t)(qs * Sh::QS_BYTES);
                 const uint32_t kt = sK + (uint32_t)(sk * Sh::TILE_BYTES);
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
+                for (int k = 0; k < KH; ++k) {
+                    const int kk = kh * KH + k;
                     const uint64_t a = tc::sdesc_sw128(qt + (kk >> 2) * Sh::QB_BYTES + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = tc::sdesc_sw128(kt + (kk >> 2) * Sh::KB_BYTES + (kk & 3) * 32, 16, 1024);
-                    tc::mma_bf16(tmem + Sh::TMEM_S + sb * T, a, b, idesc_s, kk > 0);
+                    tc::mma_bf16(s_base + sb * T, a, b, idesc_s, k > 0);
                 }
                 tc::mma_commit(s_full(sb));
                 tc::mma_commit(k_empty(sk));
-                if (seg_end) tc::mma_commit(q_empty(qs));
-            };
-            auto mma_o = [&](bool seg_start, int i) {
+                if (t.seg_end) tc::mma_commit(q_empty(qs));
+                ++i;
+            }
+            // This thread's tensor-core work done before TMEM is released.
+            tc::mma_commit(mma_done);
+            tc::mbar_wait(mma_done, 0, abort_flag, kBudget);
+        }
+    } else if (warp == 12) {
+        // ===================== O issuer (one thread) =====================
+        if (lane == 0) {
+            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(64, D, false, true);
+            Tile t;
+            int i = 0;
+            while (walker.next(t, NoOp{})) {
                 const int sv = i % VST, sb = i & 1;
+                if (!tc::mbar_wait(v_full(sv), (i / VST) & 1, abort_flag, kBudget)) break;
+                if (!tc::mbar_wait(p_full(sb), (i >> 1) & 1, abort_flag, kBudget)) break;
                 tc::fence_after_sync();
                 const uint32_t vt = sV + (uint32_t)(sv * Sh::TILE_BYTES);
 #pragma unroll
@@ -299,62 +333,13 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
 #pragma unroll
                     for (int part = 0; part < Sh::NP; ++part) {
                         const uint64_t a = tc::sdesc_sw128(p_buf(sb, part) + k2 * 32, 16, 1024);
-                        tc::mma_bf16(tmem + Sh::TMEM_O, a, b, idesc_o,
-                                     (seg_start && k2 == 0 && part == 0) ? 0u : 1u);
+                        tc::mma_bf16(tmem + Sh::TMEM_O, a, b, idesc_o, (t.seg_start && k2 == 0 && part == 0) ? 0u : 1u);
                     }
                 }
                 tc::mma_commit(v_empty(sv));
                 tc::mma_commit(o_fin(sb));
-            };
-            // Issue whichever of S(i) = Q K^T and O += P(j) V(j) is ready first, so that
-            // S of upcoming tiles is never queued behind a wait for P or V.
-            // Tiles between o_idx and the walker's position: only their segment
-            // start/end flags are needed, kept as 2 bits per tile in a register.
-            uint32_t flags = 0;
-            auto flag = [&](int idx) { return (flags >> (2 * (idx & 15))) & 3u; };
-            int n_fetched = 0, s_idx = 0, o_idx = 0;
-            bool walker_done = false;
-            long long idle_since = clock64();
-            while (true) {
-                while (!walker_done && n_fetched < o_idx + 4) {
-                    Tile t;
-                    if (walker.next(t, NoOp{})) {
-                        const int sh2 = 2 * (n_fetched & 15);
-                        flags = (flags & ~(3u << sh2)) | ((t.seg_start ? 1u : 0u) << sh2) | ((t.seg_end ? 2u : 0u) << sh2);
-                        ++n_fetched;
-                    } else {
-                        walker_done = true;
-                    }
-                }
-                if (walker_done && o_idx == n_fetched) break;
-                bool progress = false;
-                if (s_idx < n_fetched && s_idx < o_idx + 3) {
-                    const uint32_t f = flag(s_idx);
-                    if (tc::mbar_test(k_full(s_idx % KST), (s_idx / KST) & 1) &&
-                        tc::mbar_test(s_free(s_idx & 1), ((s_idx >> 1) & 1) ^ 1) &&
-                        (!(f & 1u) || tc::mbar_test(q_full(qn % NQ), (qn / NQ) & 1))) {
-                        if (f & 1u) ++qn;
-                        mma_s((f & 2u) != 0, s_idx, (qn - 1) % NQ);
-                        ++s_idx;
-                        progress = true;
-                    }
-                }
-                if (o_idx < s_idx) {
-                    if (tc::mbar_test(v_full(o_idx % VST), (o_idx / VST) & 1) &&
-                        tc::mbar_test(p_full(o_idx & 1), (o_idx >> 1) & 1)) {
-                        mma_o((flag(o_idx) & 1u) != 0, o_idx);
-                        ++o_idx;
-                        progress = true;
-                    }
-                }
-                if (progress) {
-                    idle_since = clock64();
-                } else if (*abort_flag || clock64() - idle_since > kBudget) {
-                    *abort_flag = 1;
-                    break;
-                }
+                ++i;
             }
-            // All tensor-core work of this CTA done before TMEM is released.
             tc::mma_commit(mma_done);
             tc::mbar_wait(mma_done, 0, abort_flag, kBudget);
         }
@@ -414,8 +399,10 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             if (!ok) break;
             tc::fence_after_sync();
             __syncwarp();
-            uint32_t sr[HT];
+            // S is held as two partial sums over the halves of head_dim.
+            uint32_t sr[HT], sr2[HT];
             tc::tmem_ld32(tmem + lane_base + Sh::TMEM_S + sb * T + half * HT, sr);
+            tc::tmem_ld32(tmem + lane_base + Sh::TMEM_S2 + sb * T + half * HT, sr2);
             tc::tmem_wait_ld();
             tc::fence_before_sync();
             __syncwarp();
@@ -427,7 +414,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             float s[HT];
 #pragma unroll
             for (int k = 0; k < HT; ++k)
-                s[k] = (k < nv) ? __uint_as_float(sr[k]) * scale_log2 : -CUDART_INF_F;
+                s[k] = (k < nv) ? (__uint_as_float(sr[k]) + __uint_as_float(sr2[k])) * scale_log2 : -CUDART_INF_F;
             float mx[8];
 #pragma unroll
             for (int k = 0; k < 8; ++k) mx[k] = fmaxf(fmaxf(s[k], s[k + 8]), fmaxf(s[k + 16], s[k + 24]));
