@@ -356,25 +356,14 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
         const int sw = warp - 3;    // 0..7
         const int quarter = warp & 3;
         const int half = sw >> 2;
-        const int row = quarter * 16 + lane;   // group-local query head of this thread
+        // Lane layout of the epilogue (32x32b TMEM shape): lanes 0..15 hold rows.
+        const int row = quarter * 16 + lane;   // group-local query head of this lane
         const bool has_row = lane < 16;
         const bool active = has_row && row < G;
         const int st = tid - 3 * 32;           // 0..255 among the softmax threads
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const float scale_log2 = p.scale_log2;
         int nx = 0;  // exchanges done with the partner warp
-
-        // Exchange one float per row with the partner warp; returns the partner's.
-        auto exchange = [&](float v, bool& ok_) -> float {
-            float* buf = xbuf + ((nx & 1) * 4 + quarter) * 32;
-            if (has_row) buf[half * 16 + lane] = v;
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(xbar(quarter));
-            ok_ = __all_sync(0xffffffffu, tc::mbar_wait(xbar(quarter), nx & 1, abort_flag, kBudget));
-            const float other = buf[(half ^ 1) * 16 + (lane & 15)];
-            ++nx;
-            return other;
-        };
 
         auto write_empty = [&](int b, int h) {
             const size_t r0 = (size_t)b * p.Hq + (size_t)h * G;
@@ -389,7 +378,36 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                 for (int i2 = st; i2 < G; i2 += 256) p.lse[r0 + i2] = -CUDART_INF_F;
         };
 
-        float m_used = 0.f, l = 0.f;  // l: this half's share of the row sum
+        // S is read with the 16x256b TMEM shape, which puts the quarter's 16
+        // rows on all 32 threads in the mma accumulator layout: thread t holds
+        // rows rA = t/4 and rB = t/4 + 8 of the quarter, columns 8g + 2(t%4) + 0..1
+        // of each 8-column group g of its half. Row statistics are reduced over
+        // the 4 threads of a quad, then with the partner warp (other half).
+        const int rA = quarter * 16 + (lane >> 2), rB = rA + 8;
+        const bool actA = rA < G, actB = rB < G;
+        // Exchange two per-row floats (rows rA, rB) with the partner warp.
+        auto exchange2 = [&](float va, float vb, float& oa, float& ob, bool& ok_) {
+            float* buf = xbuf + ((nx & 1) * 4 + quarter) * 32;
+            if ((lane & 3) == 0) {
+                buf[half * 16 + (lane >> 2)] = va;
+                buf[half * 16 + 8 + (lane >> 2)] = vb;
+            }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(xbar(quarter));
+            ok_ = __all_sync(0xffffffffu, tc::mbar_wait(xbar(quarter), nx & 1, abort_flag, kBudget));
+            oa = buf[(half ^ 1) * 16 + (lane >> 2)];
+            ob = buf[(half ^ 1) * 16 + 8 + (lane >> 2)];
+            ++nx;
+        };
+        // Per-row value of the quad layout moved to the lane layout (lane = row, lanes 0..15).
+        auto to_lane = [&](float a, float b) {
+            const float xa = __shfl_sync(0xffffffffu, a, (lane & 7) * 4);
+            const float xb = __shfl_sync(0xffffffffu, b, (lane & 7) * 4);
+            return (lane & 8) ? xb : xa;
+        };
+
+        float mA = 0.f, mB = 0.f;  // running maxima of rows rA, rB
+        float lA = 0.f, lB = 0.f;  // this thread's share of the row sums
         Tile t;
         int i = 0;
         bool ok = true;
@@ -400,9 +418,9 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             tc::fence_after_sync();
             __syncwarp();
             // S is held as two partial sums over the halves of head_dim.
-            uint32_t sr[HT], sr2[HT];
-            tc::tmem_ld32(tmem + lane_base + Sh::TMEM_S + sb * T + half * HT, sr);
-            tc::tmem_ld32(tmem + lane_base + Sh::TMEM_S2 + sb * T + half * HT, sr2);
+            uint32_t sr[16], sr2[16];
+            tc::tmem_ld_16x256b_x4(tmem + lane_base + Sh::TMEM_S + sb * T + half * HT, sr);
+            tc::tmem_ld_16x256b_x4(tmem + lane_base + Sh::TMEM_S2 + sb * T + half * HT, sr2);
             tc::tmem_wait_ld();
             tc::fence_before_sync();
             __syncwarp();
@@ -411,44 +429,65 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             // Scores in base-2 units; columns past the tile's last token masked.
             const int nvalid = t.tok_hi - t.tok_lo;
             const int nv = nvalid - half * HT;  // valid columns of this half (may be <= 0)
-            float s[HT];
+            float s[16];
 #pragma unroll
-            for (int k = 0; k < HT; ++k)
-                s[k] = (k < nv) ? (__uint_as_float(sr[k]) + __uint_as_float(sr2[k])) * scale_log2 : -CUDART_INF_F;
-            float mx[8];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) mx[k] = fmaxf(fmaxf(s[k], s[k + 8]), fmaxf(s[k + 16], s[k + 24]));
-#pragma unroll
-            for (int k = 0; k < 4; ++k) mx[k] = fmaxf(mx[k], mx[k + 4]);
-            const float mh = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
-            const float mt = fmaxf(mh, exchange(mh, ok));
-            if (!ok) break;
-
-            bool need = false;
-            float alpha = 1.f;
-            if (t.seg_start) {
-                m_used = mt;
-                l = 0.f;
-            } else if (mt > m_used + 8.f) {
-                need = true;
-                alpha = exp2f(m_used - mt);
-                m_used = mt;
+            for (int e = 0; e < 16; ++e) {
+                const int col = 8 * (e >> 2) + 2 * (lane & 3) + (e & 1);
+                s[e] = (col < nv) ? (__uint_as_float(sr[e]) + __uint_as_float(sr2[e])) * scale_log2 : -CUDART_INF_F;
             }
-            // P = 2^(s - m) into registers (bf16 hi part; lo part for fp32 output).
-            uint32_t hi[HT / 2], lo[F32OUT ? HT / 2 : 1];
-            float ls = 0.f;
+            float xA = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[4], s[5]));
+            float xB = fmaxf(fmaxf(s[2], s[3]), fmaxf(s[6], s[7]));
+            xA = fmaxf(xA, fmaxf(fmaxf(s[8], s[9]), fmaxf(s[12], s[13])));
+            xB = fmaxf(xB, fmaxf(fmaxf(s[10], s[11]), fmaxf(s[14], s[15])));
+            xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, 1));
+            xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, 1));
+            xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, 2));
+            xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, 2));
+            float oA, oB;
+            exchange2(xA, xB, oA, oB, ok);
+            if (!ok) break;
+            const float mtA = fmaxf(xA, oA), mtB = fmaxf(xB, oB);
+
+            bool needA = false, needB = false;
+            float alphaA = 1.f, alphaB = 1.f;
+            if (t.seg_start) {
+                mA = mtA;
+                mB = mtB;
+                lA = lB = 0.f;
+            } else {
+                if (mtA > mA + 8.f) {
+                    needA = true;
+                    alphaA = exp2f(mA - mtA);
+                    mA = mtA;
+                }
+                if (mtB > mB + 8.f) {
+                    needB = true;
+                    alphaB = exp2f(mB - mtB);
+                    mB = mtB;
+                }
+            }
+            // P = 2^(s - m), packed per row and 8-column group (bf16 hi part; lo
+            // part for fp32 output).
+            uint32_t hiA[4], hiB[4], loA[4], loB[4];
+            float lsA = 0.f, lsB = 0.f;
 #pragma unroll
-            for (int k2 = 0; k2 < HT / 2; ++k2) {
-                const float e0 = active ? tc::ex2_approx(s[2 * k2] - m_used) : 0.f;
-                const float e1 = active ? tc::ex2_approx(s[2 * k2 + 1] - m_used) : 0.f;
-                hi[k2] = pack_bf16x2(e0, e1);
+            for (int g = 0; g < 4; ++g) {
+                const float e0 = actA ? tc::ex2_approx(s[4 * g] - mA) : 0.f;
+                const float e1 = actA ? tc::ex2_approx(s[4 * g + 1] - mA) : 0.f;
+                const float e2 = actB ? tc::ex2_approx(s[4 * g + 2] - mB) : 0.f;
+                const float e3 = actB ? tc::ex2_approx(s[4 * g + 3] - mB) : 0.f;
+                hiA[g] = pack_bf16x2(e0, e1);
+                hiB[g] = pack_bf16x2(e2, e3);
                 if constexpr (F32OUT) {
-                    lo[k2] = pack_bf16x2(e0 - bf16_lo(hi[k2]), e1 - bf16_hi(hi[k2]));
-                    ls += e0 + e1;
+                    loA[g] = pack_bf16x2(e0 - bf16_lo(hiA[g]), e1 - bf16_hi(hiA[g]));
+                    loB[g] = pack_bf16x2(e2 - bf16_lo(hiB[g]), e3 - bf16_hi(hiB[g]));
+                    lsA += e0 + e1;
+                    lsB += e2 + e3;
                 } else {
                     // The weights actually multiplied into V are the rounded ones;
                     // summing those keeps the output an exact convex combination.
-                    ls += bf16_lo(hi[k2]) + bf16_hi(hi[k2]);
+                    lsA += bf16_lo(hiA[g]) + bf16_hi(hiA[g]);
+                    lsB += bf16_lo(hiB[g]) + bf16_hi(hiB[g]);
                 }
             }
 
@@ -459,7 +498,9 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                 if (!ok) break;
                 tc::fence_after_sync();
             }
-            if (__any_sync(0xffffffffu, need && has_row)) {
+            if (__any_sync(0xffffffffu, needA || needB)) {
+                // O rows sit one per TMEM lane (lanes 0..15 of the quarter).
+                const float alpha = to_lane(alphaA, alphaB);
 #pragma unroll 1
                 for (int cc = 0; cc < HD / 32; ++cc) {
                     uint32_t r[32];
@@ -473,18 +514,18 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                 }
                 tc::tmem_wait_st();
             }
-            l = l * alpha + ls;
-            if (has_row) {
-                const uint32_t prow = p_buf(sb, 0) + (uint32_t)row * 128;
-                const uint32_t prow_lo = p_buf(sb, Sh::NP - 1) + (uint32_t)row * 128;
-#pragma unroll
-                for (int ch = 0; ch < 4; ++ch) {
-                    const uint32_t off = (uint32_t)(((half * 4 + ch) ^ (row & 7)) * 16);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(prow + off), "r"(hi[4 * ch]),
-                                 "r"(hi[4 * ch + 1]), "r"(hi[4 * ch + 2]), "r"(hi[4 * ch + 3]) : "memory");
-                    if constexpr (F32OUT)
-                        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(prow_lo + off), "r"(lo[4 * ch]),
-                                     "r"(lo[4 * ch + 1]), "r"(lo[4 * ch + 2]), "r"(lo[4 * ch + 3]) : "memory");
+            lA = lA * alphaA + lsA;
+            lB = lB * alphaB + lsB;
+            {
+                // Thread t addresses row t % 8 of matrix t / 8 (= 8-column group).
+                const int rin = lane & 7, gq = lane >> 3;
+                const uint32_t offA = (uint32_t)((quarter * 16 + rin) * 128 + (((half * 4 + gq) ^ rin) * 16));
+                const uint32_t offB = offA + 8 * 128;
+                stmatrix_x4(p_buf(sb, 0) + offA, hiA[0], hiA[1], hiA[2], hiA[3]);
+                stmatrix_x4(p_buf(sb, 0) + offB, hiB[0], hiB[1], hiB[2], hiB[3]);
+                if constexpr (F32OUT) {
+                    stmatrix_x4(p_buf(sb, 1) + offA, loA[0], loA[1], loA[2], loA[3]);
+                    stmatrix_x4(p_buf(sb, 1) + offB, loB[0], loB[1], loB[2], loB[3]);
                 }
             }
             if (nvalid < T) {
@@ -508,97 +549,58 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             if (lane == 0) tc::mbar_arrive(p_full(sb));
 
             if (t.seg_end) {
-                const float ltot = l + exchange(l, ok);
+                float qA = lA + __shfl_xor_sync(0xffffffffu, lA, 1);
+                float qB = lB + __shfl_xor_sync(0xffffffffu, lB, 1);
+                qA += __shfl_xor_sync(0xffffffffu, qA, 2);
+                qB += __shfl_xor_sync(0xffffffffu, qB, 2);
+                float pA, pB;
+                exchange2(qA, qB, pA, pB, ok);
                 if (!ok) break;
+                // The epilogue works in the lane layout: this lane's row (lanes 0..15).
+                const float ltot = to_lane(qA + pA, qB + pB);
+                const float m_row = to_lane(mA, mB);
                 ok = __all_sync(0xffffffffu, tc::mbar_wait(o_fin(sb), (i >> 1) & 1, abort_flag, kBudget));
                 if (!ok) break;
                 tc::fence_after_sync();
                 const size_t pair = (size_t)t.b * p.Hkv + t.h;
                 const size_t qrow = (size_t)t.b * p.Hq + (size_t)t.h * G + row;
                 const size_t slot = (size_t)c + pair;
-                const float inv = (ltot > 0.f) ? 1.f / ltot : 0.f;
-                // Rows go out through a 1 KB staging area per warp, so that each
-                // global store instruction writes whole row pieces instead of 16
-                // bytes of 16 different rows. The staging area is the part of the P
-                // buffer this warp itself writes (its 16 rows, its half of the
-                // columns): the last O MMA has read it (o_fin), and only this warp
-                // writes it again, for the next tile, after this epilogue.
-                const bool f32_row = F32OUT || !t.full;       // 32-bit words out
-                const int words = f32_row ? 32 : 16;           // per row per 32 columns
-                const int rpr = 1024 / (words * 4);            // rows per staging round
-                const int cpr = words / 4;                     // 16-byte chunks per row piece
-                // 16-byte unit u (0..63) of the staging area -> its place in P.
-                auto stg = [&](int u) -> uint32_t {
-                    const int prow = quarter * 16 + (u >> 2);
-                    return p_buf(0, 0) + (uint32_t)(prow * 128 + (((half * 4 + (u & 3)) ^ (prow & 7)) * 16));
-                };
-                uint8_t* gbase;
-                size_t gstride;                                // bytes between rows
-                if (t.full && !F32OUT) {
-                    gbase = reinterpret_cast<uint8_t*>(p.out) + (size_t)(t.b * p.Hq + t.h * G + quarter * 16) * D * 2;
-                    gstride = (size_t)D * 2;
-                } else if (t.full) {
-                    gbase = reinterpret_cast<uint8_t*>(p.out) + (size_t)(t.b * p.Hq + t.h * G + quarter * 16) * D * 4;
-                    gstride = (size_t)D * 4;
-                } else {
-                    gbase = reinterpret_cast<uint8_t*>(p.ws_o + (slot * G + quarter * 16) * D);
-                    gstride = (size_t)D * 4;
-                }
-                const int rows_here = min(16, G - quarter * 16);  // active rows of this warp's quarter
+                // O is read with the 16x256b shape as well, so every thread holds
+                // two rows (rA, rB) and 2 adjacent columns of each 8-column group:
+                // a quad writes 32 contiguous bytes of a row (one full sector).
+                const float totA = qA + pA, totB = qB + pB;
+                const float invA = t.full ? ((totA > 0.f) ? 1.f / totA : 0.f) : 1.f;
+                const float invB = t.full ? ((totB > 0.f) ? 1.f / totB : 0.f) : 1.f;
+                const size_t grow = t.full ? (size_t)t.b * p.Hq + (size_t)t.h * G : slot * G;  // row of head 0
 #pragma unroll 1
                 for (int cc = 0; cc < HD / 32; ++cc) {
-                    uint32_t r[32];
-                    const int col = half * HD + cc * 32;
+                    const int col0 = half * HD + cc * 32 + 2 * (lane & 3);
+                    uint32_t r[16];
                     __syncwarp();
-                    tc::tmem_ld32(tmem + lane_base + Sh::TMEM_O + col, r);
+                    tc::tmem_ld_16x256b_x4(tmem + lane_base + Sh::TMEM_O + half * HD + cc * 32, r);
                     tc::tmem_wait_ld();
-                    if (rows_here <= 0) continue;
-                    // Output words in place: w[k] reads only r[k] (fp32) or r[2k], r[2k+1] (bf16).
-                    uint32_t* w = r;
-                    if (f32_row) {
-                        const float sc = t.full ? inv : 1.f;
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) w[k] = __float_as_uint(__uint_as_float(r[k]) * sc);
-                    } else {
-#pragma unroll
-                        for (int k = 0; k < 16; ++k)
-                            w[k] = pack_bf16x2(__uint_as_float(r[2 * k]) * inv, __uint_as_float(r[2 * k + 1]) * inv);
-                    }
-                    const size_t gcol = (size_t)col * (f32_row ? 4 : 2);
-                    for (int r0 = 0; r0 < rows_here; r0 += rpr) {
-                        __syncwarp();
-                        const int rl = lane - r0;  // this lane's row within the round
-                        if (has_row && rl >= 0 && rl < rpr) {
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                if (q < cpr) {
-                                    const uint32_t a = stg(rl * cpr + q);
-                                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(a), "r"(w[4 * q]),
-                                                 "r"(w[4 * q + 1]), "r"(w[4 * q + 2]), "r"(w[4 * q + 3]) : "memory");
-                                }
-                            }
-                        }
-                        __syncwarp();
-#pragma unroll
-                        for (int it = 0; it < 2; ++it) {
-                            const int idx = it * 32 + lane;      // 16-byte chunk of the round
-                            const int rr = idx / cpr, q = idx % cpr;
-                            if (r0 + rr < rows_here) {
-                                const uint32_t a = stg(rr * cpr + q);
-                                uint4 v;
-                                asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];\n"
-                                             : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a) : "memory");
-                                *reinterpret_cast<uint4*>(gbase + (size_t)(r0 + rr) * gstride + gcol + q * 16) = v;
-                            }
+                    for (int g = 0; g < 4; ++g) {
+                        const int col = col0 + 8 * g;
+                        const float a0 = __uint_as_float(r[4 * g]) * invA, a1 = __uint_as_float(r[4 * g + 1]) * invA;
+                        const float b0 = __uint_as_float(r[4 * g + 2]) * invB, b1 = __uint_as_float(r[4 * g + 3]) * invB;
+                        if (t.full && !F32OUT) {
+                            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out);
+                            if (actA) *reinterpret_cast<uint32_t*>(o + (grow + rA) * D + col) = pack_bf16x2(a0, a1);
+                            if (actB) *reinterpret_cast<uint32_t*>(o + (grow + rB) * D + col) = pack_bf16x2(b0, b1);
+                        } else {
+                            float* o = t.full ? reinterpret_cast<float*>(p.out) : p.ws_o;
+                            if (actA) *reinterpret_cast<float2*>(o + (grow + rA) * D + col) = make_float2(a0, a1);
+                            if (actB) *reinterpret_cast<float2*>(o + (grow + rB) * D + col) = make_float2(b0, b1);
                         }
                     }
                 }
                 tc::fence_before_sync();
                 if (active && half == 0) {
                     if (t.full) {
-                        if (p.lse) p.lse[qrow] = (m_used + log2f(ltot)) * 0.69314718055994531f;
+                        if (p.lse) p.lse[qrow] = (m_row + log2f(ltot)) * 0.69314718055994531f;
                     } else {
-                        p.ws_ml[slot * G + row] = make_float2(m_used, ltot);
+                        p.ws_ml[slot * G + row] = make_float2(m_row, ltot);
                     }
                 }
             }
