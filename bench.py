@@ -292,9 +292,9 @@ def run_ours(args):
     launches_per_step = 2 + (1 if n_split > 1 else 0)
 
     def step(r, stream=None):
-        kvd.kv_append(kcs[r], vcs[r], kn, vn, pos, stream=stream)
-        kvd.decode_attention(q, kcs[r], vcs[r], lens, max_len, w.scale, out, workspace=ws,
-                             n_split=args.n_split, stream=stream)
+        # append the new token's K/V rows, then attend (one call, three launches)
+        kvd.decode_step(q, kcs[r], vcs[r], kn, vn, pos, lens, max_len, w.scale, out, workspace=ws,
+                        n_split=args.n_split, stream=stream)
 
     for i in range(max(args.warmup, 3)):
         step(i % R)

@@ -152,6 +152,28 @@ kvd_status kvd_decode_attention(const void* q, const void* k_cache, const void* 
                                 int32_t* status_word, kvd_stream_t stream);
 
 /*
+ * kvd_decode_step: one generation step's cache work in one call, exactly
+ * kvd_kv_append(k_cache, v_cache, k_new, v_new, pos, ...) followed by
+ * kvd_decode_attention(q, k_cache, v_cache, seq_lens, ...) on the same stream
+ * (All About Transformer Inference, "Transformer inference basics",
+ * Generation: the new token's key and value join the cache, then its query
+ * attends over it). Arguments, layouts and errors are those of the two calls;
+ * nothing is launched if either call's arguments are rejected.
+ * Difference in timing only: the attention launch begins while the append
+ * runs. It works out its schedule and loads q and seq_lens before the append
+ * has finished, and waits for the append only before loading cache rows. So
+ * q, seq_lens and pos must be complete when this call's work starts on the
+ * stream (as for any stream-ordered input), and only the cache rows may be
+ * produced by the append.
+ */
+kvd_status kvd_decode_step(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                           const int32_t* pos, const void* q, const int32_t* seq_lens, int batch,
+                           int s_max, int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim,
+                           float scale, int n_split, void* workspace, size_t workspace_bytes,
+                           void* out, kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                           kvd_stream_t stream);
+
+/*
  * The two launches of kvd_decode_attention, exposed separately so that each
  * can be timed on its own. Arguments and errors are those of
  * kvd_decode_attention; calling kvd_split_kv_chunk then kvd_split_kv_merge on

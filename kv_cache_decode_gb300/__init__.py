@@ -29,7 +29,7 @@ STATUS_POS_OUT_OF_RANGE = 0x2
 EXPORTED = (
     "kvd_decode_plan", "kvd_kv_append", "kvd_decode_attention", "kvd_split_kv_chunk",
     "kvd_split_kv_merge", "kvd_schedule_describe", "kvd_kernel_info", "kvd_status_string",
-    "kvd_version", "kvd_decode_attention_static",
+    "kvd_version", "kvd_decode_attention_static", "kvd_decode_step",
 )
 STATIC_WORKSPACE_BYTES = 16 << 20  # KVD_STATIC_WORKSPACE_BYTES
 
@@ -70,6 +70,9 @@ def _declare(lib):
         getattr(lib, name).argtypes = dec
     lib.kvd_decode_attention_static.argtypes = [P, P, P, P, I, I, I, I, I, I, F, I, P, I, P, P, P]
     lib.kvd_decode_attention_static.restype = I
+    # append arguments (k_cache, v_cache, k_new, v_new, pos), then q, seq_lens and the rest
+    lib.kvd_decode_step.argtypes = [P, P, P, P, P, P, P] + dec[4:]
+    lib.kvd_decode_step.restype = I
     lib.kvd_schedule_describe.argtypes = [P, I, I, I, I, I, I, I, I, P, I, PI, PI]
     lib.kvd_kernel_info.argtypes = [I, I, I, I, PI, PI, PI, PI, PI, PI]
     lib.kvd_status_string.argtypes = [I]
@@ -260,6 +263,23 @@ def decode_attention_static(q, k_cache, v_cache, seq_lens, max_seq_len: int, sca
                      status, stream)
     args = a[:12] + a[14:]  # drop workspace pointer and size
     _check(load().kvd_decode_attention_static(*args), "kvd_decode_attention_static")
+
+
+def decode_step(q, k_cache, v_cache, k_new, v_new, pos, seq_lens, max_seq_len: int, scale: float,
+                out, workspace=None, n_split: int = 0, lse=None, status=None, stream=None):
+    """kv_append(k_cache, v_cache, k_new, v_new, pos) then decode_attention(...), as one
+    call whose attention launch starts while the append runs (kvd_decode_step)."""
+    import torch
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _require(t, n, torch.bfloat16, 3)
+    _require(pos, "pos", torch.int32, 1)
+    B, S, Hkv, D = k_cache.shape
+    if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or pos.shape != (B,):
+        raise ValueError("decode_step: inconsistent shapes")
+    a = _decode_args(q, k_cache, v_cache, seq_lens, max_seq_len, scale, n_split, workspace, out,
+                     lse, status, stream)
+    args = [a[1], a[2], k_new.data_ptr(), v_new.data_ptr(), pos.data_ptr(), a[0], a[3]] + a[4:]
+    _check(load().kvd_decode_step(*args), "kvd_decode_step")
 
 
 def split_kv_chunk(q, k_cache, v_cache, seq_lens, max_seq_len: int, scale: float, out,

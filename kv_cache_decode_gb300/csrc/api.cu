@@ -107,10 +107,30 @@ kvd_status plan(int batch, int Hq, int Hkv, int D, int max_len, int num_sms, int
 
 enum Phase { kBoth = 3, kChunk = 1, kMerge = 2 };
 
+// The KV append launched ahead of the attention by kvd_decode_step.
+struct AppendArgs {
+    void* k_cache;
+    void* v_cache;
+    const void* k_new;
+    const void* v_new;
+    const int32_t* pos;
+};
+
+kvd_status check_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                        const int32_t* pos, int batch, int s_max, int Hkv, int D, const int32_t* status) {
+    if (batch < 0 || s_max < 0 || Hkv <= 0 || D <= 0 || D % 8 != 0) return KVD_ERR_INVALID_ARG;
+    if (!k_cache || !v_cache || !k_new || !v_new || !pos) return KVD_ERR_INVALID_ARG;
+    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_new, 16) || !aligned(v_new, 16) ||
+        !aligned(pos, 4) || (status && !aligned(status, 4)))
+        return KVD_ERR_INVALID_ARG;
+    return KVD_OK;
+}
+
 kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_cache,
                   const int32_t* seq_lens, int batch, int s_max, int max_seq_len, int Hq, int Hkv,
                   int D, float scale, int n_split_req, void* workspace, size_t workspace_bytes,
-                  void* out, kvd_out_dtype dt, float* lse, int32_t* status, kvd_stream_t stream) {
+                  void* out, kvd_out_dtype dt, float* lse, int32_t* status, kvd_stream_t stream,
+                  const AppendArgs* app = nullptr) {
     kvd_status st = check_shape(batch, Hq, Hkv, D, dt);
     if (st != KVD_OK) return st;
     if (s_max <= 0 || max_seq_len < 0 || max_seq_len > s_max) return KVD_ERR_INVALID_ARG;
@@ -165,6 +185,15 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
+    if (app) {
+        // The append, then the chunk kernel in early mode: it starts (and works
+        // out its schedule) while the append runs, and only its cache loads
+        // wait for the append's grid.
+        if (launch_append(app->k_cache, app->v_cache, app->k_new, app->v_new, app->pos, batch, s_max, Hkv, D,
+                          status, s) != cudaSuccess)
+            return KVD_ERR_CUDA;
+        p.early = 1;
+    }
     if (phase & kChunk) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVD_ERR_CUDA;
@@ -203,12 +232,9 @@ kvd_status kvd_decode_plan(int batch, int n_heads_q, int n_heads_kv, int head_di
 kvd_status kvd_kv_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                          const int32_t* pos, int batch, int s_max, int n_heads_kv, int head_dim,
                          int32_t* status_word, kvd_stream_t stream) {
-    if (batch < 0 || s_max < 0 || n_heads_kv <= 0 || head_dim <= 0 || head_dim % 8 != 0)
-        return KVD_ERR_INVALID_ARG;
-    if (!k_cache || !v_cache || !k_new || !v_new || !pos) return KVD_ERR_INVALID_ARG;
-    if (!aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(k_new, 16) ||
-        !aligned(v_new, 16) || !aligned(pos, 4) || (status_word && !aligned(status_word, 4)))
-        return KVD_ERR_INVALID_ARG;
+    const kvd_status st = check_append(k_cache, v_cache, k_new, v_new, pos, batch, s_max, n_heads_kv,
+                                       head_dim, status_word);
+    if (st != KVD_OK) return st;
     if (batch == 0) return KVD_OK;
     return launch_append(k_cache, v_cache, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim,
                          status_word, static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -225,6 +251,21 @@ kvd_status kvd_decode_attention(const void* q, const void* k_cache, const void* 
     return decode(kBoth, q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q,
                   n_heads_kv, head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype,
                   lse_out, status_word, stream);
+}
+
+kvd_status kvd_decode_step(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                           const int32_t* pos, const void* q, const int32_t* seq_lens, int batch,
+                           int s_max, int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim,
+                           float scale, int n_split, void* workspace, size_t workspace_bytes,
+                           void* out, kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                           kvd_stream_t stream) {
+    const kvd_status st = check_append(k_cache, v_cache, k_new, v_new, pos, batch, s_max, n_heads_kv,
+                                       head_dim, status_word);
+    if (st != KVD_OK) return st;
+    const AppendArgs app{k_cache, v_cache, k_new, v_new, pos};
+    return decode(kBoth, q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q,
+                  n_heads_kv, head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype,
+                  lse_out, status_word, stream, &app);
 }
 
 kvd_status kvd_split_kv_chunk(const void* q, const void* k_cache, const void* v_cache,

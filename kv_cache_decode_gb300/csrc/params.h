@@ -16,6 +16,11 @@ struct DecodeParams {
     float scale_log2;     // scale * log2(e): scores are kept in base-2 units
     int n_split;          // CTAs launched for the chunk kernel
     int tile_tokens, seg_unit, seg_cost;  // its schedule geometry (see schedule.cuh)
+    // 1 when the launch directly follows this library's KV append on the stream
+    // (kvd_decode_step): every input except the appended cache rows was then
+    // complete when the launch began, so only the cache loads wait for the
+    // preceding grid.
+    int early;
     void* out;            // bf16 or fp32 [B, Hq, D]
     float* lse;           // optional fp32 [B, Hq]
     int32_t* status;      // optional

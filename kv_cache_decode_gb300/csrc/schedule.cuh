@@ -71,13 +71,22 @@ KVD_HD int effective_ctas(int n_split, long long total) {
     return (long long)n_split < total ? n_split : (int)total;
 }
 
+// a / b for a >= 0, b > 0, with 32-bit arithmetic when both fit (a 64-bit
+// division is a long software sequence on the GPU, and these sit on the
+// kernels' start-up path).
+KVD_HD long long div_nonneg(long long a, long long b) {
+    if (((unsigned long long)a | (unsigned long long)b) < (1ull << 32))
+        return (long long)((unsigned)a / (unsigned)b);
+    return a / b;
+}
+
 KVD_HD long long run_begin(int c, int C_eff, long long total) {
-    return (long long)c * total / C_eff;
+    return div_nonneg((long long)c * total, C_eff);
 }
 
 // The CTA whose run [run_begin(c), run_begin(c + 1)) contains position t < total.
 KVD_HD int cta_of_token(long long t, int C_eff, long long total) {
-    return (int)(((t + 1) * (long long)C_eff - 1) / total);
+    return (int)div_nonneg((t + 1) * (long long)C_eff - 1, total);
 }
 
 struct Tile {
@@ -122,7 +131,7 @@ struct Walker {
         pstart = cum0;
         L = (b < B) ? len(b) : 0;
         if (b < B && L > 0 && pstart < S) {
-            h = (int)((S - pstart) / ext());
+            h = (int)div_nonneg(S - pstart, ext());
             pstart += (long long)h * ext();
         }
         pos = S;

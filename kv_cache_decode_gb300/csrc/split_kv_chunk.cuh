@@ -99,6 +99,30 @@ __device__ __forceinline__ int block_min_int(int v, int* sh) {
     return m;
 }
 
+// Block-wide minimum of an (int, long long) pair, each taken independently.
+template <int NW>
+__device__ __forceinline__ void block_min_int_ll(int& vi, long long& vl, int* shi, long long* shl) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        vi = min(vi, __shfl_xor_sync(0xffffffffu, vi, off));
+        vl = min(vl, __shfl_xor_sync(0xffffffffu, vl, off));
+    }
+    if (lane == 0) {
+        shi[warp] = vi;
+        shl[warp] = vl;
+    }
+    __syncthreads();
+    vi = shi[0];
+    vl = shl[0];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) {
+        vi = min(vi, shi[w]);
+        vl = min(vl, shl[w]);
+    }
+    __syncthreads();
+}
+
 template <int D, int HT, int TS, int TT, int STAGES>
 struct ChunkShape {
     static constexpr int NW = HT * TS;
@@ -143,8 +167,9 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
     const int c = blockIdx.x;
     const int G = p.G;
 
-    // Inputs may be produced by the previous kernel on the stream (the append).
-    pdl_wait();
+    // Inputs may be produced by the previous kernel on the stream. After this
+    // library's append (p.early), only the cache loads need to wait for it.
+    if (!p.early) pdl_wait();
     pdl_launch_dependents();
 
     const DevLen len{p.seq_lens, p.len_cap};
@@ -162,7 +187,10 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
     if (clamped && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
     const long long total = block_sum_ll<NW>(mine, s_red) * p.Hkv;
     const int C_eff = effective_ctas(p.n_split, total);
-    if (c >= C_eff) return;
+    if (c >= C_eff) {
+        if (p.early) pdl_wait();  // no CTA finishes before the preceding grid
+        return;
+    }
     const long long S = run_begin(c, C_eff, total);
 
     // ---- first sequence touching the run ----
@@ -250,6 +278,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
     const float scale_log2 = p.scale_log2;
 
     // ---- prologue ----
+    if (p.early) pdl_wait();  // the appended rows
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
         Tile t;

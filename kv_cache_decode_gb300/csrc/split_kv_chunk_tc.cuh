@@ -183,45 +183,80 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     tc::fence_proxy_async_smem();
     if (warp == 1) tc::tmem_alloc(smem_u32(tmem_slot), Sh::TMEM_COLS);
 
-    // Inputs may be produced by the previous kernel on the stream (the append).
-    pdl_wait();
+    // Inputs may be produced by the previous kernel on the stream. After this
+    // library's append (p.early), only the cache loads need to wait for it.
+    if (!p.early) pdl_wait();
     pdl_launch_dependents();
 
     const DevLen len{p.seq_lens, p.len_cap};
     using Geo = FixedGeom<T, Sh::SEG_UNIT, SEG_COST>;
     // ---- total work, this CTA's run, first sequence (as in the mma.sync kernel) ----
-    long long mine = 0;
-    bool clamped = false;
-    for (int b = tid; b < p.B; b += Sh::THREADS) {
-        const int raw = __ldg(p.seq_lens + b);
-        const int L = clamp_len(raw, p.len_cap);
-        clamped |= (raw != L);
-        mine += pair_extent(L, Geo{});
-    }
-    if (clamped && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
-    const long long total = block_sum_ll<NW>(mine, s_red) * p.Hkv;  // also orders the set-up
-    const int C_eff = effective_ctas(p.n_split, total);
-    const bool has_work = c < C_eff;
-    const long long S = has_work ? run_begin(c, C_eff, total) : total;
-    int b0 = p.B;
-    long long cum0 = total;
-    for (long long base = 0, chunk = 0; has_work && chunk < p.B; chunk += Sh::THREADS) {
-        const int b = (int)chunk + tid;
-        const int L = (b < p.B) ? len(b) : 0;
+    long long total;
+    int C_eff, b0 = p.B;
+    bool has_work;
+    long long S, cum0;
+    if (p.B <= Sh::THREADS) {
+        // One pass (the common case), one sequence per thread: an inclusive
+        // scan gives both the total and each sequence's start; the first
+        // sequence touching the run is the first candidate, and its start is
+        // the smallest candidate start (starts never decrease with b).
+        const int b = tid;
+        int L = 0;
+        if (b < p.B) {
+            const int raw = __ldg(p.seq_lens + b);
+            L = clamp_len(raw, p.len_cap);
+            if (raw != L && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
+        }
         const long long e = pair_extent(L, Geo{});
         const long long v = e * p.Hkv;
-        long long ctot;
-        const long long cs = base + block_incl_scan_ll<NW>(v, s_red, &ctot) - v;
-        const bool cand = (b < p.B) && is_first_seq_candidate(cs, e, p.Hkv, S);
-        const int bmin = block_min_int<NW>(cand ? b : 0x7fffffff, s_redi);
-        if (bmin != 0x7fffffff) {
-            if (b == bmin) s_cum0 = cs;
-            __syncthreads();
-            b0 = bmin;
-            cum0 = s_cum0;
-            break;
+        const long long cs = block_incl_scan_ll<NW>(v, s_red, &total) - v;  // also orders the set-up
+        C_eff = effective_ctas(p.n_split, total);
+        has_work = c < C_eff;
+        S = has_work ? run_begin(c, C_eff, total) : total;
+        cum0 = total;
+        if (has_work) {
+            const bool cand = (b < p.B) && is_first_seq_candidate(cs, e, p.Hkv, S);
+            int bi = cand ? b : 0x7fffffff;
+            long long ci = cand ? cs : 0x7fffffffffffffffLL;
+            block_min_int_ll<NW>(bi, ci, s_redi, s_red);
+            if (bi != 0x7fffffff) {
+                b0 = bi;
+                cum0 = ci;
+            }
         }
-        base += ctot;
+    } else {
+        long long mine = 0;
+        bool clamped = false;
+        for (int b = tid; b < p.B; b += Sh::THREADS) {
+            const int raw = __ldg(p.seq_lens + b);
+            const int L = clamp_len(raw, p.len_cap);
+            clamped |= (raw != L);
+            mine += pair_extent(L, Geo{});
+        }
+        if (clamped && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
+        total = block_sum_ll<NW>(mine, s_red) * p.Hkv;  // also orders the set-up
+        C_eff = effective_ctas(p.n_split, total);
+        has_work = c < C_eff;
+        S = has_work ? run_begin(c, C_eff, total) : total;
+        cum0 = total;
+        for (long long base = 0, chunk = 0; has_work && chunk < p.B; chunk += Sh::THREADS) {
+            const int b = (int)chunk + tid;
+            const int L = (b < p.B) ? len(b) : 0;
+            const long long e = pair_extent(L, Geo{});
+            const long long v = e * p.Hkv;
+            long long ctot;
+            const long long cs = base + block_incl_scan_ll<NW>(v, s_red, &ctot) - v;
+            const bool cand = (b < p.B) && is_first_seq_candidate(cs, e, p.Hkv, S);
+            const int bmin = block_min_int<NW>(cand ? b : 0x7fffffff, s_redi);
+            if (bmin != 0x7fffffff) {
+                if (b == bmin) s_cum0 = cs;
+                __syncthreads();
+                b0 = bmin;
+                cum0 = s_cum0;
+                break;
+            }
+            base += ctot;
+        }
     }
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
@@ -241,6 +276,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             int j = 0, qn = 0;
             const int NS = is_k ? KST : VST;
             const CUtensorMap* map = is_k ? &maps.k : &maps.v;
+            if (p.early) pdl_wait();  // the appended rows
             while (walker.next(t, NoOp{})) {
                 if (is_k && t.seg_start) {
                     const int qs = qn % NQ;
@@ -610,6 +646,8 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     }
 
     __syncthreads();
+    // No CTA finishes before the preceding grid (CTAs without loads included).
+    if (p.early && tid == 0) pdl_wait();
     if (*abort_flag && tid == 0 && p.status) atomicOr(p.status, KVD_STATUS_TIMEOUT);
     if (warp == 1) {
         tc::fence_after_sync();

@@ -147,3 +147,35 @@ def test_append_rejects(lib, args, expect):
 
 def test_decode_batch_zero_is_noop(lib):
     assert lib.kvd_decode_attention(*_dec_args(B=0, n_split=3, ws=None)) == kvd.OK
+
+
+def _step_args(kn=FAKE, vn=FAKE, pos=FAKE, **over):
+    a = _dec_args(**over)
+    # (k_cache, v_cache, k_new, v_new, pos, q, seq_lens) + the rest of kvd_decode_attention's
+    return [a[1], a[2], kn, vn, pos, a[0], a[3]] + a[4:]
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(q=None), kvd.ERR_INVALID_ARG),
+    (dict(k=None), kvd.ERR_INVALID_ARG),
+    (dict(lens=None), kvd.ERR_INVALID_ARG),
+    (dict(out=FAKE + 4), kvd.ERR_INVALID_ARG),
+    (dict(B=-1), kvd.ERR_INVALID_ARG),
+    (dict(S=0), kvd.ERR_INVALID_ARG),
+    (dict(maxlen=65), kvd.ERR_INVALID_ARG),
+    (dict(Hq=7), kvd.ERR_INVALID_ARG),
+    (dict(Hq=130, Hkv=2), kvd.ERR_UNSUPPORTED),
+    (dict(scale=float("nan")), kvd.ERR_INVALID_ARG),
+    (dict(ws_bytes=16), kvd.ERR_WORKSPACE_TOO_SMALL),
+    (dict(kn=None), kvd.ERR_INVALID_ARG),
+    (dict(vn=FAKE + 8), kvd.ERR_INVALID_ARG),
+    (dict(pos=FAKE + 2), kvd.ERR_INVALID_ARG),
+    (dict(pos=None), kvd.ERR_INVALID_ARG),
+])
+def test_decode_step_rejects(lib, over, expect):
+    # Nothing is launched when either half's arguments are rejected (fake pointers).
+    assert lib.kvd_decode_step(*_step_args(**over)) == expect
+
+
+def test_decode_step_batch_zero_is_noop(lib):
+    assert lib.kvd_decode_step(*_step_args(B=0, n_split=3, ws=None)) == kvd.OK
