@@ -193,6 +193,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
                           status, s) != cudaSuccess)
             return KVD_ERR_CUDA;
         p.early = 1;
+        p.pos = app->pos;
     }
     if (phase & kChunk) {
         int dev = 0;

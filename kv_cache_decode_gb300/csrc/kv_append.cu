@@ -26,16 +26,15 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_ca
         const long long row = r / vec_per_row;  // b * Hkv + h
         const int ch = (int)(r - row * vec_per_row);
         const int b = (int)(row / Hkv), h = (int)(row - (long long)b * Hkv);
+        // Both loads are issued before either is used: one memory round trip.
+        const uint4 val = __ldg((which == 0 ? k_new : v_new) + r);
         const int t = __ldg(pos + b);
         if (t < 0 || t >= S_max) {
             if (status && which == 0 && h == 0 && ch == 0) atomicOr(status, KVD_STATUS_POS_OUT_OF_RANGE);
             continue;
         }
         const long long dst = (((long long)b * S_max + t) * Hkv + h) * vec_per_row + ch;
-        if (which == 0)
-            k_cache[dst] = __ldg(k_new + r);
-        else
-            v_cache[dst] = __ldg(v_new + r);
+        (which == 0 ? k_cache : v_cache)[dst] = val;
     }
 }
 

@@ -21,6 +21,7 @@ struct DecodeParams {
     // complete when the launch began, so only the cache loads wait for the
     // preceding grid.
     int early;
+    const int32_t* pos;   // early mode: where the append put each sequence's new row
     void* out;            // bf16 or fp32 [B, Hq, D]
     float* lse;           // optional fp32 [B, Hq]
     int32_t* status;      // optional

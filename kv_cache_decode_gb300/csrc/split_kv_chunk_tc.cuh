@@ -20,9 +20,9 @@
 // rescaling O in TMEM is rare; the result is identical in exact arithmetic
 // because O and l always share the same m.
 //
-// Warp roles (13 warps): 0 = TMA producer for K (and Q at each new pair),
-// 2 = TMA producer for V, 1 and 11 = S issuers (one thread each, one half of
-// head_dim each; warp 1 also owns TMEM), 12 = O issuer, 3..10 = softmax /
+// Warp roles (14 warps): 0 = TMA producer for K, 2 = TMA producer for V,
+// 13 = TMA loader for Q at each new pair, 1 and 11 = S issuers (one thread
+// each, one half of head_dim each; warp 1 also owns TMEM), 12 = O issuer, 3..10 = softmax /
 // rescale / epilogue (two warps per TMEM lane quarter w % 4, splitting the
 // token columns of S and the output columns of O).
 // Pipelines: K ring of KST stages, V ring of VST stages, two S buffers in
@@ -85,8 +85,8 @@ struct TcShape {
     static constexpr int TMEM_S2 = 2 * T;        // S, second half: columns 2T and 3T
     static constexpr int TMEM_O = 4 * T;         // O at columns [4T, 4T + D)
     static constexpr int TMEM_COLS = (4 * T + D) <= 256 ? 256 : 512;
-    // producers 0 and 2, S issuers 1 and 11, O issuer 12, softmax 3..10
-    static constexpr int NWARPS = 13;
+    // producers 0 (K) and 2 (V), S issuers 1 and 11, O issuer 12, Q loader 13, softmax 3..10
+    static constexpr int NWARPS = 14;
     static constexpr int THREADS = NWARPS * 32;
     static_assert(KST >= 2, "need at least two K stages");
     static_assert(SMEM_BYTES + STATIC_SMEM <= 227 * 1024, "shared memory budget");
@@ -271,23 +271,30 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
         if (lane == 0) {
             const bool is_k = (warp == 0);
             const uint64_t pol_kv = l2_evict_first_policy();
-            const uint64_t pol_q = tc::l2_evict_last_policy();
             Tile t;
-            int j = 0, qn = 0;
+            int j = 0;
             const int NS = is_k ? KST : VST;
             const CUtensorMap* map = is_k ? &maps.k : &maps.v;
-            if (p.early) pdl_wait();  // the appended rows
+            // Early mode: only the tile holding a pair's appended row waits for
+            // the append's grid; tiles before it stream meanwhile. pos is an input
+            // (complete at launch), read once per pair until the first wait.
+            bool waited = !p.early;
+            int pos_pair = -1, pos_b = -1;
+            if (!waited && walker.b < p.B) {  // issued now, first used at the first tile
+                pos_pair = walker.b * p.Hkv + walker.h;
+                pos_b = __ldg(p.pos + walker.b);
+            }
             while (walker.next(t, NoOp{})) {
-                if (is_k && t.seg_start) {
-                    const int qs = qn % NQ;
-                    if (!tc::mbar_wait(q_empty(qs), ((qn / NQ) & 1) ^ 1, abort_flag, kBudget)) break;
-                    tc::mbar_arrive_expect_tx(q_full(qs), (uint32_t)(KB * 128 * G));
-                    const int qrow = t.b * p.Hq + t.h * G;
-#pragma unroll
-                    for (int kb = 0; kb < KB; ++kb)
-                        tc::tma_load_2d(sQ + qs * Sh::QS_BYTES + kb * Sh::QB_BYTES, &maps.q, kb * 64, qrow,
-                                        q_full(qs), pol_q);
-                    ++qn;
+                if (!waited) {
+                    const int pair = t.b * p.Hkv + t.h;
+                    if (pair != pos_pair) {
+                        pos_pair = pair;
+                        pos_b = __ldg(p.pos + t.b);
+                    }
+                    if (pos_b >= t.tok_lo && pos_b < t.tok_hi) {
+                        pdl_wait();
+                        waited = true;
+                    }
                 }
                 const int s = j % NS;
                 const uint32_t full = is_k ? k_full(s) : v_full(s);
@@ -306,7 +313,37 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                 const int s = jj % NS;
                 tc::mbar_wait(is_k ? k_full(s) : v_full(s), (jj / NS) & 1, abort_flag, kBudget / 4);
             }
-            if (is_k && qn > 0) tc::mbar_wait(q_full((qn - 1) % NQ), ((qn - 1) / NQ) & 1, abort_flag, kBudget / 4);
+        }
+    } else if (warp == 13) {
+        // ===================== Q loader =====================
+        // Its own thread, so that waiting for the Q slot (free once the previous
+        // pair's last S is done) never holds up the K stream. When the run goes
+        // on into a next pair, that pair's Q rows are also prefetched into L2,
+        // so its load is short when its turn comes.
+        if (lane == 0) {
+            const uint64_t pol_q = tc::l2_evict_last_policy();
+            Tile t;
+            int qn = 0;
+            while (walker.next(t, NoOp{})) {
+                if (!t.seg_start) continue;
+                const int qs = qn % NQ;
+                if (!tc::mbar_wait(q_empty(qs), ((qn / NQ) & 1) ^ 1, abort_flag, kBudget)) break;
+                tc::mbar_arrive_expect_tx(q_full(qs), (uint32_t)(KB * 128 * G));
+                const int qrow = t.b * p.Hq + t.h * G;
+#pragma unroll
+                for (int kb = 0; kb < KB; ++kb)
+                    tc::tma_load_2d(sQ + qs * Sh::QS_BYTES + kb * Sh::QB_BYTES, &maps.q, kb * 64, qrow, q_full(qs),
+                                    pol_q);
+                ++qn;
+                if (walker.pstart + walker.ext() < walker.E) {
+                    const int nh = (t.h + 1 < p.Hkv) ? t.h + 1 : 0;
+                    const int nb = (t.h + 1 < p.Hkv) ? t.b : t.b + 1;
+                    if (nb < p.B)
+                        tc::prefetch_l2(reinterpret_cast<const uint8_t*>(p.q) + ((size_t)nb * p.Hq + (size_t)nh * G) * D * 2,
+                                        (uint32_t)(G * D * 2));
+                }
+            }
+            if (qn > 0) tc::mbar_wait(q_full((qn - 1) % NQ), ((qn - 1) / NQ) & 1, abort_flag, kBudget / 4);
         }
     } else if (warp == 1 || warp == 11) {
         // ===================== S issuers (one thread each) =====================
