@@ -23,6 +23,13 @@ Functions and the passages they follow (page title, section):
 * ``kv_append``: byte copy of the new token's key/value rows into the cache.
   All About Transformer Inference, "Transformer inference basics" (Generation)
   and "Implementation: JetStream" (generate).
+* ``paged_gather``, ``kv_append_paged``, ``decode_attention_paged``: the same
+  over a paged cache (a pool of pages of P tokens and a block table: token t
+  of sequence b is row t mod P of page table[b, t // P]). All About
+  Transformer Inference, "Tricks for improving generation throughput and
+  latency", the ragged HBM reads and Paged Attention bullet; the layout is
+  this library's reading (the pages give none). Attention over a paged cache
+  is attention over the gathered contiguous cache.
 
 Pins (tests/test_oracle_pins.py): closed forms (identical keys give the mean of
 V; a dominant score returns that V row; one token returns it exactly), the
@@ -83,6 +90,10 @@ def _declare(lib):
     lib.kvo_attention_weights.restype = I
     lib.kvo_kv_append.argtypes = [P, P, P, P, P, I, I, I, I]
     lib.kvo_kv_append.restype = I
+    lib.kvo_paged_gather.argtypes = [P, P, P, I, I, I, I, I, I, P]
+    lib.kvo_paged_gather.restype = I
+    lib.kvo_kv_append_paged.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
+    lib.kvo_kv_append_paged.restype = I
     lib.kvo_max_threads.argtypes = []
     lib.kvo_max_threads.restype = I
     return lib
@@ -175,6 +186,60 @@ def kv_append(k_cache, v_cache, k_new, v_new, pos, lib=None):
     if rc < 0:
         raise ValueError(f"oracle kv_append failed ({rc})")
     return kc, vc, rc
+
+
+def paged_gather(pages, block_table, seq_lens, lib=None):
+    """Contiguous cache [B, max_blocks * P, Hkv, D] from a pool [num_pages, P, Hkv, D].
+
+    Rows t < seq_lens[b] come from row t % P of page block_table[b, t // P]
+    (zero rows where that entry is not a page of the pool); the other rows are
+    bf16 NaN. Returns (cache, number of tokens that read zero rows).
+    """
+    lib = lib or _load()
+    pages, pp = _u16(pages)
+    num_pages, P, Hkv, D = pages.shape
+    block_table, tp = _i32(block_table)
+    B, max_blocks = block_table.shape
+    seq_lens, lp = _i32(seq_lens)
+    out = np.full((B, max_blocks * P, Hkv, D), 0x7FC0, dtype=np.uint16)
+    rc = lib.kvo_paged_gather(pp, tp, lp, B, max_blocks, P, num_pages, Hkv, D,
+                              out.ctypes.data_as(ctypes.c_void_p))
+    if rc < 0:
+        raise ValueError(f"oracle paged_gather failed ({rc})")
+    return out, rc
+
+
+def kv_append_paged(k_pages, v_pages, k_new, v_new, block_table, pos, lib=None):
+    """Copies of the page pools with each sequence's new row written at pos[b].
+
+    Returns (k_pages', v_pages', n_skipped, n_bad_page): sequences whose pos
+    lies outside [0, max_blocks * P) or whose block-table entry is not a page
+    of the pool are left out (the latter also counted in n_bad_page).
+    """
+    lib = lib or _load()
+    kp = np.array(k_pages, dtype=np.uint16, copy=True, order="C")
+    vp = np.array(v_pages, dtype=np.uint16, copy=True, order="C")
+    num_pages, P, Hkv, D = kp.shape
+    block_table, tp = _i32(block_table)
+    B, max_blocks = block_table.shape
+    k_new, knp = _u16(k_new)
+    v_new, vnp = _u16(v_new)
+    pos, pp = _i32(pos)
+    bad = ctypes.c_int(0)
+    rc = lib.kvo_kv_append_paged(kp.ctypes.data_as(ctypes.c_void_p), vp.ctypes.data_as(ctypes.c_void_p),
+                                 knp, vnp, tp, pp, B, max_blocks, P, num_pages, Hkv, D,
+                                 ctypes.byref(bad))
+    if rc < 0:
+        raise ValueError(f"oracle kv_append_paged failed ({rc})")
+    return kp, vp, rc, bad.value
+
+
+def decode_attention_paged(q, k_pages, v_pages, block_table, seq_lens, scale, n_threads: int = 0,
+                           lib=None):
+    """decode_attention over the caches gathered from the page pools."""
+    kc, _ = paged_gather(k_pages, block_table, seq_lens, lib=lib)
+    vc, _ = paged_gather(v_pages, block_table, seq_lens, lib=lib)
+    return decode_attention(q, kc, vc, seq_lens, scale, n_threads=n_threads, lib=lib)
 
 
 def max_threads(lib=None) -> int:

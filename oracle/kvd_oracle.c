@@ -40,6 +40,16 @@
  *    unnormalised outputs o_j = sum exp(s - m_j) v, the result is
  *    sum_j exp(m_j - M) o_j / sum_j exp(m_j - M) l_j with M = max_j m_j, and
  *    empty chunks skipped.
+ *  - Paged cache: the cache is kept in an operating-system-style page table,
+ *    so a sequence only holds the pages it uses (All About Transformer
+ *    Inference, "Tricks for improving generation throughput and latency", the
+ *    ragged HBM reads and Paged Attention bullet). The pages give no layout;
+ *    the one used is: pages of P tokens, each laid out like a cache of
+ *    capacity P ([P, K, H]), and a block table whose entry (b, j) names the
+ *    page that holds tokens [j P, (j + 1) P) of sequence b, so token t sits in
+ *    row t mod P of page table[b][t / P]. A token whose entry is not a page
+ *    of the pool reads zero key and value rows (and an append to it is
+ *    skipped); both are counted.
  *
  * All functions return 0 on success and a negative value on bad arguments.
  */
@@ -247,6 +257,62 @@ int kvo_kv_append(uint16_t* k_cache, uint16_t* v_cache, const uint16_t* k_new,
             memcpy(v_cache + dst, v_new + src, sizeof(uint16_t) * (size_t)D);
         }
     }
+    return skipped;
+}
+
+/* Paged cache -> contiguous cache: out[b, t, h, :] = pages[table[b][t / P],
+ * t mod P, h, :] for t < seq_lens[b]; zero rows where table[b][t / P] is not
+ * in [0, num_pages); rows t >= seq_lens[b] are left as the caller filled them.
+ * out is [B, max_blocks * P, Hkv, D]. Returns the number of tokens that read
+ * zero rows (or a negative value on bad arguments). */
+int kvo_paged_gather(const uint16_t* pages, const int32_t* table, const int32_t* seq_lens,
+                     int B, int max_blocks, int P, int num_pages, int Hkv, int D, uint16_t* out)
+{
+    if (B < 0 || max_blocks < 0 || P <= 0 || num_pages < 0 || Hkv <= 0 || D <= 0) return -1;
+    const size_t row = (size_t)Hkv * (size_t)D;  /* elements per token */
+    const size_t S = (size_t)max_blocks * (size_t)P;
+    int zeroed = 0;
+    for (int b = 0; b < B; ++b) {
+        const int L = seq_lens[b];
+        if (L < 0 || (size_t)L > S) return -2;
+        for (int t = 0; t < L; ++t) {
+            const int page = table[(size_t)b * max_blocks + t / P];
+            uint16_t* dst = out + ((size_t)b * S + (size_t)t) * row;
+            if (page < 0 || page >= num_pages) {
+                memset(dst, 0, sizeof(uint16_t) * row);
+                ++zeroed;
+                continue;
+            }
+            const uint16_t* src = pages + ((size_t)page * (size_t)P + (size_t)(t % P)) * row;
+            memcpy(dst, src, sizeof(uint16_t) * row);
+        }
+    }
+    return zeroed;
+}
+
+/* Paged append: pages[table[b][pos[b] / P], pos[b] mod P, h, :] = new[b, h, :]
+ * for K and V. Sequences whose pos lies outside [0, max_blocks * P), or whose
+ * entry is not a page of the pool, are skipped; *bad_page counts the latter.
+ * Returns the number of skipped sequences. */
+int kvo_kv_append_paged(uint16_t* k_pages, uint16_t* v_pages, const uint16_t* k_new,
+                        const uint16_t* v_new, const int32_t* table, const int32_t* pos,
+                        int B, int max_blocks, int P, int num_pages, int Hkv, int D, int* bad_page)
+{
+    if (B < 0 || max_blocks < 0 || P <= 0 || num_pages < 0 || Hkv <= 0 || D <= 0) return -1;
+    int skipped = 0, bad = 0;
+    for (int b = 0; b < B; ++b) {
+        const int t = pos[b];
+        if (t < 0 || (long long)t >= (long long)max_blocks * P) { ++skipped; continue; }
+        const int page = table[(size_t)b * max_blocks + t / P];
+        if (page < 0 || page >= num_pages) { ++skipped; ++bad; continue; }
+        for (int h = 0; h < Hkv; ++h) {
+            const size_t dst = (((size_t)page * P + (size_t)(t % P)) * Hkv + h) * (size_t)D;
+            const size_t src = ((size_t)b * Hkv + h) * (size_t)D;
+            memcpy(k_pages + dst, k_new + src, sizeof(uint16_t) * (size_t)D);
+            memcpy(v_pages + dst, v_new + src, sizeof(uint16_t) * (size_t)D);
+        }
+    }
+    if (bad_page) *bad_page = bad;
     return skipped;
 }
 

@@ -276,6 +276,146 @@ def check_append_is_a_byte_copy(lib):
     assert np.array_equal(k2, ek) and np.array_equal(v2, ev)
 
 
+def _page_table(seed, B, S, P, lens, spare=3):
+    """A shuffled placement of each sequence's blocks in a pool of pages.
+
+    Block j of sequence b goes to page perm[b * nb + j]; entries past a
+    sequence's blocks are -1. Returns (table, num_pages).
+    """
+    r = np.random.default_rng(seed)
+    nb = S // P
+    num_pages = B * nb + spare
+    perm = r.permutation(num_pages)[:B * nb]
+    table = np.full((B, nb), -1, np.int32)
+    for b in range(B):
+        for j in range(-(-int(lens[b]) // P)):
+            table[b, j] = perm[b * nb + j]
+    return table, num_pages
+
+
+def _fill_pool(cache, table, num_pages, seed):
+    """Pages of random bits, then block j of sequence b copied in as one slice."""
+    B, S, Hkv, D = cache.shape
+    P = S // table.shape[1]
+    pool = np.random.default_rng(seed).integers(0, 2**16, (num_pages, P, Hkv, D), dtype=np.uint16)
+    for b in range(B):
+        for j in range(table.shape[1]):
+            if table[b, j] >= 0:
+                pool[table[b, j]] = cache[b, j * P:(j + 1) * P]
+    return pool
+
+
+def check_paged_identity_pool_is_the_cache(lib):
+    # A pool that is the contiguous cache reshaped page by page, with the
+    # table naming page b * nb + j for block j of sequence b.
+    r = np.random.default_rng(60)
+    B, S, Hkv, D, P = 3, 12, 2, 4, 4
+    cache = r.integers(0, 2**16, (B, S, Hkv, D), dtype=np.uint16)
+    pool = cache.reshape(B * S // P, P, Hkv, D)
+    table = np.arange(B * S // P, dtype=np.int32).reshape(B, S // P)
+    lens = np.array([12, 5, 0], np.int32)
+    got, zeroed = oracle.paged_gather(pool, table, lens, lib=lib)
+    assert zeroed == 0
+    for b in range(B):
+        assert np.array_equal(got[b, :lens[b]], cache[b, :lens[b]]), b
+
+
+def check_paged_shuffled_pool(lib):
+    B, S, Hkv, D, P = 4, 16, 2, 8, 4
+    lens = np.array([16, 1, 7, 9], np.int32)
+    table, num_pages = _page_table(61, B, S, P, lens)
+    r = np.random.default_rng(62)
+    kc = r.integers(0, 2**16, (B, S, Hkv, D), dtype=np.uint16)
+    got, zeroed = oracle.paged_gather(_fill_pool(kc, table, num_pages, 63), table, lens, lib=lib)
+    assert zeroed == 0
+    for b in range(B):
+        assert np.array_equal(got[b, :lens[b]], kc[b, :lens[b]]), b
+    # attention over the pools equals attention over the contiguous caches
+    q = _bits(r.standard_normal((B, 4, D)))
+    kc = _bits(r.standard_normal((B, S, Hkv, D)))
+    vc = _bits(r.standard_normal((B, S, Hkv, D)))
+    kpool, vpool = _fill_pool(kc, table, num_pages, 64), _fill_pool(vc, table, num_pages, 65)
+    direct, lse_d = oracle.decode_attention(q, kc, vc, lens, 0.25, lib=lib)
+    paged, lse_p = oracle.decode_attention_paged(q, kpool, vpool, table, lens, 0.25, lib=lib)
+    assert np.array_equal(direct, paged) and np.array_equal(lse_d, lse_p)
+
+
+def check_paged_tiny_hand_example(lib):
+    # P = 2, one sequence of 3 tokens: block 0 is page 2, block 1 is page 0, so
+    # tokens 0, 1 are rows 0, 1 of page 2 and token 2 is row 0 of page 0.
+    P = 2
+    kp = np.zeros((3, P, 1, 2), np.float32)
+    vp = np.zeros((3, P, 1, 2), np.float32)
+    kp[2, 0, 0], kp[2, 1, 0], kp[0, 0, 0] = [0, 0], [1, 0], [2, 0]
+    vp[2, 0, 0], vp[2, 1, 0], vp[0, 0, 0] = [1, 0], [0, 1], [1, 1]
+    kp[0, 1, 0] = kp[1, :, 0] = [9, 9]  # never attended
+    vp[0, 1, 0] = vp[1, :, 0] = [-5, 7]
+    table = np.array([[2, 0]], np.int32)
+    q = _bits(np.array([[[1.0, 0.0]]]))
+    out, lse = oracle.decode_attention_paged(q, _bits(kp), _bits(vp), table, np.array([3], np.int32),
+                                             1.0, lib=lib)
+    e = [math.exp(0.0), math.exp(1.0), math.exp(2.0)]
+    z = sum(e)
+    want = [(e[0] + e[2]) / z, (e[1] + e[2]) / z]
+    assert abs(out[0, 0, 0] - want[0]) < 1e-15 and abs(out[0, 0, 1] - want[1]) < 1e-15, out
+    assert abs(lse[0, 0] - math.log(z)) < 1e-15
+
+
+def check_paged_invalid_entry_reads_zero_rows(lib):
+    B, S, Hkv, D, P = 2, 12, 1, 4, 4
+    lens = np.array([10, 12], np.int32)
+    table, num_pages = _page_table(66, B, S, P, lens)
+    kc = np.random.default_rng(67).integers(0, 2**16, (B, S, Hkv, D), dtype=np.uint16)
+    kpool = _fill_pool(kc, table, num_pages, 68)
+    table[1, 1] = num_pages  # not a page of the pool: tokens 4..7 of sequence 1
+    table[0, 2] = -7         # tokens 8, 9 of sequence 0
+    got, zeroed = oracle.paged_gather(kpool, table, lens, lib=lib)
+    assert zeroed == 4 + 2
+    want = kc.copy()
+    want[1, 4:8] = 0
+    want[0, 8:10] = 0
+    for b in range(B):
+        assert np.array_equal(got[b, :lens[b]], want[b, :lens[b]]), b
+
+
+def check_paged_append(lib):
+    B, S, Hkv, D, P = 5, 16, 2, 4, 8
+    lens = np.array([16, 9, 8, 1, 16], np.int32)
+    table, num_pages = _page_table(69, B, S, P, lens)
+    r = np.random.default_rng(70)
+    kpool = r.integers(0, 2**16, (num_pages, P, Hkv, D), dtype=np.uint16)
+    vpool = r.integers(0, 2**16, (num_pages, P, Hkv, D), dtype=np.uint16)
+    kn = r.integers(0, 2**16, (B, Hkv, D), dtype=np.uint16)
+    vn = r.integers(0, 2**16, (B, Hkv, D), dtype=np.uint16)
+    table[4, 1] = -1                              # sequence 4's second block is unassigned
+    pos = np.array([15, 8, 7, 0, 9], np.int32)    # page ends and starts; sequence 4 hits -1
+    k2, v2, skipped, bad = oracle.kv_append_paged(kpool, vpool, kn, vn, table, pos, lib=lib)
+    assert skipped == 1 and bad == 1
+    # exactly the named rows changed
+    ek, ev = kpool.copy(), vpool.copy()
+    ek[table[0, 1], 7], ev[table[0, 1], 7] = kn[0], vn[0]
+    ek[table[1, 1], 0], ev[table[1, 1], 0] = kn[1], vn[1]
+    ek[table[2, 0], 7], ev[table[2, 0], 7] = kn[2], vn[2]
+    ek[table[3, 0], 0], ev[table[3, 0], 0] = kn[3], vn[3]
+    assert np.array_equal(k2, ek) and np.array_equal(v2, ev)
+    # pos outside [0, capacity) is skipped without a bad-page count
+    _, _, skipped, bad = oracle.kv_append_paged(kpool, vpool, kn, vn, table,
+                                                np.array([16, -1, 0, 0, 0], np.int32), lib=lib)
+    assert skipped == 2 and bad == 0
+    # an entry one past the pool's pages: skipped and counted (the arrays hold
+    # one page more than the pool size passed, so a wrong write stays in memory)
+    import ctypes
+    kx, vx = kpool.copy(), vpool.copy()
+    t2 = table.copy()
+    t2[0, 1] = num_pages - 1
+    badc = ctypes.c_int(0)
+    ptr = lambda a: a.ctypes.data_as(ctypes.c_void_p)
+    skipped = lib.kvo_kv_append_paged(ptr(kx), ptr(vx), ptr(kn), ptr(vn), ptr(t2), ptr(pos), B,
+                                      t2.shape[1], P, num_pages - 1, Hkv, D, ctypes.byref(badc))
+    assert skipped == 2 and badc.value == 2
+    assert np.array_equal(kx[num_pages - 1], kpool[num_pages - 1])
+
+
 ALL_CHECKS = [
     check_identical_keys_give_mean_of_v,
     check_dominant_score_returns_that_row,
@@ -289,4 +429,9 @@ ALL_CHECKS = [
     check_decimal_brute_force,
     check_cached_decode_equals_recompute,
     check_append_is_a_byte_copy,
+    check_paged_identity_pool_is_the_cache,
+    check_paged_shuffled_pool,
+    check_paged_tiny_hand_example,
+    check_paged_invalid_entry_reads_zero_rows,
+    check_paged_append,
 ]

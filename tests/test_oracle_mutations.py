@@ -34,6 +34,18 @@ MUTANTS = [
     ("lse_missing_max", "return mx + log(sum);", "return log(sum);"),
     ("append_wrong_row", "const size_t dst = (((size_t)b * S_max + (size_t)t) * Hkv + h) * (size_t)D;",
      "const size_t dst = (((size_t)b * S_max + (size_t)(t > 0 ? t - 1 : t)) * Hkv + h) * (size_t)D;"),
+    ("paged_block_and_row_swapped",
+     "const uint16_t* src = pages + ((size_t)page * (size_t)P + (size_t)(t % P)) * row;",
+     "const uint16_t* src = pages + ((size_t)page * (size_t)P + (size_t)(t / P) % P) * row;"),
+    ("paged_block_index_off_by_one", "const int page = table[(size_t)b * max_blocks + t / P];\n            uint16_t*",
+     "const int page = table[(size_t)b * max_blocks + (t + 1) / P];\n            uint16_t*"),
+    ("paged_invalid_entry_not_zeroed", "memset(dst, 0, sizeof(uint16_t) * row);", ""),
+    ("paged_invalid_entry_wraps", "if (page < 0 || page >= num_pages) {\n                memset",
+     "if (page < 0) {\n                memset"),
+    ("paged_append_wrong_row", "const size_t dst = (((size_t)page * P + (size_t)(t % P)) * Hkv + h) * (size_t)D;",
+     "const size_t dst = (((size_t)page * P + (size_t)((t + 1) % P)) * Hkv + h) * (size_t)D;"),
+    ("paged_append_ignores_bad_page", "if (page < 0 || page >= num_pages) { ++skipped; ++bad; continue; }",
+     "if (page < 0) { ++skipped; ++bad; continue; }"),
 ]
 
 

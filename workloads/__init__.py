@@ -234,3 +234,51 @@ def random_small(seed: int, B: int, Hq: int, Hkv: int, D: int, S_max: int,
     w = Workload(f"small{seed}", B, Hq, Hkv, D, S_max, 0, S_max, seed,
                  peaked_frac=peaked_frac)
     return step_inputs(w, lens=np.asarray(lens, dtype=np.int32))
+
+
+@dataclass
+class PagedStepInputs:
+    """One decode step over a paged cache (bf16 tensors as uint16 bit patterns).
+
+    ``k_pages``/``v_pages`` are pools of ``page_size``-token pages laid out like
+    a cache of that capacity; ``block_table[b, j]`` names the page holding
+    tokens ``[j * page_size, (j + 1) * page_size)`` of sequence b, or -1 where
+    the sequence has no such block. ``step`` holds the same step in contiguous
+    form (its q, new rows, pos and lengths apply unchanged).
+    """
+    step: StepInputs
+    page_size: int
+    k_pages: np.ndarray      # u16 [num_pages, page_size, Hkv, D]
+    v_pages: np.ndarray
+    block_table: np.ndarray  # i32 [B, max_blocks]
+
+
+def paged_step_inputs(inp: StepInputs, page_size: int, seed: int = 0, spare: int = 3,
+                      pad_bits: int = BF16_NAN) -> PagedStepInputs:
+    """Spread a step's cache over a shuffled pool of pages.
+
+    Each sequence gets the ceil(L_b / page_size) blocks its attended length
+    needs (the appended token's slot included), placed on pages drawn in a
+    random order from a pool with ``spare`` extra pages; unused pages and the
+    rows past each sequence's cached tokens hold ``pad_bits``. A layout only:
+    page j of sequence b receives rows [j * P, (j + 1) * P) of its cache.
+    """
+    P = int(page_size)
+    B, S, Hkv, D = inp.k_cache.shape
+    max_blocks = -(-S // P)
+    nblk = [-(-int(L) // P) for L in inp.seq_lens]
+    num_pages = sum(nblk) + spare
+    order = np.random.default_rng((seed, P, B)).permutation(num_pages)
+    kp = np.full((num_pages, P, Hkv, D), pad_bits, dtype=np.uint16)
+    vp = np.full((num_pages, P, Hkv, D), pad_bits, dtype=np.uint16)
+    table = np.full((B, max_blocks), -1, dtype=np.int32)
+    nxt = 0
+    for b in range(B):
+        for j in range(nblk[b]):
+            page = int(order[nxt])
+            nxt += 1
+            table[b, j] = page
+            rows = inp.k_cache[b, j * P:(j + 1) * P]
+            kp[page, :rows.shape[0]] = rows
+            vp[page, :rows.shape[0]] = inp.v_cache[b, j * P:(j + 1) * P]
+    return PagedStepInputs(inp, P, kp, vp, table)
