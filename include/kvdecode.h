@@ -59,6 +59,7 @@ typedef void* kvd_stream_t;
 #define KVD_STATUS_SEQ_LEN_CLAMPED 0x1  /* some seq_lens[b] outside [0, min(s_max, max_seq_len)] */
 #define KVD_STATUS_POS_OUT_OF_RANGE 0x2 /* some pos[b] outside [0, s_max): that row not written */
 #define KVD_STATUS_TIMEOUT 0x4          /* an internal pipeline wait gave up (~2 s): outputs invalid */
+#define KVD_STATUS_BAD_PAGE 0x8         /* paged cache: a needed block-table entry named no page of the pool */
 
 /* Supported shapes: head_dim in {64, 128, 256}; n_heads_q a multiple of
  * n_heads_kv with group size n_heads_q / n_heads_kv <= 64. */
@@ -172,6 +173,55 @@ kvd_status kvd_decode_step(void* k_cache, void* v_cache, const void* k_new, cons
                            float scale, int n_split, void* workspace, size_t workspace_bytes,
                            void* out, kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
                            kvd_stream_t stream);
+
+/*
+ * Paged KV cache. The pages describe keeping the KV cache in an
+ * operating-system-style page table, so that each sequence holds only the
+ * memory it uses instead of a padded maximum (All About Transformer Inference,
+ * "Tricks for improving generation throughput and latency", the ragged HBM
+ * reads and Paged Attention bullet). They give no layout; this library's is:
+ *   k_pages, v_pages : bf16 [num_pages, page_size, n_heads_kv, head_dim], a pool
+ *                      of pages, each laid out like a cache of capacity
+ *                      page_size; 16-byte aligned. num_pages * page_size must
+ *                      be below 2^31.
+ *   block_table      : device int32 [batch, max_blocks], 4-byte aligned. Entry
+ *                      (b, j) names the page that holds tokens
+ *                      [j * page_size, (j + 1) * page_size) of sequence b, so
+ *                      token t of sequence b is row t % page_size of page
+ *                      block_table[b * max_blocks + t / page_size]. Only the
+ *                      entries of blocks holding tokens t < L_b (or pos[b])
+ *                      are read; others may hold anything.
+ *   page_size        : a power of two in [16, 4096]; the capacity of a
+ *                      sequence (s_max of the contiguous calls) is
+ *                      max_blocks * page_size.
+ * A needed entry outside [0, num_pages) is never dereferenced: attention
+ * reads zero key and value rows for that block's tokens, an append to it is
+ * skipped, and either sets KVD_STATUS_BAD_PAGE.
+ * Each paged call is the contiguous call with the cache replaced by the pool
+ * and the table; the other arguments, the results (bit for bit: the same
+ * kernels and schedule run, only the row addresses differ), the workspace
+ * (kvd_decode_plan with the same max_seq_len) and the errors are the same,
+ * plus KVD_ERR_INVALID_ARG for a bad page_size, max_blocks < 1 or
+ * num_pages < 1.
+ */
+kvd_status kvd_kv_append_paged(void* k_pages, void* v_pages, const void* k_new, const void* v_new,
+                               const int32_t* block_table, const int32_t* pos, int batch,
+                               int max_blocks, int page_size, int num_pages, int n_heads_kv,
+                               int head_dim, int32_t* status_word, kvd_stream_t stream);
+kvd_status kvd_decode_attention_paged(const void* q, const void* k_pages, const void* v_pages,
+                                      const int32_t* block_table, const int32_t* seq_lens,
+                                      int batch, int max_blocks, int page_size, int num_pages,
+                                      int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim,
+                                      float scale, int n_split, void* workspace,
+                                      size_t workspace_bytes, void* out, kvd_out_dtype out_dtype,
+                                      float* lse_out, int32_t* status_word, kvd_stream_t stream);
+kvd_status kvd_decode_step_paged(void* k_pages, void* v_pages, const void* k_new, const void* v_new,
+                                 const int32_t* pos, const void* q, const int32_t* block_table,
+                                 const int32_t* seq_lens, int batch, int max_blocks, int page_size,
+                                 int num_pages, int max_seq_len, int n_heads_q, int n_heads_kv,
+                                 int head_dim, float scale, int n_split, void* workspace,
+                                 size_t workspace_bytes, void* out, kvd_out_dtype out_dtype,
+                                 float* lse_out, int32_t* status_word, kvd_stream_t stream);
 
 /*
  * The two launches of kvd_decode_attention, exposed separately so that each

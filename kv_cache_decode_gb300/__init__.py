@@ -29,7 +29,8 @@ STATUS_POS_OUT_OF_RANGE = 0x2
 EXPORTED = (
     "kvd_decode_plan", "kvd_kv_append", "kvd_decode_attention", "kvd_split_kv_chunk",
     "kvd_split_kv_merge", "kvd_schedule_describe", "kvd_kernel_info", "kvd_status_string",
-    "kvd_version", "kvd_decode_attention_static", "kvd_decode_step",
+    "kvd_version", "kvd_decode_attention_static", "kvd_decode_step", "kvd_kv_append_paged",
+    "kvd_decode_attention_paged", "kvd_decode_step_paged",
 )
 STATIC_WORKSPACE_BYTES = 16 << 20  # KVD_STATIC_WORKSPACE_BYTES
 
@@ -73,6 +74,14 @@ def _declare(lib):
     # append arguments (k_cache, v_cache, k_new, v_new, pos), then q, seq_lens and the rest
     lib.kvd_decode_step.argtypes = [P, P, P, P, P, P, P] + dec[4:]
     lib.kvd_decode_step.restype = I
+    # paged: the cache becomes (pool, block_table) and s_max becomes (max_blocks, page_size, num_pages)
+    lib.kvd_kv_append_paged.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P, P]
+    lib.kvd_kv_append_paged.restype = I
+    dec_paged = [P, P, P, P, P, I, I, I, I] + dec[6:]
+    lib.kvd_decode_attention_paged.argtypes = dec_paged
+    lib.kvd_decode_attention_paged.restype = I
+    lib.kvd_decode_step_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I] + dec[6:]
+    lib.kvd_decode_step_paged.restype = I
     lib.kvd_schedule_describe.argtypes = [P, I, I, I, I, I, I, I, I, P, I, PI, PI]
     lib.kvd_kernel_info.argtypes = [I, I, I, I, PI, PI, PI, PI, PI, PI]
     lib.kvd_status_string.argtypes = [I]
@@ -263,6 +272,94 @@ def decode_attention_static(q, k_cache, v_cache, seq_lens, max_seq_len: int, sca
                      status, stream)
     args = a[:12] + a[14:]  # drop workspace pointer and size
     _check(load().kvd_decode_attention_static(*args), "kvd_decode_attention_static")
+
+
+def _paged_args(k_pages, v_pages, block_table, B, what):
+    import torch
+    _require(k_pages, "k_pages", torch.bfloat16, 4)
+    _require(v_pages, "v_pages", torch.bfloat16, 4)
+    _require(block_table, "block_table", torch.int32, 2)
+    num_pages, page, Hkv, D = k_pages.shape
+    if v_pages.shape != k_pages.shape or block_table.shape[0] != B:
+        raise ValueError(f"{what}: inconsistent shapes")
+    return block_table.shape[1], page, num_pages, Hkv, D
+
+
+def kv_append_paged(k_pages, v_pages, k_new, v_new, block_table, pos, status=None, stream=None):
+    """Paged kv_append: the new rows go to row pos[b] % page of page
+    block_table[b, pos[b] // page] of the pools [num_pages, page, Hkv, D]."""
+    import torch
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _require(t, n, torch.bfloat16, 3)
+    _require(pos, "pos", torch.int32, 1)
+    B = k_new.shape[0]
+    max_blocks, page, num_pages, Hkv, D = _paged_args(k_pages, v_pages, block_table, B, "kv_append_paged")
+    if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or pos.shape != (B,):
+        raise ValueError("kv_append_paged: inconsistent shapes")
+    _check(load().kvd_kv_append_paged(k_pages.data_ptr(), v_pages.data_ptr(), k_new.data_ptr(),
+                                      v_new.data_ptr(), block_table.data_ptr(), pos.data_ptr(), B,
+                                      max_blocks, page, num_pages, Hkv, D, _ptr(status),
+                                      _stream_handle(stream)), "kvd_kv_append_paged")
+
+
+def _decode_paged_args(q, k_pages, v_pages, block_table, seq_lens, max_seq_len, scale, n_split,
+                       workspace, out, lse, status, stream):
+    B = q.shape[0]
+    max_blocks, page, num_pages, _, _ = _paged_args(k_pages, v_pages, block_table, B, "decode_attention_paged")
+    import torch
+    _require(q, "q", torch.bfloat16, 3)
+    _require(seq_lens, "seq_lens", torch.int32, 1)
+    _require(out, "out", None, 3)
+    _, Hq, D = q.shape
+    Hkv = k_pages.shape[2]
+    if k_pages.shape[3] != D or seq_lens.shape != (B,) or out.shape != (B, Hq, D):
+        raise ValueError("decode_attention_paged: inconsistent shapes")
+    if out.dtype == torch.bfloat16:
+        code = OUT_BF16
+    elif out.dtype == torch.float32:
+        code = OUT_F32
+    else:
+        raise TypeError("out must be bfloat16 or float32")
+    if lse is not None:
+        _require(lse, "lse", torch.float32, 2)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(),
+                                                           workspace.numel() * workspace.element_size())
+    head = [B, max_blocks, page, num_pages]
+    tail = [int(max_seq_len), Hq, Hkv, D, float(scale), int(n_split), ws_ptr, ws_bytes, out.data_ptr(),
+            code, _ptr(lse), _ptr(status), _stream_handle(stream)]
+    return head, tail
+
+
+def decode_attention_paged(q, k_pages, v_pages, block_table, seq_lens, max_seq_len: int, scale: float,
+                           out, workspace=None, n_split: int = 0, lse=None, status=None, stream=None):
+    """decode_attention over a paged cache: pools [num_pages, page, Hkv, D] and
+    block_table [B, max_blocks] (token t of sequence b is row t % page of page
+    block_table[b, t // page]). Workspace as for decode_attention."""
+    head, tail = _decode_paged_args(q, k_pages, v_pages, block_table, seq_lens, max_seq_len, scale,
+                                    n_split, workspace, out, lse, status, stream)
+    _check(load().kvd_decode_attention_paged(q.data_ptr(), k_pages.data_ptr(), v_pages.data_ptr(),
+                                             block_table.data_ptr(), seq_lens.data_ptr(), *head, *tail),
+           "kvd_decode_attention_paged")
+
+
+def decode_step_paged(q, k_pages, v_pages, k_new, v_new, pos, block_table, seq_lens, max_seq_len: int,
+                      scale: float, out, workspace=None, n_split: int = 0, lse=None, status=None,
+                      stream=None):
+    """kv_append_paged then decode_attention_paged as one call (kvd_decode_step_paged)."""
+    import torch
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _require(t, n, torch.bfloat16, 3)
+    _require(pos, "pos", torch.int32, 1)
+    B = q.shape[0]
+    Hkv, D = k_pages.shape[2], k_pages.shape[3]
+    if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or pos.shape != (B,):
+        raise ValueError("decode_step_paged: inconsistent shapes")
+    head, tail = _decode_paged_args(q, k_pages, v_pages, block_table, seq_lens, max_seq_len, scale,
+                                    n_split, workspace, out, lse, status, stream)
+    _check(load().kvd_decode_step_paged(k_pages.data_ptr(), v_pages.data_ptr(), k_new.data_ptr(),
+                                        v_new.data_ptr(), pos.data_ptr(), q.data_ptr(),
+                                        block_table.data_ptr(), seq_lens.data_ptr(), *head, *tail),
+           "kvd_decode_step_paged")
 
 
 def decode_step(q, k_cache, v_cache, k_new, v_new, pos, seq_lens, max_seq_len: int, scale: float,

@@ -10,22 +10,24 @@
 
 namespace kvd {
 
-const ChunkKernel* mma_table_d64(bool f32);
-const ChunkKernel* mma_table_d128(bool f32);
-const ChunkKernel* mma_table_d256(bool f32);
+const ChunkKernel* mma_table_d64(bool f32, bool paged);
+const ChunkKernel* mma_table_d128(bool f32, bool paged);
+const ChunkKernel* mma_table_d256(bool f32, bool paged);
 
-const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out) {
+const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged) {
     switch (head_dim) {
-        case 64: return mma_table_d64(f32_out);
-        case 128: return mma_table_d128(f32_out);
-        case 256: return mma_table_d256(f32_out);
+        case 64: return mma_table_d64(f32_out, paged);
+        case 128: return mma_table_d128(f32_out, paged);
+        case 256: return mma_table_d256(f32_out, paged);
         default: return nullptr;
     }
 }
 
-const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out) {
+// The tcgen05 kernels take either cache form at run time (only their loads
+// differ); the mma.sync kernel has a compiled variant per form.
+const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged) {
     if (group < 1 || group > KVD_MAX_GROUP) return nullptr;
-    return group <= 16 ? mma_chunk_kernel(head_dim, f32_out) : tc_chunk_kernel(head_dim, f32_out, group);
+    return group <= 16 ? mma_chunk_kernel(head_dim, f32_out, paged) : tc_chunk_kernel(head_dim, f32_out, group);
 }
 
 namespace {
@@ -48,8 +50,27 @@ kvd_status check_shape(int batch, int Hq, int Hkv, int D, kvd_out_dtype dt) {
     return KVD_OK;
 }
 
-const ChunkKernel* pick_kernel(int Hq, int Hkv, int D, kvd_out_dtype dt) {
-    return find_chunk_kernel(D, Hq / Hkv, dt == KVD_OUT_F32);
+// Both forms of a variant share their launch shape and schedule geometry, so
+// planning and the host replica use the contiguous one.
+const ChunkKernel* pick_kernel(int Hq, int Hkv, int D, kvd_out_dtype dt, bool paged = false) {
+    return find_chunk_kernel(D, Hq / Hkv, dt == KVD_OUT_F32, paged);
+}
+
+// Paged cache arguments, checked; s_max of the contiguous calls becomes
+// max_blocks * page_size.
+kvd_status check_paged(const int32_t* block_table, int max_blocks, int page_size, int num_pages,
+                       PagedCache* pg, int* s_max) {
+    if (!block_table || !aligned(block_table, 4)) return KVD_ERR_INVALID_ARG;
+    if (page_size < 16 || page_size > 4096 || (page_size & (page_size - 1)) != 0) return KVD_ERR_INVALID_ARG;
+    if (max_blocks < 1 || num_pages < 1) return KVD_ERR_INVALID_ARG;
+    // Token positions and pool rows (and one past the pool) stay 32-bit.
+    if ((long long)max_blocks * page_size > 0x7fffffffLL || (long long)num_pages * page_size >= 0x7fffffffLL)
+        return KVD_ERR_INVALID_ARG;
+    int shift = 0;
+    while ((1 << shift) < page_size) ++shift;
+    *pg = PagedCache{block_table, max_blocks, shift, num_pages};
+    *s_max = max_blocks * page_size;
+    return KVD_OK;
 }
 
 kvd_status device_sms(int* sms) {
@@ -130,7 +151,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
                   const int32_t* seq_lens, int batch, int s_max, int max_seq_len, int Hq, int Hkv,
                   int D, float scale, int n_split_req, void* workspace, size_t workspace_bytes,
                   void* out, kvd_out_dtype dt, float* lse, int32_t* status, kvd_stream_t stream,
-                  const AppendArgs* app = nullptr) {
+                  const AppendArgs* app = nullptr, const PagedCache* pg = nullptr) {
     kvd_status st = check_shape(batch, Hq, Hkv, D, dt);
     if (st != KVD_OK) return st;
     if (s_max <= 0 || max_seq_len < 0 || max_seq_len > s_max) return KVD_ERR_INVALID_ARG;
@@ -139,9 +160,11 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     if (!aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) || !aligned(out, 16) ||
         !aligned(seq_lens, 4) || (lse && !aligned(lse, 4)) || (status && !aligned(status, 4)))
         return KVD_ERR_INVALID_ARG;
-    if ((size_t)batch * s_max * Hkv * D > ((size_t)1 << 62)) return KVD_ERR_INVALID_ARG;
+    // Cache rows: batch * s_max, or the pool's pages * page size.
+    const long long cache_rows = pg ? ((long long)pg->num_pages << pg->page_shift) : (long long)batch * s_max;
+    if ((size_t)cache_rows * Hkv * D > ((size_t)1 << 62)) return KVD_ERR_INVALID_ARG;
     // The tensor-core path addresses cache rows and query rows with 32-bit TMA coordinates.
-    if (Hq / Hkv > 16 && ((long long)batch * s_max > 0x7fffffffLL || (long long)batch * Hq > 0x7fffffffLL))
+    if (Hq / Hkv > 16 && (cache_rows > 0x7fffffffLL || (long long)batch * Hq > 0x7fffffffLL))
         return KVD_ERR_UNSUPPORTED;
 
     int n_split = 0;
@@ -150,6 +173,8 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     st = plan(batch, Hq, Hkv, D, max_seq_len, 0 /* query device if heuristic */, n_split_req, dt,
               &n_split, &need, &k);
     if (st != KVD_OK) return st;
+    if (pg) k = pick_kernel(Hq, Hkv, D, dt, true);
+    if (!k) return KVD_ERR_UNSUPPORTED;
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return KVD_ERR_WORKSPACE_TOO_SMALL;
         if (!aligned(workspace, 256)) return KVD_ERR_INVALID_ARG;
@@ -176,6 +201,12 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     p.out = out;
     p.lse = lse;
     p.status = status;
+    if (pg) {
+        p.block_table = pg->block_table;
+        p.max_blocks = pg->max_blocks;
+        p.page_shift = pg->page_shift;
+        p.num_pages = pg->num_pages;
+    }
     if (need > 0) {
         const size_t P = (size_t)batch * Hkv, G = (size_t)p.G, slots = (size_t)n_split + P - 1;
         uint8_t* w = static_cast<uint8_t*>(workspace);
@@ -189,8 +220,9 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
         // The append, then the chunk kernel in early mode: it starts (and works
         // out its schedule) while the append runs, and only its cache loads
         // wait for the append's grid.
+        const PagedCache none{nullptr, 0, 0, 0};
         if (launch_append(app->k_cache, app->v_cache, app->k_new, app->v_new, app->pos, batch, s_max, Hkv, D,
-                          status, s) != cudaSuccess)
+                          status, pg ? *pg : none, s) != cudaSuccess)
             return KVD_ERR_CUDA;
         p.early = 1;
         p.pos = app->pos;
@@ -237,10 +269,63 @@ kvd_status kvd_kv_append(void* k_cache, void* v_cache, const void* k_new, const 
                                        head_dim, status_word);
     if (st != KVD_OK) return st;
     if (batch == 0) return KVD_OK;
+    const PagedCache none{nullptr, 0, 0, 0};
     return launch_append(k_cache, v_cache, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim,
-                         status_word, static_cast<cudaStream_t>(stream)) == cudaSuccess
+                         status_word, none, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? KVD_OK
                : KVD_ERR_CUDA;
+}
+
+kvd_status kvd_kv_append_paged(void* k_pages, void* v_pages, const void* k_new, const void* v_new,
+                               const int32_t* block_table, const int32_t* pos, int batch,
+                               int max_blocks, int page_size, int num_pages, int n_heads_kv,
+                               int head_dim, int32_t* status_word, kvd_stream_t stream) {
+    PagedCache pg;
+    int s_max = 0;
+    kvd_status st = check_paged(block_table, max_blocks, page_size, num_pages, &pg, &s_max);
+    if (st != KVD_OK) return st;
+    st = check_append(k_pages, v_pages, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim, status_word);
+    if (st != KVD_OK) return st;
+    if (batch == 0) return KVD_OK;
+    return launch_append(k_pages, v_pages, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim,
+                         status_word, pg, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KVD_OK
+               : KVD_ERR_CUDA;
+}
+
+kvd_status kvd_decode_attention_paged(const void* q, const void* k_pages, const void* v_pages,
+                                      const int32_t* block_table, const int32_t* seq_lens,
+                                      int batch, int max_blocks, int page_size, int num_pages,
+                                      int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim,
+                                      float scale, int n_split, void* workspace,
+                                      size_t workspace_bytes, void* out, kvd_out_dtype out_dtype,
+                                      float* lse_out, int32_t* status_word, kvd_stream_t stream) {
+    PagedCache pg;
+    int s_max = 0;
+    const kvd_status st = check_paged(block_table, max_blocks, page_size, num_pages, &pg, &s_max);
+    if (st != KVD_OK) return st;
+    return decode(kBoth, q, k_pages, v_pages, seq_lens, batch, s_max, max_seq_len, n_heads_q, n_heads_kv,
+                  head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype, lse_out,
+                  status_word, stream, nullptr, &pg);
+}
+
+kvd_status kvd_decode_step_paged(void* k_pages, void* v_pages, const void* k_new, const void* v_new,
+                                 const int32_t* pos, const void* q, const int32_t* block_table,
+                                 const int32_t* seq_lens, int batch, int max_blocks, int page_size,
+                                 int num_pages, int max_seq_len, int n_heads_q, int n_heads_kv,
+                                 int head_dim, float scale, int n_split, void* workspace,
+                                 size_t workspace_bytes, void* out, kvd_out_dtype out_dtype,
+                                 float* lse_out, int32_t* status_word, kvd_stream_t stream) {
+    PagedCache pg;
+    int s_max = 0;
+    kvd_status st = check_paged(block_table, max_blocks, page_size, num_pages, &pg, &s_max);
+    if (st != KVD_OK) return st;
+    st = check_append(k_pages, v_pages, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim, status_word);
+    if (st != KVD_OK) return st;
+    const AppendArgs app{k_pages, v_pages, k_new, v_new, pos};
+    return decode(kBoth, q, k_pages, v_pages, seq_lens, batch, s_max, max_seq_len, n_heads_q, n_heads_kv,
+                  head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype, lse_out,
+                  status_word, stream, &app, &pg);
 }
 
 kvd_status kvd_decode_attention(const void* q, const void* k_cache, const void* v_cache,

@@ -1,7 +1,9 @@
 // KV append: the new token's key and value rows are copied into the cache at
 // each sequence's current length (All About Transformer Inference,
 // "Transformer inference basics", Generation: the new token's KV is appended
-// to the KV cache). A bit copy in 16-byte vectors; no arithmetic.
+// to the KV cache). A bit copy in 16-byte vectors; no arithmetic. With a paged
+// cache the row goes to its block's page (same page, "Tricks for improving
+// generation throughput and latency", Paged Attention).
 #include "../../include/kvdecode.h"
 #include "common.cuh"
 #include "params.h"
@@ -13,7 +15,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_ca
                                                        const uint4* __restrict__ v_new,
                                                        const int32_t* __restrict__ pos, int B,
                                                        int S_max, int Hkv, int vec_per_row,
-                                                       int32_t* status) {
+                                                       int32_t* status, const PagedCache pg) {
     // Let the attention kernel that follows start its launch; it waits for
     // this grid's writes before reading the cache.
     pdl_launch_dependents();
@@ -33,14 +35,23 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_ca
             if (status && which == 0 && h == 0 && ch == 0) atomicOr(status, KVD_STATUS_POS_OUT_OF_RANGE);
             continue;
         }
-        const long long dst = (((long long)b * S_max + t) * Hkv + h) * vec_per_row + ch;
+        long long trow = (long long)b * S_max + t;  // cache row of the token
+        if (pg.block_table) {
+            const int page = __ldg(pg.block_table + (size_t)b * pg.max_blocks + (t >> pg.page_shift));
+            if (page < 0 || page >= pg.num_pages) {
+                if (status && which == 0 && h == 0 && ch == 0) atomicOr(status, KVD_STATUS_BAD_PAGE);
+                continue;
+            }
+            trow = ((long long)page << pg.page_shift) + (t & ((1 << pg.page_shift) - 1));
+        }
+        const long long dst = (trow * Hkv + h) * vec_per_row + ch;
         (which == 0 ? k_cache : v_cache)[dst] = val;
     }
 }
 
 cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                           const int32_t* pos, int B, int S_max, int Hkv, int D,
-                          int32_t* status, cudaStream_t stream) {
+                          int32_t* status, const PagedCache& pg, cudaStream_t stream) {
     const int vec_per_row = D / 8;
     const long long work = 2LL * B * Hkv * vec_per_row;
     long long blocks = (work + 255) / 256;
@@ -53,7 +64,7 @@ cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const
     // The launch's own status (a stale error from earlier work is not picked up).
     return cudaLaunchKernelEx(&cfg, kv_append_kernel, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
                               static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), pos, B, S_max,
-                              Hkv, vec_per_row, status);
+                              Hkv, vec_per_row, status, pg);
 }
 
 }  // namespace kvd

@@ -27,6 +27,13 @@ struct DecodeParams {
     int32_t* status;      // optional
     float* ws_o;          // [slots, G, D] partial unnormalised outputs
     float2* ws_ml;        // [slots, G] partial (max, sum), base-2 max
+    // Paged cache (block_table non-null): k and v are pools [num_pages, page,
+    // Hkv, D] of pages of 1 << page_shift tokens, and token t of sequence b is
+    // row t & (page - 1) of page block_table[b * max_blocks + (t >> page_shift)]
+    // (S_max is then max_blocks << page_shift). Entries outside [0, num_pages)
+    // give zero rows and KVD_STATUS_BAD_PAGE.
+    const int32_t* block_table;
+    int max_blocks, page_shift, num_pages;
 };
 
 // One compiled variant of the split-KV chunk kernel.
@@ -42,13 +49,19 @@ struct ChunkKernel {
 
 // The kernel for a shape: groups of up to 16 query heads per KV head run on the
 // mma.sync kernel, wider groups (17..64) on the tcgen05 kernel.
-const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out);
-const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out);
+const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged);
+const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged);
 const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out, int group);
 
 cudaError_t launch_merge(const DecodeParams& p, int head_dim, bool f32_out, int num_sms, cudaStream_t stream);
+// A paged cache's table (block_table null: the cache is contiguous).
+struct PagedCache {
+    const int32_t* block_table;
+    int max_blocks, page_shift, num_pages;
+};
+
 cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                           const int32_t* pos, int B, int S_max, int Hkv, int D,
-                          int32_t* status, cudaStream_t stream);
+                          int32_t* status, const PagedCache& pg, cudaStream_t stream);
 
 }  // namespace kvd

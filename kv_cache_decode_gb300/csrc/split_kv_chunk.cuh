@@ -149,7 +149,7 @@ struct ChunkShape {
     static_assert(D % 16 == 0 && D >= 64, "head_dim");
 };
 
-template <int D, int HT, int TS, int TT, int STAGES, bool F32OUT, int MINB>
+template <int D, int HT, int TS, int TT, int STAGES, bool F32OUT, int MINB, bool PAGED>
 __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const DecodeParams p) {
     using Sh = ChunkShape<D, HT, TS, TT, STAGES>;
     constexpr int NW = Sh::NW, NT = Sh::NT, TW = Sh::TW, NS = Sh::NS, KS = Sh::KS,
@@ -231,22 +231,49 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
     // Row r of the stage holds token tok_lo + r; its 16-byte chunk ch is
     // stored at chunk position ch ^ (r & 7), so that ldmatrix reads of 8
     // consecutive rows hit 8 distinct bank groups.
+    // A paged cache (PAGED) finds each token's row through the block table:
+    // row t % page of page table[b][t / page]; a table entry that names no
+    // page of the pool gives zero rows (the copy reads 0 bytes) and flags it.
     auto issue = [&](const Tile& t, int stage) {
         const int nvalid = t.tok_hi - t.tok_lo;
-        const size_t row0 = ((size_t)t.b * p.S_max + t.tok_lo) * p.Hkv + t.h;
-        const __nv_bfloat16* kb = Kg + row0 * D;
-        const __nv_bfloat16* vb = Vg + row0 * D;
         const uint32_t sbase = smem_u32(stages) + stage * Sh::STAGE_BYTES;
+        if constexpr (!PAGED) {
+            const size_t row0 = ((size_t)t.b * p.S_max + t.tok_lo) * p.Hkv + t.h;
+            const __nv_bfloat16* kb = Kg + row0 * D;
+            const __nv_bfloat16* vb = Vg + row0 * D;
 #pragma unroll 4
-        for (int i = tid; i < 2 * TT * CH; i += NT) {
-            const int kv = i / (TT * CH);
-            const int r = (i / CH) % TT;
-            const int ch = i % CH;
-            const __nv_bfloat16* base = kv ? vb : kb;
-            const bool ok = r < nvalid;
-            const __nv_bfloat16* src = ok ? base + (size_t)r * row_stride + ch * 8 : base;
-            const uint32_t dst = sbase + (uint32_t)((kv * TILE_ELEMS + r * D + ((ch ^ (r & 7)) * 8)) * 2);
-            cp_async_16(dst, src, ok ? 16 : 0, policy);
+            for (int i = tid; i < 2 * TT * CH; i += NT) {
+                const int kv = i / (TT * CH);
+                const int r = (i / CH) % TT;
+                const int ch = i % CH;
+                const __nv_bfloat16* base = kv ? vb : kb;
+                const bool ok = r < nvalid;
+                const __nv_bfloat16* src = ok ? base + (size_t)r * row_stride + ch * 8 : base;
+                const uint32_t dst = sbase + (uint32_t)((kv * TILE_ELEMS + r * D + ((ch ^ (r & 7)) * 8)) * 2);
+                cp_async_16(dst, src, ok ? 16 : 0, policy);
+            }
+        } else {
+            const int32_t* table = p.block_table + (size_t)t.b * p.max_blocks;
+            const int shift = p.page_shift, in_page = (1 << shift) - 1;
+            const __nv_bfloat16* kb = Kg + (size_t)t.h * D;
+            const __nv_bfloat16* vb = Vg + (size_t)t.h * D;
+#pragma unroll 4
+            for (int i = tid; i < 2 * TT * CH; i += NT) {
+                const int kv = i / (TT * CH);
+                const int r = (i / CH) % TT;
+                const int ch = i % CH;
+                const int tok = t.tok_lo + r;
+                const int page = (r < nvalid) ? __ldg(table + (tok >> shift)) : 0;
+                const bool in_pool = (unsigned)page < (unsigned)p.num_pages;
+                if (r < nvalid && !in_pool && kv == 0 && ch == 0 && p.status)
+                    atomicOr(p.status, KVD_STATUS_BAD_PAGE);
+                const bool ok = r < nvalid && in_pool;
+                const __nv_bfloat16* base = kv ? vb : kb;
+                const __nv_bfloat16* src =
+                    ok ? base + (((size_t)page << shift) + (size_t)(tok & in_page)) * row_stride + ch * 8 : base;
+                const uint32_t dst = sbase + (uint32_t)((kv * TILE_ELEMS + r * D + ((ch ^ (r & 7)) * 8)) * 2);
+                cp_async_16(dst, src, ok ? 16 : 0, policy);
+            }
         }
     };
 

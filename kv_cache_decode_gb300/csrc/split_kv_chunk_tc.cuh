@@ -280,6 +280,8 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             // (complete at launch), read once per pair until the first wait.
             bool waited = !p.early;
             int pos_pair = -1, pos_b = -1;
+            const bool paged = p.block_table != nullptr;
+            const int box_rows = paged ? min(1 << p.page_shift, T) : T;
             if (!waited && walker.b < p.B) {  // issued now, first used at the first tile
                 pos_pair = walker.b * p.Hkv + walker.h;
                 pos_b = __ldg(p.pos + walker.b);
@@ -302,10 +304,36 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                 if (!tc::mbar_wait(empty, ((j / NS) & 1) ^ 1, abort_flag, kBudget)) break;
                 tc::mbar_arrive_expect_tx(full, (uint32_t)Sh::TILE_BYTES);
                 const uint32_t dst = (is_k ? sK : sV) + (uint32_t)(s * Sh::TILE_BYTES);
-                const int row = t.b * p.S_max + t.tok_lo;
+                if (!paged) {
+                    const int row = t.b * p.S_max + t.tok_lo;
 #pragma unroll
-                for (int kb = 0; kb < KB; ++kb)
-                    tc::tma_load_3d(dst + kb * Sh::KB_BYTES, map, kb * 64, t.h, row, full, pol_kv);
+                    for (int kb = 0; kb < KB; ++kb)
+                        tc::tma_load_3d(dst + kb * Sh::KB_BYTES, map, kb * 64, t.h, row, full, pol_kv);
+                } else {
+                    // Paged cache: the tile is fetched as boxes of box_rows
+                    // tokens (the page size, up to the tile), each from its
+                    // block's page. Tile rows are page-aligned (tiles start at
+                    // multiples of T within a sequence, and a page is at least
+                    // 16 tokens), so no box crosses a page. A box past the
+                    // tile's tokens, or whose table entry names no page, is
+                    // read from past the pool's end: zeros.
+                    const int32_t* table = p.block_table + (size_t)t.b * p.max_blocks;
+                    const int oob = p.num_pages << p.page_shift;
+                    for (int r0 = 0; r0 < T; r0 += box_rows) {
+                        const int tok = t.tok_lo + r0;
+                        int row = oob;
+                        if (tok < t.tok_hi) {
+                            const int page = __ldg(table + (tok >> p.page_shift));
+                            if ((unsigned)page < (unsigned)p.num_pages)
+                                row = (page << p.page_shift) + (tok & ((1 << p.page_shift) - 1));
+                            else if (is_k && p.status)
+                                atomicOr(p.status, KVD_STATUS_BAD_PAGE);
+                        }
+#pragma unroll
+                        for (int kb = 0; kb < KB; ++kb)
+                            tc::tma_load_3d(dst + kb * Sh::KB_BYTES + r0 * 128, map, kb * 64, t.h, row, full, pol_kv);
+                    }
+                }
                 ++j;
             }
             // Do not leave with copies in flight: wait for the last loads to land.

@@ -4,6 +4,7 @@
 
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstring>
 
 #include "split_kv_chunk_tc.cuh"
@@ -25,9 +26,15 @@ cudaError_t launch_tc_chunk(const ChunkKernel& k, const DecodeParams& p, cudaStr
         if (!tc_encode_map(&maps.q, p.q, 2, dims, strides, box)) return cudaErrorInvalidValue;
     }
     {
-        const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hkv, (cuuint64_t)p.B * p.S_max};
+        // Cache rows: [B * S_max] for a contiguous cache, [num_pages * page]
+        // for a pool of pages, whose boxes are one page (at most one tile) high.
+        constexpr int T = TcShape<D, F32, QR>::T;
+        const bool paged = p.block_table != nullptr;
+        const cuuint64_t rows = paged ? ((cuuint64_t)p.num_pages << p.page_shift) : (cuuint64_t)p.B * p.S_max;
+        const int box_rows = paged ? std::min(1 << p.page_shift, T) : T;
+        const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hkv, rows};
         const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.Hkv * D * 2};
-        const cuuint32_t box[3] = {64, 1, (cuuint32_t)TcShape<D, F32, QR>::T};
+        const cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
         if (!tc_encode_map(&maps.k, p.k, 3, dims, strides, box)) return cudaErrorInvalidValue;
         if (!tc_encode_map(&maps.v, p.v, 3, dims, strides, box)) return cudaErrorInvalidValue;
     }

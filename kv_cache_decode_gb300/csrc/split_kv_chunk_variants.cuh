@@ -22,7 +22,7 @@ struct ChunkConfig {
     static constexpr int MINB = (2 * (SMEM + 1024) <= 228 * 1024) ? 2 : 1;
 };
 
-template <int D, bool F32>
+template <int D, bool F32, bool PAGED>
 cudaError_t launch_mma_chunk(const ChunkKernel& k, const DecodeParams& p, cudaStream_t stream) {
     using C = ChunkConfig<D, 1>;
     cudaLaunchConfig_t cfg = {};
@@ -35,16 +35,16 @@ cudaError_t launch_mma_chunk(const ChunkKernel& k, const DecodeParams& p, cudaSt
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kv_chunk_kernel<D, 1, C::TS, C::TT, C::STAGES, F32, C::MINB>, p);
+    return cudaLaunchKernelEx(&cfg, split_kv_chunk_kernel<D, 1, C::TS, C::TT, C::STAGES, F32, C::MINB, PAGED>, p);
 }
 
-template <int D, bool F32>
+template <int D, bool F32, bool PAGED>
 inline ChunkKernel make_mma_chunk_kernel(int index) {
     using C = ChunkConfig<D, 1>;
     using Sh = ChunkShape<D, 1, C::TS, C::TT, C::STAGES>;
     ChunkKernel k;
-    k.fn = reinterpret_cast<const void*>(split_kv_chunk_kernel<D, 1, C::TS, C::TT, C::STAGES, F32, C::MINB>);
-    k.launch = launch_mma_chunk<D, F32>;
+    k.fn = reinterpret_cast<const void*>(split_kv_chunk_kernel<D, 1, C::TS, C::TT, C::STAGES, F32, C::MINB, PAGED>);
+    k.launch = launch_mma_chunk<D, F32, PAGED>;
     k.head_dim = D;
     k.threads = Sh::NT;
     k.smem_bytes = Sh::SMEM_BYTES;
@@ -58,11 +58,14 @@ inline ChunkKernel make_mma_chunk_kernel(int index) {
     return k;
 }
 
-#define KVD_MMA_TABLE(D, IDX)                                                                     \
-    const ChunkKernel* mma_table_d##D(bool f32) {                                                \
-        static const ChunkKernel table[2] = {make_mma_chunk_kernel<D, false>(IDX),              \
-                                             make_mma_chunk_kernel<D, true>(IDX + 1)};           \
-        return &table[f32 ? 1 : 0];                                                              \
+// Variants of one head dimension: contiguous cache at indices IDX, IDX + 1,
+// paged cache at PIDX, PIDX + 1 (bf16 and fp32 output).
+#define KVD_MMA_TABLE(D, IDX, PIDX)                                                               \
+    const ChunkKernel* mma_table_d##D(bool f32, bool paged) {                                    \
+        static const ChunkKernel table[2][2] = {                                                 \
+            {make_mma_chunk_kernel<D, false, false>(IDX), make_mma_chunk_kernel<D, true, false>(IDX + 1)}, \
+            {make_mma_chunk_kernel<D, false, true>(PIDX), make_mma_chunk_kernel<D, true, true>(PIDX + 1)}}; \
+        return &table[paged ? 1 : 0][f32 ? 1 : 0];                                               \
     }
 
 }  // namespace kvd

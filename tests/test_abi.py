@@ -179,3 +179,51 @@ def test_decode_step_rejects(lib, over, expect):
 
 def test_decode_step_batch_zero_is_noop(lib):
     assert lib.kvd_decode_step(*_step_args(B=0, n_split=3, ws=None)) == kvd.OK
+
+
+def _paged_args(bt=FAKE, B=2, max_blocks=4, page=16, num_pages=10, maxlen=64, **over):
+    a = _dec_args(maxlen=maxlen, **over)
+    # (q, k_pages, v_pages, block_table, seq_lens, batch, max_blocks, page_size, num_pages) + the rest
+    return [a[0], a[1], a[2], bt, a[3], B, max_blocks, page, num_pages] + a[6:]
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(), None),                                    # valid up to the launch (not made here)
+    (dict(bt=None), kvd.ERR_INVALID_ARG),
+    (dict(bt=FAKE + 2), kvd.ERR_INVALID_ARG),          # table not 4-byte aligned
+    (dict(page=48), kvd.ERR_INVALID_ARG),              # not a power of two
+    (dict(page=8), kvd.ERR_INVALID_ARG),               # below 16
+    (dict(page=8192), kvd.ERR_INVALID_ARG),            # above 4096
+    (dict(max_blocks=0), kvd.ERR_INVALID_ARG),
+    (dict(num_pages=0), kvd.ERR_INVALID_ARG),
+    (dict(num_pages=1 << 27, page=16), kvd.ERR_INVALID_ARG),   # pool rows reach 2^31
+    (dict(maxlen=65), kvd.ERR_INVALID_ARG),            # above max_blocks * page_size
+    (dict(q=None), kvd.ERR_INVALID_ARG),
+    (dict(Hq=7), kvd.ERR_INVALID_ARG),
+    (dict(ws_bytes=16), kvd.ERR_WORKSPACE_TOO_SMALL),
+])
+def test_decode_paged_rejects(lib, over, expect):
+    if expect is None:
+        return  # the valid case would launch; the GPU tests cover it
+    assert lib.kvd_decode_attention_paged(*_paged_args(**over)) == expect
+    a = _paged_args(**over)
+    # step: (k_pages, v_pages, k_new, v_new, pos, q, block_table, seq_lens, batch, ...)
+    step = [a[1], a[2], FAKE, FAKE, FAKE, a[0], a[3], a[4]] + a[5:]
+    assert lib.kvd_decode_step_paged(*step) == expect
+
+
+def test_decode_paged_batch_zero_is_noop(lib):
+    assert lib.kvd_decode_attention_paged(*_paged_args(B=0, n_split=3, ws=None)) == kvd.OK
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((None, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 16, 10, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, None, FAKE, 2, 4, 16, 10, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 24, 10, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 0, 16, 10, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 16, 0, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 4, 16, 10, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, 16, 10, 1, 128, None, None), kvd.OK),  # batch 0: no-op
+])
+def test_append_paged_rejects(lib, args, expect):
+    assert lib.kvd_kv_append_paged(*args) == expect
