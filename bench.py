@@ -58,6 +58,10 @@ def parse_args():
     ap.add_argument("--out-dtype", default="bf16", choices=["bf16", "f32"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--page-size", type=int, default=0,
+                    help="paged KV cache with pages of this many tokens; 0 = contiguous")
+    ap.add_argument("--page-order", default="shuffled", choices=["shuffled", "sequential"],
+                    help="paged: pages in random order over the pool, or each sequence's pages in a row")
     return ap.parse_args()
 
 
@@ -273,11 +277,21 @@ def run_ours(args):
 
     props = torch.cuda.get_device_properties(dev)
     l2 = int(getattr(props, "L2_cache_size", 126 * 2**20))
-    cache_bytes = 2 * inp.k_cache.nbytes
+    paged = args.page_size > 0
+    if paged:
+        # The same rows spread over a shuffled pool of pages; the calls take the
+        # pool and its block table instead of the contiguous cache.
+        pinp = workloads.paged_step_inputs(inp, args.page_size, seed=w.seed, pad_bits=0,
+                                           shuffle=args.page_order == "shuffled")
+        k_src, v_src = pinp.k_pages, pinp.v_pages
+        bt = torch.from_numpy(pinp.block_table).to(dev)
+    else:
+        k_src, v_src = inp.k_cache, inp.v_cache
+    cache_bytes = 2 * k_src.nbytes
     # Rotate cache copies so that each step's K/V rows are not L2-resident.
     R = max(1, math.ceil(3 * l2 / max(kv_bytes, 1)))
     R = max(1, min(R, int(40e9 // max(cache_bytes, 1)), 16))
-    kc0, vc0 = up(inp.k_cache), up(inp.v_cache)
+    kc0, vc0 = up(k_src), up(v_src)
     kcs, vcs = [kc0], [vc0]
     for _ in range(R - 1):
         kcs.append(kc0.clone())
@@ -293,8 +307,12 @@ def run_ours(args):
 
     def step(r, stream=None):
         # append the new token's K/V rows, then attend (one call, three launches)
-        kvd.decode_step(q, kcs[r], vcs[r], kn, vn, pos, lens, max_len, w.scale, out, workspace=ws,
-                        n_split=args.n_split, stream=stream)
+        if paged:
+            kvd.decode_step_paged(q, kcs[r], vcs[r], kn, vn, pos, bt, lens, max_len, w.scale, out,
+                                  workspace=ws, n_split=args.n_split, stream=stream)
+        else:
+            kvd.decode_step(q, kcs[r], vcs[r], kn, vn, pos, lens, max_len, w.scale, out, workspace=ws,
+                            n_split=args.n_split, stream=stream)
 
     for i in range(max(args.warmup, 3)):
         step(i % R)
@@ -344,6 +362,14 @@ def run_ours(args):
     torch.cuda._sleep(int(2e6 + 2e5 * args.steps))  # let the host queue ahead of the GPU
     for i in range(args.steps):
         r = i % R
+        if paged:
+            # no separate paged chunk entry point: the whole attention call is timed
+            kvd.kv_append_paged(kcs[r], vcs[r], kn, vn, bt, pos)
+            ea[i].record(stream)
+            kvd.decode_attention_paged(q, kcs[r], vcs[r], bt, lens, max_len, w.scale, out, workspace=ws,
+                                       n_split=args.n_split)
+            eb[i].record(stream)
+            continue
         kvd.kv_append(kcs[r], vcs[r], kn, vn, pos)
         ea[i].record(stream)
         kvd.split_kv_chunk(q, kcs[r], vcs[r], lens, max_len, w.scale, out, workspace=ws,
@@ -369,8 +395,9 @@ def run_ours(args):
         q_h = pin(inp.q.view(np.int16))
         kn_h, vn_h = pin(inp.k_new.view(np.int16)), pin(inp.v_new.view(np.int16))
         pos_h, lens_h = pin(inp.pos), pin(lens_np)
+        bt_h = pin(pinp.block_table if paged else np.zeros(0, np.int32))
         out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-        h2d = q_h.nbytes + kn_h.nbytes + vn_h.nbytes + pos_h.nbytes + lens_h.nbytes
+        h2d = q_h.nbytes + kn_h.nbytes + vn_h.nbytes + pos_h.nbytes + lens_h.nbytes + bt_h.nbytes
         d2h = out_h.nbytes
 
         def e2e_step(r):
@@ -379,6 +406,8 @@ def run_ours(args):
             vn.view(torch.int16).copy_(vn_h, non_blocking=True)
             pos.copy_(pos_h, non_blocking=True)
             lens.copy_(lens_h, non_blocking=True)
+            if paged:
+                bt.copy_(bt_h, non_blocking=True)  # the table changes between steps in serving
             step(r)
             out_h.copy_(out, non_blocking=True)
 
@@ -406,7 +435,7 @@ def run_ours(args):
 
     peak, peak_kind = measured_peaks()
     achieved = step_bytes / (chunk_avg_ms * 1e-3) / 1e9
-    traffic = ncu_traffic(w.name)
+    traffic = None if paged else ncu_traffic(w.name)
     cpu = None
     if not args.no_cpu_baseline:
         gbs, sec, n_rows, cores, passes = oracle_rate(w, inp, budget_s=10.0, repeats=1,
@@ -425,13 +454,16 @@ def run_ours(args):
                    "out_dtype": args.out_dtype, "n_split": n_split, "parallelism": f"replicas x{world}",
                    "l2_flush": f"{R} rotating KV-cache copies ({R * kv_bytes / 1e6:.0f} MB of K/V rows "
                                f"vs {l2 / 1e6:.0f} MB L2)",
-                   "timing": "CUDA graph per step, CUDA events on the replay stream"},
+                   "timing": "CUDA graph per step, CUDA events on the replay stream",
+                   "kv_layout": (f"paged: {args.page_size}-token pages, {pinp.k_pages.shape[0]} pages "
+                                 f"in {args.page_order} order" if paged else "contiguous")},
         "tokens_per_s": round(tokens_per_s, 1),
         "hbm_frac_of_step": round(value / world / peak, 4),
         "step_bytes": int(step_bytes), "append_bytes": int(append_bytes), "flops": int(flops),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "split_kv_chunk", "peak_source": f"{peak_kind} copy bandwidth",
+                     "kernel": "split_kv_chunk + split_kv_merge (paged)" if paged else "split_kv_chunk",
+                     "peak_source": f"{peak_kind} copy bandwidth",
                      "kernel_ms": round(chunk_avg_ms, 5)},
         "gpu_launches": int(launches_per_step * args.steps),
         "clocks": clocks,

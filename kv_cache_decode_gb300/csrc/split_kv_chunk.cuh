@@ -234,7 +234,16 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
     // A paged cache (PAGED) finds each token's row through the block table:
     // row t % page of page table[b][t / page]; a table entry that names no
     // page of the pool gives zero rows (the copy reads 0 bytes) and flags it.
-    auto issue = [&](const Tile& t, int stage) {
+    // The entries of a tile's pages (at most MAXP, pages being at least 16
+    // tokens) are staged in shared memory one tile ahead (slot = tile index
+    // & 1), so that the copies never wait on a table load.
+    constexpr int MAXP = TT / 16 + 1;
+    __shared__ int s_pages[2][MAXP];
+    auto stage_pages = [&](const Tile& t) -> int {  // this thread's entry (threads < MAXP)
+        const int first = t.tok_lo >> p.page_shift, last = (t.tok_hi - 1) >> p.page_shift;
+        return (first + tid <= last) ? __ldg(p.block_table + (size_t)t.b * p.max_blocks + first + tid) : -1;
+    };
+    auto issue = [&](const Tile& t, int stage, int ps) {
         const int nvalid = t.tok_hi - t.tok_lo;
         const uint32_t sbase = smem_u32(stages) + stage * Sh::STAGE_BYTES;
         if constexpr (!PAGED) {
@@ -253,27 +262,30 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                 cp_async_16(dst, src, ok ? 16 : 0, policy);
             }
         } else {
-            const int32_t* table = p.block_table + (size_t)t.b * p.max_blocks;
+            // Each thread copies the same chunk ch of its RPT rows of K and of
+            // V, so a row's page is looked up once for both tensors.
+            static_assert(NT % CH == 0 && TT % (NT / CH) == 0, "row split");
+            constexpr int RSTEP = NT / CH, RPT = TT / RSTEP;
             const int shift = p.page_shift, in_page = (1 << shift) - 1;
-            const __nv_bfloat16* kb = Kg + (size_t)t.h * D;
-            const __nv_bfloat16* vb = Vg + (size_t)t.h * D;
-#pragma unroll 4
-            for (int i = tid; i < 2 * TT * CH; i += NT) {
-                const int kv = i / (TT * CH);
-                const int r = (i / CH) % TT;
-                const int ch = i % CH;
+            const int first = t.tok_lo >> shift;
+            const int ch = tid % CH, r0 = tid / CH;
+            const __nv_bfloat16* kb = Kg + (size_t)t.h * D + ch * 8;
+            const __nv_bfloat16* vb = Vg + (size_t)t.h * D + ch * 8;
+            bool bad = false;
+#pragma unroll
+            for (int k = 0; k < RPT; ++k) {
+                const int r = r0 + k * RSTEP;
                 const int tok = t.tok_lo + r;
-                const int page = (r < nvalid) ? __ldg(table + (tok >> shift)) : 0;
+                const int page = (r < nvalid) ? s_pages[ps][(tok >> shift) - first] : 0;
                 const bool in_pool = (unsigned)page < (unsigned)p.num_pages;
-                if (r < nvalid && !in_pool && kv == 0 && ch == 0 && p.status)
-                    atomicOr(p.status, KVD_STATUS_BAD_PAGE);
+                bad |= (r < nvalid) && !in_pool;
                 const bool ok = r < nvalid && in_pool;
-                const __nv_bfloat16* base = kv ? vb : kb;
-                const __nv_bfloat16* src =
-                    ok ? base + (((size_t)page << shift) + (size_t)(tok & in_page)) * row_stride + ch * 8 : base;
-                const uint32_t dst = sbase + (uint32_t)((kv * TILE_ELEMS + r * D + ((ch ^ (r & 7)) * 8)) * 2);
-                cp_async_16(dst, src, ok ? 16 : 0, policy);
+                const size_t off = ok ? (((size_t)page << shift) + (size_t)(tok & in_page)) * row_stride : 0;
+                const uint32_t dst = sbase + (uint32_t)((r * D + ((ch ^ (r & 7)) * 8)) * 2);
+                cp_async_16(dst, kb + off, ok ? 16 : 0, policy);
+                cp_async_16(dst + TILE_ELEMS * 2, vb + off, ok ? 16 : 0, policy);
             }
+            if (bad && p.status) atomicOr(p.status, KVD_STATUS_BAD_PAGE);
         }
     };
 
@@ -309,8 +321,26 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
 #pragma unroll
     for (int s = 0; s < STAGES - 1; ++s) {
         Tile t;
-        if (lw.next(t, NoOp{})) issue(t, s);
+        const bool has = lw.next(t, NoOp{});
+        if constexpr (PAGED) {
+            if (has && tid < MAXP) s_pages[s & 1][tid] = stage_pages(t);
+            __syncthreads();
+        }
+        if (has) issue(t, s, s & 1);
         cp_async_commit();
+    }
+    // Paged: the entries of the next tile to issue, loaded a tile ahead.
+    int pg_next = -1;
+    auto peek_pages = [&]() {
+        if (tid < MAXP) {
+            Walker<DevLen, Geo> pk = lw;
+            Tile tn;
+            pg_next = pk.next(tn, NoOp{}) ? stage_pages(tn) : -1;
+        }
+    };
+    if constexpr (PAGED) {
+        peek_pages();
+        if (tid < MAXP) s_pages[(STAGES - 1) & 1][tid] = pg_next;
     }
 
     int it = 0;
@@ -320,8 +350,9 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
         __syncthreads();
         {
             Tile t;
-            if (lw.next(t, NoOp{})) issue(t, (it + STAGES - 1) % STAGES);
+            if (lw.next(t, NoOp{})) issue(t, (it + STAGES - 1) % STAGES, (it + STAGES - 1) & 1);
             cp_async_commit();
+            if constexpr (PAGED) peek_pages();
         }
         const int stage = it % STAGES;
         ++it;
@@ -545,6 +576,11 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                 }
             }
             if constexpr (TS > 1) __syncthreads();
+        }
+        // The next tile's page entries, for its issue after the barrier at the
+        // top of the next iteration (its slot was last read two issues ago).
+        if constexpr (PAGED) {
+            if (tid < MAXP) s_pages[(it + STAGES - 1) & 1][tid] = pg_next;
         }
     }
     cw.finish(write_empty);

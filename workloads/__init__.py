@@ -254,22 +254,24 @@ class PagedStepInputs:
 
 
 def paged_step_inputs(inp: StepInputs, page_size: int, seed: int = 0, spare: int = 3,
-                      pad_bits: int = BF16_NAN) -> PagedStepInputs:
+                      pad_bits: int = BF16_NAN, shuffle: bool = True) -> PagedStepInputs:
     """Spread a step's cache over a shuffled pool of pages.
 
     Each sequence gets the ceil(L_b / page_size) blocks its attended length
     needs (the appended token's slot included; one block for an empty
     sequence, whose placeholder new row goes to slot 0), placed on pages drawn in a
     random order from a pool with ``spare`` extra pages; unused pages and the
-    rows past each sequence's cached tokens hold ``pad_bits``. A layout only:
-    page j of sequence b receives rows [j * P, (j + 1) * P) of its cache.
+    rows past each sequence's cached tokens hold ``pad_bits``. With
+    ``shuffle=False`` the pages are taken in order (each sequence's pages
+    consecutive in the pool). A layout only: page j of sequence b receives
+    rows [j * P, (j + 1) * P) of its cache.
     """
     P = int(page_size)
     B, S, Hkv, D = inp.k_cache.shape
     max_blocks = -(-S // P)
     nblk = [max(1, -(-int(L) // P)) for L in inp.seq_lens]
     num_pages = sum(nblk) + spare
-    order = np.random.default_rng((seed, P, B)).permutation(num_pages)
+    order = np.random.default_rng((seed, P, B)).permutation(num_pages) if shuffle else np.arange(num_pages)
     kp = np.full((num_pages, P, Hkv, D), pad_bits, dtype=np.uint16)
     vp = np.full((num_pages, P, Hkv, D), pad_bits, dtype=np.uint16)
     table = np.full((B, max_blocks), -1, dtype=np.int32)
