@@ -237,55 +237,60 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
     // The entries of a tile's pages (at most MAXP, pages being at least 16
     // tokens) are staged in shared memory one tile ahead (slot = tile index
     // & 1), so that the copies never wait on a table load.
+    // Staged per page: the element offset of the page's first row (for the
+    // tile's KV head), or -1 when the entry names no page of the pool.
     constexpr int MAXP = TT / 16 + 1;
-    __shared__ int s_pages[2][MAXP];
-    auto stage_pages = [&](const Tile& t) -> int {  // this thread's entry (threads < MAXP)
-        const int first = t.tok_lo >> p.page_shift, last = (t.tok_hi - 1) >> p.page_shift;
-        return (first + tid <= last) ? __ldg(p.block_table + (size_t)t.b * p.max_blocks + first + tid) : -1;
+    __shared__ long long s_pages[2][MAXP];
+    auto page_offset = [&](int b, int blk) -> long long {  // block blk of sequence b
+        const int page = __ldg(p.block_table + (size_t)b * p.max_blocks + blk);
+        if ((unsigned)page >= (unsigned)p.num_pages) {
+            if (p.status) atomicOr(p.status, KVD_STATUS_BAD_PAGE);
+            return -1;
+        }
+        return (long long)(((size_t)page << p.page_shift) * row_stride);
     };
+    auto stage_pages = [&](const Tile& t) -> long long {  // this thread's page of tile t (threads < MAXP)
+        const int first = t.tok_lo >> p.page_shift, last = (t.tok_hi - 1) >> p.page_shift;
+        return (first + tid <= last) ? page_offset(t.b, first + tid) : -1;
+    };
+    // Each thread copies the same 16-byte chunk ch of its RPT rows of K and
+    // of V (a row's address is worked out once for both tensors).
+    static_assert(NT % CH == 0 && TT % (NT / CH) == 0, "row split");
+    constexpr int RSTEP = NT / CH, RPT = TT / RSTEP;
+    constexpr int RUNROLL = RPT >= 16 ? 2 : RPT;  // rows per step (registers allow fewer at head_dim 256)
     auto issue = [&](const Tile& t, int stage, int ps) {
         const int nvalid = t.tok_hi - t.tok_lo;
         const uint32_t sbase = smem_u32(stages) + stage * Sh::STAGE_BYTES;
+        const int ch = tid % CH, r0 = tid / CH;
         if constexpr (!PAGED) {
             const size_t row0 = ((size_t)t.b * p.S_max + t.tok_lo) * p.Hkv + t.h;
-            const __nv_bfloat16* kb = Kg + row0 * D;
-            const __nv_bfloat16* vb = Vg + row0 * D;
-#pragma unroll 4
-            for (int i = tid; i < 2 * TT * CH; i += NT) {
-                const int kv = i / (TT * CH);
-                const int r = (i / CH) % TT;
-                const int ch = i % CH;
-                const __nv_bfloat16* base = kv ? vb : kb;
-                const bool ok = r < nvalid;
-                const __nv_bfloat16* src = ok ? base + (size_t)r * row_stride + ch * 8 : base;
-                const uint32_t dst = sbase + (uint32_t)((kv * TILE_ELEMS + r * D + ((ch ^ (r & 7)) * 8)) * 2);
-                cp_async_16(dst, src, ok ? 16 : 0, policy);
-            }
-        } else {
-            // Each thread copies the same chunk ch of its RPT rows of K and of
-            // V, so a row's page is looked up once for both tensors.
-            static_assert(NT % CH == 0 && TT % (NT / CH) == 0, "row split");
-            constexpr int RSTEP = NT / CH, RPT = TT / RSTEP;
-            const int shift = p.page_shift, in_page = (1 << shift) - 1;
-            const int first = t.tok_lo >> shift;
-            const int ch = tid % CH, r0 = tid / CH;
-            const __nv_bfloat16* kb = Kg + (size_t)t.h * D + ch * 8;
-            const __nv_bfloat16* vb = Vg + (size_t)t.h * D + ch * 8;
-            bool bad = false;
-#pragma unroll
+            const __nv_bfloat16* kb = Kg + row0 * D + ch * 8;
+            const __nv_bfloat16* vb = Vg + row0 * D + ch * 8;
+#pragma unroll(RUNROLL)
             for (int k = 0; k < RPT; ++k) {
                 const int r = r0 + k * RSTEP;
-                const int tok = t.tok_lo + r;
-                const int page = (r < nvalid) ? s_pages[ps][(tok >> shift) - first] : 0;
-                const bool in_pool = (unsigned)page < (unsigned)p.num_pages;
-                bad |= (r < nvalid) && !in_pool;
-                const bool ok = r < nvalid && in_pool;
-                const size_t off = ok ? (((size_t)page << shift) + (size_t)(tok & in_page)) * row_stride : 0;
+                const bool ok = r < nvalid;
+                const size_t off = ok ? (size_t)r * row_stride : 0;
                 const uint32_t dst = sbase + (uint32_t)((r * D + ((ch ^ (r & 7)) * 8)) * 2);
                 cp_async_16(dst, kb + off, ok ? 16 : 0, policy);
                 cp_async_16(dst + TILE_ELEMS * 2, vb + off, ok ? 16 : 0, policy);
             }
-            if (bad && p.status) atomicOr(p.status, KVD_STATUS_BAD_PAGE);
+        } else {
+            const int shift = p.page_shift, in_page = (1 << shift) - 1;
+            const int first = t.tok_lo >> shift;
+            const __nv_bfloat16* kb = Kg + (size_t)t.h * D + ch * 8;
+            const __nv_bfloat16* vb = Vg + (size_t)t.h * D + ch * 8;
+#pragma unroll(RUNROLL)
+            for (int k = 0; k < RPT; ++k) {
+                const int r = r0 + k * RSTEP;
+                const int tok = t.tok_lo + r;
+                const long long po = (r < nvalid) ? s_pages[ps][(tok >> shift) - first] : -1;
+                const bool ok = po >= 0;
+                const size_t off = ok ? (size_t)po + (size_t)(tok & in_page) * row_stride : 0;
+                const uint32_t dst = sbase + (uint32_t)((r * D + ((ch ^ (r & 7)) * 8)) * 2);
+                cp_async_16(dst, kb + off, ok ? 16 : 0, policy);
+                cp_async_16(dst + TILE_ELEMS * 2, vb + off, ok ? 16 : 0, policy);
+            }
         }
     };
 
@@ -330,7 +335,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
         cp_async_commit();
     }
     // Paged: the entries of the next tile to issue, loaded a tile ahead.
-    int pg_next = -1;
+    long long pg_next = -1;
     auto peek_pages = [&]() {
         if (tid < MAXP) {
             Walker<DevLen, Geo> pk = lw;
@@ -350,9 +355,22 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
         __syncthreads();
         {
             Tile t;
-            if (lw.next(t, NoOp{})) issue(t, (it + STAGES - 1) % STAGES, (it + STAGES - 1) & 1);
+            const bool has = lw.next(t, NoOp{});
+            if (has) issue(t, (it + STAGES - 1) % STAGES, (it + STAGES - 1) & 1);
             cp_async_commit();
-            if constexpr (PAGED) peek_pages();
+            if constexpr (PAGED) {
+                // Inside a segment the next tile starts where this one ends, in
+                // the same sequence: its blocks follow directly (read only
+                // while they hold tokens of the sequence). Otherwise walk ahead.
+                if (has && !t.seg_end) {
+                    if (tid < MAXP) {
+                        const int blk = (t.tok_hi >> p.page_shift) + tid;
+                        pg_next = (((long long)blk << p.page_shift) < t.L) ? page_offset(t.b, blk) : -1;
+                    }
+                } else {
+                    peek_pages();
+                }
+            }
         }
         const int stage = it % STAGES;
         ++it;
