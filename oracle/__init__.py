@@ -30,6 +30,13 @@ Functions and the passages they follow (page title, section):
   latency", the ragged HBM reads and Paged Attention bullet; the layout is
   this library's reading (the pages give none). Attention over a paged cache
   is attention over the gathered contiguous cache.
+* ``quantize_q8``, ``dequantize_q8``, ``kv_append_q8``, ``decode_attention_q8``:
+  an int8 cache with one float32 scale per (token, KV head) row, symmetric
+  absmax (scale = max|x| / 127, codes = round-half-even(x / scale) in
+  float32). All About Transformer Inference, "Tricks for improving
+  generation throughput and latency", the quantization bullet names int8 KV
+  caches; the scheme is this library's reading. Attention over it is the
+  attention above over the rows read back (scale * code), in double.
 
 Pins (tests/test_oracle_pins.py): closed forms (identical keys give the mean of
 V; a dominant score returns that V row; one token returns it exactly), the
@@ -94,6 +101,13 @@ def _declare(lib):
     lib.kvo_paged_gather.restype = I
     lib.kvo_kv_append_paged.argtypes = [P, P, P, P, P, P, I, I, I, I, I, I, P]
     lib.kvo_kv_append_paged.restype = I
+    L = ctypes.c_long
+    lib.kvo_quantize_q8.argtypes = [P, L, I, P, P]
+    lib.kvo_quantize_q8.restype = I
+    lib.kvo_dequantize_q8.argtypes = [P, P, L, I, P]
+    lib.kvo_dequantize_q8.restype = I
+    lib.kvo_decode_attention_f64kv.argtypes = [P, P, P, P, I, I, I, I, I, Dbl, P, P, I]
+    lib.kvo_decode_attention_f64kv.restype = I
     lib.kvo_max_threads.argtypes = []
     lib.kvo_max_threads.restype = I
     return lib
@@ -240,6 +254,85 @@ def decode_attention_paged(q, k_pages, v_pages, block_table, seq_lens, scale, n_
     kc, _ = paged_gather(k_pages, block_table, seq_lens, lib=lib)
     vc, _ = paged_gather(v_pages, block_table, seq_lens, lib=lib)
     return decode_attention(q, kc, vc, seq_lens, scale, n_threads=n_threads, lib=lib)
+
+
+def quantize_q8(x, lib=None):
+    """int8 codes (same shape) and float32 scales (shape[:-1]) of bf16 rows x[..., D]."""
+    lib = lib or _load()
+    x, xp = _u16(x)
+    D = x.shape[-1]
+    rows = x.size // D
+    codes = np.zeros(x.shape, dtype=np.int8)
+    scales = np.zeros(x.shape[:-1], dtype=np.float32)
+    rc = lib.kvo_quantize_q8(xp, rows, D, codes.ctypes.data_as(ctypes.c_void_p),
+                             scales.ctypes.data_as(ctypes.c_void_p))
+    if rc != 0:
+        raise ValueError(f"oracle quantize_q8 failed ({rc})")
+    return codes, scales
+
+
+def dequantize_q8(codes, scales, lib=None):
+    """Rows read back from int8: scales[..., None] * codes, as float64."""
+    lib = lib or _load()
+    codes = np.ascontiguousarray(codes, dtype=np.int8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    D = codes.shape[-1]
+    if scales.shape != codes.shape[:-1]:
+        raise ValueError("scales must have the codes' shape without the last axis")
+    out = np.zeros(codes.shape, dtype=np.float64)
+    rc = lib.kvo_dequantize_q8(codes.ctypes.data_as(ctypes.c_void_p), scales.ctypes.data_as(ctypes.c_void_p),
+                               codes.size // D, D, out.ctypes.data_as(ctypes.c_void_p))
+    if rc != 0:
+        raise ValueError(f"oracle dequantize_q8 failed ({rc})")
+    return out
+
+
+def decode_attention_f64kv(q, k_cache, v_cache, seq_lens, scale, n_threads: int = 0, lib=None):
+    """decode_attention with float64 caches [B, S_max, Hkv, D] (e.g. rows read back from int8)."""
+    lib = lib or _load()
+    q, qp = _u16(q)
+    k = np.ascontiguousarray(k_cache, dtype=np.float64)
+    v = np.ascontiguousarray(v_cache, dtype=np.float64)
+    B, Hq, D = q.shape
+    Bk, S_max, Hkv, Dk = k.shape
+    if Bk != B or Dk != D or v.shape != k.shape:
+        raise ValueError("q [B,Hq,D] and caches [B,S_max,Hkv,D] disagree")
+    seq_lens, lp = _i32(seq_lens)
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    lse = np.zeros((B, Hq), dtype=np.float64)
+    rc = lib.kvo_decode_attention_f64kv(qp, k.ctypes.data_as(ctypes.c_void_p), v.ctypes.data_as(ctypes.c_void_p),
+                                        lp, B, S_max, Hq, Hkv, D, float(scale),
+                                        out.ctypes.data_as(ctypes.c_void_p),
+                                        lse.ctypes.data_as(ctypes.c_void_p), int(n_threads))
+    if rc != 0:
+        raise ValueError(f"oracle decode_attention_f64kv failed ({rc})")
+    return out, lse
+
+
+def kv_append_q8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, lib=None):
+    """Copies of an int8 cache (codes [B, S_max, Hkv, D], scales [B, S_max, Hkv])
+    with each sequence's new bf16 rows quantized and written at pos[b]; rows
+    with pos outside [0, S_max) are skipped. Returns (kc, vc, ks, vs, n_skipped)."""
+    kc, vc = np.array(k_codes, dtype=np.int8, copy=True), np.array(v_codes, dtype=np.int8, copy=True)
+    ks, vs = np.array(k_scales, dtype=np.float32, copy=True), np.array(v_scales, dtype=np.float32, copy=True)
+    S_max = kc.shape[1]
+    nk, nks = quantize_q8(k_new, lib=lib)
+    nv, nvs = quantize_q8(v_new, lib=lib)
+    skipped = 0
+    for b, t in enumerate(np.asarray(pos, dtype=np.int64)):
+        if t < 0 or t >= S_max:
+            skipped += 1
+            continue
+        kc[b, t], vc[b, t], ks[b, t], vs[b, t] = nk[b], nv[b], nks[b], nvs[b]
+    return kc, vc, ks, vs, skipped
+
+
+def decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, seq_lens, scale, n_threads: int = 0,
+                        lib=None):
+    """Attention over an int8 cache: the rows read back, then decode_attention_f64kv."""
+    k = dequantize_q8(k_codes, k_scales, lib=lib)
+    v = dequantize_q8(v_codes, v_scales, lib=lib)
+    return decode_attention_f64kv(q, k, v, seq_lens, scale, n_threads=n_threads, lib=lib)
 
 
 def max_threads(lib=None) -> int:

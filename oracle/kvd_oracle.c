@@ -50,6 +50,15 @@
  *    row t mod P of page table[b][t / P]. A token whose entry is not a page
  *    of the pool reads zero key and value rows (and an append to it is
  *    skipped); both are counted.
+ *  - int8 cache: the pages name int8 (and fp8, int4) quantization of the
+ *    KV cache as a way to cut its memory traffic (All About Transformer
+ *    Inference, "Tricks for improving generation throughput and latency",
+ *    the quantization bullet) but give no scheme. The one used is symmetric
+ *    absmax per (token, KV head) row: with a = max_d |x_d| (float32),
+ *    scale = a / 127 and code_d = round-half-even(x_d / scale) clamped to
+ *    [-127, 127], both divisions in IEEE float32 (a = 0: scale 0, codes 0).
+ *    A row is read back as scale * code_d. Attention over an int8 cache is
+ *    the attention above over the rows read back, in double precision.
  *
  * All functions return 0 on success and a negative value on bad arguments.
  */
@@ -314,6 +323,106 @@ int kvo_kv_append_paged(uint16_t* k_pages, uint16_t* v_pages, const uint16_t* k_
     }
     if (bad_page) *bad_page = bad;
     return skipped;
+}
+
+/* Quantize rows of D bf16 values to int8 codes and one float32 scale each
+ * (the scheme in the header comment). */
+int kvo_quantize_q8(const uint16_t* x, long rows, int D, int8_t* codes, float* scales)
+{
+    if (rows < 0 || D <= 0) return -1;
+    for (long r = 0; r < rows; ++r) {
+        const uint16_t* xr = x + (size_t)r * D;
+        float a = 0.0f;
+        for (int d = 0; d < D; ++d) {
+            const float v = fabsf((float)bf16_to_double(xr[d]));
+            if (v > a) a = v;
+        }
+        volatile float sc = a / 127.0f;  /* one IEEE float32 division, rounded to nearest */
+        scales[r] = sc;
+        for (int d = 0; d < D; ++d) {
+            int c = 0;
+            if (a > 0.0f) {
+                volatile float y = (float)bf16_to_double(xr[d]) / sc;
+                c = (int)rintf(y);  /* round half to even (default rounding mode) */
+                if (c > 127) c = 127;
+                if (c < -127) c = -127;
+            }
+            codes[(size_t)r * D + d] = (int8_t)c;
+        }
+    }
+    return 0;
+}
+
+/* Rows read back from int8 codes: out[r, d] = scales[r] * codes[r, d]. */
+int kvo_dequantize_q8(const int8_t* codes, const float* scales, long rows, int D, double* out)
+{
+    if (rows < 0 || D <= 0) return -1;
+    for (long r = 0; r < rows; ++r)
+        for (int d = 0; d < D; ++d)
+            out[(size_t)r * D + d] = (double)scales[r] * (double)codes[(size_t)r * D + d];
+    return 0;
+}
+
+/* kvo_decode_attention with the caches given as doubles (e.g. rows read back
+ * from int8): the same definition, the same loops. */
+int kvo_decode_attention_f64kv(const uint16_t* q, const double* k, const double* v,
+                               const int32_t* seq_lens, int B, int S_max, int Hq, int Hkv, int D,
+                               double scale, double* out, double* lse, int n_threads)
+{
+    if (check_dims(B, S_max, Hq, Hkv, D)) return -1;
+    for (int b = 0; b < B; ++b)
+        if (seq_lens[b] < 0 || seq_lens[b] > S_max) return -4;
+    const int G = Hq / Hkv;
+    const long n_problems = (long)B * Hq;
+    int fail = 0;
+#ifdef _OPENMP
+    if (n_threads <= 0) n_threads = omp_get_max_threads();
+#pragma omp parallel num_threads(n_threads) reduction(|:fail)
+#endif
+    {
+        double* w = (double*)malloc(sizeof(double) * (size_t)(S_max > 0 ? S_max : 1));
+        if (!w) {
+            fail = 1;
+        } else {
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+            for (long p = 0; p < n_problems; ++p) {
+                const int b = (int)(p / Hq), h = (int)(p % Hq);
+                const int kvh = h / G;  /* KV head of query head h */
+                const int len = seq_lens[b];
+                const uint16_t* qrow = q + (size_t)p * D;
+                double* o = out + (size_t)p * D;
+                for (int d = 0; d < D; ++d) o[d] = 0.0;
+                if (len == 0) {
+                    if (lse) lse[p] = -INFINITY;
+                    continue;
+                }
+                double top = -INFINITY;
+                for (int t = 0; t < len; ++t) {
+                    const double* kr = k + (((size_t)b * S_max + t) * Hkv + kvh) * (size_t)D;
+                    double acc = 0.0;
+                    for (int d = 0; d < D; ++d) acc += bf16_to_double(qrow[d]) * kr[d];
+                    w[t] = acc * scale;
+                    if (w[t] > top) top = w[t];
+                }
+                double total = 0.0;
+                for (int t = 0; t < len; ++t) {
+                    const double e = exp(w[t] - top);
+                    w[t] = e;
+                    total += e;
+                }
+                for (int t = 0; t < len; ++t) {
+                    const double* vr = v + (((size_t)b * S_max + t) * Hkv + kvh) * (size_t)D;
+                    const double wt = w[t] / total;
+                    for (int d = 0; d < D; ++d) o[d] += wt * vr[d];
+                }
+                if (lse) lse[p] = top + log(total);
+            }
+            free(w);
+        }
+    }
+    return fail ? -5 : 0;
 }
 
 /* Number of threads an OpenMP region would use (1 without OpenMP). */

@@ -416,6 +416,85 @@ def check_paged_append(lib):
     assert np.array_equal(kx[num_pages - 1], kpool[num_pages - 1])
 
 
+def check_q8_closed_forms(lib):
+    # max |x| = 127 gives scale 1, so codes are x rounded half to even and the
+    # extreme elements map to +-127; an all-zero row gives scale 0 and codes 0.
+    x = _bits(np.array([[127.0, 2.5, 3.5, -2.5, -127.0, 0.5, 1.5, 0.0],
+                        [0.0] * 8,
+                        [-6.0, 3.0, 1.5, 0.0, 0.75, -0.25, 6.0, 2.0]], np.float32))
+    codes, scales = oracle.quantize_q8(x, lib=lib)
+    assert scales[0] == 1.0 and scales[1] == 0.0
+    assert list(codes[0]) == [127, 2, 4, -2, -127, 0, 2, 0], codes[0]
+    assert list(codes[1]) == [0] * 8
+    # third row: a = 6, scale = 6/127 in float32; the extremes are exactly +-127
+    assert scales[2] == np.float32(6.0) / np.float32(127.0)
+    assert codes[2][0] == -127 and codes[2][6] == 127 and codes[2][3] == 0
+    back = oracle.dequantize_q8(codes, scales, lib=lib)
+    assert back[0][0] == 127.0 and back[0][1] == 2.0 and back[2][6] == float(scales[2]) * 127
+
+
+def check_q8_error_bound(lib):
+    # Every element reads back within half a step (the scale) of its value,
+    # the largest element of each row reads back as +-127 steps, and signs
+    # are kept.
+    r = np.random.default_rng(71)
+    mags = np.exp(r.uniform(-6, 6, size=(400, 1)))
+    xf = (r.standard_normal((400, 96)) * mags).astype(np.float32)
+    x = _bits(xf)
+    xv = _f64(x)
+    codes, scales = oracle.quantize_q8(x, lib=lib)
+    back = oracle.dequantize_q8(codes, scales, lib=lib)
+    err = np.abs(back - xv)
+    assert np.all(err <= scales[:, None].astype(np.float64) * (0.5 + 1e-5)), float(np.max(err / scales[:, None]))
+    amax = np.abs(xv).argmax(axis=1)
+    assert np.all(np.abs(codes[np.arange(400), amax]) == 127)
+    assert np.all(np.sign(codes) == np.where(np.abs(xv) < scales[:, None] / 2, 0, np.sign(xv)))
+
+
+def check_f64kv_attention_is_the_bf16_attention(lib):
+    # The double-cache attention on caches holding exactly the bf16 values is
+    # the bf16-cache attention, bit for bit.
+    q, k, v, lens, scale = _random_case(72, 3, 8, 2, 16, 10, [10, 3, 0])
+    out_a, lse_a = oracle.decode_attention(q, k, v, lens, scale, lib=lib)
+    out_b, lse_b = oracle.decode_attention_f64kv(q, _f64(k), _f64(v), lens, scale, lib=lib)
+    assert np.array_equal(out_a, out_b) and np.array_equal(lse_a, lse_b)
+
+
+def check_q8_attention_close_to_bf16(lib):
+    # Attention over the int8 rows stays within the quantization error of the
+    # bf16 attention: each row moves by at most half a step, and the output is
+    # a convex combination of value rows.
+    q, k, v, lens, scale = _random_case(73, 2, 4, 1, 64, 40, [40, 17])
+    kc, ks = oracle.quantize_q8(k, lib=lib)
+    vc, vs = oracle.quantize_q8(v, lib=lib)
+    out_q, _ = oracle.decode_attention_q8(q, kc, vc, ks, vs, lens, scale, lib=lib)
+    out_b, _ = oracle.decode_attention(q, k, v, lens, scale, lib=lib)
+    assert np.max(np.abs(out_q - out_b)) < 0.05
+    assert np.max(np.abs(out_q - out_b)) > 0.0
+
+
+def check_q8_append(lib):
+    r = np.random.default_rng(74)
+    B, S, Hkv, D = 3, 6, 2, 8
+    kc = r.integers(-127, 128, (B, S, Hkv, D), dtype=np.int8)
+    vc = r.integers(-127, 128, (B, S, Hkv, D), dtype=np.int8)
+    ks = r.random((B, S, Hkv)).astype(np.float32)
+    vs = r.random((B, S, Hkv)).astype(np.float32)
+    kn = _bits(r.standard_normal((B, Hkv, D)))
+    vn = _bits(r.standard_normal((B, Hkv, D)))
+    pos = np.array([0, 5, 6], np.int32)  # the last one is out of range
+    k2, v2, ks2, vs2, skipped = oracle.kv_append_q8(kc, vc, ks, vs, kn, vn, pos, lib=lib)
+    assert skipped == 1
+    ek, eks = oracle.quantize_q8(kn, lib=lib)
+    ev, evs = oracle.quantize_q8(vn, lib=lib)
+    want_k, want_ks = kc.copy(), ks.copy()
+    want_k[0, 0], want_k[1, 5], want_ks[0, 0], want_ks[1, 5] = ek[0], ek[1], eks[0], eks[1]
+    assert np.array_equal(k2, want_k) and np.array_equal(ks2, want_ks)
+    want_v, want_vs = vc.copy(), vs.copy()
+    want_v[0, 0], want_v[1, 5], want_vs[0, 0], want_vs[1, 5] = ev[0], ev[1], evs[0], evs[1]
+    assert np.array_equal(v2, want_v) and np.array_equal(vs2, want_vs)
+
+
 ALL_CHECKS = [
     check_identical_keys_give_mean_of_v,
     check_dominant_score_returns_that_row,
@@ -434,4 +513,9 @@ ALL_CHECKS = [
     check_paged_tiny_hand_example,
     check_paged_invalid_entry_reads_zero_rows,
     check_paged_append,
+    check_q8_closed_forms,
+    check_q8_error_bound,
+    check_f64kv_attention_is_the_bf16_attention,
+    check_q8_attention_close_to_bf16,
+    check_q8_append,
 ]

@@ -44,6 +44,14 @@ MUTANTS = [
      "if (page < 0) {\n                memset"),
     ("paged_append_wrong_row", "const size_t dst = (((size_t)page * P + (size_t)(t % P)) * Hkv + h) * (size_t)D;",
      "const size_t dst = (((size_t)page * P + (size_t)((t + 1) % P)) * Hkv + h) * (size_t)D;"),
+    ("q8_scale_over_128", "volatile float sc = a / 127.0f;", "volatile float sc = a / 128.0f;"),
+    ("q8_truncates", "c = (int)rintf(y);", "c = (int)y;"),
+    ("q8_rounds_half_away", "c = (int)rintf(y);", "c = (int)roundf(y);"),
+    ("q8_readback_drops_scale", "out[(size_t)r * D + d] = (double)scales[r] * (double)codes[(size_t)r * D + d];",
+     "out[(size_t)r * D + d] = (double)codes[(size_t)r * D + d];"),
+    ("f64kv_no_max_subtraction", "const double e = exp(w[t] - top);", "const double e = exp(w[t]);"),
+    ("f64kv_wrong_kv_head", "const int kvh = h / G;", "const int kvh = h % Hkv;"),
+    ("f64kv_scale_dropped", "w[t] = acc * scale;", "w[t] = acc;"),
     ("paged_append_ignores_bad_page", "if (page < 0 || page >= num_pages) { ++skipped; ++bad; continue; }",
      "if (page < 0) { ++skipped; ++bad; continue; }"),
 ]
