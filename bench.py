@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--page-size", type=int, default=0,
                     help="paged KV cache with pages of this many tokens; 0 = contiguous")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "int8"],
+                    help="int8: the cache quantized per (token, KV head) row (groups <= 16)")
     ap.add_argument("--page-order", default="shuffled", choices=["shuffled", "sequential"],
                     help="paged: pages in random order over the pool, or each sequence's pages in a row")
     return ap.parse_args()
@@ -267,8 +269,12 @@ def run_ours(args):
     S, Hkv = inp.k_cache.shape[1], inp.k_cache.shape[2]
     lens_np = inp.seq_lens
     max_len = int(w.S_max)
-    step_bytes = roofline.attention_step_bytes(lens_np, Hq, Hkv, D)
-    kv_bytes = roofline.attention_kv_bytes(lens_np, Hkv, D)
+    int8 = args.kv_dtype == "int8"
+    if int8 and args.page_size:
+        raise SystemExit("--kv-dtype int8 takes a contiguous cache")
+    step_bytes = (roofline.attention_step_bytes_q8(lens_np, Hq, Hkv, D) if int8
+                  else roofline.attention_step_bytes(lens_np, Hq, Hkv, D))
+    kv_bytes = roofline.attention_kv_bytes(lens_np, Hkv, D) // (2 if int8 else 1)
     append_bytes = roofline.append_bytes(B, Hkv, D)
     flops = roofline.attention_step_flops(lens_np, Hq, D)
 
@@ -296,6 +302,18 @@ def run_ours(args):
     for _ in range(R - 1):
         kcs.append(kc0.clone())
         vcs.append(vc0.clone())
+    if int8:
+        # int8 copies quantized on the GPU from the bf16 cache (its cached rows)
+        cached = torch.from_numpy(np.maximum(lens_np - 1, 0).astype(np.int32)).to(dev)
+        q8 = []
+        for kc_, vc_ in zip(kcs, vcs):
+            codes = [torch.zeros(kc_.shape, dtype=torch.int8, device=dev) for _ in range(2)]
+            scales = [torch.zeros(kc_.shape[:3], dtype=torch.float32, device=dev) for _ in range(2)]
+            kvd.kv_quantize_q8(kc_, codes[0], scales[0], cached, S)
+            kvd.kv_quantize_q8(vc_, codes[1], scales[1], cached, S)
+            q8.append((codes[0], codes[1], scales[0], scales[1]))
+        del kcs[1:], vcs[1:]
+        torch.cuda.synchronize()
     q, kn, vn = up(inp.q), up(inp.k_new), up(inp.v_new)
     pos = torch.from_numpy(inp.pos).to(dev)
     lens = torch.from_numpy(lens_np).to(dev)
@@ -307,7 +325,11 @@ def run_ours(args):
 
     def step(r, stream=None):
         # append the new token's K/V rows, then attend (one call, three launches)
-        if paged:
+        if int8:
+            kq, vq, ks, vs = q8[r]
+            kvd.decode_step_q8(q, kq, vq, ks, vs, kn, vn, pos, lens, max_len, w.scale, out, workspace=ws,
+                               n_split=args.n_split, stream=stream)
+        elif paged:
             kvd.decode_step_paged(q, kcs[r], vcs[r], kn, vn, pos, bt, lens, max_len, w.scale, out,
                                   workspace=ws, n_split=args.n_split, stream=stream)
         else:
@@ -362,6 +384,15 @@ def run_ours(args):
     torch.cuda._sleep(int(2e6 + 2e5 * args.steps))  # let the host queue ahead of the GPU
     for i in range(args.steps):
         r = i % R
+        if int8:
+            # no separate int8 chunk entry point: the whole attention call is timed
+            kq, vq, ks, vs = q8[r]
+            kvd.kv_append_q8(kq, vq, ks, vs, kn, vn, pos)
+            ea[i].record(stream)
+            kvd.decode_attention_q8(q, kq, vq, ks, vs, lens, max_len, w.scale, out, workspace=ws,
+                                    n_split=args.n_split)
+            eb[i].record(stream)
+            continue
         if paged:
             # no separate paged chunk entry point: the whole attention call is timed
             kvd.kv_append_paged(kcs[r], vcs[r], kn, vn, bt, pos)
@@ -435,9 +466,9 @@ def run_ours(args):
 
     peak, peak_kind = measured_peaks()
     achieved = step_bytes / (chunk_avg_ms * 1e-3) / 1e9
-    traffic = None if paged else ncu_traffic(w.name)
+    traffic = None if (paged or int8) else ncu_traffic(w.name)
     cpu = None
-    if not args.no_cpu_baseline:
+    if not args.no_cpu_baseline and not int8:
         gbs, sec, n_rows, cores, passes = oracle_rate(w, inp, budget_s=10.0, repeats=1,
                                                       min_total_s=10.0)
         cpu = {"value": round(gbs, 5), "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -456,13 +487,15 @@ def run_ours(args):
                                f"vs {l2 / 1e6:.0f} MB L2)",
                    "timing": "CUDA graph per step, CUDA events on the replay stream",
                    "kv_layout": (f"paged: {args.page_size}-token pages, {pinp.k_pages.shape[0]} pages "
-                                 f"in {args.page_order} order" if paged else "contiguous")},
+                                 f"in {args.page_order} order" if paged else "contiguous"),
+                   "kv_dtype": args.kv_dtype},
         "tokens_per_s": round(tokens_per_s, 1),
         "hbm_frac_of_step": round(value / world / peak, 4),
         "step_bytes": int(step_bytes), "append_bytes": int(append_bytes), "flops": int(flops),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "split_kv_chunk + split_kv_merge (paged)" if paged else "split_kv_chunk",
+                     "kernel": ("split_kv_chunk + split_kv_merge (int8)" if int8 else
+                                "split_kv_chunk + split_kv_merge (paged)" if paged else "split_kv_chunk"),
                      "peak_source": f"{peak_kind} copy bandwidth",
                      "kernel_ms": round(chunk_avg_ms, 5)},
         "gpu_launches": int(launches_per_step * args.steps),

@@ -224,6 +224,49 @@ kvd_status kvd_decode_step_paged(void* k_pages, void* v_pages, const void* k_new
                                  float* lse_out, int32_t* status_word, kvd_stream_t stream);
 
 /*
+ * int8 KV cache. The pages name quantizing the KV cache (int8, fp8, ...) as
+ * a way to cut the memory traffic of every generation step (All About
+ * Transformer Inference, "Tricks for improving generation throughput and
+ * latency", the quantization bullet) but give no scheme; this library's is
+ * symmetric absmax per (token, KV head) row:
+ *   a = max_d |x_d|, scale = a / 127, code_d = round-half-even(x_d / scale)
+ *   clamped to [-127, 127], both divisions IEEE float32 (a = 0: scale 0 and
+ *   codes 0); the row reads back as scale * code_d.
+ *   k_codes, v_codes   : int8 [batch, s_max, n_heads_kv, head_dim], 16-byte aligned
+ *   k_scales, v_scales : float32 [batch, s_max, n_heads_kv], 4-byte aligned
+ * kvd_kv_quantize_q8 converts rows t < seq_lens[b] (clamped to max_seq_len)
+ * of one bf16 cache (K or V) into codes and scales, leaving other rows
+ * untouched (a prefill's cache, say). kvd_kv_append_q8 quantizes the new
+ * token's rows and writes them at pos[b], as kvd_kv_append. The attention
+ * and step calls are kvd_decode_attention and kvd_decode_step over the rows
+ * read back: q stays bf16, the cache rows are exact small integers times
+ * their scale, and the kernels compute in f16 MMAs with fp32 accumulation,
+ * with each score multiplied by its key row's scale and each weight by its
+ * value row's scale. Groups of up to 16 query heads per KV head (the
+ * mma.sync kernel; wider groups return KVD_ERR_UNSUPPORTED); head_dim 64,
+ * 128 or 256; contiguous caches only. q must lie in f16's range (|q| <
+ * 65504). Workspace, results and errors otherwise as the bf16 calls, plus
+ * KVD_ERR_INVALID_ARG for null or misaligned scale arrays.
+ */
+kvd_status kvd_kv_quantize_q8(const void* cache, void* codes, float* scales, const int32_t* seq_lens, int batch,
+                              int s_max, int max_seq_len, int n_heads_kv, int head_dim, kvd_stream_t stream);
+kvd_status kvd_kv_append_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales, const void* k_new,
+                            const void* v_new, const int32_t* pos, int batch, int s_max, int n_heads_kv,
+                            int head_dim, int32_t* status_word, kvd_stream_t stream);
+kvd_status kvd_decode_attention_q8(const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
+                                   const float* v_scales, const int32_t* seq_lens, int batch, int s_max,
+                                   int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim, float scale,
+                                   int n_split, void* workspace, size_t workspace_bytes, void* out,
+                                   kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                                   kvd_stream_t stream);
+kvd_status kvd_decode_step_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales, const void* k_new,
+                              const void* v_new, const int32_t* pos, const void* q, const int32_t* seq_lens,
+                              int batch, int s_max, int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim,
+                              float scale, int n_split, void* workspace, size_t workspace_bytes, void* out,
+                              kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                              kvd_stream_t stream);
+
+/*
  * The two launches of kvd_decode_attention, exposed separately so that each
  * can be timed on its own. Arguments and errors are those of
  * kvd_decode_attention; calling kvd_split_kv_chunk then kvd_split_kv_merge on

@@ -30,7 +30,8 @@ EXPORTED = (
     "kvd_decode_plan", "kvd_kv_append", "kvd_decode_attention", "kvd_split_kv_chunk",
     "kvd_split_kv_merge", "kvd_schedule_describe", "kvd_kernel_info", "kvd_status_string",
     "kvd_version", "kvd_decode_attention_static", "kvd_decode_step", "kvd_kv_append_paged",
-    "kvd_decode_attention_paged", "kvd_decode_step_paged",
+    "kvd_decode_attention_paged", "kvd_decode_step_paged", "kvd_kv_quantize_q8", "kvd_kv_append_q8",
+    "kvd_decode_attention_q8", "kvd_decode_step_q8",
 )
 STATIC_WORKSPACE_BYTES = 16 << 20  # KVD_STATIC_WORKSPACE_BYTES
 
@@ -82,6 +83,15 @@ def _declare(lib):
     lib.kvd_decode_attention_paged.restype = I
     lib.kvd_decode_step_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I] + dec[6:]
     lib.kvd_decode_step_paged.restype = I
+    # int8: codes in place of the cache, plus the two scale arrays
+    lib.kvd_kv_quantize_q8.argtypes = [P, P, P, P, I, I, I, I, I, P]
+    lib.kvd_kv_quantize_q8.restype = I
+    lib.kvd_kv_append_q8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P, P]
+    lib.kvd_kv_append_q8.restype = I
+    lib.kvd_decode_attention_q8.argtypes = [P, P, P, P, P] + dec[3:]
+    lib.kvd_decode_attention_q8.restype = I
+    lib.kvd_decode_step_q8.argtypes = [P, P, P, P, P, P, P, P, P] + dec[4:]
+    lib.kvd_decode_step_q8.restype = I
     lib.kvd_schedule_describe.argtypes = [P, I, I, I, I, I, I, I, I, P, I, PI, PI]
     lib.kvd_kernel_info.argtypes = [I, I, I, I, PI, PI, PI, PI, PI, PI]
     lib.kvd_status_string.argtypes = [I]
@@ -360,6 +370,99 @@ def decode_step_paged(q, k_pages, v_pages, k_new, v_new, pos, block_table, seq_l
                                         v_new.data_ptr(), pos.data_ptr(), q.data_ptr(),
                                         block_table.data_ptr(), seq_lens.data_ptr(), *head, *tail),
            "kvd_decode_step_paged")
+
+
+def _q8_args(k_codes, v_codes, k_scales, v_scales):
+    import torch
+    _require(k_codes, "k_codes", torch.int8, 4)
+    _require(v_codes, "v_codes", torch.int8, 4)
+    _require(k_scales, "k_scales", torch.float32, 3)
+    _require(v_scales, "v_scales", torch.float32, 3)
+    if v_codes.shape != k_codes.shape or k_scales.shape != k_codes.shape[:3] or v_scales.shape != k_scales.shape:
+        raise ValueError("int8 cache: codes [B, S_max, Hkv, D] and scales [B, S_max, Hkv] disagree")
+
+
+def kv_quantize_q8(cache, codes, scales, seq_lens, max_seq_len: int, stream=None):
+    """codes/scales of rows t < seq_lens[b] of a bf16 cache [B, S_max, Hkv, D]."""
+    import torch
+    _require(cache, "cache", torch.bfloat16, 4)
+    _require(codes, "codes", torch.int8, 4)
+    _require(scales, "scales", torch.float32, 3)
+    _require(seq_lens, "seq_lens", torch.int32, 1)
+    B, S, Hkv, D = cache.shape
+    if codes.shape != cache.shape or scales.shape != (B, S, Hkv) or seq_lens.shape != (B,):
+        raise ValueError("kv_quantize_q8: inconsistent shapes")
+    _check(load().kvd_kv_quantize_q8(cache.data_ptr(), codes.data_ptr(), scales.data_ptr(), seq_lens.data_ptr(),
+                                     B, S, int(max_seq_len), Hkv, D, _stream_handle(stream)), "kvd_kv_quantize_q8")
+
+
+def kv_append_q8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, status=None, stream=None):
+    """The new bf16 rows quantized and written at pos[b] of the int8 cache."""
+    import torch
+    _q8_args(k_codes, v_codes, k_scales, v_scales)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _require(t, n, torch.bfloat16, 3)
+    _require(pos, "pos", torch.int32, 1)
+    B, S, Hkv, D = k_codes.shape
+    if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or pos.shape != (B,):
+        raise ValueError("kv_append_q8: inconsistent shapes")
+    _check(load().kvd_kv_append_q8(k_codes.data_ptr(), v_codes.data_ptr(), k_scales.data_ptr(),
+                                   v_scales.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), pos.data_ptr(), B, S,
+                                   Hkv, D, _ptr(status), _stream_handle(stream)), "kvd_kv_append_q8")
+
+
+def _decode_q8_args(q, k_codes, v_codes, k_scales, v_scales, seq_lens, max_seq_len, scale, n_split, workspace,
+                    out, lse, status, stream):
+    """(seq_lens pointer, batch, s_max, ...) as for kvd_decode_attention, after the int8 cache."""
+    import torch
+    _q8_args(k_codes, v_codes, k_scales, v_scales)
+    _require(q, "q", torch.bfloat16, 3)
+    _require(seq_lens, "seq_lens", torch.int32, 1)
+    _require(out, "out", None, 3)
+    B, Hq, D = q.shape
+    _, S, Hkv, Dk = k_codes.shape
+    if k_codes.shape[0] != B or Dk != D or seq_lens.shape != (B,) or out.shape != (B, Hq, D):
+        raise ValueError("decode_attention_q8: inconsistent shapes")
+    if out.dtype == torch.bfloat16:
+        code = OUT_BF16
+    elif out.dtype == torch.float32:
+        code = OUT_F32
+    else:
+        raise TypeError("out must be bfloat16 or float32")
+    if lse is not None:
+        _require(lse, "lse", torch.float32, 2)
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(),
+                                                           workspace.numel() * workspace.element_size())
+    return [seq_lens.data_ptr(), B, S, int(max_seq_len), Hq, Hkv, D, float(scale), int(n_split), ws_ptr, ws_bytes,
+            out.data_ptr(), code, _ptr(lse), _ptr(status), _stream_handle(stream)]
+
+
+def decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, seq_lens, max_seq_len: int, scale: float, out,
+                        workspace=None, n_split: int = 0, lse=None, status=None, stream=None):
+    """decode_attention over an int8 cache (codes [B, S_max, Hkv, D] int8, scales
+    [B, S_max, Hkv] float32; a row reads back as scale * code). Groups <= 16."""
+    tail = _decode_q8_args(q, k_codes, v_codes, k_scales, v_scales, seq_lens, max_seq_len, scale, n_split,
+                           workspace, out, lse, status, stream)
+    _check(load().kvd_decode_attention_q8(q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(),
+                                          k_scales.data_ptr(), v_scales.data_ptr(), *tail),
+           "kvd_decode_attention_q8")
+
+
+def decode_step_q8(q, k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, seq_lens, max_seq_len: int,
+                   scale: float, out, workspace=None, n_split: int = 0, lse=None, status=None, stream=None):
+    """kv_append_q8 then decode_attention_q8 as one call (kvd_decode_step_q8)."""
+    import torch
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _require(t, n, torch.bfloat16, 3)
+    _require(pos, "pos", torch.int32, 1)
+    B, S, Hkv, D = k_codes.shape
+    if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or pos.shape != (B,):
+        raise ValueError("decode_step_q8: inconsistent shapes")
+    tail = _decode_q8_args(q, k_codes, v_codes, k_scales, v_scales, seq_lens, max_seq_len, scale, n_split,
+                           workspace, out, lse, status, stream)
+    _check(load().kvd_decode_step_q8(k_codes.data_ptr(), v_codes.data_ptr(), k_scales.data_ptr(),
+                                     v_scales.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), pos.data_ptr(),
+                                     q.data_ptr(), *tail), "kvd_decode_step_q8")
 
 
 def decode_step(q, k_cache, v_cache, k_new, v_new, pos, seq_lens, max_seq_len: int, scale: float,

@@ -10,24 +10,26 @@
 
 namespace kvd {
 
-const ChunkKernel* mma_table_d64(bool f32, bool paged);
-const ChunkKernel* mma_table_d128(bool f32, bool paged);
-const ChunkKernel* mma_table_d256(bool f32, bool paged);
+const ChunkKernel* mma_table_d64(bool f32, bool paged, bool kv8);
+const ChunkKernel* mma_table_d128(bool f32, bool paged, bool kv8);
+const ChunkKernel* mma_table_d256(bool f32, bool paged, bool kv8);
 
-const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged) {
+const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool kv8) {
     switch (head_dim) {
-        case 64: return mma_table_d64(f32_out, paged);
-        case 128: return mma_table_d128(f32_out, paged);
-        case 256: return mma_table_d256(f32_out, paged);
+        case 64: return mma_table_d64(f32_out, paged, kv8);
+        case 128: return mma_table_d128(f32_out, paged, kv8);
+        case 256: return mma_table_d256(f32_out, paged, kv8);
         default: return nullptr;
     }
 }
 
 // The tcgen05 kernels take either cache form at run time (only their loads
 // differ); the mma.sync kernel has a compiled variant per form.
-const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged) {
+// int8 caches run on the mma.sync kernel only (groups of up to 16).
+const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8) {
     if (group < 1 || group > KVD_MAX_GROUP) return nullptr;
-    return group <= 16 ? mma_chunk_kernel(head_dim, f32_out, paged) : tc_chunk_kernel(head_dim, f32_out, group);
+    if (kv8) return (group <= 16 && !paged) ? mma_chunk_kernel(head_dim, f32_out, false, true) : nullptr;
+    return group <= 16 ? mma_chunk_kernel(head_dim, f32_out, paged, false) : tc_chunk_kernel(head_dim, f32_out, group);
 }
 
 namespace {
@@ -52,9 +54,15 @@ kvd_status check_shape(int batch, int Hq, int Hkv, int D, kvd_out_dtype dt) {
 
 // Both forms of a variant share their launch shape and schedule geometry, so
 // planning and the host replica use the contiguous one.
-const ChunkKernel* pick_kernel(int Hq, int Hkv, int D, kvd_out_dtype dt, bool paged = false) {
-    return find_chunk_kernel(D, Hq / Hkv, dt == KVD_OUT_F32, paged);
+const ChunkKernel* pick_kernel(int Hq, int Hkv, int D, kvd_out_dtype dt, bool paged = false, bool kv8 = false) {
+    return find_chunk_kernel(D, Hq / Hkv, dt == KVD_OUT_F32, paged, kv8);
 }
+
+// int8 cache: the row scales of K and V.
+struct QuantCache {
+    float* k_scale;
+    float* v_scale;
+};
 
 // Paged cache arguments, checked; s_max of the contiguous calls becomes
 // max_blocks * page_size.
@@ -151,7 +159,8 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
                   const int32_t* seq_lens, int batch, int s_max, int max_seq_len, int Hq, int Hkv,
                   int D, float scale, int n_split_req, void* workspace, size_t workspace_bytes,
                   void* out, kvd_out_dtype dt, float* lse, int32_t* status, kvd_stream_t stream,
-                  const AppendArgs* app = nullptr, const PagedCache* pg = nullptr) {
+                  const AppendArgs* app = nullptr, const PagedCache* pg = nullptr,
+                  const QuantCache* q8 = nullptr) {
     kvd_status st = check_shape(batch, Hq, Hkv, D, dt);
     if (st != KVD_OK) return st;
     if (s_max <= 0 || max_seq_len < 0 || max_seq_len > s_max) return KVD_ERR_INVALID_ARG;
@@ -174,6 +183,11 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
               &n_split, &need, &k);
     if (st != KVD_OK) return st;
     if (pg) k = pick_kernel(Hq, Hkv, D, dt, true);
+    if (q8) {
+        if (!q8->k_scale || !q8->v_scale || !aligned(q8->k_scale, 4) || !aligned(q8->v_scale, 4))
+            return KVD_ERR_INVALID_ARG;
+        k = pick_kernel(Hq, Hkv, D, dt, false, true);
+    }
     if (!k) return KVD_ERR_UNSUPPORTED;
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return KVD_ERR_WORKSPACE_TOO_SMALL;
@@ -201,6 +215,10 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     p.out = out;
     p.lse = lse;
     p.status = status;
+    if (q8) {
+        p.k_scale = q8->k_scale;
+        p.v_scale = q8->v_scale;
+    }
     if (pg) {
         p.block_table = pg->block_table;
         p.max_blocks = pg->max_blocks;
@@ -221,9 +239,12 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
         // out its schedule) while the append runs, and only its cache loads
         // wait for the append's grid.
         const PagedCache none{nullptr, 0, 0, 0};
-        if (launch_append(app->k_cache, app->v_cache, app->k_new, app->v_new, app->pos, batch, s_max, Hkv, D,
-                          status, pg ? *pg : none, s) != cudaSuccess)
-            return KVD_ERR_CUDA;
+        const cudaError_t e =
+            q8 ? launch_append_q8(app->k_cache, app->v_cache, q8->k_scale, q8->v_scale, app->k_new, app->v_new,
+                                  app->pos, batch, s_max, Hkv, D, status, s)
+               : launch_append(app->k_cache, app->v_cache, app->k_new, app->v_new, app->pos, batch, s_max, Hkv,
+                               D, status, pg ? *pg : none, s);
+        if (e != cudaSuccess) return KVD_ERR_CUDA;
         p.early = 1;
         p.pos = app->pos;
     }
@@ -274,6 +295,63 @@ kvd_status kvd_kv_append(void* k_cache, void* v_cache, const void* k_new, const 
                          status_word, none, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? KVD_OK
                : KVD_ERR_CUDA;
+}
+
+kvd_status kvd_kv_quantize_q8(const void* cache, void* codes, float* scales, const int32_t* seq_lens, int batch,
+                              int s_max, int max_seq_len, int n_heads_kv, int head_dim, kvd_stream_t stream) {
+    if (batch < 0 || s_max <= 0 || max_seq_len < 0 || max_seq_len > s_max || n_heads_kv <= 0) return KVD_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVD_ERR_UNSUPPORTED;
+    if (!cache || !codes || !scales || !seq_lens || !aligned(cache, 16) || !aligned(codes, 16) ||
+        !aligned(scales, 4) || !aligned(seq_lens, 4))
+        return KVD_ERR_INVALID_ARG;
+    if (batch == 0) return KVD_OK;
+    return launch_quantize_q8(cache, codes, scales, seq_lens, batch, s_max, max_seq_len, n_heads_kv, head_dim,
+                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KVD_OK
+               : KVD_ERR_CUDA;
+}
+
+kvd_status kvd_kv_append_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales, const void* k_new,
+                            const void* v_new, const int32_t* pos, int batch, int s_max, int n_heads_kv,
+                            int head_dim, int32_t* status_word, kvd_stream_t stream) {
+    kvd_status st = check_append(k_codes, v_codes, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim,
+                                 status_word);
+    if (st != KVD_OK) return st;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVD_ERR_UNSUPPORTED;
+    if (!k_scales || !v_scales || !aligned(k_scales, 4) || !aligned(v_scales, 4)) return KVD_ERR_INVALID_ARG;
+    if (batch == 0) return KVD_OK;
+    return launch_append_q8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, batch, s_max, n_heads_kv,
+                            head_dim, status_word, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KVD_OK
+               : KVD_ERR_CUDA;
+}
+
+kvd_status kvd_decode_attention_q8(const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
+                                   const float* v_scales, const int32_t* seq_lens, int batch, int s_max,
+                                   int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim, float scale,
+                                   int n_split, void* workspace, size_t workspace_bytes, void* out,
+                                   kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                                   kvd_stream_t stream) {
+    const QuantCache q8{const_cast<float*>(k_scales), const_cast<float*>(v_scales)};
+    return decode(kBoth, q, k_codes, v_codes, seq_lens, batch, s_max, max_seq_len, n_heads_q, n_heads_kv,
+                  head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype, lse_out, status_word,
+                  stream, nullptr, nullptr, &q8);
+}
+
+kvd_status kvd_decode_step_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales, const void* k_new,
+                              const void* v_new, const int32_t* pos, const void* q, const int32_t* seq_lens,
+                              int batch, int s_max, int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim,
+                              float scale, int n_split, void* workspace, size_t workspace_bytes, void* out,
+                              kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                              kvd_stream_t stream) {
+    const kvd_status st = check_append(k_codes, v_codes, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim,
+                                       status_word);
+    if (st != KVD_OK) return st;
+    const AppendArgs app{k_codes, v_codes, k_new, v_new, pos};
+    const QuantCache q8{k_scales, v_scales};
+    return decode(kBoth, q, k_codes, v_codes, seq_lens, batch, s_max, max_seq_len, n_heads_q, n_heads_kv,
+                  head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype, lse_out, status_word,
+                  stream, &app, nullptr, &q8);
 }
 
 kvd_status kvd_kv_append_paged(void* k_pages, void* v_pages, const void* k_new, const void* v_new,

@@ -34,6 +34,10 @@ struct DecodeParams {
     // give zero rows and KVD_STATUS_BAD_PAGE.
     const int32_t* block_table;
     int max_blocks, page_shift, num_pages;
+    // int8 cache (k_scale non-null): k and v hold int8 codes, and row (b, t, h)
+    // reads back as k_scale[(b * S_max + t) * Hkv + h] * code (v likewise).
+    const float* k_scale;
+    const float* v_scale;
 };
 
 // One compiled variant of the split-KV chunk kernel.
@@ -44,13 +48,13 @@ struct ChunkKernel {
     int seg_unit;    // tokens per schedule position (1 or tile_tokens, see schedule.cuh)
     int seg_cost;    // positions charged per pair by the schedule
     bool f32_out, tensor_core;
-    int index;  // position in the variant table (0..29), for the per-device attribute bitmask
+    int index;  // position in the variant table (0..41), for the per-device attribute bitmask
 };
 
 // The kernel for a shape: groups of up to 16 query heads per KV head run on the
 // mma.sync kernel, wider groups (17..64) on the tcgen05 kernel.
-const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged);
-const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged);
+const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8 = false);
+const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool kv8);
 const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out, int group);
 
 cudaError_t launch_merge(const DecodeParams& p, int head_dim, bool f32_out, int num_sms, cudaStream_t stream);
@@ -63,5 +67,12 @@ struct PagedCache {
 cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                           const int32_t* pos, int B, int S_max, int Hkv, int D,
                           int32_t* status, const PagedCache& pg, cudaStream_t stream);
+// int8 cache (kv_quant.cu): the append quantizes the new rows; the bulk
+// conversion quantizes rows t < seq_lens[b] of a bf16 cache.
+cudaError_t launch_append_q8(void* k_codes, void* v_codes, float* k_scale, float* v_scale, const void* k_new,
+                             const void* v_new, const int32_t* pos, int B, int S_max, int Hkv, int D,
+                             int32_t* status, cudaStream_t stream);
+cudaError_t launch_quantize_q8(const void* src, void* codes, float* scales, const int32_t* seq_lens, int B,
+                               int S_max, int len_cap, int Hkv, int D, cudaStream_t stream);
 
 }  // namespace kvd

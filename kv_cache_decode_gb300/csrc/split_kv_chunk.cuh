@@ -123,7 +123,7 @@ __device__ __forceinline__ void block_min_int_ll(int& vi, long long& vl, int* sh
     __syncthreads();
 }
 
-template <int D, int HT, int TS, int TT, int STAGES>
+template <int D, int HT, int TS, int TT, int STAGES, bool KV8 = false>
 struct ChunkShape {
     static constexpr int NW = HT * TS;
     static constexpr int NT = NW * 32;
@@ -133,25 +133,37 @@ struct ChunkShape {
     static constexpr int ND = D / 8;    // output n-tiles (8 columns each)
     static constexpr int CH = D / 8;    // 16-byte chunks per K/V row
     static constexpr int TILE_ELEMS = TT * D;
-    static constexpr int STAGE_BYTES = 2 * TILE_ELEMS * 2;
+    // A stage holds a tile's K and V rows: bf16, or (KV8) int8 codes followed
+    // by the tile's float32 K and V row scales. The int8 tiles are converted to
+    // f16 in CONV_BYTES, laid out like a bf16 stage, which the MMAs read.
+    static constexpr int STAGE_BYTES = KV8 ? 2 * TILE_ELEMS + 2 * TT * 4 : 2 * TILE_ELEMS * 2;
+    static constexpr int CONV_BYTES = KV8 ? 2 * TILE_ELEMS * 2 : 0;
     static constexpr int MB_FLOATS_PER_WARP = (ND * 4 + 4) * 32;
     // The token slices are merged at the end of a segment through the stage of
-    // the segment's last tile, which every warp has finished reading by then.
+    // the segment's last tile (KV8: the conversion buffer), which every warp
+    // has finished reading by then.
     static constexpr int MB_BYTES = (TS - 1) * HT * MB_FLOATS_PER_WARP * 4;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + CONV_BYTES;
     // Schedule: runs balanced in tokens (the kernel is bandwidth-bound, so a
     // short tile costs less than a full one), no charge per pair (a new pair's
     // queries come from L2 while the previous tiles are still in flight).
     static constexpr int SEG_UNIT = 1;
     static constexpr int SEG_COST = 0;
-    static_assert(MB_BYTES <= STAGE_BYTES, "warp-merge data must fit in one stage");
+    static_assert(MB_BYTES <= (KV8 ? CONV_BYTES : STAGE_BYTES), "warp-merge data must fit in one stage");
+    static_assert(STAGE_BYTES % 128 == 0, "stage alignment");
     static_assert(TW % 16 == 0, "each warp needs whole 16-token k-steps");
     static_assert(D % 16 == 0 && D >= 64, "head_dim");
 };
 
-template <int D, int HT, int TS, int TT, int STAGES, bool F32OUT, int MINB, bool PAGED>
+// KV8: the cache holds int8 codes with a float32 scale per (token, KV head)
+// row; K and V tiles are converted to f16 in shared memory (exactly: the codes
+// are small integers), q is taken to f16, the MMAs run in f16, each score is
+// multiplied by its key row's scale and each weight by its value row's scale
+// before P V.
+template <int D, int HT, int TS, int TT, int STAGES, bool F32OUT, int MINB, bool PAGED, bool KV8 = false>
 __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const DecodeParams p) {
-    using Sh = ChunkShape<D, HT, TS, TT, STAGES>;
+    static_assert(!(PAGED && KV8), "paged int8 caches are not built");
+    using Sh = ChunkShape<D, HT, TS, TT, STAGES, KV8>;
     constexpr int NW = Sh::NW, NT = Sh::NT, TW = Sh::TW, NS = Sh::NS, KS = Sh::KS,
                   ND = Sh::ND, CH = Sh::CH, TILE_ELEMS = Sh::TILE_ELEMS, SEG_COST = Sh::SEG_COST;
 
@@ -262,7 +274,31 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
         const int nvalid = t.tok_hi - t.tok_lo;
         const uint32_t sbase = smem_u32(stages) + stage * Sh::STAGE_BYTES;
         const int ch = tid % CH, r0 = tid / CH;
-        if constexpr (!PAGED) {
+        if constexpr (KV8) {
+            // int8 rows: D / 16 chunks of 16 bytes each, unswizzled; then the
+            // tile's row scales, one 4-byte copy per row and tensor.
+            constexpr int CH8 = D / 16, RSTEP8 = NT / CH8, RPT8 = TT / RSTEP8;
+            static_assert(NT % CH8 == 0 && TT % RSTEP8 == 0 && NT >= 2 * TT, "int8 row split");
+            const size_t row0 = ((size_t)t.b * p.S_max + t.tok_lo) * p.Hkv + t.h;
+            const int c8 = tid % CH8, q0 = tid / CH8;
+            const int8_t* kb = reinterpret_cast<const int8_t*>(p.k) + row0 * D + c8 * 16;
+            const int8_t* vb = reinterpret_cast<const int8_t*>(p.v) + row0 * D + c8 * 16;
+#pragma unroll
+            for (int k = 0; k < RPT8; ++k) {
+                const int r = q0 + k * RSTEP8;
+                const bool ok = r < nvalid;
+                const size_t off = ok ? (size_t)r * row_stride : 0;
+                const uint32_t dst = sbase + (uint32_t)(r * D + c8 * 16);
+                cp_async_16(dst, kb + off, ok ? 16 : 0, policy);
+                cp_async_16(dst + TILE_ELEMS, vb + off, ok ? 16 : 0, policy);
+            }
+            if (tid < 2 * TT) {
+                const int r = tid % TT;
+                const float* sc = (tid < TT ? p.k_scale : p.v_scale) + row0 + (size_t)r * p.Hkv;
+                const bool ok = r < nvalid;
+                cp_async_4(sbase + 2 * TILE_ELEMS + tid * 4, ok ? sc : p.k_scale, ok ? 4 : 0);
+            }
+        } else if constexpr (!PAGED) {
             const size_t row0 = ((size_t)t.b * p.S_max + t.tok_lo) * p.Hkv + t.h;
             const __nv_bfloat16* kb = Kg + row0 * D + ch * 8;
             const __nv_bfloat16* vb = Vg + row0 * D + ch * 8;
@@ -388,6 +424,10 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                 qf[kk][1] = v1 ? __ldg(q1 + w) : 0u;
                 qf[kk][2] = v0 ? __ldg(q0 + w + 4) : 0u;
                 qf[kk][3] = v1 ? __ldg(q1 + w + 4) : 0u;
+                if constexpr (KV8) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) qf[kk][e] = bf16x2_to_f16x2(qf[kk][e]);
+                }
             }
             m0 = m1 = -CUDART_INF_F;
             l0 = l1 = 0.f;
@@ -398,7 +438,37 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
         const int nvalid = ct.tok_hi - ct.tok_lo;
         const int wbase = ts * TW;
         if (wbase < nvalid) {
-            const uint32_t kbase = smem_u32(stages) + stage * Sh::STAGE_BYTES;
+            uint32_t kbase = smem_u32(stages) + stage * Sh::STAGE_BYTES;
+            const float* kscale = nullptr;
+            const float* vscale = nullptr;
+            if constexpr (KV8) {
+                // This warp's TW rows of K and V, int8 -> f16, into the
+                // conversion buffer in the bf16 stage layout (16-byte chunk c
+                // of row r at chunk c ^ (r & 7)). Only this warp reads them.
+                const uint8_t* st8 = smem + stage * Sh::STAGE_BYTES;
+                const uint32_t conv = smem_u32(smem) + STAGES * Sh::STAGE_BYTES;
+                constexpr int CH8 = D / 16;
+#pragma unroll
+                for (int i = lane; i < 2 * TW * CH8; i += 32) {
+                    const int kv = i / (TW * CH8), rr = (i / CH8) % TW, c8 = i % CH8;
+                    const int r = wbase + rr;
+                    const uint4 w = *reinterpret_cast<const uint4*>(st8 + kv * TILE_ELEMS + r * D + c8 * 16);
+                    uint4 a, b;
+                    i8x4_to_f16x2x2(w.x, a.x, a.y);
+                    i8x4_to_f16x2x2(w.y, a.z, a.w);
+                    i8x4_to_f16x2x2(w.z, b.x, b.y);
+                    i8x4_to_f16x2x2(w.w, b.z, b.w);
+                    const uint32_t rowb = conv + (uint32_t)(kv * TILE_ELEMS * 2 + r * D * 2);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(rowb + (uint32_t)((((2 * c8) ^ (r & 7)) * 8) * 2)),
+                                 "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w));
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(rowb + (uint32_t)((((2 * c8 + 1) ^ (r & 7)) * 8) * 2)),
+                                 "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w));
+                }
+                __syncwarp();
+                kbase = conv;
+                kscale = reinterpret_cast<const float*>(st8 + 2 * TILE_ELEMS);
+                vscale = kscale + TT;
+            }
             const uint32_t vbase = kbase + TILE_ELEMS * 2;
 
             // S = q K^T over this warp's TW tokens, as two independent accumulation
@@ -416,11 +486,11 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                     uint32_t b0, b1, b2, b3;
                     ldmatrix_x4(kbase + (uint32_t)((row * D + ((ch ^ (row & 7)) * 8)) * 2), b0, b1, b2, b3);
                     if (kk & 1) {
-                        mma_bf16_16816(s2[2 * n2], qf[kk], b0, b1);
-                        mma_bf16_16816(s2[2 * n2 + 1], qf[kk], b2, b3);
+                        mma_16816<KV8>(s2[2 * n2], qf[kk], b0, b1);
+                        mma_16816<KV8>(s2[2 * n2 + 1], qf[kk], b2, b3);
                     } else {
-                        mma_bf16_16816(s[2 * n2], qf[kk], b0, b1);
-                        mma_bf16_16816(s[2 * n2 + 1], qf[kk], b2, b3);
+                        mma_16816<KV8>(s[2 * n2], qf[kk], b0, b1);
+                        mma_16816<KV8>(s[2 * n2 + 1], qf[kk], b2, b3);
                     }
                 }
             }
@@ -436,7 +506,9 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const int tok = wbase + j * 8 + (lane & 3) * 2 + (e & 1);
-                    s[j][e] = (tok < nvalid) ? s[j][e] * scale_log2 : -CUDART_INF_F;
+                    float sc = scale_log2;
+                    if constexpr (KV8) sc *= kscale[tok];
+                    s[j][e] = (tok < nvalid) ? s[j][e] * sc : -CUDART_INF_F;
                 }
                 mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
                 mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
@@ -461,6 +533,22 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
             for (int j = 0; j < NS; ++j) {
                 const float e0 = exp2f(s[j][0] - mu0), e1 = exp2f(s[j][1] - mu0);
                 const float e2 = exp2f(s[j][2] - mu1), e3 = exp2f(s[j][3] - mu1);
+                if constexpr (KV8) {
+                    // Weights times the value rows' scales, in f16; the sums
+                    // take the weights themselves.
+                    const int tok = wbase + j * 8 + (lane & 3) * 2;
+                    const float w0 = vscale[tok], w1 = vscale[tok + 1];
+                    const uint32_t h01 = pack_f16x2(e0 * w0, e1 * w1), h23 = pack_f16x2(e2 * w0, e3 * w1);
+                    pa[j >> 1][(j & 1) * 2 + 0] = h01;
+                    pa[j >> 1][(j & 1) * 2 + 1] = h23;
+                    if constexpr (F32OUT) {
+                        pl[j >> 1][(j & 1) * 2 + 0] = pack_f16x2(e0 * w0 - f16_lo(h01), e1 * w1 - f16_hi(h01));
+                        pl[j >> 1][(j & 1) * 2 + 1] = pack_f16x2(e2 * w0 - f16_lo(h23), e3 * w1 - f16_hi(h23));
+                    }
+                    ls0 += e0 + e1;
+                    ls1 += e2 + e3;
+                    continue;
+                }
                 const uint32_t h01 = pack_bf16x2(e0, e1), h23 = pack_bf16x2(e2, e3);
                 pa[j >> 1][(j & 1) * 2 + 0] = h01;
                 pa[j >> 1][(j & 1) * 2 + 1] = h23;
@@ -497,11 +585,11 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                     const int ch = n2 * 2 + ((lane >> 4) & 1);
                     uint32_t v0, v1, v2, v3;
                     ldmatrix_x4_trans(vbase + (uint32_t)((row * D + ((ch ^ (row & 7)) * 8)) * 2), v0, v1, v2, v3);
-                    mma_bf16_16816(o[2 * n2], pa[k2], v0, v1);
-                    mma_bf16_16816(o[2 * n2 + 1], pa[k2], v2, v3);
+                    mma_16816<KV8>(o[2 * n2], pa[k2], v0, v1);
+                    mma_16816<KV8>(o[2 * n2 + 1], pa[k2], v2, v3);
                     if constexpr (F32OUT) {
-                        mma_bf16_16816(o[2 * n2], pl[k2], v0, v1);
-                        mma_bf16_16816(o[2 * n2 + 1], pl[k2], v2, v3);
+                        mma_16816<KV8>(o[2 * n2], pl[k2], v0, v1);
+                        mma_16816<KV8>(o[2 * n2 + 1], pl[k2], v2, v3);
                     }
                 }
             }
@@ -515,7 +603,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
             l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
 
             if constexpr (TS > 1) {
-                float* mbuf = reinterpret_cast<float*>(smem + stage * Sh::STAGE_BYTES);
+                float* mbuf = reinterpret_cast<float*>(smem + (KV8 ? STAGES * Sh::STAGE_BYTES : stage * Sh::STAGE_BYTES));
                 __syncthreads();  // every warp is done with this stage's K/V rows
                 if (ts > 0) {
                     float* mb = mbuf + ((ts - 1) * HT + ht) * Sh::MB_FLOATS_PER_WARP;

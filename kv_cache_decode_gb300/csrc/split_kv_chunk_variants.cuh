@@ -20,11 +20,17 @@ struct ChunkConfig {
     // of it is reserved per CTA); __launch_bounds__ then caps registers to match.
     static constexpr int SMEM = ChunkShape<D, HT, TS, TT, STAGES>::SMEM_BYTES;
     static constexpr int MINB = (2 * (SMEM + 1024) <= 228 * 1024) ? 2 : 1;
+    // int8 cache: stages of int8 tiles (half the bytes, so more of them) and
+    // one f16 conversion buffer, with the same CTAs per SM.
+    static constexpr int STAGES8 = (D == 64) ? 8 : 4;
+    static constexpr int SMEM8 = ChunkShape<D, HT, TS, TT, STAGES8, true>::SMEM_BYTES;
+    static constexpr int MINB8 = (2 * (SMEM8 + 1024) <= 228 * 1024) ? 2 : 1;
 };
 
-template <int D, bool F32, bool PAGED>
+template <int D, bool F32, bool PAGED, bool KV8>
 cudaError_t launch_mma_chunk(const ChunkKernel& k, const DecodeParams& p, cudaStream_t stream) {
     using C = ChunkConfig<D, 1>;
+    constexpr int ST = KV8 ? C::STAGES8 : C::STAGES, MB = KV8 ? C::MINB8 : C::MINB;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)p.n_split, 1, 1);
     cfg.blockDim = dim3((unsigned)k.threads, 1, 1);
@@ -35,21 +41,22 @@ cudaError_t launch_mma_chunk(const ChunkKernel& k, const DecodeParams& p, cudaSt
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kv_chunk_kernel<D, 1, C::TS, C::TT, C::STAGES, F32, C::MINB, PAGED>, p);
+    return cudaLaunchKernelEx(&cfg, split_kv_chunk_kernel<D, 1, C::TS, C::TT, ST, F32, MB, PAGED, KV8>, p);
 }
 
-template <int D, bool F32, bool PAGED>
+template <int D, bool F32, bool PAGED, bool KV8 = false>
 inline ChunkKernel make_mma_chunk_kernel(int index) {
     using C = ChunkConfig<D, 1>;
-    using Sh = ChunkShape<D, 1, C::TS, C::TT, C::STAGES>;
+    constexpr int ST = KV8 ? C::STAGES8 : C::STAGES, MB = KV8 ? C::MINB8 : C::MINB;
+    using Sh = ChunkShape<D, 1, C::TS, C::TT, ST, KV8>;
     ChunkKernel k;
-    k.fn = reinterpret_cast<const void*>(split_kv_chunk_kernel<D, 1, C::TS, C::TT, C::STAGES, F32, C::MINB, PAGED>);
-    k.launch = launch_mma_chunk<D, F32, PAGED>;
+    k.fn = reinterpret_cast<const void*>(split_kv_chunk_kernel<D, 1, C::TS, C::TT, ST, F32, MB, PAGED, KV8>);
+    k.launch = launch_mma_chunk<D, F32, PAGED, KV8>;
     k.head_dim = D;
     k.threads = Sh::NT;
     k.smem_bytes = Sh::SMEM_BYTES;
     k.tile_tokens = C::TT;
-    k.ctas_per_sm = C::MINB;
+    k.ctas_per_sm = MB;
     k.seg_unit = Sh::SEG_UNIT;
     k.seg_cost = Sh::SEG_COST;
     k.f32_out = F32;
@@ -58,14 +65,16 @@ inline ChunkKernel make_mma_chunk_kernel(int index) {
     return k;
 }
 
-// Variants of one head dimension: contiguous cache at indices IDX, IDX + 1,
-// paged cache at PIDX, PIDX + 1 (bf16 and fp32 output).
-#define KVD_MMA_TABLE(D, IDX, PIDX)                                                               \
-    const ChunkKernel* mma_table_d##D(bool f32, bool paged) {                                    \
-        static const ChunkKernel table[2][2] = {                                                 \
+// Variants of one head dimension: contiguous bf16 cache at indices IDX,
+// IDX + 1, paged at PIDX, PIDX + 1, int8 at QIDX, QIDX + 1 (bf16 and fp32 output).
+#define KVD_MMA_TABLE(D, IDX, PIDX, QIDX)                                                         \
+    const ChunkKernel* mma_table_d##D(bool f32, bool paged, bool kv8) {                          \
+        static const ChunkKernel table[3][2] = {                                                 \
             {make_mma_chunk_kernel<D, false, false>(IDX), make_mma_chunk_kernel<D, true, false>(IDX + 1)}, \
-            {make_mma_chunk_kernel<D, false, true>(PIDX), make_mma_chunk_kernel<D, true, true>(PIDX + 1)}}; \
-        return &table[paged ? 1 : 0][f32 ? 1 : 0];                                               \
+            {make_mma_chunk_kernel<D, false, true>(PIDX), make_mma_chunk_kernel<D, true, true>(PIDX + 1)}, \
+            {make_mma_chunk_kernel<D, false, false, true>(QIDX),                                 \
+             make_mma_chunk_kernel<D, true, false, true>(QIDX + 1)}};                            \
+        return &table[kv8 ? 2 : (paged ? 1 : 0)][f32 ? 1 : 0];                                   \
     }
 
 }  // namespace kvd

@@ -52,6 +52,14 @@ def attention_step_bytes(seq_lens: Iterable[int], n_heads_q: int, n_heads_kv: in
             + 2 * B * n_heads_q * head_dim * bytes_per_elem)
 
 
+def attention_step_bytes_q8(seq_lens: Iterable[int], n_heads_q: int, n_heads_kv: int, head_dim: int) -> int:
+    """attention_step_bytes for an int8 cache: each valid K and V row is head_dim
+    one-byte codes plus one float32 scale; q in and the output out stay bf16."""
+    lens = np.asarray(list(seq_lens), dtype=np.int64)
+    B = int(lens.size)
+    return int(lens.sum()) * n_heads_kv * (head_dim + 4) * 2 + 2 * B * n_heads_q * head_dim * 2
+
+
 def append_bytes(batch: int, n_heads_kv: int, head_dim: int, bytes_per_elem: int = 2) -> int:
     """Algorithmic bytes of one append: read k_new and v_new, write two cache rows."""
     return 4 * batch * n_heads_kv * head_dim * bytes_per_elem

@@ -227,3 +227,53 @@ def test_decode_paged_batch_zero_is_noop(lib):
 ])
 def test_append_paged_rejects(lib, args, expect):
     assert lib.kvd_kv_append_paged(*args) == expect
+
+
+def _q8_args(ks=FAKE, vs=FAKE, **over):
+    a = _dec_args(**over)
+    # (q, k_codes, v_codes, k_scales, v_scales, seq_lens, batch, ...) as kvd_decode_attention after the cache
+    return [a[0], a[1], a[2], ks, vs] + a[3:]
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(ks=None), kvd.ERR_INVALID_ARG),
+    (dict(vs=FAKE + 2), kvd.ERR_INVALID_ARG),          # scales not 4-byte aligned
+    (dict(Hq=34, Hkv=2), kvd.ERR_UNSUPPORTED),         # group 17: int8 runs on groups <= 16 only
+    (dict(D=96), kvd.ERR_UNSUPPORTED),
+    (dict(q=None), kvd.ERR_INVALID_ARG),
+    (dict(k=FAKE + 8), kvd.ERR_INVALID_ARG),
+    (dict(ws_bytes=16), kvd.ERR_WORKSPACE_TOO_SMALL),
+])
+def test_decode_q8_rejects(lib, over, expect):
+    assert lib.kvd_decode_attention_q8(*_q8_args(**over)) == expect
+    a = _q8_args(**over)
+    # step: (k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, q, seq_lens, batch, ...)
+    step = [a[1], a[2], a[3], a[4], FAKE, FAKE, FAKE, a[0], a[5]] + a[6:]
+    assert lib.kvd_decode_step_q8(*step) == expect
+
+
+def test_decode_q8_batch_zero_is_noop(lib):
+    assert lib.kvd_decode_attention_q8(*_q8_args(B=0, n_split=3, ws=None)) == kvd.OK
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((None, FAKE, FAKE, FAKE, 2, 8, 8, 1, 128, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, None, FAKE, 2, 8, 8, 1, 128, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE + 8, FAKE, FAKE, 2, 8, 8, 1, 128, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 2, 8, 9, 1, 128, None), kvd.ERR_INVALID_ARG),   # max_seq_len > s_max
+    ((FAKE, FAKE, FAKE, FAKE, 2, 8, 8, 1, 96, None), kvd.ERR_UNSUPPORTED),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 8, 8, 1, 128, None), kvd.OK),               # batch 0: no-op
+])
+def test_quantize_q8_rejects(lib, args, expect):
+    assert lib.kvd_kv_quantize_q8(*args) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, 2, 8, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE + 2, FAKE, FAKE, FAKE, 2, 8, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, 2, 8, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 1, 96, None, None), kvd.ERR_UNSUPPORTED),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 8, 1, 128, None, None), kvd.OK),
+])
+def test_append_q8_rejects(lib, args, expect):
+    assert lib.kvd_kv_append_q8(*args) == expect

@@ -65,3 +65,13 @@ def test_step_bytes_and_flops():
     assert roofline.attention_step_bytes(lens, 4, 2, 4) == 256 + 192
     assert roofline.attention_step_flops(lens, 4, 4) == 4 * 4 * 4 * 8
     assert roofline.append_bytes(3, 2, 4) == 4 * 3 * 2 * 4 * 2
+
+
+def test_step_bytes_int8():
+    # Two sequences of 3 and 5 tokens, 2 KV heads of width 64, 8 query heads:
+    # 8 tokens x 2 heads x (64 codes + 4 scale bytes) x 2 (K, V), plus q and out in bf16.
+    got = roofline.attention_step_bytes_q8([3, 5], 8, 2, 64)
+    assert got == 8 * 2 * 68 * 2 + 2 * 2 * 8 * 64 * 2
+    # against the bf16 count: the cache part shrinks to (D + 4) / (2 D)
+    bf = roofline.attention_kv_bytes([3, 5], 2, 64)
+    assert got - 2 * 2 * 8 * 64 * 2 == bf * (64 + 4) // (2 * 64)
