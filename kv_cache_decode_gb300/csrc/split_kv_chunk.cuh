@@ -441,31 +441,45 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
             uint32_t kbase = smem_u32(stages) + stage * Sh::STAGE_BYTES;
             const float* kscale = nullptr;
             const float* vscale = nullptr;
-            if constexpr (KV8) {
-                // This warp's TW rows of K and V, int8 -> f16, into the
-                // conversion buffer in the bf16 stage layout (16-byte chunk c
-                // of row r at chunk c ^ (r & 7)). Only this warp reads them.
-                const uint8_t* st8 = smem + stage * Sh::STAGE_BYTES;
-                const uint32_t conv = smem_u32(smem) + STAGES * Sh::STAGE_BYTES;
-                constexpr int CH8 = D / 16;
+            // KV8: this warp's TW rows of K (here) and V (after the score
+            // MMAs are issued, so that the conversion overlaps them), int8 ->
+            // f16, into the conversion buffer in the bf16 stage layout (16-byte
+            // chunk c of row r at chunk c ^ (r & 7)). Only this warp reads
+            // them. A lane's chunks are all loaded before any is converted.
+            const uint8_t* st8 = smem + stage * Sh::STAGE_BYTES;
+            uint8_t* conv8 = smem + STAGES * Sh::STAGE_BYTES;
+            auto convert_rows = [&](int kv) {
+                // chunks per lane, per batch (head_dim 256 leaves no registers to batch)
+                constexpr int CH8 = D / 16, NC = TW * CH8 / 32, NB = D >= 256 ? 1 : (NC > 4 ? 4 : NC);
+                static_assert(TW * CH8 % 32 == 0 && NC % NB == 0, "whole chunks per lane");
 #pragma unroll
-                for (int i = lane; i < 2 * TW * CH8; i += 32) {
-                    const int kv = i / (TW * CH8), rr = (i / CH8) % TW, c8 = i % CH8;
-                    const int r = wbase + rr;
-                    const uint4 w = *reinterpret_cast<const uint4*>(st8 + kv * TILE_ELEMS + r * D + c8 * 16);
-                    uint4 a, b;
-                    i8x4_to_f16x2x2(w.x, a.x, a.y);
-                    i8x4_to_f16x2x2(w.y, a.z, a.w);
-                    i8x4_to_f16x2x2(w.z, b.x, b.y);
-                    i8x4_to_f16x2x2(w.w, b.z, b.w);
-                    const uint32_t rowb = conv + (uint32_t)(kv * TILE_ELEMS * 2 + r * D * 2);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(rowb + (uint32_t)((((2 * c8) ^ (r & 7)) * 8) * 2)),
-                                 "r"(a.x), "r"(a.y), "r"(a.z), "r"(a.w));
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(rowb + (uint32_t)((((2 * c8 + 1) ^ (r & 7)) * 8) * 2)),
-                                 "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w));
+                for (int j0 = 0; j0 < NC; j0 += NB) {
+                    uint4 w[NB];
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) {
+                        const int i = lane + 32 * (j0 + j), rr = i / CH8, c8 = i % CH8;
+                        w[j] = *reinterpret_cast<const uint4*>(st8 + kv * TILE_ELEMS + (wbase + rr) * D + c8 * 16);
+                    }
+#pragma unroll
+                    for (int j = 0; j < NB; ++j) {
+                        const int i = lane + 32 * (j0 + j), rr = i / CH8, c8 = i % CH8, r = wbase + rr;
+                        uint4 a, b;
+                        i8x4_to_f16x2x2(w[j].x, a.x, a.y);
+                        i8x4_to_f16x2x2(w[j].y, a.z, a.w);
+                        i8x4_to_f16x2x2(w[j].z, b.x, b.y);
+                        i8x4_to_f16x2x2(w[j].w, b.z, b.w);
+                        uint8_t* row = conv8 + kv * TILE_ELEMS * 2 + r * D * 2;
+                        *reinterpret_cast<uint4*>(row + (((2 * c8) ^ (r & 7)) * 16)) = a;
+                        *reinterpret_cast<uint4*>(row + (((2 * c8 + 1) ^ (r & 7)) * 16)) = b;
+                    }
                 }
+            };
+            constexpr bool kLateV = D <= 128;  // convert V after issuing the score MMAs
+            if constexpr (KV8) {
+                convert_rows(0);
+                if constexpr (!kLateV) convert_rows(1);
                 __syncwarp();
-                kbase = conv;
+                kbase = smem_u32(conv8);
                 kscale = reinterpret_cast<const float*>(st8 + 2 * TILE_ELEMS);
                 vscale = kscale + TT;
             }
@@ -494,6 +508,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                     }
                 }
             }
+            if constexpr (KV8 && kLateV) convert_rows(1);  // V, while the score MMAs complete
 #pragma unroll
             for (int j = 0; j < NS; ++j)
 #pragma unroll
@@ -576,6 +591,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                 }
             }
 
+            if constexpr (KV8 && kLateV) __syncwarp();  // the V rows converted above
             // O += P V.
 #pragma unroll
             for (int k2 = 0; k2 < NS / 2; ++k2) {
