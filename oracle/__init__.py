@@ -37,6 +37,14 @@ Functions and the passages they follow (page title, section):
   generation throughput and latency", the quantization bullet names int8 KV
   caches; the scheme is this library's reading. Attention over it is the
   attention above over the rows read back (scale * code), in double.
+* ``kv_append_multi``, ``decode_attention_multi``: T new tokens per sequence
+  (a speculative-decoding check step): their rows are appended at pos[b] ..
+  pos[b] + T - 1, and query token i attends to the cached tokens and the new
+  tokens up to itself, i.e. to the first L_b - T + 1 + i tokens (causal).
+  All About Transformer Inference, appendix "Speculative Sampling" (the large
+  model scores all drafted tokens in one pass over the shared KV cache) and
+  "Transformer inference basics" (a token attends to itself and earlier
+  tokens). Built on ``decode_attention`` once per query token.
 
 Pins (tests/test_oracle_pins.py): closed forms (identical keys give the mean of
 V; a dominant score returns that V row; one token returns it exactly), the
@@ -333,6 +341,33 @@ def decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, seq_lens, scale
     k = dequantize_q8(k_codes, k_scales, lib=lib)
     v = dequantize_q8(v_codes, v_scales, lib=lib)
     return decode_attention_f64kv(q, k, v, seq_lens, scale, n_threads=n_threads, lib=lib)
+
+
+def kv_append_multi(k_cache, v_cache, k_new, v_new, pos, lib=None):
+    """Copies of the caches with T new rows per sequence (k_new [B, T, Hkv, D])
+    written at pos[b] + i; rows outside [0, S_max) are skipped and counted."""
+    kc = np.array(k_cache, dtype=np.uint16, copy=True, order="C")
+    vc = np.array(v_cache, dtype=np.uint16, copy=True, order="C")
+    T = k_new.shape[1]
+    skipped = 0
+    for i in range(T):
+        kc, vc, n = kv_append(kc, vc, k_new[:, i], v_new[:, i], np.asarray(pos, np.int64) + i, lib=lib)
+        skipped += n
+    return kc, vc, skipped
+
+
+def decode_attention_multi(q, k_cache, v_cache, seq_lens, scale, n_threads: int = 0, lib=None):
+    """q [B, T, Hq, D]; query token i of sequence b attends to its first
+    max(0, L_b - T + 1 + i) cached tokens. Returns out [B, T, Hq, D], lse [B, T, Hq]."""
+    q = np.ascontiguousarray(q, dtype=np.uint16)
+    B, T, Hq, D = q.shape
+    L = np.asarray(seq_lens, dtype=np.int64)
+    out = np.zeros((B, T, Hq, D), dtype=np.float64)
+    lse = np.zeros((B, T, Hq), dtype=np.float64)
+    for i in range(T):
+        Li = np.clip(L - T + 1 + i, 0, None).astype(np.int32)
+        out[:, i], lse[:, i] = decode_attention(q[:, i], k_cache, v_cache, Li, scale, n_threads=n_threads, lib=lib)
+    return out, lse
 
 
 def max_threads(lib=None) -> int:

@@ -495,6 +495,53 @@ def check_q8_append(lib):
     assert np.array_equal(v2, want_v) and np.array_equal(vs2, want_vs)
 
 
+def check_multi_token_one_is_single(lib):
+    q, k, v, lens, scale = _random_case(80, 3, 8, 2, 16, 12, [12, 5, 0])
+    a, la = oracle.decode_attention(q, k, v, lens, scale, lib=lib)
+    b, lb = oracle.decode_attention_multi(q[:, None], k, v, lens, scale, lib=lib)
+    assert np.array_equal(a, b[:, 0]) and np.array_equal(la, lb[:, 0])
+
+
+def check_multi_token_against_torch_causal(lib):
+    # The last T positions of a causal self-attention (torch float64, explicit
+    # causal mask over the whole sequence) are the multi-token decode.
+    torch = __import__("pytest").importorskip("torch")
+    B, T, Hq, Hkv, D, S = 2, 3, 4, 2, 8, 9
+    q, k, v, _, scale = _random_case(81, B, Hq, Hkv, D, S, [S, S])
+    r = np.random.default_rng(82)
+    qm = _bits(r.standard_normal((B, T, Hq, D)))
+    lens = np.array([9, 6], np.int32)
+    out, _ = oracle.decode_attention_multi(qm, k, v, lens, scale, lib=lib)
+    G = Hq // Hkv
+    for b in range(B):
+        L = int(lens[b])
+        kk = torch.from_numpy(_f64(k[b, :L])).permute(1, 0, 2).repeat_interleave(G, dim=0)  # [Hq, L, D]
+        vv = torch.from_numpy(_f64(v[b, :L])).permute(1, 0, 2).repeat_interleave(G, dim=0)
+        qq = torch.from_numpy(_f64(qm[b])).permute(1, 0, 2)                                    # [Hq, T, D]
+        pos_q = torch.arange(L - T, L)[:, None]
+        mask = torch.arange(L)[None, :] <= pos_q                                               # [T, L]
+        ref = torch.nn.functional.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask, scale=scale)
+        assert np.max(np.abs(ref.permute(1, 0, 2).numpy() - out[b])) < 1e-12, b
+
+
+def check_multi_token_append(lib):
+    r = np.random.default_rng(83)
+    B, S, Hkv, D, T = 3, 8, 2, 4, 3
+    kc = r.integers(0, 2**16, (B, S, Hkv, D), dtype=np.uint16)
+    vc = r.integers(0, 2**16, (B, S, Hkv, D), dtype=np.uint16)
+    kn = r.integers(0, 2**16, (B, T, Hkv, D), dtype=np.uint16)
+    vn = r.integers(0, 2**16, (B, T, Hkv, D), dtype=np.uint16)
+    pos = np.array([0, 5, 7], np.int32)  # the last sequence has room for one of its three rows
+    k2, v2, skipped = oracle.kv_append_multi(kc, vc, kn, vn, pos, lib=lib)
+    assert skipped == 2
+    ek, ev = kc.copy(), vc.copy()
+    for b, p0 in enumerate(pos):
+        for i in range(T):
+            if p0 + i < S:
+                ek[b, p0 + i], ev[b, p0 + i] = kn[b, i], vn[b, i]
+    assert np.array_equal(k2, ek) and np.array_equal(v2, ev)
+
+
 ALL_CHECKS = [
     check_identical_keys_give_mean_of_v,
     check_dominant_score_returns_that_row,
@@ -518,4 +565,7 @@ ALL_CHECKS = [
     check_f64kv_attention_is_the_bf16_attention,
     check_q8_attention_close_to_bf16,
     check_q8_append,
+    check_multi_token_one_is_single,
+    check_multi_token_against_torch_causal,
+    check_multi_token_append,
 ]
