@@ -267,6 +267,44 @@ kvd_status kvd_decode_step_q8(void* k_codes, void* v_codes, float* k_scales, flo
                               kvd_stream_t stream);
 
 /*
+ * Multi-token decode: n_tokens = T new tokens per sequence at once, as when a
+ * large model checks T drafted tokens in one pass over the shared KV cache
+ * (All About Transformer Inference, appendix "Speculative Sampling"). The T
+ * rows of each sequence are appended at pos[b] .. pos[b] + T - 1, and query
+ * token i attends to the first L_b - T + 1 + i cached tokens (the cache plus
+ * the new tokens up to itself; L_b = seq_lens[b] after the append, so
+ * seq_lens = old length + T). Layouts:
+ *   q, out    : [batch, T, n_heads_q, head_dim] (bf16 q; out as out_dtype)
+ *   lse_out   : optional fp32 [batch, T, n_heads_q]
+ *   k_new, v_new : bf16 [batch, T, n_heads_kv, head_dim]
+ * A query token that sees no token (L_b < T - i) gets a zero row and lse -inf.
+ * Supported where T * (n_heads_q / n_heads_kv) <= 16 (the mma.sync kernel;
+ * otherwise KVD_ERR_UNSUPPORTED); T = 1 is exactly the single-token call. The
+ * workspace holds T times the rows: size it with kvd_decode_plan_multi. Rows of
+ * the append outside [0, s_max) are skipped with KVD_STATUS_POS_OUT_OF_RANGE.
+ * Other arguments, results and errors as the single-token calls, plus
+ * KVD_ERR_INVALID_ARG for n_tokens < 1.
+ */
+kvd_status kvd_decode_plan_multi(int batch, int n_tokens, int n_heads_q, int n_heads_kv, int head_dim,
+                                 int max_seq_len, int num_sms, int n_split_request, kvd_out_dtype out_dtype,
+                                 int* n_split_out, size_t* workspace_bytes_out);
+kvd_status kvd_kv_append_multi(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                               const int32_t* pos, int batch, int n_tokens, int s_max, int n_heads_kv,
+                               int head_dim, int32_t* status_word, kvd_stream_t stream);
+kvd_status kvd_decode_attention_multi(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* seq_lens, int batch, int n_tokens, int s_max,
+                                      int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim, float scale,
+                                      int n_split, void* workspace, size_t workspace_bytes, void* out,
+                                      kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                                      kvd_stream_t stream);
+kvd_status kvd_decode_step_multi(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                                 const int32_t* pos, const void* q, const int32_t* seq_lens, int batch,
+                                 int n_tokens, int s_max, int max_seq_len, int n_heads_q, int n_heads_kv,
+                                 int head_dim, float scale, int n_split, void* workspace, size_t workspace_bytes,
+                                 void* out, kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                                 kvd_stream_t stream);
+
+/*
  * The two launches of kvd_decode_attention, exposed separately so that each
  * can be timed on its own. Arguments and errors are those of
  * kvd_decode_attention; calling kvd_split_kv_chunk then kvd_split_kv_merge on

@@ -31,7 +31,8 @@ EXPORTED = (
     "kvd_split_kv_merge", "kvd_schedule_describe", "kvd_kernel_info", "kvd_status_string",
     "kvd_version", "kvd_decode_attention_static", "kvd_decode_step", "kvd_kv_append_paged",
     "kvd_decode_attention_paged", "kvd_decode_step_paged", "kvd_kv_quantize_q8", "kvd_kv_append_q8",
-    "kvd_decode_attention_q8", "kvd_decode_step_q8",
+    "kvd_decode_attention_q8", "kvd_decode_step_q8", "kvd_decode_plan_multi", "kvd_kv_append_multi",
+    "kvd_decode_attention_multi", "kvd_decode_step_multi",
 )
 STATIC_WORKSPACE_BYTES = 16 << 20  # KVD_STATIC_WORKSPACE_BYTES
 
@@ -92,6 +93,15 @@ def _declare(lib):
     lib.kvd_decode_attention_q8.restype = I
     lib.kvd_decode_step_q8.argtypes = [P, P, P, P, P, P, P, P, P] + dec[4:]
     lib.kvd_decode_step_q8.restype = I
+    # multi-token: n_tokens after batch
+    lib.kvd_decode_plan_multi.argtypes = [I, I, I, I, I, I, I, I, I, PI, PSZ]
+    lib.kvd_decode_plan_multi.restype = I
+    lib.kvd_kv_append_multi.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P]
+    lib.kvd_kv_append_multi.restype = I
+    lib.kvd_decode_attention_multi.argtypes = dec[:5] + [I] + dec[5:]
+    lib.kvd_decode_attention_multi.restype = I
+    lib.kvd_decode_step_multi.argtypes = [P, P, P, P, P, P, P, I, I] + dec[5:]
+    lib.kvd_decode_step_multi.restype = I
     lib.kvd_schedule_describe.argtypes = [P, I, I, I, I, I, I, I, I, P, I, PI, PI]
     lib.kvd_kernel_info.argtypes = [I, I, I, I, PI, PI, PI, PI, PI, PI]
     lib.kvd_status_string.argtypes = [I]
@@ -463,6 +473,81 @@ def decode_step_q8(q, k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, s
     _check(load().kvd_decode_step_q8(k_codes.data_ptr(), v_codes.data_ptr(), k_scales.data_ptr(),
                                      v_scales.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), pos.data_ptr(),
                                      q.data_ptr(), *tail), "kvd_decode_step_q8")
+
+
+def decode_plan_multi(batch: int, n_tokens: int, n_heads_q: int, n_heads_kv: int, head_dim: int,
+                      max_seq_len: int, num_sms: int = 0, n_split: int = 0, out_dtype="bf16") -> Tuple[int, int]:
+    """(n_split, workspace_bytes) for a multi-token call of this shape."""
+    lib = load()
+    n = ctypes.c_int(0)
+    ws = ctypes.c_size_t(0)
+    _check(lib.kvd_decode_plan_multi(batch, n_tokens, n_heads_q, n_heads_kv, head_dim, max_seq_len, num_sms,
+                                     n_split, _out_code(out_dtype), ctypes.byref(n), ctypes.byref(ws)),
+           "kvd_decode_plan_multi")
+    return n.value, ws.value
+
+
+def kv_append_multi(k_cache, v_cache, k_new, v_new, pos, status=None, stream=None):
+    """The T new rows of each sequence (k_new [B, T, Hkv, D]) at pos[b] + i."""
+    import torch
+    for t, n in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        _require(t, n, torch.bfloat16, 4)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _require(t, n, torch.bfloat16, 4)
+    _require(pos, "pos", torch.int32, 1)
+    B, S, Hkv, D = k_cache.shape
+    T = k_new.shape[1]
+    if v_cache.shape != k_cache.shape or k_new.shape != (B, T, Hkv, D) or v_new.shape != k_new.shape \
+            or pos.shape != (B,):
+        raise ValueError("kv_append_multi: inconsistent shapes")
+    _check(load().kvd_kv_append_multi(k_cache.data_ptr(), v_cache.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                      pos.data_ptr(), B, T, S, Hkv, D, _ptr(status), _stream_handle(stream)),
+           "kvd_kv_append_multi")
+
+
+def _decode_multi_args(q, k_cache, v_cache, seq_lens, max_seq_len, scale, n_split, workspace, out, lse, status,
+                       stream):
+    import torch
+    _require(q, "q", torch.bfloat16, 4)
+    _require(out, "out", None, 4)
+    B, T, Hq, D = q.shape
+    if out.shape != q.shape:
+        raise ValueError("decode_attention_multi: out must be [B, T, Hq, D]")
+    if lse is not None:
+        _require(lse, "lse", torch.float32, 3)
+        if lse.shape != (B, T, Hq):
+            raise ValueError("decode_attention_multi: lse must be [B, T, Hq]")
+    # the single-token checks on [B, T*Hq, D] views (rows of one sequence are contiguous)
+    a = _decode_args(q.view(B, T * Hq, D), k_cache, v_cache, seq_lens, max_seq_len, scale, n_split, workspace,
+                     out.view(B, T * Hq, D), None if lse is None else lse.view(B, T * Hq), status, stream)
+    a[7] = Hq  # n_heads_q proper
+    return a[:5] + [T] + a[5:]
+
+
+def decode_attention_multi(q, k_cache, v_cache, seq_lens, max_seq_len: int, scale: float, out, workspace=None,
+                           n_split: int = 0, lse=None, status=None, stream=None):
+    """T query tokens per sequence (q, out [B, T, Hq, D]); token i attends to the
+    first seq_lens[b] - T + 1 + i cached tokens. Needs T * G <= 16."""
+    args = _decode_multi_args(q, k_cache, v_cache, seq_lens, max_seq_len, scale, n_split, workspace, out, lse,
+                              status, stream)
+    _check(load().kvd_decode_attention_multi(*args), "kvd_decode_attention_multi")
+
+
+def decode_step_multi(q, k_cache, v_cache, k_new, v_new, pos, seq_lens, max_seq_len: int, scale: float, out,
+                      workspace=None, n_split: int = 0, lse=None, status=None, stream=None):
+    """kv_append_multi then decode_attention_multi as one call (kvd_decode_step_multi)."""
+    import torch
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _require(t, n, torch.bfloat16, 4)
+    _require(pos, "pos", torch.int32, 1)
+    a = _decode_multi_args(q, k_cache, v_cache, seq_lens, max_seq_len, scale, n_split, workspace, out, lse,
+                           status, stream)
+    B, T, Hq, D = q.shape
+    if k_new.shape != (B, T, k_cache.shape[2], D) or v_new.shape != k_new.shape or pos.shape != (B,):
+        raise ValueError("decode_step_multi: inconsistent shapes")
+    # (k_cache, v_cache, k_new, v_new, pos, q, seq_lens, batch, T, ...)
+    args = [a[1], a[2], k_new.data_ptr(), v_new.data_ptr(), pos.data_ptr(), a[0], a[3], a[4], a[5]] + a[6:]
+    _check(load().kvd_decode_step_multi(*args), "kvd_decode_step_multi")
 
 
 def decode_step(q, k_cache, v_cache, k_new, v_new, pos, seq_lens, max_seq_len: int, scale: float,

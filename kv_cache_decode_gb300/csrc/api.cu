@@ -113,7 +113,7 @@ size_t workspace_for(int n_split, int batch, int Hq, int Hkv, int D) {
 }
 
 kvd_status plan(int batch, int Hq, int Hkv, int D, int max_len, int num_sms, int n_split_req,
-                kvd_out_dtype dt, int* n_split, size_t* ws, const ChunkKernel** kern) {
+                kvd_out_dtype dt, int* n_split, size_t* ws, const ChunkKernel** kern, int T = 1) {
     kvd_status st = check_shape(batch, Hq, Hkv, D, dt);
     if (st != KVD_OK) return st;
     if (max_len < 0 || n_split_req < 0 || num_sms < 0) return KVD_ERR_INVALID_ARG;
@@ -129,7 +129,7 @@ kvd_status plan(int batch, int Hq, int Hkv, int D, int max_len, int num_sms, int
         n = heuristic_split(k, batch, Hkv, max_len, sms);
     }
     *n_split = n;
-    *ws = workspace_for(n, batch, Hq, Hkv, D);
+    *ws = workspace_for(n, batch, Hq * T, Hkv, D);  // T * G rows per slot
     if (kern) *kern = k;
     return KVD_OK;
 }
@@ -160,7 +160,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
                   int D, float scale, int n_split_req, void* workspace, size_t workspace_bytes,
                   void* out, kvd_out_dtype dt, float* lse, int32_t* status, kvd_stream_t stream,
                   const AppendArgs* app = nullptr, const PagedCache* pg = nullptr,
-                  const QuantCache* q8 = nullptr) {
+                  const QuantCache* q8 = nullptr, int T = 1) {
     kvd_status st = check_shape(batch, Hq, Hkv, D, dt);
     if (st != KVD_OK) return st;
     if (s_max <= 0 || max_seq_len < 0 || max_seq_len > s_max) return KVD_ERR_INVALID_ARG;
@@ -179,8 +179,11 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     int n_split = 0;
     size_t need = 0;
     const ChunkKernel* k = nullptr;
+    // T > 1 query tokens: the mma.sync kernel, whose 16 rows per pair hold T * G.
+    if (T < 1) return KVD_ERR_INVALID_ARG;
+    if (T > 1 && (Hq / Hkv) * T > 16) return KVD_ERR_UNSUPPORTED;
     st = plan(batch, Hq, Hkv, D, max_seq_len, 0 /* query device if heuristic */, n_split_req, dt,
-              &n_split, &need, &k);
+              &n_split, &need, &k, T);
     if (st != KVD_OK) return st;
     if (pg) k = pick_kernel(Hq, Hkv, D, dt, true);
     if (q8) {
@@ -215,6 +218,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     p.out = out;
     p.lse = lse;
     p.status = status;
+    p.T = T;
     if (q8) {
         p.k_scale = q8->k_scale;
         p.v_scale = q8->v_scale;
@@ -226,10 +230,11 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
         p.num_pages = pg->num_pages;
     }
     if (need > 0) {
-        const size_t P = (size_t)batch * Hkv, G = (size_t)p.G, slots = (size_t)n_split + P - 1;
+        // T * G rows per slot (as workspace_for with T query tokens)
+        const size_t P = (size_t)batch * Hkv, rows = (size_t)p.G * T, slots = (size_t)n_split + P - 1;
         uint8_t* w = static_cast<uint8_t*>(workspace);
         p.ws_o = reinterpret_cast<float*>(w);
-        w += align256(slots * G * D * sizeof(float));
+        w += align256(slots * rows * D * sizeof(float));
         p.ws_ml = reinterpret_cast<float2*>(w);
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -243,7 +248,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
             q8 ? launch_append_q8(app->k_cache, app->v_cache, q8->k_scale, q8->v_scale, app->k_new, app->v_new,
                                   app->pos, batch, s_max, Hkv, D, status, s)
                : launch_append(app->k_cache, app->v_cache, app->k_new, app->v_new, app->pos, batch, s_max, Hkv,
-                               D, status, pg ? *pg : none, s);
+                               D, status, pg ? *pg : none, s, T);
         if (e != cudaSuccess) return KVD_ERR_CUDA;
         p.early = 1;
         p.pos = app->pos;
@@ -295,6 +300,56 @@ kvd_status kvd_kv_append(void* k_cache, void* v_cache, const void* k_new, const 
                          status_word, none, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? KVD_OK
                : KVD_ERR_CUDA;
+}
+
+kvd_status kvd_decode_plan_multi(int batch, int n_tokens, int n_heads_q, int n_heads_kv, int head_dim,
+                                 int max_seq_len, int num_sms, int n_split_request, kvd_out_dtype out_dtype,
+                                 int* n_split_out, size_t* workspace_bytes_out) {
+    if (!n_split_out || !workspace_bytes_out || n_tokens < 1) return KVD_ERR_INVALID_ARG;
+    if (n_heads_kv > 0 && n_tokens > 1 && (n_heads_q / n_heads_kv) * n_tokens > 16) return KVD_ERR_UNSUPPORTED;
+    return plan(batch, n_heads_q, n_heads_kv, head_dim, max_seq_len, num_sms, n_split_request, out_dtype,
+                n_split_out, workspace_bytes_out, nullptr, n_tokens);
+}
+
+kvd_status kvd_kv_append_multi(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                               const int32_t* pos, int batch, int n_tokens, int s_max, int n_heads_kv,
+                               int head_dim, int32_t* status_word, kvd_stream_t stream) {
+    if (n_tokens < 1) return KVD_ERR_INVALID_ARG;
+    const kvd_status st = check_append(k_cache, v_cache, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim,
+                                       status_word);
+    if (st != KVD_OK) return st;
+    if (batch == 0) return KVD_OK;
+    const PagedCache none{nullptr, 0, 0, 0};
+    return launch_append(k_cache, v_cache, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim, status_word,
+                         none, static_cast<cudaStream_t>(stream), n_tokens) == cudaSuccess
+               ? KVD_OK
+               : KVD_ERR_CUDA;
+}
+
+kvd_status kvd_decode_attention_multi(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* seq_lens, int batch, int n_tokens, int s_max,
+                                      int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim, float scale,
+                                      int n_split, void* workspace, size_t workspace_bytes, void* out,
+                                      kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                                      kvd_stream_t stream) {
+    return decode(kBoth, q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q, n_heads_kv,
+                  head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype, lse_out, status_word,
+                  stream, nullptr, nullptr, nullptr, n_tokens);
+}
+
+kvd_status kvd_decode_step_multi(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                                 const int32_t* pos, const void* q, const int32_t* seq_lens, int batch,
+                                 int n_tokens, int s_max, int max_seq_len, int n_heads_q, int n_heads_kv,
+                                 int head_dim, float scale, int n_split, void* workspace, size_t workspace_bytes,
+                                 void* out, kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                                 kvd_stream_t stream) {
+    const kvd_status st = check_append(k_cache, v_cache, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim,
+                                       status_word);
+    if (st != KVD_OK) return st;
+    const AppendArgs app{k_cache, v_cache, k_new, v_new, pos};
+    return decode(kBoth, q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q, n_heads_kv,
+                  head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype, lse_out, status_word,
+                  stream, &app, nullptr, nullptr, n_tokens);
 }
 
 kvd_status kvd_kv_quantize_q8(const void* cache, void* codes, float* scales, const int32_t* seq_lens, int batch,

@@ -15,22 +15,24 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_ca
                                                        const uint4* __restrict__ v_new,
                                                        const int32_t* __restrict__ pos, int B,
                                                        int S_max, int Hkv, int vec_per_row,
-                                                       int32_t* status, const PagedCache pg) {
+                                                       int32_t* status, const PagedCache pg, int T) {
     // Let the attention kernel that follows start its launch; it waits for
     // this grid's writes before reading the cache.
     pdl_launch_dependents();
-    const long long rows = (long long)B * Hkv;
+    const long long rows = (long long)B * T * Hkv;  // new rows: (b, i, h)
     const long long per_tensor = rows * vec_per_row;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < 2 * per_tensor;
          i += (long long)gridDim.x * blockDim.x) {
         const int which = (int)(i / per_tensor);
         const long long r = i - which * per_tensor;
-        const long long row = r / vec_per_row;  // b * Hkv + h
+        const long long row = r / vec_per_row;  // (b * T + i) * Hkv + h
         const int ch = (int)(r - row * vec_per_row);
-        const int b = (int)(row / Hkv), h = (int)(row - (long long)b * Hkv);
+        const long long bi = row / Hkv;
+        const int h = (int)(row - bi * Hkv);
+        const int b = (int)(bi / T), tk = (int)(bi - (long long)b * T);  // token tk of sequence b
         // Both loads are issued before either is used: one memory round trip.
         const uint4 val = __ldg((which == 0 ? k_new : v_new) + r);
-        const int t = __ldg(pos + b);
+        const int t = __ldg(pos + b) + tk;
         if (t < 0 || t >= S_max) {
             if (status && which == 0 && h == 0 && ch == 0) atomicOr(status, KVD_STATUS_POS_OUT_OF_RANGE);
             continue;
@@ -51,9 +53,9 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_ca
 
 cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                           const int32_t* pos, int B, int S_max, int Hkv, int D,
-                          int32_t* status, const PagedCache& pg, cudaStream_t stream) {
+                          int32_t* status, const PagedCache& pg, cudaStream_t stream, int T) {
     const int vec_per_row = D / 8;
-    const long long work = 2LL * B * Hkv * vec_per_row;
+    const long long work = 2LL * B * T * Hkv * vec_per_row;
     long long blocks = (work + 255) / 256;
     if (blocks > 4096) blocks = 4096;
     if (blocks < 1) blocks = 1;
@@ -64,7 +66,7 @@ cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const
     // The launch's own status (a stale error from earlier work is not picked up).
     return cudaLaunchKernelEx(&cfg, kv_append_kernel, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
                               static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), pos, B, S_max,
-                              Hkv, vec_per_row, status, pg);
+                              Hkv, vec_per_row, status, pg, T);
 }
 
 }  // namespace kvd

@@ -38,6 +38,11 @@ struct DecodeParams {
     // reads back as k_scale[(b * S_max + t) * Hkv + h] * code (v likewise).
     const float* k_scale;
     const float* v_scale;
+    // Query tokens per sequence (1, or T > 1 for a speculative check step on
+    // the mma.sync kernel): q, out [B, T, Hq, D], lse [B, T, Hq]; query token i
+    // of sequence b attends to its first seq_lens[b] - T + 1 + i tokens, and
+    // the workspace holds T * G rows per slot.
+    int T;
 };
 
 // One compiled variant of the split-KV chunk kernel.
@@ -64,9 +69,10 @@ struct PagedCache {
     int max_blocks, page_shift, num_pages;
 };
 
+// T rows per sequence (k_new [B, T, Hkv, D]) go to pos[b] .. pos[b] + T - 1.
 cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                           const int32_t* pos, int B, int S_max, int Hkv, int D,
-                          int32_t* status, const PagedCache& pg, cudaStream_t stream);
+                          int32_t* status, const PagedCache& pg, cudaStream_t stream, int T = 1);
 // int8 cache (kv_quant.cu): the append quantizes the new rows; the bulk
 // conversion quantizes rows t < seq_lens[b] of a bf16 cache.
 cudaError_t launch_append_q8(void* k_codes, void* v_codes, float* k_scale, float* v_scale, const void* k_new,

@@ -178,6 +178,14 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
     const int ht = warp / TS, ts = warp % TS;
     const int c = blockIdx.x;
     const int G = p.G;
+    // T query tokens per sequence (T > 1: a speculative check step): a pair
+    // has T * G rows, row r being query token r / G of head r % G, and query
+    // token i attends to the first L - T + 1 + i tokens.
+    const int T = p.T, TG = T * G;
+    auto out_row = [&](int b, int h, int r) {  // row of out / lse ([B, T, Hq])
+        const int i = r / G;
+        return ((size_t)b * T + i) * p.Hq + (size_t)h * G + (r - i * G);
+    };
 
     // Inputs may be produced by the previous kernel on the stream. After this
     // library's append (p.early), only the cache loads need to wait for it.
@@ -332,16 +340,15 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
 
     // Zero output for an empty pair this CTA owns.
     auto write_empty = [&](int b, int h) {
-        const size_t row = (size_t)b * p.Hq + (size_t)h * G;
-        if constexpr (F32OUT) {
-            float* o = reinterpret_cast<float*>(p.out) + row * D;
-            for (int i = tid; i < G * D; i += NT) o[i] = 0.f;
-        } else {
-            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + row * D;
-            for (int i = tid; i < G * D; i += NT) o[i] = __float2bfloat16_rn(0.f);
+        for (int i = tid; i < TG * D; i += NT) {
+            const size_t e = out_row(b, h, i / D) * D + (i % D);
+            if constexpr (F32OUT)
+                reinterpret_cast<float*>(p.out)[e] = 0.f;
+            else
+                reinterpret_cast<__nv_bfloat16*>(p.out)[e] = __float2bfloat16_rn(0.f);
         }
         if (p.lse)
-            for (int i = tid; i < G; i += NT) p.lse[row + i] = -CUDART_INF_F;
+            for (int i = tid; i < TG; i += NT) p.lse[out_row(b, h, i)] = -CUDART_INF_F;
     };
 
     // ---- per-warp state ----
@@ -353,8 +360,9 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) qf[kk][0] = qf[kk][1] = qf[kk][2] = qf[kk][3] = 0u;
 
-    const int r0 = ht * 16 + (lane >> 2);  // group-local query heads of this thread's rows
+    const int r0 = ht * 16 + (lane >> 2);  // pair-local rows of this thread
     const int r1 = r0 + 8;
+    const int cq0 = T - 1 - r0 / G, cq1 = T - 1 - r1 / G;  // tokens a row sees fewer than the last
     const float scale_log2 = p.scale_log2;
 
     // ---- prologue ----
@@ -412,11 +420,10 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
         ++it;
 
         if (ct.seg_start) {
-            const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(p.q) +
-                                      ((size_t)ct.b * p.Hq + (size_t)ct.h * G) * D;
-            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qb + (size_t)r0 * D);
-            const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qb + (size_t)r1 * D);
-            const bool v0 = r0 < G, v1 = r1 < G;
+            const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(p.q);
+            const bool v0 = r0 < TG, v1 = r1 < TG;
+            const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qb + (v0 ? out_row(ct.b, ct.h, r0) : 0) * D);
+            const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qb + (v1 ? out_row(ct.b, ct.h, r1) : 0) * D);
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
                 const int w = kk * 8 + (lane & 3);  // 32-bit word index of column kk*16 + 2*(lane&3)
@@ -437,6 +444,8 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
 
         const int nvalid = ct.tok_hi - ct.tok_lo;
         const int wbase = ts * TW;
+        // Causal limits of this thread's rows, relative to the tile (T = 1: the tile's end or beyond).
+        const int lim0 = ct.L - cq0 - ct.tok_lo, lim1 = ct.L - cq1 - ct.tok_lo;
         if (wbase < nvalid) {
             uint32_t kbase = smem_u32(stages) + stage * Sh::STAGE_BYTES;
             const float* kscale = nullptr;
@@ -523,7 +532,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                     const int tok = wbase + j * 8 + (lane & 3) * 2 + (e & 1);
                     float sc = scale_log2;
                     if constexpr (KV8) sc *= kscale[tok];
-                    s[j][e] = (tok < nvalid) ? s[j][e] * sc : -CUDART_INF_F;
+                    s[j][e] = (tok < nvalid && tok < (e < 2 ? lim0 : lim1)) ? s[j][e] * sc : -CUDART_INF_F;
                 }
                 mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
                 mx1 = fmaxf(mx1, fmaxf(s[j][2], s[j][3]));
@@ -642,8 +651,10 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                         const float ol0 = mb[(ND * 4 + 2) * 32 + lane];
                         const float ol1 = mb[(ND * 4 + 3) * 32 + lane];
                         const float M0 = fmaxf(m0, om0), M1 = fmaxf(m1, om1);
-                        const float A0 = exp2f(m0 - M0), B0 = exp2f(om0 - M0);
-                        const float A1 = exp2f(m1 - M1), B1 = exp2f(om1 - M1);
+                        // a row no slice has seen a token of (causal rows) stays empty
+                        const float U0 = (M0 == -CUDART_INF_F) ? 0.f : M0, U1 = (M1 == -CUDART_INF_F) ? 0.f : M1;
+                        const float A0 = exp2f(m0 - U0), B0 = exp2f(om0 - U0);
+                        const float A1 = exp2f(m1 - U1), B1 = exp2f(om1 - U1);
                         l0 = A0 * l0 + B0 * ol0;
                         l1 = A1 * l1 + B1 * ol1;
                         m0 = M0;
@@ -661,30 +672,31 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
 
             if (ts == 0) {
                 const size_t pair = (size_t)ct.b * p.Hkv + ct.h;
-                const size_t qrow = (size_t)ct.b * p.Hq + (size_t)ct.h * G;
-                const bool v0 = r0 < G, v1 = r1 < G;
+                const bool v0 = r0 < TG, v1 = r1 < TG;
+                const size_t or0 = v0 ? out_row(ct.b, ct.h, r0) : 0, or1 = v1 ? out_row(ct.b, ct.h, r1) : 0;
                 if (ct.full) {
-                    const float i0 = 1.f / l0, i1 = 1.f / l1;
+                    // (a row that sees no token, possible only when L < T, is zero)
+                    const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
 #pragma unroll
                     for (int n = 0; n < ND; ++n) {
                         const int d = n * 8 + (lane & 3) * 2;
                         if constexpr (F32OUT) {
                             float* out = reinterpret_cast<float*>(p.out);
-                            if (v0) *reinterpret_cast<float2*>(out + (qrow + r0) * D + d) = make_float2(o[n][0] * i0, o[n][1] * i0);
-                            if (v1) *reinterpret_cast<float2*>(out + (qrow + r1) * D + d) = make_float2(o[n][2] * i1, o[n][3] * i1);
+                            if (v0) *reinterpret_cast<float2*>(out + or0 * D + d) = make_float2(o[n][0] * i0, o[n][1] * i0);
+                            if (v1) *reinterpret_cast<float2*>(out + or1 * D + d) = make_float2(o[n][2] * i1, o[n][3] * i1);
                         } else {
                             __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-                            if (v0) *reinterpret_cast<uint32_t*>(out + (qrow + r0) * D + d) = pack_bf16x2(o[n][0] * i0, o[n][1] * i0);
-                            if (v1) *reinterpret_cast<uint32_t*>(out + (qrow + r1) * D + d) = pack_bf16x2(o[n][2] * i1, o[n][3] * i1);
+                            if (v0) *reinterpret_cast<uint32_t*>(out + or0 * D + d) = pack_bf16x2(o[n][0] * i0, o[n][1] * i0);
+                            if (v1) *reinterpret_cast<uint32_t*>(out + or1 * D + d) = pack_bf16x2(o[n][2] * i1, o[n][3] * i1);
                         }
                     }
                     if (p.lse && (lane & 3) == 0) {
-                        if (v0) p.lse[qrow + r0] = (m0 + log2f(l0)) * 0.69314718055994531f;
-                        if (v1) p.lse[qrow + r1] = (m1 + log2f(l1)) * 0.69314718055994531f;
+                        if (v0) p.lse[or0] = l0 > 0.f ? (m0 + log2f(l0)) * 0.69314718055994531f : -CUDART_INF_F;
+                        if (v1) p.lse[or1] = l1 > 0.f ? (m1 + log2f(l1)) * 0.69314718055994531f : -CUDART_INF_F;
                     }
                 } else {
                     const size_t slot = (size_t)c + pair;
-                    float* wo = p.ws_o + slot * G * D;
+                    float* wo = p.ws_o + slot * TG * D;
 #pragma unroll
                     for (int n = 0; n < ND; ++n) {
                         const int d = n * 8 + (lane & 3) * 2;
@@ -692,8 +704,8 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                         if (v1) *reinterpret_cast<float2*>(wo + (size_t)r1 * D + d) = make_float2(o[n][2], o[n][3]);
                     }
                     if ((lane & 3) == 0) {
-                        if (v0) p.ws_ml[slot * G + r0] = make_float2(m0, l0);
-                        if (v1) p.ws_ml[slot * G + r1] = make_float2(m1, l1);
+                        if (v0) p.ws_ml[slot * TG + r0] = make_float2(m0, l0);
+                        if (v1) p.ws_ml[slot * TG + r1] = make_float2(m1, l1);
                     }
                 }
             }

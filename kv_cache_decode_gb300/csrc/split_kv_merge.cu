@@ -42,17 +42,21 @@ __global__ void __launch_bounds__(NT, 768 / NT) split_kv_merge_kernel(const Deco
     __shared__ longlong2 s_sum[NT / 32];
 
     const int G = p.G;
+    // Output rows: (b, i, query head) with T query tokens per sequence; a
+    // pair's partial slot holds T * G rows, row i * G + g.
+    const int T = p.T, TG = T * G;
+    const long long rows_per_seq = (long long)T * p.Hq;
     const int tid = threadIdx.x;
     const int col = tid % COLS, sub = (tid / COLS) % S, rloc = tid / (COLS * S);
     const int rows_per_cta = NT / (COLS * S);
-    const long long rows = (long long)p.B * p.Hq;
+    const long long rows = (long long)p.B * rows_per_seq;
     const long long row = (long long)blockIdx.x * rows_per_cta + rloc;
 
     // ---- the schedule, from the lengths (before the dependency wait) ----
     const RuntimeGeom geo{p.tile_tokens, p.seg_unit, p.seg_cost};
     auto ext = [&](int b) { return pair_extent(clamp_len(__ldg(p.seq_lens + b), p.len_cap), geo); };
     const long long row_lo = (long long)blockIdx.x * rows_per_cta;
-    const int b_lo = (int)(row_lo / p.Hq);  // first sequence among this CTA's rows
+    const int b_lo = (int)(row_lo / rows_per_seq);  // first sequence among this CTA's rows
     long long tot = 0, pre = 0;
     for (int b = tid; b < p.B; b += NT) {
         const long long e = ext(b);
@@ -78,9 +82,12 @@ __global__ void __launch_bounds__(NT, 768 / NT) split_kv_merge_kernel(const Deco
     int n = 0, g = 0;
     size_t slot0 = 0;
     if (row < rows) {
-        const int pair = (int)(row / G);
-        g = (int)(row % G);
-        const int b = pair / p.Hkv, h = pair % p.Hkv;
+        const int b = (int)(row / rows_per_seq);
+        const int rem = (int)(row - (long long)b * rows_per_seq);  // i * Hq + query head
+        const int i = rem / p.Hq, hq = rem - i * p.Hq;
+        const int h = hq / G;
+        g = i * G + (hq - h * G);  // row within the pair's slot
+        const int pair = b * p.Hkv + h;
         long long cum = pre * p.Hkv;
         for (int bb = b_lo; bb < b; ++bb) cum += ext(bb) * p.Hkv;
         const long long e = ext(b);
@@ -99,10 +106,10 @@ __global__ void __launch_bounds__(NT, 768 / NT) split_kv_merge_kernel(const Deco
 
     pdl_wait();  // partials come from the chunk kernel just before on the stream
 
-    const size_t ml_stride = (size_t)G * S;         // float2 stride between this subset's slots
-    const size_t o_stride = (size_t)G * D / 4 * S;  // float4 stride between this subset's slots
-    const float2* mlp = p.ws_ml + (slot0 + sub) * G + g;
-    const float4* op = reinterpret_cast<const float4*>(p.ws_o + ((slot0 + sub) * G + g) * D) + col * kVec;
+    const size_t ml_stride = (size_t)TG * S;         // float2 stride between this subset's slots
+    const size_t o_stride = (size_t)TG * D / 4 * S;  // float4 stride between this subset's slots
+    const float2* mlp = p.ws_ml + (slot0 + sub) * TG + g;
+    const float4* op = reinterpret_cast<const float4*>(p.ws_o + ((slot0 + sub) * TG + g) * D) + col * kVec;
     const int mine = active && sub < n ? (n - sub + S - 1) / S : 0;  // partials of this subset
 
     float M = -CUDART_INF_F, L = 0.f;
@@ -214,7 +221,7 @@ static cudaError_t launch_merge_t(const DecodeParams& p, int num_sms, cudaStream
     // stay resident at once (768 per SM at this register cap); past that,
     // more batches per thread cost less than a second wave of CTAs.
     const long long pairs = (long long)p.B * p.Hkv;
-    const long long rows = (long long)p.B * p.Hq;
+    const long long rows = (long long)p.B * p.T * p.Hq;
     const long long expect = (long long)p.n_split / (pairs > 0 ? pairs : 1) + 2;
     const long long resident = (long long)num_sms * 768;
     int S = 1;

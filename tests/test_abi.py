@@ -277,3 +277,30 @@ def test_quantize_q8_rejects(lib, args, expect):
 ])
 def test_append_q8_rejects(lib, args, expect):
     assert lib.kvd_kv_append_q8(*args) == expect
+
+
+@pytest.mark.parametrize("T,Hq,Hkv,expect", [
+    (0, 8, 2, kvd.ERR_INVALID_ARG),
+    (4, 8, 2, kvd.OK),          # T * G = 16
+    (5, 8, 2, kvd.ERR_UNSUPPORTED),
+    (2, 48, 1, kvd.ERR_UNSUPPORTED),
+    (1, 48, 1, kvd.OK),         # T = 1: any group, as the single-token plan
+])
+def test_plan_multi(lib, T, Hq, Hkv, expect):
+    n = ctypes.c_int(0)
+    ws = ctypes.c_size_t(0)
+    assert lib.kvd_decode_plan_multi(2, T, Hq, Hkv, 128, 1000, 152, 0, 0, ctypes.byref(n), ctypes.byref(ws)) == expect
+    if expect == kvd.OK and T > 1:
+        n1, ws1 = kvd.decode_plan(2, Hq, Hkv, 128, 1000, 152)
+        assert n.value == n1 and ws.value >= T * (ws1 - 512)
+
+
+@pytest.mark.parametrize("T,over,expect", [
+    (0, dict(), kvd.ERR_INVALID_ARG),
+    (5, dict(), kvd.ERR_UNSUPPORTED),       # T * G = 20 > 16 (G = 4)
+    (2, dict(q=None), kvd.ERR_INVALID_ARG),
+    (2, dict(ws_bytes=16), kvd.ERR_WORKSPACE_TOO_SMALL),
+])
+def test_decode_multi_rejects(lib, T, over, expect):
+    a = _dec_args(**over)
+    assert lib.kvd_decode_attention_multi(*(a[:5] + [T] + a[5:])) == expect

@@ -1,0 +1,116 @@
+"""Multi-token decode on the GPU (T drafted tokens per sequence, causal among
+them), through the C ABI, against the oracle; T = 1 against the single-token
+calls bit for bit. Shapes cover the head dimensions and groups the mma.sync
+kernel takes (T * G <= 16), ragged lengths down to T, and split and unsplit
+pairs."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from gpu_helpers import assert_close, bf16_tensor_bits, cuda_or_skip, to_dev_bf16
+from workloads import bf16_bits_to_f32
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    # name, B, Hq, Hkv, D, S, lengths lo..hi, seed, T
+    ("g4t4", 6, 32, 8, 128, 700, 4, 700, 61, 4),
+    ("mha_t8", 5, 6, 6, 64, 400, 8, 400, 62, 8),
+    ("g2t3d256", 4, 8, 4, 256, 300, 3, 300, 63, 3),
+    ("g8t2", 7, 16, 2, 128, 900, 2, 900, 64, 2),
+    ("g1t16", 3, 4, 4, 128, 500, 16, 500, 65, 16),
+]
+
+
+def _run(mi, dev, out_dtype, n_split, fused=True):
+    import torch
+    import kv_cache_decode_gb300 as kvd
+    q, kc, vc, kn, vn = (to_dev_bf16(x, dev) for x in (mi.q, mi.k_cache, mi.v_cache, mi.k_new, mi.v_new))
+    pos = torch.from_numpy(mi.pos).to(dev)
+    lens = torch.from_numpy(mi.seq_lens).to(dev)
+    B, T, Hq, D = mi.q.shape
+    S, Hkv = mi.k_cache.shape[1], mi.k_cache.shape[2]
+    tdt = torch.bfloat16 if out_dtype == "bf16" else torch.float32
+    out = torch.full((B, T, Hq, D), float("nan"), dtype=tdt, device=dev)
+    lse = torch.full((B, T, Hq), float("nan"), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    _, nbytes = kvd.decode_plan_multi(B, T, Hq, Hkv, D, S, 0, n_split, out_dtype)
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    if fused:
+        kvd.decode_step_multi(q, kc, vc, kn, vn, pos, lens, S, mi.workload.scale, out, workspace=ws,
+                              n_split=n_split, lse=lse, status=status)
+    else:
+        kvd.kv_append_multi(kc, vc, kn, vn, pos, status=status)
+        kvd.decode_attention_multi(q, kc, vc, lens, S, mi.workload.scale, out, workspace=ws, n_split=n_split,
+                                   lse=lse, status=status)
+    torch.cuda.synchronize()
+    o = bf16_tensor_bits(out) if out_dtype == "bf16" else out.cpu().numpy()
+    return o, lse.cpu().numpy(), bf16_tensor_bits(kc), bf16_tensor_bits(vc), int(status.item())
+
+
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+@pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
+def test_multi_step_matches_oracle(case, out_dtype):
+    dev = cuda_or_skip()
+    name, B, Hq, Hkv, D, S, lo, hi, seed, T = case
+    mi = workloads.multi_step_inputs(workloads.Workload(name, B, Hq, Hkv, D, S, lo, hi, seed), T)
+    kc, vc, skipped = oracle.kv_append_multi(mi.k_cache, mi.v_cache, mi.k_new, mi.v_new, mi.pos)
+    assert skipped == 0
+    want, want_lse = oracle.decode_attention_multi(mi.q, kc, vc, mi.seq_lens, mi.workload.scale)
+    for n_split in (0, 7):
+        o, l, gk, gv, status = _run(mi, dev, out_dtype, n_split)
+        assert status == 0
+        assert np.array_equal(gk, kc) and np.array_equal(gv, vc), "caches after the append"
+        o64 = bf16_bits_to_f32(o).astype(np.float64) if out_dtype == "bf16" else o.astype(np.float64)
+        assert_close(o64.reshape(B, T * Hq, D), want.reshape(B, T * Hq, D), out_dtype, f"{name} n_split {n_split}")
+        tol = 4e-3 if out_dtype == "bf16" else 1e-4
+        assert np.max(np.abs(l - want_lse)) < tol
+
+
+@pytest.mark.parametrize("case", [CASES[0], CASES[4]], ids=["g4t4", "g1t16"])
+def test_multi_step_equals_two_calls(case):
+    dev = cuda_or_skip()
+    name, B, Hq, Hkv, D, S, lo, hi, seed, T = case
+    mi = workloads.multi_step_inputs(workloads.Workload(name, B, Hq, Hkv, D, S, lo, hi, seed), T)
+    a = _run(mi, dev, "f32", 5, fused=True)
+    b = _run(mi, dev, "f32", 5, fused=False)
+    for x, y, what in zip(a[:4], b[:4], ("out", "lse", "k", "v")):
+        assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8)), what
+    assert a[4] == b[4] == 0
+
+
+def test_multi_one_token_is_the_single_token_call():
+    import torch
+    import kv_cache_decode_gb300 as kvd
+    dev = cuda_or_skip()
+    w = workloads.Workload("one", 5, 32, 8, 128, 600, 1, 600, 66)
+    mi = workloads.multi_step_inputs(w, 1)
+    a = _run(mi, dev, "bf16", 7)
+    q, kc, vc, kn, vn = (to_dev_bf16(x, dev) for x in (mi.q[:, 0], mi.k_cache, mi.v_cache, mi.k_new[:, 0], mi.v_new[:, 0]))
+    out = torch.full(q.shape, float("nan"), dtype=torch.bfloat16, device=dev)
+    lse = torch.full(q.shape[:2], float("nan"), dtype=torch.float32, device=dev)
+    ws = kvd.alloc_workspace(q, kc, w.S_max, 7)
+    kvd.decode_step(q, kc, vc, kn, vn, torch.from_numpy(mi.pos).to(dev), torch.from_numpy(mi.seq_lens).to(dev),
+                    w.S_max, w.scale, out, workspace=ws, n_split=7, lse=lse)
+    torch.cuda.synchronize()
+    assert np.array_equal(a[0][:, 0], bf16_tensor_bits(out))
+    assert np.array_equal(a[1][:, 0].view(np.uint32), lse.cpu().numpy().view(np.uint32))
+
+
+def test_multi_rows_past_capacity_are_skipped():
+    import torch
+    import kv_cache_decode_gb300 as kvd
+    dev = cuda_or_skip()
+    w = workloads.Workload("cap", 3, 8, 2, 128, 64, 4, 64, 67)
+    mi = workloads.multi_step_inputs(w, 4, lens=np.array([64, 10, 4], np.int32))
+    pos = mi.pos.copy()
+    pos[1] = 62  # rows 62, 63 fit, 64 and 65 do not
+    kc, vc = to_dev_bf16(mi.k_cache, dev), to_dev_bf16(mi.v_cache, dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kvd.kv_append_multi(kc, vc, to_dev_bf16(mi.k_new, dev), to_dev_bf16(mi.v_new, dev),
+                        torch.from_numpy(pos).to(dev), status=status)
+    torch.cuda.synchronize()
+    ek, ev, skipped = oracle.kv_append_multi(mi.k_cache, mi.v_cache, mi.k_new, mi.v_new, pos)
+    assert skipped == 2 and int(status.item()) == 0x2
+    assert np.array_equal(bf16_tensor_bits(kc), ek) and np.array_equal(bf16_tensor_bits(vc), ev)

@@ -41,7 +41,7 @@ from typing import Dict, Iterable, List, Optional
 import numpy as np
 
 # Stream tags.
-_TAG_LEN, _TAG_Q, _TAG_K, _TAG_V, _TAG_KMASK = 0, 1, 2, 3, 4
+_TAG_LEN, _TAG_Q, _TAG_K, _TAG_V, _TAG_KMASK, _TAG_QM = 0, 1, 2, 3, 4, 5
 
 #: bf16 quiet NaN. Cache slots past a sequence's length are filled with it in
 #: tests, so that any read beyond the valid length poisons the result.
@@ -285,3 +285,47 @@ def paged_step_inputs(inp: StepInputs, page_size: int, seed: int = 0, spare: int
             kp[page, :rows.shape[0]] = rows
             vp[page, :rows.shape[0]] = inp.v_cache[b, j * P:(j + 1) * P]
     return PagedStepInputs(inp, P, kp, vp, table)
+
+
+@dataclass
+class MultiStepInputs:
+    """One multi-token step: T new tokens per sequence (bf16 bits).
+
+    The cache holds the first ``seq_lens[b] - T`` rows; the T new rows
+    (``k_new``/``v_new`` [B, T, Hkv, D]) go to ``pos[b] = seq_lens[b] - T``
+    onward, and ``q`` [B, T, Hq, D] holds the T queries.
+    """
+    workload: Workload
+    T: int
+    q: np.ndarray
+    k_cache: np.ndarray
+    v_cache: np.ndarray
+    k_new: np.ndarray
+    v_new: np.ndarray
+    pos: np.ndarray
+    seq_lens: np.ndarray
+
+
+def multi_step_inputs(w: Workload, T: int, lens: Optional[np.ndarray] = None,
+                      pad_bits: int = BF16_NAN) -> MultiStepInputs:
+    """A step with T new tokens per sequence: lengths drawn as for the
+    workload (or ``lens``), each at least T; the last T rows of each sequence's
+    key/value draw are the new tokens, and its T queries come from a stream of
+    their own."""
+    L = (seq_lens(w) if lens is None else np.asarray(lens, dtype=np.int32)).astype(np.int32)
+    if (L < T).any() or (L > w.S_max).any():
+        raise ValueError("lengths must lie in [T, S_max]")
+    B = w.B
+    q = np.empty((B, T, w.Hq, w.D), dtype=np.uint16)
+    kc = np.full((B, w.S_max, w.Hkv, w.D), pad_bits, dtype=np.uint16)
+    vc = np.full((B, w.S_max, w.Hkv, w.D), pad_bits, dtype=np.uint16)
+    kn = np.zeros((B, T, w.Hkv, w.D), dtype=np.uint16)
+    vn = np.zeros((B, T, w.Hkv, w.D), dtype=np.uint16)
+    for b in range(B):
+        r = _rng(w.seed, _TAG_QM, b)
+        q[b] = f32_to_bf16_bits(r.standard_normal((T, w.Hq, w.D), dtype=np.float32))
+        Lb = int(L[b])
+        k, v = kv_rows(w, b, Lb)
+        kc[b, :Lb - T], vc[b, :Lb - T] = k[:Lb - T], v[:Lb - T]
+        kn[b], vn[b] = k[Lb - T:], v[Lb - T:]
+    return MultiStepInputs(w, T, q, kc, vc, kn, vn, (L - T).astype(np.int32), L)
