@@ -60,6 +60,8 @@ def parse_args():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--page-size", type=int, default=0,
                     help="paged KV cache with pages of this many tokens; 0 = contiguous")
+    ap.add_argument("--tokens", type=int, default=1,
+                    help="query tokens per sequence (T > 1: a speculative check step; T * G <= 16)")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "int8"],
                     help="int8: the cache quantized per (token, KV head) row (groups <= 16)")
     ap.add_argument("--page-order", default="shuffled", choices=["shuffled", "sequential"],
@@ -264,8 +266,13 @@ def run_ours(args):
     w = workloads.get(args.config)
     if args.batch:
         w = w.with_batch(min(args.batch, w.B))
-    inp = workloads.step_inputs(w, pad_bits=0)
-    B, Hq, D = inp.q.shape
+    T = args.tokens
+    multi = T > 1
+    if multi and (args.page_size or args.kv_dtype != "bf16"):
+        raise SystemExit("--tokens > 1 takes a contiguous bf16 cache")
+    # T > 1: the same lengths, the last T tokens of each sequence new this step
+    inp = (workloads.multi_step_inputs(w, T, pad_bits=0) if multi else workloads.step_inputs(w, pad_bits=0))
+    B, Hq, D = inp.q.shape[0], inp.q.shape[-2], inp.q.shape[-1]
     S, Hkv = inp.k_cache.shape[1], inp.k_cache.shape[2]
     lens_np = inp.seq_lens
     max_len = int(w.S_max)
@@ -275,6 +282,8 @@ def run_ours(args):
     step_bytes = (roofline.attention_step_bytes_q8(lens_np, Hq, Hkv, D) if int8
                   else roofline.attention_step_bytes(lens_np, Hq, Hkv, D))
     kv_bytes = roofline.attention_kv_bytes(lens_np, Hkv, D) // (2 if int8 else 1)
+    if multi:
+        step_bytes += 2 * B * (T - 1) * Hq * D * 2  # T queries in and T output rows out; the cache once
     append_bytes = roofline.append_bytes(B, Hkv, D)
     flops = roofline.attention_step_flops(lens_np, Hq, D)
 
@@ -318,14 +327,20 @@ def run_ours(args):
     pos = torch.from_numpy(inp.pos).to(dev)
     lens = torch.from_numpy(lens_np).to(dev)
     out_t = torch.bfloat16 if args.out_dtype == "bf16" else torch.float32
-    out = torch.empty((B, Hq, D), dtype=out_t, device=dev)
-    n_split, ws_bytes = kvd.decode_plan(B, Hq, Hkv, D, max_len, 0, args.n_split, args.out_dtype)
+    out = torch.empty(inp.q.shape, dtype=out_t, device=dev)
+    if multi:
+        n_split, ws_bytes = kvd.decode_plan_multi(B, T, Hq, Hkv, D, max_len, 0, args.n_split, args.out_dtype)
+    else:
+        n_split, ws_bytes = kvd.decode_plan(B, Hq, Hkv, D, max_len, 0, args.n_split, args.out_dtype)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     launches_per_step = 2 + (1 if n_split > 1 else 0)
 
     def step(r, stream=None):
         # append the new token's K/V rows, then attend (one call, three launches)
-        if int8:
+        if multi:
+            kvd.decode_step_multi(q, kcs[r], vcs[r], kn, vn, pos, lens, max_len, w.scale, out, workspace=ws,
+                                  n_split=args.n_split, stream=stream)
+        elif int8:
             kq, vq, ks, vs = q8[r]
             kvd.decode_step_q8(q, kq, vq, ks, vs, kn, vn, pos, lens, max_len, w.scale, out, workspace=ws,
                                n_split=args.n_split, stream=stream)
@@ -384,6 +399,14 @@ def run_ours(args):
     torch.cuda._sleep(int(2e6 + 2e5 * args.steps))  # let the host queue ahead of the GPU
     for i in range(args.steps):
         r = i % R
+        if multi:
+            # no separate multi-token chunk entry point: the whole attention call is timed
+            kvd.kv_append_multi(kcs[r], vcs[r], kn, vn, pos)
+            ea[i].record(stream)
+            kvd.decode_attention_multi(q, kcs[r], vcs[r], lens, max_len, w.scale, out, workspace=ws,
+                                       n_split=args.n_split)
+            eb[i].record(stream)
+            continue
         if int8:
             # no separate int8 chunk entry point: the whole attention call is timed
             kq, vq, ks, vs = q8[r]
@@ -417,7 +440,7 @@ def run_ours(args):
 
     ms_per_step = total_ms / args.steps
     value = job_rate_gbs(world, step_bytes, ms_per_step)
-    tokens_per_s = world * B / (ms_per_step * 1e-3)
+    tokens_per_s = world * B * T / (ms_per_step * 1e-3)  # query tokens scored per second
 
     # ---- end to end through the public API with host buffers ----
     e2e = None
@@ -459,16 +482,16 @@ def run_ours(args):
         e2e_ms, = max_over_ranks([e2e_ms], device=dev)
         e2e = {"value": round(job_rate_gbs(world, step_bytes, e2e_ms), 2), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": round(e2e_ms, 4), "tokens_per_s": round(world * B / (e2e_ms * 1e-3), 1)}
+               "ms_per_step": round(e2e_ms, 4), "tokens_per_s": round(world * B * T / (e2e_ms * 1e-3), 1)}
 
     if rank != 0:
         return
 
     peak, peak_kind = measured_peaks()
     achieved = step_bytes / (chunk_avg_ms * 1e-3) / 1e9
-    traffic = None if (paged or int8) else ncu_traffic(w.name)
+    traffic = None if (paged or int8 or multi) else ncu_traffic(w.name)
     cpu = None
-    if not args.no_cpu_baseline and not int8:
+    if not args.no_cpu_baseline and not int8 and not multi:
         gbs, sec, n_rows, cores, passes = oracle_rate(w, inp, budget_s=10.0, repeats=1,
                                                       min_total_s=10.0)
         cpu = {"value": round(gbs, 5), "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -488,13 +511,14 @@ def run_ours(args):
                    "timing": "CUDA graph per step, CUDA events on the replay stream",
                    "kv_layout": (f"paged: {args.page_size}-token pages, {pinp.k_pages.shape[0]} pages "
                                  f"in {args.page_order} order" if paged else "contiguous"),
-                   "kv_dtype": args.kv_dtype},
+                   "kv_dtype": args.kv_dtype, "query_tokens": T},
         "tokens_per_s": round(tokens_per_s, 1),
         "hbm_frac_of_step": round(value / world / peak, 4),
         "step_bytes": int(step_bytes), "append_bytes": int(append_bytes), "flops": int(flops),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": ("split_kv_chunk + split_kv_merge (int8)" if int8 else
+                     "kernel": ("split_kv_chunk + split_kv_merge (multi-token)" if multi else
+                                "split_kv_chunk + split_kv_merge (int8)" if int8 else
                                 "split_kv_chunk + split_kv_merge (paged)" if paged else "split_kv_chunk"),
                      "peak_source": f"{peak_kind} copy bandwidth",
                      "kernel_ms": round(chunk_avg_ms, 5)},
