@@ -114,3 +114,37 @@ def test_multi_rows_past_capacity_are_skipped():
     ek, ev, skipped = oracle.kv_append_multi(mi.k_cache, mi.v_cache, mi.k_new, mi.v_new, pos)
     assert skipped == 2 and int(status.item()) == 0x2
     assert np.array_equal(bf16_tensor_bits(kc), ek) and np.array_equal(bf16_tensor_bits(vc), ev)
+
+
+def test_multi_short_sequences_give_empty_rows():
+    """A sequence shorter than T: its first query tokens see no token (zero rows,
+    lse -inf), the rest see what exists; rows appended before position 0 are
+    skipped."""
+    import torch
+    import kv_cache_decode_gb300 as kvd
+    dev = cuda_or_skip()
+    T = 4
+    w = workloads.Workload("short_mt", 3, 8, 2, 128, 64, 4, 64, 68)
+    mi = workloads.multi_step_inputs(w, T, lens=np.array([4, 9, 6], np.int32))
+    lens = np.array([2, 9, 0], np.int32)  # sequence 0 holds 2 tokens after the step, sequence 2 none
+    pos = lens - T                        # -2, 5, -4: rows before position 0 are skipped
+    q, kc, vc, kn, vn = (to_dev_bf16(x, dev) for x in (mi.q, mi.k_cache, mi.v_cache, mi.k_new, mi.v_new))
+    out = torch.full(mi.q.shape, float("nan"), dtype=torch.float32, device=dev)
+    lse = torch.full(mi.q.shape[:3], float("nan"), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    B, _, Hq, D = mi.q.shape
+    _, nbytes = kvd.decode_plan_multi(B, T, Hq, 2, D, 64, 0, 3, "f32")
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    kvd.decode_step_multi(q, kc, vc, kn, vn, torch.from_numpy(pos.astype(np.int32)).to(dev),
+                          torch.from_numpy(lens).to(dev), 64, w.scale, out, workspace=ws, n_split=3, lse=lse,
+                          status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0x2
+    ekc, evc, skipped = oracle.kv_append_multi(mi.k_cache, mi.v_cache, mi.k_new, mi.v_new, pos)
+    assert skipped == 2 + 4
+    want, want_lse = oracle.decode_attention_multi(mi.q, ekc, evc, lens, w.scale)
+    got = out.cpu().numpy().astype(np.float64)
+    assert_close(got.reshape(B, T * Hq, D), want.reshape(B, T * Hq, D), "f32", "short multi")
+    l = lse.cpu().numpy()
+    assert np.all(np.isneginf(l[0, :2])) and np.all(np.isneginf(l[2])) and np.all(got[0, :2] == 0)
+    assert np.max(np.abs(l[np.isfinite(want_lse)] - want_lse[np.isfinite(want_lse)])) < 1e-4
