@@ -305,6 +305,40 @@ kvd_status kvd_decode_step_multi(void* k_cache, void* v_cache, const void* k_new
                                  kvd_stream_t stream);
 
 /*
+ * kvd_decode_ex: one entry point for every combination of the cache forms and
+ * options above that the kernels support, with the cache described by a
+ * struct:
+ *   - bf16 or int8 (k_scales and v_scales non-NULL: k and v hold int8 codes);
+ *   - contiguous (block_table NULL: k, v [batch, s_max, Hkv, D]) or paged
+ *     (k, v are page pools; bf16 only);
+ *   - n_tokens query tokens per sequence (layouts as kvd_decode_attention_multi;
+ *     T * G <= 16 for T > 1);
+ *   - with the step's append (k_new, v_new and pos all non-NULL; the new rows,
+ *     [batch, n_tokens, Hkv, D] bf16, are appended, quantized for an int8
+ *     cache, before the attention, as kvd_decode_step) or without it (all three
+ *     NULL).
+ * Each combination is bit-identical to the dedicated call where one exists.
+ * Errors: KVD_ERR_INVALID_ARG for a NULL cache, a cache description that fails
+ * the dedicated calls' checks, or only some of k_new, v_new, pos given;
+ * KVD_ERR_UNSUPPORTED for a paged int8 cache; the rest as the dedicated calls.
+ */
+typedef struct kvd_cache {
+    void* k;                       /* bf16 cache or page pool, or int8 codes */
+    void* v;
+    float* k_scales;               /* int8: float32 [batch, s_max, Hkv]; NULL for bf16 */
+    float* v_scales;
+    const int32_t* block_table;    /* paged: int32 [batch, max_blocks]; NULL for contiguous */
+    int s_max;                     /* contiguous: capacity of each sequence */
+    int max_blocks, page_size, num_pages;  /* paged */
+} kvd_cache;
+
+kvd_status kvd_decode_ex(const kvd_cache* cache, const void* q, const int32_t* seq_lens, int batch, int n_tokens,
+                         int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim, float scale, int n_split,
+                         void* workspace, size_t workspace_bytes, void* out, kvd_out_dtype out_dtype,
+                         float* lse_out, const void* k_new, const void* v_new, const int32_t* pos,
+                         int32_t* status_word, kvd_stream_t stream);
+
+/*
  * The two launches of kvd_decode_attention, exposed separately so that each
  * can be timed on its own. Arguments and errors are those of
  * kvd_decode_attention; calling kvd_split_kv_chunk then kvd_split_kv_merge on

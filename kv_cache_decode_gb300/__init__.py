@@ -32,7 +32,7 @@ EXPORTED = (
     "kvd_version", "kvd_decode_attention_static", "kvd_decode_step", "kvd_kv_append_paged",
     "kvd_decode_attention_paged", "kvd_decode_step_paged", "kvd_kv_quantize_q8", "kvd_kv_append_q8",
     "kvd_decode_attention_q8", "kvd_decode_step_q8", "kvd_decode_plan_multi", "kvd_kv_append_multi",
-    "kvd_decode_attention_multi", "kvd_decode_step_multi",
+    "kvd_decode_attention_multi", "kvd_decode_step_multi", "kvd_decode_ex",
 )
 STATIC_WORKSPACE_BYTES = 16 << 20  # KVD_STATIC_WORKSPACE_BYTES
 
@@ -61,6 +61,13 @@ def load(path: str = LIB_PATH):
             raise RuntimeError(f"{path} is older than its sources: rebuild it")
         _lib = _declare(ctypes.CDLL(path))
         return _lib
+
+
+class _CCache(ctypes.Structure):
+    """struct kvd_cache of kvdecode.h."""
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("k_scales", ctypes.c_void_p),
+                ("v_scales", ctypes.c_void_p), ("block_table", ctypes.c_void_p), ("s_max", ctypes.c_int),
+                ("max_blocks", ctypes.c_int), ("page_size", ctypes.c_int), ("num_pages", ctypes.c_int)]
 
 
 def _declare(lib):
@@ -102,6 +109,9 @@ def _declare(lib):
     lib.kvd_decode_attention_multi.restype = I
     lib.kvd_decode_step_multi.argtypes = [P, P, P, P, P, P, P, I, I] + dec[5:]
     lib.kvd_decode_step_multi.restype = I
+    lib.kvd_decode_ex.argtypes = [ctypes.POINTER(_CCache), P, P, I, I, I, I, I, I, F, I, P, SZ, P, I, P, P, P, P,
+                                  P, P]
+    lib.kvd_decode_ex.restype = I
     lib.kvd_schedule_describe.argtypes = [P, I, I, I, I, I, I, I, I, P, I, PI, PI]
     lib.kvd_kernel_info.argtypes = [I, I, I, I, PI, PI, PI, PI, PI, PI]
     lib.kvd_status_string.argtypes = [I]
@@ -548,6 +558,40 @@ def decode_step_multi(q, k_cache, v_cache, k_new, v_new, pos, seq_lens, max_seq_
     # (k_cache, v_cache, k_new, v_new, pos, q, seq_lens, batch, T, ...)
     args = [a[1], a[2], k_new.data_ptr(), v_new.data_ptr(), pos.data_ptr(), a[0], a[3], a[4], a[5]] + a[6:]
     _check(load().kvd_decode_step_multi(*args), "kvd_decode_step_multi")
+
+
+def decode_ex(q, k, v, seq_lens, max_seq_len: int, scale: float, out, *, k_scales=None, v_scales=None,
+              block_table=None, k_new=None, v_new=None, pos=None, workspace=None, n_split: int = 0, lse=None,
+              status=None, stream=None):
+    """Any supported combination in one call (kvd_decode_ex): q [B, Hq, D] or
+    [B, T, Hq, D]; k, v a contiguous cache [B, S_max, Hkv, D] (bf16, or int8 codes
+    with k_scales/v_scales [B, S_max, Hkv]) or, with block_table [B, max_blocks],
+    bf16 page pools [num_pages, page, Hkv, D]; k_new, v_new ([B, Hkv, D] or
+    [B, T, Hkv, D]) and pos to append first. Workspace: decode_plan_multi."""
+    import torch
+    T = q.shape[1] if q.dim() == 4 else 1
+    B, Hq, D = q.shape[0], q.shape[-2], q.shape[-1]
+    Hkv = k.shape[2]
+    c = _CCache()
+    c.k, c.v = k.data_ptr(), v.data_ptr()
+    c.k_scales, c.v_scales = _ptr(k_scales), _ptr(v_scales)
+    if block_table is not None:
+        _require(block_table, "block_table", torch.int32, 2)
+        c.block_table, c.max_blocks, c.page_size, c.num_pages = (block_table.data_ptr(), block_table.shape[1],
+                                                                   k.shape[1], k.shape[0])
+    else:
+        c.s_max = k.shape[1]
+    if out.shape != q.shape or k.shape[3] != D or v.shape != k.shape:
+        raise ValueError("decode_ex: inconsistent shapes")
+    code = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32 if out.dtype == torch.float32 else None
+    if code is None:
+        raise TypeError("out must be bfloat16 or float32")
+    ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(),
+                                                           workspace.numel() * workspace.element_size())
+    _check(load().kvd_decode_ex(ctypes.byref(c), q.data_ptr(), seq_lens.data_ptr(), B, T, int(max_seq_len), Hq,
+                                Hkv, D, float(scale), int(n_split), ws_ptr, ws_bytes, out.data_ptr(), code,
+                                _ptr(lse), _ptr(k_new), _ptr(v_new), _ptr(pos), _ptr(status),
+                                _stream_handle(stream)), "kvd_decode_ex")
 
 
 def decode_step(q, k_cache, v_cache, k_new, v_new, pos, seq_lens, max_seq_len: int, scale: float,

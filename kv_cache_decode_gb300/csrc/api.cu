@@ -185,6 +185,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     st = plan(batch, Hq, Hkv, D, max_seq_len, 0 /* query device if heuristic */, n_split_req, dt,
               &n_split, &need, &k, T);
     if (st != KVD_OK) return st;
+    if (pg && q8) return KVD_ERR_UNSUPPORTED;  // paged int8 caches are not built
     if (pg) k = pick_kernel(Hq, Hkv, D, dt, true);
     if (q8) {
         if (!q8->k_scale || !q8->v_scale || !aligned(q8->k_scale, 4) || !aligned(q8->v_scale, 4))
@@ -246,7 +247,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
         const PagedCache none{nullptr, 0, 0, 0};
         const cudaError_t e =
             q8 ? launch_append_q8(app->k_cache, app->v_cache, q8->k_scale, q8->v_scale, app->k_new, app->v_new,
-                                  app->pos, batch, s_max, Hkv, D, status, s)
+                                  app->pos, batch, s_max, Hkv, D, status, s, T)
                : launch_append(app->k_cache, app->v_cache, app->k_new, app->v_new, app->pos, batch, s_max, Hkv,
                                D, status, pg ? *pg : none, s, T);
         if (e != cudaSuccess) return KVD_ERR_CUDA;
@@ -350,6 +351,37 @@ kvd_status kvd_decode_step_multi(void* k_cache, void* v_cache, const void* k_new
     return decode(kBoth, q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q, n_heads_kv,
                   head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype, lse_out, status_word,
                   stream, &app, nullptr, nullptr, n_tokens);
+}
+
+kvd_status kvd_decode_ex(const kvd_cache* cache, const void* q, const int32_t* seq_lens, int batch, int n_tokens,
+                         int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim, float scale, int n_split,
+                         void* workspace, size_t workspace_bytes, void* out, kvd_out_dtype out_dtype,
+                         float* lse_out, const void* k_new, const void* v_new, const int32_t* pos,
+                         int32_t* status_word, kvd_stream_t stream) {
+    if (!cache) return KVD_ERR_INVALID_ARG;
+    const bool append = k_new || v_new || pos;
+    if (append && !(k_new && v_new && pos)) return KVD_ERR_INVALID_ARG;
+    if ((cache->k_scales != nullptr) != (cache->v_scales != nullptr)) return KVD_ERR_INVALID_ARG;
+    PagedCache pg;
+    int s_max = cache->s_max;
+    const bool paged = cache->block_table != nullptr;
+    if (paged) {
+        const kvd_status st = check_paged(cache->block_table, cache->max_blocks, cache->page_size,
+                                          cache->num_pages, &pg, &s_max);
+        if (st != KVD_OK) return st;
+    }
+    const QuantCache q8{cache->k_scales, cache->v_scales};
+    const bool int8 = cache->k_scales != nullptr;
+    if (paged && int8) return KVD_ERR_UNSUPPORTED;
+    AppendArgs app{cache->k, cache->v, k_new, v_new, pos};
+    if (append) {
+        const kvd_status st = check_append(cache->k, cache->v, k_new, v_new, pos, batch, s_max, n_heads_kv,
+                                           head_dim, status_word);
+        if (st != KVD_OK) return st;
+    }
+    return decode(kBoth, q, cache->k, cache->v, seq_lens, batch, s_max, max_seq_len, n_heads_q, n_heads_kv,
+                  head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype, lse_out, status_word,
+                  stream, append ? &app : nullptr, paged ? &pg : nullptr, int8 ? &q8 : nullptr, n_tokens);
 }
 
 kvd_status kvd_kv_quantize_q8(const void* cache, void* codes, float* scales, const int32_t* seq_lens, int batch,

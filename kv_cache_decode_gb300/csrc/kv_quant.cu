@@ -54,21 +54,24 @@ __global__ void __launch_bounds__(256) kv_append_q8_kernel(int8_t* __restrict__ 
                                                           const uint4* __restrict__ k_new,
                                                           const uint4* __restrict__ v_new,
                                                           const int32_t* __restrict__ pos, int B, int S_max,
-                                                          int Hkv, int32_t* status) {
+                                                          int Hkv, int32_t* status, int T) {
     // The attention kernel that follows may start; it waits for this grid
     // before reading the cache.
     pdl_launch_dependents();
     constexpr int VPR = D / 8;
-    const long long rows = 2LL * B * Hkv;  // (K or V, b, h)
+    const long long per = (long long)B * T * Hkv;  // new rows of one tensor: (b, token i, h)
+    const long long rows = 2 * per;
     const int sub = threadIdx.x % VPR;
     const long long groups = (long long)gridDim.x * (blockDim.x / VPR);
     for (long long g = (long long)blockIdx.x * (blockDim.x / VPR) + threadIdx.x / VPR;
          g - (threadIdx.x / VPR) < rows; g += groups) {
         const bool in = g < rows;
-        const int which = in ? (int)(g / ((long long)B * Hkv)) : 0;
-        const long long r = in ? g - (long long)which * B * Hkv : 0;  // b * Hkv + h
-        const int b = (int)(r / Hkv), h = (int)(r - (long long)b * Hkv);
-        const int t = in ? __ldg(pos + b) : 0;
+        const int which = in ? (int)(g / per) : 0;
+        const long long r = in ? g - which * per : 0;  // (b * T + i) * Hkv + h
+        const long long bi = r / Hkv;
+        const int h = (int)(r - bi * Hkv);
+        const int b = (int)(bi / T), i = (int)(bi - (long long)b * T);
+        const int t = in ? __ldg(pos + b) + i : 0;
         const bool ok = in && t >= 0 && t < S_max;
         if (in && !ok && status && which == 0 && h == 0 && sub == 0) atomicOr(status, KVD_STATUS_POS_OUT_OF_RANGE);
         const long long dst_row = ((long long)b * S_max + (ok ? t : 0)) * Hkv + h;
@@ -102,8 +105,8 @@ __global__ void __launch_bounds__(256) kv_quantize_q8_kernel(const uint4* __rest
 
 cudaError_t launch_append_q8(void* k_codes, void* v_codes, float* k_scale, float* v_scale, const void* k_new,
                              const void* v_new, const int32_t* pos, int B, int S_max, int Hkv, int D,
-                             int32_t* status, cudaStream_t stream) {
-    const long long rows = 2LL * B * Hkv;
+                             int32_t* status, cudaStream_t stream, int T) {
+    const long long rows = 2LL * B * T * Hkv;
     const int rows_per_block = 256 / (D / 8);
     long long blocks = (rows + rows_per_block - 1) / rows_per_block;
     if (blocks > 4096) blocks = 4096;
@@ -117,9 +120,9 @@ cudaError_t launch_append_q8(void* k_codes, void* v_codes, float* k_scale, float
     auto* kn = static_cast<const uint4*>(k_new);
     auto* vn = static_cast<const uint4*>(v_new);
     switch (D) {
-        case 64: return cudaLaunchKernelEx(&cfg, kv_append_q8_kernel<64>, kc, vc, k_scale, v_scale, kn, vn, pos, B, S_max, Hkv, status);
-        case 128: return cudaLaunchKernelEx(&cfg, kv_append_q8_kernel<128>, kc, vc, k_scale, v_scale, kn, vn, pos, B, S_max, Hkv, status);
-        case 256: return cudaLaunchKernelEx(&cfg, kv_append_q8_kernel<256>, kc, vc, k_scale, v_scale, kn, vn, pos, B, S_max, Hkv, status);
+        case 64: return cudaLaunchKernelEx(&cfg, kv_append_q8_kernel<64>, kc, vc, k_scale, v_scale, kn, vn, pos, B, S_max, Hkv, status, T);
+        case 128: return cudaLaunchKernelEx(&cfg, kv_append_q8_kernel<128>, kc, vc, k_scale, v_scale, kn, vn, pos, B, S_max, Hkv, status, T);
+        case 256: return cudaLaunchKernelEx(&cfg, kv_append_q8_kernel<256>, kc, vc, k_scale, v_scale, kn, vn, pos, B, S_max, Hkv, status, T);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -77,7 +77,7 @@ cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const
 // conversion quantizes rows t < seq_lens[b] of a bf16 cache.
 cudaError_t launch_append_q8(void* k_codes, void* v_codes, float* k_scale, float* v_scale, const void* k_new,
                              const void* v_new, const int32_t* pos, int B, int S_max, int Hkv, int D,
-                             int32_t* status, cudaStream_t stream);
+                             int32_t* status, cudaStream_t stream, int T = 1);
 cudaError_t launch_quantize_q8(const void* src, void* codes, float* scales, const int32_t* seq_lens, int B,
                                int S_max, int len_cap, int Hkv, int D, cudaStream_t stream);
 

@@ -304,3 +304,23 @@ def test_plan_multi(lib, T, Hq, Hkv, expect):
 def test_decode_multi_rejects(lib, T, over, expect):
     a = _dec_args(**over)
     assert lib.kvd_decode_attention_multi(*(a[:5] + [T] + a[5:])) == expect
+
+
+def test_decode_ex_rejects(lib):
+    c = kvd._CCache(k=FAKE, v=FAKE, s_max=64)
+    a = _dec_args()  # q, k, v, lens, B, S, maxlen, Hq, Hkv, D, scale, n_split, ws, ws_bytes, out, dt, lse, status, stream
+    def call(cache, kn=None, vn=None, pos=None, T=1, **over):
+        b = _dec_args(**over)
+        return lib.kvd_decode_ex(cache, b[0], b[3], b[4], T, b[6], b[7], b[8], b[9], b[10], b[11], b[12], b[13],
+                                 b[14], b[15], b[16], kn, vn, pos, b[17], b[18])
+    assert call(None) == kvd.ERR_INVALID_ARG
+    assert call(ctypes.byref(c), kn=FAKE) == kvd.ERR_INVALID_ARG            # only part of the append
+    cq = kvd._CCache(k=FAKE, v=FAKE, k_scales=FAKE, s_max=64)
+    assert call(ctypes.byref(cq)) == kvd.ERR_INVALID_ARG                    # one scale array only
+    cpq = kvd._CCache(k=FAKE, v=FAKE, k_scales=FAKE, v_scales=FAKE, block_table=FAKE, max_blocks=4,
+                      page_size=16, num_pages=10)
+    assert call(ctypes.byref(cpq)) == kvd.ERR_UNSUPPORTED                    # paged int8
+    cp = kvd._CCache(k=FAKE, v=FAKE, block_table=FAKE, max_blocks=4, page_size=24, num_pages=10)
+    assert call(ctypes.byref(cp)) == kvd.ERR_INVALID_ARG                     # page size not a power of two
+    assert call(ctypes.byref(c), T=5) == kvd.ERR_UNSUPPORTED                 # T * G = 20
+    assert call(ctypes.byref(c), B=0, ws=None, n_split=3) == kvd.OK          # batch 0: no-op
