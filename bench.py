@@ -61,9 +61,9 @@ def parse_args():
     ap.add_argument("--page-size", type=int, default=0,
                     help="paged KV cache with pages of this many tokens; 0 = contiguous")
     ap.add_argument("--tokens", type=int, default=1,
-                    help="query tokens per sequence (T > 1: a speculative check step; T * G <= 16)")
+                    help="query tokens per sequence (T > 1: a speculative check step; up to 64)")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "int8"],
-                    help="int8: the cache quantized per (token, KV head) row (groups <= 16)")
+                    help="int8: the cache quantized per (token, KV head) row")
     ap.add_argument("--page-order", default="shuffled", choices=["shuffled", "sequential"],
                     help="paged: pages in random order over the pool, or each sequence's pages in a row")
     return ap.parse_args()

@@ -64,6 +64,8 @@ typedef void* kvd_stream_t;
 /* Supported shapes: head_dim in {64, 128, 256}; n_heads_q a multiple of
  * n_heads_kv with group size n_heads_q / n_heads_kv <= 64. */
 #define KVD_MAX_GROUP 64
+/* Query tokens per sequence of the multi-token calls: 1 .. KVD_MAX_TOKENS. */
+#define KVD_MAX_TOKENS 64
 
 /*
  * kvd_decode_plan: split count and workspace size for kvd_decode_attention.
@@ -242,10 +244,11 @@ kvd_status kvd_decode_step_paged(void* k_pages, void* v_pages, const void* k_new
  * read back: q stays bf16, the cache rows are exact small integers times
  * their scale, and the kernels compute in f16 MMAs with fp32 accumulation,
  * with each score multiplied by its key row's scale and each weight by its
- * value row's scale. Groups of up to 16 query heads per KV head (the
- * mma.sync kernel; wider groups return KVD_ERR_UNSUPPORTED); head_dim 64,
- * 128 or 256; contiguous caches only. q must lie in f16's range (|q| <
- * 65504). Workspace, results and errors otherwise as the bf16 calls, plus
+ * value row's scale. Every supported group (the mma.sync kernel, one CTA per
+ * 16 query heads of a group and token run); head_dim 64, 128 or 256;
+ * contiguous caches only. The split count and workspace are kvd_decode_plan's.
+ * q must lie in f16's range (|q| < 65504). Results and errors otherwise as the
+ * bf16 calls, plus
  * KVD_ERR_INVALID_ARG for null or misaligned scale arrays.
  */
 kvd_status kvd_kv_quantize_q8(const void* cache, void* codes, float* scales, const int32_t* seq_lens, int batch,
@@ -278,9 +281,11 @@ kvd_status kvd_decode_step_q8(void* k_codes, void* v_codes, float* k_scales, flo
  *   lse_out   : optional fp32 [batch, T, n_heads_q]
  *   k_new, v_new : bf16 [batch, T, n_heads_kv, head_dim]
  * A query token that sees no token (L_b < T - i) gets a zero row and lse -inf.
- * Supported where T * (n_heads_q / n_heads_kv) <= 16 (the mma.sync kernel;
- * otherwise KVD_ERR_UNSUPPORTED); T = 1 is exactly the single-token call. The
- * workspace holds T times the rows: size it with kvd_decode_plan_multi. Rows of
+ * T from 1 to KVD_MAX_TOKENS (above: KVD_ERR_UNSUPPORTED), any supported
+ * group; T > 1 runs on the mma.sync kernel, one CTA per 16 of a pair's T * G
+ * rows and token run. T = 1 is exactly the single-token call. The split count
+ * is the single-token plan's, and the workspace holds T times the rows: size
+ * it with kvd_decode_plan_multi. Rows of
  * the append outside [0, s_max) are skipped with KVD_STATUS_POS_OUT_OF_RANGE.
  * Other arguments, results and errors as the single-token calls, plus
  * KVD_ERR_INVALID_ARG for n_tokens < 1.
@@ -312,7 +317,7 @@ kvd_status kvd_decode_step_multi(void* k_cache, void* v_cache, const void* k_new
  *   - contiguous (block_table NULL: k, v [batch, s_max, Hkv, D]) or paged
  *     (k, v are page pools; bf16 only);
  *   - n_tokens query tokens per sequence (layouts as kvd_decode_attention_multi;
- *     T * G <= 16 for T > 1);
+ *     1 .. KVD_MAX_TOKENS; workspace from kvd_decode_plan_multi);
  *   - with the step's append (k_new, v_new and pos all non-NULL; the new rows,
  *     [batch, n_tokens, Hkv, D] bf16, are appended, quantized for an int8
  *     cache, before the attention, as kvd_decode_step) or without it (all three

@@ -460,7 +460,7 @@ def _decode_q8_args(q, k_codes, v_codes, k_scales, v_scales, seq_lens, max_seq_l
 def decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, seq_lens, max_seq_len: int, scale: float, out,
                         workspace=None, n_split: int = 0, lse=None, status=None, stream=None):
     """decode_attention over an int8 cache (codes [B, S_max, Hkv, D] int8, scales
-    [B, S_max, Hkv] float32; a row reads back as scale * code). Groups <= 16."""
+    [B, S_max, Hkv] float32; a row reads back as scale * code). Any group."""
     tail = _decode_q8_args(q, k_codes, v_codes, k_scales, v_scales, seq_lens, max_seq_len, scale, n_split,
                            workspace, out, lse, status, stream)
     _check(load().kvd_decode_attention_q8(q.data_ptr(), k_codes.data_ptr(), v_codes.data_ptr(),
@@ -537,7 +537,7 @@ def _decode_multi_args(q, k_cache, v_cache, seq_lens, max_seq_len, scale, n_spli
 def decode_attention_multi(q, k_cache, v_cache, seq_lens, max_seq_len: int, scale: float, out, workspace=None,
                            n_split: int = 0, lse=None, status=None, stream=None):
     """T query tokens per sequence (q, out [B, T, Hq, D]); token i attends to the
-    first seq_lens[b] - T + 1 + i cached tokens. Needs T * G <= 16."""
+    first seq_lens[b] - T + 1 + i cached tokens. T from 1 to 64."""
     args = _decode_multi_args(q, k_cache, v_cache, seq_lens, max_seq_len, scale, n_split, workspace, out, lse,
                               status, stream)
     _check(load().kvd_decode_attention_multi(*args), "kvd_decode_attention_multi")

@@ -24,12 +24,14 @@ const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool
 }
 
 // The tcgen05 kernels take either cache form at run time (only their loads
-// differ); the mma.sync kernel has a compiled variant per form.
-// int8 caches run on the mma.sync kernel only (groups of up to 16).
-const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8) {
-    if (group < 1 || group > KVD_MAX_GROUP) return nullptr;
-    if (kv8) return (group <= 16 && !paged) ? mma_chunk_kernel(head_dim, f32_out, false, true) : nullptr;
-    return group <= 16 ? mma_chunk_kernel(head_dim, f32_out, paged, false) : tc_chunk_kernel(head_dim, f32_out, group);
+// differ); the mma.sync kernel has a compiled variant per form. int8 caches
+// (contiguous only) and T > 1 query tokens run on the mma.sync kernel, whose
+// CTAs take 16 of a pair's T * G rows each, for every group.
+const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8, int T) {
+    if (group < 1 || group > KVD_MAX_GROUP || T < 1) return nullptr;
+    if (kv8) return paged ? nullptr : mma_chunk_kernel(head_dim, f32_out, false, true);
+    if (group <= 16 || T > 1) return mma_chunk_kernel(head_dim, f32_out, paged, false);
+    return tc_chunk_kernel(head_dim, f32_out, group);
 }
 
 namespace {
@@ -53,9 +55,12 @@ kvd_status check_shape(int batch, int Hq, int Hkv, int D, kvd_out_dtype dt) {
 }
 
 // Both forms of a variant share their launch shape and schedule geometry, so
-// planning and the host replica use the contiguous one.
-const ChunkKernel* pick_kernel(int Hq, int Hkv, int D, kvd_out_dtype dt, bool paged = false, bool kv8 = false) {
-    return find_chunk_kernel(D, Hq / Hkv, dt == KVD_OUT_F32, paged, kv8);
+// planning and the host replica use the contiguous one. The split count is
+// planned for the single-token bf16 kernel of the shape whatever the cache
+// dtype and query tokens, so that one plan sizes every form's workspace.
+const ChunkKernel* pick_kernel(int Hq, int Hkv, int D, kvd_out_dtype dt, bool paged = false, bool kv8 = false,
+                               int T = 1) {
+    return find_chunk_kernel(D, Hq / Hkv, dt == KVD_OUT_F32, paged, kv8, T);
 }
 
 // int8 cache: the row scales of K and V.
@@ -172,27 +177,26 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     // Cache rows: batch * s_max, or the pool's pages * page size.
     const long long cache_rows = pg ? ((long long)pg->num_pages << pg->page_shift) : (long long)batch * s_max;
     if ((size_t)cache_rows * Hkv * D > ((size_t)1 << 62)) return KVD_ERR_INVALID_ARG;
-    // The tensor-core path addresses cache rows and query rows with 32-bit TMA coordinates.
-    if (Hq / Hkv > 16 && (cache_rows > 0x7fffffffLL || (long long)batch * Hq > 0x7fffffffLL))
-        return KVD_ERR_UNSUPPORTED;
 
     int n_split = 0;
     size_t need = 0;
     const ChunkKernel* k = nullptr;
-    // T > 1 query tokens: the mma.sync kernel, whose 16 rows per pair hold T * G.
     if (T < 1) return KVD_ERR_INVALID_ARG;
-    if (T > 1 && (Hq / Hkv) * T > 16) return KVD_ERR_UNSUPPORTED;
+    if (T > KVD_MAX_TOKENS) return KVD_ERR_UNSUPPORTED;
     st = plan(batch, Hq, Hkv, D, max_seq_len, 0 /* query device if heuristic */, n_split_req, dt,
               &n_split, &need, &k, T);
     if (st != KVD_OK) return st;
     if (pg && q8) return KVD_ERR_UNSUPPORTED;  // paged int8 caches are not built
-    if (pg) k = pick_kernel(Hq, Hkv, D, dt, true);
-    if (q8) {
-        if (!q8->k_scale || !q8->v_scale || !aligned(q8->k_scale, 4) || !aligned(q8->v_scale, 4))
-            return KVD_ERR_INVALID_ARG;
-        k = pick_kernel(Hq, Hkv, D, dt, false, true);
-    }
+    if (q8 && (!q8->k_scale || !q8->v_scale || !aligned(q8->k_scale, 4) || !aligned(q8->v_scale, 4)))
+        return KVD_ERR_INVALID_ARG;
+    k = pick_kernel(Hq, Hkv, D, dt, pg != nullptr, q8 != nullptr, T);
     if (!k) return KVD_ERR_UNSUPPORTED;
+    // The tensor-core path addresses cache rows and query rows with 32-bit TMA coordinates.
+    if (k->tensor_core && (cache_rows > 0x7fffffffLL || (long long)batch * Hq > 0x7fffffffLL))
+        return KVD_ERR_UNSUPPORTED;
+    // mma.sync kernel: 16 of a pair's T * G rows per CTA.
+    const int row_blocks = k->tensor_core ? 1 : (Hq / Hkv * T + 15) / 16;
+    if ((long long)n_split * row_blocks > 0x7fffffffLL) return KVD_ERR_INVALID_ARG;
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return KVD_ERR_WORKSPACE_TOO_SMALL;
         if (!aligned(workspace, 256)) return KVD_ERR_INVALID_ARG;
@@ -220,6 +224,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     p.lse = lse;
     p.status = status;
     p.T = T;
+    p.row_blocks = row_blocks;
     if (q8) {
         p.k_scale = q8->k_scale;
         p.v_scale = q8->v_scale;
@@ -307,7 +312,7 @@ kvd_status kvd_decode_plan_multi(int batch, int n_tokens, int n_heads_q, int n_h
                                  int max_seq_len, int num_sms, int n_split_request, kvd_out_dtype out_dtype,
                                  int* n_split_out, size_t* workspace_bytes_out) {
     if (!n_split_out || !workspace_bytes_out || n_tokens < 1) return KVD_ERR_INVALID_ARG;
-    if (n_heads_kv > 0 && n_tokens > 1 && (n_heads_q / n_heads_kv) * n_tokens > 16) return KVD_ERR_UNSUPPORTED;
+    if (n_tokens > KVD_MAX_TOKENS) return KVD_ERR_UNSUPPORTED;
     return plan(batch, n_heads_q, n_heads_kv, head_dim, max_seq_len, num_sms, n_split_request, out_dtype,
                 n_split_out, workspace_bytes_out, nullptr, n_tokens);
 }

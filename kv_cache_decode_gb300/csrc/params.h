@@ -43,6 +43,9 @@ struct DecodeParams {
     // of sequence b attends to its first seq_lens[b] - T + 1 + i tokens, and
     // the workspace holds T * G rows per slot.
     int T;
+    // mma.sync kernel: blocks of 16 of a pair's T * G rows, one CTA each per
+    // token run (n_split * row_blocks CTAs); 1 for the tcgen05 kernel.
+    int row_blocks;
 };
 
 // One compiled variant of the split-KV chunk kernel.
@@ -56,9 +59,12 @@ struct ChunkKernel {
     int index;  // position in the variant table (0..41), for the per-device attribute bitmask
 };
 
-// The kernel for a shape: groups of up to 16 query heads per KV head run on the
-// mma.sync kernel, wider groups (17..64) on the tcgen05 kernel.
-const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8 = false);
+// The kernel for a shape: single-token bf16 groups of up to 16 query heads per
+// KV head run on the mma.sync kernel, wider groups (17..64) on the tcgen05
+// kernel; int8 caches and T > 1 query tokens run on the mma.sync kernel for
+// every group, in blocks of 16 rows.
+const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8 = false,
+                                     int T = 1);
 const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool kv8);
 const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out, int group);
 

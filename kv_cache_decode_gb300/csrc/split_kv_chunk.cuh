@@ -176,12 +176,19 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int ht = warp / TS, ts = warp % TS;
-    const int c = blockIdx.x;
     const int G = p.G;
     // T query tokens per sequence (T > 1: a speculative check step): a pair
     // has T * G rows, row r being query token r / G of head r % G, and query
     // token i attends to the first L - T + 1 + i tokens.
     const int T = p.T, TG = T * G;
+    // Pairs with more rows than one CTA holds (HT * 16) are split into
+    // row_blocks blocks of rows: the CTAs of one token run are launched side by
+    // side, one per block, and read the same K/V rows (the later reads mostly
+    // from L2). Each writes the outputs or partial-state rows of its block.
+    constexpr int ROWS = HT * 16;
+    const int c = blockIdx.x / p.row_blocks;
+    const int rbase = (blockIdx.x - c * p.row_blocks) * ROWS;
+    const int rend = min(TG, rbase + ROWS);
     auto out_row = [&](int b, int h, int r) {  // row of out / lse ([B, T, Hq])
         const int i = r / G;
         return ((size_t)b * T + i) * p.Hq + (size_t)h * G + (r - i * G);
@@ -204,7 +211,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
         clamped |= (raw != L);
         mine += pair_extent(L, Geo{});
     }
-    if (clamped && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
+    if (clamped && blockIdx.x == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
     const long long total = block_sum_ll<NW>(mine, s_red) * p.Hkv;
     const int C_eff = effective_ctas(p.n_split, total);
     if (c >= C_eff) {
@@ -338,9 +345,9 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
         }
     };
 
-    // Zero output for an empty pair this CTA owns.
+    // Zero output for an empty pair this CTA owns (its block of rows).
     auto write_empty = [&](int b, int h) {
-        for (int i = tid; i < TG * D; i += NT) {
+        for (int i = rbase * D + tid; i < rend * D; i += NT) {
             const size_t e = out_row(b, h, i / D) * D + (i % D);
             if constexpr (F32OUT)
                 reinterpret_cast<float*>(p.out)[e] = 0.f;
@@ -348,7 +355,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                 reinterpret_cast<__nv_bfloat16*>(p.out)[e] = __float2bfloat16_rn(0.f);
         }
         if (p.lse)
-            for (int i = tid; i < TG; i += NT) p.lse[out_row(b, h, i)] = -CUDART_INF_F;
+            for (int i = rbase + tid; i < rend; i += NT) p.lse[out_row(b, h, i)] = -CUDART_INF_F;
     };
 
     // ---- per-warp state ----
@@ -360,7 +367,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
 #pragma unroll
     for (int kk = 0; kk < KS; ++kk) qf[kk][0] = qf[kk][1] = qf[kk][2] = qf[kk][3] = 0u;
 
-    const int r0 = ht * 16 + (lane >> 2);  // pair-local rows of this thread
+    const int r0 = rbase + ht * 16 + (lane >> 2);  // pair-local rows of this thread
     const int r1 = r0 + 8;
     const int cq0 = T - 1 - r0 / G, cq1 = T - 1 - r1 / G;  // tokens a row sees fewer than the last
     const float scale_log2 = p.scale_log2;

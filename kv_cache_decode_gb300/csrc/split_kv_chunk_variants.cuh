@@ -32,7 +32,7 @@ cudaError_t launch_mma_chunk(const ChunkKernel& k, const DecodeParams& p, cudaSt
     using C = ChunkConfig<D, 1>;
     constexpr int ST = KV8 ? C::STAGES8 : C::STAGES, MB = KV8 ? C::MINB8 : C::MINB;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)p.n_split, 1, 1);
+    cfg.gridDim = dim3((unsigned)(p.n_split * p.row_blocks), 1, 1);  // row blocks of one run side by side
     cfg.blockDim = dim3((unsigned)k.threads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)k.smem_bytes;
     cfg.stream = stream;

@@ -238,7 +238,7 @@ def _q8_args(ks=FAKE, vs=FAKE, **over):
 @pytest.mark.parametrize("over,expect", [
     (dict(ks=None), kvd.ERR_INVALID_ARG),
     (dict(vs=FAKE + 2), kvd.ERR_INVALID_ARG),          # scales not 4-byte aligned
-    (dict(Hq=34, Hkv=2), kvd.ERR_UNSUPPORTED),         # group 17: int8 runs on groups <= 16 only
+    (dict(Hq=130, Hkv=2), kvd.ERR_UNSUPPORTED),        # group 65 > KVD_MAX_GROUP
     (dict(D=96), kvd.ERR_UNSUPPORTED),
     (dict(q=None), kvd.ERR_INVALID_ARG),
     (dict(k=FAKE + 8), kvd.ERR_INVALID_ARG),
@@ -281,9 +281,12 @@ def test_append_q8_rejects(lib, args, expect):
 
 @pytest.mark.parametrize("T,Hq,Hkv,expect", [
     (0, 8, 2, kvd.ERR_INVALID_ARG),
-    (4, 8, 2, kvd.OK),          # T * G = 16
-    (5, 8, 2, kvd.ERR_UNSUPPORTED),
-    (2, 48, 1, kvd.ERR_UNSUPPORTED),
+    (4, 8, 2, kvd.OK),          # T * G = 16: one block of rows
+    (5, 8, 2, kvd.OK),          # T * G = 20: two blocks of rows
+    (2, 48, 1, kvd.OK),         # MQA, T * G = 96: six blocks
+    (64, 64, 1, kvd.OK),        # the largest: KVD_MAX_TOKENS x KVD_MAX_GROUP
+    (65, 8, 2, kvd.ERR_UNSUPPORTED),  # T > KVD_MAX_TOKENS
+    (2, 130, 2, kvd.ERR_UNSUPPORTED),  # group 65
     (1, 48, 1, kvd.OK),         # T = 1: any group, as the single-token plan
 ])
 def test_plan_multi(lib, T, Hq, Hkv, expect):
@@ -297,7 +300,7 @@ def test_plan_multi(lib, T, Hq, Hkv, expect):
 
 @pytest.mark.parametrize("T,over,expect", [
     (0, dict(), kvd.ERR_INVALID_ARG),
-    (5, dict(), kvd.ERR_UNSUPPORTED),       # T * G = 20 > 16 (G = 4)
+    (65, dict(), kvd.ERR_UNSUPPORTED),      # T > KVD_MAX_TOKENS
     (2, dict(q=None), kvd.ERR_INVALID_ARG),
     (2, dict(ws_bytes=16), kvd.ERR_WORKSPACE_TOO_SMALL),
 ])
@@ -322,5 +325,5 @@ def test_decode_ex_rejects(lib):
     assert call(ctypes.byref(cpq)) == kvd.ERR_UNSUPPORTED                    # paged int8
     cp = kvd._CCache(k=FAKE, v=FAKE, block_table=FAKE, max_blocks=4, page_size=24, num_pages=10)
     assert call(ctypes.byref(cp)) == kvd.ERR_INVALID_ARG                     # page size not a power of two
-    assert call(ctypes.byref(c), T=5) == kvd.ERR_UNSUPPORTED                 # T * G = 20
+    assert call(ctypes.byref(c), T=65) == kvd.ERR_UNSUPPORTED                # T > KVD_MAX_TOKENS
     assert call(ctypes.byref(c), B=0, ws=None, n_split=3) == kvd.OK          # batch 0: no-op

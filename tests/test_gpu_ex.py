@@ -17,13 +17,13 @@ def _ws(kvd, torch, B, T, Hq, Hkv, D, S, dev, out_dtype="bf16"):
     return torch.empty(max(n, 1), dtype=torch.uint8, device=dev)
 
 
-@pytest.mark.parametrize("page", [16, 64])
-def test_paged_multi_equals_contiguous_multi(page):
+@pytest.mark.parametrize("page,Hq,Hkv,D,T", [(16, 32, 8, 128, 4), (64, 32, 8, 128, 4), (32, 48, 1, 256, 2)],
+                         ids=["p16_g4t4", "p64_g4t4", "p32_mqa48t2"])
+def test_paged_multi_equals_contiguous_multi(page, Hq, Hkv, D, T):
     import torch
     import kv_cache_decode_gb300 as kvd
     dev = cuda_or_skip()
-    T = 4
-    w = workloads.Workload("pm", 6, 32, 8, 128, 700, 4, 700, 71)
+    w = workloads.Workload("pm", 6, Hq, Hkv, D, 700, T, 700, 71)
     mi = workloads.multi_step_inputs(w, T)
     B, _, Hq, D = mi.q.shape
     S, Hkv = mi.k_cache.shape[1], mi.k_cache.shape[2]
@@ -49,12 +49,12 @@ def test_paged_multi_equals_contiguous_multi(page):
     assert np.array_equal(bf16_tensor_bits(got), bf16_tensor_bits(ref))
 
 
-def test_int8_multi_matches_oracle():
+@pytest.mark.parametrize("Hq,Hkv,D,T", [(16, 4, 128, 3), (48, 1, 256, 2)], ids=["g4t3", "mqa48t2"])
+def test_int8_multi_matches_oracle(Hq, Hkv, D, T):
     import torch
     import kv_cache_decode_gb300 as kvd
     dev = cuda_or_skip()
-    T = 3
-    w = workloads.Workload("qm", 5, 16, 4, 128, 600, 3, 600, 72)
+    w = workloads.Workload("qm", 5, Hq, Hkv, D, 600, T, 600, 72)
     mi = workloads.multi_step_inputs(w, T)
     B, _, Hq, D = mi.q.shape
     S, Hkv = mi.k_cache.shape[1], mi.k_cache.shape[2]

@@ -46,11 +46,12 @@ def test_paged_full_size_equals_contiguous(name, page):
     assert np.array_equal(got, ref)
 
 
-def test_int8_gqa_full_size():
+@pytest.mark.parametrize("name", ["gqa", "palm"])
+def test_int8_full_size(name):
     import torch
     import kv_cache_decode_gb300 as kvd
     dev = cuda_or_skip()
-    w = workloads.get("gqa")
+    w = workloads.get(name)
     inp = workloads.step_inputs(w)
     B, S, Hkv, D = inp.k_cache.shape
     cached = torch.from_numpy(np.maximum(inp.seq_lens - 1, 0).astype(np.int32)).to(dev)
@@ -70,7 +71,7 @@ def test_int8_gqa_full_size():
     assert int(status.item()) == 0
     got = bf16_bits_to_f32(bf16_tensor_bits(out)).astype(np.float64)
     L = inp.seq_lens
-    rows = sorted({int(np.argmin(L)), int(np.argmax(L)), 17, 100})
+    rows = sorted({int(np.argmin(L)), int(np.argmax(L)), 17, B - 1})
     for b in rows:
         n = int(L[b]) - 1
         kc = np.zeros((1, S, Hkv, D), np.int8)
@@ -81,10 +82,10 @@ def test_int8_gqa_full_size():
         vc[0, :n], vs[0, :n] = oracle.quantize_q8(inp.v_cache[b, :n])
         kc, vc, ks, vs, _ = oracle.kv_append_q8(kc, vc, ks, vs, inp.k_new[b:b + 1], inp.v_new[b:b + 1], inp.pos[b:b + 1])
         want, _ = oracle.decode_attention_q8(inp.q[b:b + 1], kc, vc, ks, vs, L[b:b + 1], w.scale)
-        assert_close(got[b:b + 1], want, "bf16", f"gqa int8 row {b}")
+        assert_close(got[b:b + 1], want, "bf16", f"{name} int8 row {b}")
 
 
-@pytest.mark.parametrize("name,T", [("gqa", 4), ("mha", 16)])
+@pytest.mark.parametrize("name,T", [("gqa", 4), ("mha", 16), ("gqa", 8), ("palm", 2)])
 def test_multi_token_full_size(name, T):
     import torch
     import kv_cache_decode_gb300 as kvd

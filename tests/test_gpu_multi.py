@@ -1,8 +1,8 @@
 """Multi-token decode on the GPU (T drafted tokens per sequence, causal among
 them), through the C ABI, against the oracle; T = 1 against the single-token
-calls bit for bit. Shapes cover the head dimensions and groups the mma.sync
-kernel takes (T * G <= 16), ragged lengths down to T, and split and unsplit
-pairs."""
+calls bit for bit. Shapes cover the head dimensions, groups from MHA to MQA,
+pairs of one block of 16 rows (T * G <= 16) and of several (the last one
+partly filled), ragged lengths down to T, and split and unsplit pairs."""
 import numpy as np
 import pytest
 
@@ -20,6 +20,11 @@ CASES = [
     ("g2t3d256", 4, 8, 4, 256, 300, 3, 300, 63, 3),
     ("g8t2", 7, 16, 2, 128, 900, 2, 900, 64, 2),
     ("g1t16", 3, 4, 4, 128, 500, 16, 500, 65, 16),
+    # several blocks of 16 rows per pair
+    ("g4t8", 5, 32, 8, 128, 600, 8, 600, 66, 8),          # 32 rows: 2 blocks
+    ("mqa48t2", 4, 48, 1, 256, 500, 2, 500, 67, 2),       # 96 rows: 6 blocks, MQA
+    ("g20t3d64", 3, 20, 1, 64, 400, 3, 400, 68, 3),       # 60 rows: 4 blocks, the last of 12
+    ("g16t5", 3, 32, 2, 128, 450, 5, 450, 69, 5),         # 80 rows: 5 blocks
 ]
 
 
@@ -68,7 +73,7 @@ def test_multi_step_matches_oracle(case, out_dtype):
         assert np.max(np.abs(l - want_lse)) < tol
 
 
-@pytest.mark.parametrize("case", [CASES[0], CASES[4]], ids=["g4t4", "g1t16"])
+@pytest.mark.parametrize("case", [CASES[0], CASES[4], CASES[6]], ids=["g4t4", "g1t16", "mqa48t2"])
 def test_multi_step_equals_two_calls(case):
     dev = cuda_or_skip()
     name, B, Hq, Hkv, D, S, lo, hi, seed, T = case
@@ -116,7 +121,8 @@ def test_multi_rows_past_capacity_are_skipped():
     assert np.array_equal(bf16_tensor_bits(kc), ek) and np.array_equal(bf16_tensor_bits(vc), ev)
 
 
-def test_multi_short_sequences_give_empty_rows():
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 2, 128), (48, 1, 256)], ids=["one_block", "twelve_blocks"])
+def test_multi_short_sequences_give_empty_rows(Hq, Hkv, D):
     """A sequence shorter than T: its first query tokens see no token (zero rows,
     lse -inf), the rest see what exists; rows appended before position 0 are
     skipped."""
@@ -124,7 +130,7 @@ def test_multi_short_sequences_give_empty_rows():
     import kv_cache_decode_gb300 as kvd
     dev = cuda_or_skip()
     T = 4
-    w = workloads.Workload("short_mt", 3, 8, 2, 128, 64, 4, 64, 68)
+    w = workloads.Workload("short_mt", 3, Hq, Hkv, D, 64, 4, 64, 68)
     mi = workloads.multi_step_inputs(w, T, lens=np.array([4, 9, 6], np.int32))
     lens = np.array([2, 9, 0], np.int32)  # sequence 0 holds 2 tokens after the step, sequence 2 none
     pos = lens - T                        # -2, 5, -4: rows before position 0 are skipped
@@ -133,7 +139,7 @@ def test_multi_short_sequences_give_empty_rows():
     lse = torch.full(mi.q.shape[:3], float("nan"), dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     B, _, Hq, D = mi.q.shape
-    _, nbytes = kvd.decode_plan_multi(B, T, Hq, 2, D, 64, 0, 3, "f32")
+    _, nbytes = kvd.decode_plan_multi(B, T, Hq, Hkv, D, 64, 0, 3, "f32")
     ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
     kvd.decode_step_multi(q, kc, vc, kn, vn, torch.from_numpy(pos.astype(np.int32)).to(dev),
                           torch.from_numpy(lens).to(dev), 64, w.scale, out, workspace=ws, n_split=3, lse=lse,

@@ -1,8 +1,9 @@
 """int8 KV cache on the GPU, through the C ABI: bulk quantization and the
 quantizing append against the oracle's quantizer (bit for bit: every code and
 scale), and attention over the int8 cache against the oracle's attention over
-the rows read back (the usual tolerances). Shapes cover the mma.sync engine's
-head dimensions and groups, ragged and empty sequences; rows past each
+the rows read back (the usual tolerances). Shapes cover the head dimensions
+and groups from MHA to MQA (above 16 query heads per KV head, in several CTAs
+of 16 per token run), ragged and empty sequences; rows past each
 sequence's end hold an invalid code and NaN scales, so any over-read fails.
 """
 import numpy as np
@@ -21,6 +22,10 @@ CASES = [
     ("mha64", 5, 6, 6, 64, 400, 1, 400, 52),
     ("g8d256", 4, 16, 2, 256, 300, 1, 300, 53),
     ("g16", 3, 16, 1, 128, 1100, 1, 1100, 54),
+    # groups above 16: several CTAs of 16 query heads per token run
+    ("mqa48", 4, 48, 1, 256, 700, 1, 700, 56),
+    ("g32d128", 5, 64, 2, 128, 600, 0, 600, 57),
+    ("g20d64", 3, 20, 1, 64, 520, 1, 520, 58),
 ]
 
 
@@ -126,7 +131,7 @@ def test_q8_step_matches_oracle(case, out_dtype):
         assert np.all(np.isneginf(l[~finite]))
 
 
-@pytest.mark.parametrize("case", [CASES[0], CASES[2]], ids=["d128", "d256"])
+@pytest.mark.parametrize("case", [CASES[0], CASES[2], CASES[4]], ids=["d128", "d256", "mqa48"])
 def test_q8_step_equals_two_calls(case):
     dev = cuda_or_skip()
     name, B, Hq, Hkv, D, S, lo, hi, seed = case
