@@ -245,8 +245,13 @@ kvd_status kvd_decode_step_paged(void* k_pages, void* v_pages, const void* k_new
  * their scale, and the kernels compute in f16 MMAs with fp32 accumulation,
  * with each score multiplied by its key row's scale and each weight by its
  * value row's scale. Every supported group (the mma.sync kernel, one CTA per
- * 16 query heads of a group and token run); head_dim 64, 128 or 256;
- * contiguous caches only. The split count and workspace are kvd_decode_plan's.
+ * 16 query heads of a group and token run); head_dim 64, 128 or 256. The
+ * split count and workspace are kvd_decode_plan's. A paged int8 cache (code
+ * pools [num_pages, page_size, n_heads_kv, head_dim] and scale pools
+ * [num_pages, page_size, n_heads_kv], one block table for both) is appended
+ * to by kvd_kv_append_q8_paged and read by kvd_decode_ex; its rows are found
+ * as kvd_kv_append_paged's, and an entry that names no page reads as zero
+ * rows (KVD_STATUS_BAD_PAGE).
  * q must lie in f16's range (|q| < 65504). Results and errors otherwise as the
  * bf16 calls, plus
  * KVD_ERR_INVALID_ARG for null or misaligned scale arrays.
@@ -256,6 +261,11 @@ kvd_status kvd_kv_quantize_q8(const void* cache, void* codes, float* scales, con
 kvd_status kvd_kv_append_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales, const void* k_new,
                             const void* v_new, const int32_t* pos, int batch, int s_max, int n_heads_kv,
                             int head_dim, int32_t* status_word, kvd_stream_t stream);
+kvd_status kvd_kv_append_q8_paged(void* k_code_pages, void* v_code_pages, float* k_scale_pages,
+                                  float* v_scale_pages, const void* k_new, const void* v_new,
+                                  const int32_t* block_table, const int32_t* pos, int batch, int max_blocks,
+                                  int page_size, int num_pages, int n_heads_kv, int head_dim,
+                                  int32_t* status_word, kvd_stream_t stream);
 kvd_status kvd_decode_attention_q8(const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
                                    const float* v_scales, const int32_t* seq_lens, int batch, int s_max,
                                    int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim, float scale,
@@ -315,7 +325,7 @@ kvd_status kvd_decode_step_multi(void* k_cache, void* v_cache, const void* k_new
  * struct:
  *   - bf16 or int8 (k_scales and v_scales non-NULL: k and v hold int8 codes);
  *   - contiguous (block_table NULL: k, v [batch, s_max, Hkv, D]) or paged
- *     (k, v are page pools; bf16 only);
+ *     (k, v are page pools, and for int8 k_scales, v_scales too);
  *   - n_tokens query tokens per sequence (layouts as kvd_decode_attention_multi;
  *     1 .. KVD_MAX_TOKENS; workspace from kvd_decode_plan_multi);
  *   - with the step's append (k_new, v_new and pos all non-NULL; the new rows,
@@ -324,13 +334,13 @@ kvd_status kvd_decode_step_multi(void* k_cache, void* v_cache, const void* k_new
  *     NULL).
  * Each combination is bit-identical to the dedicated call where one exists.
  * Errors: KVD_ERR_INVALID_ARG for a NULL cache, a cache description that fails
- * the dedicated calls' checks, or only some of k_new, v_new, pos given;
- * KVD_ERR_UNSUPPORTED for a paged int8 cache; the rest as the dedicated calls.
+ * the dedicated calls' checks, or only some of k_new, v_new, pos given; the
+ * rest as the dedicated calls.
  */
 typedef struct kvd_cache {
     void* k;                       /* bf16 cache or page pool, or int8 codes */
     void* v;
-    float* k_scales;               /* int8: float32 [batch, s_max, Hkv]; NULL for bf16 */
+    float* k_scales;               /* int8: float32 [batch, s_max, Hkv] (paged: [num_pages, page_size, Hkv]); NULL for bf16 */
     float* v_scales;
     const int32_t* block_table;    /* paged: int32 [batch, max_blocks]; NULL for contiguous */
     int s_max;                     /* contiguous: capacity of each sequence */

@@ -32,7 +32,7 @@ EXPORTED = (
     "kvd_version", "kvd_decode_attention_static", "kvd_decode_step", "kvd_kv_append_paged",
     "kvd_decode_attention_paged", "kvd_decode_step_paged", "kvd_kv_quantize_q8", "kvd_kv_append_q8",
     "kvd_decode_attention_q8", "kvd_decode_step_q8", "kvd_decode_plan_multi", "kvd_kv_append_multi",
-    "kvd_decode_attention_multi", "kvd_decode_step_multi", "kvd_decode_ex",
+    "kvd_decode_attention_multi", "kvd_decode_step_multi", "kvd_decode_ex", "kvd_kv_append_q8_paged",
 )
 STATIC_WORKSPACE_BYTES = 16 << 20  # KVD_STATIC_WORKSPACE_BYTES
 
@@ -96,6 +96,8 @@ def _declare(lib):
     lib.kvd_kv_quantize_q8.restype = I
     lib.kvd_kv_append_q8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P, P]
     lib.kvd_kv_append_q8.restype = I
+    lib.kvd_kv_append_q8_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P]
+    lib.kvd_kv_append_q8_paged.restype = I
     lib.kvd_decode_attention_q8.argtypes = [P, P, P, P, P] + dec[3:]
     lib.kvd_decode_attention_q8.restype = I
     lib.kvd_decode_step_q8.argtypes = [P, P, P, P, P, P, P, P, P] + dec[4:]
@@ -431,6 +433,29 @@ def kv_append_q8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, status
                                    Hkv, D, _ptr(status), _stream_handle(stream)), "kvd_kv_append_q8")
 
 
+def kv_append_q8_paged(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages, k_new, v_new, block_table, pos,
+                       status=None, stream=None):
+    """The new bf16 rows quantized and written, as kv_append_paged places them,
+    into int8 page pools: codes [num_pages, page, Hkv, D], scales
+    [num_pages, page, Hkv]."""
+    import torch
+    _q8_args(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages)
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _require(t, n, torch.bfloat16, 3)
+    _require(pos, "pos", torch.int32, 1)
+    _require(block_table, "block_table", torch.int32, 2)
+    num_pages, page, Hkv, D = k_code_pages.shape
+    B = k_new.shape[0]
+    if (k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or pos.shape != (B,)
+            or block_table.shape[0] != B):
+        raise ValueError("kv_append_q8_paged: inconsistent shapes")
+    _check(load().kvd_kv_append_q8_paged(k_code_pages.data_ptr(), v_code_pages.data_ptr(), k_scale_pages.data_ptr(),
+                                         v_scale_pages.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
+                                         block_table.data_ptr(), pos.data_ptr(), B, block_table.shape[1], page,
+                                         num_pages, Hkv, D, _ptr(status), _stream_handle(stream)),
+           "kvd_kv_append_q8_paged")
+
+
 def _decode_q8_args(q, k_codes, v_codes, k_scales, v_scales, seq_lens, max_seq_len, scale, n_split, workspace,
                     out, lse, status, stream):
     """(seq_lens pointer, batch, s_max, ...) as for kvd_decode_attention, after the int8 cache."""
@@ -566,8 +591,9 @@ def decode_ex(q, k, v, seq_lens, max_seq_len: int, scale: float, out, *, k_scale
     """Any supported combination in one call (kvd_decode_ex): q [B, Hq, D] or
     [B, T, Hq, D]; k, v a contiguous cache [B, S_max, Hkv, D] (bf16, or int8 codes
     with k_scales/v_scales [B, S_max, Hkv]) or, with block_table [B, max_blocks],
-    bf16 page pools [num_pages, page, Hkv, D]; k_new, v_new ([B, Hkv, D] or
-    [B, T, Hkv, D]) and pos to append first. Workspace: decode_plan_multi."""
+    page pools [num_pages, page, Hkv, D] (bf16, or int8 codes with scale pools
+    [num_pages, page, Hkv]); k_new, v_new ([B, Hkv, D] or [B, T, Hkv, D]) and pos
+    to append first. Workspace: decode_plan_multi."""
     import torch
     T = q.shape[1] if q.dim() == 4 else 1
     B, Hq, D = q.shape[0], q.shape[-2], q.shape[-1]

@@ -25,12 +25,12 @@ const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool
 
 // The tcgen05 kernels take either cache form at run time (only their loads
 // differ); the mma.sync kernel has a compiled variant per form. int8 caches
-// (contiguous only) and T > 1 query tokens run on the mma.sync kernel, whose
-// CTAs take 16 of a pair's T * G rows each, for every group.
-const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8, int T) {
-    if (group < 1 || group > KVD_MAX_GROUP || T < 1) return nullptr;
-    if (kv8) return paged ? nullptr : mma_chunk_kernel(head_dim, f32_out, false, true);
-    if (group <= 16 || T > 1) return mma_chunk_kernel(head_dim, f32_out, paged, false);
+// (contiguous or paged) run on the mma.sync kernel, whose CTAs take 16 of a
+// pair's rows each, for every group.
+const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8) {
+    if (group < 1 || group > KVD_MAX_GROUP) return nullptr;
+    if (kv8) return mma_chunk_kernel(head_dim, f32_out, paged, true);
+    if (group <= 16) return mma_chunk_kernel(head_dim, f32_out, paged, false);
     return tc_chunk_kernel(head_dim, f32_out, group);
 }
 
@@ -58,9 +58,8 @@ kvd_status check_shape(int batch, int Hq, int Hkv, int D, kvd_out_dtype dt) {
 // planning and the host replica use the contiguous one. The split count is
 // planned for the single-token bf16 kernel of the shape whatever the cache
 // dtype and query tokens, so that one plan sizes every form's workspace.
-const ChunkKernel* pick_kernel(int Hq, int Hkv, int D, kvd_out_dtype dt, bool paged = false, bool kv8 = false,
-                               int T = 1) {
-    return find_chunk_kernel(D, Hq / Hkv, dt == KVD_OUT_F32, paged, kv8, T);
+const ChunkKernel* pick_kernel(int Hq, int Hkv, int D, kvd_out_dtype dt, bool paged = false, bool kv8 = false) {
+    return find_chunk_kernel(D, Hq / Hkv, dt == KVD_OUT_F32, paged, kv8);
 }
 
 // int8 cache: the row scales of K and V.
@@ -186,17 +185,19 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     st = plan(batch, Hq, Hkv, D, max_seq_len, 0 /* query device if heuristic */, n_split_req, dt,
               &n_split, &need, &k, T);
     if (st != KVD_OK) return st;
-    if (pg && q8) return KVD_ERR_UNSUPPORTED;  // paged int8 caches are not built
     if (q8 && (!q8->k_scale || !q8->v_scale || !aligned(q8->k_scale, 4) || !aligned(q8->v_scale, 4)))
         return KVD_ERR_INVALID_ARG;
-    k = pick_kernel(Hq, Hkv, D, dt, pg != nullptr, q8 != nullptr, T);
+    k = pick_kernel(Hq, Hkv, D, dt, pg != nullptr, q8 != nullptr);
     if (!k) return KVD_ERR_UNSUPPORTED;
     // The tensor-core path addresses cache rows and query rows with 32-bit TMA coordinates.
-    if (k->tensor_core && (cache_rows > 0x7fffffffLL || (long long)batch * Hq > 0x7fffffffLL))
+    if (k->tensor_core && (cache_rows > 0x7fffffffLL || (long long)batch * T * Hq > 0x7fffffffLL))
         return KVD_ERR_UNSUPPORTED;
-    // mma.sync kernel: 16 of a pair's T * G rows per CTA.
+    // mma.sync kernel: 16 of a pair's T * G rows per CTA. tcgen05 kernel: T
+    // query tokens as T virtual sequences of one query token each.
     const int row_blocks = k->tensor_core ? 1 : (Hq / Hkv * T + 15) / 16;
+    const int vT = k->tensor_core ? T : 1;
     if ((long long)n_split * row_blocks > 0x7fffffffLL) return KVD_ERR_INVALID_ARG;
+    if ((long long)batch * vT > 0x7fffffffLL) return KVD_ERR_INVALID_ARG;
     if (need > 0) {
         if (!workspace || workspace_bytes < need) return KVD_ERR_WORKSPACE_TOO_SMALL;
         if (!aligned(workspace, 256)) return KVD_ERR_INVALID_ARG;
@@ -209,7 +210,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     p.k = k_cache;
     p.v = v_cache;
     p.seq_lens = seq_lens;
-    p.B = batch;
+    p.B = batch * vT;
     p.S_max = s_max;
     p.len_cap = std::min(s_max, max_seq_len);
     p.Hq = Hq;
@@ -223,8 +224,9 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     p.out = out;
     p.lse = lse;
     p.status = status;
-    p.T = T;
+    p.T = T / vT;
     p.row_blocks = row_blocks;
+    p.vT = vT;
     if (q8) {
         p.k_scale = q8->k_scale;
         p.v_scale = q8->v_scale;
@@ -236,8 +238,9 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
         p.num_pages = pg->num_pages;
     }
     if (need > 0) {
-        // T * G rows per slot (as workspace_for with T query tokens)
-        const size_t P = (size_t)batch * Hkv, rows = (size_t)p.G * T, slots = (size_t)n_split + P - 1;
+        // T * G rows per slot (as workspace_for with T query tokens), or G
+        // rows per virtual pair, which takes no more space.
+        const size_t P = (size_t)p.B * Hkv, rows = (size_t)p.G * p.T, slots = (size_t)n_split + P - 1;
         uint8_t* w = static_cast<uint8_t*>(workspace);
         p.ws_o = reinterpret_cast<float*>(w);
         w += align256(slots * rows * D * sizeof(float));
@@ -252,7 +255,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
         const PagedCache none{nullptr, 0, 0, 0};
         const cudaError_t e =
             q8 ? launch_append_q8(app->k_cache, app->v_cache, q8->k_scale, q8->v_scale, app->k_new, app->v_new,
-                                  app->pos, batch, s_max, Hkv, D, status, s, T)
+                                  app->pos, batch, s_max, Hkv, D, status, pg ? *pg : none, s, T)
                : launch_append(app->k_cache, app->v_cache, app->k_new, app->v_new, app->pos, batch, s_max, Hkv,
                                D, status, pg ? *pg : none, s, T);
         if (e != cudaSuccess) return KVD_ERR_CUDA;
@@ -377,7 +380,6 @@ kvd_status kvd_decode_ex(const kvd_cache* cache, const void* q, const int32_t* s
     }
     const QuantCache q8{cache->k_scales, cache->v_scales};
     const bool int8 = cache->k_scales != nullptr;
-    if (paged && int8) return KVD_ERR_UNSUPPORTED;
     AppendArgs app{cache->k, cache->v, k_new, v_new, pos};
     if (append) {
         const kvd_status st = check_append(cache->k, cache->v, k_new, v_new, pos, batch, s_max, n_heads_kv,
@@ -412,8 +414,32 @@ kvd_status kvd_kv_append_q8(void* k_codes, void* v_codes, float* k_scales, float
     if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVD_ERR_UNSUPPORTED;
     if (!k_scales || !v_scales || !aligned(k_scales, 4) || !aligned(v_scales, 4)) return KVD_ERR_INVALID_ARG;
     if (batch == 0) return KVD_OK;
+    const PagedCache none{nullptr, 0, 0, 0};
     return launch_append_q8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, batch, s_max, n_heads_kv,
-                            head_dim, status_word, static_cast<cudaStream_t>(stream)) == cudaSuccess
+                            head_dim, status_word, none, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KVD_OK
+               : KVD_ERR_CUDA;
+}
+
+kvd_status kvd_kv_append_q8_paged(void* k_code_pages, void* v_code_pages, float* k_scale_pages,
+                                  float* v_scale_pages, const void* k_new, const void* v_new,
+                                  const int32_t* block_table, const int32_t* pos, int batch, int max_blocks,
+                                  int page_size, int num_pages, int n_heads_kv, int head_dim,
+                                  int32_t* status_word, kvd_stream_t stream) {
+    PagedCache pg;
+    int s_max = 0;
+    kvd_status st = check_paged(block_table, max_blocks, page_size, num_pages, &pg, &s_max);
+    if (st != KVD_OK) return st;
+    st = check_append(k_code_pages, v_code_pages, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim,
+                      status_word);
+    if (st != KVD_OK) return st;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVD_ERR_UNSUPPORTED;
+    if (!k_scale_pages || !v_scale_pages || !aligned(k_scale_pages, 4) || !aligned(v_scale_pages, 4))
+        return KVD_ERR_INVALID_ARG;
+    if (batch == 0) return KVD_OK;
+    return launch_append_q8(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages, k_new, v_new, pos, batch,
+                            s_max, n_heads_kv, head_dim, status_word, pg, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
                ? KVD_OK
                : KVD_ERR_CUDA;
 }

@@ -47,14 +47,16 @@ __device__ __forceinline__ void quantize_row(const uint4* src, uint2* dst_codes,
     }
 }
 
-// The new token's K and V rows, quantized and written at pos[b].
+// The new tokens' K and V rows, quantized and written at pos[b] + i; with a
+// paged cache (pg.block_table non-null) at the row of the block's page, as
+// the bf16 append.
 template <int D>
 __global__ void __launch_bounds__(256) kv_append_q8_kernel(int8_t* __restrict__ k_codes, int8_t* __restrict__ v_codes,
                                                           float* __restrict__ k_scale, float* __restrict__ v_scale,
                                                           const uint4* __restrict__ k_new,
                                                           const uint4* __restrict__ v_new,
                                                           const int32_t* __restrict__ pos, int B, int S_max,
-                                                          int Hkv, int32_t* status, int T) {
+                                                          int Hkv, int32_t* status, int T, const PagedCache pg) {
     // The attention kernel that follows may start; it waits for this grid
     // before reading the cache.
     pdl_launch_dependents();
@@ -72,9 +74,20 @@ __global__ void __launch_bounds__(256) kv_append_q8_kernel(int8_t* __restrict__ 
         const int h = (int)(r - bi * Hkv);
         const int b = (int)(bi / T), i = (int)(bi - (long long)b * T);
         const int t = in ? __ldg(pos + b) + i : 0;
-        const bool ok = in && t >= 0 && t < S_max;
+        bool ok = in && t >= 0 && t < S_max;
         if (in && !ok && status && which == 0 && h == 0 && sub == 0) atomicOr(status, KVD_STATUS_POS_OUT_OF_RANGE);
-        const long long dst_row = ((long long)b * S_max + (ok ? t : 0)) * Hkv + h;
+        long long trow = (long long)b * S_max + (ok ? t : 0);  // cache row of the token
+        if (pg.block_table && ok) {
+            const int page = __ldg(pg.block_table + (size_t)b * pg.max_blocks + (t >> pg.page_shift));
+            if (page < 0 || page >= pg.num_pages) {
+                if (status && which == 0 && h == 0 && sub == 0) atomicOr(status, KVD_STATUS_BAD_PAGE);
+                ok = false;
+                trow = 0;
+            } else {
+                trow = ((long long)page << pg.page_shift) + (t & ((1 << pg.page_shift) - 1));
+            }
+        }
+        const long long dst_row = trow * Hkv + h;
         quantize_row<D>((which ? v_new : k_new) + r * VPR,
                         reinterpret_cast<uint2*>((which ? v_codes : k_codes) + dst_row * D),
                         (which ? v_scale : k_scale) + dst_row, ok, sub);
@@ -105,7 +118,7 @@ __global__ void __launch_bounds__(256) kv_quantize_q8_kernel(const uint4* __rest
 
 cudaError_t launch_append_q8(void* k_codes, void* v_codes, float* k_scale, float* v_scale, const void* k_new,
                              const void* v_new, const int32_t* pos, int B, int S_max, int Hkv, int D,
-                             int32_t* status, cudaStream_t stream, int T) {
+                             int32_t* status, const PagedCache& pg, cudaStream_t stream, int T) {
     const long long rows = 2LL * B * T * Hkv;
     const int rows_per_block = 256 / (D / 8);
     long long blocks = (rows + rows_per_block - 1) / rows_per_block;
@@ -120,9 +133,9 @@ cudaError_t launch_append_q8(void* k_codes, void* v_codes, float* k_scale, float
     auto* kn = static_cast<const uint4*>(k_new);
     auto* vn = static_cast<const uint4*>(v_new);
     switch (D) {
-        case 64: return cudaLaunchKernelEx(&cfg, kv_append_q8_kernel<64>, kc, vc, k_scale, v_scale, kn, vn, pos, B, S_max, Hkv, status, T);
-        case 128: return cudaLaunchKernelEx(&cfg, kv_append_q8_kernel<128>, kc, vc, k_scale, v_scale, kn, vn, pos, B, S_max, Hkv, status, T);
-        case 256: return cudaLaunchKernelEx(&cfg, kv_append_q8_kernel<256>, kc, vc, k_scale, v_scale, kn, vn, pos, B, S_max, Hkv, status, T);
+        case 64: return cudaLaunchKernelEx(&cfg, kv_append_q8_kernel<64>, kc, vc, k_scale, v_scale, kn, vn, pos, B, S_max, Hkv, status, T, pg);
+        case 128: return cudaLaunchKernelEx(&cfg, kv_append_q8_kernel<128>, kc, vc, k_scale, v_scale, kn, vn, pos, B, S_max, Hkv, status, T, pg);
+        case 256: return cudaLaunchKernelEx(&cfg, kv_append_q8_kernel<256>, kc, vc, k_scale, v_scale, kn, vn, pos, B, S_max, Hkv, status, T, pg);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -46,6 +46,11 @@ struct DecodeParams {
     // mma.sync kernel: blocks of 16 of a pair's T * G rows, one CTA each per
     // token run (n_split * row_blocks CTAs); 1 for the tcgen05 kernel.
     int row_blocks;
+    // tcgen05 kernel with vT > 1 query tokens per sequence: B is then B * vT
+    // virtual sequences (query token i of sequence s is sequence s * vT + i,
+    // attending to its first L_s - vT + 1 + i tokens) and T is 1; the merge
+    // reads the lengths the same way. 1 otherwise.
+    int vT;
 };
 
 // One compiled variant of the split-KV chunk kernel.
@@ -56,15 +61,14 @@ struct ChunkKernel {
     int seg_unit;    // tokens per schedule position (1 or tile_tokens, see schedule.cuh)
     int seg_cost;    // positions charged per pair by the schedule
     bool f32_out, tensor_core;
-    int index;  // position in the variant table (0..41), for the per-device attribute bitmask
+    int index;  // position in the variant table (0..47), for the per-device attribute bitmask
 };
 
-// The kernel for a shape: single-token bf16 groups of up to 16 query heads per
-// KV head run on the mma.sync kernel, wider groups (17..64) on the tcgen05
-// kernel; int8 caches and T > 1 query tokens run on the mma.sync kernel for
-// every group, in blocks of 16 rows.
-const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8 = false,
-                                     int T = 1);
+// The kernel for a shape: bf16 groups of up to 16 query heads per KV head run
+// on the mma.sync kernel (T query tokens as T * G rows, in blocks of 16),
+// wider groups (17..64) on the tcgen05 kernel (T query tokens as T virtual
+// sequences); int8 caches run on the mma.sync kernel for every group.
+const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8 = false);
 const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool kv8);
 const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out, int group);
 
@@ -79,11 +83,12 @@ struct PagedCache {
 cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                           const int32_t* pos, int B, int S_max, int Hkv, int D,
                           int32_t* status, const PagedCache& pg, cudaStream_t stream, int T = 1);
-// int8 cache (kv_quant.cu): the append quantizes the new rows; the bulk
-// conversion quantizes rows t < seq_lens[b] of a bf16 cache.
+// int8 cache (kv_quant.cu): the append quantizes the new rows (into pages
+// when pg.block_table is set); the bulk conversion quantizes rows
+// t < seq_lens[b] of a bf16 cache.
 cudaError_t launch_append_q8(void* k_codes, void* v_codes, float* k_scale, float* v_scale, const void* k_new,
                              const void* v_new, const int32_t* pos, int B, int S_max, int Hkv, int D,
-                             int32_t* status, cudaStream_t stream, int T = 1);
+                             int32_t* status, const PagedCache& pg, cudaStream_t stream, int T = 1);
 cudaError_t launch_quantize_q8(const void* src, void* codes, float* scales, const int32_t* seq_lens, int B,
                                int S_max, int len_cap, int Hkv, int D, cudaStream_t stream);
 

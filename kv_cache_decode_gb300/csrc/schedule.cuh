@@ -39,6 +39,29 @@ namespace kvd {
 
 KVD_HD int clamp_len(int L, int cap) { return L < 0 ? 0 : (L > cap ? cap : L); }
 
+// Attended length of sequence b. With vt > 1 (the tcgen05 kernel's form of
+// vt query tokens per sequence) b is a virtual sequence s * vt + i: query
+// token i of cache sequence s, which attends to the first L_s - vt + 1 + i
+// tokens (none when that is not positive).
+struct DevLen {
+    const int32_t* lens;
+    int cap;
+    int vt;
+    KVD_HD int operator()(int b) const {
+        if (vt <= 1) return clamp_len(load(b), cap);
+        const int s = b / vt;
+        const int L = clamp_len(load(s), cap) - vt + 1 + (b - s * vt);
+        return L > 0 ? L : 0;
+    }
+    KVD_HD int load(int s) const {
+#ifdef __CUDA_ARCH__
+        return __ldg(lens + s);
+#else
+        return lens[s];
+#endif
+    }
+};
+
 // Geometry of the walk: tokens per tile TT, tokens per position U (1 or TT)
 // and start-up cost X (positions). Compile-time constants in kernels, so that
 // the divisions become shifts and a zero cost compiles away; run-time values

@@ -32,18 +32,6 @@
 
 namespace kvd {
 
-struct DevLen {
-    const int32_t* lens;
-    int cap;
-    KVD_HD int operator()(int b) const {
-#ifdef __CUDA_ARCH__
-        return clamp_len(__ldg(lens + b), cap);
-#else
-        return clamp_len(lens[b], cap);
-#endif
-    }
-};
-
 struct NoOp {
     KVD_HD void operator()(int, int) const {}
 };
@@ -162,7 +150,6 @@ struct ChunkShape {
 // before P V.
 template <int D, int HT, int TS, int TT, int STAGES, bool F32OUT, int MINB, bool PAGED, bool KV8 = false>
 __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const DecodeParams p) {
-    static_assert(!(PAGED && KV8), "paged int8 caches are not built");
     using Sh = ChunkShape<D, HT, TS, TT, STAGES, KV8>;
     constexpr int NW = Sh::NW, NT = Sh::NT, TW = Sh::TW, NS = Sh::NS, KS = Sh::KS,
                   ND = Sh::ND, CH = Sh::CH, TILE_ELEMS = Sh::TILE_ELEMS, SEG_COST = Sh::SEG_COST;
@@ -199,7 +186,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
     if (!p.early) pdl_wait();
     pdl_launch_dependents();
 
-    const DevLen len{p.seq_lens, p.len_cap};
+    const DevLen len{p.seq_lens, p.len_cap, 1};  // T query tokens are rows of one pair here
     using Geo = FixedGeom<TT, Sh::SEG_UNIT, SEG_COST>;
 
     // ---- total work and this CTA's token run ----
@@ -289,7 +276,38 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
         const int nvalid = t.tok_hi - t.tok_lo;
         const uint32_t sbase = smem_u32(stages) + stage * Sh::STAGE_BYTES;
         const int ch = tid % CH, r0 = tid / CH;
-        if constexpr (KV8) {
+        if constexpr (KV8 && PAGED) {
+            // int8 rows from their pages (as the bf16 paged rows below), then
+            // the row scales: a page's scales start at its first row's element
+            // offset / D. An entry that names no page reads zero codes and a
+            // zero scale.
+            constexpr int CH8 = D / 16, RSTEP8 = NT / CH8, RPT8 = TT / RSTEP8;
+            static_assert(NT % CH8 == 0 && TT % RSTEP8 == 0 && NT >= 2 * TT, "int8 row split");
+            const int shift = p.page_shift, in_page = (1 << shift) - 1;
+            const int first = t.tok_lo >> shift;
+            const int c8 = tid % CH8, q0 = tid / CH8;
+            const int8_t* kb = reinterpret_cast<const int8_t*>(p.k) + (size_t)t.h * D + c8 * 16;
+            const int8_t* vb = reinterpret_cast<const int8_t*>(p.v) + (size_t)t.h * D + c8 * 16;
+#pragma unroll
+            for (int k = 0; k < RPT8; ++k) {
+                const int r = q0 + k * RSTEP8;
+                const int tok = t.tok_lo + r;
+                const long long po = (r < nvalid) ? s_pages[ps][(tok >> shift) - first] : -1;
+                const bool ok = po >= 0;
+                const size_t off = ok ? (size_t)po + (size_t)(tok & in_page) * row_stride : 0;
+                const uint32_t dst = sbase + (uint32_t)(r * D + c8 * 16);
+                cp_async_16(dst, kb + off, ok ? 16 : 0, policy);
+                cp_async_16(dst + TILE_ELEMS, vb + off, ok ? 16 : 0, policy);
+            }
+            if (tid < 2 * TT) {
+                const int r = tid % TT, tok = t.tok_lo + r;
+                const long long po = (r < nvalid) ? s_pages[ps][(tok >> shift) - first] : -1;
+                const bool ok = po >= 0;
+                const float* base = tid < TT ? p.k_scale : p.v_scale;
+                const size_t so = ok ? (size_t)po / D + (size_t)(tok & in_page) * p.Hkv + t.h : 0;
+                cp_async_4(sbase + 2 * TILE_ELEMS + tid * 4, base + so, ok ? 4 : 0);
+            }
+        } else if constexpr (KV8) {
             // int8 rows: D / 16 chunks of 16 bytes each, unswizzled; then the
             // tile's row scales, one 4-byte copy per row and tensor.
             constexpr int CH8 = D / 16, RSTEP8 = NT / CH8, RPT8 = TT / RSTEP8;

@@ -188,7 +188,12 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     if (!p.early) pdl_wait();
     pdl_launch_dependents();
 
-    const DevLen len{p.seq_lens, p.len_cap};
+    // p.vT > 1 query tokens per sequence run as p.B = B * vT virtual
+    // sequences (see DevLen): their q, out and lse rows are those of the
+    // [B, vT, Hq] layouts, and virtual sequence b reads the cache rows (and
+    // pos, and block-table row) of sequence b / vT.
+    const int vt = p.vT > 1 ? p.vT : 1;
+    const DevLen len{p.seq_lens, p.len_cap, vt};
     using Geo = FixedGeom<T, Sh::SEG_UNIT, SEG_COST>;
     // ---- total work, this CTA's run, first sequence (as in the mma.sync kernel) ----
     long long total;
@@ -203,9 +208,9 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
         const int b = tid;
         int L = 0;
         if (b < p.B) {
-            const int raw = __ldg(p.seq_lens + b);
-            L = clamp_len(raw, p.len_cap);
-            if (raw != L && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
+            const int raw = __ldg(p.seq_lens + b / vt);
+            L = len(b);
+            if (raw != clamp_len(raw, p.len_cap) && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
         }
         const long long e = pair_extent(L, Geo{});
         const long long v = e * p.Hkv;
@@ -228,10 +233,9 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
         long long mine = 0;
         bool clamped = false;
         for (int b = tid; b < p.B; b += Sh::THREADS) {
-            const int raw = __ldg(p.seq_lens + b);
-            const int L = clamp_len(raw, p.len_cap);
-            clamped |= (raw != L);
-            mine += pair_extent(L, Geo{});
+            const int raw = __ldg(p.seq_lens + b / vt);
+            clamped |= (raw != clamp_len(raw, p.len_cap));
+            mine += pair_extent(len(b), Geo{});
         }
         if (clamped && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
         total = block_sum_ll<NW>(mine, s_red) * p.Hkv;  // also orders the set-up
@@ -275,25 +279,26 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             int j = 0;
             const int NS = is_k ? KST : VST;
             const CUtensorMap* map = is_k ? &maps.k : &maps.v;
-            // Early mode: only the tile holding a pair's appended row waits for
-            // the append's grid; tiles before it stream meanwhile. pos is an input
-            // (complete at launch), read once per pair until the first wait.
+            // Early mode: only tiles holding a pair's appended rows (those from
+            // pos on) wait for the append's grid; tiles before them stream
+            // meanwhile. pos is an input (complete at launch), read once per
+            // pair until the first wait.
             bool waited = !p.early;
             int pos_pair = -1, pos_b = -1;
             const bool paged = p.block_table != nullptr;
             const int box_rows = paged ? min(1 << p.page_shift, T) : T;
             if (!waited && walker.b < p.B) {  // issued now, first used at the first tile
                 pos_pair = walker.b * p.Hkv + walker.h;
-                pos_b = __ldg(p.pos + walker.b);
+                pos_b = __ldg(p.pos + walker.b / vt);
             }
             while (walker.next(t, NoOp{})) {
                 if (!waited) {
                     const int pair = t.b * p.Hkv + t.h;
                     if (pair != pos_pair) {
                         pos_pair = pair;
-                        pos_b = __ldg(p.pos + t.b);
+                        pos_b = __ldg(p.pos + t.b / vt);
                     }
-                    if (pos_b >= t.tok_lo && pos_b < t.tok_hi) {
+                    if (t.tok_hi > pos_b) {
                         pdl_wait();
                         waited = true;
                     }
@@ -305,7 +310,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                 tc::mbar_arrive_expect_tx(full, (uint32_t)Sh::TILE_BYTES);
                 const uint32_t dst = (is_k ? sK : sV) + (uint32_t)(s * Sh::TILE_BYTES);
                 if (!paged) {
-                    const int row = t.b * p.S_max + t.tok_lo;
+                    const int row = (t.b / vt) * p.S_max + t.tok_lo;
 #pragma unroll
                     for (int kb = 0; kb < KB; ++kb)
                         tc::tma_load_3d(dst + kb * Sh::KB_BYTES, map, kb * 64, t.h, row, full, pol_kv);
@@ -317,7 +322,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                     // 16 tokens), so no box crosses a page. A box past the
                     // tile's tokens, or whose table entry names no page, is
                     // read from past the pool's end: zeros.
-                    const int32_t* table = p.block_table + (size_t)t.b * p.max_blocks;
+                    const int32_t* table = p.block_table + (size_t)(t.b / vt) * p.max_blocks;
                     const int oob = p.num_pages << p.page_shift;
                     for (int r0 = 0; r0 < T; r0 += box_rows) {
                         const int tok = t.tok_lo + r0;

@@ -30,7 +30,8 @@ cudaError_t launch_tc_chunk(const ChunkKernel& k, const DecodeParams& p, cudaStr
         // for a pool of pages, whose boxes are one page (at most one tile) high.
         constexpr int T = TcShape<D, F32, QR>::T;
         const bool paged = p.block_table != nullptr;
-        const cuuint64_t rows = paged ? ((cuuint64_t)p.num_pages << p.page_shift) : (cuuint64_t)p.B * p.S_max;
+        const int cache_batch = p.vT > 1 ? p.B / p.vT : p.B;  // virtual sequences share their cache's rows
+        const cuuint64_t rows = paged ? ((cuuint64_t)p.num_pages << p.page_shift) : (cuuint64_t)cache_batch * p.S_max;
         const int box_rows = paged ? std::min(1 << p.page_shift, T) : T;
         const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)p.Hkv, rows};
         const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)p.Hkv * D * 2};

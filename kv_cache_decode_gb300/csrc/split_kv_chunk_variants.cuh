@@ -66,15 +66,18 @@ inline ChunkKernel make_mma_chunk_kernel(int index) {
 }
 
 // Variants of one head dimension: contiguous bf16 cache at indices IDX,
-// IDX + 1, paged at PIDX, PIDX + 1, int8 at QIDX, QIDX + 1 (bf16 and fp32 output).
-#define KVD_MMA_TABLE(D, IDX, PIDX, QIDX)                                                         \
+// IDX + 1, paged at PIDX, PIDX + 1, int8 at QIDX, QIDX + 1, paged int8 at
+// PQIDX, PQIDX + 1 (bf16 and fp32 output).
+#define KVD_MMA_TABLE(D, IDX, PIDX, QIDX, PQIDX)                                                  \
     const ChunkKernel* mma_table_d##D(bool f32, bool paged, bool kv8) {                          \
-        static const ChunkKernel table[3][2] = {                                                 \
+        static const ChunkKernel table[4][2] = {                                                 \
             {make_mma_chunk_kernel<D, false, false>(IDX), make_mma_chunk_kernel<D, true, false>(IDX + 1)}, \
             {make_mma_chunk_kernel<D, false, true>(PIDX), make_mma_chunk_kernel<D, true, true>(PIDX + 1)}, \
             {make_mma_chunk_kernel<D, false, false, true>(QIDX),                                 \
-             make_mma_chunk_kernel<D, true, false, true>(QIDX + 1)}};                            \
-        return &table[kv8 ? 2 : (paged ? 1 : 0)][f32 ? 1 : 0];                                   \
+             make_mma_chunk_kernel<D, true, false, true>(QIDX + 1)},                             \
+            {make_mma_chunk_kernel<D, false, true, true>(PQIDX),                                 \
+             make_mma_chunk_kernel<D, true, true, true>(PQIDX + 1)}};                            \
+        return &table[(kv8 ? 2 : 0) + (paged ? 1 : 0)][f32 ? 1 : 0];                             \
     }
 
 }  // namespace kvd

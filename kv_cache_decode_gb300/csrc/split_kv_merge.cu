@@ -54,7 +54,8 @@ __global__ void __launch_bounds__(NT, 768 / NT) split_kv_merge_kernel(const Deco
 
     // ---- the schedule, from the lengths (before the dependency wait) ----
     const RuntimeGeom geo{p.tile_tokens, p.seg_unit, p.seg_cost};
-    auto ext = [&](int b) { return pair_extent(clamp_len(__ldg(p.seq_lens + b), p.len_cap), geo); };
+    const DevLen len{p.seq_lens, p.len_cap, p.vT};
+    auto ext = [&](int b) { return pair_extent(len(b), geo); };
     const long long row_lo = (long long)blockIdx.x * rows_per_cta;
     const int b_lo = (int)(row_lo / rows_per_seq);  // first sequence among this CTA's rows
     long long tot = 0, pre = 0;

@@ -37,6 +37,12 @@ Functions and the passages they follow (page title, section):
   generation throughput and latency", the quantization bullet names int8 KV
   caches; the scheme is this library's reading. Attention over it is the
   attention above over the rows read back (scale * code), in double.
+* ``paged_gather_q8``, ``kv_append_q8_paged``, ``decode_attention_q8_paged``:
+  an int8 cache in page pools (codes [num_pages, P, Hkv, D], scales
+  [num_pages, P, Hkv]), the two readings above combined: the page gather and
+  paged append move the codes' and scales' bytes exactly as they move bf16
+  rows (the same C routines over the bytes), and attention is the int8
+  attention over the gathered cache.
 * ``kv_append_multi``, ``decode_attention_multi``: T new tokens per sequence
   (a speculative-decoding check step): their rows are appended at pos[b] ..
   pos[b] + T - 1, and query token i attends to the cached tokens and the new
@@ -333,6 +339,51 @@ def kv_append_q8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, lib=No
             continue
         kc[b, t], vc[b, t], ks[b, t], vs[b, t] = nk[b], nv[b], nks[b], nvs[b]
     return kc, vc, ks, vs, skipped
+
+
+def _u16_rows(a, dtype):
+    """A C-contiguous array of dtype viewed as rows of 16-bit words (the last
+    axis's bytes; a scale array gets a last axis of its one float)."""
+    a = np.ascontiguousarray(a, dtype=dtype)
+    if dtype == np.float32:
+        a = a[..., None]
+    return a.view(np.uint16)
+
+
+def paged_gather_q8(code_pool, scale_pool, block_table, seq_lens, lib=None):
+    """Contiguous int8 cache (codes [B, max_blocks * P, Hkv, D], scales
+    [B, max_blocks * P, Hkv]) from page pools, gathered as paged_gather moves
+    bf16 rows: rows t < seq_lens[b] from row t % P of page block_table[b, t // P],
+    zero codes and a zero scale where the entry names no page; rows past the
+    length are not defined. Returns (codes, scales, tokens that read zero rows)."""
+    codes, zeroed = paged_gather(_u16_rows(code_pool, np.int8), block_table, seq_lens, lib=lib)
+    scales, _ = paged_gather(_u16_rows(scale_pool, np.float32), block_table, seq_lens, lib=lib)
+    return codes.view(np.int8), scales.view(np.float32)[..., 0], zeroed
+
+
+def kv_append_q8_paged(k_code_pool, v_code_pool, k_scale_pool, v_scale_pool, k_new, v_new, block_table, pos,
+                       lib=None):
+    """Copies of int8 page pools with each sequence's new bf16 rows quantized
+    (quantize_q8) and written at pos[b], as kv_append_paged writes bf16 rows.
+    Returns (kc, vc, ks, vs, n_skipped, n_bad_page)."""
+    nk, nks = quantize_q8(k_new, lib=lib)
+    nv, nvs = quantize_q8(v_new, lib=lib)
+    kc, vc, skipped, bad = kv_append_paged(_u16_rows(k_code_pool, np.int8), _u16_rows(v_code_pool, np.int8),
+                                           _u16_rows(nk, np.int8), _u16_rows(nv, np.int8), block_table, pos,
+                                           lib=lib)
+    ks, vs, _, _ = kv_append_paged(_u16_rows(k_scale_pool, np.float32), _u16_rows(v_scale_pool, np.float32),
+                                   _u16_rows(nks, np.float32), _u16_rows(nvs, np.float32), block_table, pos,
+                                   lib=lib)
+    return (kc.view(np.int8), vc.view(np.int8), ks.view(np.float32)[..., 0], vs.view(np.float32)[..., 0],
+            skipped, bad)
+
+
+def decode_attention_q8_paged(q, k_code_pool, v_code_pool, k_scale_pool, v_scale_pool, block_table, seq_lens,
+                              scale, n_threads: int = 0, lib=None):
+    """decode_attention_q8 over the int8 cache gathered from the page pools."""
+    kc, ks, _ = paged_gather_q8(k_code_pool, k_scale_pool, block_table, seq_lens, lib=lib)
+    vc, vs, _ = paged_gather_q8(v_code_pool, v_scale_pool, block_table, seq_lens, lib=lib)
+    return decode_attention_q8(q, kc, vc, ks, vs, seq_lens, scale, n_threads=n_threads, lib=lib)
 
 
 def decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, seq_lens, scale, n_threads: int = 0,

@@ -542,6 +542,80 @@ def check_multi_token_append(lib):
     assert np.array_equal(k2, ek) and np.array_equal(v2, ev)
 
 
+def _q8_pool(cache_codes, cache_scales, table, num_pages, seed):
+    """int8 page pools: pages of random codes and scales, then block j of
+    sequence b copied in as one slice (as _fill_pool does for bf16)."""
+    B, S, Hkv, D = cache_codes.shape
+    P = S // table.shape[1]
+    r = np.random.default_rng(seed)
+    cp = r.integers(-128, 128, (num_pages, P, Hkv, D), dtype=np.int8)
+    sp = r.standard_normal((num_pages, P, Hkv)).astype(np.float32)
+    for b in range(B):
+        for j in range(table.shape[1]):
+            if table[b, j] >= 0:
+                cp[table[b, j]] = cache_codes[b, j * P:(j + 1) * P]
+                sp[table[b, j]] = cache_scales[b, j * P:(j + 1) * P]
+    return cp, sp
+
+
+def check_paged_q8_pools_are_the_cache(lib):
+    # Shuffled int8 pools gather back to the contiguous codes and scales
+    # exactly, and attention over them equals the contiguous int8 attention.
+    B, S, Hkv, D, P = 4, 16, 2, 8, 4
+    lens = np.array([16, 1, 7, 0], np.int32)
+    table, num_pages = _page_table(80, B, S, P, lens)
+    r = np.random.default_rng(81)
+    kc, ks = oracle.quantize_q8(_bits(r.standard_normal((B, S, Hkv, D))), lib=lib)
+    vc, vs = oracle.quantize_q8(_bits(r.standard_normal((B, S, Hkv, D))), lib=lib)
+    kcp, ksp = _q8_pool(kc, ks, table, num_pages, 82)
+    vcp, vsp = _q8_pool(vc, vs, table, num_pages, 83)
+    gc, gs, zeroed = oracle.paged_gather_q8(kcp, ksp, table, lens, lib=lib)
+    assert zeroed == 0 and gc.dtype == np.int8 and gs.dtype == np.float32
+    for b in range(B):
+        assert np.array_equal(gc[b, :lens[b]], kc[b, :lens[b]]), b
+        assert np.array_equal(gs[b, :lens[b]].view(np.uint32), ks[b, :lens[b]].view(np.uint32)), b
+    q = _bits(r.standard_normal((B, 4, D)))
+    direct, lse_d = oracle.decode_attention_q8(q, kc, vc, ks, vs, lens, 0.5, lib=lib)
+    paged, lse_p = oracle.decode_attention_q8_paged(q, kcp, vcp, ksp, vsp, table, lens, 0.5, lib=lib)
+    assert np.array_equal(direct, paged) and np.array_equal(lse_d, lse_p)
+    # an entry that names no page reads zero codes and a zero scale
+    table[0, 1] = -2
+    gc, gs, zeroed = oracle.paged_gather_q8(kcp, ksp, table, lens, lib=lib)
+    assert zeroed == P and not gc[0, P:2 * P].any() and not gs[0, P:2 * P].any()
+    assert np.array_equal(gc[0, :P], kc[0, :P]) and np.array_equal(gc[0, 2 * P:], kc[0, 2 * P:])
+
+
+def check_paged_q8_append(lib):
+    # The paged int8 append writes the rows the contiguous int8 append writes,
+    # at the table's pages; a position past the capacity or an entry that
+    # names no page is skipped.
+    B, S, Hkv, D, P = 5, 16, 2, 8, 8
+    lens = np.array([16, 9, 8, 1, 16], np.int32)
+    table, num_pages = _page_table(84, B, S, P, lens)
+    r = np.random.default_rng(85)
+    kc, ks = oracle.quantize_q8(_bits(r.standard_normal((B, S, Hkv, D))), lib=lib)
+    vc, vs = oracle.quantize_q8(_bits(r.standard_normal((B, S, Hkv, D))), lib=lib)
+    kcp, ksp = _q8_pool(kc, ks, table, num_pages, 86)
+    vcp, vsp = _q8_pool(vc, vs, table, num_pages, 87)
+    kn = _bits(r.standard_normal((B, Hkv, D)))
+    vn = _bits(r.standard_normal((B, Hkv, D)))
+    pos = np.array([15, 8, 7, 0, 16], np.int32)  # page ends and starts; sequence 4 past the capacity
+    table[2, 0] = num_pages                      # sequence 2's row names no page
+    got = oracle.kv_append_q8_paged(kcp, vcp, ksp, vsp, kn, vn, table, pos, lib=lib)
+    assert got[4] == 2 and got[5] == 1
+    want = oracle.kv_append_q8(kc, vc, ks, vs, kn, vn, np.where(np.arange(B) == 2, -1, pos), lib=lib)
+    for b, t in ((0, 15), (1, 8), (3, 0)):
+        page, row = table[b, t // P], t % P
+        for g, w in zip(got[:4], want[:4]):
+            assert np.array_equal(np.asarray(g[page, row]).view(np.uint8), np.asarray(w[b, t]).view(np.uint8)), (b, t)
+    # nothing else changed
+    changed = np.zeros((num_pages, P), bool)
+    for b, t in ((0, 15), (1, 8), (3, 0)):
+        changed[table[b, t // P], t % P] = True
+    assert np.array_equal(got[0][~changed], kcp[~changed]) and np.array_equal(got[3][~changed].view(np.uint32),
+                                                                               vsp[~changed].view(np.uint32))
+
+
 ALL_CHECKS = [
     check_identical_keys_give_mean_of_v,
     check_dominant_score_returns_that_row,
@@ -565,6 +639,8 @@ ALL_CHECKS = [
     check_f64kv_attention_is_the_bf16_attention,
     check_q8_attention_close_to_bf16,
     check_q8_append,
+    check_paged_q8_pools_are_the_cache,
+    check_paged_q8_append,
     check_multi_token_one_is_single,
     check_multi_token_against_torch_causal,
     check_multi_token_append,

@@ -229,6 +229,19 @@ def test_append_paged_rejects(lib, args, expect):
     assert lib.kvd_kv_append_paged(*args) == expect
 
 
+@pytest.mark.parametrize("args,expect", [
+    # (k_codes, v_codes, k_scales, v_scales, k_new, v_new, table, pos, B, max_blocks, page, num_pages, Hkv, D, status, stream)
+    ((FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 16, 10, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE + 2, FAKE, FAKE, FAKE, FAKE, 2, 4, 16, 10, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, None, FAKE, 2, 4, 16, 10, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 24, 10, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 4, 16, 10, 1, 96, None, None), kvd.ERR_UNSUPPORTED),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, 16, 10, 1, 128, None, None), kvd.OK),  # batch 0
+])
+def test_append_q8_paged_rejects(lib, args, expect):
+    assert lib.kvd_kv_append_q8_paged(*args) == expect
+
+
 def _q8_args(ks=FAKE, vs=FAKE, **over):
     a = _dec_args(**over)
     # (q, k_codes, v_codes, k_scales, v_scales, seq_lens, batch, ...) as kvd_decode_attention after the cache
@@ -322,7 +335,11 @@ def test_decode_ex_rejects(lib):
     assert call(ctypes.byref(cq)) == kvd.ERR_INVALID_ARG                    # one scale array only
     cpq = kvd._CCache(k=FAKE, v=FAKE, k_scales=FAKE, v_scales=FAKE, block_table=FAKE, max_blocks=4,
                       page_size=16, num_pages=10)
-    assert call(ctypes.byref(cpq)) == kvd.ERR_UNSUPPORTED                    # paged int8
+    # paged int8 passes every check up to the workspace (none given here)
+    assert call(ctypes.byref(cpq)) == kvd.ERR_WORKSPACE_TOO_SMALL
+    cpq2 = kvd._CCache(k=FAKE, v=FAKE, k_scales=FAKE, v_scales=FAKE + 2, block_table=FAKE, max_blocks=4,
+                       page_size=16, num_pages=10)
+    assert call(ctypes.byref(cpq2)) == kvd.ERR_INVALID_ARG                   # scales not 4-byte aligned
     cp = kvd._CCache(k=FAKE, v=FAKE, block_table=FAKE, max_blocks=4, page_size=24, num_pages=10)
     assert call(ctypes.byref(cp)) == kvd.ERR_INVALID_ARG                     # page size not a power of two
     assert call(ctypes.byref(c), T=65) == kvd.ERR_UNSUPPORTED                # T > KVD_MAX_TOKENS
