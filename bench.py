@@ -64,6 +64,9 @@ def parse_args():
                     help="query tokens per sequence (T > 1: a speculative check step; up to 64)")
     ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "int8"],
                     help="int8: the cache quantized per (token, KV head) row")
+    ap.add_argument("--softmax", default="online", choices=["online", "unified"],
+                    help="unified: every split's partial softmax against one maximum phi (plain-sum merge)")
+    ap.add_argument("--phi", type=float, default=0.0, help="the unified maximum, in logit units")
     ap.add_argument("--page-order", default="shuffled", choices=["shuffled", "sequential"],
                     help="paged: pages in random order over the pool, or each sequence's pages in a row")
     return ap.parse_args()
@@ -270,6 +273,9 @@ def run_ours(args):
     multi = T > 1
     if multi and (args.page_size or args.kv_dtype != "bf16"):
         raise SystemExit("--tokens > 1 takes a contiguous bf16 cache")
+    umax = args.softmax == "unified"
+    if umax and (multi or args.page_size or args.kv_dtype != "bf16"):
+        raise SystemExit("--softmax unified takes one query token and a contiguous bf16 cache")
     # T > 1: the same lengths, the last T tokens of each sequence new this step
     inp = (workloads.multi_step_inputs(w, T, pad_bits=0) if multi else workloads.step_inputs(w, pad_bits=0))
     B, Hq, D = inp.q.shape[0], inp.q.shape[-2], inp.q.shape[-1]
@@ -347,6 +353,9 @@ def run_ours(args):
         elif paged:
             kvd.decode_step_paged(q, kcs[r], vcs[r], kn, vn, pos, bt, lens, max_len, w.scale, out,
                                   workspace=ws, n_split=args.n_split, stream=stream)
+        elif umax:
+            kvd.decode_step_umax(q, kcs[r], vcs[r], kn, vn, pos, lens, max_len, w.scale, args.phi, out,
+                                 workspace=ws, n_split=args.n_split, stream=stream)
         else:
             kvd.decode_step(q, kcs[r], vcs[r], kn, vn, pos, lens, max_len, w.scale, out, workspace=ws,
                             n_split=args.n_split, stream=stream)
@@ -489,7 +498,7 @@ def run_ours(args):
 
     peak, peak_kind = measured_peaks()
     achieved = step_bytes / (chunk_avg_ms * 1e-3) / 1e9
-    traffic = None if (paged or int8 or multi) else ncu_traffic(w.name)
+    traffic = None if (paged or int8 or multi or umax) else ncu_traffic(w.name)
     cpu = None
     if not args.no_cpu_baseline and not int8 and not multi:
         gbs, sec, n_rows, cores, passes = oracle_rate(w, inp, budget_s=10.0, repeats=1,
@@ -511,7 +520,8 @@ def run_ours(args):
                    "timing": "CUDA graph per step, CUDA events on the replay stream",
                    "kv_layout": (f"paged: {args.page_size}-token pages, {pinp.k_pages.shape[0]} pages "
                                  f"in {args.page_order} order" if paged else "contiguous"),
-                   "kv_dtype": args.kv_dtype, "query_tokens": T},
+                   "kv_dtype": args.kv_dtype, "query_tokens": T,
+                   "softmax": f"unified max, phi {args.phi}" if umax else "online max"},
         "tokens_per_s": round(tokens_per_s, 1),
         "hbm_frac_of_step": round(value / world / peak, 4),
         "step_bytes": int(step_bytes), "append_bytes": int(append_bytes), "flops": int(flops),

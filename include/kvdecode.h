@@ -60,6 +60,7 @@ typedef void* kvd_stream_t;
 #define KVD_STATUS_POS_OUT_OF_RANGE 0x2 /* some pos[b] outside [0, s_max): that row not written */
 #define KVD_STATUS_TIMEOUT 0x4          /* an internal pipeline wait gave up (~2 s): outputs invalid */
 #define KVD_STATUS_BAD_PAGE 0x8         /* paged cache: a needed block-table entry named no page of the pool */
+#define KVD_STATUS_UMAX_FALLBACK 0x10   /* unified-maximum calls: some row's scores left the window around phi */
 
 /* Supported shapes: head_dim in {64, 128, 256}; n_heads_q a multiple of
  * n_heads_kv with group size n_heads_q / n_heads_kv <= 64. */
@@ -175,6 +176,34 @@ kvd_status kvd_decode_step(void* k_cache, void* v_cache, const void* k_new, cons
                            float scale, int n_split, void* workspace, size_t workspace_bytes,
                            void* out, kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
                            kvd_stream_t stream);
+
+/*
+ * Unified-maximum softmax: kvd_decode_attention and kvd_decode_step with the
+ * partial softmax of every split taken against one caller-given maximum phi
+ * (in the units of the logits scale * q.k) instead of each split's own,
+ * FlashDecoding++'s asynchronized softmax with a unified maximum (the
+ * FlashDecoding++ summary page, solution 1: partial softmax results need no
+ * synchronised update when they share the maximum). Where a row's scores
+ * stay within [phi - 64 ln 2, phi + 8 ln 2] every partial of the row holds
+ * exp(s - phi) sums, so the merge is a plain sum; the pages leave the
+ * out-of-range case open, and here a row whose scores leave that window falls
+ * back to the usual running maximum in the kernel (no recomputation; the
+ * result is the same softmax either way) and KVD_STATUS_UMAX_FALLBACK is set.
+ * phi must be finite (KVD_ERR_INVALID_ARG); bf16 caches only. Arguments,
+ * results and errors otherwise as kvd_decode_attention and kvd_decode_step.
+ */
+kvd_status kvd_decode_attention_umax(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* seq_lens, int batch, int s_max, int max_seq_len,
+                                     int n_heads_q, int n_heads_kv, int head_dim, float scale, float phi,
+                                     int n_split, void* workspace, size_t workspace_bytes, void* out,
+                                     kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                                     kvd_stream_t stream);
+kvd_status kvd_decode_step_umax(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                                const int32_t* pos, const void* q, const int32_t* seq_lens, int batch, int s_max,
+                                int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim, float scale,
+                                float phi, int n_split, void* workspace, size_t workspace_bytes, void* out,
+                                kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                                kvd_stream_t stream);
 
 /*
  * Paged KV cache. The pages describe keeping the KV cache in an

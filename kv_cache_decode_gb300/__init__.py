@@ -24,6 +24,7 @@ OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_WORKSPACE_TOO_SMALL, ERR_CUDA = range(
 OUT_BF16, OUT_F32 = 0, 1
 STATUS_SEQ_LEN_CLAMPED = 0x1
 STATUS_POS_OUT_OF_RANGE = 0x2
+STATUS_UMAX_FALLBACK = 0x10
 
 # Every symbol include/kvdecode.h declares.
 EXPORTED = (
@@ -33,6 +34,7 @@ EXPORTED = (
     "kvd_decode_attention_paged", "kvd_decode_step_paged", "kvd_kv_quantize_q8", "kvd_kv_append_q8",
     "kvd_decode_attention_q8", "kvd_decode_step_q8", "kvd_decode_plan_multi", "kvd_kv_append_multi",
     "kvd_decode_attention_multi", "kvd_decode_step_multi", "kvd_decode_ex", "kvd_kv_append_q8_paged",
+    "kvd_decode_attention_umax", "kvd_decode_step_umax",
 )
 STATIC_WORKSPACE_BYTES = 16 << 20  # KVD_STATIC_WORKSPACE_BYTES
 
@@ -98,6 +100,11 @@ def _declare(lib):
     lib.kvd_kv_append_q8.restype = I
     lib.kvd_kv_append_q8_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P]
     lib.kvd_kv_append_q8_paged.restype = I
+    # unified maximum: decode_attention / decode_step with phi after scale
+    lib.kvd_decode_attention_umax.argtypes = dec[:11] + [F] + dec[11:]
+    lib.kvd_decode_attention_umax.restype = I
+    lib.kvd_decode_step_umax.argtypes = [P, P, P, P, P, P, P] + dec[4:11] + [F] + dec[11:]
+    lib.kvd_decode_step_umax.restype = I
     lib.kvd_decode_attention_q8.argtypes = [P, P, P, P, P] + dec[3:]
     lib.kvd_decode_attention_q8.restype = I
     lib.kvd_decode_step_q8.argtypes = [P, P, P, P, P, P, P, P, P] + dec[4:]
@@ -635,6 +642,32 @@ def decode_step(q, k_cache, v_cache, k_new, v_new, pos, seq_lens, max_seq_len: i
                      lse, status, stream)
     args = [a[1], a[2], k_new.data_ptr(), v_new.data_ptr(), pos.data_ptr(), a[0], a[3]] + a[4:]
     _check(load().kvd_decode_step(*args), "kvd_decode_step")
+
+
+def decode_attention_umax(q, k_cache, v_cache, seq_lens, max_seq_len: int, scale: float, phi: float, out,
+                          workspace=None, n_split: int = 0, lse=None, status=None, stream=None):
+    """decode_attention with the unified-maximum softmax: every split's partial
+    softmax is taken against phi (logit units) while a row's scores allow,
+    so the merge is a plain sum (kvd_decode_attention_umax)."""
+    a = _decode_args(q, k_cache, v_cache, seq_lens, max_seq_len, scale, n_split, workspace, out, lse, status,
+                     stream)
+    _check(load().kvd_decode_attention_umax(*(a[:11] + [float(phi)] + a[11:])), "kvd_decode_attention_umax")
+
+
+def decode_step_umax(q, k_cache, v_cache, k_new, v_new, pos, seq_lens, max_seq_len: int, scale: float, phi: float,
+                     out, workspace=None, n_split: int = 0, lse=None, status=None, stream=None):
+    """decode_step with the unified-maximum softmax (kvd_decode_step_umax)."""
+    import torch
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _require(t, n, torch.bfloat16, 3)
+    _require(pos, "pos", torch.int32, 1)
+    B, S, Hkv, D = k_cache.shape
+    if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or pos.shape != (B,):
+        raise ValueError("decode_step_umax: inconsistent shapes")
+    a = _decode_args(q, k_cache, v_cache, seq_lens, max_seq_len, scale, n_split, workspace, out, lse, status,
+                     stream)
+    args = [a[1], a[2], k_new.data_ptr(), v_new.data_ptr(), pos.data_ptr(), a[0], a[3]] + a[4:11] + [float(phi)] + a[11:]
+    _check(load().kvd_decode_step_umax(*args), "kvd_decode_step_umax")
 
 
 def split_kv_chunk(q, k_cache, v_cache, seq_lens, max_seq_len: int, scale: float, out,

@@ -164,7 +164,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
                   int D, float scale, int n_split_req, void* workspace, size_t workspace_bytes,
                   void* out, kvd_out_dtype dt, float* lse, int32_t* status, kvd_stream_t stream,
                   const AppendArgs* app = nullptr, const PagedCache* pg = nullptr,
-                  const QuantCache* q8 = nullptr, int T = 1) {
+                  const QuantCache* q8 = nullptr, int T = 1, const float* umax_phi = nullptr) {
     kvd_status st = check_shape(batch, Hq, Hkv, D, dt);
     if (st != KVD_OK) return st;
     if (s_max <= 0 || max_seq_len < 0 || max_seq_len > s_max) return KVD_ERR_INVALID_ARG;
@@ -182,6 +182,10 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     const ChunkKernel* k = nullptr;
     if (T < 1) return KVD_ERR_INVALID_ARG;
     if (T > KVD_MAX_TOKENS) return KVD_ERR_UNSUPPORTED;
+    // Unified maximum: phi in the logits' units (scale * q.k), bf16 caches.
+    const float phi2 = umax_phi ? *umax_phi * 1.4426950408889634f : 0.f;
+    if (umax_phi && !std::isfinite(phi2)) return KVD_ERR_INVALID_ARG;
+    if (umax_phi && q8) return KVD_ERR_UNSUPPORTED;
     st = plan(batch, Hq, Hkv, D, max_seq_len, 0 /* query device if heuristic */, n_split_req, dt,
               &n_split, &need, &k, T);
     if (st != KVD_OK) return st;
@@ -227,6 +231,8 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     p.T = T / vT;
     p.row_blocks = row_blocks;
     p.vT = vT;
+    p.umax = umax_phi ? 1 : 0;
+    p.umax_phi2 = phi2;
     if (q8) {
         p.k_scale = q8->k_scale;
         p.v_scale = q8->v_scale;
@@ -548,6 +554,32 @@ kvd_status kvd_decode_step(void* k_cache, void* v_cache, const void* k_new, cons
     return decode(kBoth, q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q,
                   n_heads_kv, head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype,
                   lse_out, status_word, stream, &app);
+}
+
+kvd_status kvd_decode_attention_umax(const void* q, const void* k_cache, const void* v_cache,
+                                     const int32_t* seq_lens, int batch, int s_max, int max_seq_len,
+                                     int n_heads_q, int n_heads_kv, int head_dim, float scale, float phi,
+                                     int n_split, void* workspace, size_t workspace_bytes, void* out,
+                                     kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                                     kvd_stream_t stream) {
+    return decode(kBoth, q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q, n_heads_kv,
+                  head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype, lse_out, status_word,
+                  stream, nullptr, nullptr, nullptr, 1, &phi);
+}
+
+kvd_status kvd_decode_step_umax(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                                const int32_t* pos, const void* q, const int32_t* seq_lens, int batch, int s_max,
+                                int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim, float scale,
+                                float phi, int n_split, void* workspace, size_t workspace_bytes, void* out,
+                                kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                                kvd_stream_t stream) {
+    const kvd_status st = check_append(k_cache, v_cache, k_new, v_new, pos, batch, s_max, n_heads_kv,
+                                       head_dim, status_word);
+    if (st != KVD_OK) return st;
+    const AppendArgs app{k_cache, v_cache, k_new, v_new, pos};
+    return decode(kBoth, q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q, n_heads_kv,
+                  head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype, lse_out, status_word,
+                  stream, &app, nullptr, nullptr, 1, &phi);
 }
 
 kvd_status kvd_split_kv_chunk(const void* q, const void* k_cache, const void* v_cache,

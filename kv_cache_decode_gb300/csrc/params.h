@@ -51,6 +51,11 @@ struct DecodeParams {
     // attending to its first L_s - vT + 1 + i tokens) and T is 1; the merge
     // reads the lengths the same way. 1 otherwise.
     int vT;
+    // Unified-maximum softmax (bf16 caches): each segment's running maximum
+    // starts at umax_phi2 = phi * log2(e) in the kernels' base-2 score units
+    // and stays there while the row's scores allow (see the kernels).
+    int umax;
+    float umax_phi2;
 };
 
 // One compiled variant of the split-KV chunk kernel.

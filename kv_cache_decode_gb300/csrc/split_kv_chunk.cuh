@@ -380,6 +380,11 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
     uint32_t qf[KS][4];
     float o[ND][4];
     float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+    // Unified-maximum softmax (bf16 caches): m starts each segment at phi, and
+    // an0/an1 record that a row has had a score in it since.
+    const bool umax = !KV8 && p.umax;
+    const float phi2 = p.umax_phi2;
+    bool an0 = false, an1 = false;
 #pragma unroll
     for (int n = 0; n < ND; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
 #pragma unroll
@@ -461,7 +466,8 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                     for (int e = 0; e < 4; ++e) qf[kk][e] = bf16x2_to_f16x2(qf[kk][e]);
                 }
             }
-            m0 = m1 = -CUDART_INF_F;
+            m0 = m1 = umax ? phi2 : -CUDART_INF_F;
+            an0 = an1 = false;
             l0 = l1 = 0.f;
 #pragma unroll
             for (int n = 0; n < ND; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
@@ -567,12 +573,34 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                 mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
                 mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
             }
-            const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-            const float mu0 = (mn0 == -CUDART_INF_F) ? 0.f : mn0;
-            const float mu1 = (mn1 == -CUDART_INF_F) ? 0.f : mn1;
-            const float a0 = exp2f(m0 - mu0), a1 = exp2f(m1 - mu1);
-            m0 = mn0;
-            m1 = mn1;
+            float mu0, mu1, a0, a1;
+            if (umax) {
+                // Unified maximum (FlashDecoding++'s asynchronized softmax): m
+                // stays at phi while the row's scores lie within [phi - 64,
+                // phi + 8] (base 2), so every partial of such a row shares it
+                // and the merges reduce to plain sums. A larger score moves m
+                // up with the usual rescale, and a row whose first scores lie
+                // below the window starts from its own maximum (nothing is
+                // accumulated yet, so no rescale): the result stays exact.
+                const float n0 = (mx0 > m0 + 8.f || (!an0 && mx0 < m0 - 64.f && mx0 > -CUDART_INF_F)) ? mx0 : m0;
+                const float n1 = (mx1 > m1 + 8.f || (!an1 && mx1 < m1 - 64.f && mx1 > -CUDART_INF_F)) ? mx1 : m1;
+                a0 = (an0 && n0 != m0) ? exp2f(m0 - n0) : 1.f;
+                a1 = (an1 && n1 != m1) ? exp2f(m1 - n1) : 1.f;
+                if ((n0 != m0 || n1 != m1) && (lane & 3) == 0 && p.status)
+                    atomicOr(p.status, KVD_STATUS_UMAX_FALLBACK);
+                an0 |= mx0 > -CUDART_INF_F;
+                an1 |= mx1 > -CUDART_INF_F;
+                mu0 = m0 = n0;
+                mu1 = m1 = n1;
+            } else {
+                const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+                mu0 = (mn0 == -CUDART_INF_F) ? 0.f : mn0;
+                mu1 = (mn1 == -CUDART_INF_F) ? 0.f : mn1;
+                a0 = exp2f(m0 - mu0);
+                a1 = exp2f(m1 - mu1);
+                m0 = mn0;
+                m1 = mn1;
+            }
 
             // P = 2^(s - m) as bf16 A fragments (hi part; lo part for fp32 output).
             uint32_t pa[NS / 2][4];
@@ -675,11 +703,16 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                         const float om1 = mb[(ND * 4 + 1) * 32 + lane];
                         const float ol0 = mb[(ND * 4 + 2) * 32 + lane];
                         const float ol1 = mb[(ND * 4 + 3) * 32 + lane];
-                        const float M0 = fmaxf(m0, om0), M1 = fmaxf(m1, om1);
-                        // a row no slice has seen a token of (causal rows) stays empty
+                        // A slice with nothing summed (l = 0) takes no part: its
+                        // maximum may be -inf or, with the unified maximum, the
+                        // phi it started from. A row no slice has seen a token
+                        // of (causal rows) stays empty.
+                        const float e0 = l0 > 0.f ? m0 : -CUDART_INF_F, f0 = ol0 > 0.f ? om0 : -CUDART_INF_F;
+                        const float e1 = l1 > 0.f ? m1 : -CUDART_INF_F, f1 = ol1 > 0.f ? om1 : -CUDART_INF_F;
+                        const float M0 = fmaxf(e0, f0), M1 = fmaxf(e1, f1);
                         const float U0 = (M0 == -CUDART_INF_F) ? 0.f : M0, U1 = (M1 == -CUDART_INF_F) ? 0.f : M1;
-                        const float A0 = exp2f(m0 - U0), B0 = exp2f(om0 - U0);
-                        const float A1 = exp2f(m1 - U1), B1 = exp2f(om1 - U1);
+                        const float A0 = exp2f(e0 - U0), B0 = exp2f(f0 - U0);
+                        const float A1 = exp2f(e1 - U1), B1 = exp2f(f1 - U1);
                         l0 = A0 * l0 + B0 * ol0;
                         l1 = A1 * l1 + B1 * ol1;
                         m0 = M0;

@@ -559,6 +559,19 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             if (t.seg_start) {
                 mA = mtA;
                 mB = mtB;
+                if (p.umax) {
+                    // Unified maximum (FlashDecoding++'s asynchronized softmax):
+                    // a row whose first tile's maximum lies within [phi - 64,
+                    // phi + 8] (base 2) takes m = phi, shared by all partials of
+                    // such rows, so the merge reduces to plain sums; otherwise
+                    // it starts from its own maximum. The lazy rescale below
+                    // moves m up past phi + 8 (exact either way).
+                    const float phi2 = p.umax_phi2;
+                    if (mtA >= phi2 - 64.f && mtA <= phi2 + 8.f) mA = phi2;
+                    if (mtB >= phi2 - 64.f && mtB <= phi2 + 8.f) mB = phi2;
+                    if (((actA && mA != phi2) || (actB && mB != phi2)) && p.status)
+                        atomicOr(p.status, KVD_STATUS_UMAX_FALLBACK);
+                }
                 lA = lB = 0.f;
             } else {
                 if (mtA > mA + 8.f) {
@@ -571,6 +584,8 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                     alphaB = exp2f(mB - mtB);
                     mB = mtB;
                 }
+                if (p.umax && ((actA && needA) || (actB && needB)) && p.status)
+                    atomicOr(p.status, KVD_STATUS_UMAX_FALLBACK);
             }
             // P = 2^(s - m), packed per row and 8-column group (bf16 hi part; lo
             // part for fp32 output).

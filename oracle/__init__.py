@@ -43,6 +43,14 @@ Functions and the passages they follow (page title, section):
   paged append move the codes' and scales' bytes exactly as they move bf16
   rows (the same C routines over the bytes), and attention is the int8
   attention over the gathered cache.
+* ``decode_attention_unified_max``: FlashDecoding++'s asynchronized softmax
+  with a unified maximum (FlashDecoding++ summary page, solution 1: the
+  partial softmax results of the splits share one maximum phi and need no
+  synchronised update). Each of n_chunks chunks sums exp(s - phi) and
+  exp(s - phi) v with no maximum of its own and the chunks are added up; the
+  page leaves the out-of-range case open, and here a row with a score outside
+  [phi - 64 ln 2, phi + 8 ln 2] is recomputed by ``decode_attention`` and
+  reported. Plain numpy, float64.
 * ``kv_append_multi``, ``decode_attention_multi``: T new tokens per sequence
   (a speculative-decoding check step): their rows are appended at pos[b] ..
   pos[b] + T - 1, and query token i attends to the cached tokens and the new
@@ -62,6 +70,7 @@ small shapes, and a 50-digit decimal brute force on tiny inputs.
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 import subprocess
 import threading
@@ -179,6 +188,55 @@ def decode_attention_chunked(q, k_cache, v_cache, seq_lens, scale, n_chunks: int
     if rc != 0:
         raise ValueError(f"oracle decode_attention_chunked failed ({rc})")
     return out, lse
+
+
+UMAX_WINDOW = (-64.0 * math.log(2.0), 8.0 * math.log(2.0))  # s - phi, natural-log units
+
+
+def _bf16_f64(bits):
+    return (np.asarray(bits, dtype=np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def decode_attention_unified_max(q, k_cache, v_cache, seq_lens, scale, phi, n_chunks: int, lib=None):
+    """Unified-maximum attention: (out [B, Hq, D], lse [B, Hq], fell_back [B, Hq]).
+
+    Per (b, h), the L_b scores s_t = scale * q . k_t go to n_chunks contiguous
+    chunks of ceil(L_b / n_chunks) tokens; chunk j holds l_j = sum exp(s_t - phi)
+    and o_j = sum exp(s_t - phi) v_t, and the row is (sum_j o_j) / (sum_j l_j),
+    lse = phi + ln(sum_j l_j). A row with any s_t - phi outside UMAX_WINDOW is
+    taken from decode_attention instead and flagged. Empty rows: zeros, -inf.
+    """
+    B, S_max, Hq, Hkv, D = _shapes(q, k_cache)
+    G = Hq // Hkv
+    qf, kf, vf = _bf16_f64(q), _bf16_f64(k_cache), _bf16_f64(v_cache)
+    lens = np.asarray(seq_lens, dtype=np.int64)
+    out = np.zeros((B, Hq, D), dtype=np.float64)
+    lse = np.full((B, Hq), -np.inf)
+    fell_back = np.zeros((B, Hq), dtype=bool)
+    lo, hi = UMAX_WINDOW
+    for b in range(B):
+        L = int(max(0, min(lens[b], S_max)))
+        if L == 0:
+            continue
+        c = -(-L // n_chunks)
+        for h in range(Hq):
+            g = h // G
+            s = scale * (kf[b, :L, g, :] @ qf[b, h])
+            if np.any(s - phi < lo) or np.any(s - phi > hi):
+                fell_back[b, h] = True
+                continue
+            l_sum, o_sum = 0.0, np.zeros(D)
+            for j0 in range(0, L, c):
+                j1 = min(j0 + c, L)
+                w = np.exp(s[j0:j1] - phi)
+                l_sum += w.sum()
+                o_sum += w @ vf[b, j0:j1, g, :]
+            out[b, h] = o_sum / l_sum
+            lse[b, h] = phi + math.log(l_sum)
+    if fell_back.any():
+        ref, ref_lse = decode_attention(q, k_cache, v_cache, seq_lens, scale, lib=lib)
+        out[fell_back], lse[fell_back] = ref[fell_back], ref_lse[fell_back]
+    return out, lse, fell_back
 
 
 def attention_weights(q, k_cache, seq_lens, scale, b: int, h: int, lib=None):

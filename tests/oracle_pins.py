@@ -616,6 +616,53 @@ def check_paged_q8_append(lib):
                                                                                vsp[~changed].view(np.uint32))
 
 
+def check_unified_max_equals_definition(lib):
+    # Scores within the window: every chunking gives the softmax itself (out
+    # and lse), with no row falling back.
+    r = np.random.default_rng(90)
+    B, S, Hq, Hkv, D = 3, 40, 4, 2, 8
+    q = _bits(r.standard_normal((B, Hq, D)))
+    k = _bits(r.standard_normal((B, S, Hkv, D)))
+    v = _bits(r.standard_normal((B, S, Hkv, D)))
+    lens = np.array([40, 17, 1], np.int32)
+    want, want_lse = oracle.decode_attention(q, k, v, lens, 0.3, lib=lib)
+    for phi in (0.0, 1.5, -2.0):
+        for n_chunks in (1, 3, 40):
+            out, lse, fb = oracle.decode_attention_unified_max(q, k, v, lens, 0.3, phi, n_chunks, lib=lib)
+            assert not fb.any()
+            assert np.max(np.abs(out - want)) < 1e-13 and np.max(np.abs(lse - want_lse)) < 1e-13, (phi, n_chunks)
+
+
+def check_unified_max_closed_form(lib):
+    # Identical keys with phi equal to their score: every weight is exp(0) = 1,
+    # so the output is the plain mean of the value rows and lse = phi + ln L.
+    D, L = 4, 6
+    q = _bits(np.array([[[1.0, 2.0, 0.0, 0.0]]]))
+    k = _bits(np.tile(np.array([0.5, 0.25, 3.0, -1.0]), (1, L, 1, 1)))
+    vals = np.arange(L * D, dtype=np.float64).reshape(1, L, 1, D)
+    v = _bits(vals)
+    phi = 0.5 * (0.5 + 0.5)  # scale * q . k with scale 0.5
+    out, lse, fb = oracle.decode_attention_unified_max(q, k, v, np.array([L], np.int32), 0.5, phi, 4, lib=lib)
+    assert not fb.any()
+    assert np.array_equal(out[0, 0], vals[0, :, 0, :].mean(axis=0))
+    assert abs(lse[0, 0] - (phi + math.log(L))) < 1e-15
+
+
+def check_unified_max_window_edges(lib):
+    # One token per row, scores 0: phi = -8 ln 2 puts the score on the upper
+    # edge (kept), a little lower phi outside (recomputed); likewise the lower
+    # edge at phi = 64 ln 2. Recomputed rows equal the definition.
+    q = _bits(np.zeros((1, 1, 2)))
+    k = _bits(np.ones((1, 1, 1, 2)))
+    v = _bits(np.array([[[[3.0, -1.0]]]]))
+    lens = np.array([1], np.int32)
+    lo, hi = oracle.UMAX_WINDOW
+    for phi, falls in ((-hi, False), (-hi - 1e-9, True), (-lo, False), (-lo + 1e-9, True)):
+        out, lse, fb = oracle.decode_attention_unified_max(q, k, v, lens, 1.0, phi, 1, lib=lib)
+        assert bool(fb[0, 0]) == falls, phi
+        assert np.max(np.abs(out[0, 0] - [3.0, -1.0])) < 1e-14 and abs(lse[0, 0]) < 1e-12
+
+
 ALL_CHECKS = [
     check_identical_keys_give_mean_of_v,
     check_dominant_score_returns_that_row,
@@ -641,6 +688,9 @@ ALL_CHECKS = [
     check_q8_append,
     check_paged_q8_pools_are_the_cache,
     check_paged_q8_append,
+    check_unified_max_equals_definition,
+    check_unified_max_closed_form,
+    check_unified_max_window_edges,
     check_multi_token_one_is_single,
     check_multi_token_against_torch_causal,
     check_multi_token_append,

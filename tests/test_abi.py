@@ -322,6 +322,21 @@ def test_decode_multi_rejects(lib, T, over, expect):
     assert lib.kvd_decode_attention_multi(*(a[:5] + [T] + a[5:])) == expect
 
 
+@pytest.mark.parametrize("phi,over,expect", [
+    (float("inf"), dict(), kvd.ERR_INVALID_ARG),
+    (float("nan"), dict(), kvd.ERR_INVALID_ARG),
+    (3e38, dict(), kvd.ERR_INVALID_ARG),              # phi * log2(e) overflows float
+    (0.0, dict(q=None), kvd.ERR_INVALID_ARG),
+    (0.0, dict(D=96), kvd.ERR_UNSUPPORTED),
+    (0.0, dict(ws_bytes=16), kvd.ERR_WORKSPACE_TOO_SMALL),
+])
+def test_decode_umax_rejects(lib, phi, over, expect):
+    a = _dec_args(**over)
+    assert lib.kvd_decode_attention_umax(*(a[:11] + [phi] + a[11:])) == expect
+    step = [a[1], a[2], FAKE, FAKE, FAKE, a[0], a[3]] + a[4:11] + [phi] + a[11:]
+    assert lib.kvd_decode_step_umax(*step) == expect
+
+
 def test_decode_ex_rejects(lib):
     c = kvd._CCache(k=FAKE, v=FAKE, s_max=64)
     a = _dec_args()  # q, k, v, lens, B, S, maxlen, Hq, Hkv, D, scale, n_split, ws, ws_bytes, out, dt, lse, status, stream
