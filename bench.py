@@ -463,7 +463,18 @@ def run_ours(args):
         h2d = q_h.nbytes + kn_h.nbytes + vn_h.nbytes + pos_h.nbytes + lens_h.nbytes + bt_h.nbytes
         d2h = out_h.nbytes
 
+        host_steps = None
+        if not (paged or int8 or umax):
+            # the library's host-input step: five input copies, the step, the output copy, in one call
+            bf = lambda t: t.view(torch.bfloat16)
+            staging = torch.empty(kvd.step_staging_bytes(B, T, Hq, Hkv, D), dtype=torch.uint8, device=dev)
+            host_steps = [kvd.HostStep(bf(q_h), bf(kn_h), bf(vn_h), pos_h, lens_h, kcs[r], vcs[r], staging, max_len,
+                                       w.scale, out, out_h, workspace=ws, n_split=args.n_split) for r in range(R)]
+
         def e2e_step(r):
+            if host_steps is not None:
+                host_steps[r]()
+                return
             q.view(torch.int16).copy_(q_h, non_blocking=True)
             kn.view(torch.int16).copy_(kn_h, non_blocking=True)
             vn.view(torch.int16).copy_(vn_h, non_blocking=True)

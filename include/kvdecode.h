@@ -444,6 +444,31 @@ kvd_status kvd_kernel_info(int n_heads_q, int n_heads_kv, int head_dim, kvd_out_
                            int* ctas_per_sm_out, int* seg_unit_out, int* seg_cost_out);
 
 /*
+ * kvd_decode_step_host: one step whose per-step inputs come from the host and
+ * whose result goes back to it, in one call (a deployment convenience, not
+ * part of the method): q_host [batch, n_tokens, Hq, D] bf16, k_new_host,
+ * v_new_host [batch, n_tokens, Hkv, D] bf16, pos_host and seq_lens_host
+ * int32 [batch] are copied (cudaMemcpyAsync on `stream`; pinned host memory
+ * makes the copies asynchronous) into `staging`, a device buffer of at least
+ * kvd_step_staging_bytes(...) bytes, 256-byte aligned; then the step runs as
+ * kvd_decode_step_multi on the staged inputs (n_tokens = 1: kvd_decode_step),
+ * writing `out` on the device, and `out` is copied to out_host (same size).
+ * Nothing is synchronised: out_host is valid once `stream` has reached the end
+ * of this call's work. Every argument is checked before any copy is queued;
+ * errors as kvd_decode_step_multi, plus KVD_ERR_INVALID_ARG for a NULL host
+ * pointer or a missing, small or misaligned staging buffer. The caller owns
+ * all buffers; the cache, workspace, out and lse_out are device memory.
+ */
+size_t kvd_step_staging_bytes(int batch, int n_tokens, int n_heads_q, int n_heads_kv, int head_dim);
+kvd_status kvd_decode_step_host(void* k_cache, void* v_cache, const void* q_host, const void* k_new_host,
+                                const void* v_new_host, const int32_t* pos_host, const int32_t* seq_lens_host,
+                                void* staging, size_t staging_bytes, int batch, int n_tokens, int s_max,
+                                int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim, float scale,
+                                int n_split, void* workspace, size_t workspace_bytes, void* out, void* out_host,
+                                kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                                kvd_stream_t stream);
+
+/*
  * kvd_decode_attention_static: kvd_decode_attention for callers that cannot
  * allocate device memory. (The sources have no counterpart: this is a
  * deployment convenience, not part of the method.)

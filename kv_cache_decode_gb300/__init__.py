@@ -34,7 +34,7 @@ EXPORTED = (
     "kvd_decode_attention_paged", "kvd_decode_step_paged", "kvd_kv_quantize_q8", "kvd_kv_append_q8",
     "kvd_decode_attention_q8", "kvd_decode_step_q8", "kvd_decode_plan_multi", "kvd_kv_append_multi",
     "kvd_decode_attention_multi", "kvd_decode_step_multi", "kvd_decode_ex", "kvd_kv_append_q8_paged",
-    "kvd_decode_attention_umax", "kvd_decode_step_umax",
+    "kvd_decode_attention_umax", "kvd_decode_step_umax", "kvd_step_staging_bytes", "kvd_decode_step_host",
 )
 STATIC_WORKSPACE_BYTES = 16 << 20  # KVD_STATIC_WORKSPACE_BYTES
 
@@ -105,6 +105,11 @@ def _declare(lib):
     lib.kvd_decode_attention_umax.restype = I
     lib.kvd_decode_step_umax.argtypes = [P, P, P, P, P, P, P] + dec[4:11] + [F] + dec[11:]
     lib.kvd_decode_step_umax.restype = I
+    lib.kvd_step_staging_bytes.argtypes = [I, I, I, I, I]
+    lib.kvd_step_staging_bytes.restype = SZ
+    lib.kvd_decode_step_host.argtypes = [P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, I, F, I, P, SZ, P, P, I, P,
+                                         P, P]
+    lib.kvd_decode_step_host.restype = I
     lib.kvd_decode_attention_q8.argtypes = [P, P, P, P, P] + dec[3:]
     lib.kvd_decode_attention_q8.restype = I
     lib.kvd_decode_step_q8.argtypes = [P, P, P, P, P, P, P, P, P] + dec[4:]
@@ -668,6 +673,64 @@ def decode_step_umax(q, k_cache, v_cache, k_new, v_new, pos, seq_lens, max_seq_l
                      stream)
     args = [a[1], a[2], k_new.data_ptr(), v_new.data_ptr(), pos.data_ptr(), a[0], a[3]] + a[4:11] + [float(phi)] + a[11:]
     _check(load().kvd_decode_step_umax(*args), "kvd_decode_step_umax")
+
+
+def step_staging_bytes(batch: int, n_tokens: int, n_heads_q: int, n_heads_kv: int, head_dim: int) -> int:
+    """Device staging bytes decode_step_host needs (kvd_step_staging_bytes)."""
+    return int(load().kvd_step_staging_bytes(batch, n_tokens, n_heads_q, n_heads_kv, head_dim))
+
+
+class HostStep:
+    """A step from host inputs to a host result (kvd_decode_step_host) with its
+    buffers bound once: the CPU tensors q_host [B, Hq, D] or [B, T, Hq, D]
+    (bf16), k_new_host, v_new_host ([B, Hkv, D] or [B, T, Hkv, D]), pos_host,
+    seq_lens_host (int32 [B]), the device cache, the device buffer `staging`
+    (step_staging_bytes), `out` and its CPU copy out_host. Each call copies the
+    host inputs' current contents in, runs the step and copies `out` back, on
+    `stream` (pin the host tensors for asynchronous copies); nothing is
+    synchronised. Arguments are checked here and by the library on every call."""
+
+    def __init__(self, q_host, k_new_host, v_new_host, pos_host, seq_lens_host, k_cache, v_cache, staging,
+                 max_seq_len: int, scale: float, out, out_host, workspace=None, n_split: int = 0, lse=None,
+                 status=None, stream=None):
+        import torch
+        for t, n in ((q_host, "q_host"), (k_new_host, "k_new_host"), (v_new_host, "v_new_host")):
+            if t.dtype != torch.bfloat16 or t.device.type != "cpu" or not t.is_contiguous():
+                raise TypeError(f"{n} must be a contiguous bfloat16 CPU tensor")
+        for t, n in ((pos_host, "pos_host"), (seq_lens_host, "seq_lens_host")):
+            if t.dtype != torch.int32 or t.device.type != "cpu" or not t.is_contiguous():
+                raise TypeError(f"{n} must be a contiguous int32 CPU tensor")
+        if out_host.device.type != "cpu" or out_host.dtype != out.dtype or out_host.shape != out.shape:
+            raise TypeError("out_host must be a CPU tensor like out")
+        _require(k_cache, "k_cache", torch.bfloat16, 4)
+        _require(v_cache, "v_cache", torch.bfloat16, 4)
+        T = q_host.shape[1] if q_host.dim() == 4 else 1
+        B, Hq, D = q_host.shape[0], q_host.shape[-2], q_host.shape[-1]
+        S, Hkv = k_cache.shape[1], k_cache.shape[2]
+        code = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32 if out.dtype == torch.float32 else None
+        if code is None or out.shape != q_host.shape:
+            raise TypeError("out must be bfloat16 or float32, shaped like q")
+        ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(),
+                                                               workspace.numel() * workspace.element_size())
+        self._keep = (q_host, k_new_host, v_new_host, pos_host, seq_lens_host, k_cache, v_cache, staging, out,
+                      out_host, workspace, lse, status)
+        self._fn = load().kvd_decode_step_host
+        self._args = (k_cache.data_ptr(), v_cache.data_ptr(), q_host.data_ptr(), k_new_host.data_ptr(),
+                      v_new_host.data_ptr(), pos_host.data_ptr(), seq_lens_host.data_ptr(), staging.data_ptr(),
+                      staging.numel() * staging.element_size(), B, T, S, int(max_seq_len), Hq, Hkv, D,
+                      float(scale), int(n_split), ws_ptr, ws_bytes, out.data_ptr(), out_host.data_ptr(), code,
+                      _ptr(lse), _ptr(status), _stream_handle(stream))
+
+    def __call__(self):
+        _check(self._fn(*self._args), "kvd_decode_step_host")
+
+
+def decode_step_host(q_host, k_new_host, v_new_host, pos_host, seq_lens_host, k_cache, v_cache, staging,
+                     max_seq_len: int, scale: float, out, out_host, workspace=None, n_split: int = 0, lse=None,
+                     status=None, stream=None):
+    """One HostStep call: copy the host inputs in, run the step, copy out back."""
+    HostStep(q_host, k_new_host, v_new_host, pos_host, seq_lens_host, k_cache, v_cache, staging, max_seq_len,
+             scale, out, out_host, workspace, n_split, lse, status, stream)()
 
 
 def split_kv_chunk(q, k_cache, v_cache, seq_lens, max_seq_len: int, scale: float, out,

@@ -367,6 +367,62 @@ kvd_status kvd_decode_step_multi(void* k_cache, void* v_cache, const void* k_new
                   stream, &app, nullptr, nullptr, n_tokens);
 }
 
+size_t kvd_step_staging_bytes(int batch, int n_tokens, int n_heads_q, int n_heads_kv, int head_dim) {
+    if (batch < 0 || n_tokens < 1 || n_heads_q < 1 || n_heads_kv < 1 || head_dim < 1) return 0;
+    const size_t BT = (size_t)batch * n_tokens;
+    return align256(BT * n_heads_q * head_dim * 2) + 2 * align256(BT * n_heads_kv * head_dim * 2) +
+           2 * align256((size_t)batch * 4);
+}
+
+kvd_status kvd_decode_step_host(void* k_cache, void* v_cache, const void* q_host, const void* k_new_host,
+                                const void* v_new_host, const int32_t* pos_host, const int32_t* seq_lens_host,
+                                void* staging, size_t staging_bytes, int batch, int n_tokens, int s_max,
+                                int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim, float scale,
+                                int n_split, void* workspace, size_t workspace_bytes, void* out, void* out_host,
+                                kvd_out_dtype out_dtype, float* lse_out, int32_t* status_word,
+                                kvd_stream_t stream) {
+    if (!q_host || !k_new_host || !v_new_host || !pos_host || !seq_lens_host || !out_host || !staging)
+        return KVD_ERR_INVALID_ARG;
+    kvd_status st = check_shape(batch, n_heads_q, n_heads_kv, head_dim, out_dtype);
+    if (st != KVD_OK) return st;
+    if (n_tokens < 1) return KVD_ERR_INVALID_ARG;
+    if (!aligned(staging, 256) || staging_bytes < kvd_step_staging_bytes(batch, n_tokens, n_heads_q, n_heads_kv,
+                                                                         head_dim))
+        return KVD_ERR_INVALID_ARG;
+    if (batch == 0) return KVD_OK;
+    // The staged inputs: q | k_new | v_new | pos | seq_lens, each 256-byte aligned.
+    const size_t BT = (size_t)batch * n_tokens;
+    const size_t qb = BT * n_heads_q * head_dim * 2, kb = BT * n_heads_kv * head_dim * 2, ib = (size_t)batch * 4;
+    uint8_t* w = static_cast<uint8_t*>(staging);
+    void* q = w;
+    void* k_new = w + align256(qb);
+    void* v_new = static_cast<uint8_t*>(k_new) + align256(kb);
+    int32_t* pos = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(v_new) + align256(kb));
+    int32_t* seq_lens = reinterpret_cast<int32_t*>(reinterpret_cast<uint8_t*>(pos) + align256(ib));
+    // Everything the step checks, before any copy is queued.
+    st = check_append(k_cache, v_cache, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim, status_word);
+    if (st != KVD_OK) return st;
+    int n = 0;
+    size_t need = 0;
+    st = plan(batch, n_heads_q, n_heads_kv, head_dim, max_seq_len, 0, n_split, out_dtype, &n, &need, nullptr,
+              n_tokens);
+    if (st != KVD_OK) return st;
+    if (need > 0 && (!workspace || workspace_bytes < need)) return KVD_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const struct { void* dst; const void* src; size_t n; } h2d[5] = {
+        {q, q_host, qb}, {k_new, k_new_host, kb}, {v_new, v_new_host, kb}, {pos, pos_host, ib},
+        {seq_lens, seq_lens_host, ib}};
+    for (const auto& c : h2d)
+        if (cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, s) != cudaSuccess) return KVD_ERR_CUDA;
+    const AppendArgs app{k_cache, v_cache, k_new, v_new, pos};
+    st = decode(kBoth, q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q, n_heads_kv, head_dim,
+                scale, n_split, workspace, workspace_bytes, out, out_dtype, lse_out, status_word, stream, &app,
+                nullptr, nullptr, n_tokens);
+    if (st != KVD_OK) return st;
+    const size_t ob = BT * n_heads_q * head_dim * (out_dtype == KVD_OUT_F32 ? 4 : 2);
+    return cudaMemcpyAsync(out_host, out, ob, cudaMemcpyDeviceToHost, s) == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
+}
+
 kvd_status kvd_decode_ex(const kvd_cache* cache, const void* q, const int32_t* seq_lens, int batch, int n_tokens,
                          int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim, float scale, int n_split,
                          void* workspace, size_t workspace_bytes, void* out, kvd_out_dtype out_dtype,

@@ -27,7 +27,7 @@ def lib():
 
 def test_exports_every_declared_symbol(lib):
     text = open(HEADER).read()
-    declared = set(re.findall(r"^\s*(?:kvd_status|const char\*)\s+(kvd_\w+)\s*\(", text, re.M))
+    declared = set(re.findall(r"^\s*(?:kvd_status|const char\*|size_t)\s+(kvd_\w+)\s*\(", text, re.M))
     assert declared == set(kvd.EXPORTED)
     for name in declared:
         assert hasattr(lib, name), name
@@ -335,6 +335,39 @@ def test_decode_umax_rejects(lib, phi, over, expect):
     assert lib.kvd_decode_attention_umax(*(a[:11] + [phi] + a[11:])) == expect
     step = [a[1], a[2], FAKE, FAKE, FAKE, a[0], a[3]] + a[4:11] + [phi] + a[11:]
     assert lib.kvd_decode_step_umax(*step) == expect
+
+
+def test_step_staging_bytes(lib):
+    al = lambda x: -(-x // 256) * 256
+    # q | k_new | v_new | pos | seq_lens, each 256-byte aligned
+    assert lib.kvd_step_staging_bytes(3, 2, 8, 2, 128) == al(6 * 8 * 128 * 2) + 2 * al(6 * 2 * 128 * 2) + 2 * al(12)
+    assert lib.kvd_step_staging_bytes(3, 0, 8, 2, 128) == 0
+
+
+def _host_step_args(**over):
+    a = dict(k=FAKE, v=FAKE, qh=FAKE, knh=FAKE, vnh=FAKE, posh=FAKE, lensh=FAKE, stg=FAKE, stg_bytes=1 << 20, B=2,
+             T=1, S=64, maxlen=64, Hq=8, Hkv=2, D=128, scale=0.088, n_split=4, ws=FAKE, ws_bytes=1 << 20,
+             out=FAKE, outh=FAKE, dt=0, lse=None, status=None, stream=None)
+    a.update(over)
+    return list(a.values())
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(qh=None), kvd.ERR_INVALID_ARG),
+    (dict(lensh=None), kvd.ERR_INVALID_ARG),
+    (dict(outh=None), kvd.ERR_INVALID_ARG),
+    (dict(stg=None), kvd.ERR_INVALID_ARG),
+    (dict(stg=FAKE + 16), kvd.ERR_INVALID_ARG),       # staging not 256-byte aligned
+    (dict(stg_bytes=1024), kvd.ERR_INVALID_ARG),      # staging too small
+    (dict(T=0), kvd.ERR_INVALID_ARG),
+    (dict(D=96), kvd.ERR_UNSUPPORTED),
+    (dict(k=None), kvd.ERR_INVALID_ARG),
+    (dict(ws_bytes=16), kvd.ERR_WORKSPACE_TOO_SMALL),
+    (dict(B=0), kvd.OK),                              # nothing to copy or launch
+])
+def test_decode_step_host_rejects(lib, over, expect):
+    # every rejection comes before any copy is queued (the pointers are fake)
+    assert lib.kvd_decode_step_host(*_host_step_args(**over)) == expect
 
 
 def test_decode_ex_rejects(lib):
