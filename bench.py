@@ -467,8 +467,12 @@ def run_ours(args):
         if not (paged or int8 or umax):
             # the library's host-input step: five input copies, the step, the output copy, in one call
             bf = lambda t: t.view(torch.bfloat16)
+            # the step's inputs in one pinned packet laid out like the device staging buffer: one copy in
             staging = torch.empty(kvd.step_staging_bytes(B, T, Hq, Hkv, D), dtype=torch.uint8, device=dev)
-            host_steps = [kvd.HostStep(bf(q_h), bf(kn_h), bf(vn_h), pos_h, lens_h, kcs[r], vcs[r], staging, max_len,
+            _, pq, pkn, pvn, ppos, plens = kvd.alloc_host_packet(B, T, Hq, Hkv, D)
+            for dst, src in ((pq, bf(q_h)), (pkn, bf(kn_h)), (pvn, bf(vn_h)), (ppos, pos_h), (plens, lens_h)):
+                dst.copy_(src)
+            host_steps = [kvd.HostStep(pq, pkn, pvn, ppos, plens, kcs[r], vcs[r], staging, max_len,
                                        w.scale, out, out_h, workspace=ws, n_split=args.n_split) for r in range(R)]
 
         def e2e_step(r):

@@ -453,6 +453,9 @@ kvd_status kvd_kernel_info(int n_heads_q, int n_heads_kv, int head_dim, kvd_out_
  * kvd_step_staging_bytes(...) bytes, 256-byte aligned; then the step runs as
  * kvd_decode_step_multi on the staged inputs (n_tokens = 1: kvd_decode_step),
  * writing `out` on the device, and `out` is copied to out_host (same size).
+ * Host inputs laid out like the staging buffer (q | k_new | v_new | pos |
+ * seq_lens, each 256-byte aligned, one host packet starting at q_host) are
+ * copied with one cudaMemcpyAsync instead of five.
  * Nothing is synchronised: out_host is valid once `stream` has reached the end
  * of this call's work. Every argument is checked before any copy is queued;
  * errors as kvd_decode_step_multi, plus KVD_ERR_INVALID_ARG for a NULL host

@@ -725,6 +725,26 @@ class HostStep:
         _check(self._fn(*self._args), "kvd_decode_step_host")
 
 
+def alloc_host_packet(batch: int, n_tokens: int, n_heads_q: int, n_heads_kv: int, head_dim: int):
+    """One pinned host buffer laid out like decode_step_host's staging buffer,
+    and its views (q, k_new, v_new, pos, seq_lens; shapes as decode_step_host
+    takes them). A HostStep over these views copies its inputs in one copy."""
+    import torch
+    B, T = batch, n_tokens
+    al = lambda n: -(-n // 256) * 256
+    nq, nk, ni = B * T * n_heads_q * head_dim * 2, B * T * n_heads_kv * head_dim * 2, B * 4
+    packet = torch.empty(step_staging_bytes(B, T, n_heads_q, n_heads_kv, head_dim), dtype=torch.uint8).pin_memory()
+    offs = [0, al(nq), al(nq) + al(nk), al(nq) + 2 * al(nk), al(nq) + 2 * al(nk) + al(ni)]
+    qs = (B, n_heads_q, head_dim) if T == 1 else (B, T, n_heads_q, head_dim)
+    ks = (B, n_heads_kv, head_dim) if T == 1 else (B, T, n_heads_kv, head_dim)
+    q = packet[offs[0]:offs[0] + nq].view(torch.bfloat16).view(qs)
+    kn = packet[offs[1]:offs[1] + nk].view(torch.bfloat16).view(ks)
+    vn = packet[offs[2]:offs[2] + nk].view(torch.bfloat16).view(ks)
+    pos = packet[offs[3]:offs[3] + ni].view(torch.int32)
+    lens = packet[offs[4]:offs[4] + ni].view(torch.int32)
+    return packet, q, kn, vn, pos, lens
+
+
 def decode_step_host(q_host, k_new_host, v_new_host, pos_host, seq_lens_host, k_cache, v_cache, staging,
                      max_seq_len: int, scale: float, out, out_host, workspace=None, n_split: int = 0, lse=None,
                      status=None, stream=None):

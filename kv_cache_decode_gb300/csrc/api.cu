@@ -409,11 +409,24 @@ kvd_status kvd_decode_step_host(void* k_cache, void* v_cache, const void* q_host
     if (st != KVD_OK) return st;
     if (need > 0 && (!workspace || workspace_bytes < need)) return KVD_ERR_WORKSPACE_TOO_SMALL;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    const struct { void* dst; const void* src; size_t n; } h2d[5] = {
-        {q, q_host, qb}, {k_new, k_new_host, kb}, {v_new, v_new_host, kb}, {pos, pos_host, ib},
-        {seq_lens, seq_lens_host, ib}};
-    for (const auto& c : h2d)
-        if (cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, s) != cudaSuccess) return KVD_ERR_CUDA;
+    // Host inputs laid out like the staging buffer (one packet from q_host on)
+    // go in one copy; otherwise one copy each.
+    const uint8_t* hq = static_cast<const uint8_t*>(q_host);
+    const uint8_t* stg = static_cast<const uint8_t*>(staging);
+    auto at = [&](const void* dev) { return hq + (static_cast<const uint8_t*>(dev) - stg); };
+    const bool packed = k_new_host == at(k_new) && v_new_host == at(v_new) &&
+                        reinterpret_cast<const uint8_t*>(pos_host) == at(pos) &&
+                        reinterpret_cast<const uint8_t*>(seq_lens_host) == at(seq_lens);
+    if (packed) {
+        const size_t total = static_cast<const uint8_t*>(static_cast<const void*>(seq_lens)) + ib - stg;
+        if (cudaMemcpyAsync(staging, q_host, total, cudaMemcpyHostToDevice, s) != cudaSuccess) return KVD_ERR_CUDA;
+    } else {
+        const struct { void* dst; const void* src; size_t n; } h2d[5] = {
+            {q, q_host, qb}, {k_new, k_new_host, kb}, {v_new, v_new_host, kb}, {pos, pos_host, ib},
+            {seq_lens, seq_lens_host, ib}};
+        for (const auto& c : h2d)
+            if (cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, s) != cudaSuccess) return KVD_ERR_CUDA;
+    }
     const AppendArgs app{k_cache, v_cache, k_new, v_new, pos};
     st = decode(kBoth, q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q, n_heads_kv, head_dim,
                 scale, n_split, workspace, workspace_bytes, out, out_dtype, lse_out, status_word, stream, &app,

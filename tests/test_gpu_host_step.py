@@ -52,3 +52,36 @@ def test_host_step_equals_device_step(Hq, Hkv, D, T):
     got = out_h.float().numpy()
     assert np.all(np.isfinite(got)) and not np.array_equal(out_h.view(torch.int16).numpy().view(np.uint16),
                                                            bf16_tensor_bits(ref))
+
+
+@pytest.mark.parametrize("T", [1, 2])
+def test_packed_host_inputs_equal_separate(T):
+    """Inputs in one pinned packet laid out like the staging buffer (one copy
+    in) give the same step as separate host tensors (five copies)."""
+    import torch
+    import kv_cache_decode_gb300 as kvd
+    dev = cuda_or_skip()
+    Hq, Hkv, D = 16, 4, 128
+    w = workloads.Workload("hp", 5, Hq, Hkv, D, 500, T, 500, 112)
+    mi = workloads.multi_step_inputs(w, T)
+    B, S = mi.q.shape[0], mi.k_cache.shape[1]
+    squeeze = (lambda a: a[:, 0]) if T == 1 else (lambda a: a)
+    q_np, kn_np, vn_np = squeeze(mi.q), squeeze(mi.k_new), squeeze(mi.v_new)
+    _, nbytes = kvd.decode_plan_multi(B, T, Hq, Hkv, D, S, 0, 0, "bf16")
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    staging = torch.empty(kvd.step_staging_bytes(B, T, Hq, Hkv, D), dtype=torch.uint8, device=dev)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    sep = [pin(a.view(np.int16)).view(torch.bfloat16) for a in (q_np, kn_np, vn_np)] + [pin(mi.pos), pin(mi.seq_lens)]
+    packet, *views = kvd.alloc_host_packet(B, T, Hq, Hkv, D)
+    for dst, src in zip(views, sep):
+        dst.copy_(src)
+    outs = []
+    for inputs in (sep, views):
+        kc, vc = to_dev_bf16(mi.k_cache, dev), to_dev_bf16(mi.v_cache, dev)
+        out = torch.empty(q_np.shape, dtype=torch.bfloat16, device=dev)
+        out_h = torch.full(q_np.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+        kvd.decode_step_host(*inputs, kc, vc, staging, S, w.scale, out, out_h, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append((out_h.view(torch.int16).numpy().copy(), bf16_tensor_bits(kc)))
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+    assert not np.isnan((outs[1][0].view(np.uint16).astype(np.uint32) << 16).view(np.float32)).any()
