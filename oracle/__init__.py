@@ -37,6 +37,13 @@ Functions and the passages they follow (page title, section):
   generation throughput and latency", the quantization bullet names int8 KV
   caches; the scheme is this library's reading. Attention over it is the
   attention above over the rows read back (scale * code), in double.
+* ``quantize_fp8``, ``dequantize_fp8``, ``e4m3_encode``, ``e4m3_value``: the
+  fp8 cache, the same per-row scheme with the OCP E4M3 format in place of
+  int8 (scale = max|x| / 448, code = E4M3(x / scale), round to nearest even,
+  saturating, +0 for values that round to zero); the same page names fp8 KV
+  caches beside int8. The encoder searches the format's finite values, so it
+  follows from the format's definition alone. The 8-bit functions below take
+  ``fmt="fp8"`` for it.
 * ``paged_gather_q8``, ``kv_append_q8_paged``, ``decode_attention_q8_paged``:
   an int8 cache in page pools (codes [num_pages, P, Hkv, D], scales
   [num_pages, P, Hkv]), the two readings above combined: the page gather and
@@ -131,6 +138,14 @@ def _declare(lib):
     lib.kvo_dequantize_q8.restype = I
     lib.kvo_decode_attention_f64kv.argtypes = [P, P, P, P, I, I, I, I, I, Dbl, P, P, I]
     lib.kvo_decode_attention_f64kv.restype = I
+    lib.kvo_e4m3_encode.argtypes = [ctypes.c_float]
+    lib.kvo_e4m3_encode.restype = I
+    lib.kvo_e4m3_value.argtypes = [I]
+    lib.kvo_e4m3_value.restype = Dbl
+    lib.kvo_quantize_fp8.argtypes = [P, L, I, P, P]
+    lib.kvo_quantize_fp8.restype = I
+    lib.kvo_dequantize_fp8.argtypes = [P, P, L, I, P]
+    lib.kvo_dequantize_fp8.restype = I
     lib.kvo_max_threads.argtypes = []
     lib.kvo_max_threads.restype = I
     return lib
@@ -359,6 +374,59 @@ def dequantize_q8(codes, scales, lib=None):
     return out
 
 
+def quantize_fp8(x, lib=None):
+    """fp8 E4M3 codes (uint8, same shape) and float32 scales (shape[:-1]) of bf16
+    rows x[..., D]: scale = max|x| / 448, code = E4M3(x / scale) (kvo_e4m3_encode)."""
+    lib = lib or _load()
+    x, xp = _u16(x)
+    D = x.shape[-1]
+    codes = np.zeros(x.shape, dtype=np.uint8)
+    scales = np.zeros(x.shape[:-1], dtype=np.float32)
+    rc = lib.kvo_quantize_fp8(xp, x.size // D, D, codes.ctypes.data_as(ctypes.c_void_p),
+                              scales.ctypes.data_as(ctypes.c_void_p))
+    if rc != 0:
+        raise ValueError(f"oracle quantize_fp8 failed ({rc})")
+    return codes, scales
+
+
+def dequantize_fp8(codes, scales, lib=None):
+    """Rows read back from fp8: scales[..., None] * E4M3 value of codes, as float64."""
+    lib = lib or _load()
+    codes = np.ascontiguousarray(codes, dtype=np.uint8)
+    scales = np.ascontiguousarray(scales, dtype=np.float32)
+    D = codes.shape[-1]
+    if scales.shape != codes.shape[:-1]:
+        raise ValueError("scales must have the codes' shape without the last axis")
+    out = np.zeros(codes.shape, dtype=np.float64)
+    rc = lib.kvo_dequantize_fp8(codes.ctypes.data_as(ctypes.c_void_p), scales.ctypes.data_as(ctypes.c_void_p),
+                                codes.size // D, D, out.ctypes.data_as(ctypes.c_void_p))
+    if rc != 0:
+        raise ValueError(f"oracle dequantize_fp8 failed ({rc})")
+    return out
+
+
+def e4m3_encode(y: float, lib=None) -> int:
+    """The E4M3 code of one float32 value (round to nearest even, saturating, +0 for zero)."""
+    return int((lib or _load()).kvo_e4m3_encode(float(y)))
+
+
+def e4m3_value(code: int, lib=None) -> float:
+    """The value an E4M3 code stands for."""
+    return float((lib or _load()).kvo_e4m3_value(int(code)))
+
+
+# The 8-bit cache formats: code dtype, quantizer, reader.
+_FORMATS = {"int8": (np.int8, "quantize_q8", "dequantize_q8"),
+            "fp8": (np.uint8, "quantize_fp8", "dequantize_fp8")}
+
+
+def _fmt(fmt):
+    if fmt not in _FORMATS:
+        raise ValueError(f"unknown 8-bit cache format {fmt!r}")
+    dt, qn, dn = _FORMATS[fmt]
+    return dt, globals()[qn], globals()[dn]
+
+
 def decode_attention_f64kv(q, k_cache, v_cache, seq_lens, scale, n_threads: int = 0, lib=None):
     """decode_attention with float64 caches [B, S_max, Hkv, D] (e.g. rows read back from int8)."""
     lib = lib or _load()
@@ -381,15 +449,17 @@ def decode_attention_f64kv(q, k_cache, v_cache, seq_lens, scale, n_threads: int 
     return out, lse
 
 
-def kv_append_q8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, lib=None):
-    """Copies of an int8 cache (codes [B, S_max, Hkv, D], scales [B, S_max, Hkv])
-    with each sequence's new bf16 rows quantized and written at pos[b]; rows
-    with pos outside [0, S_max) are skipped. Returns (kc, vc, ks, vs, n_skipped)."""
-    kc, vc = np.array(k_codes, dtype=np.int8, copy=True), np.array(v_codes, dtype=np.int8, copy=True)
+def kv_append_q8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, lib=None, fmt="int8"):
+    """Copies of an 8-bit cache (codes [B, S_max, Hkv, D], int8 or, fmt "fp8",
+    E4M3 as uint8; scales [B, S_max, Hkv]) with each sequence's new bf16 rows
+    quantized and written at pos[b]; rows with pos outside [0, S_max) are
+    skipped. Returns (kc, vc, ks, vs, n_skipped)."""
+    dt, quant, _ = _fmt(fmt)
+    kc, vc = np.array(k_codes, dtype=dt, copy=True), np.array(v_codes, dtype=dt, copy=True)
     ks, vs = np.array(k_scales, dtype=np.float32, copy=True), np.array(v_scales, dtype=np.float32, copy=True)
     S_max = kc.shape[1]
-    nk, nks = quantize_q8(k_new, lib=lib)
-    nv, nvs = quantize_q8(v_new, lib=lib)
+    nk, nks = quant(k_new, lib=lib)
+    nv, nvs = quant(v_new, lib=lib)
     skipped = 0
     for b, t in enumerate(np.asarray(pos, dtype=np.int64)):
         if t < 0 or t >= S_max:
@@ -408,47 +478,50 @@ def _u16_rows(a, dtype):
     return a.view(np.uint16)
 
 
-def paged_gather_q8(code_pool, scale_pool, block_table, seq_lens, lib=None):
+def paged_gather_q8(code_pool, scale_pool, block_table, seq_lens, lib=None, fmt="int8"):
     """Contiguous int8 cache (codes [B, max_blocks * P, Hkv, D], scales
     [B, max_blocks * P, Hkv]) from page pools, gathered as paged_gather moves
     bf16 rows: rows t < seq_lens[b] from row t % P of page block_table[b, t // P],
     zero codes and a zero scale where the entry names no page; rows past the
     length are not defined. Returns (codes, scales, tokens that read zero rows)."""
-    codes, zeroed = paged_gather(_u16_rows(code_pool, np.int8), block_table, seq_lens, lib=lib)
+    dt = _fmt(fmt)[0]
+    codes, zeroed = paged_gather(_u16_rows(code_pool, dt), block_table, seq_lens, lib=lib)
     scales, _ = paged_gather(_u16_rows(scale_pool, np.float32), block_table, seq_lens, lib=lib)
-    return codes.view(np.int8), scales.view(np.float32)[..., 0], zeroed
+    return codes.view(dt), scales.view(np.float32)[..., 0], zeroed
 
 
 def kv_append_q8_paged(k_code_pool, v_code_pool, k_scale_pool, v_scale_pool, k_new, v_new, block_table, pos,
-                       lib=None):
+                       lib=None, fmt="int8"):
     """Copies of int8 page pools with each sequence's new bf16 rows quantized
     (quantize_q8) and written at pos[b], as kv_append_paged writes bf16 rows.
     Returns (kc, vc, ks, vs, n_skipped, n_bad_page)."""
-    nk, nks = quantize_q8(k_new, lib=lib)
-    nv, nvs = quantize_q8(v_new, lib=lib)
-    kc, vc, skipped, bad = kv_append_paged(_u16_rows(k_code_pool, np.int8), _u16_rows(v_code_pool, np.int8),
-                                           _u16_rows(nk, np.int8), _u16_rows(nv, np.int8), block_table, pos,
-                                           lib=lib)
+    dt, quant, _ = _fmt(fmt)
+    nk, nks = quant(k_new, lib=lib)
+    nv, nvs = quant(v_new, lib=lib)
+    kc, vc, skipped, bad = kv_append_paged(_u16_rows(k_code_pool, dt), _u16_rows(v_code_pool, dt),
+                                           _u16_rows(nk, dt), _u16_rows(nv, dt), block_table, pos, lib=lib)
     ks, vs, _, _ = kv_append_paged(_u16_rows(k_scale_pool, np.float32), _u16_rows(v_scale_pool, np.float32),
                                    _u16_rows(nks, np.float32), _u16_rows(nvs, np.float32), block_table, pos,
                                    lib=lib)
-    return (kc.view(np.int8), vc.view(np.int8), ks.view(np.float32)[..., 0], vs.view(np.float32)[..., 0],
+    return (kc.view(dt), vc.view(dt), ks.view(np.float32)[..., 0], vs.view(np.float32)[..., 0],
             skipped, bad)
 
 
 def decode_attention_q8_paged(q, k_code_pool, v_code_pool, k_scale_pool, v_scale_pool, block_table, seq_lens,
-                              scale, n_threads: int = 0, lib=None):
-    """decode_attention_q8 over the int8 cache gathered from the page pools."""
-    kc, ks, _ = paged_gather_q8(k_code_pool, k_scale_pool, block_table, seq_lens, lib=lib)
-    vc, vs, _ = paged_gather_q8(v_code_pool, v_scale_pool, block_table, seq_lens, lib=lib)
-    return decode_attention_q8(q, kc, vc, ks, vs, seq_lens, scale, n_threads=n_threads, lib=lib)
+                              scale, n_threads: int = 0, lib=None, fmt="int8"):
+    """decode_attention_q8 over the 8-bit cache gathered from the page pools."""
+    kc, ks, _ = paged_gather_q8(k_code_pool, k_scale_pool, block_table, seq_lens, lib=lib, fmt=fmt)
+    vc, vs, _ = paged_gather_q8(v_code_pool, v_scale_pool, block_table, seq_lens, lib=lib, fmt=fmt)
+    return decode_attention_q8(q, kc, vc, ks, vs, seq_lens, scale, n_threads=n_threads, lib=lib, fmt=fmt)
 
 
 def decode_attention_q8(q, k_codes, v_codes, k_scales, v_scales, seq_lens, scale, n_threads: int = 0,
-                        lib=None):
-    """Attention over an int8 cache: the rows read back, then decode_attention_f64kv."""
-    k = dequantize_q8(k_codes, k_scales, lib=lib)
-    v = dequantize_q8(v_codes, v_scales, lib=lib)
+                        lib=None, fmt="int8"):
+    """Attention over an 8-bit cache (int8, or fmt "fp8": E4M3): the rows read
+    back, then decode_attention_f64kv."""
+    deq = _fmt(fmt)[2]
+    k = deq(k_codes, k_scales, lib=lib)
+    v = deq(v_codes, v_scales, lib=lib)
     return decode_attention_f64kv(q, k, v, seq_lens, scale, n_threads=n_threads, lib=lib)
 
 

@@ -363,6 +363,76 @@ int kvo_dequantize_q8(const int8_t* codes, const float* scales, long rows, int D
     return 0;
 }
 
+/* ---- fp8 (E4M3) KV cache ----
+ * The OCP 8-bit floating-point format E4M3: a sign bit, 4 exponent bits with
+ * bias 7 and 3 mantissa bits; exponent field 0 holds the subnormals
+ * m/8 * 2^-6, the all-ones pattern S.1111.111 is NaN, there are no
+ * infinities, and the largest finite magnitude is 1.75 * 2^8 = 448. */
+static double e4m3_value(int code)
+{
+    const int e = (code >> 3) & 15, m = code & 7;
+    const double v = (e == 0) ? ldexp(m / 8.0, -6) : ldexp(1.0 + m / 8.0, e - 7);
+    return (code & 0x80) ? -v : v;
+}
+
+/* The E4M3 code nearest to y: round to nearest, ties to the code with the even
+ * low bit (adjacent codes alternate), magnitudes past 448 saturate to 448, and
+ * a value that rounds to zero is stored as +0 (code 0). A search over the 127
+ * finite magnitudes, in order, so the comparison is plain. */
+int kvo_e4m3_encode(float y)
+{
+    const double a = fabs((double)y);
+    int best = 0;
+    double bd = a;  /* distance to code 0 */
+    for (int c = 1; c <= 0x7E; ++c) {
+        const double d = fabs(e4m3_value(c) - a);
+        if (d < bd || (d == bd && (c & 1) == 0)) {
+            best = c;
+            bd = d;
+        }
+    }
+    if (best == 0) return 0;
+    return (y < 0.0f) ? (best | 0x80) : best;
+}
+
+double kvo_e4m3_value(int code) { return e4m3_value(code & 0xFF); }
+
+/* fp8 rows: a = max_d |x_d|, scale = a / 448, code_d = E4M3(x_d / scale), both
+ * divisions IEEE float32 (a = 0: scale 0 and codes 0). */
+int kvo_quantize_fp8(const uint16_t* x, long rows, int D, uint8_t* codes, float* scales)
+{
+    if (rows < 0 || D <= 0) return -1;
+    for (long r = 0; r < rows; ++r) {
+        const uint16_t* xr = x + (size_t)r * D;
+        float a = 0.0f;
+        for (int d = 0; d < D; ++d) {
+            const float v = fabsf((float)bf16_to_double(xr[d]));
+            if (v > a) a = v;
+        }
+        volatile float sc = a / 448.0f;
+        scales[r] = sc;
+        for (int d = 0; d < D; ++d) {
+            int c = 0;
+            if (a > 0.0f) {
+                volatile float y = (float)bf16_to_double(xr[d]) / sc;
+                c = kvo_e4m3_encode(y);
+            }
+            codes[(size_t)r * D + d] = (uint8_t)c;
+        }
+    }
+    return 0;
+}
+
+/* Rows read back from fp8 codes: out[r, d] = scales[r] * E4M3 value of codes[r, d]. */
+int kvo_dequantize_fp8(const uint8_t* codes, const float* scales, long rows, int D, double* out)
+{
+    if (rows < 0 || D <= 0) return -1;
+    for (long r = 0; r < rows; ++r)
+        for (int d = 0; d < D; ++d)
+            out[(size_t)r * D + d] = (double)scales[r] * e4m3_value(codes[(size_t)r * D + d]);
+    return 0;
+}
+
 /* kvo_decode_attention with the caches given as doubles (e.g. rows read back
  * from int8): the same definition, the same loops. */
 int kvo_decode_attention_f64kv(const uint16_t* q, const double* k, const double* v,

@@ -14,6 +14,7 @@ import math
 from decimal import Decimal, getcontext
 
 import numpy as np
+import pytest
 
 import oracle
 from workloads import bf16_bits_to_f32, f32_to_bf16_bits
@@ -663,6 +664,87 @@ def check_unified_max_window_edges(lib):
         assert np.max(np.abs(out[0, 0] - [3.0, -1.0])) < 1e-14 and abs(lse[0, 0]) < 1e-12
 
 
+def check_e4m3_format_values(lib):
+    # Values the E4M3 definition fixes: bias 7, 3 mantissa bits, subnormals
+    # m/8 * 2^-6, largest finite 1.75 * 2^8.
+    fixed = {0x00: 0.0, 0x01: 2.0 ** -9, 0x07: 7 * 2.0 ** -9, 0x08: 2.0 ** -6, 0x38: 1.0, 0x3F: 1.875,
+             0x40: 2.0, 0x7E: 448.0, 0xB8: -1.0, 0xFE: -448.0, 0x81: -(2.0 ** -9)}
+    for code, want in fixed.items():
+        assert oracle.e4m3_value(code, lib=lib) == want, hex(code)
+
+
+def check_e4m3_rounding(lib):
+    # Every finite value encodes to its own code (+-0 to +0); midpoints between
+    # neighbours go to the code with the even low bit; past 448 saturates.
+    for c in list(range(1, 0x7F)) + list(range(0x81, 0xFF)):
+        assert oracle.e4m3_encode(oracle.e4m3_value(c, lib=lib), lib=lib) == c, hex(c)
+    assert oracle.e4m3_encode(-0.0, lib=lib) == 0 and oracle.e4m3_encode(-1e-9, lib=lib) == 0
+    for c in range(0, 0x7E):
+        lo, hi = oracle.e4m3_value(c, lib=lib), oracle.e4m3_value(c + 1, lib=lib)
+        mid = np.float32((lo + hi) / 2)
+        if float(mid) != (lo + hi) / 2:
+            continue  # not a float32 value
+        want = c if c % 2 == 0 else c + 1
+        assert oracle.e4m3_encode(float(mid), lib=lib) == (want if want else 0), hex(c)
+    for y in (448.0, 449.0, 464.0, 500.0, 1e30):
+        assert oracle.e4m3_encode(y, lib=lib) == 0x7E and oracle.e4m3_encode(-y, lib=lib) == 0xFE
+
+
+def check_e4m3_against_torch(lib):
+    # torch's float8_e4m3fn conversion (round to nearest even) agrees on every
+    # value inside the finite range, subnormals included (torch keeps the sign
+    # of a zero result; the scheme here stores +0).
+    torch = pytest.importorskip("torch")
+    r = np.random.default_rng(73)
+    ys = np.concatenate([r.uniform(-448, 448, 3000), r.uniform(-0.02, 0.02, 3000),
+                         np.exp(r.uniform(-12, 6, 3000)) * r.choice([-1, 1], 3000)]).astype(np.float32)
+    ref = torch.from_numpy(ys).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ref = np.where((ref & 0x7F) == 0, 0, ref)
+    got = np.array([oracle.e4m3_encode(float(y), lib=lib) for y in ys])
+    assert np.array_equal(got, ref), ys[got != ref][:5]
+
+
+def check_fp8_quantizer(lib):
+    # The largest element of each row reads back as +-448 steps of its scale
+    # and every element within half an E4M3 spacing of its value.
+    r = np.random.default_rng(74)
+    mags = np.exp(r.uniform(-6, 6, size=(300, 1)))
+    x = _bits((r.standard_normal((300, 64)) * mags).astype(np.float32))
+    xv = _f64(x)
+    codes, scales = oracle.quantize_fp8(x, lib=lib)
+    assert codes.dtype == np.uint8
+    back = oracle.dequantize_fp8(codes, scales, lib=lib)
+    amax = np.abs(xv).argmax(axis=1)
+    assert np.all((codes[np.arange(300), amax] & 0x7F) == 0x7E)
+    y = np.abs(xv) / scales[:, None]
+    spacing = np.where(y < 2.0 ** -6, 2.0 ** -9, 2.0 ** (np.floor(np.log2(np.maximum(y, 2.0 ** -6))) - 3))
+    assert np.all(np.abs(back - xv) <= scales[:, None] * spacing * (0.5 + 1e-3))
+    # int8 and fp8 paged caches gather back to their contiguous rows byte for byte
+    B, S, Hkv, D, P = 2, 8, 1, 64, 4
+    lens = np.array([8, 5], np.int32)
+    table = np.array([[3, 0], [1, 2]], np.int32)
+    cc, cs = codes[:B * S].reshape(B, S, Hkv, D), scales[:B * S].reshape(B, S, Hkv)
+    pool_c = np.zeros((4, P, Hkv, D), np.uint8)
+    pool_s = np.zeros((4, P, Hkv), np.float32)
+    for b in range(B):
+        for j in range(2):
+            pool_c[table[b, j]], pool_s[table[b, j]] = cc[b, j * P:(j + 1) * P], cs[b, j * P:(j + 1) * P]
+    gc, gs, _ = oracle.paged_gather_q8(pool_c, pool_s, table, lens, lib=lib, fmt="fp8")
+    for b in range(B):
+        assert np.array_equal(gc[b, :lens[b]], cc[b, :lens[b]]) and np.array_equal(gs[b, :lens[b]], cs[b, :lens[b]])
+
+
+def check_fp8_attention_close_to_bf16(lib):
+    # Attention over the fp8 rows of N(0, 1) caches stays near the bf16
+    # attention (E4M3 keeps 3 mantissa bits: about 3 % per element).
+    q, k, v, lens, scale = _random_case(75, 3, 8, 2, 32, 40, [40, 9, 1])
+    kc, ks = oracle.quantize_fp8(k, lib=lib)
+    vc, vs = oracle.quantize_fp8(v, lib=lib)
+    ref, _ = oracle.decode_attention(q, k, v, lens, scale, lib=lib)
+    got, _ = oracle.decode_attention_q8(q, kc, vc, ks, vs, lens, scale, lib=lib, fmt="fp8")
+    assert np.max(np.abs(got - ref)) < 0.1
+
+
 ALL_CHECKS = [
     check_identical_keys_give_mean_of_v,
     check_dominant_score_returns_that_row,
@@ -691,6 +773,11 @@ ALL_CHECKS = [
     check_unified_max_equals_definition,
     check_unified_max_closed_form,
     check_unified_max_window_edges,
+    check_e4m3_format_values,
+    check_e4m3_rounding,
+    check_e4m3_against_torch,
+    check_fp8_quantizer,
+    check_fp8_attention_close_to_bf16,
     check_multi_token_one_is_single,
     check_multi_token_against_torch_causal,
     check_multi_token_append,
