@@ -154,3 +154,25 @@ def test_multi_short_sequences_give_empty_rows(Hq, Hkv, D):
     l = lse.cpu().numpy()
     assert np.all(np.isneginf(l[0, :2])) and np.all(np.isneginf(l[2])) and np.all(got[0, :2] == 0)
     assert np.max(np.abs(l[np.isfinite(want_lse)] - want_lse[np.isfinite(want_lse)])) < 1e-4
+
+
+@pytest.mark.parametrize("Hq,Hkv,D", [(64, 1, 64), (16, 1, 64)], ids=["tcgen05_g64", "mma_g16"])
+def test_multi_token_maximum_sizes(Hq, Hkv, D):
+    """T = KVD_MAX_TOKENS (64) with the widest group of each engine: 64 virtual
+    sequences per sequence on the tcgen05 engine (group 64), 64 blocks of 16
+    rows per pair on the mma.sync engine (group 16)."""
+    dev = cuda_or_skip()
+    T = 64
+    w = workloads.Workload("maxT", 2, Hq, Hkv, D, 200, T, 200, 113)
+    mi = workloads.multi_step_inputs(w, T)
+    kc, vc, skipped = oracle.kv_append_multi(mi.k_cache, mi.v_cache, mi.k_new, mi.v_new, mi.pos)
+    assert skipped == 0
+    want, want_lse = oracle.decode_attention_multi(mi.q, kc, vc, mi.seq_lens, mi.workload.scale)
+    B = mi.q.shape[0]
+    for n_split in (0, 5):
+        o, l, gk, gv, status = _run(mi, dev, "f32", n_split)
+        assert status == 0
+        assert np.array_equal(gk, kc) and np.array_equal(gv, vc)
+        assert_close(o.astype(np.float64).reshape(B, T * Hq, D), want.reshape(B, T * Hq, D), "f32",
+                     f"max T n_split {n_split}")
+        assert np.max(np.abs(l - want_lse)) < 1e-4
