@@ -62,8 +62,8 @@ def parse_args():
                     help="paged KV cache with pages of this many tokens; 0 = contiguous")
     ap.add_argument("--tokens", type=int, default=1,
                     help="query tokens per sequence (T > 1: a speculative check step; up to 64)")
-    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "int8"],
-                    help="int8: the cache quantized per (token, KV head) row")
+    ap.add_argument("--kv-dtype", default="bf16", choices=["bf16", "int8", "fp8"],
+                    help="int8 / fp8 (E4M3): the cache quantized per (token, KV head) row")
     ap.add_argument("--softmax", default="online", choices=["online", "unified"],
                     help="unified: every split's partial softmax against one maximum phi (plain-sum merge)")
     ap.add_argument("--phi", type=float, default=0.0, help="the unified maximum, in logit units")
@@ -282,9 +282,10 @@ def run_ours(args):
     S, Hkv = inp.k_cache.shape[1], inp.k_cache.shape[2]
     lens_np = inp.seq_lens
     max_len = int(w.S_max)
-    int8 = args.kv_dtype == "int8"
+    int8 = args.kv_dtype in ("int8", "fp8")  # an 8-bit cache: codes and row scales
+    fp8 = args.kv_dtype == "fp8"
     if int8 and args.page_size:
-        raise SystemExit("--kv-dtype int8 takes a contiguous cache")
+        raise SystemExit("--kv-dtype int8/fp8 takes a contiguous cache")
     step_bytes = (roofline.attention_step_bytes_q8(lens_np, Hq, Hkv, D) if int8
                   else roofline.attention_step_bytes(lens_np, Hq, Hkv, D))
     kv_bytes = roofline.attention_kv_bytes(lens_np, Hkv, D) // (2 if int8 else 1)
@@ -318,14 +319,15 @@ def run_ours(args):
         kcs.append(kc0.clone())
         vcs.append(vc0.clone())
     if int8:
-        # int8 copies quantized on the GPU from the bf16 cache (its cached rows)
+        # 8-bit copies quantized on the GPU from the bf16 cache (its cached rows)
         cached = torch.from_numpy(np.maximum(lens_np - 1, 0).astype(np.int32)).to(dev)
         q8 = []
+        quantize = kvd.kv_quantize_fp8 if fp8 else kvd.kv_quantize_q8
         for kc_, vc_ in zip(kcs, vcs):
-            codes = [torch.zeros(kc_.shape, dtype=torch.int8, device=dev) for _ in range(2)]
+            codes = [torch.zeros(kc_.shape, dtype=torch.uint8 if fp8 else torch.int8, device=dev) for _ in range(2)]
             scales = [torch.zeros(kc_.shape[:3], dtype=torch.float32, device=dev) for _ in range(2)]
-            kvd.kv_quantize_q8(kc_, codes[0], scales[0], cached, S)
-            kvd.kv_quantize_q8(vc_, codes[1], scales[1], cached, S)
+            quantize(kc_, codes[0], scales[0], cached, S)
+            quantize(vc_, codes[1], scales[1], cached, S)
             q8.append((codes[0], codes[1], scales[0], scales[1]))
         del kcs[1:], vcs[1:]
         torch.cuda.synchronize()
@@ -346,6 +348,10 @@ def run_ours(args):
         if multi:
             kvd.decode_step_multi(q, kcs[r], vcs[r], kn, vn, pos, lens, max_len, w.scale, out, workspace=ws,
                                   n_split=args.n_split, stream=stream)
+        elif fp8:
+            kq, vq, ks, vs = q8[r]
+            kvd.decode_ex(q, kq, vq, lens, max_len, w.scale, out, k_scales=ks, v_scales=vs, k_new=kn, v_new=vn,
+                          pos=pos, workspace=ws, n_split=args.n_split, stream=stream)
         elif int8:
             kq, vq, ks, vs = q8[r]
             kvd.decode_step_q8(q, kq, vq, ks, vs, kn, vn, pos, lens, max_len, w.scale, out, workspace=ws,
@@ -419,10 +425,10 @@ def run_ours(args):
         if int8:
             # no separate int8 chunk entry point: the whole attention call is timed
             kq, vq, ks, vs = q8[r]
-            kvd.kv_append_q8(kq, vq, ks, vs, kn, vn, pos)
+            (kvd.kv_append_fp8 if fp8 else kvd.kv_append_q8)(kq, vq, ks, vs, kn, vn, pos)
             ea[i].record(stream)
-            kvd.decode_attention_q8(q, kq, vq, ks, vs, lens, max_len, w.scale, out, workspace=ws,
-                                    n_split=args.n_split)
+            kvd.decode_ex(q, kq, vq, lens, max_len, w.scale, out, k_scales=ks, v_scales=vs, workspace=ws,
+                          n_split=args.n_split)
             eb[i].record(stream)
             continue
         if paged:
@@ -543,7 +549,7 @@ def run_ours(args):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": ("split_kv_chunk + split_kv_merge (multi-token)" if multi else
-                                "split_kv_chunk + split_kv_merge (int8)" if int8 else
+                                f"split_kv_chunk + split_kv_merge ({args.kv_dtype})" if int8 else
                                 "split_kv_chunk + split_kv_merge (paged)" if paged else "split_kv_chunk"),
                      "peak_source": f"{peak_kind} copy bandwidth",
                      "kernel_ms": round(chunk_avg_ms, 5)},

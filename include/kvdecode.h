@@ -295,6 +295,33 @@ kvd_status kvd_kv_append_q8_paged(void* k_code_pages, void* v_code_pages, float*
                                   const int32_t* block_table, const int32_t* pos, int batch, int max_blocks,
                                   int page_size, int num_pages, int n_heads_kv, int head_dim,
                                   int32_t* status_word, kvd_stream_t stream);
+
+/*
+ * fp8 KV cache: the int8 scheme above with the OCP 8-bit floating-point
+ * format E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ * subnormals, largest finite 448, no infinities) in place of int8, the other
+ * 8-bit format the same page names:
+ *   a = max_d |x_d|, scale = a / 448, code_d = x_d / scale rounded to the
+ *   nearest E4M3 value (ties to the even code, magnitudes past 448 saturate to
+ *   448), a result of zero stored as +0 (0x00); both divisions IEEE float32
+ *   (a = 0: scale 0 and codes 0); the row reads back as scale * value(code_d).
+ * Codes are bytes (uint8, bit-compatible with a float8 e4m3 "fn" tensor);
+ * layouts, alignment, row selection, status and errors exactly as the int8
+ * calls. Attention over an fp8 cache goes through kvd_decode_ex with
+ * kvd_cache.fp8 = 1 (contiguous or paged, any supported group, T query
+ * tokens, with or without the append); the kernels convert the codes to f16
+ * exactly and compute as for int8.
+ */
+kvd_status kvd_kv_quantize_fp8(const void* cache, void* codes, float* scales, const int32_t* seq_lens, int batch,
+                               int s_max, int max_seq_len, int n_heads_kv, int head_dim, kvd_stream_t stream);
+kvd_status kvd_kv_append_fp8(void* k_codes, void* v_codes, float* k_scales, float* v_scales, const void* k_new,
+                             const void* v_new, const int32_t* pos, int batch, int s_max, int n_heads_kv,
+                             int head_dim, int32_t* status_word, kvd_stream_t stream);
+kvd_status kvd_kv_append_fp8_paged(void* k_code_pages, void* v_code_pages, float* k_scale_pages,
+                                   float* v_scale_pages, const void* k_new, const void* v_new,
+                                   const int32_t* block_table, const int32_t* pos, int batch, int max_blocks,
+                                   int page_size, int num_pages, int n_heads_kv, int head_dim,
+                                   int32_t* status_word, kvd_stream_t stream);
 kvd_status kvd_decode_attention_q8(const void* q, const void* k_codes, const void* v_codes, const float* k_scales,
                                    const float* v_scales, const int32_t* seq_lens, int batch, int s_max,
                                    int max_seq_len, int n_heads_q, int n_heads_kv, int head_dim, float scale,
@@ -352,7 +379,8 @@ kvd_status kvd_decode_step_multi(void* k_cache, void* v_cache, const void* k_new
  * kvd_decode_ex: one entry point for every combination of the cache forms and
  * options above that the kernels support, with the cache described by a
  * struct:
- *   - bf16 or int8 (k_scales and v_scales non-NULL: k and v hold int8 codes);
+ *   - bf16, int8 (k_scales and v_scales non-NULL: k and v hold int8 codes) or
+ *     fp8 (the scales and fp8 = 1: k and v hold E4M3 codes);
  *   - contiguous (block_table NULL: k, v [batch, s_max, Hkv, D]) or paged
  *     (k, v are page pools, and for int8 k_scales, v_scales too);
  *   - n_tokens query tokens per sequence (layouts as kvd_decode_attention_multi;
@@ -363,8 +391,8 @@ kvd_status kvd_decode_step_multi(void* k_cache, void* v_cache, const void* k_new
  *     NULL).
  * Each combination is bit-identical to the dedicated call where one exists.
  * Errors: KVD_ERR_INVALID_ARG for a NULL cache, a cache description that fails
- * the dedicated calls' checks, or only some of k_new, v_new, pos given; the
- * rest as the dedicated calls.
+ * the dedicated calls' checks (fp8 set without scales included), or only some
+ * of k_new, v_new, pos given; the rest as the dedicated calls.
  */
 typedef struct kvd_cache {
     void* k;                       /* bf16 cache or page pool, or int8 codes */
@@ -374,6 +402,7 @@ typedef struct kvd_cache {
     const int32_t* block_table;    /* paged: int32 [batch, max_blocks]; NULL for contiguous */
     int s_max;                     /* contiguous: capacity of each sequence */
     int max_blocks, page_size, num_pages;  /* paged */
+    int fp8;                       /* with the scales: 1 = k, v hold fp8 E4M3 codes, 0 = int8 codes */
 } kvd_cache;
 
 kvd_status kvd_decode_ex(const kvd_cache* cache, const void* q, const int32_t* seq_lens, int batch, int n_tokens,

@@ -35,6 +35,7 @@ EXPORTED = (
     "kvd_decode_attention_q8", "kvd_decode_step_q8", "kvd_decode_plan_multi", "kvd_kv_append_multi",
     "kvd_decode_attention_multi", "kvd_decode_step_multi", "kvd_decode_ex", "kvd_kv_append_q8_paged",
     "kvd_decode_attention_umax", "kvd_decode_step_umax", "kvd_step_staging_bytes", "kvd_decode_step_host",
+    "kvd_kv_quantize_fp8", "kvd_kv_append_fp8", "kvd_kv_append_fp8_paged",
 )
 STATIC_WORKSPACE_BYTES = 16 << 20  # KVD_STATIC_WORKSPACE_BYTES
 
@@ -69,7 +70,8 @@ class _CCache(ctypes.Structure):
     """struct kvd_cache of kvdecode.h."""
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("k_scales", ctypes.c_void_p),
                 ("v_scales", ctypes.c_void_p), ("block_table", ctypes.c_void_p), ("s_max", ctypes.c_int),
-                ("max_blocks", ctypes.c_int), ("page_size", ctypes.c_int), ("num_pages", ctypes.c_int)]
+                ("max_blocks", ctypes.c_int), ("page_size", ctypes.c_int), ("num_pages", ctypes.c_int),
+                ("fp8", ctypes.c_int)]
 
 
 def _declare(lib):
@@ -99,6 +101,12 @@ def _declare(lib):
     lib.kvd_kv_append_q8.argtypes = [P, P, P, P, P, P, P, I, I, I, I, P, P]
     lib.kvd_kv_append_q8.restype = I
     lib.kvd_kv_append_q8_paged.argtypes = [P, P, P, P, P, P, P, P, I, I, I, I, I, I, P, P]
+    lib.kvd_kv_quantize_fp8.argtypes = lib.kvd_kv_quantize_q8.argtypes
+    lib.kvd_kv_quantize_fp8.restype = I
+    lib.kvd_kv_append_fp8.argtypes = lib.kvd_kv_append_q8.argtypes
+    lib.kvd_kv_append_fp8.restype = I
+    lib.kvd_kv_append_fp8_paged.argtypes = lib.kvd_kv_append_q8_paged.argtypes
+    lib.kvd_kv_append_fp8_paged.restype = I
     lib.kvd_kv_append_q8_paged.restype = I
     # unified maximum: decode_attention / decode_step with phi after scale
     lib.kvd_decode_attention_umax.argtypes = dec[:11] + [F] + dec[11:]
@@ -239,7 +247,7 @@ def _require(t, name, dtype=None, ndim=None):
         raise ValueError(f"{name} must be on a CUDA device")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
-    if dtype is not None and t.dtype != dtype:
+    if dtype is not None and t.dtype not in (dtype if isinstance(dtype, tuple) else (dtype,)):
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if ndim is not None and t.dim() != ndim:
         raise ValueError(f"{name} must have {ndim} dims, got {t.dim()}")
@@ -406,52 +414,86 @@ def decode_step_paged(q, k_pages, v_pages, k_new, v_new, pos, block_table, seq_l
            "kvd_decode_step_paged")
 
 
-def _q8_args(k_codes, v_codes, k_scales, v_scales):
+def _code_dtypes(fmt):
+    """Tensor dtypes an 8-bit cache's codes may have: int8, or for fp8 E4M3
+    bytes (uint8) or torch's float8_e4m3fn (the same bits)."""
     import torch
-    _require(k_codes, "k_codes", torch.int8, 4)
-    _require(v_codes, "v_codes", torch.int8, 4)
+    if fmt == "int8":
+        return (torch.int8,)
+    if fmt == "fp8":
+        return (torch.uint8, torch.float8_e4m3fn)
+    raise ValueError(f"unknown 8-bit cache format {fmt!r}")
+
+
+def _is_fp8(codes) -> bool:
+    import torch
+    return codes.dtype in (torch.uint8, torch.float8_e4m3fn)
+
+
+def _q8_args(k_codes, v_codes, k_scales, v_scales, fmt="int8"):
+    import torch
+    _require(k_codes, "k_codes", _code_dtypes(fmt), 4)
+    _require(v_codes, "v_codes", _code_dtypes(fmt), 4)
     _require(k_scales, "k_scales", torch.float32, 3)
     _require(v_scales, "v_scales", torch.float32, 3)
     if v_codes.shape != k_codes.shape or k_scales.shape != k_codes.shape[:3] or v_scales.shape != k_scales.shape:
-        raise ValueError("int8 cache: codes [B, S_max, Hkv, D] and scales [B, S_max, Hkv] disagree")
+        raise ValueError(f"{fmt} cache: codes [B, S_max, Hkv, D] and scales [B, S_max, Hkv] disagree")
 
 
-def kv_quantize_q8(cache, codes, scales, seq_lens, max_seq_len: int, stream=None):
-    """codes/scales of rows t < seq_lens[b] of a bf16 cache [B, S_max, Hkv, D]."""
+def _quantize8(cache, codes, scales, seq_lens, max_seq_len, stream, fmt):
     import torch
     _require(cache, "cache", torch.bfloat16, 4)
-    _require(codes, "codes", torch.int8, 4)
+    _require(codes, "codes", _code_dtypes(fmt), 4)
     _require(scales, "scales", torch.float32, 3)
     _require(seq_lens, "seq_lens", torch.int32, 1)
     B, S, Hkv, D = cache.shape
     if codes.shape != cache.shape or scales.shape != (B, S, Hkv) or seq_lens.shape != (B,):
-        raise ValueError("kv_quantize_q8: inconsistent shapes")
-    _check(load().kvd_kv_quantize_q8(cache.data_ptr(), codes.data_ptr(), scales.data_ptr(), seq_lens.data_ptr(),
-                                     B, S, int(max_seq_len), Hkv, D, _stream_handle(stream)), "kvd_kv_quantize_q8")
+        raise ValueError(f"kv_quantize_{fmt}: inconsistent shapes")
+    name = "kvd_kv_quantize_q8" if fmt == "int8" else "kvd_kv_quantize_fp8"
+    _check(getattr(load(), name)(cache.data_ptr(), codes.data_ptr(), scales.data_ptr(), seq_lens.data_ptr(), B, S,
+                                 int(max_seq_len), Hkv, D, _stream_handle(stream)), name)
 
 
-def kv_append_q8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, status=None, stream=None):
-    """The new bf16 rows quantized and written at pos[b] of the int8 cache."""
+def kv_quantize_q8(cache, codes, scales, seq_lens, max_seq_len: int, stream=None):
+    """int8 codes/scales of rows t < seq_lens[b] of a bf16 cache [B, S_max, Hkv, D]."""
+    _quantize8(cache, codes, scales, seq_lens, max_seq_len, stream, "int8")
+
+
+def kv_quantize_fp8(cache, codes, scales, seq_lens, max_seq_len: int, stream=None):
+    """fp8 E4M3 codes (uint8 or float8_e4m3fn) and scales of rows t < seq_lens[b]
+    of a bf16 cache [B, S_max, Hkv, D] (kvd_kv_quantize_fp8)."""
+    _quantize8(cache, codes, scales, seq_lens, max_seq_len, stream, "fp8")
+
+
+def _append8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, status, stream, fmt):
     import torch
-    _q8_args(k_codes, v_codes, k_scales, v_scales)
+    _q8_args(k_codes, v_codes, k_scales, v_scales, fmt)
     for t, n in ((k_new, "k_new"), (v_new, "v_new")):
         _require(t, n, torch.bfloat16, 3)
     _require(pos, "pos", torch.int32, 1)
     B, S, Hkv, D = k_codes.shape
     if k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or pos.shape != (B,):
-        raise ValueError("kv_append_q8: inconsistent shapes")
-    _check(load().kvd_kv_append_q8(k_codes.data_ptr(), v_codes.data_ptr(), k_scales.data_ptr(),
-                                   v_scales.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), pos.data_ptr(), B, S,
-                                   Hkv, D, _ptr(status), _stream_handle(stream)), "kvd_kv_append_q8")
+        raise ValueError(f"kv_append_{fmt}: inconsistent shapes")
+    name = "kvd_kv_append_q8" if fmt == "int8" else "kvd_kv_append_fp8"
+    _check(getattr(load(), name)(k_codes.data_ptr(), v_codes.data_ptr(), k_scales.data_ptr(), v_scales.data_ptr(),
+                                 k_new.data_ptr(), v_new.data_ptr(), pos.data_ptr(), B, S, Hkv, D, _ptr(status),
+                                 _stream_handle(stream)), name)
 
 
-def kv_append_q8_paged(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages, k_new, v_new, block_table, pos,
-                       status=None, stream=None):
-    """The new bf16 rows quantized and written, as kv_append_paged places them,
-    into int8 page pools: codes [num_pages, page, Hkv, D], scales
-    [num_pages, page, Hkv]."""
+def kv_append_q8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, status=None, stream=None):
+    """The new bf16 rows quantized and written at pos[b] of the int8 cache."""
+    _append8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, status, stream, "int8")
+
+
+def kv_append_fp8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, status=None, stream=None):
+    """The new bf16 rows quantized to fp8 E4M3 and written at pos[b] (kvd_kv_append_fp8)."""
+    _append8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, status, stream, "fp8")
+
+
+def _append8_paged(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages, k_new, v_new, block_table, pos,
+                   status, stream, fmt):
     import torch
-    _q8_args(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages)
+    _q8_args(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages, fmt)
     for t, n in ((k_new, "k_new"), (v_new, "v_new")):
         _require(t, n, torch.bfloat16, 3)
     _require(pos, "pos", torch.int32, 1)
@@ -460,12 +502,28 @@ def kv_append_q8_paged(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages,
     B = k_new.shape[0]
     if (k_new.shape != (B, Hkv, D) or v_new.shape != (B, Hkv, D) or pos.shape != (B,)
             or block_table.shape[0] != B):
-        raise ValueError("kv_append_q8_paged: inconsistent shapes")
-    _check(load().kvd_kv_append_q8_paged(k_code_pages.data_ptr(), v_code_pages.data_ptr(), k_scale_pages.data_ptr(),
-                                         v_scale_pages.data_ptr(), k_new.data_ptr(), v_new.data_ptr(),
-                                         block_table.data_ptr(), pos.data_ptr(), B, block_table.shape[1], page,
-                                         num_pages, Hkv, D, _ptr(status), _stream_handle(stream)),
-           "kvd_kv_append_q8_paged")
+        raise ValueError(f"kv_append_{fmt}_paged: inconsistent shapes")
+    name = "kvd_kv_append_q8_paged" if fmt == "int8" else "kvd_kv_append_fp8_paged"
+    _check(getattr(load(), name)(k_code_pages.data_ptr(), v_code_pages.data_ptr(), k_scale_pages.data_ptr(),
+                                 v_scale_pages.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), block_table.data_ptr(),
+                                 pos.data_ptr(), B, block_table.shape[1], page, num_pages, Hkv, D, _ptr(status),
+                                 _stream_handle(stream)), name)
+
+
+def kv_append_q8_paged(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages, k_new, v_new, block_table, pos,
+                       status=None, stream=None):
+    """The new bf16 rows quantized and written, as kv_append_paged places them,
+    into int8 page pools: codes [num_pages, page, Hkv, D], scales
+    [num_pages, page, Hkv]."""
+    _append8_paged(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages, k_new, v_new, block_table, pos,
+                   status, stream, "int8")
+
+
+def kv_append_fp8_paged(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages, k_new, v_new, block_table, pos,
+                        status=None, stream=None):
+    """kv_append_q8_paged for fp8 E4M3 page pools (kvd_kv_append_fp8_paged)."""
+    _append8_paged(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages, k_new, v_new, block_table, pos,
+                   status, stream, "fp8")
 
 
 def _decode_q8_args(q, k_codes, v_codes, k_scales, v_scales, seq_lens, max_seq_len, scale, n_split, workspace,
@@ -601,9 +659,10 @@ def decode_ex(q, k, v, seq_lens, max_seq_len: int, scale: float, out, *, k_scale
               block_table=None, k_new=None, v_new=None, pos=None, workspace=None, n_split: int = 0, lse=None,
               status=None, stream=None):
     """Any supported combination in one call (kvd_decode_ex): q [B, Hq, D] or
-    [B, T, Hq, D]; k, v a contiguous cache [B, S_max, Hkv, D] (bf16, or int8 codes
-    with k_scales/v_scales [B, S_max, Hkv]) or, with block_table [B, max_blocks],
-    page pools [num_pages, page, Hkv, D] (bf16, or int8 codes with scale pools
+    [B, T, Hq, D]; k, v a contiguous cache [B, S_max, Hkv, D] (bf16, or 8-bit
+    codes with k_scales/v_scales [B, S_max, Hkv]: int8 codes, or fp8 E4M3 codes
+    as uint8 or float8_e4m3fn) or, with block_table [B, max_blocks], page pools
+    [num_pages, page, Hkv, D] (bf16, or 8-bit codes with scale pools
     [num_pages, page, Hkv]); k_new, v_new ([B, Hkv, D] or [B, T, Hkv, D]) and pos
     to append first. Workspace: decode_plan_multi."""
     import torch
@@ -613,6 +672,7 @@ def decode_ex(q, k, v, seq_lens, max_seq_len: int, scale: float, out, *, k_scale
     c = _CCache()
     c.k, c.v = k.data_ptr(), v.data_ptr()
     c.k_scales, c.v_scales = _ptr(k_scales), _ptr(v_scales)
+    c.fp8 = 1 if (k_scales is not None and _is_fp8(k)) else 0
     if block_table is not None:
         _require(block_table, "block_table", torch.int32, 2)
         c.block_table, c.max_blocks, c.page_size, c.num_pages = (block_table.data_ptr(), block_table.shape[1],

@@ -10,15 +10,15 @@
 
 namespace kvd {
 
-const ChunkKernel* mma_table_d64(bool f32, bool paged, bool kv8);
-const ChunkKernel* mma_table_d128(bool f32, bool paged, bool kv8);
-const ChunkKernel* mma_table_d256(bool f32, bool paged, bool kv8);
+const ChunkKernel* mma_table_d64(bool f32, bool paged, bool kv8, bool fp8);
+const ChunkKernel* mma_table_d128(bool f32, bool paged, bool kv8, bool fp8);
+const ChunkKernel* mma_table_d256(bool f32, bool paged, bool kv8, bool fp8);
 
-const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool kv8) {
+const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool kv8, bool fp8) {
     switch (head_dim) {
-        case 64: return mma_table_d64(f32_out, paged, kv8);
-        case 128: return mma_table_d128(f32_out, paged, kv8);
-        case 256: return mma_table_d256(f32_out, paged, kv8);
+        case 64: return mma_table_d64(f32_out, paged, kv8, fp8);
+        case 128: return mma_table_d128(f32_out, paged, kv8, fp8);
+        case 256: return mma_table_d256(f32_out, paged, kv8, fp8);
         default: return nullptr;
     }
 }
@@ -27,10 +27,10 @@ const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool
 // differ); the mma.sync kernel has a compiled variant per form. int8 caches
 // (contiguous or paged) run on the mma.sync kernel, whose CTAs take 16 of a
 // pair's rows each, for every group.
-const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8) {
+const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8, bool fp8) {
     if (group < 1 || group > KVD_MAX_GROUP) return nullptr;
-    if (kv8) return mma_chunk_kernel(head_dim, f32_out, paged, true);
-    if (group <= 16) return mma_chunk_kernel(head_dim, f32_out, paged, false);
+    if (kv8) return mma_chunk_kernel(head_dim, f32_out, paged, true, fp8);
+    if (group <= 16) return mma_chunk_kernel(head_dim, f32_out, paged, false, false);
     return tc_chunk_kernel(head_dim, f32_out, group);
 }
 
@@ -58,14 +58,16 @@ kvd_status check_shape(int batch, int Hq, int Hkv, int D, kvd_out_dtype dt) {
 // planning and the host replica use the contiguous one. The split count is
 // planned for the single-token bf16 kernel of the shape whatever the cache
 // dtype and query tokens, so that one plan sizes every form's workspace.
-const ChunkKernel* pick_kernel(int Hq, int Hkv, int D, kvd_out_dtype dt, bool paged = false, bool kv8 = false) {
-    return find_chunk_kernel(D, Hq / Hkv, dt == KVD_OUT_F32, paged, kv8);
+const ChunkKernel* pick_kernel(int Hq, int Hkv, int D, kvd_out_dtype dt, bool paged = false, bool kv8 = false,
+                               bool fp8 = false) {
+    return find_chunk_kernel(D, Hq / Hkv, dt == KVD_OUT_F32, paged, kv8, fp8);
 }
 
 // int8 cache: the row scales of K and V.
 struct QuantCache {
     float* k_scale;
     float* v_scale;
+    bool fp8 = false;  // E4M3 codes rather than int8
 };
 
 // Paged cache arguments, checked; s_max of the contiguous calls becomes
@@ -191,7 +193,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     if (st != KVD_OK) return st;
     if (q8 && (!q8->k_scale || !q8->v_scale || !aligned(q8->k_scale, 4) || !aligned(q8->v_scale, 4)))
         return KVD_ERR_INVALID_ARG;
-    k = pick_kernel(Hq, Hkv, D, dt, pg != nullptr, q8 != nullptr);
+    k = pick_kernel(Hq, Hkv, D, dt, pg != nullptr, q8 != nullptr, q8 && q8->fp8);
     if (!k) return KVD_ERR_UNSUPPORTED;
     // The tensor-core path addresses cache rows and query rows with 32-bit TMA coordinates.
     if (k->tensor_core && (cache_rows > 0x7fffffffLL || (long long)batch * T * Hq > 0x7fffffffLL))
@@ -236,6 +238,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     if (q8) {
         p.k_scale = q8->k_scale;
         p.v_scale = q8->v_scale;
+        p.kv_fp8 = q8->fp8 ? 1 : 0;
     }
     if (pg) {
         p.block_table = pg->block_table;
@@ -261,7 +264,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
         const PagedCache none{nullptr, 0, 0, 0};
         const cudaError_t e =
             q8 ? launch_append_q8(app->k_cache, app->v_cache, q8->k_scale, q8->v_scale, app->k_new, app->v_new,
-                                  app->pos, batch, s_max, Hkv, D, status, pg ? *pg : none, s, T)
+                                  app->pos, batch, s_max, Hkv, D, status, pg ? *pg : none, s, T, q8->fp8)
                : launch_append(app->k_cache, app->v_cache, app->k_new, app->v_new, app->pos, batch, s_max, Hkv,
                                D, status, pg ? *pg : none, s, T);
         if (e != cudaSuccess) return KVD_ERR_CUDA;
@@ -453,8 +456,9 @@ kvd_status kvd_decode_ex(const kvd_cache* cache, const void* q, const int32_t* s
                                           cache->num_pages, &pg, &s_max);
         if (st != KVD_OK) return st;
     }
-    const QuantCache q8{cache->k_scales, cache->v_scales};
-    const bool int8 = cache->k_scales != nullptr;
+    if (cache->fp8 && !cache->k_scales) return KVD_ERR_INVALID_ARG;  // fp8 codes need their scales
+    const QuantCache q8{cache->k_scales, cache->v_scales, cache->fp8 != 0};
+    const bool quant = cache->k_scales != nullptr;
     AppendArgs app{cache->k, cache->v, k_new, v_new, pos};
     if (append) {
         const kvd_status st = check_append(cache->k, cache->v, k_new, v_new, pos, batch, s_max, n_heads_kv,
@@ -463,11 +467,12 @@ kvd_status kvd_decode_ex(const kvd_cache* cache, const void* q, const int32_t* s
     }
     return decode(kBoth, q, cache->k, cache->v, seq_lens, batch, s_max, max_seq_len, n_heads_q, n_heads_kv,
                   head_dim, scale, n_split, workspace, workspace_bytes, out, out_dtype, lse_out, status_word,
-                  stream, append ? &app : nullptr, paged ? &pg : nullptr, int8 ? &q8 : nullptr, n_tokens);
+                  stream, append ? &app : nullptr, paged ? &pg : nullptr, quant ? &q8 : nullptr, n_tokens);
 }
 
-kvd_status kvd_kv_quantize_q8(const void* cache, void* codes, float* scales, const int32_t* seq_lens, int batch,
-                              int s_max, int max_seq_len, int n_heads_kv, int head_dim, kvd_stream_t stream) {
+// The 8-bit quantizer and appends (int8, or fp8 E4M3 when fp8 is set).
+static kvd_status quantize8(const void* cache, void* codes, float* scales, const int32_t* seq_lens, int batch,
+                            int s_max, int max_seq_len, int n_heads_kv, int head_dim, kvd_stream_t stream, bool fp8) {
     if (batch < 0 || s_max <= 0 || max_seq_len < 0 || max_seq_len > s_max || n_heads_kv <= 0) return KVD_ERR_INVALID_ARG;
     if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVD_ERR_UNSUPPORTED;
     if (!cache || !codes || !scales || !seq_lens || !aligned(cache, 16) || !aligned(codes, 16) ||
@@ -475,25 +480,60 @@ kvd_status kvd_kv_quantize_q8(const void* cache, void* codes, float* scales, con
         return KVD_ERR_INVALID_ARG;
     if (batch == 0) return KVD_OK;
     return launch_quantize_q8(cache, codes, scales, seq_lens, batch, s_max, max_seq_len, n_heads_kv, head_dim,
-                              static_cast<cudaStream_t>(stream)) == cudaSuccess
+                              static_cast<cudaStream_t>(stream), fp8) == cudaSuccess
                ? KVD_OK
                : KVD_ERR_CUDA;
 }
 
-kvd_status kvd_kv_append_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales, const void* k_new,
-                            const void* v_new, const int32_t* pos, int batch, int s_max, int n_heads_kv,
-                            int head_dim, int32_t* status_word, kvd_stream_t stream) {
+static kvd_status append8(void* k_codes, void* v_codes, float* k_scales, float* v_scales, const void* k_new,
+                          const void* v_new, const int32_t* pos, int batch, int s_max, int n_heads_kv, int head_dim,
+                          int32_t* status_word, kvd_stream_t stream, const PagedCache& pg, bool fp8) {
     kvd_status st = check_append(k_codes, v_codes, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim,
                                  status_word);
     if (st != KVD_OK) return st;
     if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVD_ERR_UNSUPPORTED;
     if (!k_scales || !v_scales || !aligned(k_scales, 4) || !aligned(v_scales, 4)) return KVD_ERR_INVALID_ARG;
     if (batch == 0) return KVD_OK;
-    const PagedCache none{nullptr, 0, 0, 0};
     return launch_append_q8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, batch, s_max, n_heads_kv,
-                            head_dim, status_word, none, static_cast<cudaStream_t>(stream)) == cudaSuccess
+                            head_dim, status_word, pg, static_cast<cudaStream_t>(stream), 1, fp8) == cudaSuccess
                ? KVD_OK
                : KVD_ERR_CUDA;
+}
+
+static kvd_status append8_paged(void* k_code_pages, void* v_code_pages, float* k_scale_pages, float* v_scale_pages,
+                                const void* k_new, const void* v_new, const int32_t* block_table, const int32_t* pos,
+                                int batch, int max_blocks, int page_size, int num_pages, int n_heads_kv,
+                                int head_dim, int32_t* status_word, kvd_stream_t stream, bool fp8) {
+    PagedCache pg;
+    int s_max = 0;
+    const kvd_status st = check_paged(block_table, max_blocks, page_size, num_pages, &pg, &s_max);
+    if (st != KVD_OK) return st;
+    return append8(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages, k_new, v_new, pos, batch, s_max,
+                   n_heads_kv, head_dim, status_word, stream, pg, fp8);
+}
+
+kvd_status kvd_kv_quantize_q8(const void* cache, void* codes, float* scales, const int32_t* seq_lens, int batch,
+                              int s_max, int max_seq_len, int n_heads_kv, int head_dim, kvd_stream_t stream) {
+    return quantize8(cache, codes, scales, seq_lens, batch, s_max, max_seq_len, n_heads_kv, head_dim, stream, false);
+}
+
+kvd_status kvd_kv_quantize_fp8(const void* cache, void* codes, float* scales, const int32_t* seq_lens, int batch,
+                               int s_max, int max_seq_len, int n_heads_kv, int head_dim, kvd_stream_t stream) {
+    return quantize8(cache, codes, scales, seq_lens, batch, s_max, max_seq_len, n_heads_kv, head_dim, stream, true);
+}
+
+kvd_status kvd_kv_append_q8(void* k_codes, void* v_codes, float* k_scales, float* v_scales, const void* k_new,
+                            const void* v_new, const int32_t* pos, int batch, int s_max, int n_heads_kv,
+                            int head_dim, int32_t* status_word, kvd_stream_t stream) {
+    return append8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim,
+                   status_word, stream, PagedCache{nullptr, 0, 0, 0}, false);
+}
+
+kvd_status kvd_kv_append_fp8(void* k_codes, void* v_codes, float* k_scales, float* v_scales, const void* k_new,
+                             const void* v_new, const int32_t* pos, int batch, int s_max, int n_heads_kv,
+                             int head_dim, int32_t* status_word, kvd_stream_t stream) {
+    return append8(k_codes, v_codes, k_scales, v_scales, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim,
+                   status_word, stream, PagedCache{nullptr, 0, 0, 0}, true);
 }
 
 kvd_status kvd_kv_append_q8_paged(void* k_code_pages, void* v_code_pages, float* k_scale_pages,
@@ -501,22 +541,17 @@ kvd_status kvd_kv_append_q8_paged(void* k_code_pages, void* v_code_pages, float*
                                   const int32_t* block_table, const int32_t* pos, int batch, int max_blocks,
                                   int page_size, int num_pages, int n_heads_kv, int head_dim,
                                   int32_t* status_word, kvd_stream_t stream) {
-    PagedCache pg;
-    int s_max = 0;
-    kvd_status st = check_paged(block_table, max_blocks, page_size, num_pages, &pg, &s_max);
-    if (st != KVD_OK) return st;
-    st = check_append(k_code_pages, v_code_pages, k_new, v_new, pos, batch, s_max, n_heads_kv, head_dim,
-                      status_word);
-    if (st != KVD_OK) return st;
-    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVD_ERR_UNSUPPORTED;
-    if (!k_scale_pages || !v_scale_pages || !aligned(k_scale_pages, 4) || !aligned(v_scale_pages, 4))
-        return KVD_ERR_INVALID_ARG;
-    if (batch == 0) return KVD_OK;
-    return launch_append_q8(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages, k_new, v_new, pos, batch,
-                            s_max, n_heads_kv, head_dim, status_word, pg, static_cast<cudaStream_t>(stream)) ==
-                   cudaSuccess
-               ? KVD_OK
-               : KVD_ERR_CUDA;
+    return append8_paged(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages, k_new, v_new, block_table, pos,
+                         batch, max_blocks, page_size, num_pages, n_heads_kv, head_dim, status_word, stream, false);
+}
+
+kvd_status kvd_kv_append_fp8_paged(void* k_code_pages, void* v_code_pages, float* k_scale_pages,
+                                   float* v_scale_pages, const void* k_new, const void* v_new,
+                                   const int32_t* block_table, const int32_t* pos, int batch, int max_blocks,
+                                   int page_size, int num_pages, int n_heads_kv, int head_dim,
+                                   int32_t* status_word, kvd_stream_t stream) {
+    return append8_paged(k_code_pages, v_code_pages, k_scale_pages, v_scale_pages, k_new, v_new, block_table, pos,
+                         batch, max_blocks, page_size, num_pages, n_heads_kv, head_dim, status_word, stream, true);
 }
 
 kvd_status kvd_decode_attention_q8(const void* q, const void* k_codes, const void* v_codes, const float* k_scales,

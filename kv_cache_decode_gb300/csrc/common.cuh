@@ -3,6 +3,7 @@
 
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <stdint.h>
 
 namespace kvd {
@@ -111,6 +112,20 @@ __device__ __forceinline__ void i8x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32
     __half2 hb = __hsub2(*reinterpret_cast<__half2*>(&b), bias);
     lo = *reinterpret_cast<uint32_t*>(&ha);
     hi = *reinterpret_cast<uint32_t*>(&hb);
+}
+// Four fp8 E4M3 codes (byte i = column i) as two f16x2 values equal to the
+// codes' values divided by 256, exactly. E4M3 (sign, 4 exponent bits with bias
+// 7, 3 mantissa bits) and f16 (bias 15) differ by 8 in the exponent bias, so
+// placing a code's exponent and mantissa bits at the top of an f16's exponent
+// and mantissa fields (and its sign on the sign bit) reads as value * 2^-8,
+// subnormals included. Each byte goes to bits 15..8 of a 16-bit lane (byte
+// permute), the exponent and mantissa bits move down by one, the sign stays.
+__device__ __forceinline__ void e4m3x4_to_f16x2x2_div256(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    uint32_t a, b;
+    asm("prmt.b32 %0, %1, 0, 0x1404;" : "=r"(a) : "r"(w));  // byte 0 -> bits 15..8, byte 1 -> bits 31..24
+    asm("prmt.b32 %0, %1, 0, 0x3424;" : "=r"(b) : "r"(w));  // bytes 2, 3 likewise
+    lo = (a & 0x80008000u) | ((a >> 1) & 0x3f803f80u);
+    hi = (b & 0x80008000u) | ((b >> 1) & 0x3f803f80u);
 }
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }

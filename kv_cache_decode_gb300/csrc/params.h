@@ -34,10 +34,12 @@ struct DecodeParams {
     // give zero rows and KVD_STATUS_BAD_PAGE.
     const int32_t* block_table;
     int max_blocks, page_shift, num_pages;
-    // int8 cache (k_scale non-null): k and v hold int8 codes, and row (b, t, h)
-    // reads back as k_scale[(b * S_max + t) * Hkv + h] * code (v likewise).
+    // 8-bit cache (k_scale non-null): k and v hold int8 codes (kv_fp8 = 0) or
+    // fp8 E4M3 codes (kv_fp8 = 1: the kernel's FP8 variant), and row (b, t, h) reads back as
+    // k_scale[(b * S_max + t) * Hkv + h] * value(code) (v likewise).
     const float* k_scale;
     const float* v_scale;
+    int kv_fp8;
     // Query tokens per sequence (1, or T > 1 for a speculative check step on
     // the mma.sync kernel): q, out [B, T, Hq, D], lse [B, T, Hq]; query token i
     // of sequence b attends to its first seq_lens[b] - T + 1 + i tokens, and
@@ -66,15 +68,16 @@ struct ChunkKernel {
     int seg_unit;    // tokens per schedule position (1 or tile_tokens, see schedule.cuh)
     int seg_cost;    // positions charged per pair by the schedule
     bool f32_out, tensor_core;
-    int index;  // position in the variant table (0..47), for the per-device attribute bitmask
+    int index;  // position in the variant table (0..59), for the per-device attribute bitmask
 };
 
 // The kernel for a shape: bf16 groups of up to 16 query heads per KV head run
 // on the mma.sync kernel (T query tokens as T * G rows, in blocks of 16),
 // wider groups (17..64) on the tcgen05 kernel (T query tokens as T virtual
 // sequences); int8 caches run on the mma.sync kernel for every group.
-const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8 = false);
-const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool kv8);
+const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8 = false,
+                                     bool fp8 = false);
+const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool kv8, bool fp8);
 const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out, int group);
 
 cudaError_t launch_merge(const DecodeParams& p, int head_dim, bool f32_out, int num_sms, cudaStream_t stream);
@@ -93,8 +96,9 @@ cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const
 // t < seq_lens[b] of a bf16 cache.
 cudaError_t launch_append_q8(void* k_codes, void* v_codes, float* k_scale, float* v_scale, const void* k_new,
                              const void* v_new, const int32_t* pos, int B, int S_max, int Hkv, int D,
-                             int32_t* status, const PagedCache& pg, cudaStream_t stream, int T = 1);
+                             int32_t* status, const PagedCache& pg, cudaStream_t stream, int T = 1,
+                             bool fp8 = false);
 cudaError_t launch_quantize_q8(const void* src, void* codes, float* scales, const int32_t* seq_lens, int B,
-                               int S_max, int len_cap, int Hkv, int D, cudaStream_t stream);
+                               int S_max, int len_cap, int Hkv, int D, cudaStream_t stream, bool fp8 = false);
 
 }  // namespace kvd

@@ -143,13 +143,18 @@ struct ChunkShape {
     static_assert(D % 16 == 0 && D >= 64, "head_dim");
 };
 
-// KV8: the cache holds int8 codes with a float32 scale per (token, KV head)
-// row; K and V tiles are converted to f16 in shared memory (exactly: the codes
-// are small integers), q is taken to f16, the MMAs run in f16, each score is
-// multiplied by its key row's scale and each weight by its value row's scale
-// before P V.
-template <int D, int HT, int TS, int TT, int STAGES, bool F32OUT, int MINB, bool PAGED, bool KV8 = false>
+// KV8: the cache holds 8-bit codes (int8, or fp8 E4M3 with FP8) with a
+// float32 scale per (token, KV head) row; K and V tiles are converted to f16
+// in shared memory (exactly: int8 codes are small integers, and E4M3 codes
+// become their values / 256, which f16 holds exactly), q is taken to f16, the
+// MMAs run in f16, each score is multiplied by its key row's scale and each
+// weight by its value row's scale before P V (FP8: the scores by 256 more,
+// and the output by 256 before it is written).
+template <int D, int HT, int TS, int TT, int STAGES, bool F32OUT, int MINB, bool PAGED, bool KV8 = false,
+          bool FP8 = false>
 __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const DecodeParams p) {
+    static_assert(!FP8 || KV8, "fp8 codes are an 8-bit cache");
+    constexpr float OSC = FP8 ? 256.f : 1.f;  // output scale: E4M3 value rows arrive divided by 256
     using Sh = ChunkShape<D, HT, TS, TT, STAGES, KV8>;
     constexpr int NW = Sh::NW, NT = Sh::NT, TW = Sh::TW, NS = Sh::NS, KS = Sh::KS,
                   ND = Sh::ND, CH = Sh::CH, TILE_ELEMS = Sh::TILE_ELEMS, SEG_COST = Sh::SEG_COST;
@@ -504,10 +509,17 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                     for (int j = 0; j < NB; ++j) {
                         const int i = lane + 32 * (j0 + j), rr = i / CH8, c8 = i % CH8, r = wbase + rr;
                         uint4 a, b;
-                        i8x4_to_f16x2x2(w[j].x, a.x, a.y);
-                        i8x4_to_f16x2x2(w[j].y, a.z, a.w);
-                        i8x4_to_f16x2x2(w[j].z, b.x, b.y);
-                        i8x4_to_f16x2x2(w[j].w, b.z, b.w);
+                        if constexpr (FP8) {
+                            e4m3x4_to_f16x2x2_div256(w[j].x, a.x, a.y);
+                            e4m3x4_to_f16x2x2_div256(w[j].y, a.z, a.w);
+                            e4m3x4_to_f16x2x2_div256(w[j].z, b.x, b.y);
+                            e4m3x4_to_f16x2x2_div256(w[j].w, b.z, b.w);
+                        } else {
+                            i8x4_to_f16x2x2(w[j].x, a.x, a.y);
+                            i8x4_to_f16x2x2(w[j].y, a.z, a.w);
+                            i8x4_to_f16x2x2(w[j].z, b.x, b.y);
+                            i8x4_to_f16x2x2(w[j].w, b.z, b.w);
+                        }
                         uint8_t* row = conv8 + kv * TILE_ELEMS * 2 + r * D * 2;
                         *reinterpret_cast<uint4*>(row + (((2 * c8) ^ (r & 7)) * 16)) = a;
                         *reinterpret_cast<uint4*>(row + (((2 * c8 + 1) ^ (r & 7)) * 16)) = b;
@@ -562,7 +574,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                 for (int e = 0; e < 4; ++e) {
                     const int tok = wbase + j * 8 + (lane & 3) * 2 + (e & 1);
                     float sc = scale_log2;
-                    if constexpr (KV8) sc *= kscale[tok];
+                    if constexpr (KV8) sc *= kscale[tok] * (FP8 ? 256.f : 1.f);
                     s[j][e] = (tok < nvalid && tok < (e < 2 ? lim0 : lim1)) ? s[j][e] * sc : -CUDART_INF_F;
                 }
                 mx0 = fmaxf(mx0, fmaxf(s[j][0], s[j][1]));
@@ -734,7 +746,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                 const size_t or0 = v0 ? out_row(ct.b, ct.h, r0) : 0, or1 = v1 ? out_row(ct.b, ct.h, r1) : 0;
                 if (ct.full) {
                     // (a row that sees no token, possible only when L < T, is zero)
-                    const float i0 = l0 > 0.f ? 1.f / l0 : 0.f, i1 = l1 > 0.f ? 1.f / l1 : 0.f;
+                    const float i0 = l0 > 0.f ? OSC / l0 : 0.f, i1 = l1 > 0.f ? OSC / l1 : 0.f;
 #pragma unroll
                     for (int n = 0; n < ND; ++n) {
                         const int d = n * 8 + (lane & 3) * 2;
@@ -758,8 +770,8 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
 #pragma unroll
                     for (int n = 0; n < ND; ++n) {
                         const int d = n * 8 + (lane & 3) * 2;
-                        if (v0) *reinterpret_cast<float2*>(wo + (size_t)r0 * D + d) = make_float2(o[n][0], o[n][1]);
-                        if (v1) *reinterpret_cast<float2*>(wo + (size_t)r1 * D + d) = make_float2(o[n][2], o[n][3]);
+                        if (v0) *reinterpret_cast<float2*>(wo + (size_t)r0 * D + d) = make_float2(o[n][0] * OSC, o[n][1] * OSC);
+                        if (v1) *reinterpret_cast<float2*>(wo + (size_t)r1 * D + d) = make_float2(o[n][2] * OSC, o[n][3] * OSC);
                     }
                     if ((lane & 3) == 0) {
                         if (v0) p.ws_ml[slot * TG + r0] = make_float2(m0, l0);

@@ -2,5 +2,5 @@
 #include "split_kv_chunk_variants.cuh"
 
 namespace kvd {
-KVD_MMA_TABLE(256, 4, 34, 40, 46)
+KVD_MMA_TABLE(256, 4, 34, 40, 46, 56)
 }  // namespace kvd

@@ -27,7 +27,7 @@ struct ChunkConfig {
     static constexpr int MINB8 = (2 * (SMEM8 + 1024) <= 228 * 1024) ? 2 : 1;
 };
 
-template <int D, bool F32, bool PAGED, bool KV8>
+template <int D, bool F32, bool PAGED, bool KV8, bool FP8>
 cudaError_t launch_mma_chunk(const ChunkKernel& k, const DecodeParams& p, cudaStream_t stream) {
     using C = ChunkConfig<D, 1>;
     constexpr int ST = KV8 ? C::STAGES8 : C::STAGES, MB = KV8 ? C::MINB8 : C::MINB;
@@ -41,17 +41,17 @@ cudaError_t launch_mma_chunk(const ChunkKernel& k, const DecodeParams& p, cudaSt
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kv_chunk_kernel<D, 1, C::TS, C::TT, ST, F32, MB, PAGED, KV8>, p);
+    return cudaLaunchKernelEx(&cfg, split_kv_chunk_kernel<D, 1, C::TS, C::TT, ST, F32, MB, PAGED, KV8, FP8>, p);
 }
 
-template <int D, bool F32, bool PAGED, bool KV8 = false>
+template <int D, bool F32, bool PAGED, bool KV8 = false, bool FP8 = false>
 inline ChunkKernel make_mma_chunk_kernel(int index) {
     using C = ChunkConfig<D, 1>;
     constexpr int ST = KV8 ? C::STAGES8 : C::STAGES, MB = KV8 ? C::MINB8 : C::MINB;
     using Sh = ChunkShape<D, 1, C::TS, C::TT, ST, KV8>;
     ChunkKernel k;
-    k.fn = reinterpret_cast<const void*>(split_kv_chunk_kernel<D, 1, C::TS, C::TT, ST, F32, MB, PAGED, KV8>);
-    k.launch = launch_mma_chunk<D, F32, PAGED, KV8>;
+    k.fn = reinterpret_cast<const void*>(split_kv_chunk_kernel<D, 1, C::TS, C::TT, ST, F32, MB, PAGED, KV8, FP8>);
+    k.launch = launch_mma_chunk<D, F32, PAGED, KV8, FP8>;
     k.head_dim = D;
     k.threads = Sh::NT;
     k.smem_bytes = Sh::SMEM_BYTES;
@@ -67,17 +67,22 @@ inline ChunkKernel make_mma_chunk_kernel(int index) {
 
 // Variants of one head dimension: contiguous bf16 cache at indices IDX,
 // IDX + 1, paged at PIDX, PIDX + 1, int8 at QIDX, QIDX + 1, paged int8 at
-// PQIDX, PQIDX + 1 (bf16 and fp32 output).
-#define KVD_MMA_TABLE(D, IDX, PIDX, QIDX, PQIDX)                                                  \
-    const ChunkKernel* mma_table_d##D(bool f32, bool paged, bool kv8) {                          \
-        static const ChunkKernel table[4][2] = {                                                 \
+// PQIDX, PQIDX + 1, fp8 at FIDX, FIDX + 1 and paged fp8 at FIDX + 2, FIDX + 3
+// (bf16 and fp32 output).
+#define KVD_MMA_TABLE(D, IDX, PIDX, QIDX, PQIDX, FIDX)                                            \
+    const ChunkKernel* mma_table_d##D(bool f32, bool paged, bool kv8, bool fp8) {                \
+        static const ChunkKernel table[6][2] = {                                                 \
             {make_mma_chunk_kernel<D, false, false>(IDX), make_mma_chunk_kernel<D, true, false>(IDX + 1)}, \
             {make_mma_chunk_kernel<D, false, true>(PIDX), make_mma_chunk_kernel<D, true, true>(PIDX + 1)}, \
             {make_mma_chunk_kernel<D, false, false, true>(QIDX),                                 \
              make_mma_chunk_kernel<D, true, false, true>(QIDX + 1)},                             \
             {make_mma_chunk_kernel<D, false, true, true>(PQIDX),                                 \
-             make_mma_chunk_kernel<D, true, true, true>(PQIDX + 1)}};                            \
-        return &table[(kv8 ? 2 : 0) + (paged ? 1 : 0)][f32 ? 1 : 0];                             \
+             make_mma_chunk_kernel<D, true, true, true>(PQIDX + 1)},                             \
+            {make_mma_chunk_kernel<D, false, false, true, true>(FIDX),                           \
+             make_mma_chunk_kernel<D, true, false, true, true>(FIDX + 1)},                       \
+            {make_mma_chunk_kernel<D, false, true, true, true>(FIDX + 2),                        \
+             make_mma_chunk_kernel<D, true, true, true, true>(FIDX + 3)}};                       \
+        return &table[(kv8 ? (fp8 ? 4 : 2) : 0) + (paged ? 1 : 0)][f32 ? 1 : 0];                 \
     }
 
 }  // namespace kvd

@@ -370,6 +370,33 @@ def test_decode_step_host_rejects(lib, over, expect):
     assert lib.kvd_decode_step_host(*_host_step_args(**over)) == expect
 
 
+@pytest.mark.parametrize("fn", ["kvd_kv_quantize_fp8", "kvd_kv_quantize_q8"])
+@pytest.mark.parametrize("args,expect", [
+    ((None, FAKE, FAKE, FAKE, 2, 8, 8, 1, 128, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 2, 8, 8, 1, 96, None), kvd.ERR_UNSUPPORTED),
+    ((FAKE, FAKE + 8, FAKE, FAKE, 2, 8, 8, 1, 128, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, 0, 8, 8, 1, 128, None), kvd.OK),
+])
+def test_quantize_8bit_rejects(lib, fn, args, expect):
+    assert getattr(lib, fn)(*args) == expect
+
+
+@pytest.mark.parametrize("args,expect", [
+    ((FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, 2, 8, 1, 128, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 1, 96, None, None), kvd.ERR_UNSUPPORTED),
+    ((FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 8, 1, 128, None, None), kvd.OK),
+])
+def test_append_fp8_rejects(lib, args, expect):
+    assert lib.kvd_kv_append_fp8(*args) == expect
+
+
+def test_append_fp8_paged_rejects(lib):
+    ok = (FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 4, 16, 10, 1, 128, None, None)
+    assert lib.kvd_kv_append_fp8_paged(*ok) == kvd.OK
+    bad_page = ok[:10] + (24,) + ok[11:]
+    assert lib.kvd_kv_append_fp8_paged(*bad_page) == kvd.ERR_INVALID_ARG
+
+
 def test_decode_ex_rejects(lib):
     c = kvd._CCache(k=FAKE, v=FAKE, s_max=64)
     a = _dec_args()  # q, k, v, lens, B, S, maxlen, Hq, Hkv, D, scale, n_split, ws, ws_bytes, out, dt, lse, status, stream
@@ -381,6 +408,8 @@ def test_decode_ex_rejects(lib):
     assert call(ctypes.byref(c), kn=FAKE) == kvd.ERR_INVALID_ARG            # only part of the append
     cq = kvd._CCache(k=FAKE, v=FAKE, k_scales=FAKE, s_max=64)
     assert call(ctypes.byref(cq)) == kvd.ERR_INVALID_ARG                    # one scale array only
+    cf = kvd._CCache(k=FAKE, v=FAKE, s_max=64, fp8=1)
+    assert call(ctypes.byref(cf)) == kvd.ERR_INVALID_ARG                    # fp8 codes without scales
     cpq = kvd._CCache(k=FAKE, v=FAKE, k_scales=FAKE, v_scales=FAKE, block_table=FAKE, max_blocks=4,
                       page_size=16, num_pages=10)
     # paged int8 passes every check up to the workspace (none given here)
