@@ -348,11 +348,13 @@ kvd_status kvd_decode_step_q8(void* k_codes, void* v_codes, float* k_scales, flo
  *   k_new, v_new : bf16 [batch, T, n_heads_kv, head_dim]
  * A query token that sees no token (L_b < T - i) gets a zero row and lse -inf.
  * T from 1 to KVD_MAX_TOKENS (above: KVD_ERR_UNSUPPORTED), any supported
- * group; T > 1 runs on the mma.sync kernel, one CTA per 16 of a pair's T * G
- * rows and token run. T = 1 is exactly the single-token call. The split count
- * is the single-token plan's, and the workspace holds T times the rows: size
- * it with kvd_decode_plan_multi. Rows of
- * the append outside [0, s_max) are skipped with KVD_STATUS_POS_OUT_OF_RANGE.
+ * group. Groups of up to 16 run on the mma.sync kernel, one CTA per 16 of a
+ * pair's T * G rows and token run; wider groups on the tcgen05 kernel, each
+ * query token as a sequence of its own over the shared cache rows. T = 1 is
+ * exactly the single-token call. The split count is the single-token plan's,
+ * and the workspace holds T times the rows: size it with
+ * kvd_decode_plan_multi. Rows of the append outside [0, s_max) are skipped
+ * with KVD_STATUS_POS_OUT_OF_RANGE.
  * Other arguments, results and errors as the single-token calls, plus
  * KVD_ERR_INVALID_ARG for n_tokens < 1.
  */

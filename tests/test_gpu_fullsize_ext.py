@@ -1,4 +1,4 @@
-"""The paged, int8 and multi-token paths at the workloads' full sizes, in the
+"""The paged, 8-bit (int8 and fp8) and multi-token paths at the workloads' full sizes, in the
 launch configuration the benchmark uses (heuristic split): paged steps
 bit-identical to the contiguous steps (which the full-size tests hold to the
 oracle), int8 and multi-token steps against the oracle on a sample of whole
@@ -47,42 +47,49 @@ def test_paged_full_size_equals_contiguous(name, page):
 
 
 @pytest.mark.parametrize("name", ["gqa", "palm"])
-def test_int8_full_size(name):
+@pytest.mark.parametrize("fmt", ["int8", "fp8"])
+def test_8bit_full_size(name, fmt):
     import torch
     import kv_cache_decode_gb300 as kvd
     dev = cuda_or_skip()
     w = workloads.get(name)
     inp = workloads.step_inputs(w)
     B, S, Hkv, D = inp.k_cache.shape
+    fp8 = fmt == "fp8"
     cached = torch.from_numpy(np.maximum(inp.seq_lens - 1, 0).astype(np.int32)).to(dev)
     dev_q8 = []
     for c in (inp.k_cache, inp.v_cache):
-        codes = torch.full((B, S, Hkv, D), -128, dtype=torch.int8, device=dev)
+        codes = torch.full((B, S, Hkv, D), 0x7F if fp8 else -128, dtype=torch.uint8 if fp8 else torch.int8,
+                           device=dev)
         scales = torch.full((B, S, Hkv), float("nan"), dtype=torch.float32, device=dev)
-        kvd.kv_quantize_q8(to_dev_bf16(c, dev), codes, scales, cached, S)
+        (kvd.kv_quantize_fp8 if fp8 else kvd.kv_quantize_q8)(to_dev_bf16(c, dev), codes, scales, cached, S)
         dev_q8 += [codes, scales]
     q, kn, vn = (to_dev_bf16(x, dev) for x in (inp.q, inp.k_new, inp.v_new))
     out = torch.full(inp.q.shape, float("nan"), dtype=torch.bfloat16, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     ws = kvd.alloc_workspace(q, inp.k_cache, S)
-    kvd.decode_step_q8(q, dev_q8[0], dev_q8[2], dev_q8[1], dev_q8[3], kn, vn, torch.from_numpy(inp.pos).to(dev),
-                       torch.from_numpy(inp.seq_lens).to(dev), S, w.scale, out, workspace=ws, status=status)
+    kvd.decode_ex(q, dev_q8[0], dev_q8[2], torch.from_numpy(inp.seq_lens).to(dev), S, w.scale, out,
+                  k_scales=dev_q8[1], v_scales=dev_q8[3], k_new=kn, v_new=vn, pos=torch.from_numpy(inp.pos).to(dev),
+                  workspace=ws, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     got = bf16_bits_to_f32(bf16_tensor_bits(out)).astype(np.float64)
     L = inp.seq_lens
+    quant = oracle.quantize_fp8 if fp8 else oracle.quantize_q8
+    cdt = np.uint8 if fp8 else np.int8
     rows = sorted({int(np.argmin(L)), int(np.argmax(L)), 17, B - 1})
     for b in rows:
         n = int(L[b]) - 1
-        kc = np.zeros((1, S, Hkv, D), np.int8)
-        vc = np.zeros((1, S, Hkv, D), np.int8)
+        kc = np.zeros((1, S, Hkv, D), cdt)
+        vc = np.zeros((1, S, Hkv, D), cdt)
         ks = np.zeros((1, S, Hkv), np.float32)
         vs = np.zeros((1, S, Hkv), np.float32)
-        kc[0, :n], ks[0, :n] = oracle.quantize_q8(inp.k_cache[b, :n])
-        vc[0, :n], vs[0, :n] = oracle.quantize_q8(inp.v_cache[b, :n])
-        kc, vc, ks, vs, _ = oracle.kv_append_q8(kc, vc, ks, vs, inp.k_new[b:b + 1], inp.v_new[b:b + 1], inp.pos[b:b + 1])
-        want, _ = oracle.decode_attention_q8(inp.q[b:b + 1], kc, vc, ks, vs, L[b:b + 1], w.scale)
-        assert_close(got[b:b + 1], want, "bf16", f"{name} int8 row {b}")
+        kc[0, :n], ks[0, :n] = quant(inp.k_cache[b, :n])
+        vc[0, :n], vs[0, :n] = quant(inp.v_cache[b, :n])
+        kc, vc, ks, vs, _ = oracle.kv_append_q8(kc, vc, ks, vs, inp.k_new[b:b + 1], inp.v_new[b:b + 1],
+                                                inp.pos[b:b + 1], fmt=fmt)
+        want, _ = oracle.decode_attention_q8(inp.q[b:b + 1], kc, vc, ks, vs, L[b:b + 1], w.scale, fmt=fmt)
+        assert_close(got[b:b + 1], want, "bf16", f"{name} {fmt} row {b}")
 
 
 @pytest.mark.parametrize("name,T", [("gqa", 4), ("mha", 16), ("gqa", 8), ("palm", 2)])
