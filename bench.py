@@ -478,8 +478,9 @@ def run_ours(args):
             _, pq, pkn, pvn, ppos, plens = kvd.alloc_host_packet(B, T, Hq, Hkv, D)
             for dst, src in ((pq, bf(q_h)), (pkn, bf(kn_h)), (pvn, bf(vn_h)), (ppos, pos_h), (plens, lens_h)):
                 dst.copy_(src)
+            # out=None: the kernels write the result straight into the pinned out_h
             host_steps = [kvd.HostStep(pq, pkn, pvn, ppos, plens, kcs[r], vcs[r], staging, max_len,
-                                       w.scale, out, out_h, workspace=ws, n_split=args.n_split) for r in range(R)]
+                                       w.scale, None, out_h, workspace=ws, n_split=args.n_split) for r in range(R)]
 
         def e2e_step(r):
             if host_steps is not None:

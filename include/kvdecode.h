@@ -486,7 +486,10 @@ kvd_status kvd_kernel_info(int n_heads_q, int n_heads_kv, int head_dim, kvd_out_
  * writing `out` on the device, and `out` is copied to out_host (same size).
  * Host inputs laid out like the staging buffer (q | k_new | v_new | pos |
  * seq_lens, each 256-byte aligned, one host packet starting at q_host) are
- * copied with one cudaMemcpyAsync instead of five.
+ * copied with one cudaMemcpyAsync instead of five. With out = NULL the kernels
+ * write the result straight into out_host, which must then be page-locked
+ * host memory the device can address (cudaHostAlloc / cudaHostRegister, 16-byte
+ * aligned; else KVD_ERR_INVALID_ARG), and no copy back is queued.
  * Nothing is synchronised: out_host is valid once `stream` has reached the end
  * of this call's work. Every argument is checked before any copy is queued;
  * errors as kvd_decode_step_multi, plus KVD_ERR_INVALID_ARG for a NULL host

@@ -748,7 +748,8 @@ class HostStep:
     (step_staging_bytes), `out` and its CPU copy out_host. Each call copies the
     host inputs' current contents in, runs the step and copies `out` back, on
     `stream` (pin the host tensors for asynchronous copies); nothing is
-    synchronised. Arguments are checked here and by the library on every call."""
+    synchronised. With out=None the kernels write the result straight into the
+    pinned out_host. Arguments are checked here and by the library on every call."""
 
     def __init__(self, q_host, k_new_host, v_new_host, pos_host, seq_lens_host, k_cache, v_cache, staging,
                  max_seq_len: int, scale: float, out, out_host, workspace=None, n_split: int = 0, lse=None,
@@ -760,15 +761,19 @@ class HostStep:
         for t, n in ((pos_host, "pos_host"), (seq_lens_host, "seq_lens_host")):
             if t.dtype != torch.int32 or t.device.type != "cpu" or not t.is_contiguous():
                 raise TypeError(f"{n} must be a contiguous int32 CPU tensor")
-        if out_host.device.type != "cpu" or out_host.dtype != out.dtype or out_host.shape != out.shape:
+        # out None: the kernels write the result straight into out_host (pinned)
+        if out is None and not out_host.is_pinned():
+            raise ValueError("out=None needs a pinned out_host")
+        like = out if out is not None else out_host
+        if out_host.device.type != "cpu" or out_host.dtype != like.dtype or out_host.shape != like.shape:
             raise TypeError("out_host must be a CPU tensor like out")
         _require(k_cache, "k_cache", torch.bfloat16, 4)
         _require(v_cache, "v_cache", torch.bfloat16, 4)
         T = q_host.shape[1] if q_host.dim() == 4 else 1
         B, Hq, D = q_host.shape[0], q_host.shape[-2], q_host.shape[-1]
         S, Hkv = k_cache.shape[1], k_cache.shape[2]
-        code = OUT_BF16 if out.dtype == torch.bfloat16 else OUT_F32 if out.dtype == torch.float32 else None
-        if code is None or out.shape != q_host.shape:
+        code = OUT_BF16 if like.dtype == torch.bfloat16 else OUT_F32 if like.dtype == torch.float32 else None
+        if code is None or like.shape != q_host.shape:
             raise TypeError("out must be bfloat16 or float32, shaped like q")
         ws_ptr, ws_bytes = (None, 0) if workspace is None else (workspace.data_ptr(),
                                                                workspace.numel() * workspace.element_size())
@@ -778,7 +783,8 @@ class HostStep:
         self._args = (k_cache.data_ptr(), v_cache.data_ptr(), q_host.data_ptr(), k_new_host.data_ptr(),
                       v_new_host.data_ptr(), pos_host.data_ptr(), seq_lens_host.data_ptr(), staging.data_ptr(),
                       staging.numel() * staging.element_size(), B, T, S, int(max_seq_len), Hq, Hkv, D,
-                      float(scale), int(n_split), ws_ptr, ws_bytes, out.data_ptr(), out_host.data_ptr(), code,
+                      float(scale), int(n_split), ws_ptr, ws_bytes, None if out is None else out.data_ptr(),
+                      out_host.data_ptr(), code,
                       _ptr(lse), _ptr(status), _stream_handle(stream))
 
     def __call__(self):

@@ -392,6 +392,16 @@ kvd_status kvd_decode_step_host(void* k_cache, void* v_cache, const void* q_host
     if (!aligned(staging, 256) || staging_bytes < kvd_step_staging_bytes(batch, n_tokens, n_heads_q, n_heads_kv,
                                                                          head_dim))
         return KVD_ERR_INVALID_ARG;
+    // out == NULL: the kernels write the result straight into out_host, which
+    // must then be page-locked host memory the device can address.
+    void* out_dev = out;
+    if (!out) {
+        cudaPointerAttributes a;
+        if (cudaPointerGetAttributes(&a, out_host) != cudaSuccess || a.type != cudaMemoryTypeHost ||
+            !a.devicePointer || !aligned(a.devicePointer, 16))
+            return KVD_ERR_INVALID_ARG;
+        out_dev = a.devicePointer;
+    }
     if (batch == 0) return KVD_OK;
     // The staged inputs: q | k_new | v_new | pos | seq_lens, each 256-byte aligned.
     const size_t BT = (size_t)batch * n_tokens;
@@ -432,9 +442,10 @@ kvd_status kvd_decode_step_host(void* k_cache, void* v_cache, const void* q_host
     }
     const AppendArgs app{k_cache, v_cache, k_new, v_new, pos};
     st = decode(kBoth, q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q, n_heads_kv, head_dim,
-                scale, n_split, workspace, workspace_bytes, out, out_dtype, lse_out, status_word, stream, &app,
+                scale, n_split, workspace, workspace_bytes, out_dev, out_dtype, lse_out, status_word, stream, &app,
                 nullptr, nullptr, n_tokens);
     if (st != KVD_OK) return st;
+    if (!out) return KVD_OK;  // written in place over the host link
     const size_t ob = BT * n_heads_q * head_dim * (out_dtype == KVD_OUT_F32 ? 4 : 2);
     return cudaMemcpyAsync(out_host, out, ob, cudaMemcpyDeviceToHost, s) == cudaSuccess ? KVD_OK : KVD_ERR_CUDA;
 }

@@ -364,6 +364,7 @@ def _host_step_args(**over):
     (dict(k=None), kvd.ERR_INVALID_ARG),
     (dict(ws_bytes=16), kvd.ERR_WORKSPACE_TOO_SMALL),
     (dict(B=0), kvd.OK),                              # nothing to copy or launch
+    (dict(out=None), kvd.ERR_INVALID_ARG),            # direct write needs pinned host memory
 ])
 def test_decode_step_host_rejects(lib, over, expect):
     # every rejection comes before any copy is queued (the pointers are fake)

@@ -85,3 +85,34 @@ def test_packed_host_inputs_equal_separate(T):
         outs.append((out_h.view(torch.int16).numpy().copy(), bf16_tensor_bits(kc)))
     assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
     assert not np.isnan((outs[1][0].view(np.uint16).astype(np.uint32) << 16).view(np.float32)).any()
+
+
+@pytest.mark.parametrize("T", [1, 2])
+def test_direct_host_output_equals_copy(T):
+    """out=None: the kernels write the result straight into pinned host memory;
+    the same bits as the device output copied back."""
+    import torch
+    import kv_cache_decode_gb300 as kvd
+    dev = cuda_or_skip()
+    Hq, Hkv, D = 48, 1, 256
+    w = workloads.Workload("hd", 6, Hq, Hkv, D, 500, T, 500, 114)
+    mi = workloads.multi_step_inputs(w, T)
+    B, S = mi.q.shape[0], mi.k_cache.shape[1]
+    squeeze = (lambda a: a[:, 0]) if T == 1 else (lambda a: a)
+    _, nbytes = kvd.decode_plan_multi(B, T, Hq, Hkv, D, S, 0, 0, "bf16")
+    ws = torch.empty(max(nbytes, 1), dtype=torch.uint8, device=dev)
+    staging = torch.empty(kvd.step_staging_bytes(B, T, Hq, Hkv, D), dtype=torch.uint8, device=dev)
+    packet, *views = kvd.alloc_host_packet(B, T, Hq, Hkv, D)
+    for dst, src in zip(views, (squeeze(mi.q), squeeze(mi.k_new), squeeze(mi.v_new), mi.pos, mi.seq_lens)):
+        dst.copy_(torch.from_numpy(np.ascontiguousarray(src.view(np.int16) if src.dtype == np.uint16 else src))
+                  .view(dst.dtype))
+    outs = []
+    for direct in (False, True):
+        kc, vc = to_dev_bf16(mi.k_cache, dev), to_dev_bf16(mi.v_cache, dev)
+        out = None if direct else torch.empty(views[0].shape, dtype=torch.bfloat16, device=dev)
+        out_h = torch.full(views[0].shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+        kvd.decode_step_host(*views, kc, vc, staging, S, w.scale, out, out_h, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append(out_h.view(torch.int16).numpy().copy())
+    assert np.array_equal(outs[0], outs[1])
+    assert not np.isnan((outs[1].view(np.uint16).astype(np.uint32) << 16).view(np.float32)).any()
