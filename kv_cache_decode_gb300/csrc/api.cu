@@ -202,6 +202,20 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     // query tokens as T virtual sequences of one query token each.
     const int row_blocks = k->tensor_core ? 1 : (Hq / Hkv * T + 15) / 16;
     const int vT = k->tensor_core ? T : 1;
+    if (n_split_req == 0 && row_blocks > 1) {
+        // The heuristic split fills the GPU with one CTA per resident slot; a
+        // pair in row blocks launches row_blocks CTAs per token run, so the
+        // run count is cut to keep the launch to one wave (a second, partial
+        // wave measured up to a quarter slower). Fewer runs need less workspace.
+        int sms = 0;
+        st = device_sms(&sms);
+        if (st != KVD_OK) return st;
+        const int per_wave = (int)std::max(1LL, (long long)sms * k->ctas_per_sm / row_blocks);
+        if (n_split > per_wave) {
+            n_split = per_wave;
+            need = workspace_for(n_split, batch, Hq * T, Hkv, D);
+        }
+    }
     if ((long long)n_split * row_blocks > 0x7fffffffLL) return KVD_ERR_INVALID_ARG;
     if ((long long)batch * vT > 0x7fffffffLL) return KVD_ERR_INVALID_ARG;
     if (need > 0) {
