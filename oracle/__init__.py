@@ -58,6 +58,13 @@ Functions and the passages they follow (page title, section):
   page leaves the out-of-range case open, and here a row with a score outside
   [phi - 64 ln 2, phi + 8 ln 2] is recomputed by ``decode_attention`` and
   reported. Plain numpy, float64.
+* ``merge_attention``: attention results of disjoint shards of each
+  sequence's tokens (each normalised, with its natural-log normaliser lse)
+  combined into the attention over all of them: with L = ln sum_j exp(lse_j),
+  out = sum_j exp(lse_j - L) out_j and lse = L (shards with lse = -inf hold
+  no token and add nothing). All About Transformer Inference, "Sharding the
+  KV cache": sequence-sharded partial results are accumulated as in Flash
+  Attention; the identity is the textbook one. Plain numpy, float64.
 * ``kv_append_multi``, ``decode_attention_multi``: T new tokens per sequence
   (a speculative-decoding check step): their rows are appended at pos[b] ..
   pos[b] + T - 1, and query token i attends to the cached tokens and the new
@@ -252,6 +259,23 @@ def decode_attention_unified_max(q, k_cache, v_cache, seq_lens, scale, phi, n_ch
         ref, ref_lse = decode_attention(q, k_cache, v_cache, seq_lens, scale, lib=lib)
         out[fell_back], lse[fell_back] = ref[fell_back], ref_lse[fell_back]
     return out, lse, fell_back
+
+
+def merge_attention(outs, lses):
+    """(out [..., D], lse [...]) from shard results outs [n, ..., D] and lses [n, ...]."""
+    outs = np.asarray(outs, dtype=np.float64)
+    lses = np.asarray(lses, dtype=np.float64)
+    if outs.shape[:-1] != lses.shape:
+        raise ValueError("outs [n, ..., D] and lses [n, ...] disagree")
+    top = np.max(lses, axis=0)
+    live = np.isfinite(top)
+    shifted = np.where(live, top, 0.0)
+    w = np.where(np.isfinite(lses), np.exp(lses - shifted), 0.0)  # exp(lse_j - max)
+    total = w.sum(axis=0)
+    out = np.where(live[..., None], np.einsum("n...,n...d->...d", w, outs) / np.where(live, total, 1.0)[..., None],
+                   0.0)
+    lse = np.where(live, shifted + np.log(np.where(live, total, 1.0)), -np.inf)
+    return out, lse
 
 
 def attention_weights(q, k_cache, seq_lens, scale, b: int, h: int, lib=None):

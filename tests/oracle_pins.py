@@ -745,6 +745,36 @@ def check_fp8_attention_close_to_bf16(lib):
     assert np.max(np.abs(got - ref)) < 0.1
 
 
+def check_merge_attention_of_shards(lib):
+    # Attention over a sequence's tokens split into disjoint shards, each
+    # attended alone, merges back to the attention over all of them; a shard
+    # with no tokens adds nothing, and a row with none anywhere stays empty.
+    r = np.random.default_rng(91)
+    B, S, Hq, Hkv, D = 3, 30, 4, 2, 8
+    q = _bits(r.standard_normal((B, Hq, D)))
+    k = _bits(r.standard_normal((B, S, Hkv, D)))
+    v = _bits(r.standard_normal((B, S, Hkv, D)))
+    lens = np.array([30, 11, 0], np.int32)
+    want, want_lse = oracle.decode_attention(q, k, v, lens, 0.4, lib=lib)
+    cuts = [0, 7, 7, 19, 30]  # shard 1 holds no tokens
+    outs, lses = [], []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        sl = np.clip(lens - a, 0, b - a).astype(np.int32)
+        o, l = oracle.decode_attention(q, np.ascontiguousarray(k[:, a:b]) if b > a else k[:, :1] * 0,
+                                       np.ascontiguousarray(v[:, a:b]) if b > a else v[:, :1] * 0,
+                                       sl if b > a else np.zeros(B, np.int32), 0.4, lib=lib)
+        outs.append(o)
+        lses.append(l)
+    out, lse = oracle.merge_attention(outs, lses)
+    assert np.max(np.abs(out - want)) < 1e-13
+    live = np.isfinite(want_lse)
+    assert np.max(np.abs(lse[live] - want_lse[live])) < 1e-13 and np.all(np.isneginf(lse[~live]))
+    assert np.all(out[2] == 0)
+    # one shard alone is itself
+    o1, l1 = oracle.merge_attention(outs[:1], lses[:1])
+    assert np.array_equal(o1[:2], outs[0][:2])
+
+
 ALL_CHECKS = [
     check_identical_keys_give_mean_of_v,
     check_dominant_score_returns_that_row,
@@ -778,6 +808,7 @@ ALL_CHECKS = [
     check_e4m3_against_torch,
     check_fp8_quantizer,
     check_fp8_attention_close_to_bf16,
+    check_merge_attention_of_shards,
     check_multi_token_one_is_single,
     check_multi_token_against_torch_causal,
     check_multi_token_append,
