@@ -475,6 +475,30 @@ kvd_status kvd_kernel_info(int n_heads_q, int n_heads_kv, int head_dim, kvd_out_
                            int* ctas_per_sm_out, int* seg_unit_out, int* seg_cost_out);
 
 /*
+ * kvd_merge_attention: attention results over disjoint shards of each
+ * sequence's tokens combined into the result over all of them, the exchange
+ * step of sequence-sharded KV (All About Transformer Inference, "Sharding the
+ * KV cache": the shards' results accumulate as in Flash Attention): given, per
+ * shard j, the normalised output out_j and its natural-log normaliser lse_j
+ * (as kvd_decode_attention returns them in out and lse_out), with
+ * L = ln sum_j exp(lse_j):  out = sum_j exp(lse_j - L) out_j,  lse = L.
+ * A shard with lse = -inf holds no token and adds nothing; a row with no token
+ * in any shard gets a zero row and lse -inf.
+ *   outs    : [n_shards, rows, head_dim] bf16 or fp32 (in_dtype), 16-byte aligned
+ *   lses    : fp32 [n_shards, rows]
+ *   out     : [rows, head_dim] (out_dtype), 16-byte aligned; lse_out: optional fp32 [rows]
+ * rows is B * Hq (or B * T * Hq) of the shards' calls. The shards may come
+ * from other devices (copied here first) or from separate caches on this one
+ * (a shared prefix and a per-sequence suffix). Errors: KVD_ERR_INVALID_ARG for
+ * NULL or misaligned pointers, n_shards < 1, rows < 0 or a bad dtype;
+ * KVD_ERR_UNSUPPORTED for head_dim outside {64, 128, 256}; KVD_ERR_CUDA if the
+ * launch fails.
+ */
+kvd_status kvd_merge_attention(const void* outs, const float* lses, int n_shards, long long rows, int head_dim,
+                               kvd_out_dtype in_dtype, void* out, kvd_out_dtype out_dtype, float* lse_out,
+                               kvd_stream_t stream);
+
+/*
  * kvd_decode_step_host: one step whose per-step inputs come from the host and
  * whose result goes back to it, in one call (a deployment convenience, not
  * part of the method): q_host [batch, n_tokens, Hq, D] bf16, k_new_host,

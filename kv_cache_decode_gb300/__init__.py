@@ -35,7 +35,7 @@ EXPORTED = (
     "kvd_decode_attention_q8", "kvd_decode_step_q8", "kvd_decode_plan_multi", "kvd_kv_append_multi",
     "kvd_decode_attention_multi", "kvd_decode_step_multi", "kvd_decode_ex", "kvd_kv_append_q8_paged",
     "kvd_decode_attention_umax", "kvd_decode_step_umax", "kvd_step_staging_bytes", "kvd_decode_step_host",
-    "kvd_kv_quantize_fp8", "kvd_kv_append_fp8", "kvd_kv_append_fp8_paged",
+    "kvd_kv_quantize_fp8", "kvd_kv_append_fp8", "kvd_kv_append_fp8_paged", "kvd_merge_attention",
 )
 STATIC_WORKSPACE_BYTES = 16 << 20  # KVD_STATIC_WORKSPACE_BYTES
 
@@ -113,6 +113,8 @@ def _declare(lib):
     lib.kvd_decode_attention_umax.restype = I
     lib.kvd_decode_step_umax.argtypes = [P, P, P, P, P, P, P] + dec[4:11] + [F] + dec[11:]
     lib.kvd_decode_step_umax.restype = I
+    lib.kvd_merge_attention.argtypes = [P, P, I, ctypes.c_longlong, I, I, P, I, P, P]
+    lib.kvd_merge_attention.restype = I
     lib.kvd_step_staging_bytes.argtypes = [I, I, I, I, I]
     lib.kvd_step_staging_bytes.restype = SZ
     lib.kvd_decode_step_host.argtypes = [P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, I, F, I, P, SZ, P, P, I, P,
@@ -733,6 +735,27 @@ def decode_step_umax(q, k_cache, v_cache, k_new, v_new, pos, seq_lens, max_seq_l
                      stream)
     args = [a[1], a[2], k_new.data_ptr(), v_new.data_ptr(), pos.data_ptr(), a[0], a[3]] + a[4:11] + [float(phi)] + a[11:]
     _check(load().kvd_decode_step_umax(*args), "kvd_decode_step_umax")
+
+
+def merge_attention(outs, lses, out, lse=None, stream=None):
+    """Results over disjoint token shards combined by their normalisers
+    (kvd_merge_attention): outs [n, ..., D] bf16 or fp32 and lses [n, ...] fp32
+    as the attention calls return out and lse; out [..., D] bf16 or fp32."""
+    import torch
+    _require(outs, "outs", (torch.bfloat16, torch.float32))
+    _require(lses, "lses", torch.float32)
+    _require(out, "out", (torch.bfloat16, torch.float32))
+    n, D = outs.shape[0], outs.shape[-1]
+    if lses.shape != outs.shape[:-1] or out.shape != outs.shape[1:]:
+        raise ValueError("merge_attention: outs [n, ..., D], lses [n, ...] and out [..., D] disagree")
+    if lse is not None:
+        _require(lse, "lse", torch.float32)
+        if lse.shape != lses.shape[1:]:
+            raise ValueError("merge_attention: lse must be shaped like lses[0]")
+    rows = out.numel() // D
+    code = lambda t: OUT_BF16 if t.dtype == torch.bfloat16 else OUT_F32
+    _check(load().kvd_merge_attention(outs.data_ptr(), lses.data_ptr(), n, rows, D, code(outs), out.data_ptr(),
+                                      code(out), _ptr(lse), _stream_handle(stream)), "kvd_merge_attention")
 
 
 def step_staging_bytes(batch: int, n_tokens: int, n_heads_q: int, n_heads_kv: int, head_dim: int) -> int:

@@ -384,6 +384,23 @@ kvd_status kvd_decode_step_multi(void* k_cache, void* v_cache, const void* k_new
                   stream, &app, nullptr, nullptr, n_tokens);
 }
 
+kvd_status kvd_merge_attention(const void* outs, const float* lses, int n_shards, long long rows, int head_dim,
+                               kvd_out_dtype in_dtype, void* out, kvd_out_dtype out_dtype, float* lse_out,
+                               kvd_stream_t stream) {
+    if (!outs || !lses || !out || n_shards < 1 || rows < 0) return KVD_ERR_INVALID_ARG;
+    if ((in_dtype != KVD_OUT_BF16 && in_dtype != KVD_OUT_F32) || (out_dtype != KVD_OUT_BF16 && out_dtype != KVD_OUT_F32))
+        return KVD_ERR_INVALID_ARG;
+    if (head_dim != 64 && head_dim != 128 && head_dim != 256) return KVD_ERR_UNSUPPORTED;
+    if (!aligned(outs, 16) || !aligned(out, 16) || !aligned(lses, 4) || (lse_out && !aligned(lse_out, 4)))
+        return KVD_ERR_INVALID_ARG;
+    if ((unsigned long long)rows * (unsigned long long)(head_dim / 8) > 0x7fffffffULL * 256ULL) return KVD_ERR_INVALID_ARG;
+    if (rows == 0) return KVD_OK;
+    return launch_merge_shards(outs, lses, n_shards, rows, head_dim, in_dtype == KVD_OUT_F32, out,
+                               out_dtype == KVD_OUT_F32, lse_out, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KVD_OK
+               : KVD_ERR_CUDA;
+}
+
 size_t kvd_step_staging_bytes(int batch, int n_tokens, int n_heads_q, int n_heads_kv, int head_dim) {
     if (batch < 0 || n_tokens < 1 || n_heads_q < 1 || n_heads_kv < 1 || head_dim < 1) return 0;
     const size_t BT = (size_t)batch * n_tokens;

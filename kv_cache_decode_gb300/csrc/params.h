@@ -81,6 +81,9 @@ const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool
 const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out, int group);
 
 cudaError_t launch_merge(const DecodeParams& p, int head_dim, bool f32_out, int num_sms, cudaStream_t stream);
+// Results of disjoint token shards combined by their normalisers (split_kv_merge.cu).
+cudaError_t launch_merge_shards(const void* outs, const float* lses, int n, long long rows, int head_dim, bool in_f32,
+                                void* out, bool out_f32, float* lse_out, cudaStream_t stream);
 // A paged cache's table (block_table null: the cache is contiguous).
 struct PagedCache {
     const int32_t* block_table;

@@ -252,4 +252,89 @@ cudaError_t launch_merge(const DecodeParams& p, int head_dim, bool f32_out, int 
     }
 }
 
+// Shard merge: n attention results over disjoint shards of each sequence's
+// tokens (each normalised, with its natural-log normaliser lse, as the
+// attention calls return them) combined into the result over all shards:
+// L = ln sum_j exp(lse_j), out = sum_j exp(lse_j - L) out_j, lse = L; shards
+// with lse = -inf hold no token and add nothing (All About Transformer
+// Inference, "Sharding the KV cache": sequence-sharded results accumulate as
+// in Flash Attention). One thread per 8 columns of a row; each thread of a row
+// forms the row's weights from the n lse values itself.
+template <int D, bool IN_F32, bool OUT_F32>
+__global__ void __launch_bounds__(256) merge_shards_kernel(const void* __restrict__ outs,
+                                                           const float* __restrict__ lses, int n, long long rows,
+                                                           void* __restrict__ out, float* __restrict__ lse_out) {
+    constexpr int VPR = D / 8;
+    const long long g = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    const long long row = g / VPR;
+    const int c8 = (int)(g - row * VPR);
+    if (row >= rows) return;
+    float M = -CUDART_INF_F;
+    for (int j = 0; j < n; ++j) M = fmaxf(M, __ldg(lses + (size_t)j * rows + row));
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    float tot = 0.f;
+    if (M > -CUDART_INF_F) {
+        for (int j = 0; j < n; ++j) {
+            const float lj = __ldg(lses + (size_t)j * rows + row);
+            if (!(lj > -CUDART_INF_F)) continue;
+            const float w = expf(lj - M);
+            tot += w;
+            const size_t e = ((size_t)j * rows + row) * D + c8 * 8;
+            if constexpr (IN_F32) {
+                const float4 a = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(outs) + e));
+                const float4 b = __ldg(reinterpret_cast<const float4*>(static_cast<const float*>(outs) + e) + 1);
+                const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[i] += w * v[i];
+            } else {
+                const uint4 a = __ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(outs) + e));
+                const uint32_t u[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    acc[2 * i] += w * bf16_lo(u[i]);
+                    acc[2 * i + 1] += w * bf16_hi(u[i]);
+                }
+            }
+        }
+        const float inv = 1.f / tot;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] *= inv;
+    }
+    const size_t o = (size_t)row * D + c8 * 8;
+    if constexpr (OUT_F32) {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(out) + o);
+        dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+        dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    } else {
+        *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(out) + o) =
+            make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
+                       pack_bf16x2(acc[6], acc[7]));
+    }
+    if (lse_out && c8 == 0) lse_out[row] = (M > -CUDART_INF_F) ? M + logf(tot) : -CUDART_INF_F;
+}
+
+template <int D>
+static cudaError_t launch_shards_t(const void* outs, const float* lses, int n, long long rows, bool in_f32,
+                                   void* out, bool out_f32, float* lse_out, cudaStream_t s) {
+    const long long threads = rows * (D / 8);
+    const unsigned blocks = (unsigned)((threads + 255) / 256);
+    if (in_f32 && out_f32) merge_shards_kernel<D, true, true><<<blocks, 256, 0, s>>>(outs, lses, n, rows, out, lse_out);
+    else if (in_f32) merge_shards_kernel<D, true, false><<<blocks, 256, 0, s>>>(outs, lses, n, rows, out, lse_out);
+    else if (out_f32) merge_shards_kernel<D, false, true><<<blocks, 256, 0, s>>>(outs, lses, n, rows, out, lse_out);
+    else merge_shards_kernel<D, false, false><<<blocks, 256, 0, s>>>(outs, lses, n, rows, out, lse_out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_merge_shards(const void* outs, const float* lses, int n, long long rows, int head_dim, bool in_f32,
+                                void* out, bool out_f32, float* lse_out, cudaStream_t stream) {
+    switch (head_dim) {
+        case 64: return launch_shards_t<64>(outs, lses, n, rows, in_f32, out, out_f32, lse_out, stream);
+        case 128: return launch_shards_t<128>(outs, lses, n, rows, in_f32, out, out_f32, lse_out, stream);
+        case 256: return launch_shards_t<256>(outs, lses, n, rows, in_f32, out, out_f32, lse_out, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
 }  // namespace kvd

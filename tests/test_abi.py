@@ -398,6 +398,20 @@ def test_append_fp8_paged_rejects(lib):
     assert lib.kvd_kv_append_fp8_paged(*bad_page) == kvd.ERR_INVALID_ARG
 
 
+@pytest.mark.parametrize("args,expect", [
+    # (outs, lses, n_shards, rows, head_dim, in_dtype, out, out_dtype, lse_out, stream)
+    ((None, FAKE, 2, 10, 128, 1, FAKE, 0, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, 0, 10, 128, 1, FAKE, 0, None, None), kvd.ERR_INVALID_ARG),     # no shard
+    ((FAKE, FAKE, 2, -1, 128, 1, FAKE, 0, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, FAKE, 2, 10, 96, 1, FAKE, 0, None, None), kvd.ERR_UNSUPPORTED),
+    ((FAKE + 8, FAKE, 2, 10, 128, 1, FAKE, 0, None, None), kvd.ERR_INVALID_ARG),  # outs not 16-byte aligned
+    ((FAKE, FAKE, 2, 10, 128, 7, FAKE, 0, None, None), kvd.ERR_INVALID_ARG),      # bad dtype
+    ((FAKE, FAKE, 2, 0, 128, 1, FAKE, 0, None, None), kvd.OK),                    # no rows: no-op
+])
+def test_merge_attention_rejects(lib, args, expect):
+    assert lib.kvd_merge_attention(*args) == expect
+
+
 def test_decode_ex_rejects(lib):
     c = kvd._CCache(k=FAKE, v=FAKE, s_max=64)
     a = _dec_args()  # q, k, v, lens, B, S, maxlen, Hq, Hkv, D, scale, n_split, ws, ws_bytes, out, dt, lse, status, stream
