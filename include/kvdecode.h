@@ -483,14 +483,18 @@ kvd_status kvd_kernel_info(int n_heads_q, int n_heads_kv, int head_dim, kvd_out_
  * (as kvd_decode_attention returns them in out and lse_out), with
  * L = ln sum_j exp(lse_j):  out = sum_j exp(lse_j - L) out_j,  lse = L.
  * A shard with lse = -inf holds no token and adds nothing; a row with no token
- * in any shard gets a zero row and lse -inf.
+ * in any shard gets a zero row and lse -inf. A row where any shard's lse is
+ * NaN or +inf (no valid attention result) gets NaN in every column and in
+ * lse_out, so that a corrupted shard cannot pass for a plausible result.
  *   outs    : [n_shards, rows, head_dim] bf16 or fp32 (in_dtype), 16-byte aligned
  *   lses    : fp32 [n_shards, rows]
  *   out     : [rows, head_dim] (out_dtype), 16-byte aligned; lse_out: optional fp32 [rows]
  * rows is B * Hq (or B * T * Hq) of the shards' calls. The shards may come
  * from other devices (copied here first) or from separate caches on this one
- * (a shared prefix and a per-sequence suffix). Errors: KVD_ERR_INVALID_ARG for
- * NULL or misaligned pointers, n_shards < 1, rows < 0 or a bad dtype;
+ * (a shared prefix and a per-sequence suffix). The call cannot work in place:
+ * out and lse_out must overlap neither outs, lses nor each other. Errors:
+ * KVD_ERR_INVALID_ARG for NULL or misaligned pointers, overlapping written and
+ * read ranges, n_shards < 1, rows < 0 or a bad dtype;
  * KVD_ERR_UNSUPPORTED for head_dim outside {64, 128, 256}; KVD_ERR_CUDA if the
  * launch fails.
  */
@@ -548,7 +552,10 @@ kvd_status kvd_decode_step_host(void* k_cache, void* v_cache, const void* q_host
  *     and launches nothing (a smaller n_split lowers the need).
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture. The address is cached per device and
+ *     context: after the device's context is destroyed and re-created
+ *     (cudaDeviceReset), the next call looks it up again (make that call
+ *     outside stream capture as well).
  *   - All calls share the one array and it keeps the last call's contents.
  *     Nothing in it needs to start at zero, but calls that overlap on the GPU
  *     (e.g. on two streams) race on it: serialise them.

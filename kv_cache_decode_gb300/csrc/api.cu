@@ -45,6 +45,17 @@ std::atomic<uint64_t> g_smem_ready[kMaxDevices];
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// A byte range [p, p + n) of device memory; empty when n == 0.
+struct ByteRange {
+    const void* p;
+    size_t n;
+    bool overlaps(const ByteRange& o) const {
+        if (n == 0 || o.n == 0) return false;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(o.p);
+        return a < b + o.n && b < a + n;
+    }
+};
+
 kvd_status check_shape(int batch, int Hq, int Hkv, int D, kvd_out_dtype dt) {
     if (batch < 0 || Hq <= 0 || Hkv <= 0 || D <= 0) return KVD_ERR_INVALID_ARG;
     if (Hq % Hkv != 0) return KVD_ERR_INVALID_ARG;
@@ -395,6 +406,15 @@ kvd_status kvd_merge_attention(const void* outs, const float* lses, int n_shards
         return KVD_ERR_INVALID_ARG;
     if ((unsigned long long)rows * (unsigned long long)(head_dim / 8) > 0x7fffffffULL * 256ULL) return KVD_ERR_INVALID_ARG;
     if (rows == 0) return KVD_OK;
+    // The kernel reads outs and lses while it writes out and lse_out: the
+    // written ranges may overlap neither the read ones nor each other.
+    const size_t in_es = in_dtype == KVD_OUT_F32 ? 4 : 2, out_es = out_dtype == KVD_OUT_F32 ? 4 : 2;
+    const size_t n_rows = (size_t)rows, n_sh = (size_t)n_shards, d = (size_t)head_dim;
+    const ByteRange r_outs{outs, n_sh * n_rows * d * in_es}, r_lses{lses, n_sh * n_rows * 4},
+        r_out{out, n_rows * d * out_es}, r_lse{lse_out, lse_out ? n_rows * 4 : 0};
+    if (r_out.overlaps(r_outs) || r_out.overlaps(r_lses) || r_lse.overlaps(r_outs) || r_lse.overlaps(r_lses) ||
+        r_lse.overlaps(r_out))
+        return KVD_ERR_INVALID_ARG;
     return launch_merge_shards(outs, lses, n_shards, rows, head_dim, in_dtype == KVD_OUT_F32, out,
                                out_dtype == KVD_OUT_F32, lse_out, static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? KVD_OK

@@ -269,13 +269,21 @@ __global__ void __launch_bounds__(256) merge_shards_kernel(const void* __restric
     const long long row = g / VPR;
     const int c8 = (int)(g - row * VPR);
     if (row >= rows) return;
+    // A normaliser that is NaN or +inf is no shard's valid result: the row
+    // is then NaN (out and lse), rather than a plausible-looking mix of the
+    // other shards (fmaxf would skip a NaN, and +inf - +inf gives NaN weights).
     float M = -CUDART_INF_F;
-    for (int j = 0; j < n; ++j) M = fmaxf(M, __ldg(lses + (size_t)j * rows + row));
+    bool bad = false;
+    for (int j = 0; j < n; ++j) {
+        const float lj = __ldg(lses + (size_t)j * rows + row);
+        bad |= !(lj < CUDART_INF_F) && !(lj == -CUDART_INF_F);
+        M = fmaxf(M, lj);
+    }
     float acc[8];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int i = 0; i < 8; ++i) acc[i] = bad ? CUDART_NAN_F : 0.f;
     float tot = 0.f;
-    if (M > -CUDART_INF_F) {
+    if (!bad && M > -CUDART_INF_F) {
         for (int j = 0; j < n; ++j) {
             const float lj = __ldg(lses + (size_t)j * rows + row);
             if (!(lj > -CUDART_INF_F)) continue;
@@ -312,7 +320,7 @@ __global__ void __launch_bounds__(256) merge_shards_kernel(const void* __restric
             make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]),
                        pack_bf16x2(acc[6], acc[7]));
     }
-    if (lse_out && c8 == 0) lse_out[row] = (M > -CUDART_INF_F) ? M + logf(tot) : -CUDART_INF_F;
+    if (lse_out && c8 == 0) lse_out[row] = bad ? CUDART_NAN_F : (M > -CUDART_INF_F) ? M + logf(tot) : -CUDART_INF_F;
 }
 
 template <int D>

@@ -8,9 +8,10 @@
 // __device__ array of KVD_STATIC_WORKSPACE_BYTES, present on every GPU that
 // loads the library until the process exits. Inputs and outputs are still the
 // caller's.
+#include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
+#include <mutex>
 
 #include "../../include/kvdecode.h"
 
@@ -19,20 +20,59 @@ namespace {
 static __device__ __align__(256) unsigned char g_static_workspace[KVD_STATIC_WORKSPACE_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::atomic<void*> g_static_workspace_addr[kMaxDevices];
+
+// The array's device address, per device, with the context it was looked up
+// in: the module (and so the array) is loaded again, possibly elsewhere, when
+// a device's primary context is destroyed and re-created (cudaDeviceReset), so
+// the cached address is used only while the same context (by its unique id) is
+// current.
+struct CachedAddress {
+    std::mutex m;
+    unsigned long long ctx_id = 0;
+    void* addr = nullptr;
+};
+CachedAddress g_static_workspace_addr[kMaxDevices];
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+template <class F>
+F driver_fn(const char* name) {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+        return nullptr;
+    return reinterpret_cast<F>(f);
+}
+
+// Unique id of the current context (0 if none is current or it cannot be read).
+unsigned long long current_ctx_id() {
+    static const CtxGetCurrentFn get = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+    static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get || !get_id || get(&ctx) != CUDA_SUCCESS || ctx == nullptr || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 // In host code g_static_workspace names a host-side stand-in, not device
-// memory: its device address is looked up once per device, with that device
-// current, and cached.
+// memory: its device address is looked up with the device current, once per
+// device and context, and cached.
 kvd_status static_workspace_address(void** addr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVD_ERR_CUDA;
-    void* p = g_static_workspace_addr[dev].load(std::memory_order_acquire);
-    if (p == nullptr) {
+    CachedAddress& c = g_static_workspace_addr[dev];
+    std::lock_guard<std::mutex> lock(c.m);
+    const unsigned long long id = current_ctx_id();
+    if (c.addr == nullptr || id == 0 || c.ctx_id != id) {
+        // The lookup also makes the device's primary context current if none was.
+        void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_static_workspace) != cudaSuccess || p == nullptr) return KVD_ERR_CUDA;
-        g_static_workspace_addr[dev].store(p, std::memory_order_release);
+        c.addr = p;
+        c.ctx_id = current_ctx_id();
     }
-    *addr = p;
+    *addr = c.addr;
     return KVD_OK;
 }
 

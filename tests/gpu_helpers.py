@@ -2,6 +2,9 @@
 ABI and compare it with the CPU oracle."""
 from __future__ import annotations
 
+import json
+import os
+
 import numpy as np
 import pytest
 
@@ -124,20 +127,102 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return np.exp2(np.floor(np.log2(ax)) - 7)
 
 
-def assert_close(got: np.ndarray, ref: np.ndarray, out_dtype: str, what: str = ""):
-    """bf16 output: max-abs error 1e-2, except where one bf16 step at the
-    reference's magnitude is itself above 1e-2 (|ref| >= 2), where one bf16
-    ulp is allowed. fp32 output: max-abs error 1e-4 everywhere."""
+#: bf16 unit roundoff: a weight rounded to bf16 (round to nearest even) carries
+#: a relative error of at most 2^-9.
+BF16_U = 2.0 ** -9
+#: Slack for the float32 parts of the kernels (scores, exponentials, sums),
+#: the level the fp32-output mode is held to everywhere.
+F32_SLACK = 1e-4
+
+#: One record per assert_close call: what was compared and how many bf16
+#: elements needed the rounding allowance above 1e-2.
+PARITY_LOG = []
+
+
+def weight_rounding_bound(spread: np.ndarray) -> np.ndarray:
+    """Bound on what rounding the softmax weights to bf16 moves an output.
+
+    With exact weights w_t and rounded ones w_t (1 + d_t), |d_t| <= u, the
+    normalised output moves by sum_t (w'_t - w_t)(v_t - out), and
+    |w'_t - w_t| <= w_t * 2u / (1 - u); so the move is at most
+    2u / (1 - u) * sum_t w_t |v_t - out| = that factor times ``spread``."""
+    return 2.0 * BF16_U / (1.0 - BF16_U) * spread
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, out_dtype: str, what: str = "", spread=None):
+    """Compare a GPU result with the oracle's.
+
+    fp32 output: max-abs error 1e-4 everywhere.
+    bf16 output: max-abs error 1e-2. An element above 1e-2 is accepted only
+    if its error is within what the kernels' bf16 roundings can produce: half
+    a bf16 step at its magnitude (the output's own rounding), plus the bound
+    on the weights' rounding to bf16 (``weight_rounding_bound``), plus the
+    fp32 slack. ``spread(flat_indices)`` gives sum_t w_t |v_t - ref| for those
+    elements (exact weights); without it the weight term is taken as zero.
+    The number of elements that needed the allowance and their largest |ref|
+    are recorded (``PARITY_LOG``; also appended as JSON lines to the file
+    named by KVD_PARITY_LOG, if set)."""
     assert got.shape == ref.shape
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     err = np.abs(got - ref)
+    rec = {"what": what, "dtype": out_dtype, "n": int(err.size), "max_err": float(err.max(initial=0.0))}
     if out_dtype == "bf16":
-        tol = np.maximum(1e-2, bf16_ulp(ref))
+        over = np.flatnonzero(err.ravel() > 1e-2)
+        tol = np.full(err.shape, 1e-2)
+        if over.size:
+            r = ref.ravel()[over]
+            mag = np.maximum(np.abs(r), np.abs(got.ravel()[over]))
+            allow = 0.5 * bf16_ulp(mag) + F32_SLACK
+            if spread is not None:
+                allow = allow + weight_rounding_bound(np.asarray(spread(over), np.float64))
+            tol.ravel()[over] = np.maximum(1e-2, allow)
+        rec["n_over_1e-2"] = int(over.size)
+        rec["max_abs_ref_over"] = float(np.abs(ref.ravel()[over]).max(initial=0.0))
     else:
         tol = np.full_like(ref, 1e-4)
+        rec["n_over_1e-2"] = 0
     bad = err > tol
+    rec["n_bad"] = int(bad.sum())
+    PARITY_LOG.append(rec)
+    path = os.environ.get("KVD_PARITY_LOG")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(rec) + "\n")
     if bad.any():
         i = np.unravel_index(np.argmax(err - tol), err.shape)
         raise AssertionError(f"{what}: {int(bad.sum())} elements out of tolerance; worst at {i}: "
                              f"got {got[i]!r} ref {ref[i]!r} err {err[i]:.3e} tol {tol[i]:.3e}")
     return float(err.max(initial=0.0))
+
+
+def spread_step(inp: StepInputs, rows=None, lens=None):
+    """``spread`` for assert_close over oracle_step(inp, rows, lens): for the
+    flat indices of elements (row i, query head h, column d) of the [rows, Hq,
+    D] output, sum_t w_t |v_t[d] - ref| with the oracle's exact weights of
+    (rows[i], h) over the post-append cache."""
+    rows = np.arange(inp.q.shape[0]) if rows is None else np.asarray(rows)
+    L_all = inp.seq_lens if lens is None else np.asarray(lens, np.int32)
+    _, Hq, D = inp.q.shape
+    Hkv = inp.k_cache.shape[2]
+    G = Hq // Hkv
+    ref_cache = {}
+
+    def fn(flat):
+        out = np.empty(len(flat))
+        for j, f in enumerate(flat):
+            i, rem = divmod(int(f), Hq * D)
+            h, d = divmod(rem, D)
+            b = int(rows[i])
+            key = (b, h)
+            if key not in ref_cache:
+                L = int(L_all[b])
+                kc = inp.k_cache[b:b + 1].copy()
+                vc = inp.v_cache[b:b + 1].copy()
+                kc, vc, _ = oracle.kv_append(kc, vc, inp.k_new[b:b + 1], inp.v_new[b:b + 1], inp.pos[b:b + 1])
+                w = oracle.attention_weights(inp.q[b:b + 1], kc, np.array([L], np.int32), inp.workload.scale, 0, h)
+                v = bf16_bits_to_f32(vc[0, :L, h // G, :]).astype(np.float64)
+                ref_cache[key] = (w, v, w @ v)
+            w, v, o = ref_cache[key]
+            out[j] = float(w @ np.abs(v[:, d] - o[d]))
+        return out
+    return fn

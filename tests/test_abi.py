@@ -407,6 +407,14 @@ def test_append_fp8_paged_rejects(lib):
     ((FAKE + 8, FAKE, 2, 10, 128, 1, FAKE, 0, None, None), kvd.ERR_INVALID_ARG),  # outs not 16-byte aligned
     ((FAKE, FAKE, 2, 10, 128, 7, FAKE, 0, None, None), kvd.ERR_INVALID_ARG),      # bad dtype
     ((FAKE, FAKE, 2, 0, 128, 1, FAKE, 0, None, None), kvd.OK),                    # no rows: no-op
+    # written ranges overlapping read ones (in place), or each other; outs
+    # [2, 10, 128] fp32 is 10240 bytes, out [10, 128] bf16 2560
+    ((FAKE, FAKE + (1 << 24), 2, 10, 128, 1, FAKE, 0, None, None), kvd.ERR_INVALID_ARG),         # out = outs[0]
+    ((FAKE, FAKE + (1 << 24), 2, 10, 128, 1, FAKE + 5120, 0, None, None), kvd.ERR_INVALID_ARG),  # out = outs[1]
+    ((FAKE, FAKE + (1 << 24), 2, 10, 128, 1, FAKE + (2 << 24), 0, FAKE + (1 << 24), None),
+     kvd.ERR_INVALID_ARG),                                                                       # lse_out = lses[0]
+    ((FAKE, FAKE + (1 << 24), 2, 10, 128, 1, FAKE + (2 << 24), 0, FAKE + (2 << 24) + 2048, None),
+     kvd.ERR_INVALID_ARG),                                                                       # lse_out inside out
 ])
 def test_merge_attention_rejects(lib, args, expect):
     assert lib.kvd_merge_attention(*args) == expect

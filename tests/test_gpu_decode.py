@@ -1,8 +1,9 @@
 """Decode attention on the GPU against the CPU oracle.
 
 * The five workloads at full size, in the launch configuration the benchmark
-  uses (heuristic split), with the oracle computing a sample of whole
-  sequences (every head) one by one.
+  uses (heuristic split), every sequence and every head compared with the
+  oracle; all 16 ragged long-context trials on their longest and shortest
+  sequences.
 * Random small shapes spanning several tiles and a ragged tail, every
   supported head dimension and a range of group sizes, with forced split
   counts 1, 2, 3, 7 and more CTAs than tokens.
@@ -10,8 +11,10 @@
   NaN-filled cache padding (any read past a sequence's end poisons the
   output), guard bands around the outputs and the workspace, and bitwise
   determinism across runs.
-Tolerances: bf16 output within 1e-2 (one bf16 step where that step exceeds
-1e-2); fp32 output within 1e-4. The natural-log normaliser lse within 1e-4 in
+Tolerances: bf16 output within 1e-2; an element above it must lie within half
+a bf16 step at its magnitude plus the bound on the bf16 weights' rounding
+(gpu_helpers.assert_close), and the count of such elements is recorded; fp32
+output within 1e-4. The natural-log normaliser lse within 1e-4 in
 fp32 mode; in bf16 mode the normaliser sums the bf16-rounded weights (the ones
 multiplied into V, so that the output stays an exact convex combination of V
 rows), which carry up to 2^-9 relative rounding each, so lse is held to 2^-8.
@@ -20,7 +23,7 @@ import numpy as np
 import pytest
 
 import workloads
-from gpu_helpers import assert_close, cuda_or_skip, oracle_step, run_step
+from gpu_helpers import assert_close, cuda_or_skip, oracle_step, run_step, spread_step
 
 pytestmark = pytest.mark.gpu
 
@@ -34,7 +37,7 @@ def _check(inp, r, out_dtype, rows=None, what=""):
     ref, ref_lse = oracle_step(inp, rows)
     got = r.out if rows is None else r.out[np.asarray(rows)]
     lse = r.lse if rows is None else r.lse[np.asarray(rows)]
-    err = assert_close(got, ref, out_dtype, what)
+    err = assert_close(got, ref, out_dtype, what, spread=spread_step(inp, rows))
     fin = np.isfinite(ref_lse)
     assert np.array_equal(np.isfinite(lse), fin), what
     lse_tol = 1e-4 if out_dtype == "f32" else 2.0 ** -8
@@ -48,14 +51,6 @@ def _check(inp, r, out_dtype, rows=None, what=""):
 # ---------------------------------------------------------------------------
 # Full-size workloads
 # ---------------------------------------------------------------------------
-
-_SAMPLE_ROWS = {
-    "palm": lambda L: [0, 31, 63],
-    "mha": lambda L: sorted({int(np.argmin(L)), int(np.argmax(L)), 5}),
-    "gqa": lambda L: sorted({int(np.argmin(L)), int(np.argmax(L)), 17, 100}),
-    "long": lambda L: [2],
-}
-
 
 @pytest.fixture(scope="module")
 def full_inputs():
@@ -75,11 +70,10 @@ def test_workload_full_size(dev, full_inputs, name, out_dtype):
     inp = full_inputs(name)
     r = run_step(inp, dev, out_dtype)
     assert r.status == 0
-    rows = None if name == "tiny" else _SAMPLE_ROWS[name](inp.seq_lens)
-    _check(inp, r, out_dtype, rows, f"{name}/{out_dtype}/n_split={r.n_split}")
+    _check(inp, r, out_dtype, None, f"{name}/{out_dtype}/n_split={r.n_split}")
 
 
-@pytest.mark.parametrize("trial", [0, 7])
+@pytest.mark.parametrize("trial", range(16))
 def test_long_ragged_trial(dev, trial):
     w = workloads.long_trial(trial)
     inp = workloads.step_inputs(w)

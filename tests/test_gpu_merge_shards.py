@@ -52,3 +52,29 @@ def test_shards_merge_to_the_whole(Hq, Hkv, D, dt):
     so = (bf16_bits_to_f32(bf16_tensor_bits(outs)) if dt == "bf16" else outs.cpu().numpy()).astype(np.float64)
     mo, _ = oracle.merge_attention(so, lses.cpu().numpy())
     assert np.max(np.abs(got - mo)) < (1e-2 if dt == "bf16" else 1e-5)
+
+
+@pytest.mark.parametrize("bad", [float("nan"), float("inf")], ids=["nan", "inf"])
+def test_invalid_shard_normaliser_gives_nan_row(bad):
+    """A shard whose normaliser is NaN or +inf is no valid result: its row comes
+    out NaN (every column and lse) instead of a mix of the other shards; the
+    other rows are untouched by it."""
+    import torch
+    import kv_cache_decode_gb300 as kvd
+    dev = cuda_or_skip()
+    n, rows, D = 3, 5, 128
+    g = torch.Generator().manual_seed(7)
+    outs = torch.randn((n, rows, D), generator=g).to(dev)
+    lses = torch.randn((n, rows), generator=g).to(dev)
+    lses[1, 2] = bad
+    out = torch.zeros((rows, D), dtype=torch.float32, device=dev)
+    lse = torch.zeros((rows,), dtype=torch.float32, device=dev)
+    kvd.merge_attention(outs, lses, out, lse=lse)
+    torch.cuda.synchronize()
+    o, l = out.cpu().numpy(), lse.cpu().numpy()
+    assert np.all(np.isnan(o[2])) and np.isnan(l[2])
+    good = [r for r in range(rows) if r != 2]
+    want, want_lse = oracle.merge_attention(outs.cpu().numpy().astype(np.float64)[:, good],
+                                            lses.cpu().numpy().astype(np.float64)[:, good])
+    assert np.max(np.abs(o[good] - want)) < 1e-5
+    assert np.max(np.abs(l[good] - want_lse)) < 1e-5

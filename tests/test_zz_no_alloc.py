@@ -5,9 +5,10 @@ serving loop with a frozen memory budget, a plugin handed only its tensors, a
 path that must not risk the synchronisation cudaMalloc can cause): it uses a
 scratch array compiled into the library instead of a caller workspace.
 
-Checked through the C ABI against kvd_decode_attention (same tolerance as the
-other parity tests), on two calls in a row, since the shared array keeps the
-previous call's contents. Kept in a file of its own that pytest collects last.
+Checked through the C ABI against kvd_decode_attention and against the CPU
+oracle (same tolerances as the other parity tests), on two calls in a row,
+since the shared array keeps the previous call's contents. Kept in a file of
+its own that pytest collects last.
 """
 import ctypes
 
@@ -15,7 +16,7 @@ import numpy as np
 import pytest
 
 import workloads
-from gpu_helpers import assert_close, bf16_tensor_bits, cuda_or_skip, to_dev_bf16
+from gpu_helpers import assert_close, bf16_tensor_bits, cuda_or_skip, oracle_step, spread_step, to_dev_bf16
 from workloads import bf16_bits_to_f32
 
 pytestmark = pytest.mark.gpu
@@ -53,6 +54,7 @@ def test_static_entry_point_matches_workspace_entry_point(case, out_dtype):
     torch.cuda.synchronize()
     ref_h = _host(ref, out_dtype)
 
+    want, _ = oracle_step(inp)
     lib = kvd.load()
     code = kvd.OUT_BF16 if out_dtype == "bf16" else kvd.OUT_F32
     for call in range(2):
@@ -65,7 +67,9 @@ def test_static_entry_point_matches_workspace_entry_point(case, out_dtype):
         assert rc == kvd.OK, kvd.status_string(rc)
         torch.cuda.synchronize()
         assert status.item() == 0
-        assert_close(_host(out, out_dtype), ref_h, out_dtype, f"{name} static call {call}")
+        got = _host(out, out_dtype)
+        assert_close(got, ref_h, out_dtype, f"{name} static call {call}")
+        assert_close(got, want, out_dtype, f"{name} static call {call} vs oracle", spread=spread_step(inp))
 
 
 def test_static_entry_point_rejects_oversized_workspace():
