@@ -69,6 +69,10 @@ def parse_args():
     ap.add_argument("--phi", type=float, default=0.0, help="the unified maximum, in logit units")
     ap.add_argument("--page-order", default="shuffled", choices=["shuffled", "sequential"],
                     help="paged: pages in random order over the pool, or each sequence's pages in a row")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip timing the other workloads (tiny, mha, gqa, long, the 16 long trials)")
+    ap.add_argument("--probe", choices=["read"], default=None,
+                    help="read: only run the read-only streaming probe over a range of sizes")
     return ap.parse_args()
 
 
@@ -215,33 +219,52 @@ def oracle_rate(w, inp, budget_s: float, repeats: int = 1, min_total_s: float = 
     return nbytes / sec / 1e9, sec, n, cores, len(times)
 
 
+def bench_config(w, B, Hq, Hkv, D, lens_np, args) -> dict:
+    """The workload and run options, identical in both arms' lines."""
+    return {"workload": w.name, "description": w.description, "batch": B, "n_heads_q": Hq,
+            "n_heads_kv": Hkv, "head_dim": D, "context": [int(lens_np.min()), int(lens_np.max())],
+            "out_dtype": args.out_dtype, "parallelism": f"replicas x{args.gpus}",
+            "l2_flush": "K/V rows read from HBM every step: rotating cache copies totalling >= 3x L2",
+            "kv_layout": (f"paged: {args.page_size}-token pages in {args.page_order} order" if args.page_size
+                          else "contiguous"),
+            "kv_dtype": args.kv_dtype, "query_tokens": args.tokens,
+            "softmax": f"unified max, phi {args.phi}" if args.softmax == "unified" else "online max"}
+
+
 def run_reference(args):
+    """The reference arm: the float64 CPU oracle, as it stands, on the host's
+    cores, over the whole batch of the workload every step."""
     rank, _, _ = dist_env()
     if rank != 0:
         return
+    import oracle
+    oracle.build()
+    cores = oracle.max_threads()
     w = workloads.get(args.config)
-    # the oracle only needs the sampled rows; generate a handful of sequences
-    B_sample = min(w.B, 8)
-    inp = workloads.step_inputs(w, batch_index=range(B_sample), pad_bits=0)
-    per_step = min(10.0, 150.0 / max(1, args.steps + args.warmup))
-    gbs_list = []
-    n_rows = cores = 0
+    if args.batch:
+        w = w.with_batch(min(args.batch, w.B))
+    inp = workloads.step_inputs(w, pad_bits=0)
+    kc, vc, _ = oracle.kv_append(inp.k_cache, inp.v_cache, inp.k_new, inp.v_new, inp.pos)
+    times = []
     for i in range(args.warmup + args.steps):
-        gbs, sec, n_rows, cores, _ = oracle_rate(w, inp, per_step)
+        t = time.perf_counter()
+        oracle.decode_attention(inp.q, kc, vc, inp.seq_lens, w.scale)
         if i >= args.warmup:
-            gbs_list.append(gbs)
-    value = statistics.median(gbs_list)
-    step_bytes_full = roofline.attention_step_bytes(workloads.seq_lens(w), w.Hq, w.Hkv, w.D)
-    ms = step_bytes_full / (value * 1e9) * 1e3
+            times.append(time.perf_counter() - t)
+    sec = sum(times) / len(times)
+    step_bytes = roofline.attention_step_bytes(inp.seq_lens, w.Hq, w.Hkv, w.D)
+    value = step_bytes / sec / 1e9
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
-        "ms_per_step": round(ms, 3), "higher_is_better": True, "scaling": "weak",
+        "ms_per_step": round(sec * 1e3, 3), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "description": w.description, "batch": w.B,
-                   "n_heads_q": w.Hq, "n_heads_kv": w.Hkv, "head_dim": w.D},
+        "config": bench_config(w, w.B, w.Hq, w.Hkv, w.D, inp.seq_lens, args),
+        "tokens_per_s": round(w.B / sec, 2),
+        "timing": "wall clock (perf_counter) around each oracle pass over the whole batch",
         "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"{n_rows} of {w.B} sequences per step (all heads), float64 C oracle"},
+                         "sample": f"all {w.B} sequences (all heads) per step, float64 C oracle, "
+                                   f"mean of {len(times)} passes"},
         "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -250,6 +273,196 @@ def run_reference(args):
 # ---------------------------------------------------------------------------
 # Our arm
 # ---------------------------------------------------------------------------
+
+def rotation_count(kv_bytes: int, cache_bytes: int, l2: int) -> int:
+    """Cache copies to rotate through so that a step's K/V rows are not
+    L2-resident: together at least 3x L2, at most 16 copies or 40 GB."""
+    R = max(1, math.ceil(3 * l2 / max(kv_bytes, 1)))
+    return max(1, min(R, int(40e9 // max(cache_bytes, 1)), 16))
+
+
+def time_replays(graphs, steps: int, warmup: int) -> float:
+    """Milliseconds per step of `steps` graph replays (round-robin over
+    `graphs`), queued behind a spin kernel so the GPU never waits for the host,
+    between CUDA events on the replay stream."""
+    import torch
+    for i in range(warmup):
+        graphs[i % len(graphs)].replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(int(2e6 + 2e5 * steps))
+    e0.record()
+    for i in range(steps):
+        graphs[i % len(graphs)].replay()
+    e1.record()
+    e1.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def isolated_replay_us(graph, reps: int) -> float:
+    """Median device time of one graph replay with the GPU otherwise idle
+    (the step's latency rather than its throughput), in microseconds."""
+    import torch
+    times = []
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record()
+        graph.replay()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b) * 1e3)
+    return statistics.median(times)
+
+
+def capture(fn, dev):
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=torch.cuda.Stream(device=dev)):
+        fn()
+    return g
+
+
+def read_probe(kvd, dev, nbytes: int, l2: int, reps: int = 20) -> dict:
+    """One read-only streaming pass over nbytes (kvd_probe_read), buffers
+    rotated so the bytes come from HBM: median device time and GB/s."""
+    import torch
+    R = rotation_count(nbytes, nbytes, l2)
+    bufs = [torch.ones(nbytes // 2, dtype=torch.bfloat16, device=dev) for _ in range(R)]
+    sink = torch.zeros(1024, dtype=torch.int64, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    for i in range(3 * R):
+        kvd.probe_read(bufs[i % R], sink=sink, status=status)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    torch.cuda._sleep(int(2e6 + 2e5 * reps))
+    for i, (a, b) in enumerate(ev):
+        a.record()
+        kvd.probe_read(bufs[i % R], sink=sink, status=status)
+        b.record()
+    torch.cuda.synchronize()
+    us = statistics.median(a.elapsed_time(b) * 1e3 for a, b in ev)
+    if int(status.item()) != 0:
+        raise RuntimeError("read probe: a copy wait timed out")
+    del bufs
+    torch.cuda.empty_cache()
+    return {"bytes": int(nbytes), "us": round(us, 3), "gbs": round(nbytes / (us * 1e-6) / 1e9, 1),
+            "copies_rotated": R}
+
+
+def measure_shape(kvd, dev, w, steps: int, warmup: int, l2: int, peak: float, latency: bool = False) -> dict:
+    """One workload's bf16 decode step (kvd_decode_step: append + attention),
+    measured as the headline workload is: CUDA graphs over rotating cache
+    copies, step time and the chunk kernel's time from CUDA events."""
+    import torch
+    inp = workloads.step_inputs(w, pad_bits=0)
+    B, Hq, D = inp.q.shape
+    S, Hkv = inp.k_cache.shape[1], inp.k_cache.shape[2]
+    lens_np = inp.seq_lens.copy()
+    step_bytes = roofline.attention_step_bytes(lens_np, Hq, Hkv, D)
+    kv_bytes = roofline.attention_kv_bytes(lens_np, Hkv, D)
+    R = rotation_count(kv_bytes, 2 * inp.k_cache.nbytes, l2)
+
+    def up(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).to(dev).view(torch.bfloat16)
+
+    kcs, vcs = [up(inp.k_cache)], [up(inp.v_cache)]
+    for _ in range(R - 1):
+        kcs.append(kcs[0].clone())
+        vcs.append(vcs[0].clone())
+    q, kn, vn = up(inp.q), up(inp.k_new), up(inp.v_new)
+    pos, lens = torch.from_numpy(inp.pos).to(dev), torch.from_numpy(lens_np).to(dev)
+    del inp
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    n_split, ws_bytes = kvd.decode_plan(B, Hq, Hkv, D, S)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    step = lambda r: kvd.decode_step(q, kcs[r], vcs[r], kn, vn, pos, lens, S, w.scale, out, workspace=ws)
+    for i in range(3 * R):
+        step(i % R)
+    torch.cuda.synchronize()
+    graphs = [capture(lambda r=r: step(r), dev) for r in range(R)]
+    res = {"batch": B, "n_heads_q": Hq, "n_heads_kv": Hkv, "head_dim": D,
+           "context": [int(lens_np.min()), int(lens_np.max())], "n_split": n_split, "step_bytes": int(step_bytes)}
+    if latency:
+        res["latency_us"] = round(isolated_replay_us(graphs[0], 50), 3)
+    ms = time_replays(graphs, steps, warmup)
+    chunk_ms = time_chunk(kvd, lambda r: (kcs[r], vcs[r]), R, steps, q, kn, vn, pos, lens, S, w.scale, out, ws)
+    gbs = step_bytes / (ms * 1e-3) / 1e9
+    achieved = step_bytes / (chunk_ms * 1e-3) / 1e9
+    res.update({"ms_per_step": round(ms, 5), "gbs": round(gbs, 1), "hbm_frac_of_step": round(gbs / peak, 4),
+                "tokens_per_s": round(B / (ms * 1e-3), 1), "kernel_ms": round(chunk_ms, 5),
+                "roofline_frac": round(achieved / peak, 4), "copies_rotated": R})
+    del kcs, vcs, graphs
+    torch.cuda.empty_cache()
+    return res
+
+
+def time_chunk(kvd, cache, R, steps, q, kn, vn, pos, lens, max_len, scale, out, ws, n_split=0) -> float:
+    """Mean duration of the split-KV chunk kernel's launches (CUDA events on
+    its stream, around each launch, after each step's append)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    ea = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    eb = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda._sleep(int(2e6 + 2e5 * steps))
+    for i in range(steps):
+        kc, vc = cache(i % R)
+        kvd.kv_append(kc, vc, kn, vn, pos)
+        ea[i].record(stream)
+        kvd.split_kv_chunk(q, kc, vc, lens, max_len, scale, out, workspace=ws, n_split=n_split)
+        eb[i].record(stream)
+        kvd.split_kv_merge(q, kc, vc, lens, max_len, scale, out, workspace=ws, n_split=n_split)
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in zip(ea, eb))
+
+
+def measure_long_trials(kvd, dev, steps: int, warmup: int, l2: int, peak: float) -> dict:
+    """The 16 ragged long-context trials (lengths U[1, 131072] per trial): one
+    step graph per cache copy, replayed with each trial's lengths. The K/V
+    values do not change the work, so one seeded N(0, 1) cache drawn on the
+    GPU serves every trial."""
+    import torch
+    w0 = workloads.long_trial(0)
+    B, Hq, Hkv, D, S = w0.B, w0.Hq, w0.Hkv, w0.D, w0.S_max
+    g = torch.Generator(device=dev)
+    g.manual_seed(w0.seed)
+    rnd = lambda *shape: torch.randn(shape, generator=g, device=dev, dtype=torch.float32).to(torch.bfloat16)
+    kc0, vc0 = rnd(B, S, Hkv, D), rnd(B, S, Hkv, D)
+    R = rotation_count(B * S * Hkv * D * 4 // 2, 2 * kc0.numel() * 2, l2)
+    kcs, vcs = [kc0] + [kc0.clone() for _ in range(R - 1)], [vc0] + [vc0.clone() for _ in range(R - 1)]
+    q, kn, vn = rnd(B, Hq, D), rnd(B, Hkv, D), rnd(B, Hkv, D)
+    lens = torch.zeros(B, dtype=torch.int32, device=dev)
+    pos = torch.zeros(B, dtype=torch.int32, device=dev)
+    out = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    n_split, ws_bytes = kvd.decode_plan(B, Hq, Hkv, D, S)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    step = lambda r: kvd.decode_step(q, kcs[r], vcs[r], kn, vn, pos, lens, S, w0.scale, out, workspace=ws)
+    trials = []
+    graphs = None
+    for i in range(16):
+        L = workloads.seq_lens(workloads.long_trial(i))
+        lens.copy_(torch.from_numpy(L))
+        pos.copy_(torch.from_numpy(np.maximum(L - 1, 0).astype(np.int32)))
+        torch.cuda.synchronize()
+        if graphs is None:
+            for j in range(3 * R):
+                step(j % R)
+            torch.cuda.synchronize()
+            graphs = [capture(lambda r=r: step(r), dev) for r in range(R)]
+        ms = time_replays(graphs, steps, warmup)
+        nbytes = roofline.attention_step_bytes(L, Hq, Hkv, D)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        trials.append({"trial": i, "tokens": int(L.sum()), "ms_per_step": round(ms, 5), "gbs": round(gbs, 1),
+                       "hbm_frac_of_step": round(gbs / peak, 4)})
+    del kcs, vcs, graphs
+    torch.cuda.empty_cache()
+    fr = [t["hbm_frac_of_step"] for t in trials]
+    return {"n_split": n_split, "trials": trials, "hbm_frac_of_step_median": round(statistics.median(fr), 4),
+            "hbm_frac_of_step_min": min(fr), "hbm_frac_of_step_max": max(fr),
+            "values": "one N(0,1) cache drawn on the GPU (torch generator, seed 500); each trial's own lengths"}
+
 
 def run_ours(args):
     import torch
@@ -262,6 +475,7 @@ def run_ours(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
+    peak_est, _ = measured_peaks()
     from kv_cache_decode_gb300 import _build
     _build.build()
     kvd.load()
@@ -475,7 +689,7 @@ def run_ours(args):
             bf = lambda t: t.view(torch.bfloat16)
             # the step's inputs in one pinned packet laid out like the device staging buffer: one copy in
             staging = torch.empty(kvd.step_staging_bytes(B, T, Hq, Hkv, D), dtype=torch.uint8, device=dev)
-            _, pq, pkn, pvn, ppos, plens = kvd.alloc_host_packet(B, T, Hq, Hkv, D)
+            packet, pq, pkn, pvn, ppos, plens = kvd.alloc_host_packet(B, T, Hq, Hkv, D)
             for dst, src in ((pq, bf(q_h)), (pkn, bf(kn_h)), (pvn, bf(vn_h)), (ppos, pos_h), (plens, lens_h)):
                 dst.copy_(src)
             # out=None: the kernels write the result straight into the pinned out_h
@@ -513,7 +727,31 @@ def run_ours(args):
         e2e_ms, = max_over_ranks([e2e_ms], device=dev)
         e2e = {"value": round(job_rate_gbs(world, step_bytes, e2e_ms), 2), "unit": UNIT,
                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "ms_per_step": round(e2e_ms, 4), "tokens_per_s": round(world * B * T / (e2e_ms * 1e-3), 1)}
+               "ms_per_step": round(e2e_ms, 4), "tokens_per_s": round(world * B * T / (e2e_ms * 1e-3), 1),
+               "api": ("kvd_decode_step_host per step (inputs in one pinned packet, one copy in; the kernels "
+                       "write the result into pinned host memory)" if host_steps is not None else
+                       "torch copies in, the step call, a copy back, per step")}
+        if host_steps is not None:
+            # Where the time goes: the packet's copy in alone, the device step
+            # alone (ms_per_step above), and the same host step captured once
+            # per cache copy in a CUDA graph (copy-in node, kernels writing the
+            # result to host memory) and replayed: no per-step launch cost.
+            hs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * 20)]
+            for i in range(20):
+                torch.cuda.synchronize()
+                hs[2 * i].record()
+                staging.copy_(packet, non_blocking=True)
+                hs[2 * i + 1].record()
+            torch.cuda.synchronize()
+            h2d_us = statistics.median(hs[2 * i].elapsed_time(hs[2 * i + 1]) * 1e3 for i in range(20))
+            host_graphs = [capture(host_steps[r], dev) for r in range(R)]
+            g_ms = time_replays(host_graphs, args.steps, args.warmup)
+            g_ms, = max_over_ranks([g_ms], device=dev)
+            e2e["breakdown"] = {"h2d_copy_us": round(h2d_us, 2), "device_step_us": round(ms_per_step * 1e3, 2),
+                                "api_call_us": round(e2e_ms * 1e3, 2),
+                                "graph_replay_us": round(g_ms * 1e3, 2),
+                                "graph_replay_gbs": round(job_rate_gbs(world, step_bytes, g_ms), 2)}
+            del host_graphs
 
     if rank != 0:
         return
@@ -529,21 +767,28 @@ def run_ours(args):
                "sample": f"{n_rows} of {B} sequences (all heads), float64 C oracle, "
                          f"median of {passes} passes of {sec:.3f} s"}
 
+    # ---- the other workloads, the same way (default run only) ----
+    per_config = None
+    default_run = (w.name == "palm" and not (paged or int8 or multi or umax or args.batch or args.n_split)
+                   and args.out_dtype == "bf16" and world == 1)
+    probes = None
+    if default_run and not args.no_per_config:
+        per_config = {}
+        for name in ("tiny", "mha", "gqa", "long"):
+            per_config[name] = measure_shape(kvd, dev, workloads.get(name), min(args.steps, 20),
+                                             max(args.warmup, 3), l2, peak_est, latency=(name == "tiny"))
+        per_config["long_trials"] = measure_long_trials(kvd, dev, 10, 3, l2, peak_est)
+        probes = [read_probe(kvd, dev, kv_bytes, l2), read_probe(kvd, dev, 2 << 30, l2)]
+
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": w.name, "description": w.description, "batch": B, "n_heads_q": Hq,
-                   "n_heads_kv": Hkv, "head_dim": D, "context": [int(lens_np.min()), int(lens_np.max())],
-                   "out_dtype": args.out_dtype, "n_split": n_split, "parallelism": f"replicas x{world}",
-                   "l2_flush": f"{R} rotating KV-cache copies ({R * kv_bytes / 1e6:.0f} MB of K/V rows "
-                               f"vs {l2 / 1e6:.0f} MB L2)",
-                   "timing": "CUDA graph per step, CUDA events on the replay stream",
-                   "kv_layout": (f"paged: {args.page_size}-token pages, {pinp.k_pages.shape[0]} pages "
-                                 f"in {args.page_order} order" if paged else "contiguous"),
-                   "kv_dtype": args.kv_dtype, "query_tokens": T,
-                   "softmax": f"unified max, phi {args.phi}" if umax else "online max"},
+        "config": bench_config(w, B, Hq, Hkv, D, lens_np, args),
+        "n_split": n_split,
+        "l2_detail": f"{R} rotating KV-cache copies ({R * kv_bytes / 1e6:.0f} MB of K/V rows vs {l2 / 1e6:.0f} MB L2)",
+        "timing": "CUDA graph per step, CUDA events on the replay stream",
         "tokens_per_s": round(tokens_per_s, 1),
         "hbm_frac_of_step": round(value / world / peak, 4),
         "step_bytes": int(step_bytes), "append_bytes": int(append_bytes), "flops": int(flops),
@@ -558,13 +803,43 @@ def run_ours(args):
         "clocks": clocks,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "per_config": per_config,
+        "read_probe": probes,
         "impl": "ours",
     }
     print(json.dumps(line), flush=True)
 
 
+def run_probe(args):
+    """--probe read: the read-only streaming probe alone, over the workloads'
+    K/V byte counts and a few larger buffers; one JSON line."""
+    import torch
+
+    import kv_cache_decode_gb300 as kvd
+    from kv_cache_decode_gb300 import _build
+    _build.build()
+    kvd.load()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 126 * 2**20))
+    sizes = {name: roofline.attention_kv_bytes(workloads.seq_lens(workloads.get(name)), workloads.get(name).Hkv,
+                                               workloads.get(name).D) for name in ("palm", "long", "mha", "gqa")}
+    sizes.update({"512MiB": 512 << 20, "2GiB": 2 << 30, "8GiB": 8 << 30})
+    peak, kind = measured_peaks()
+    res = {}
+    for name, n in sizes.items():
+        r = read_probe(kvd, dev, int(n) // 16 * 16, l2)
+        r["frac_of_copy_peak"] = round(r["gbs"] / peak, 4)
+        res[name] = r
+    print(json.dumps({"probe": "read", "unit": "GB/s", "copy_peak": peak, "peak_source": kind, "results": res}),
+          flush=True)
+
+
 def main():
     args = parse_args()
+    if args.probe:
+        run_probe(args)
+        return
     if args.impl == "reference":
         run_reference(args)
     else:

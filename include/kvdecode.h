@@ -568,6 +568,26 @@ kvd_status kvd_decode_attention_static(const void* q, const void* k_cache, const
                                        int n_split, void* out, kvd_out_dtype out_dtype, float* lse_out,
                                        int32_t* status_word, kvd_stream_t stream);
 
+/*
+ * kvd_probe_read: a measurement aid, not part of the method. One pass that only
+ * reads [src, src + bytes) into shared memory, the way the attention kernels
+ * read the KV cache (bulk asynchronous copies into a ring of 32 KB stages, one
+ * CTA per SM with a contiguous slice each; L2 evict-first), so that the time
+ * of one launch bounds from below what any kernel reading those bytes once
+ * can take, its launch, first-data latency and drain included. Decode
+ * attention is bound by that read (Efficiently Scaling Transformer Inference,
+ * section 2; All About Transformer Inference, "What about attention?").
+ *   src         : device memory, 16-byte aligned; bytes rounded down to 16
+ *   ctas        : CTAs launched (0 = the device's SM count)
+ *   sink        : optional device u64[ctas]: a word per CTA derived from the
+ *                 data read (so the reads have a consumer); 8-byte aligned
+ *   status_word : optional; KVD_STATUS_TIMEOUT if a copy wait gave up (~2 s)
+ * Errors: KVD_ERR_INVALID_ARG for a NULL src, misaligned pointers or
+ * ctas < 0; KVD_ERR_CUDA if the launch fails. Fewer than 16 bytes: no launch.
+ */
+kvd_status kvd_probe_read(const void* src, size_t bytes, int ctas, unsigned long long* sink,
+                          int32_t* status_word, kvd_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char* kvd_status_string(kvd_status s);
 

@@ -36,6 +36,7 @@ EXPORTED = (
     "kvd_decode_attention_multi", "kvd_decode_step_multi", "kvd_decode_ex", "kvd_kv_append_q8_paged",
     "kvd_decode_attention_umax", "kvd_decode_step_umax", "kvd_step_staging_bytes", "kvd_decode_step_host",
     "kvd_kv_quantize_fp8", "kvd_kv_append_fp8", "kvd_kv_append_fp8_paged", "kvd_merge_attention",
+    "kvd_probe_read",
 )
 STATIC_WORKSPACE_BYTES = 16 << 20  # KVD_STATIC_WORKSPACE_BYTES
 
@@ -115,6 +116,8 @@ def _declare(lib):
     lib.kvd_decode_step_umax.restype = I
     lib.kvd_merge_attention.argtypes = [P, P, I, ctypes.c_longlong, I, I, P, I, P, P]
     lib.kvd_merge_attention.restype = I
+    lib.kvd_probe_read.argtypes = [P, SZ, I, P, P, P]
+    lib.kvd_probe_read.restype = I
     lib.kvd_step_staging_bytes.argtypes = [I, I, I, I, I]
     lib.kvd_step_staging_bytes.restype = SZ
     lib.kvd_decode_step_host.argtypes = [P, P, P, P, P, P, P, P, SZ, I, I, I, I, I, I, I, F, I, P, SZ, P, P, I, P,
@@ -756,6 +759,15 @@ def merge_attention(outs, lses, out, lse=None, stream=None):
     code = lambda t: OUT_BF16 if t.dtype == torch.bfloat16 else OUT_F32
     _check(load().kvd_merge_attention(outs.data_ptr(), lses.data_ptr(), n, rows, D, code(outs), out.data_ptr(),
                                       code(out), _ptr(lse), _stream_handle(stream)), "kvd_merge_attention")
+
+
+def probe_read(src, nbytes: int = 0, ctas: int = 0, sink=None, status=None, stream=None):
+    """One read-only streaming pass over a device tensor's bytes (kvd_probe_read):
+    a measurement aid giving the read ceiling of a kernel that reads those
+    bytes once. nbytes = 0 reads the whole tensor."""
+    n = nbytes or src.numel() * src.element_size()
+    _check(load().kvd_probe_read(src.data_ptr(), n, ctas, _ptr(sink), _ptr(status), _stream_handle(stream)),
+           "kvd_probe_read")
 
 
 def step_staging_bytes(batch: int, n_tokens: int, n_heads_q: int, n_heads_kv: int, head_dim: int) -> int:

@@ -96,6 +96,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar), "l"(policy)
         : "memory");
 }
+// Untiled bulk copy of `bytes` (a multiple of 16) from global src to shared dst
+// (both 16-byte aligned), completing on the mbarrier's transaction count.
+__device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar,
+                                             uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;\n" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar), "l"(policy)
+        : "memory");
+}
 // 2^x on the special-function unit (PTX ex2.approx, flush-to-zero). Its error
 // is far below the bf16 rounding of P and the fp32-mode tolerance; the parity
 // tests bound the end result.

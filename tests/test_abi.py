@@ -444,3 +444,15 @@ def test_decode_ex_rejects(lib):
     assert call(ctypes.byref(cp)) == kvd.ERR_INVALID_ARG                     # page size not a power of two
     assert call(ctypes.byref(c), T=65) == kvd.ERR_UNSUPPORTED                # T > KVD_MAX_TOKENS
     assert call(ctypes.byref(c), B=0, ws=None, n_split=3) == kvd.OK          # batch 0: no-op
+
+
+@pytest.mark.parametrize("args,expect", [
+    # (src, bytes, ctas, sink, status_word, stream)
+    ((None, 1 << 20, 0, None, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE + 8, 1 << 20, 0, None, None, None), kvd.ERR_INVALID_ARG),    # src not 16-byte aligned
+    ((FAKE, 1 << 20, -1, None, None, None), kvd.ERR_INVALID_ARG),
+    ((FAKE, 1 << 20, 0, FAKE + 4, None, None), kvd.ERR_INVALID_ARG),    # sink not 8-byte aligned
+    ((FAKE, 15, 0, None, None, None), kvd.OK),                          # under 16 bytes: nothing to read
+])
+def test_probe_read_rejects(lib, args, expect):
+    assert lib.kvd_probe_read(*args) == expect

@@ -119,8 +119,13 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     no NaN/Inf special case is needed; it is still handled for safety.
     """
     x = np.ascontiguousarray(x, dtype=np.float32)
-    u = x.view(np.uint32).astype(np.uint64)
-    rounded = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    u = x.view(np.uint32)
+    # No finite value (nor infinity) overflows 32 bits here: |x| <= 0x7F800000.
+    r = (u >> 16) & np.uint32(1)
+    r += u
+    r += np.uint32(0x7FFF)
+    r >>= 16
+    rounded = r.astype(np.uint16)
     nan = np.isnan(x)
     if nan.any():
         rounded[nan] = BF16_NAN
