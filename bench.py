@@ -744,7 +744,17 @@ def run_ours(args):
                 hs[2 * i + 1].record()
             torch.cuda.synchronize()
             h2d_us = statistics.median(hs[2 * i].elapsed_time(hs[2 * i + 1]) * 1e3 for i in range(20))
-            host_graphs = [capture(host_steps[r], dev) for r in range(R)]
+            # the steps bound to a capture stream (HostStep takes its stream when built)
+            cs = torch.cuda.Stream(device=dev)
+            host_steps_g = [kvd.HostStep(pq, pkn, pvn, ppos, plens, kcs[r], vcs[r], staging, max_len, w.scale,
+                                         None, out_h, workspace=ws, n_split=args.n_split, stream=cs)
+                            for r in range(R)]
+            host_graphs = []
+            for r in range(R):
+                g = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(g, stream=cs):
+                    host_steps_g[r]()
+                host_graphs.append(g)
             g_ms = time_replays(host_graphs, args.steps, args.warmup)
             g_ms, = max_over_ranks([g_ms], device=dev)
             e2e["breakdown"] = {"h2d_copy_us": round(h2d_us, 2), "device_step_us": round(ms_per_step * 1e3, 2),
