@@ -122,15 +122,11 @@ int heuristic_split(const ChunkKernel* k, int batch, int Hkv, int max_len, int n
     return (int)std::max(1LL, std::min(slots, by_work));
 }
 
-// Partial states: slots of T * G rows (o and (m, l)); then one arrival
-// counter per (sequence, query token, KV head) for the fused merge (the
-// tcgen05 kernel's virtual pairs are that many).
-size_t workspace_for(int n_split, int batch, int Hq, int Hkv, int D, int T = 1) {
+size_t workspace_for(int n_split, int batch, int Hq, int Hkv, int D) {
     if (n_split <= 1 || batch == 0) return 0;
-    const size_t P = (size_t)batch * Hkv, rows = (size_t)(Hq / Hkv) * T;
+    const size_t P = (size_t)batch * Hkv, G = (size_t)(Hq / Hkv);
     const size_t slots = (size_t)n_split + P - 1;
-    return align256(slots * rows * D * sizeof(float)) + align256(slots * rows * sizeof(float2)) +
-           align256(P * T * sizeof(unsigned));
+    return align256(slots * G * D * sizeof(float)) + align256(slots * G * sizeof(float2));
 }
 
 kvd_status plan(int batch, int Hq, int Hkv, int D, int max_len, int num_sms, int n_split_req,
@@ -150,17 +146,12 @@ kvd_status plan(int batch, int Hq, int Hkv, int D, int max_len, int num_sms, int
         n = heuristic_split(k, batch, Hkv, max_len, sms);
     }
     *n_split = n;
-    *ws = workspace_for(n, batch, Hq, Hkv, D, T);  // T * G rows per slot
+    *ws = workspace_for(n, batch, Hq * T, Hkv, D);  // T * G rows per slot
     if (kern) *kern = k;
     return KVD_OK;
 }
 
 enum Phase { kBoth = 3, kChunk = 1, kMerge = 2 };
-
-// Pairs split over at most this many CTAs are merged inside the tcgen05 chunk
-// kernel, by the last of them to finish (each merge reads that many partial
-// states from L2 on one SM, so the count is kept small).
-constexpr int kFuseMax = 4;
 
 // The KV append launched ahead of the attention by kvd_decode_step.
 struct AppendArgs {
@@ -233,7 +224,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
         const int per_wave = (int)std::max(1LL, (long long)sms * k->ctas_per_sm / row_blocks);
         if (n_split > per_wave) {
             n_split = per_wave;
-            need = workspace_for(n_split, batch, Hq, Hkv, D, T);
+            need = workspace_for(n_split, batch, Hq * T, Hkv, D);
         }
     }
     if ((long long)n_split * row_blocks > 0x7fffffffLL) return KVD_ERR_INVALID_ARG;
@@ -288,11 +279,6 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
         p.ws_o = reinterpret_cast<float*>(w);
         w += align256(slots * rows * D * sizeof(float));
         p.ws_ml = reinterpret_cast<float2*>(w);
-        w += align256(slots * rows * sizeof(float2));
-        p.ws_cnt = reinterpret_cast<unsigned*>(w);  // P counters (virtual pairs for the tcgen05 kernel)
-        // The tcgen05 kernel merges pairs split over few CTAs itself, when it
-        // runs with its merge (one call); the merge kernel takes the rest.
-        if (phase == kBoth && k->tensor_core) p.fuse_max = kFuseMax;
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
@@ -301,21 +287,14 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
         // out its schedule) while the append runs, and only its cache loads
         // wait for the append's grid.
         const PagedCache none{nullptr, 0, 0, 0};
-        // The bf16 append also zeroes the fused merge's counters.
-        const int n_cnt = p.fuse_max ? p.B * Hkv : 0;
         const cudaError_t e =
             q8 ? launch_append_q8(app->k_cache, app->v_cache, q8->k_scale, q8->v_scale, app->k_new, app->v_new,
                                   app->pos, batch, s_max, Hkv, D, status, pg ? *pg : none, s, T, q8->fp8)
                : launch_append(app->k_cache, app->v_cache, app->k_new, app->v_new, app->pos, batch, s_max, Hkv,
-                               D, status, pg ? *pg : none, s, T, p.ws_cnt, n_cnt);
+                               D, status, pg ? *pg : none, s, T);
         if (e != cudaSuccess) return KVD_ERR_CUDA;
-        if (q8 && p.fuse_max) {
-            if (launch_zero(p.ws_cnt, p.B * Hkv, s) != cudaSuccess) return KVD_ERR_CUDA;
-        }
         p.early = 1;
         p.pos = app->pos;
-    } else if (p.fuse_max) {
-        if (launch_zero(p.ws_cnt, p.B * Hkv, s) != cudaSuccess) return KVD_ERR_CUDA;
     }
     if (phase & kChunk) {
         int dev = 0;
@@ -329,9 +308,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
         }
         if (k->launch(*k, p, s) != cudaSuccess) return KVD_ERR_CUDA;
     }
-    // With the fused merge on, a pair has at most n_split contributing CTAs,
-    // so there is nothing left for the merge kernel when n_split <= kFuseMax.
-    if ((phase & kMerge) && n_split > 1 && !(p.fuse_max && n_split <= p.fuse_max)) {
+    if ((phase & kMerge) && n_split > 1) {
         int sms = 0;
         if (device_sms(&sms) != KVD_OK) return KVD_ERR_CUDA;
         if (launch_merge(p, D, dt == KVD_OUT_F32, sms, s) != cudaSuccess) return KVD_ERR_CUDA;

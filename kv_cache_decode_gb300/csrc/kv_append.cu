@@ -4,8 +4,6 @@
 // to the KV cache). A bit copy in 16-byte vectors; no arithmetic. With a paged
 // cache the row goes to its block's page (same page, "Tricks for improving
 // generation throughput and latency", Paged Attention).
-#include <algorithm>
-
 #include "../../include/kvdecode.h"
 #include "common.cuh"
 #include "params.h"
@@ -17,12 +15,10 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_ca
                                                        const uint4* __restrict__ v_new,
                                                        const int32_t* __restrict__ pos, int B,
                                                        int S_max, int Hkv, int vec_per_row,
-                                                       int32_t* status, const PagedCache pg, int T,
-                                                       unsigned* zero, int n_zero) {
+                                                       int32_t* status, const PagedCache pg, int T) {
     // Let the attention kernel that follows start its launch; it waits for
-    // this grid's writes before reading the cache (and the zeroed words).
+    // this grid's writes before reading the cache.
     pdl_launch_dependents();
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n_zero; i += gridDim.x * blockDim.x) zero[i] = 0u;
     const long long rows = (long long)B * T * Hkv;  // new rows: (b, i, h)
     const long long per_tensor = rows * vec_per_row;
     for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < 2 * per_tensor;
@@ -57,8 +53,7 @@ __global__ void __launch_bounds__(256) kv_append_kernel(uint4* __restrict__ k_ca
 
 cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                           const int32_t* pos, int B, int S_max, int Hkv, int D,
-                          int32_t* status, const PagedCache& pg, cudaStream_t stream, int T,
-                          unsigned* zero, int n_zero) {
+                          int32_t* status, const PagedCache& pg, cudaStream_t stream, int T) {
     const int vec_per_row = D / 8;
     const long long work = 2LL * B * T * Hkv * vec_per_row;
     long long blocks = (work + 255) / 256;
@@ -71,23 +66,7 @@ cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const
     // The launch's own status (a stale error from earlier work is not picked up).
     return cudaLaunchKernelEx(&cfg, kv_append_kernel, static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache),
                               static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), pos, B, S_max,
-                              Hkv, vec_per_row, status, pg, T, zero, n_zero);
-}
-
-__global__ void __launch_bounds__(256) zero_words_kernel(unsigned* __restrict__ p, int n) {
-    pdl_launch_dependents();
-    for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) p[i] = 0u;
-}
-
-cudaError_t launch_zero(unsigned* p, int n, cudaStream_t stream) {
-    // A plain launch: it starts once the preceding work has finished (which
-    // may still be using the words); the launch after it may start early.
-    const int blocks = (int)std::min<long long>(std::max(1, (n + 255) / 256), 1024);
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)blocks, 1, 1);
-    cfg.blockDim = dim3(256, 1, 1);
-    cfg.stream = stream;
-    return cudaLaunchKernelEx(&cfg, zero_words_kernel, p, n);
+                              Hkv, vec_per_row, status, pg, T);
 }
 
 }  // namespace kvd

@@ -27,13 +27,6 @@ struct DecodeParams {
     int32_t* status;      // optional
     float* ws_o;          // [slots, G, D] partial unnormalised outputs
     float2* ws_ml;        // [slots, G] partial (max, sum), base-2 max
-    // Fused merge (tcgen05 kernel): a pair whose tokens are split over at
-    // most fuse_max CTAs (2..fuse_max) is merged by the last of them to
-    // finish, found with one arrival counter per pair (ws_cnt, zero when the
-    // launch starts; the last arrival returns it to zero). Pairs split over
-    // more CTAs are left to the merge kernel. fuse_max = 0: no fused merge.
-    unsigned* ws_cnt;
-    int fuse_max;
     // Paged cache (block_table non-null): k and v are pools [num_pages, page,
     // Hkv, D] of pages of 1 << page_shift tokens, and token t of sequence b is
     // row t & (page - 1) of page block_table[b * max_blocks + (t >> page_shift)]
@@ -100,11 +93,7 @@ struct PagedCache {
 // T rows per sequence (k_new [B, T, Hkv, D]) go to pos[b] .. pos[b] + T - 1.
 cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                           const int32_t* pos, int B, int S_max, int Hkv, int D,
-                          int32_t* status, const PagedCache& pg, cudaStream_t stream, int T = 1,
-                          unsigned* zero = nullptr, int n_zero = 0);
-// Zeroes n words (the fused merge's arrival counters) once the preceding work
-// on the stream has finished; lets the next launch start early.
-cudaError_t launch_zero(unsigned* p, int n, cudaStream_t stream);
+                          int32_t* status, const PagedCache& pg, cudaStream_t stream, int T = 1);
 // int8 cache (kv_quant.cu): the append quantizes the new rows (into pages
 // when pg.block_table is set); the bulk conversion quantizes rows
 // t < seq_lens[b] of a bf16 cache.

@@ -205,13 +205,6 @@ struct Walker {
         return true;
     }
 
-    // The CTAs c0..c1 whose runs hold tokens of the current pair (the one of
-    // the tile next() returned last).
-    KVD_HD void pair_ctas(int& c0, int& c1) const {
-        c0 = cta_of_token(pstart + g.x(), C_eff, total);
-        c1 = cta_of_token(pstart + ext() - 1, C_eff, total);
-    }
-
     // After the last tile: the last CTA also owns the empty pairs that sit at
     // the very end of the line.
     KVD_HD_TEMPLATE

@@ -76,8 +76,8 @@ struct TcShape {
     static constexpr int OFF_P = OFF_V + VST * TILE_BYTES;
     static constexpr int OFF_BAR = OFF_P + NP * P_BYTES;
     // barriers: k_full, k_empty [KST]; v_full, v_empty [VST]; q_full, q_empty [NQ];
-    // s_full, s_free, p_full, o_fin [2]; mma_done; xbar [4]; gbar (softmax warps)
-    static constexpr int NBAR = 2 * KST + 2 * VST + 2 * NQ + 8 + 1 + 4 + 1;
+    // s_full, s_free, p_full, o_fin [2]; mma_done; xbar [4]
+    static constexpr int NBAR = 2 * KST + 2 * VST + 2 * NQ + 8 + 1 + 4;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int STATIC_SMEM = 2048;  // block scans and the exchange buffer (checked by ptxas -v)
@@ -100,80 +100,6 @@ struct TcMaps {
     CUtensorMap v;
 };
 
-// Fused merge of a pair split over CTAs c0 .. c0 + n - 1 (n <= 4), run by the
-// 256 softmax threads (index st) of the CTA that arrived last at the pair's
-// counter: the n partial states are combined by log-sum-exp in base 2, as the
-// merge kernel does, into the output rows qrow0 .. qrow0 + G - 1 (and lse).
-// wts: 1 KB of shared memory for the weights; sync: the softmax warps'
-// barrier.
-template <int D, bool F32OUT, class Sync>
-__device__ __forceinline__ bool tc_fused_merge(const float* ws_o, const float2* ws_ml, void* out, float* lse,
-                                            size_t pair, size_t qrow0, int G, int c0, int n, int st, float* wts,
-                                            Sync& sync) {
-    // Weights per row: w[j][row] = 2^(m_j - M) / L, L = sum_j 2^(m_j - M) l_j.
-    if (st < G) {
-        float2 ml[4];
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            ml[j] = j < n ? __ldcg(ws_ml + ((size_t)c0 + j + pair) * G + st) : make_float2(0.f, 0.f);
-        float M = -CUDART_INF_F;
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            if (ml[j].y > 0.f) M = fmaxf(M, ml[j].x);
-        float w[4], L = 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            w[j] = ml[j].y > 0.f ? exp2f(ml[j].x - M) : 0.f;
-            L += w[j] * ml[j].y;
-        }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) wts[j * 64 + st] = w[j] * inv;
-        if (lse) lse[qrow0 + st] = L > 0.f ? (M + log2f(L)) * 0.69314718055994531f : -CUDART_INF_F;
-    }
-    if (!sync()) return false;
-    // Columns: item = (row, float4 column c4); two items per batch of loads.
-    constexpr int C4 = D / 4, NU = 2;
-    const int items = G * C4;
-    for (int i0 = st; i0 < items; i0 += NU * 256) {
-        float4 o[NU][4];
-#pragma unroll
-        for (int u = 0; u < NU; ++u) {
-            const int it = i0 + u * 256;
-            const int row = it / C4, c4 = it - row * C4;
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                if (it < items && j < n)
-                    o[u][j] = __ldcg(reinterpret_cast<const float4*>(ws_o + (((size_t)c0 + j + pair) * G + row) * D) +
-                                     c4);
-        }
-#pragma unroll
-        for (int u = 0; u < NU; ++u) {
-            const int it = i0 + u * 256;
-            if (it >= items) break;
-            const int row = it / C4, c4 = it - row * C4;
-            float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (j < n) {
-                    const float wj = wts[j * 64 + row];
-                    a.x += wj * o[u][j].x;
-                    a.y += wj * o[u][j].y;
-                    a.z += wj * o[u][j].z;
-                    a.w += wj * o[u][j].w;
-                }
-            }
-            if constexpr (F32OUT) {
-                reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + (qrow0 + row) * D)[c4] = a;
-            } else {
-                reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + (qrow0 + row) * D)[c4] =
-                    make_uint2(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w));
-            }
-        }
-    }
-    return sync();  // the weights are read before the next tile's P overwrites them
-}
-
 template <int D, bool F32OUT, int QR>
 __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     split_kv_chunk_tc_kernel(const DecodeParams p, const __grid_constant__ TcMaps maps) {
@@ -187,7 +113,6 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     __shared__ int s_redi[NW];
     __shared__ long long s_cum0;
     __shared__ float xbuf[2 * 4 * 32];  // [exchange parity][quarter][half][16 rows]
-    __shared__ int s_last;              // fused merge: this CTA arrived last at the pair
 
     uint8_t* smem = smem_raw;  // 1024-byte aligned (128-byte swizzle atoms need it)
     const uint32_t sbase = smem_u32(smem);
@@ -210,8 +135,6 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     auto o_fin = [&](int b) { return sBar2 + 8u * (7 + b); };
     const uint32_t mma_done = sBar2 + 8u * 9;
     auto xbar = [&](int q) { return sBar2 + 8u * (10 + q); };
-    // All eight softmax warps (one arrival each): orders the fused merge's steps.
-    const uint32_t gbar = sBar2 + 8u * 14;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Sh::OFF_MISC + 8);
     // The P buffer, part 0 = hi, 1 = lo. One buffer: P(i) is written only once
@@ -249,7 +172,6 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
         }
         tc::mbar_init(mma_done, 3);  // S issuers and O issuer
         for (int q = 0; q < 4; ++q) tc::mbar_init(xbar(q), 2);
-        tc::mbar_init(gbar, 8);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
@@ -590,17 +512,6 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             return (lane & 8) ? xb : xa;
         };
 
-        // Barrier of the eight softmax warps (bounded wait, so an abort cannot
-        // strand a warp): ng counts the phases passed.
-        int ng = 0;
-        auto gsync = [&]() {
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(gbar);
-            const bool r = __all_sync(0xffffffffu, tc::mbar_wait(gbar, ng & 1, abort_flag, kBudget));
-            ++ng;
-            return r;
-        };
-
         float mA = 0.f, mB = 0.f;  // running maxima of rows rA, rB
         float lA = 0.f, lB = 0.f;  // this thread's share of the row sums
         Tile t;
@@ -811,29 +722,6 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                         if (p.lse) p.lse[qrow] = (m_row + log2f(ltot)) * 0.69314718055994531f;
                     } else {
                         p.ws_ml[slot * G + row] = make_float2(m_row, ltot);
-                    }
-                }
-                if (!t.full && p.fuse_max) {
-                    int c0, c1;
-                    walker.pair_ctas(c0, c1);
-                    if (c1 - c0 + 1 <= p.fuse_max) {
-                        __threadfence();  // this thread's partial stores, before the arrival
-                        ok = gsync();
-                        if (!ok) break;
-                        if (st == 0) {
-                            if (p.early) pdl_wait();  // the counters were zeroed by the preceding grid
-                            s_last = atomicInc(p.ws_cnt + (size_t)t.b * p.Hkv + t.h, (unsigned)(c1 - c0)) ==
-                                     (unsigned)(c1 - c0);
-                        }
-                        ok = gsync();
-                        if (!ok) break;
-                        if (s_last) {
-                            __threadfence();  // the other CTAs' partials, after their arrivals
-                            ok = tc_fused_merge<D, F32OUT>(p.ws_o, p.ws_ml, p.out, p.lse, (size_t)t.b * p.Hkv + t.h,
-                                                           (size_t)t.b * p.Hq + (size_t)t.h * G, G, c0, c1 - c0 + 1,
-                                                           st, reinterpret_cast<float*>(smem + Sh::OFF_P), gsync);
-                            if (!ok) break;
-                        }
                     }
                 }
             }

@@ -96,10 +96,8 @@ __global__ void __launch_bounds__(NT, 768 / NT) split_kv_merge_kernel(const Deco
             const long long pstart = cum + (long long)h * e;
             const int c0 = cta_of_token(pstart + geo.x(), C_eff, total);
             const int c1 = cta_of_token(pstart + e - 1, C_eff, total);
-            // c0 == c1: the one contributing CTA wrote the final row itself;
-            // with the fused merge on, a pair of at most fuse_max contributing
-            // CTAs was merged by the last of them.
-            if (c1 > c0 && !(p.fuse_max && c1 - c0 + 1 <= p.fuse_max)) {
+            // c0 == c1: the one contributing CTA wrote the final row itself.
+            if (c1 > c0) {
                 active = true;
                 n = c1 - c0 + 1;
                 slot0 = (size_t)c0 + pair;

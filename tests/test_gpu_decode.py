@@ -156,18 +156,3 @@ def test_deterministic(dev, full_inputs):
     a = run_step(inp, dev, "bf16")
     b = run_step(inp, dev, "bf16")
     assert np.array_equal(a.out, b.out) and np.array_equal(a.lse, b.lse)
-
-
-@pytest.mark.parametrize("n_split", [2, 4, 5, 12, 13, 40])
-@pytest.mark.parametrize("out_dtype", ["bf16", "f32"])
-def test_fused_merge_contributor_counts(dev, n_split, out_dtype):
-    """Multiquery pairs (the tcgen05 engine) split over 2..n CTAs: pairs over at
-    most four CTAs are merged inside the chunk kernel by the last CTA to finish,
-    the others by the merge kernel; both against the oracle, with the workspace
-    (counters included) starting as garbage, and bit-identical on a repeat."""
-    inp = workloads.random_small(31, 3, 48, 1, 256, 1100, [1024, 1000, 1100])
-    a = run_step(inp, dev, out_dtype, n_split=n_split)
-    assert a.status == 0
-    _check(inp, a, out_dtype, None, f"fused n_split={n_split}/{out_dtype}")
-    b = run_step(inp, dev, out_dtype, n_split=n_split)
-    assert np.array_equal(a.out, b.out) and np.array_equal(a.lse, b.lse)
