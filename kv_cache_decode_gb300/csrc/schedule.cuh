@@ -135,6 +135,7 @@ struct Walker {
     int b, h, L;
     long long pstart, pos;  // position of the current pair, position reached
 
+    Walker() = default;
     KVD_HD_TEMPLATE
     KVD_HD Walker(LenFn f, Geom g_, int B_, int Hkv_, int c_, int C_eff_, long long total_)
         : len(f), g(g_), B(B_), Hkv(Hkv_), c(c_), C_eff(C_eff_), total(total_) {

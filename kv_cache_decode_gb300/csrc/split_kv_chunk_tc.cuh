@@ -7,12 +7,14 @@
 // tile of one (sequence, KV head) pair:
 //   S  = Q K^T      tcgen05.mma, M = 64 query heads (group padded to 64),
 //                   N = 64 tokens, K = head_dim; fp32 accumulator in TMEM
-//   P  = 2^(S*scale*log2e - m)   four softmax warps, one query head per thread
-//   O += P V        tcgen05.mma, M = 64, N = head_dim, K = 64 tokens; O in TMEM
-// Operands never pass through registers: TMA writes K, V and Q tiles into
+//   P  = 2^(S*scale*log2e - m)   four softmax warps, two threads per query head
+//   O += P V        tcgen05.mma, M = 64, N = head_dim, K = 64 tokens, with P
+//                   read from TMEM as the A operand; O in TMEM
+// K, V and Q never pass through registers: TMA writes their tiles into
 // 128-byte-swizzled shared memory, and the MMAs read them there, so each K/V
 // byte crosses shared memory once (the mma.sync kernel re-reads it once per
-// 16-head tile). The online softmax follows the log-sum-exp accumulation of
+// 16-head tile). P goes from the softmax registers to TMEM and from there into
+// the P V product, without a shared-memory pass. The online softmax follows the log-sum-exp accumulation of
 // sequence-sharded KV (All About Transformer Inference, "Sharding the KV
 // cache") in base 2 (Efficiently Scaling Transformer Inference, section 3.5).
 // The running maximum m used for the exponentials is only raised when a tile's
@@ -20,14 +22,16 @@
 // rescaling O in TMEM is rare; the result is identical in exact arithmetic
 // because O and l always share the same m.
 //
-// Warp roles (14 warps): 0 = TMA producer for K, 2 = TMA producer for V,
-// 13 = TMA loader for Q at each new pair, 1 and 11 = S issuers (one thread
-// each, one half of head_dim each; warp 1 also owns TMEM), 12 = O issuer, 3..10 = softmax /
-// rescale / epilogue (two warps per TMEM lane quarter w % 4, splitting the
-// token columns of S and the output columns of O).
-// Pipelines: K ring of KST stages, V ring of VST stages, two S buffers in
-// TMEM, two P buffers in shared memory, one Q buffer, O in TMEM. Every wait is
-// bounded; a timeout flags KVD_STATUS_TIMEOUT and all roles wind down.
+// Warp roles (10 warps): 0 = TMA producer for K, 2 = TMA producer for V,
+// 9 = TMA loader for Q at each new pair, 1 and 7 = S issuers (one thread
+// each, one half of head_dim each; warp 1 also owns TMEM), 8 = O issuer,
+// 3..6 = softmax / rescale / epilogue (one warp per TMEM lane quarter w % 4;
+// within a warp, the two threads of a query head take one half of the tile's
+// token columns each, and one half of O's columns in the epilogue).
+// Pipelines: K ring of KST stages, V ring of VST stages, one S buffer (two
+// partial sums) in TMEM, two P buffers in TMEM, Q slots in shared memory, O in
+// TMEM. Every wait is bounded; a timeout flags KVD_STATUS_TIMEOUT and all
+// roles wind down.
 #pragma once
 
 #include <math_constants.h>
@@ -62,36 +66,38 @@ struct TcShape {
     static constexpr int NQ = QR <= 16 ? 4 : 1;
     static constexpr int QS_BYTES = KB * QB_BYTES;  // one slot
     static constexpr int Q_BYTES = NQ * QS_BYTES;
-    static constexpr int P_BYTES = 64 * T * 2;   // one P buffer (64 rows x 64 tokens)
     static constexpr int NP = F32OUT ? 2 : 1;    // hi (and lo) parts of P
     // Stage counts: three V stages (a V stage is held until P V of its tile is
     // done, so the V ring needs the depth), K stages as the budget allows.
     static constexpr int VST = D == 256 ? 3 : (D == 128 ? 6 : 8);
-    static constexpr int BUDGET = 224 * 1024 - Q_BYTES - NP * P_BYTES - VST * TILE_BYTES;
+    static constexpr int BUDGET = 224 * 1024 - Q_BYTES - VST * TILE_BYTES;
     static constexpr int KST_FIT = BUDGET / TILE_BYTES;
     static constexpr int KST = KST_FIT > 8 ? 8 : KST_FIT;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
     static constexpr int OFF_V = OFF_K + KST * TILE_BYTES;
-    static constexpr int OFF_P = OFF_V + VST * TILE_BYTES;
-    static constexpr int OFF_BAR = OFF_P + NP * P_BYTES;
+    static constexpr int OFF_BAR = OFF_V + VST * TILE_BYTES;
     // barriers: k_full, k_empty [KST]; v_full, v_empty [VST]; q_full, q_empty [NQ];
-    // s_full, s_free, p_full, o_fin [2]; mma_done; xbar [4]
-    static constexpr int NBAR = 2 * KST + 2 * VST + 2 * NQ + 8 + 1 + 4;
+    // s_full, s_free; p_full, o_fin [2]; mma_done
+    static constexpr int NBAR = 2 * KST + 2 * VST + 2 * NQ + 2 + 4 + 1;
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
-    static constexpr int STATIC_SMEM = 2048;  // block scans and the exchange buffer (checked by ptxas -v)
-    static constexpr int TMEM_S = 0;             // S, first head_dim half: columns 0 and T
-    static constexpr int TMEM_S2 = 2 * T;        // S, second half: columns 2T and 3T
-    static constexpr int TMEM_O = 4 * T;         // O at columns [4T, 4T + D)
-    static constexpr int TMEM_COLS = (4 * T + D) <= 256 ? 256 : 512;
-    // producers 0 (K) and 2 (V), S issuers 1 and 11, O issuer 12, Q loader 13, softmax 3..10
-    static constexpr int NWARPS = 14;
+    static constexpr int STATIC_SMEM = 1024;  // block scans (checked by ptxas -v)
+    // TMEM columns: S as two partial sums over the halves of head_dim, two P
+    // buffers (bf16 pairs, 32 columns per part), O.
+    static constexpr int TMEM_S = 0;             // S, first head_dim half: columns [0, T)
+    static constexpr int TMEM_S2 = T;            // S, second half: columns [T, 2T)
+    static constexpr int PCOLS = NP * T / 2;     // one P buffer
+    static constexpr int TMEM_P = 2 * T;         // P buffers at [2T, 2T + 2 PCOLS)
+    static constexpr int TMEM_O = 256;           // O at columns [256, 256 + D)
+    static constexpr int TMEM_COLS = 512;
+    // producers 0 (K) and 2 (V), S issuers 1 and 7, O issuer 8, Q loader 9, softmax 3..6
+    static constexpr int NWARPS = 10;
     static constexpr int THREADS = NWARPS * 32;
     static_assert(KST >= 2, "need at least two K stages");
     static_assert(SMEM_BYTES + STATIC_SMEM <= 227 * 1024, "shared memory budget");
     static_assert(QR % 8 == 0 && QR <= 64, "Q rows per block");
-    static_assert(4 * T + D <= 512, "TMEM columns");
+    static_assert(TMEM_P + 2 * PCOLS <= TMEM_O && TMEM_O + D <= TMEM_COLS, "TMEM columns");
 };
 
 struct TcMaps {
@@ -112,12 +118,11 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     __shared__ long long s_red[NW];
     __shared__ int s_redi[NW];
     __shared__ long long s_cum0;
-    __shared__ float xbuf[2 * 4 * 32];  // [exchange parity][quarter][half][16 rows]
 
     uint8_t* smem = smem_raw;  // 1024-byte aligned (128-byte swizzle atoms need it)
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + Sh::OFF_Q, sK = sbase + Sh::OFF_K, sV = sbase + Sh::OFF_V,
-                   sP = sbase + Sh::OFF_P, sBar = sbase + Sh::OFF_BAR;
+                   sBar = sbase + Sh::OFF_BAR;
     auto k_full = [&](int s) { return sBar + 8u * s; };
     auto k_empty = [&](int s) { return sBar + 8u * (KST + s); };
     auto v_full = [&](int s) { return sBar + 8u * (2 * KST + s); };
@@ -125,21 +130,19 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     constexpr int NQ = Sh::NQ;
     auto q_full = [&](int s) { return sBar + 8u * (2 * KST + 2 * VST + s); };
     auto q_empty = [&](int s) { return sBar + 8u * (2 * KST + 2 * VST + NQ + s); };
-    const uint32_t sBar2 = sBar + 8u * (2 * KST + 2 * VST + 2 * NQ - 1);  // base of the rest
-    auto s_full = [&](int b) { return sBar2 + 8u * (1 + b); };
-    auto s_free = [&](int b) { return sBar2 + 8u * (3 + b); };
-    auto p_full = [&](int b) { return sBar2 + 8u * (5 + b); };
-    // o_fin[i & 1] completes when O += P(i) V(i) has finished. One barrier per
-    // P buffer (rather than one for all tiles) keeps every waiter within one
-    // phase of the completion it waits for, so parity waits are unambiguous.
-    auto o_fin = [&](int b) { return sBar2 + 8u * (7 + b); };
-    const uint32_t mma_done = sBar2 + 8u * 9;
-    auto xbar = [&](int q) { return sBar2 + 8u * (10 + q); };
+    const uint32_t sBar2 = sBar + 8u * (2 * KST + 2 * VST + 2 * NQ);  // base of the rest
+    // One S buffer: s_full completes when both halves of S(i) are in TMEM,
+    // s_free once the four softmax warps have read them.
+    const uint32_t s_full = sBar2, s_free = sBar2 + 8u;
+    auto p_full = [&](int b) { return sBar2 + 8u * (2 + b); };
+    // o_fin[i & 1] completes when O += P(i) V(i) has finished (and P buffer
+    // i & 1 may be written again). One barrier per P buffer (rather than one
+    // for all tiles) keeps every waiter within one phase of the completion it
+    // waits for, so parity waits are unambiguous.
+    auto o_fin = [&](int b) { return sBar2 + 8u * (4 + b); };
+    const uint32_t mma_done = sBar2 + 8u * 6;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Sh::OFF_MISC + 8);
-    // The P buffer, part 0 = hi, 1 = lo. One buffer: P(i) is written only once
-    // P(i-1) V(i-1) has completed.
-    auto p_buf = [&](int /*tile parity*/, int part) { return sP + (uint32_t)(part * Sh::P_BYTES); };
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = blockIdx.x;
@@ -164,24 +167,24 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             tc::mbar_init(q_full(s), 1);
             tc::mbar_init(q_empty(s), 2);
         }
+        tc::mbar_init(s_full, 2);  // both S issuers
+        tc::mbar_init(s_free, 4);  // the softmax warps
         for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(s_full(b), 2);
-            tc::mbar_init(s_free(b), 8);
-            tc::mbar_init(p_full(b), 8);
+            tc::mbar_init(p_full(b), 4);
             tc::mbar_init(o_fin(b), 1);
         }
         tc::mbar_init(mma_done, 3);  // S issuers and O issuer
-        for (int q = 0; q < 4; ++q) tc::mbar_init(xbar(q), 2);
         *abort_flag = 0;
         tc::mbar_fence_init();
     }
-    // Rows of Q past the group, and P rows of padded heads, stay zero.
+    // Rows of Q past the group stay zero.
     for (int i = tid; i < Sh::Q_BYTES / 16; i += Sh::THREADS)
         reinterpret_cast<uint4*>(smem + Sh::OFF_Q)[i] = make_uint4(0, 0, 0, 0);
-    for (int i = tid; i < Sh::NP * Sh::P_BYTES / 16; i += Sh::THREADS)
-        reinterpret_cast<uint4*>(smem + Sh::OFF_P)[i] = make_uint4(0, 0, 0, 0);
     tc::fence_proxy_async_smem();
-    if (warp == 1) tc::tmem_alloc(smem_u32(tmem_slot), Sh::TMEM_COLS);
+    if (warp == 1) {
+        tc::tmem_alloc(smem_u32(tmem_slot), Sh::TMEM_COLS);
+        tc::fence_before_sync();
+    }
 
     // Inputs may be produced by the previous kernel on the stream. After this
     // library's append (p.early), only the cache loads need to wait for it.
@@ -195,41 +198,80 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
     const int vt = p.vT > 1 ? p.vT : 1;
     const DevLen len{p.seq_lens, p.len_cap, vt};
     using Geo = FixedGeom<T, Sh::SEG_UNIT, SEG_COST>;
-    // ---- total work, this CTA's run, first sequence (as in the mma.sync kernel) ----
-    long long total;
-    int C_eff, b0 = p.B;
-    bool has_work;
-    long long S, cum0;
-    if (p.B <= Sh::THREADS) {
-        // One pass (the common case), one sequence per thread: an inclusive
-        // scan gives both the total and each sequence's start; the first
-        // sequence touching the run is the first candidate, and its start is
-        // the smallest candidate start (starts never decrease with b).
-        const int b = tid;
-        int L = 0;
-        if (b < p.B) {
-            const int raw = __ldg(p.seq_lens + b / vt);
-            L = len(b);
-            if (raw != clamp_len(raw, p.len_cap) && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
-        }
-        const long long e = pair_extent(L, Geo{});
-        const long long v = e * p.Hkv;
-        const long long cs = block_incl_scan_ll<NW>(v, s_red, &total) - v;  // also orders the set-up
-        C_eff = effective_ctas(p.n_split, total);
-        has_work = c < C_eff;
-        S = has_work ? run_begin(c, C_eff, total) : total;
-        cum0 = total;
-        if (has_work) {
-            const bool cand = (b < p.B) && is_first_seq_candidate(cs, e, p.Hkv, S);
-            int bi = cand ? b : 0x7fffffff;
-            long long ci = cand ? cs : 0x7fffffffffffffffLL;
-            block_min_int_ll<NW>(bi, ci, s_redi, s_red);
-            if (bi != 0x7fffffff) {
-                b0 = bi;
-                cum0 = ci;
+    // ---- total work, this CTA's run, first sequence ----
+    // Warp 0 works the schedule out and leaves the walker, positioned at the
+    // start of this CTA's run, in shared memory; each role takes a copy after
+    // the set-up barrier. Up to 32 * WK sequences (the common case) it does so
+    // with warp shuffles only, lane l taking sequences l, l + 32, ...; past
+    // that, the whole block scans the lengths.
+    using WalkerT = Walker<DevLen, Geo>;
+    __shared__ __align__(16) unsigned char s_walker[sizeof(WalkerT)];
+    __shared__ int s_has_work;
+    constexpr int WK = 8;
+    const bool by_warp = p.B <= 32 * WK;
+    auto publish = [&](int C_eff, long long total, bool has_work, int b0, long long cum0) {
+        WalkerT w(len, Geo{}, p.B, p.Hkv, c, has_work ? C_eff : c + 1, has_work ? total : 0);
+        w.start(b0, cum0);
+        memcpy(s_walker, &w, sizeof(WalkerT));
+        s_has_work = has_work ? 1 : 0;
+    };
+    if (by_warp) {
+        if (warp == 0) {
+            int ext_r[WK];
+            bool clamped = false;
+#pragma unroll
+            for (int k = 0; k < WK; ++k) {
+                const int b = lane + 32 * k;
+                ext_r[k] = 0;
+                if (b < p.B) {
+                    const int raw = __ldg(p.seq_lens + b / vt);
+                    clamped |= (raw != clamp_len(raw, p.len_cap));
+                    ext_r[k] = (int)pair_extent(len(b), Geo{});
+                }
             }
+            if (clamped && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
+            int tot = 0;
+#pragma unroll
+            for (int k = 0; k < WK; ++k) tot += ext_r[k];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+            const long long total = (long long)tot * p.Hkv;
+            const int C_eff = effective_ctas(p.n_split, total);
+            const bool has_work = c < C_eff;
+            const long long S = has_work ? run_begin(c, C_eff, total) : total;
+            int b0 = p.B;
+            long long cum0 = total;
+            if (has_work) {
+                // The first sequence touching the run: the first candidate in b
+                // order (the condition, once true, stays true).
+                long long carry = 0;
+#pragma unroll
+                for (int k = 0; k < WK; ++k) {
+                    if (32 * k >= p.B) break;
+                    const int x = ext_r[k];
+                    int incl = x;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    const long long cs = carry + (long long)(incl - x) * p.Hkv;
+                    const bool cand = (lane + 32 * k < p.B) && is_first_seq_candidate(cs, x, p.Hkv, S);
+                    const unsigned m = __ballot_sync(0xffffffffu, cand);
+                    if (m) {
+                        const int f = __ffs(m) - 1;
+                        b0 = 32 * k + f;
+                        cum0 = __shfl_sync(0xffffffffu, cs, f);
+                        break;
+                    }
+                    carry += (long long)__shfl_sync(0xffffffffu, incl, 31) * p.Hkv;
+                }
+            }
+            if (lane == 0) publish(C_eff, total, has_work, b0, cum0);
         }
+        __syncthreads();  // set-up done, walker published
     } else {
+        __syncthreads();  // set-up done
         long long mine = 0;
         bool clamped = false;
         for (int b = tid; b < p.B; b += Sh::THREADS) {
@@ -238,11 +280,12 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             mine += pair_extent(len(b), Geo{});
         }
         if (clamped && c == 0 && p.status) atomicOr(p.status, KVD_STATUS_SEQ_LEN_CLAMPED);
-        total = block_sum_ll<NW>(mine, s_red) * p.Hkv;  // also orders the set-up
-        C_eff = effective_ctas(p.n_split, total);
-        has_work = c < C_eff;
-        S = has_work ? run_begin(c, C_eff, total) : total;
-        cum0 = total;
+        const long long total = block_sum_ll<NW>(mine, s_red) * p.Hkv;
+        const int C_eff = effective_ctas(p.n_split, total);
+        const bool has_work = c < C_eff;
+        const long long S = has_work ? run_begin(c, C_eff, total) : total;
+        int b0 = p.B;
+        long long cum0 = total;
         for (long long base = 0, chunk = 0; has_work && chunk < p.B; chunk += Sh::THREADS) {
             const int b = (int)chunk + tid;
             const int L = (b < p.B) ? len(b) : 0;
@@ -261,12 +304,14 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             }
             base += ctot;
         }
+        if (tid == 0) publish(C_eff, total, has_work, b0, cum0);
+        __syncthreads();
     }
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-
-    Walker<DevLen, Geo> walker(len, Geo{}, p.B, p.Hkv, c, has_work ? C_eff : c + 1, has_work ? total : 0);
-    walker.start(b0, cum0);
+    WalkerT walker;
+    memcpy(&walker, s_walker, sizeof(WalkerT));
+    const bool has_work = s_has_work != 0;
 
     if (!has_work) {
         // no tokens for this CTA: fall through to the common exit (TMEM release)
@@ -347,7 +392,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                 tc::mbar_wait(is_k ? k_full(s) : v_full(s), (jj / NS) & 1, abort_flag, kBudget / 4);
             }
         }
-    } else if (warp == 13) {
+    } else if (warp == 9) {
         // ===================== Q loader =====================
         // Its own thread, so that waiting for the Q slot (free once the previous
         // pair's last S is done) never holds up the K stream. When the run goes
@@ -378,30 +423,31 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             }
             if (qn > 0) tc::mbar_wait(q_full((qn - 1) % NQ), ((qn - 1) / NQ) & 1, abort_flag, kBudget / 4);
         }
-    } else if (warp == 1 || warp == 11) {
+    } else if (warp == 1 || warp == 7) {
         // ===================== S issuers (one thread each) =====================
         // S = Q K^T is issued as two independent accumulations over the two
-        // halves of head_dim, by two threads into two TMEM buffers that the
-        // softmax adds: a tcgen05.mma of this shape costs its issuing thread
-        // about as long as the tensor core needs for two of them, so two
-        // issuers finish a tile's S in half the time and release its K stage
-        // sooner.
+        // halves of head_dim, by two threads into two TMEM column ranges that
+        // the softmax adds: a tcgen05.mma of this shape costs its issuing
+        // thread about as long as the tensor core needs for two of them, so
+        // two issuers finish a tile's S in half the time and release its K
+        // stage sooner. One S buffer: S(i) is issued once the softmax has read
+        // S(i - 1) out of TMEM, early in that tile's softmax.
         if (lane == 0) {
-            const int kh = (warp == 11) ? 1 : 0;
+            const int kh = (warp == 7) ? 1 : 0;
             constexpr int KH = D / 32;  // k-steps per half
             constexpr uint32_t idesc_s = tc::idesc_bf16_f32(64, T, false, false);
             const uint32_t s_base = tmem + (kh ? Sh::TMEM_S2 : Sh::TMEM_S);
             Tile t;
             int i = 0, qn = 0;
             while (walker.next(t, NoOp{})) {
-                const int sk = i % KST, sb = i & 1;
+                const int sk = i % KST;
                 if (t.seg_start) {
                     if (!tc::mbar_wait(q_full(qn % NQ), (qn / NQ) & 1, abort_flag, kBudget)) break;
                     ++qn;
                 }
                 const int qs = (qn - 1) % NQ;
                 if (!tc::mbar_wait(k_full(sk), (i / KST) & 1, abort_flag, kBudget)) break;
-                if (!tc::mbar_wait(s_free(sb), ((i >> 1) & 1) ^ 1, abort_flag, kBudget)) break;
+                if (!tc::mbar_wait(s_free, (i & 1) ^ 1, abort_flag, kBudget)) break;
                 tc::fence_after_sync();
                 const uint32_t qt = sQ + (uint32_t)(qs * Sh::QS_BYTES);
                 const uint32_t kt = sK + (uint32_t)(sk * Sh::TILE_BYTES);
@@ -410,9 +456,9 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                     const int kk = kh * KH + k;
                     const uint64_t a = tc::sdesc_sw128(qt + (kk >> 2) * Sh::QB_BYTES + (kk & 3) * 32, 16, 1024);
                     const uint64_t b = tc::sdesc_sw128(kt + (kk >> 2) * Sh::KB_BYTES + (kk & 3) * 32, 16, 1024);
-                    tc::mma_bf16(s_base + sb * T, a, b, idesc_s, k > 0);
+                    tc::mma_bf16(s_base, a, b, idesc_s, k > 0);
                 }
-                tc::mma_commit(s_full(sb));
+                tc::mma_commit(s_full);
                 tc::mma_commit(k_empty(sk));
                 if (t.seg_end) tc::mma_commit(q_empty(qs));
                 ++i;
@@ -421,144 +467,105 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             tc::mma_commit(mma_done);
             tc::mbar_wait(mma_done, 0, abort_flag, kBudget);
         }
-    } else if (warp == 12) {
+    } else if (warp == 8) {
         // ===================== O issuer (one thread) =====================
+        // O += P(i) V(i): A = P from TMEM buffer i & 1 (the hi part, then the
+        // lo part for fp32 output), B = the V stage in MN-major layout.
         if (lane == 0) {
             constexpr uint32_t idesc_o = tc::idesc_bf16_f32(64, D, false, true);
             Tile t;
             int i = 0;
             while (walker.next(t, NoOp{})) {
-                const int sv = i % VST, sb = i & 1;
+                const int sv = i % VST, pb = i & 1;
                 if (!tc::mbar_wait(v_full(sv), (i / VST) & 1, abort_flag, kBudget)) break;
-                if (!tc::mbar_wait(p_full(sb), (i >> 1) & 1, abort_flag, kBudget)) break;
+                if (!tc::mbar_wait(p_full(pb), (i >> 1) & 1, abort_flag, kBudget)) break;
                 tc::fence_after_sync();
                 const uint32_t vt = sV + (uint32_t)(sv * Sh::TILE_BYTES);
+                const uint32_t pa = tmem + (uint32_t)(Sh::TMEM_P + pb * Sh::PCOLS);
 #pragma unroll
                 for (int k2 = 0; k2 < T / 16; ++k2) {
                     const uint64_t b = tc::sdesc_sw128(vt + k2 * 2048, Sh::KB_BYTES, 1024);
 #pragma unroll
-                    for (int part = 0; part < Sh::NP; ++part) {
-                        const uint64_t a = tc::sdesc_sw128(p_buf(sb, part) + k2 * 32, 16, 1024);
-                        tc::mma_bf16(tmem + Sh::TMEM_O, a, b, idesc_o, (t.seg_start && k2 == 0 && part == 0) ? 0u : 1u);
-                    }
+                    for (int part = 0; part < Sh::NP; ++part)
+                        tc::mma_bf16_ts(tmem + Sh::TMEM_O, pa + (uint32_t)(part * (T / 2) + k2 * 8), b, idesc_o,
+                                        (t.seg_start && k2 == 0 && part == 0) ? 0u : 1u);
                 }
                 tc::mma_commit(v_empty(sv));
-                tc::mma_commit(o_fin(sb));
+                tc::mma_commit(o_fin(pb));
                 ++i;
             }
             tc::mma_commit(mma_done);
             tc::mbar_wait(mma_done, 0, abort_flag, kBudget);
         }
-    } else {
-        // ===================== softmax / epilogue (warps 3..10) =====================
-        // Two warps serve each TMEM lane quarter (a warp reaches the 32 lanes
-        // 32 * (warp % 4) ...): the warp of half 0 takes token columns [0, 32)
-        // of every S tile and output columns [0, D/2), the other the upper
-        // halves. Row maxima and row sums are exchanged between the two through
-        // shared memory, synchronised by a two-arrival mbarrier per quarter
-        // (bounded waits, so an abort cannot strand the partner warp).
-        constexpr int HT = T / 2;   // token columns per half
-        constexpr int HD = D / 2;   // output columns per half
-        const int sw = warp - 3;    // 0..7
+    } else if (warp >= 3 && warp <= 6) {
+        // ===================== softmax / epilogue (warps 3..6) =====================
+        // One warp per TMEM lane quarter (a warp reaches the 32 lanes
+        // 32 * (warp % 4) ...), whose 16 accumulator rows are query heads
+        // 16 * quarter ... 16 * quarter + 15. Through the 16x32bx2 shape each
+        // head goes to two threads of the warp: thread l takes head
+        // 16 * quarter + l % 16 and token columns [32 (l / 16), 32 (l / 16) + 32)
+        // of every S tile (P columns likewise), and output columns
+        // [(D / 2)(l / 16), (D / 2)(l / 16) + D / 2) in the epilogue. A row's
+        // maximum and sum need one shuffle between its two threads; no other
+        // warp takes part.
+        constexpr int HT = T / 2;   // token columns per thread
+        constexpr int HD = D / 2;   // output columns per thread
         const int quarter = warp & 3;
-        const int half = sw >> 2;
-        // Lane layout of the epilogue (32x32b TMEM shape): lanes 0..15 hold rows.
-        const int row = quarter * 16 + lane;   // group-local query head of this lane
-        const bool has_row = lane < 16;
-        const bool active = has_row && row < G;
-        const int st = tid - 3 * 32;           // 0..255 among the softmax threads
+        const int hl = lane >> 4;
+        const int row = quarter * 16 + (lane & 15);  // group-local query head of this thread
+        const bool active = row < G;
+        const int st = tid - 3 * 32;                 // 0..127 among the softmax threads
         const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
         const float scale_log2 = p.scale_log2;
-        int nx = 0;  // exchanges done with the partner warp
 
         auto write_empty = [&](int b, int h) {
             const size_t r0 = (size_t)b * p.Hq + (size_t)h * G;
             if constexpr (F32OUT) {
                 float* o = reinterpret_cast<float*>(p.out) + r0 * D;
-                for (int i2 = st; i2 < G * D; i2 += 256) o[i2] = 0.f;
+                for (int i2 = st; i2 < G * D; i2 += 128) o[i2] = 0.f;
             } else {
                 __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + r0 * D;
-                for (int i2 = st; i2 < G * D; i2 += 256) o[i2] = __float2bfloat16_rn(0.f);
+                for (int i2 = st; i2 < G * D; i2 += 128) o[i2] = __float2bfloat16_rn(0.f);
             }
             if (p.lse)
-                for (int i2 = st; i2 < G; i2 += 256) p.lse[r0 + i2] = -CUDART_INF_F;
+                for (int i2 = st; i2 < G; i2 += 128) p.lse[r0 + i2] = -CUDART_INF_F;
         };
 
-        // S is read with the 16x256b TMEM shape, which puts the quarter's 16
-        // rows on all 32 threads in the mma accumulator layout: thread t holds
-        // rows rA = t/4 and rB = t/4 + 8 of the quarter, columns 8g + 2(t%4) + 0..1
-        // of each 8-column group g of its half. Row statistics are reduced over
-        // the 4 threads of a quad, then with the partner warp (other half).
-        const int rA = quarter * 16 + (lane >> 2), rB = rA + 8;
-        const bool actA = rA < G, actB = rB < G;
-        // Exchange two per-row floats (rows rA, rB) with the partner warp.
-        auto exchange2 = [&](float va, float vb, float& oa, float& ob, bool& ok_) {
-            float* buf = xbuf + ((nx & 1) * 4 + quarter) * 32;
-            if ((lane & 3) == 0) {
-                buf[half * 16 + (lane >> 2)] = va;
-                buf[half * 16 + 8 + (lane >> 2)] = vb;
-            }
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(xbar(quarter));
-            ok_ = __all_sync(0xffffffffu, tc::mbar_wait(xbar(quarter), nx & 1, abort_flag, kBudget));
-            oa = buf[(half ^ 1) * 16 + (lane >> 2)];
-            ob = buf[(half ^ 1) * 16 + 8 + (lane >> 2)];
-            ++nx;
-        };
-        // Per-row value of the quad layout moved to the lane layout (lane = row, lanes 0..15).
-        auto to_lane = [&](float a, float b) {
-            const float xa = __shfl_sync(0xffffffffu, a, (lane & 7) * 4);
-            const float xb = __shfl_sync(0xffffffffu, b, (lane & 7) * 4);
-            return (lane & 8) ? xb : xa;
-        };
-
-        float mA = 0.f, mB = 0.f;  // running maxima of rows rA, rB
-        float lA = 0.f, lB = 0.f;  // this thread's share of the row sums
+        float m = 0.f;  // running maximum of this thread's row (the same in both of its threads)
+        float l = 0.f;  // this thread's share of the row sum
         Tile t;
         int i = 0;
         bool ok = true;
         while (ok && walker.next(t, write_empty)) {
-            const int sb = i & 1;
-            ok = __all_sync(0xffffffffu, tc::mbar_wait(s_full(sb), (i >> 1) & 1, abort_flag, kBudget));
+            ok = __all_sync(0xffffffffu, tc::mbar_wait(s_full, i & 1, abort_flag, kBudget));
             if (!ok) break;
             tc::fence_after_sync();
             __syncwarp();
             // S is held as two partial sums over the halves of head_dim.
-            uint32_t sr[16], sr2[16];
-            tc::tmem_ld_16x256b_x4(tmem + lane_base + Sh::TMEM_S + sb * T + half * HT, sr);
-            tc::tmem_ld_16x256b_x4(tmem + lane_base + Sh::TMEM_S2 + sb * T + half * HT, sr2);
-            tc::tmem_wait_ld();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(s_free(sb));
-
-            // Scores in base-2 units; columns past the tile's last token masked.
-            const int nvalid = t.tok_hi - t.tok_lo;
-            const int nv = nvalid - half * HT;  // valid columns of this half (may be <= 0)
-            float s[16];
+            float s[HT];
+            {
+                uint32_t sa[HT], sb[HT];
+                tc::tmem_ld_16x32bx2_x32<HT>(tmem + lane_base + Sh::TMEM_S, sa);
+                tc::tmem_ld_16x32bx2_x32<HT>(tmem + lane_base + Sh::TMEM_S2, sb);
+                tc::tmem_wait_ld();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(s_free);
+                // Scores in base-2 units; columns past the tile's last token masked.
+                const int nv = (t.tok_hi - t.tok_lo) - hl * HT;  // valid columns of this thread (may be <= 0)
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-                const int col = 8 * (e >> 2) + 2 * (lane & 3) + (e & 1);
-                s[e] = (col < nv) ? (__uint_as_float(sr[e]) + __uint_as_float(sr2[e])) * scale_log2 : -CUDART_INF_F;
+                for (int e = 0; e < HT; ++e)
+                    s[e] = (e < nv) ? (__uint_as_float(sa[e]) + __uint_as_float(sb[e])) * scale_log2 : -CUDART_INF_F;
             }
-            float xA = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[4], s[5]));
-            float xB = fmaxf(fmaxf(s[2], s[3]), fmaxf(s[6], s[7]));
-            xA = fmaxf(xA, fmaxf(fmaxf(s[8], s[9]), fmaxf(s[12], s[13])));
-            xB = fmaxf(xB, fmaxf(fmaxf(s[10], s[11]), fmaxf(s[14], s[15])));
-            xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, 1));
-            xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, 1));
-            xA = fmaxf(xA, __shfl_xor_sync(0xffffffffu, xA, 2));
-            xB = fmaxf(xB, __shfl_xor_sync(0xffffffffu, xB, 2));
-            float oA, oB;
-            exchange2(xA, xB, oA, oB, ok);
-            if (!ok) break;
-            const float mtA = fmaxf(xA, oA), mtB = fmaxf(xB, oB);
+            float mx = s[0];
+#pragma unroll
+            for (int e = 1; e < HT; ++e) mx = fmaxf(mx, s[e]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
 
-            bool needA = false, needB = false;
-            float alphaA = 1.f, alphaB = 1.f;
+            bool need = false;
+            float alpha = 1.f;
             if (t.seg_start) {
-                mA = mtA;
-                mB = mtB;
+                m = mx;
                 if (p.umax) {
                     // Unified maximum (FlashDecoding++'s asynchronized softmax):
                     // a row whose first tile's maximum lies within [phi - 64,
@@ -567,88 +574,67 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                     // it starts from its own maximum. The lazy rescale below
                     // moves m up past phi + 8 (exact either way).
                     const float phi2 = p.umax_phi2;
-                    if (mtA >= phi2 - 64.f && mtA <= phi2 + 8.f) mA = phi2;
-                    if (mtB >= phi2 - 64.f && mtB <= phi2 + 8.f) mB = phi2;
-                    if (((actA && mA != phi2) || (actB && mB != phi2)) && p.status)
-                        atomicOr(p.status, KVD_STATUS_UMAX_FALLBACK);
+                    if (mx >= phi2 - 64.f && mx <= phi2 + 8.f) m = phi2;
+                    if (active && m != phi2 && p.status) atomicOr(p.status, KVD_STATUS_UMAX_FALLBACK);
                 }
-                lA = lB = 0.f;
-            } else {
-                if (mtA > mA + 8.f) {
-                    needA = true;
-                    alphaA = exp2f(mA - mtA);
-                    mA = mtA;
-                }
-                if (mtB > mB + 8.f) {
-                    needB = true;
-                    alphaB = exp2f(mB - mtB);
-                    mB = mtB;
-                }
-                if (p.umax && ((actA && needA) || (actB && needB)) && p.status)
-                    atomicOr(p.status, KVD_STATUS_UMAX_FALLBACK);
+                l = 0.f;
+            } else if (mx > m + 8.f) {
+                need = true;
+                alpha = exp2f(m - mx);
+                m = mx;
+                if (p.umax && active && p.status) atomicOr(p.status, KVD_STATUS_UMAX_FALLBACK);
             }
-            // P = 2^(s - m), packed per row and 8-column group (bf16 hi part; lo
+            // P = 2^(s - m), packed in pairs of adjacent tokens (bf16 hi part; lo
             // part for fp32 output).
-            uint32_t hiA[4], hiB[4], loA[4], loB[4];
-            float lsA = 0.f, lsB = 0.f;
+            uint32_t hi[HT / 2], lo[HT / 2];
+            float ls = 0.f;
 #pragma unroll
-            for (int g = 0; g < 4; ++g) {
-                const float e0 = actA ? tc::ex2_approx(s[4 * g] - mA) : 0.f;
-                const float e1 = actA ? tc::ex2_approx(s[4 * g + 1] - mA) : 0.f;
-                const float e2 = actB ? tc::ex2_approx(s[4 * g + 2] - mB) : 0.f;
-                const float e3 = actB ? tc::ex2_approx(s[4 * g + 3] - mB) : 0.f;
-                hiA[g] = pack_bf16x2(e0, e1);
-                hiB[g] = pack_bf16x2(e2, e3);
+            for (int g = 0; g < HT / 2; ++g) {
+                const float e0 = active ? tc::ex2_approx(s[2 * g] - m) : 0.f;
+                const float e1 = active ? tc::ex2_approx(s[2 * g + 1] - m) : 0.f;
+                hi[g] = pack_bf16x2(e0, e1);
                 if constexpr (F32OUT) {
-                    loA[g] = pack_bf16x2(e0 - bf16_lo(hiA[g]), e1 - bf16_hi(hiA[g]));
-                    loB[g] = pack_bf16x2(e2 - bf16_lo(hiB[g]), e3 - bf16_hi(hiB[g]));
-                    lsA += e0 + e1;
-                    lsB += e2 + e3;
+                    lo[g] = pack_bf16x2(e0 - bf16_lo(hi[g]), e1 - bf16_hi(hi[g]));
+                    ls += e0 + e1;
                 } else {
                     // The weights actually multiplied into V are the rounded ones;
                     // summing those keeps the output an exact convex combination.
-                    lsA += bf16_lo(hiA[g]) + bf16_hi(hiA[g]);
-                    lsB += bf16_lo(hiB[g]) + bf16_hi(hiB[g]);
+                    ls += bf16_lo(hi[g]) + bf16_hi(hi[g]);
                 }
             }
 
-            // O += P(i-1) V(i-1) must have completed: it reads the P buffer, and O
-            // is rescaled below if the running maximum moved.
-            if (i > 0) {
-                ok = __all_sync(0xffffffffu, tc::mbar_wait(o_fin((i - 1) & 1), ((i - 1) >> 1) & 1, abort_flag, kBudget));
+            // P buffer i & 1 is free once O += P(i-2) V(i-2) has completed.
+            const int pb = i & 1;
+            if (i >= 2) {
+                ok = __all_sync(0xffffffffu,
+                                tc::mbar_wait(o_fin(pb), ((i >> 1) - 1) & 1, abort_flag, kBudget));
                 if (!ok) break;
                 tc::fence_after_sync();
             }
-            if (__any_sync(0xffffffffu, needA || needB)) {
-                // O rows sit one per TMEM lane (lanes 0..15 of the quarter).
-                const float alpha = to_lane(alphaA, alphaB);
+            if (__any_sync(0xffffffffu, need)) {
+                // The running maximum moved: O (with P(i-1) V(i-1) in it) is
+                // rescaled before P(i) V(i) joins it.
+                ok = __all_sync(0xffffffffu,
+                                tc::mbar_wait(o_fin((i - 1) & 1), ((i - 1) >> 1) & 1, abort_flag, kBudget));
+                if (!ok) break;
+                tc::fence_after_sync();
 #pragma unroll 1
                 for (int cc = 0; cc < HD / 32; ++cc) {
                     uint32_t r[32];
-                    const uint32_t ta = tmem + lane_base + Sh::TMEM_O + half * HD + cc * 32;
-                    __syncwarp();
-                    tc::tmem_ld32(ta, r);
+                    const uint32_t ta = tmem + lane_base + Sh::TMEM_O + cc * 32;
+                    tc::tmem_ld_16x32bx2_x32<HD>(ta, r);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-                    tc::tmem_st32(ta, r);
-                }
-                tc::tmem_wait_st();
-            }
-            lA = lA * alphaA + lsA;
-            lB = lB * alphaB + lsB;
-            {
-                // Thread t addresses row t % 8 of matrix t / 8 (= 8-column group).
-                const int rin = lane & 7, gq = lane >> 3;
-                const uint32_t offA = (uint32_t)((quarter * 16 + rin) * 128 + (((half * 4 + gq) ^ rin) * 16));
-                const uint32_t offB = offA + 8 * 128;
-                stmatrix_x4(p_buf(sb, 0) + offA, hiA[0], hiA[1], hiA[2], hiA[3]);
-                stmatrix_x4(p_buf(sb, 0) + offB, hiB[0], hiB[1], hiB[2], hiB[3]);
-                if constexpr (F32OUT) {
-                    stmatrix_x4(p_buf(sb, 1) + offA, loA[0], loA[1], loA[2], loA[3]);
-                    stmatrix_x4(p_buf(sb, 1) + offB, loB[0], loB[1], loB[2], loB[3]);
+                    tc::tmem_st_16x32bx2_x32<HD>(ta, r);
                 }
             }
+            l = l * alpha + ls;
+            const uint32_t pt = tmem + lane_base + (uint32_t)(Sh::TMEM_P + pb * Sh::PCOLS);
+            tc::tmem_st_16x32bx2_x16<HT / 2>(pt, hi);
+            if constexpr (F32OUT) tc::tmem_st_16x32bx2_x16<HT / 2>(pt + T / 2, lo);
+            tc::tmem_wait_st();
+            const int nvalid = t.tok_hi - t.tok_lo;
             if (nvalid < T) {
                 // Rows past the sequence's end came from the cache's padding (or the
                 // next sequence): zero them so that 0-weights never meet NaN.
@@ -657,71 +643,57 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                 if (!ok) break;
                 uint8_t* vt = smem + Sh::OFF_V + sv * Sh::TILE_BYTES;
                 const int n16 = (T - nvalid) * KB * 8;
-                for (int idx = st; idx < n16; idx += 256) {
+                for (int idx = st; idx < n16; idx += 128) {
                     const int r = nvalid + idx / (KB * 8);
                     const int rem = idx % (KB * 8);
                     *reinterpret_cast<uint4*>(vt + (rem >> 3) * Sh::KB_BYTES + r * 128 + (rem & 7) * 16) =
                         make_uint4(0, 0, 0, 0);
                 }
+                tc::fence_proxy_async_smem();
             }
-            tc::fence_proxy_async_smem();
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(p_full(sb));
+            if (lane == 0) tc::mbar_arrive(p_full(pb));
 
             if (t.seg_end) {
-                float qA = lA + __shfl_xor_sync(0xffffffffu, lA, 1);
-                float qB = lB + __shfl_xor_sync(0xffffffffu, lB, 1);
-                qA += __shfl_xor_sync(0xffffffffu, qA, 2);
-                qB += __shfl_xor_sync(0xffffffffu, qB, 2);
-                float pA, pB;
-                exchange2(qA, qB, pA, pB, ok);
-                if (!ok) break;
-                // The epilogue works in the lane layout: this lane's row (lanes 0..15).
-                const float ltot = to_lane(qA + pA, qB + pB);
-                const float m_row = to_lane(mA, mB);
-                ok = __all_sync(0xffffffffu, tc::mbar_wait(o_fin(sb), (i >> 1) & 1, abort_flag, kBudget));
+                const float ltot = l + __shfl_xor_sync(0xffffffffu, l, 16);
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(o_fin(pb), (i >> 1) & 1, abort_flag, kBudget));
                 if (!ok) break;
                 tc::fence_after_sync();
                 const size_t pair = (size_t)t.b * p.Hkv + t.h;
                 const size_t qrow = (size_t)t.b * p.Hq + (size_t)t.h * G + row;
                 const size_t slot = (size_t)c + pair;
-                // O is read with the 16x256b shape as well, so every thread holds
-                // two rows (rA, rB) and 2 adjacent columns of each 8-column group:
-                // a quad writes 32 contiguous bytes of a row (one full sector).
-                const float totA = qA + pA, totB = qB + pB;
-                const float invA = t.full ? ((totA > 0.f) ? 1.f / totA : 0.f) : 1.f;
-                const float invB = t.full ? ((totB > 0.f) ? 1.f / totB : 0.f) : 1.f;
-                const size_t grow = t.full ? (size_t)t.b * p.Hq + (size_t)t.h * G : slot * G;  // row of head 0
+                // Each thread writes 32 contiguous columns of its row per step.
+                const float inv = t.full ? ((ltot > 0.f) ? 1.f / ltot : 0.f) : 1.f;
+                const size_t grow = t.full ? qrow : slot * G + row;  // output (or partial) row
 #pragma unroll 1
                 for (int cc = 0; cc < HD / 32; ++cc) {
-                    const int col0 = half * HD + cc * 32 + 2 * (lane & 3);
-                    uint32_t r[16];
-                    __syncwarp();
-                    tc::tmem_ld_16x256b_x4(tmem + lane_base + Sh::TMEM_O + half * HD + cc * 32, r);
+                    const int col0 = hl * HD + cc * 32;
+                    uint32_t r[32];
+                    tc::tmem_ld_16x32bx2_x32<HD>(tmem + lane_base + Sh::TMEM_O + cc * 32, r);
                     tc::tmem_wait_ld();
+                    if (active && t.full && !F32OUT) {
+                        uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + grow * D + col0);
 #pragma unroll
-                    for (int g = 0; g < 4; ++g) {
-                        const int col = col0 + 8 * g;
-                        const float a0 = __uint_as_float(r[4 * g]) * invA, a1 = __uint_as_float(r[4 * g + 1]) * invA;
-                        const float b0 = __uint_as_float(r[4 * g + 2]) * invB, b1 = __uint_as_float(r[4 * g + 3]) * invB;
-                        if (t.full && !F32OUT) {
-                            __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out);
-                            if (actA) *reinterpret_cast<uint32_t*>(o + (grow + rA) * D + col) = pack_bf16x2(a0, a1);
-                            if (actB) *reinterpret_cast<uint32_t*>(o + (grow + rB) * D + col) = pack_bf16x2(b0, b1);
-                        } else {
-                            float* o = t.full ? reinterpret_cast<float*>(p.out) : p.ws_o;
-                            if (actA) *reinterpret_cast<float2*>(o + (grow + rA) * D + col) = make_float2(a0, a1);
-                            if (actB) *reinterpret_cast<float2*>(o + (grow + rB) * D + col) = make_float2(b0, b1);
-                        }
+                        for (int k = 0; k < 4; ++k)
+                            o[k] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * k]) * inv, __uint_as_float(r[8 * k + 1]) * inv),
+                                              pack_bf16x2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv),
+                                              pack_bf16x2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv),
+                                              pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv));
+                    } else if (active) {
+                        float4* o = reinterpret_cast<float4*>((t.full ? reinterpret_cast<float*>(p.out) : p.ws_o) + grow * D + col0);
+#pragma unroll
+                        for (int k = 0; k < 8; ++k)
+                            o[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
+                                               __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
                     }
                 }
                 tc::fence_before_sync();
-                if (active && half == 0) {
+                if (active && hl == 0) {
                     if (t.full) {
-                        if (p.lse) p.lse[qrow] = (m_row + log2f(ltot)) * 0.69314718055994531f;
+                        if (p.lse) p.lse[qrow] = (m + log2f(ltot)) * 0.69314718055994531f;
                     } else {
-                        p.ws_ml[slot * G + row] = make_float2(m_row, ltot);
+                        p.ws_ml[slot * G + row] = make_float2(m, ltot);
                     }
                 }
             }
