@@ -160,6 +160,12 @@ struct AppendArgs {
     const void* k_new;
     const void* v_new;
     const int32_t* pos;
+    // The host-input step: the append also copies copy_bytes from copy_src
+    // (page-locked host memory the device addresses) to copy_dst (the staged
+    // queries), and the attention's Q loads wait for it.
+    const void* copy_src = nullptr;
+    void* copy_dst = nullptr;
+    size_t copy_bytes = 0;
 };
 
 kvd_status check_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
@@ -283,6 +289,8 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
     if (app) {
+        int copy_sms = 0;
+        if (app->copy_bytes > 0 && device_sms(&copy_sms) != KVD_OK) return KVD_ERR_CUDA;
         // The append, then the chunk kernel in early mode: it starts (and works
         // out its schedule) while the append runs, and only its cache loads
         // wait for the append's grid.
@@ -291,9 +299,11 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
             q8 ? launch_append_q8(app->k_cache, app->v_cache, q8->k_scale, q8->v_scale, app->k_new, app->v_new,
                                   app->pos, batch, s_max, Hkv, D, status, pg ? *pg : none, s, T, q8->fp8)
                : launch_append(app->k_cache, app->v_cache, app->k_new, app->v_new, app->pos, batch, s_max, Hkv,
-                               D, status, pg ? *pg : none, s, T);
+                               D, status, pg ? *pg : none, s, T, app->copy_src, app->copy_dst, app->copy_bytes,
+                               copy_sms);  // one CTA per SM: the attention's CTAs fit beside them
         if (e != cudaSuccess) return KVD_ERR_CUDA;
         p.early = 1;
+        p.q_wait = app->copy_bytes > 0 ? 1 : 0;
         p.pos = app->pos;
     }
     if (phase & kChunk) {
@@ -481,7 +491,29 @@ kvd_status kvd_decode_step_host(void* k_cache, void* v_cache, const void* q_host
     const bool packed = k_new_host == at(k_new) && v_new_host == at(v_new) &&
                         reinterpret_cast<const uint8_t*>(pos_host) == at(pos) &&
                         reinterpret_cast<const uint8_t*>(seq_lens_host) == at(seq_lens);
-    if (packed) {
+    // A packet the device can address (page-locked and mapped): the append
+    // reads k_new, v_new and pos from it and copies q into the staging buffer,
+    // and the attention reads pos and seq_lens from it, so that the host
+    // link's transfer overlaps the attention's start (its cache loads run
+    // meanwhile; its Q loads wait for the append). Otherwise the inputs are
+    // copied in first (one cudaMemcpyAsync for a packet, else five).
+    cudaPointerAttributes pa;
+    const bool mapped = packed && cudaPointerGetAttributes(&pa, q_host) == cudaSuccess &&
+                        pa.type == cudaMemoryTypeHost && pa.devicePointer && aligned(pa.devicePointer, 256);
+    if (!mapped) (void)cudaGetLastError();
+    AppendArgs app{k_cache, v_cache, k_new, v_new, pos};
+    const int32_t* lens_dev = seq_lens;
+    if (mapped) {
+        const uint8_t* hd = static_cast<const uint8_t*>(pa.devicePointer);
+        auto dev_at = [&](const void* staged) { return hd + (static_cast<const uint8_t*>(staged) - stg); };
+        app.k_new = dev_at(k_new);
+        app.v_new = dev_at(v_new);
+        app.pos = reinterpret_cast<const int32_t*>(dev_at(pos));
+        app.copy_src = hd;
+        app.copy_dst = q;
+        app.copy_bytes = qb;
+        lens_dev = reinterpret_cast<const int32_t*>(dev_at(seq_lens));
+    } else if (packed) {
         const size_t total = static_cast<const uint8_t*>(static_cast<const void*>(seq_lens)) + ib - stg;
         if (cudaMemcpyAsync(staging, q_host, total, cudaMemcpyHostToDevice, s) != cudaSuccess) return KVD_ERR_CUDA;
     } else {
@@ -491,8 +523,7 @@ kvd_status kvd_decode_step_host(void* k_cache, void* v_cache, const void* q_host
         for (const auto& c : h2d)
             if (cudaMemcpyAsync(c.dst, c.src, c.n, cudaMemcpyHostToDevice, s) != cudaSuccess) return KVD_ERR_CUDA;
     }
-    const AppendArgs app{k_cache, v_cache, k_new, v_new, pos};
-    st = decode(kBoth, q, k_cache, v_cache, seq_lens, batch, s_max, max_seq_len, n_heads_q, n_heads_kv, head_dim,
+    st = decode(kBoth, q, k_cache, v_cache, lens_dev, batch, s_max, max_seq_len, n_heads_q, n_heads_kv, head_dim,
                 scale, n_split, workspace, workspace_bytes, out_dev, out_dtype, lse_out, status_word, stream, &app,
                 nullptr, nullptr, n_tokens);
     if (st != KVD_OK) return st;

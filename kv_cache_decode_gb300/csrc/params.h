@@ -21,6 +21,9 @@ struct DecodeParams {
     // complete when the launch began, so only the cache loads wait for the
     // preceding grid.
     int early;
+    // Early mode after the host-input step's append, which also stages q: the
+    // Q loads wait for the append's grid as well.
+    int q_wait;
     const int32_t* pos;   // early mode: where the append put each sequence's new row
     void* out;            // bf16 or fp32 [B, Hq, D]
     float* lse;           // optional fp32 [B, Hq]
@@ -93,7 +96,9 @@ struct PagedCache {
 // T rows per sequence (k_new [B, T, Hkv, D]) go to pos[b] .. pos[b] + T - 1.
 cudaError_t launch_append(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                           const int32_t* pos, int B, int S_max, int Hkv, int D,
-                          int32_t* status, const PagedCache& pg, cudaStream_t stream, int T = 1);
+                          int32_t* status, const PagedCache& pg, cudaStream_t stream, int T = 1,
+                          const void* copy_src = nullptr, void* copy_dst = nullptr, size_t copy_bytes = 0,
+                          int copy_blocks = 0);
 // int8 cache (kv_quant.cu): the append quantizes the new rows (into pages
 // when pg.block_table is set); the bulk conversion quantizes rows
 // t < seq_lens[b] of a bf16 cache.

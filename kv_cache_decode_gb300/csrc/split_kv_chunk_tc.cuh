@@ -400,6 +400,8 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
         // so its load is short when its turn comes.
         if (lane == 0) {
             const uint64_t pol_q = tc::l2_evict_last_policy();
+            // q staged by the preceding append (host-input step): wait for it.
+            if (p.early && p.q_wait) pdl_wait();
             Tile t;
             int qn = 0;
             while (walker.next(t, NoOp{})) {
