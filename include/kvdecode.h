@@ -514,7 +514,13 @@ kvd_status kvd_merge_attention(const void* outs, const float* lses, int n_shards
  * writing `out` on the device, and `out` is copied to out_host (same size).
  * Host inputs laid out like the staging buffer (q | k_new | v_new | pos |
  * seq_lens, each 256-byte aligned, one host packet starting at q_host) are
- * copied with one cudaMemcpyAsync instead of five. With out = NULL the kernels
+ * copied with one cudaMemcpyAsync instead of five; if that packet is
+ * page-locked memory the device addresses (256-byte aligned), nothing is
+ * copied ahead: the append kernel reads k_new, v_new and pos from it and pulls
+ * q into `staging` over the host link while the attention's cache loads run,
+ * and the attention reads pos and seq_lens from it (q's loads wait for the
+ * append). The packet must then stay unchanged until the call's work on
+ * `stream` is done. With out = NULL the kernels
  * write the result straight into out_host, which must then be page-locked
  * host memory the device can address (cudaHostAlloc / cudaHostRegister, 16-byte
  * aligned; else KVD_ERR_INVALID_ARG), and no copy back is queued.
