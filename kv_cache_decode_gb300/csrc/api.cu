@@ -27,11 +27,11 @@ const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool
 // differ); the mma.sync kernel has a compiled variant per form. int8 caches
 // (contiguous or paged) run on the mma.sync kernel, whose CTAs take 16 of a
 // pair's rows each, for every group.
-const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8, bool fp8) {
+const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8, bool fp8, int T) {
     if (group < 1 || group > KVD_MAX_GROUP) return nullptr;
     if (kv8) return mma_chunk_kernel(head_dim, f32_out, paged, true, fp8);
     if (group <= 16) return mma_chunk_kernel(head_dim, f32_out, paged, false, false);
-    return tc_chunk_kernel(head_dim, f32_out, group);
+    return tc_chunk_kernel(head_dim, f32_out, group, T);
 }
 
 namespace {
@@ -70,8 +70,8 @@ kvd_status check_shape(int batch, int Hq, int Hkv, int D, kvd_out_dtype dt) {
 // planned for the single-token bf16 kernel of the shape whatever the cache
 // dtype and query tokens, so that one plan sizes every form's workspace.
 const ChunkKernel* pick_kernel(int Hq, int Hkv, int D, kvd_out_dtype dt, bool paged = false, bool kv8 = false,
-                               bool fp8 = false) {
-    return find_chunk_kernel(D, Hq / Hkv, dt == KVD_OUT_F32, paged, kv8, fp8);
+                               bool fp8 = false, int T = 1) {
+    return find_chunk_kernel(D, Hq / Hkv, dt == KVD_OUT_F32, paged, kv8, fp8, T);
 }
 
 // int8 cache: the row scales of K and V.
@@ -210,15 +210,16 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     if (st != KVD_OK) return st;
     if (q8 && (!q8->k_scale || !q8->v_scale || !aligned(q8->k_scale, 4) || !aligned(q8->v_scale, 4)))
         return KVD_ERR_INVALID_ARG;
-    k = pick_kernel(Hq, Hkv, D, dt, pg != nullptr, q8 != nullptr, q8 && q8->fp8);
+    k = pick_kernel(Hq, Hkv, D, dt, pg != nullptr, q8 != nullptr, q8 && q8->fp8, T);
     if (!k) return KVD_ERR_UNSUPPORTED;
     // The tensor-core path addresses cache rows and query rows with 32-bit TMA coordinates.
     if (k->tensor_core && (cache_rows > 0x7fffffffLL || (long long)batch * T * Hq > 0x7fffffffLL))
         return KVD_ERR_UNSUPPORTED;
     // mma.sync kernel: 16 of a pair's T * G rows per CTA. tcgen05 kernel: T
-    // query tokens as T virtual sequences of one query token each.
+    // query tokens stacked in one 128-row tile, or (when they do not fit) as T
+    // virtual sequences of one query token each.
     const int row_blocks = k->tensor_core ? 1 : (Hq / Hkv * T + 15) / 16;
-    const int vT = k->tensor_core ? T : 1;
+    const int vT = (k->tensor_core && k->mma_rows != 128) ? T : 1;
     if (n_split_req == 0 && row_blocks > 1) {
         // The heuristic split fills the GPU with one CTA per resident slot; a
         // pair in row blocks launches row_blocks CTAs per token run, so the

@@ -44,9 +44,10 @@ struct DecodeParams {
     const float* v_scale;
     int kv_fp8;
     // Query tokens per sequence (1, or T > 1 for a speculative check step on
-    // the mma.sync kernel): q, out [B, T, Hq, D], lse [B, T, Hq]; query token i
-    // of sequence b attends to its first seq_lens[b] - T + 1 + i tokens, and
-    // the workspace holds T * G rows per slot.
+    // the mma.sync kernel or the tcgen05 kernel's 128-row variant): q, out
+    // [B, T, Hq, D], lse [B, T, Hq]; query token i of sequence b attends to its
+    // first seq_lens[b] - T + 1 + i tokens, and the workspace holds T * G rows
+    // per slot.
     int T;
     // mma.sync kernel: blocks of 16 of a pair's T * G rows, one CTA each per
     // token run (n_split * row_blocks CTAs); 1 for the tcgen05 kernel.
@@ -71,17 +72,19 @@ struct ChunkKernel {
     int seg_unit;    // tokens per schedule position (1 or tile_tokens, see schedule.cuh)
     int seg_cost;    // positions charged per pair by the schedule
     bool f32_out, tensor_core;
+    int mma_rows;  // tcgen05 kernel: rows of its MMAs (128: several query tokens of a sequence in one tile)
     int index;  // position in the variant table (0..59), for the per-device attribute bitmask
 };
 
 // The kernel for a shape: bf16 groups of up to 16 query heads per KV head run
 // on the mma.sync kernel (T query tokens as T * G rows, in blocks of 16),
-// wider groups (17..64) on the tcgen05 kernel (T query tokens as T virtual
+// wider groups (17..64) on the tcgen05 kernel (T query tokens stacked in one
+// 128-row tile when T times the group rounded up to 8 fits, else as T virtual
 // sequences); int8 caches run on the mma.sync kernel for every group.
 const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8 = false,
-                                     bool fp8 = false);
+                                     bool fp8 = false, int T = 1);
 const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool kv8, bool fp8);
-const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out, int group);
+const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out, int group, int T = 1);
 
 cudaError_t launch_merge(const DecodeParams& p, int head_dim, bool f32_out, int num_sms, cudaStream_t stream);
 // Results of disjoint token shards combined by their normalisers (split_kv_merge.cu).

@@ -39,12 +39,13 @@ const ChunkKernel* tc_table_d64(bool f32, int qr);
 const ChunkKernel* tc_table_d128(bool f32, int qr);
 const ChunkKernel* tc_table_d256(bool f32, int qr);
 
-// Q is stored in blocks of the group size rounded up (8, 16, 48 or 64 rows):
-// narrow groups then fit a ring of Q slots, and groups of up to 48 leave room
-// for a third K stage at head_dim 256.
-const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out, int group) {
-    if (group < 1 || group > 64) return nullptr;
-    const int qr = group <= 8 ? 8 : (group <= 16 ? 16 : (group <= 48 ? 48 : 64));
+// Q is stored in blocks of the group size rounded up (48 or 64 rows: groups
+// of up to 48 leave room for a third K stage at head_dim 256); several query
+// tokens whose rows (T times the group rounded up to 8) fit in 128 run on the
+// 128-row variant, which stacks them in one tile.
+const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out, int group, int T) {
+    if (group < 17 || group > 64 || T < 1) return nullptr;
+    const int qr = (T > 1 && T * ((group + 7) & ~7) <= 128) ? 128 : (group <= 48 ? 48 : 64);
     switch (head_dim) {
         case 64: return tc_table_d64(f32_out, qr);
         case 128: return tc_table_d128(f32_out, qr);

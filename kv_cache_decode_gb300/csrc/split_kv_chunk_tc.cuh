@@ -45,9 +45,12 @@
 
 namespace kvd {
 
-template <int D, bool F32OUT, int QR>
+// MR: rows of the MMAs (64, or 128 for several query tokens of a sequence
+// stacked in one tile); QR: Q rows stored per head_dim block.
+template <int D, bool F32OUT, int QR, int MR = 64>
 struct TcShape {
     static constexpr int T = 64;                 // tokens per tile
+    static constexpr int NG = MR / 64;           // 16-row groups per softmax thread
     // Schedule: runs balanced in whole tiles (a tile's time is set by the
     // pipeline's latency, whatever its length), plus one tile's charge for
     // starting a pair inside a run (its Q load and first K tile).
@@ -92,11 +95,13 @@ struct TcShape {
     static constexpr int TMEM_O = 256;           // O at columns [256, 256 + D)
     static constexpr int TMEM_COLS = 512;
     // producers 0 (K) and 2 (V), S issuers 1 and 7, O issuer 8, Q loader 9, softmax 3..6
-    static constexpr int NWARPS = 10;
+    // (and at MR = 128, 10..13 for the quarters' second group of 16 rows)
+    static constexpr int NSW = 4 * NG;           // softmax warps
+    static constexpr int NWARPS = 6 + NSW;
     static constexpr int THREADS = NWARPS * 32;
     static_assert(KST >= 2, "need at least two K stages");
     static_assert(SMEM_BYTES + STATIC_SMEM <= 227 * 1024, "shared memory budget");
-    static_assert(QR % 8 == 0 && QR <= 64, "Q rows per block");
+    static_assert(QR % 8 == 0 && QR <= MR && (MR == 64 || MR == 128), "Q rows per block");
     static_assert(TMEM_P + 2 * PCOLS <= TMEM_O && TMEM_O + D <= TMEM_COLS, "TMEM columns");
 };
 
@@ -106,10 +111,10 @@ struct TcMaps {
     CUtensorMap v;
 };
 
-template <int D, bool F32OUT, int QR>
-__global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
+template <int D, bool F32OUT, int QR, int MR>
+__global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
     split_kv_chunk_tc_kernel(const DecodeParams p, const __grid_constant__ TcMaps maps) {
-    using Sh = TcShape<D, F32OUT, QR>;
+    using Sh = TcShape<D, F32OUT, QR, MR>;
     constexpr int T = Sh::T, KB = Sh::KB, KST = Sh::KST, VST = Sh::VST, NW = Sh::NWARPS,
                   SEG_COST = Sh::SEG_COST;
     constexpr long long kBudget = 4000000000LL;  // ~2 s of clock cycles per wait
@@ -168,9 +173,9 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             tc::mbar_init(q_empty(s), 2);
         }
         tc::mbar_init(s_full, 2);  // both S issuers
-        tc::mbar_init(s_free, 4);  // the softmax warps
+        tc::mbar_init(s_free, Sh::NSW);  // the softmax warps
         for (int b = 0; b < 2; ++b) {
-            tc::mbar_init(p_full(b), 4);
+            tc::mbar_init(p_full(b), Sh::NSW);
             tc::mbar_init(o_fin(b), 1);
         }
         tc::mbar_init(mma_done, 3);  // S issuers and O issuer
@@ -408,19 +413,27 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                 if (!t.seg_start) continue;
                 const int qs = qn % NQ;
                 if (!tc::mbar_wait(q_empty(qs), ((qn / NQ) & 1) ^ 1, abort_flag, kBudget)) break;
-                tc::mbar_arrive_expect_tx(q_full(qs), (uint32_t)(KB * 128 * G));
-                const int qrow = t.b * p.Hq + t.h * G;
+                // The pair's query rows: its G heads, or at M = 128 the G heads
+                // of each of the sequence's TQ query tokens, token i at rows
+                // i * G8 (8-row aligned, as the swizzled layout needs).
+                const int TQ = (MR == 128) ? p.T : 1, G8 = (G + 7) & ~7;
+                tc::mbar_arrive_expect_tx(q_full(qs), (uint32_t)(KB * 128 * G * TQ));
+                for (int i2 = 0; i2 < TQ; ++i2) {
+                    const int qrow = (t.b * TQ + i2) * p.Hq + t.h * G;
 #pragma unroll
-                for (int kb = 0; kb < KB; ++kb)
-                    tc::tma_load_2d(sQ + qs * Sh::QS_BYTES + kb * Sh::QB_BYTES, &maps.q, kb * 64, qrow, q_full(qs),
-                                    pol_q);
+                    for (int kb = 0; kb < KB; ++kb)
+                        tc::tma_load_2d(sQ + qs * Sh::QS_BYTES + kb * Sh::QB_BYTES + i2 * G8 * 128, &maps.q, kb * 64,
+                                        qrow, q_full(qs), pol_q);
+                }
                 ++qn;
                 if (walker.pstart + walker.ext() < walker.E) {
                     const int nh = (t.h + 1 < p.Hkv) ? t.h + 1 : 0;
                     const int nb = (t.h + 1 < p.Hkv) ? t.b : t.b + 1;
                     if (nb < p.B)
-                        tc::prefetch_l2(reinterpret_cast<const uint8_t*>(p.q) + ((size_t)nb * p.Hq + (size_t)nh * G) * D * 2,
-                                        (uint32_t)(G * D * 2));
+                        for (int i2 = 0; i2 < TQ; ++i2)
+                            tc::prefetch_l2(reinterpret_cast<const uint8_t*>(p.q) +
+                                                (((size_t)nb * TQ + i2) * p.Hq + (size_t)nh * G) * D * 2,
+                                            (uint32_t)(G * D * 2));
                 }
             }
             if (qn > 0) tc::mbar_wait(q_full((qn - 1) % NQ), ((qn - 1) / NQ) & 1, abort_flag, kBudget / 4);
@@ -437,7 +450,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
         if (lane == 0) {
             const int kh = (warp == 7) ? 1 : 0;
             constexpr int KH = D / 32;  // k-steps per half
-            constexpr uint32_t idesc_s = tc::idesc_bf16_f32(64, T, false, false);
+            constexpr uint32_t idesc_s = tc::idesc_bf16_f32(MR, T, false, false);
             const uint32_t s_base = tmem + (kh ? Sh::TMEM_S2 : Sh::TMEM_S);
             Tile t;
             int i = 0, qn = 0;
@@ -474,7 +487,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
         // O += P(i) V(i): A = P from TMEM buffer i & 1 (the hi part, then the
         // lo part for fp32 output), B = the V stage in MN-major layout.
         if (lane == 0) {
-            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(64, D, false, true);
+            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(MR, D, false, true);
             Tile t;
             int i = 0;
             while (walker.next(t, NoOp{})) {
@@ -499,42 +512,66 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             tc::mma_commit(mma_done);
             tc::mbar_wait(mma_done, 0, abort_flag, kBudget);
         }
-    } else if (warp >= 3 && warp <= 6) {
-        // ===================== softmax / epilogue (warps 3..6) =====================
+    } else if ((warp >= 3 && warp <= 6) || warp >= 10) {
+        // ===================== softmax / epilogue (warps 3..6, 10..13) =====================
         // One warp per TMEM lane quarter (a warp reaches the 32 lanes
-        // 32 * (warp % 4) ...), whose 16 accumulator rows are query heads
-        // 16 * quarter ... 16 * quarter + 15. Through the 16x32bx2 shape each
-        // head goes to two threads of the warp: thread l takes head
-        // 16 * quarter + l % 16 and token columns [32 (l / 16), 32 (l / 16) + 32)
-        // of every S tile (P columns likewise), and output columns
-        // [(D / 2)(l / 16), (D / 2)(l / 16) + D / 2) in the epilogue. A row's
-        // maximum and sum need one shuffle between its two threads; no other
-        // warp takes part.
+        // 32 * (warp % 4) ...). At M = 64 its accumulator rows sit in lanes
+        // 0-15 of the quarter (rows 16 q .. 16 q + 15); at M = 128 in all 32
+        // lanes (rows 32 q .. 32 q + 31), two groups of 16, each with a warp of
+        // its own (warps 3..6 the first, 10..13 the second). Through
+        // the 16x32bx2 shape each row goes to two threads of the warp: thread
+        // l takes row (16 lanes of the warp's group) + l % 16 and token columns
+        // [32 (l / 16), 32 (l / 16) + 32) of every S tile (P columns
+        // likewise), and output columns [(D / 2)(l / 16), ...) in the
+        // epilogue. A row's maximum and sum need one shuffle between its two
+        // threads; no other warp takes part.
+        // Rows: at M = 64 the group's query heads; at M = 128 the T query
+        // tokens of a sequence stacked (row = token * G8 + head, G8 = the group
+        // rounded up to 8), token i seeing the first L - T + 1 + i tokens.
+        constexpr int NG = 1;                        // row groups per warp
+        constexpr int NST = Sh::NSW * 32;            // softmax threads
         constexpr int HT = T / 2;   // token columns per thread
         constexpr int HD = D / 2;   // output columns per thread
         const int quarter = warp & 3;
+        const int rgw = warp >= 10 ? 1 : 0;          // this warp's group of 16 rows in its quarter
         const int hl = lane >> 4;
-        const int row = quarter * 16 + (lane & 15);  // group-local query head of this thread
-        const bool active = row < G;
-        const int st = tid - 3 * 32;                 // 0..127 among the softmax threads
-        const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
+        const int st = (warp >= 10 ? warp - 6 : warp - 3) * 32 + lane;  // 0..NST-1 among the softmax threads
         const float scale_log2 = p.scale_log2;
-
-        auto write_empty = [&](int b, int h) {
-            const size_t r0 = (size_t)b * p.Hq + (size_t)h * G;
-            if constexpr (F32OUT) {
-                float* o = reinterpret_cast<float*>(p.out) + r0 * D;
-                for (int i2 = st; i2 < G * D; i2 += 128) o[i2] = 0.f;
-            } else {
-                __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + r0 * D;
-                for (int i2 = st; i2 < G * D; i2 += 128) o[i2] = __float2bfloat16_rn(0.f);
-            }
-            if (p.lse)
-                for (int i2 = st; i2 < G; i2 += 128) p.lse[r0 + i2] = -CUDART_INF_F;
+        const int TQ = (MR == 128) ? p.T : 1;        // query tokens stacked in the rows
+        const int G8 = (G + 7) & ~7;
+        int tok_[NG], hd_[NG];
+        bool act_[NG];
+#pragma unroll
+        for (int rg = 0; rg < NG; ++rg) {
+            const int row = quarter * 16 * Sh::NG + 16 * (rg + rgw) + (lane & 15);
+            tok_[rg] = (MR == 128) ? row / G8 : 0;
+            hd_[rg] = (MR == 128) ? row - tok_[rg] * G8 : row;
+            act_[rg] = tok_[rg] < TQ && hd_[rg] < G;
+        }
+        auto lanes = [&](int rg) { return (uint32_t)(quarter * 32 + 16 * (rg + rgw)) << 16; };
+        // Output (or lse) row of (sequence b, KV head h, token i, head g); partial-state row within a slot.
+        auto out_row = [&](int b, int h, int i2, int g) {
+            return ((size_t)b * TQ + i2) * p.Hq + (size_t)h * G + g;
         };
 
-        float m = 0.f;  // running maximum of this thread's row (the same in both of its threads)
-        float l = 0.f;  // this thread's share of the row sum
+        auto write_empty = [&](int b, int h) {
+            for (int i2 = 0; i2 < TQ; ++i2) {
+                const size_t r0 = out_row(b, h, i2, 0);
+                if constexpr (F32OUT) {
+                    float* o = reinterpret_cast<float*>(p.out) + r0 * D;
+                    for (int k = st; k < G * D; k += NST) o[k] = 0.f;
+                } else {
+                    __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(p.out) + r0 * D;
+                    for (int k = st; k < G * D; k += NST) o[k] = __float2bfloat16_rn(0.f);
+                }
+                if (p.lse)
+                    for (int k = st; k < G; k += NST) p.lse[r0 + k] = -CUDART_INF_F;
+            }
+        };
+
+        float m[NG], l[NG];  // running maximum of each row (the same in both of its threads); row-sum share
+#pragma unroll
+        for (int rg = 0; rg < NG; ++rg) m[rg] = l[rg] = 0.f;
         Tile t;
         int i = 0;
         bool ok = true;
@@ -543,68 +580,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             if (!ok) break;
             tc::fence_after_sync();
             __syncwarp();
-            // S is held as two partial sums over the halves of head_dim.
-            float s[HT];
-            {
-                uint32_t sa[HT], sb[HT];
-                tc::tmem_ld_16x32bx2_x32<HT>(tmem + lane_base + Sh::TMEM_S, sa);
-                tc::tmem_ld_16x32bx2_x32<HT>(tmem + lane_base + Sh::TMEM_S2, sb);
-                tc::tmem_wait_ld();
-                tc::fence_before_sync();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(s_free);
-                // Scores in base-2 units; columns past the tile's last token masked.
-                const int nv = (t.tok_hi - t.tok_lo) - hl * HT;  // valid columns of this thread (may be <= 0)
-#pragma unroll
-                for (int e = 0; e < HT; ++e)
-                    s[e] = (e < nv) ? (__uint_as_float(sa[e]) + __uint_as_float(sb[e])) * scale_log2 : -CUDART_INF_F;
-            }
-            float mx = s[0];
-#pragma unroll
-            for (int e = 1; e < HT; ++e) mx = fmaxf(mx, s[e]);
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-
-            bool need = false;
-            float alpha = 1.f;
-            if (t.seg_start) {
-                m = mx;
-                if (p.umax) {
-                    // Unified maximum (FlashDecoding++'s asynchronized softmax):
-                    // a row whose first tile's maximum lies within [phi - 64,
-                    // phi + 8] (base 2) takes m = phi, shared by all partials of
-                    // such rows, so the merge reduces to plain sums; otherwise
-                    // it starts from its own maximum. The lazy rescale below
-                    // moves m up past phi + 8 (exact either way).
-                    const float phi2 = p.umax_phi2;
-                    if (mx >= phi2 - 64.f && mx <= phi2 + 8.f) m = phi2;
-                    if (active && m != phi2 && p.status) atomicOr(p.status, KVD_STATUS_UMAX_FALLBACK);
-                }
-                l = 0.f;
-            } else if (mx > m + 8.f) {
-                need = true;
-                alpha = exp2f(m - mx);
-                m = mx;
-                if (p.umax && active && p.status) atomicOr(p.status, KVD_STATUS_UMAX_FALLBACK);
-            }
-            // P = 2^(s - m), packed in pairs of adjacent tokens (bf16 hi part; lo
-            // part for fp32 output).
-            uint32_t hi[HT / 2], lo[HT / 2];
-            float ls = 0.f;
-#pragma unroll
-            for (int g = 0; g < HT / 2; ++g) {
-                const float e0 = active ? tc::ex2_approx(s[2 * g] - m) : 0.f;
-                const float e1 = active ? tc::ex2_approx(s[2 * g + 1] - m) : 0.f;
-                hi[g] = pack_bf16x2(e0, e1);
-                if constexpr (F32OUT) {
-                    lo[g] = pack_bf16x2(e0 - bf16_lo(hi[g]), e1 - bf16_hi(hi[g]));
-                    ls += e0 + e1;
-                } else {
-                    // The weights actually multiplied into V are the rounded ones;
-                    // summing those keeps the output an exact convex combination.
-                    ls += bf16_lo(hi[g]) + bf16_hi(hi[g]);
-                }
-            }
-
+            const int nvalid = t.tok_hi - t.tok_lo;
             // P buffer i & 1 is free once O += P(i-2) V(i-2) has completed.
             const int pb = i & 1;
             if (i >= 2) {
@@ -613,30 +589,107 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                 if (!ok) break;
                 tc::fence_after_sync();
             }
-            if (__any_sync(0xffffffffu, need)) {
-                // The running maximum moved: O (with P(i-1) V(i-1) in it) is
+            float alpha[NG];
+            bool need_any = false;
+#pragma unroll
+            for (int rg = 0; rg < NG; ++rg) {
+                // S is held as two partial sums over the halves of head_dim.
+                float s[HT];
+                {
+                    uint32_t sa[HT], sb[HT];
+                    tc::tmem_ld_16x32bx2_x32<HT>(tmem + lanes(rg) + Sh::TMEM_S, sa);
+                    tc::tmem_ld_16x32bx2_x32<HT>(tmem + lanes(rg) + Sh::TMEM_S2, sb);
+                    tc::tmem_wait_ld();
+                    if (rg == NG - 1) {
+                        tc::fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(s_free);
+                    }
+                    // Scores in base-2 units; columns past the tile's last token
+                    // (or, at M = 128, past the row's token's causal limit) masked.
+                    int vis = nvalid;
+                    if (MR == 128) vis = min(vis, t.L - (TQ - 1 - tok_[rg]) - t.tok_lo);
+                    const int nv = vis - hl * HT;  // valid columns of this thread (may be <= 0)
+#pragma unroll
+                    for (int e = 0; e < HT; ++e)
+                        s[e] = (e < nv) ? (__uint_as_float(sa[e]) + __uint_as_float(sb[e])) * scale_log2
+                                        : -CUDART_INF_F;
+                }
+                float mx = s[0];
+#pragma unroll
+                for (int e = 1; e < HT; ++e) mx = fmaxf(mx, s[e]);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const bool active = act_[rg];
+                alpha[rg] = 1.f;
+                if (t.seg_start) {
+                    m[rg] = mx;
+                    if (p.umax) {
+                        // Unified maximum (FlashDecoding++'s asynchronized softmax):
+                        // a row whose first tile's maximum lies within [phi - 64,
+                        // phi + 8] (base 2) takes m = phi, shared by all partials of
+                        // such rows, so the merge reduces to plain sums; otherwise
+                        // it starts from its own maximum. The lazy rescale below
+                        // moves m up past phi + 8 (exact either way).
+                        const float phi2 = p.umax_phi2;
+                        if (mx >= phi2 - 64.f && mx <= phi2 + 8.f) m[rg] = phi2;
+                        if (active && m[rg] != phi2 && p.status) atomicOr(p.status, KVD_STATUS_UMAX_FALLBACK);
+                    }
+                    l[rg] = 0.f;
+                } else if (mx > m[rg] + 8.f) {
+                    // (a row with no visible column yet keeps m = -inf and takes its first maximum here)
+                    need_any = true;
+                    alpha[rg] = (m[rg] == -CUDART_INF_F) ? 0.f : exp2f(m[rg] - mx);
+                    m[rg] = mx;
+                    if (p.umax && active && p.status) atomicOr(p.status, KVD_STATUS_UMAX_FALLBACK);
+                }
+                // P = 2^(s - m), packed in pairs of adjacent tokens (bf16 hi part;
+                // lo part for fp32 output). A row that has seen no column yet
+                // (m = -inf, M = 128 only) gives zeros.
+                const bool live = active && m[rg] != -CUDART_INF_F;
+                uint32_t hi[HT / 2], lo[HT / 2];
+                float ls = 0.f;
+#pragma unroll
+                for (int g = 0; g < HT / 2; ++g) {
+                    const float e0 = live ? tc::ex2_approx(s[2 * g] - m[rg]) : 0.f;
+                    const float e1 = live ? tc::ex2_approx(s[2 * g + 1] - m[rg]) : 0.f;
+                    hi[g] = pack_bf16x2(e0, e1);
+                    if constexpr (F32OUT) {
+                        lo[g] = pack_bf16x2(e0 - bf16_lo(hi[g]), e1 - bf16_hi(hi[g]));
+                        ls += e0 + e1;
+                    } else {
+                        // The weights actually multiplied into V are the rounded ones;
+                        // summing those keeps the output an exact convex combination.
+                        ls += bf16_lo(hi[g]) + bf16_hi(hi[g]);
+                    }
+                }
+                l[rg] = l[rg] * alpha[rg] + ls;
+                const uint32_t pt = tmem + lanes(rg) + (uint32_t)(Sh::TMEM_P + pb * Sh::PCOLS);
+                tc::tmem_st_16x32bx2_x16<HT / 2>(pt, hi);
+                if constexpr (F32OUT) tc::tmem_st_16x32bx2_x16<HT / 2>(pt + T / 2, lo);
+            }
+            if (__any_sync(0xffffffffu, need_any)) {
+                // A running maximum moved: O (with P(i-1) V(i-1) in it) is
                 // rescaled before P(i) V(i) joins it.
                 ok = __all_sync(0xffffffffu,
                                 tc::mbar_wait(o_fin((i - 1) & 1), ((i - 1) >> 1) & 1, abort_flag, kBudget));
                 if (!ok) break;
                 tc::fence_after_sync();
-#pragma unroll 1
-                for (int cc = 0; cc < HD / 32; ++cc) {
-                    uint32_t r[32];
-                    const uint32_t ta = tmem + lane_base + Sh::TMEM_O + cc * 32;
-                    tc::tmem_ld_16x32bx2_x32<HD>(ta, r);
-                    tc::tmem_wait_ld();
 #pragma unroll
-                    for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha);
-                    tc::tmem_st_16x32bx2_x32<HD>(ta, r);
+                for (int rg = 0; rg < NG; ++rg) {
+                    if (!__any_sync(0xffffffffu, alpha[rg] != 1.f)) continue;
+#pragma unroll 1
+                    for (int cc = 0; cc < HD / 32; ++cc) {
+                        uint32_t r[32];
+                        const uint32_t ta = tmem + lanes(rg) + Sh::TMEM_O + cc * 32;
+                        tc::tmem_ld_16x32bx2_x32<HD>(ta, r);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) r[k] = __float_as_uint(__uint_as_float(r[k]) * alpha[rg]);
+                        tc::tmem_st_16x32bx2_x32<HD>(ta, r);
+                    }
                 }
             }
-            l = l * alpha + ls;
-            const uint32_t pt = tmem + lane_base + (uint32_t)(Sh::TMEM_P + pb * Sh::PCOLS);
-            tc::tmem_st_16x32bx2_x16<HT / 2>(pt, hi);
-            if constexpr (F32OUT) tc::tmem_st_16x32bx2_x16<HT / 2>(pt + T / 2, lo);
             tc::tmem_wait_st();
-            const int nvalid = t.tok_hi - t.tok_lo;
             if (nvalid < T) {
                 // Rows past the sequence's end came from the cache's padding (or the
                 // next sequence): zero them so that 0-weights never meet NaN.
@@ -645,7 +698,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
                 if (!ok) break;
                 uint8_t* vt = smem + Sh::OFF_V + sv * Sh::TILE_BYTES;
                 const int n16 = (T - nvalid) * KB * 8;
-                for (int idx = st; idx < n16; idx += 128) {
+                for (int idx = st; idx < n16; idx += NST) {
                     const int r = nvalid + idx / (KB * 8);
                     const int rem = idx % (KB * 8);
                     *reinterpret_cast<uint4*>(vt + (rem >> 3) * Sh::KB_BYTES + r * 128 + (rem & 7) * 16) =
@@ -658,46 +711,52 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR>::THREADS, 1)
             if (lane == 0) tc::mbar_arrive(p_full(pb));
 
             if (t.seg_end) {
-                const float ltot = l + __shfl_xor_sync(0xffffffffu, l, 16);
                 ok = __all_sync(0xffffffffu, tc::mbar_wait(o_fin(pb), (i >> 1) & 1, abort_flag, kBudget));
                 if (!ok) break;
                 tc::fence_after_sync();
                 const size_t pair = (size_t)t.b * p.Hkv + t.h;
-                const size_t qrow = (size_t)t.b * p.Hq + (size_t)t.h * G + row;
                 const size_t slot = (size_t)c + pair;
-                // Each thread writes 32 contiguous columns of its row per step.
-                const float inv = t.full ? ((ltot > 0.f) ? 1.f / ltot : 0.f) : 1.f;
-                const size_t grow = t.full ? qrow : slot * G + row;  // output (or partial) row
+#pragma unroll
+                for (int rg = 0; rg < NG; ++rg) {
+                    const float ltot = l[rg] + __shfl_xor_sync(0xffffffffu, l[rg], 16);
+                    const bool active = act_[rg];
+                    const size_t qrow = out_row(t.b, t.h, tok_[rg], hd_[rg]);
+                    // Partial slots hold the pair's T * G rows, token-major.
+                    const size_t prow = slot * (size_t)(TQ * G) + (size_t)tok_[rg] * G + hd_[rg];
+                    // Each thread writes 32 contiguous columns of its row per step.
+                    const float inv = t.full ? ((ltot > 0.f) ? 1.f / ltot : 0.f) : 1.f;
+                    const size_t grow = t.full ? qrow : prow;  // output (or partial) row
 #pragma unroll 1
-                for (int cc = 0; cc < HD / 32; ++cc) {
-                    const int col0 = hl * HD + cc * 32;
-                    uint32_t r[32];
-                    tc::tmem_ld_16x32bx2_x32<HD>(tmem + lane_base + Sh::TMEM_O + cc * 32, r);
-                    tc::tmem_wait_ld();
-                    if (active && t.full && !F32OUT) {
-                        uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + grow * D + col0);
+                    for (int cc = 0; cc < HD / 32; ++cc) {
+                        const int col0 = hl * HD + cc * 32;
+                        uint32_t r[32];
+                        tc::tmem_ld_16x32bx2_x32<HD>(tmem + lanes(rg) + Sh::TMEM_O + cc * 32, r);
+                        tc::tmem_wait_ld();
+                        if (active && t.full && !F32OUT) {
+                            uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + grow * D + col0);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k)
-                            o[k] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * k]) * inv, __uint_as_float(r[8 * k + 1]) * inv),
-                                              pack_bf16x2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv),
-                                              pack_bf16x2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv),
-                                              pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv));
-                    } else if (active) {
-                        float4* o = reinterpret_cast<float4*>((t.full ? reinterpret_cast<float*>(p.out) : p.ws_o) + grow * D + col0);
+                            for (int k = 0; k < 4; ++k)
+                                o[k] = make_uint4(pack_bf16x2(__uint_as_float(r[8 * k]) * inv, __uint_as_float(r[8 * k + 1]) * inv),
+                                                  pack_bf16x2(__uint_as_float(r[8 * k + 2]) * inv, __uint_as_float(r[8 * k + 3]) * inv),
+                                                  pack_bf16x2(__uint_as_float(r[8 * k + 4]) * inv, __uint_as_float(r[8 * k + 5]) * inv),
+                                                  pack_bf16x2(__uint_as_float(r[8 * k + 6]) * inv, __uint_as_float(r[8 * k + 7]) * inv));
+                        } else if (active) {
+                            float4* o = reinterpret_cast<float4*>((t.full ? reinterpret_cast<float*>(p.out) : p.ws_o) + grow * D + col0);
 #pragma unroll
-                        for (int k = 0; k < 8; ++k)
-                            o[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
-                                               __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
+                            for (int k = 0; k < 8; ++k)
+                                o[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
+                                                   __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
+                        }
+                    }
+                    if (active && hl == 0) {
+                        if (t.full) {
+                            if (p.lse) p.lse[qrow] = (ltot > 0.f) ? (m[rg] + log2f(ltot)) * 0.69314718055994531f : -CUDART_INF_F;
+                        } else {
+                            p.ws_ml[prow] = make_float2(m[rg], ltot);
+                        }
                     }
                 }
                 tc::fence_before_sync();
-                if (active && hl == 0) {
-                    if (t.full) {
-                        if (p.lse) p.lse[qrow] = (m + log2f(ltot)) * 0.69314718055994531f;
-                    } else {
-                        p.ws_ml[slot * G + row] = make_float2(m, ltot);
-                    }
-                }
             }
             ++i;
         }

@@ -4,13 +4,12 @@
 namespace kvd {
 
 const ChunkKernel* tc_table_d128(bool f32, int qr) {
-    static const ChunkKernel table[4][2] = {
-        {make_tc<128, false, 8>(14), make_tc<128, true, 8>(15)},
-        {make_tc<128, false, 16>(16), make_tc<128, true, 16>(17)},
-        {make_tc<128, false, 48>(18), make_tc<128, true, 48>(19)},
-        {make_tc<128, false, 64>(20), make_tc<128, true, 64>(21)},
+    static const ChunkKernel table[3][2] = {
+        {make_tc<128, false, 48>(14), make_tc<128, true, 48>(15)},
+        {make_tc<128, false, 64>(16), make_tc<128, true, 64>(17)},
+        {make_tc<128, false, 128, 128>(18), make_tc<128, true, 128, 128>(19)},
     };
-    const int r = qr == 8 ? 0 : (qr == 16 ? 1 : (qr == 48 ? 2 : 3));
+    const int r = qr == 48 ? 0 : (qr == 64 ? 1 : 2);
     return &table[r][f32 ? 1 : 0];
 }
 

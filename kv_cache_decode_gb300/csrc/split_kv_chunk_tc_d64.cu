@@ -4,13 +4,12 @@
 namespace kvd {
 
 const ChunkKernel* tc_table_d64(bool f32, int qr) {
-    static const ChunkKernel table[4][2] = {
-        {make_tc<64, false, 8>(6), make_tc<64, true, 8>(7)},
-        {make_tc<64, false, 16>(8), make_tc<64, true, 16>(9)},
-        {make_tc<64, false, 48>(10), make_tc<64, true, 48>(11)},
-        {make_tc<64, false, 64>(12), make_tc<64, true, 64>(13)},
+    static const ChunkKernel table[3][2] = {
+        {make_tc<64, false, 48>(6), make_tc<64, true, 48>(7)},
+        {make_tc<64, false, 64>(8), make_tc<64, true, 64>(9)},
+        {make_tc<64, false, 128, 128>(10), make_tc<64, true, 128, 128>(11)},
     };
-    const int r = qr == 8 ? 0 : (qr == 16 ? 1 : (qr == 48 ? 2 : 3));
+    const int r = qr == 48 ? 0 : (qr == 64 ? 1 : 2);
     return &table[r][f32 ? 1 : 0];
 }
 

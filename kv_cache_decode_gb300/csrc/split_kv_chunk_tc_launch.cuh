@@ -15,12 +15,13 @@ namespace kvd {
 bool tc_encode_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
                    const cuuint64_t* strides, const cuuint32_t* box);
 
-template <int D, bool F32, int QR>
+template <int D, bool F32, int QR, int MR>
 cudaError_t launch_tc_chunk(const ChunkKernel& k, const DecodeParams& p, cudaStream_t stream) {
     TcMaps maps;
     std::memset(&maps, 0, sizeof maps);
     {
-        const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)p.B * p.Hq};
+        // q rows: B * Hq, times T query tokens when they are stacked in one tile.
+        const cuuint64_t dims[2] = {(cuuint64_t)D, (cuuint64_t)p.B * p.T * p.Hq};
         const cuuint64_t strides[1] = {(cuuint64_t)D * 2};
         const cuuint32_t box[2] = {64, (cuuint32_t)p.G};
         if (!tc_encode_map(&maps.q, p.q, 2, dims, strides, box)) return cudaErrorInvalidValue;
@@ -28,7 +29,7 @@ cudaError_t launch_tc_chunk(const ChunkKernel& k, const DecodeParams& p, cudaStr
     {
         // Cache rows: [B * S_max] for a contiguous cache, [num_pages * page]
         // for a pool of pages, whose boxes are one page (at most one tile) high.
-        constexpr int T = TcShape<D, F32, QR>::T;
+        constexpr int T = TcShape<D, F32, QR, MR>::T;
         const bool paged = p.block_table != nullptr;
         const int cache_batch = p.vT > 1 ? p.B / p.vT : p.B;  // virtual sequences share their cache's rows
         const cuuint64_t rows = paged ? ((cuuint64_t)p.num_pages << p.page_shift) : (cuuint64_t)cache_batch * p.S_max;
@@ -49,15 +50,15 @@ cudaError_t launch_tc_chunk(const ChunkKernel& k, const DecodeParams& p, cudaStr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, split_kv_chunk_tc_kernel<D, F32, QR>, p, maps);
+    return cudaLaunchKernelEx(&cfg, split_kv_chunk_tc_kernel<D, F32, QR, MR>, p, maps);
 }
 
-template <int D, bool F32, int QR>
+template <int D, bool F32, int QR, int MR = 64>
 static ChunkKernel make_tc(int index) {
-    using Sh = TcShape<D, F32, QR>;
+    using Sh = TcShape<D, F32, QR, MR>;
     ChunkKernel k;
-    k.fn = reinterpret_cast<const void*>(split_kv_chunk_tc_kernel<D, F32, QR>);
-    k.launch = launch_tc_chunk<D, F32, QR>;
+    k.fn = reinterpret_cast<const void*>(split_kv_chunk_tc_kernel<D, F32, QR, MR>);
+    k.launch = launch_tc_chunk<D, F32, QR, MR>;
     k.head_dim = D;
     k.threads = Sh::THREADS;
     k.smem_bytes = Sh::SMEM_BYTES;
@@ -67,6 +68,7 @@ static ChunkKernel make_tc(int index) {
     k.seg_cost = Sh::SEG_COST;
     k.f32_out = F32;
     k.tensor_core = true;
+    k.mma_rows = MR;
     k.index = index;
     return k;
 }

@@ -61,6 +61,7 @@ inline ChunkKernel make_mma_chunk_kernel(int index) {
     k.seg_cost = Sh::SEG_COST;
     k.f32_out = F32;
     k.tensor_core = false;
+    k.mma_rows = 0;
     k.index = index;
     return k;
 }

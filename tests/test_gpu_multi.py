@@ -25,6 +25,9 @@ CASES = [
     ("mqa48t2", 4, 48, 1, 256, 500, 2, 500, 67, 2),       # 96 rows: 6 blocks, MQA
     ("g20t3d64", 3, 20, 1, 64, 400, 3, 400, 68, 3),       # 60 rows: 4 blocks, the last of 12
     ("g16t5", 3, 32, 2, 128, 450, 5, 450, 69, 5),         # 80 rows: 5 blocks
+    # the tcgen05 kernel's 128-row tile with the tokens stacked: two KV heads
+    # (each token's query rows a separate box), and a group of 20 padded to 24
+    ("g24t4kv2", 5, 48, 2, 128, 500, 4, 500, 70, 4),      # 4 x 24 = 96 rows in one tile
 ]
 
 
@@ -121,7 +124,8 @@ def test_multi_rows_past_capacity_are_skipped():
     assert np.array_equal(bf16_tensor_bits(kc), ek) and np.array_equal(bf16_tensor_bits(vc), ev)
 
 
-@pytest.mark.parametrize("Hq,Hkv,D", [(8, 2, 128), (48, 1, 256)], ids=["one_block", "twelve_blocks"])
+@pytest.mark.parametrize("Hq,Hkv,D", [(8, 2, 128), (48, 1, 256), (32, 1, 128)],
+                         ids=["one_block", "twelve_blocks", "one_tile_of_128"])
 def test_multi_short_sequences_give_empty_rows(Hq, Hkv, D):
     """A sequence shorter than T: its first query tokens see no token (zero rows,
     lse -inf), the rest see what exists; rows appended before position 0 are
