@@ -3,9 +3,15 @@
 Each mutant is the oracle's C source with one textual change (a dropped term, a
 wrong sign, a wrong index, a transposed operand, an off-by-one), compiled to a
 temporary library on the CPU. The pins of oracle_pins must fail on every one.
+The pins run on each mutant in a child process: a mutant may index outside its
+buffers (an unchecked page number, say), and its writes must not reach the
+test process's own memory. A child killed by such an access has shown the
+mistake as well.
 """
+import json
 import os
 import subprocess
+import sys
 import tempfile
 
 import pytest
@@ -70,11 +76,22 @@ def test_pins_catch_mutant(name, old, new, workdir):
     with open(src, "w") as f:
         f.write(SRC.replace(old, new))
     lib_path = oracle.build(force=True, src=src, out=os.path.join(workdir, f"{name}.so"))
-    lib = oracle._load(lib_path)
-    failed = []
-    for check in oracle_pins.ALL_CHECKS:
-        try:
-            check(lib)
-        except (AssertionError, ValueError, FloatingPointError):
-            failed.append(check.__name__)
+    here = os.path.dirname(os.path.abspath(__file__))
+    code = (
+        "import json, sys\n"
+        f"sys.path[:0] = [{here!r}, {os.path.dirname(here)!r}]\n"
+        "import oracle, oracle_pins\n"
+        f"lib = oracle._load({lib_path!r})\n"
+        "failed = []\n"
+        "for check in oracle_pins.ALL_CHECKS:\n"
+        "    try:\n"
+        "        check(lib)\n"
+        "    except (AssertionError, ValueError, FloatingPointError):\n"
+        "        failed.append(check.__name__)\n"
+        "print(json.dumps(failed))\n")
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, timeout=600)
+    if r.returncode < 0:
+        return  # killed by a signal: the mutant's stray access showed up
+    assert r.returncode == 0, r.stderr[-2000:]
+    failed = json.loads(r.stdout.strip().splitlines()[-1])
     assert failed, f"no pin caught the planted mistake {name}"
