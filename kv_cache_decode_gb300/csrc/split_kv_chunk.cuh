@@ -121,35 +121,77 @@ struct ChunkShape {
     static constexpr int ND = D / 8;    // output n-tiles (8 columns each)
     static constexpr int CH = D / 8;    // 16-byte chunks per K/V row
     static constexpr int TILE_ELEMS = TT * D;
-    // A stage holds a tile's K and V rows: bf16, or (KV8) int8 codes followed
-    // by the tile's float32 K and V row scales. The int8 tiles are converted to
-    // f16 in CONV_BYTES, laid out like a bf16 stage, which the MMAs read.
+    // A stage holds a tile's K and V rows: bf16, or (KV8) 8-bit codes followed
+    // by the tile's float32 K and V row scales.
     static constexpr int STAGE_BYTES = KV8 ? 2 * TILE_ELEMS + 2 * TT * 4 : 2 * TILE_ELEMS * 2;
-    static constexpr int CONV_BYTES = KV8 ? 2 * TILE_ELEMS * 2 : 0;
     static constexpr int MB_FLOATS_PER_WARP = (ND * 4 + 4) * 32;
     // The token slices are merged at the end of a segment through the stage of
-    // the segment's last tile (KV8: the conversion buffer), which every warp
-    // has finished reading by then.
+    // the segment's last tile, which every warp has finished reading by then
+    // (KV8: through a buffer of their own, an 8-bit stage being too small).
     static constexpr int MB_BYTES = (TS - 1) * HT * MB_FLOATS_PER_WARP * 4;
-    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + CONV_BYTES;
+    static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + (KV8 ? MB_BYTES : 0);
     // Schedule: runs balanced in tokens (the kernel is bandwidth-bound, so a
     // short tile costs less than a full one), no charge per pair (a new pair's
     // queries come from L2 while the previous tiles are still in flight).
     static constexpr int SEG_UNIT = 1;
     static constexpr int SEG_COST = 0;
-    static_assert(MB_BYTES <= (KV8 ? CONV_BYTES : STAGE_BYTES), "warp-merge data must fit in one stage");
+    static_assert(KV8 || MB_BYTES <= STAGE_BYTES, "warp-merge data must fit in one stage");
+    static_assert(!KV8 || TW == 16, "8-bit tiles: one 16-token k-step per warp");
     static_assert(STAGE_BYTES % 128 == 0, "stage alignment");
     static_assert(TW % 16 == 0, "each warp needs whole 16-token k-steps");
     static_assert(D % 16 == 0 && D >= 64, "head_dim");
 };
 
 // KV8: the cache holds 8-bit codes (int8, or fp8 E4M3 with FP8) with a
-// float32 scale per (token, KV head) row; K and V tiles are converted to f16
-// in shared memory (exactly: int8 codes are small integers, and E4M3 codes
-// become their values / 256, which f16 holds exactly), q is taken to f16, the
-// MMAs run in f16, each score is multiplied by its key row's scale and each
-// weight by its value row's scale before P V (FP8: the scores by 256 more,
-// and the output by 256 before it is written).
+// float32 scale per (token, KV head) row. The codes are staged as they are
+// and converted to f16 in registers, straight into the MMAs' B fragments
+// (exactly: int8 codes are small integers, and E4M3 codes become their values
+// / 256, which f16 holds exactly); q is taken to f16, the MMAs run in f16,
+// each score is multiplied by its key row's scale and each weight by its
+// value row's scale before P V (FP8: the scores by 256 more, and the output by
+// 256 before it is written).
+//
+// Fragments from 8-bit rows: ldmatrix moves 16-byte rows of 8 threads' bytes
+// as 8x8 matrices of 16-bit elements, so a thread receives 4 consecutive codes
+// of one row (non-transposed) or 2 codes of each of 2 consecutive rows
+// (transposed). The MMA's k index is then mapped to head-dim columns in a
+// permuted order that matches those bytes, which a dot product allows as long
+// as both operands use it:
+// * S = q K^T: within each 16-column chunk, k = 2j, 2j + 1, 2j + 8, 2j + 9 of
+//   thread j = lane % 4 are columns 4j .. 4j + 3 (q's A fragment is loaded in
+//   the same order);
+// * O += P V: the 8 columns of an n-tile are every other head-dim column of a
+//   16-column chunk (even tile 2c: columns 16c + 2n, odd tile 2c + 1:
+//   16c + 2n + 1), so thread j holds columns 16c + 4j .. 16c + 4j + 3 of its
+//   rows across the two tiles, which the output writes put back in order.
+// 8-bit rows are staged with 16-byte chunk c of row r at chunk position
+// swz8<D>(r, c), so that the 8 rows of an ldmatrix matrix hit 8 distinct
+// 16-byte bank groups.
+template <int D>
+__device__ __forceinline__ int swz8(int r, int c) {
+    return D >= 128 ? (c ^ (r & 7)) : (c ^ ((r >> 1) & 3));
+}
+// Two 8-bit codes of w (bytes selected by SEL_I8 / SEL_F8 as prmt selectors)
+// as one f16x2: int8 codes biased to 0..255 (u = w ^ 0x80808080 given as w),
+// placed in the low mantissa bits of 1024.0h and 1152 subtracted; E4M3 codes
+// sign-extended to 16 bits, shifted so the exponent and mantissa bits sit at
+// the top of an f16's exponent and mantissa (the bias difference of 8 makes
+// the f16 equal to the code's value / 256; subnormals map the same way), and
+// the sign's copy at bit 14 cleared.
+template <bool FP8, uint32_t SEL_I8, uint32_t SEL_F8>
+__device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t w) {
+    uint32_t a;
+    if constexpr (FP8) {
+        asm("prmt.b32 %0, %1, 0, %2;" : "=r"(a) : "r"(w), "n"(SEL_F8));
+        return (a << 7) & 0xbf80bf80u;
+    } else {
+        asm("prmt.b32 %0, %1, %2, %3;" : "=r"(a) : "r"(w), "r"(0x64646464u), "n"(SEL_I8));
+        const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));  // 1152
+        __half2 h = __hsub2(*reinterpret_cast<__half2*>(&a), bias);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
 template <int D, int HT, int TS, int TT, int STAGES, bool F32OUT, int MINB, bool PAGED, bool KV8 = false,
           bool FP8 = false>
 __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const DecodeParams p) {
@@ -282,7 +324,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
         const uint32_t sbase = smem_u32(stages) + stage * Sh::STAGE_BYTES;
         const int ch = tid % CH, r0 = tid / CH;
         if constexpr (KV8 && PAGED) {
-            // int8 rows from their pages (as the bf16 paged rows below), then
+            // 8-bit rows from their pages (as the bf16 paged rows below), then
             // the row scales: a page's scales start at its first row's element
             // offset / D. An entry that names no page reads zero codes and a
             // zero scale.
@@ -300,7 +342,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                 const long long po = (r < nvalid) ? s_pages[ps][(tok >> shift) - first] : -1;
                 const bool ok = po >= 0;
                 const size_t off = ok ? (size_t)po + (size_t)(tok & in_page) * row_stride : 0;
-                const uint32_t dst = sbase + (uint32_t)(r * D + c8 * 16);
+                const uint32_t dst = sbase + (uint32_t)(r * D + swz8<D>(r, c8) * 16);
                 cp_async_16(dst, kb + off, ok ? 16 : 0, policy);
                 cp_async_16(dst + TILE_ELEMS, vb + off, ok ? 16 : 0, policy);
             }
@@ -313,8 +355,9 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                 cp_async_4(sbase + 2 * TILE_ELEMS + tid * 4, base + so, ok ? 4 : 0);
             }
         } else if constexpr (KV8) {
-            // int8 rows: D / 16 chunks of 16 bytes each, unswizzled; then the
-            // tile's row scales, one 4-byte copy per row and tensor.
+            // 8-bit rows: D / 16 chunks of 16 bytes each (chunk c of row r at
+            // swz8(r, c)); then the tile's row scales, one 4-byte copy per row
+            // and tensor.
             constexpr int CH8 = D / 16, RSTEP8 = NT / CH8, RPT8 = TT / RSTEP8;
             static_assert(NT % CH8 == 0 && TT % RSTEP8 == 0 && NT >= 2 * TT, "int8 row split");
             const size_t row0 = ((size_t)t.b * p.S_max + t.tok_lo) * p.Hkv + t.h;
@@ -326,7 +369,7 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                 const int r = q0 + k * RSTEP8;
                 const bool ok = r < nvalid;
                 const size_t off = ok ? (size_t)r * row_stride : 0;
-                const uint32_t dst = sbase + (uint32_t)(r * D + c8 * 16);
+                const uint32_t dst = sbase + (uint32_t)(r * D + swz8<D>(r, c8) * 16);
                 cp_async_16(dst, kb + off, ok ? 16 : 0, policy);
                 cp_async_16(dst + TILE_ELEMS, vb + off, ok ? 16 : 0, policy);
             }
@@ -461,14 +504,21 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
             const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qb + (v1 ? out_row(ct.b, ct.h, r1) : 0) * D);
 #pragma unroll
             for (int kk = 0; kk < KS; ++kk) {
-                const int w = kk * 8 + (lane & 3);  // 32-bit word index of column kk*16 + 2*(lane&3)
-                qf[kk][0] = v0 ? __ldg(q0 + w) : 0u;
-                qf[kk][1] = v1 ? __ldg(q1 + w) : 0u;
-                qf[kk][2] = v0 ? __ldg(q0 + w + 4) : 0u;
-                qf[kk][3] = v1 ? __ldg(q1 + w + 4) : 0u;
                 if constexpr (KV8) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) qf[kk][e] = bf16x2_to_f16x2(qf[kk][e]);
+                    // k = 2j, 2j + 1 | 2j + 8, 2j + 9 are columns 4j .. 4j + 3 of the chunk
+                    const int w = kk * 8 + 2 * (lane & 3);
+                    const uint2 a = v0 ? __ldg(reinterpret_cast<const uint2*>(q0 + w)) : make_uint2(0u, 0u);
+                    const uint2 b = v1 ? __ldg(reinterpret_cast<const uint2*>(q1 + w)) : make_uint2(0u, 0u);
+                    qf[kk][0] = bf16x2_to_f16x2(a.x);
+                    qf[kk][1] = bf16x2_to_f16x2(b.x);
+                    qf[kk][2] = bf16x2_to_f16x2(a.y);
+                    qf[kk][3] = bf16x2_to_f16x2(b.y);
+                } else {
+                    const int w = kk * 8 + (lane & 3);  // 32-bit word index of column kk*16 + 2*(lane&3)
+                    qf[kk][0] = v0 ? __ldg(q0 + w) : 0u;
+                    qf[kk][1] = v1 ? __ldg(q1 + w) : 0u;
+                    qf[kk][2] = v0 ? __ldg(q0 + w + 4) : 0u;
+                    qf[kk][3] = v1 ? __ldg(q1 + w + 4) : 0u;
                 }
             }
             m0 = m1 = umax ? phi2 : -CUDART_INF_F;
@@ -483,59 +533,14 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
         // Causal limits of this thread's rows, relative to the tile (T = 1: the tile's end or beyond).
         const int lim0 = ct.L - cq0 - ct.tok_lo, lim1 = ct.L - cq1 - ct.tok_lo;
         if (wbase < nvalid) {
-            uint32_t kbase = smem_u32(stages) + stage * Sh::STAGE_BYTES;
+            const uint32_t kbase = smem_u32(stages) + stage * Sh::STAGE_BYTES;
+            const uint32_t vbase = kbase + (KV8 ? TILE_ELEMS : TILE_ELEMS * 2);
             const float* kscale = nullptr;
             const float* vscale = nullptr;
-            // KV8: this warp's TW rows of K (here) and V (after the score
-            // MMAs are issued, so that the conversion overlaps them), int8 ->
-            // f16, into the conversion buffer in the bf16 stage layout (16-byte
-            // chunk c of row r at chunk c ^ (r & 7)). Only this warp reads
-            // them. A lane's chunks are all loaded before any is converted.
-            const uint8_t* st8 = smem + stage * Sh::STAGE_BYTES;
-            uint8_t* conv8 = smem + STAGES * Sh::STAGE_BYTES;
-            auto convert_rows = [&](int kv) {
-                // chunks per lane, per batch (head_dim 256 leaves no registers to batch)
-                constexpr int CH8 = D / 16, NC = TW * CH8 / 32, NB = D >= 256 ? 1 : (NC > 4 ? 4 : NC);
-                static_assert(TW * CH8 % 32 == 0 && NC % NB == 0, "whole chunks per lane");
-#pragma unroll
-                for (int j0 = 0; j0 < NC; j0 += NB) {
-                    uint4 w[NB];
-#pragma unroll
-                    for (int j = 0; j < NB; ++j) {
-                        const int i = lane + 32 * (j0 + j), rr = i / CH8, c8 = i % CH8;
-                        w[j] = *reinterpret_cast<const uint4*>(st8 + kv * TILE_ELEMS + (wbase + rr) * D + c8 * 16);
-                    }
-#pragma unroll
-                    for (int j = 0; j < NB; ++j) {
-                        const int i = lane + 32 * (j0 + j), rr = i / CH8, c8 = i % CH8, r = wbase + rr;
-                        uint4 a, b;
-                        if constexpr (FP8) {
-                            e4m3x4_to_f16x2x2_div256(w[j].x, a.x, a.y);
-                            e4m3x4_to_f16x2x2_div256(w[j].y, a.z, a.w);
-                            e4m3x4_to_f16x2x2_div256(w[j].z, b.x, b.y);
-                            e4m3x4_to_f16x2x2_div256(w[j].w, b.z, b.w);
-                        } else {
-                            i8x4_to_f16x2x2(w[j].x, a.x, a.y);
-                            i8x4_to_f16x2x2(w[j].y, a.z, a.w);
-                            i8x4_to_f16x2x2(w[j].z, b.x, b.y);
-                            i8x4_to_f16x2x2(w[j].w, b.z, b.w);
-                        }
-                        uint8_t* row = conv8 + kv * TILE_ELEMS * 2 + r * D * 2;
-                        *reinterpret_cast<uint4*>(row + (((2 * c8) ^ (r & 7)) * 16)) = a;
-                        *reinterpret_cast<uint4*>(row + (((2 * c8 + 1) ^ (r & 7)) * 16)) = b;
-                    }
-                }
-            };
-            constexpr bool kLateV = D <= 128;  // convert V after issuing the score MMAs
             if constexpr (KV8) {
-                convert_rows(0);
-                if constexpr (!kLateV) convert_rows(1);
-                __syncwarp();
-                kbase = smem_u32(conv8);
-                kscale = reinterpret_cast<const float*>(st8 + 2 * TILE_ELEMS);
+                kscale = reinterpret_cast<const float*>(smem + stage * Sh::STAGE_BYTES + 2 * TILE_ELEMS);
                 vscale = kscale + TT;
             }
-            const uint32_t vbase = kbase + TILE_ELEMS * 2;
 
             // S = q K^T over this warp's TW tokens, as two independent accumulation
             // chains (even and odd k-steps) to halve the MMA dependency chain.
@@ -543,24 +548,45 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
 #pragma unroll
             for (int j = 0; j < NS; ++j)
                 s[j][0] = s[j][1] = s[j][2] = s[j][3] = s2[j][0] = s2[j][1] = s2[j][2] = s2[j][3] = 0.f;
+            if constexpr (KV8) {
+                // Matrix mi of an ldmatrix: tokens 8 (mi & 1) .. + 7 of the
+                // warp's 16, head-dim chunk 2 kc + (mi >> 1).
 #pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
+                for (int kc = 0; kc < KS / 2; ++kc) {
+                    const int row = wbase + ((lane >> 3) & 1) * 8 + (lane & 7);
+                    const int ch = 2 * kc + (lane >> 4);
+                    uint32_t r[4];
+                    ldmatrix_x4(kbase + (uint32_t)(row * D + swz8<D>(row, ch) * 16), r[0], r[1], r[2], r[3]);
 #pragma unroll
-                for (int n2 = 0; n2 < NS / 2; ++n2) {
-                    const int row = wbase + n2 * 16 + ((lane >> 4) & 1) * 8 + (lane & 7);
-                    const int ch = kk * 2 + ((lane >> 3) & 1);
-                    uint32_t b0, b1, b2, b3;
-                    ldmatrix_x4(kbase + (uint32_t)((row * D + ((ch ^ (row & 7)) * 8)) * 2), b0, b1, b2, b3);
-                    if (kk & 1) {
-                        mma_16816<KV8>(s2[2 * n2], qf[kk], b0, b1);
-                        mma_16816<KV8>(s2[2 * n2 + 1], qf[kk], b2, b3);
-                    } else {
-                        mma_16816<KV8>(s[2 * n2], qf[kk], b0, b1);
-                        mma_16816<KV8>(s[2 * n2 + 1], qf[kk], b2, b3);
+                    for (int mi = 0; mi < 4; ++mi) {
+                        const uint32_t w = FP8 ? r[mi] : (r[mi] ^ 0x80808080u);
+                        const uint32_t b0 = codes_to_f16x2<FP8, 0x4140, 0x9180>(w);
+                        const uint32_t b1 = codes_to_f16x2<FP8, 0x4342, 0xb3a2>(w);
+                        if (mi >> 1)
+                            mma_16816<true>(s2[mi & 1], qf[2 * kc + 1], b0, b1);
+                        else
+                            mma_16816<true>(s[mi & 1], qf[2 * kc], b0, b1);
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+                    for (int n2 = 0; n2 < NS / 2; ++n2) {
+                        const int row = wbase + n2 * 16 + ((lane >> 4) & 1) * 8 + (lane & 7);
+                        const int ch = kk * 2 + ((lane >> 3) & 1);
+                        uint32_t b0, b1, b2, b3;
+                        ldmatrix_x4(kbase + (uint32_t)((row * D + ((ch ^ (row & 7)) * 8)) * 2), b0, b1, b2, b3);
+                        if (kk & 1) {
+                            mma_16816<false>(s2[2 * n2], qf[kk], b0, b1);
+                            mma_16816<false>(s2[2 * n2 + 1], qf[kk], b2, b3);
+                        } else {
+                            mma_16816<false>(s[2 * n2], qf[kk], b0, b1);
+                            mma_16816<false>(s[2 * n2 + 1], qf[kk], b2, b3);
+                        }
                     }
                 }
             }
-            if constexpr (KV8 && kLateV) convert_rows(1);  // V, while the score MMAs complete
 #pragma unroll
             for (int j = 0; j < NS; ++j)
 #pragma unroll
@@ -665,21 +691,49 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                 }
             }
 
-            if constexpr (KV8 && kLateV) __syncwarp();  // the V rows converted above
             // O += P V.
+            if constexpr (KV8) {
+                // Matrix mi of a transposed ldmatrix: tokens 8 (mi & 1) .. + 7,
+                // head-dim chunk 2 qq + (mi >> 1); a thread holds columns 2g,
+                // 2g + 1 of the chunk for tokens 2j, 2j + 1 (or + 8).
 #pragma unroll
-            for (int k2 = 0; k2 < NS / 2; ++k2) {
+                for (int qq = 0; qq < KS / 2; ++qq) {
+                    const int row = wbase + ((lane >> 3) & 1) * 8 + (lane & 7);
+                    const int ch = 2 * qq + (lane >> 4);
+                    uint32_t r[4];
+                    ldmatrix_x4_trans(vbase + (uint32_t)(row * D + swz8<D>(row, ch) * 16), r[0], r[1], r[2], r[3]);
 #pragma unroll
-                for (int n2 = 0; n2 < ND / 2; ++n2) {
-                    const int row = wbase + k2 * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
-                    const int ch = n2 * 2 + ((lane >> 4) & 1);
-                    uint32_t v0, v1, v2, v3;
-                    ldmatrix_x4_trans(vbase + (uint32_t)((row * D + ((ch ^ (row & 7)) * 8)) * 2), v0, v1, v2, v3);
-                    mma_16816<KV8>(o[2 * n2], pa[k2], v0, v1);
-                    mma_16816<KV8>(o[2 * n2 + 1], pa[k2], v2, v3);
-                    if constexpr (F32OUT) {
-                        mma_16816<KV8>(o[2 * n2], pl[k2], v0, v1);
-                        mma_16816<KV8>(o[2 * n2 + 1], pl[k2], v2, v3);
+                    for (int c = 0; c < 2; ++c) {
+                        const uint32_t lo = FP8 ? r[2 * c] : (r[2 * c] ^ 0x80808080u);
+                        const uint32_t hi = FP8 ? r[2 * c + 1] : (r[2 * c + 1] ^ 0x80808080u);
+                        const int q = 2 * qq + c;
+                        const uint32_t e0 = codes_to_f16x2<FP8, 0x4240, 0xa280>(lo);
+                        const uint32_t e1 = codes_to_f16x2<FP8, 0x4240, 0xa280>(hi);
+                        const uint32_t d0 = codes_to_f16x2<FP8, 0x4341, 0xb391>(lo);
+                        const uint32_t d1 = codes_to_f16x2<FP8, 0x4341, 0xb391>(hi);
+                        mma_16816<true>(o[2 * q], pa[0], e0, e1);
+                        mma_16816<true>(o[2 * q + 1], pa[0], d0, d1);
+                        if constexpr (F32OUT) {
+                            mma_16816<true>(o[2 * q], pl[0], e0, e1);
+                            mma_16816<true>(o[2 * q + 1], pl[0], d0, d1);
+                        }
+                    }
+                }
+            } else {
+#pragma unroll
+                for (int k2 = 0; k2 < NS / 2; ++k2) {
+#pragma unroll
+                    for (int n2 = 0; n2 < ND / 2; ++n2) {
+                        const int row = wbase + k2 * 16 + ((lane >> 3) & 1) * 8 + (lane & 7);
+                        const int ch = n2 * 2 + ((lane >> 4) & 1);
+                        uint32_t v0, v1, v2, v3;
+                        ldmatrix_x4_trans(vbase + (uint32_t)((row * D + ((ch ^ (row & 7)) * 8)) * 2), v0, v1, v2, v3);
+                        mma_16816<false>(o[2 * n2], pa[k2], v0, v1);
+                        mma_16816<false>(o[2 * n2 + 1], pa[k2], v2, v3);
+                        if constexpr (F32OUT) {
+                            mma_16816<false>(o[2 * n2], pl[k2], v0, v1);
+                            mma_16816<false>(o[2 * n2 + 1], pl[k2], v2, v3);
+                        }
                     }
                 }
             }
@@ -741,6 +795,19 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
             }
 
             if (ts == 0) {
+                // Output column pair n of this thread: columns col_of(n), + 1
+                // of rows r0 (acc(n, 0), acc(n, 1)) and r1 (acc(n, 2), acc(n, 3)).
+                // KV8: pairs 2c and 2c + 1 are columns 16c + 4j .. + 3, from
+                // the even and odd n-tiles of chunk c alternately.
+                auto col_of = [&](int n) {
+                    return KV8 ? (n >> 1) * 16 + (lane & 3) * 4 + (n & 1) * 2 : n * 8 + (lane & 3) * 2;
+                };
+                auto acc = [&](int n, int e) -> float {
+                    if constexpr (KV8)
+                        return o[(n & ~1) + (e & 1)][(e & 2) + (n & 1)];
+                    else
+                        return o[n][e];
+                };
                 const size_t pair = (size_t)ct.b * p.Hkv + ct.h;
                 const bool v0 = r0 < TG, v1 = r1 < TG;
                 const size_t or0 = v0 ? out_row(ct.b, ct.h, r0) : 0, or1 = v1 ? out_row(ct.b, ct.h, r1) : 0;
@@ -749,15 +816,15 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                     const float i0 = l0 > 0.f ? OSC / l0 : 0.f, i1 = l1 > 0.f ? OSC / l1 : 0.f;
 #pragma unroll
                     for (int n = 0; n < ND; ++n) {
-                        const int d = n * 8 + (lane & 3) * 2;
+                        const int d = col_of(n);
                         if constexpr (F32OUT) {
                             float* out = reinterpret_cast<float*>(p.out);
-                            if (v0) *reinterpret_cast<float2*>(out + or0 * D + d) = make_float2(o[n][0] * i0, o[n][1] * i0);
-                            if (v1) *reinterpret_cast<float2*>(out + or1 * D + d) = make_float2(o[n][2] * i1, o[n][3] * i1);
+                            if (v0) *reinterpret_cast<float2*>(out + or0 * D + d) = make_float2(acc(n, 0) * i0, acc(n, 1) * i0);
+                            if (v1) *reinterpret_cast<float2*>(out + or1 * D + d) = make_float2(acc(n, 2) * i1, acc(n, 3) * i1);
                         } else {
                             __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
-                            if (v0) *reinterpret_cast<uint32_t*>(out + or0 * D + d) = pack_bf16x2(o[n][0] * i0, o[n][1] * i0);
-                            if (v1) *reinterpret_cast<uint32_t*>(out + or1 * D + d) = pack_bf16x2(o[n][2] * i1, o[n][3] * i1);
+                            if (v0) *reinterpret_cast<uint32_t*>(out + or0 * D + d) = pack_bf16x2(acc(n, 0) * i0, acc(n, 1) * i0);
+                            if (v1) *reinterpret_cast<uint32_t*>(out + or1 * D + d) = pack_bf16x2(acc(n, 2) * i1, acc(n, 3) * i1);
                         }
                     }
                     if (p.lse && (lane & 3) == 0) {
@@ -769,9 +836,9 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                     float* wo = p.ws_o + slot * TG * D;
 #pragma unroll
                     for (int n = 0; n < ND; ++n) {
-                        const int d = n * 8 + (lane & 3) * 2;
-                        if (v0) *reinterpret_cast<float2*>(wo + (size_t)r0 * D + d) = make_float2(o[n][0] * OSC, o[n][1] * OSC);
-                        if (v1) *reinterpret_cast<float2*>(wo + (size_t)r1 * D + d) = make_float2(o[n][2] * OSC, o[n][3] * OSC);
+                        const int d = col_of(n);
+                        if (v0) *reinterpret_cast<float2*>(wo + (size_t)r0 * D + d) = make_float2(acc(n, 0) * OSC, acc(n, 1) * OSC);
+                        if (v1) *reinterpret_cast<float2*>(wo + (size_t)r1 * D + d) = make_float2(acc(n, 2) * OSC, acc(n, 3) * OSC);
                     }
                     if ((lane & 3) == 0) {
                         if (v0) p.ws_ml[slot * TG + r0] = make_float2(m0, l0);

@@ -20,9 +20,9 @@ struct ChunkConfig {
     // of it is reserved per CTA); __launch_bounds__ then caps registers to match.
     static constexpr int SMEM = ChunkShape<D, HT, TS, TT, STAGES>::SMEM_BYTES;
     static constexpr int MINB = (2 * (SMEM + 1024) <= 228 * 1024) ? 2 : 1;
-    // int8 cache: stages of int8 tiles (half the bytes, so more of them) and
-    // one f16 conversion buffer, with the same CTAs per SM.
-    static constexpr int STAGES8 = (D == 64) ? 8 : 4;
+    // 8-bit cache: stages of 8-bit tiles (half the bytes, so more of them) and
+    // the token slices' merge buffer, with the same CTAs per SM.
+    static constexpr int STAGES8 = (D == 64) ? 8 : 5;
     static constexpr int SMEM8 = ChunkShape<D, HT, TS, TT, STAGES8, true>::SMEM_BYTES;
     static constexpr int MINB8 = (2 * (SMEM8 + 1024) <= 228 * 1024) ? 2 : 1;
 };
