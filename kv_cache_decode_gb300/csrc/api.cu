@@ -24,12 +24,16 @@ const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool
 }
 
 // The tcgen05 kernels take either cache form at run time (only their loads
-// differ); the mma.sync kernel has a compiled variant per form. int8 caches
-// (contiguous or paged) run on the mma.sync kernel, whose CTAs take 16 of a
+// differ); the mma.sync kernel has a compiled variant per form. 8-bit caches
+// run on the tcgen05 kernel's converting variant when the group is wide (see
+// tc8_chunk_kernel), else on the mma.sync kernel, whose CTAs take 16 of a
 // pair's rows each, for every group.
 const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8, bool fp8, int T) {
     if (group < 1 || group > KVD_MAX_GROUP) return nullptr;
-    if (kv8) return mma_chunk_kernel(head_dim, f32_out, paged, true, fp8);
+    if (kv8) {
+        const ChunkKernel* k = tc8_chunk_kernel(head_dim, f32_out, group, fp8);
+        return k ? k : mma_chunk_kernel(head_dim, f32_out, paged, true, fp8);
+    }
     if (group <= 16) return mma_chunk_kernel(head_dim, f32_out, paged, false, false);
     return tc_chunk_kernel(head_dim, f32_out, group, T);
 }
@@ -38,9 +42,9 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_num_sms[kMaxDevices];
-// Bit i of g_smem_ready[dev] is set once kernel variant i may use its
-// dynamic shared memory size on device dev.
-std::atomic<uint64_t> g_smem_ready[kMaxDevices];
+// Bit i % 64 of g_smem_ready[dev][i / 64] is set once kernel variant i may
+// use its dynamic shared memory size on device dev.
+std::atomic<uint64_t> g_smem_ready[kMaxDevices][2];
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -310,12 +314,13 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     if (phase & kChunk) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KVD_ERR_CUDA;
-        const uint64_t bit = 1ull << k->index;
-        if (!(g_smem_ready[dev].load(std::memory_order_acquire) & bit)) {
+        const uint64_t bit = 1ull << (k->index & 63);
+        std::atomic<uint64_t>& ready = g_smem_ready[dev][(k->index >> 6) & 1];
+        if (!(ready.load(std::memory_order_acquire) & bit)) {
             if (cudaFuncSetAttribute(k->fn, cudaFuncAttributeMaxDynamicSharedMemorySize, k->smem_bytes) !=
                 cudaSuccess)
                 return KVD_ERR_CUDA;
-            g_smem_ready[dev].fetch_or(bit, std::memory_order_acq_rel);
+            ready.fetch_or(bit, std::memory_order_acq_rel);
         }
         if (k->launch(*k, p, s) != cudaSuccess) return KVD_ERR_CUDA;
     }

@@ -73,18 +73,21 @@ struct ChunkKernel {
     int seg_cost;    // positions charged per pair by the schedule
     bool f32_out, tensor_core;
     int mma_rows;  // tcgen05 kernel: rows of its MMAs (128: several query tokens of a sequence in one tile)
-    int index;  // position in the variant table (0..59), for the per-device attribute bitmask
+    int index;  // position in the variant table (0..127), for the per-device attribute bitmask
 };
 
 // The kernel for a shape: bf16 groups of up to 16 query heads per KV head run
 // on the mma.sync kernel (T query tokens as T * G rows, in blocks of 16),
 // wider groups (17..64) on the tcgen05 kernel (T query tokens stacked in one
 // 128-row tile when T times the group rounded up to 8 fits, else as T virtual
-// sequences); int8 caches run on the mma.sync kernel for every group.
+// sequences). 8-bit caches run on the tcgen05 kernel's converting variant
+// for groups of 17..64 at head_dim 128 or 17..48 at 256 (T query tokens as
+// virtual sequences), else on the mma.sync kernel.
 const ChunkKernel* find_chunk_kernel(int head_dim, int group, bool f32_out, bool paged, bool kv8 = false,
                                      bool fp8 = false, int T = 1);
 const ChunkKernel* mma_chunk_kernel(int head_dim, bool f32_out, bool paged, bool kv8, bool fp8);
 const ChunkKernel* tc_chunk_kernel(int head_dim, bool f32_out, int group, int T = 1);
+const ChunkKernel* tc8_chunk_kernel(int head_dim, bool f32_out, int group, bool fp8);
 
 cudaError_t launch_merge(const DecodeParams& p, int head_dim, bool f32_out, int num_sms, cudaStream_t stream);
 // Results of disjoint token shards combined by their normalisers (split_kv_merge.cu).

@@ -32,6 +32,15 @@
 // partial sums) in TMEM, two P buffers in TMEM, Q slots in shared memory, O in
 // TMEM. Every wait is bounded; a timeout flags KVD_STATUS_TIMEOUT and all
 // roles wind down.
+//
+// 8-bit caches (KV8: int8 codes, or E4M3 codes with FP8, each row with a
+// float32 scale): TMA fills 8-bit rings instead, and 8 more warps (4 per
+// tensor) convert each tile exactly to f16 in the K and V rings (the layout
+// TMA gives bf16 rows) and copy its row scales into a scale slot. The Q
+// loader converts each pair's Q rows to f16 in place, the MMAs take f16
+// operands, the softmax multiplies each score by its key row's scale and
+// each weight by its value row's scale (E4M3 codes become their values / 256
+// in f16: scores and output are scaled back by 256).
 #pragma once
 
 #include <math_constants.h>
@@ -46,8 +55,10 @@
 namespace kvd {
 
 // MR: rows of the MMAs (64, or 128 for several query tokens of a sequence
-// stacked in one tile); QR: Q rows stored per head_dim block.
-template <int D, bool F32OUT, int QR, int MR = 64>
+// stacked in one tile); QR: Q rows stored per head_dim block. KV8: an 8-bit
+// cache (int8 codes, or E4M3 codes with FP8) with a float32 scale per (token,
+// KV head) row, converted to f16 tiles in shared memory by converter warps.
+template <int D, bool F32OUT, int QR, int MR = 64, bool KV8 = false>
 struct TcShape {
     static constexpr int T = 64;                 // tokens per tile
     static constexpr int NG = MR / 64;           // 16-row groups per softmax thread
@@ -57,7 +68,7 @@ struct TcShape {
     static constexpr int SEG_UNIT = T;
     static constexpr int SEG_COST = 1;
     static constexpr int KB = D / 64;            // 128-byte swizzle atoms across head_dim
-    static constexpr int TILE_BYTES = T * D * 2; // one K (or V) tile
+    static constexpr int TILE_BYTES = T * D * 2; // one K (or V) tile (bf16, or f16 converted from 8-bit codes)
     static constexpr int KB_BYTES = T * 128;     // one 64-column block of a tile
     // Q is stored as KB blocks of QR rows (the group rounded up to 8, capped at
     // 64). The M = 64 MMA reads 64 rows from each block start; for QR < 64 the
@@ -70,19 +81,38 @@ struct TcShape {
     static constexpr int QS_BYTES = KB * QB_BYTES;  // one slot
     static constexpr int Q_BYTES = NQ * QS_BYTES;
     static constexpr int NP = F32OUT ? 2 : 1;    // hi (and lo) parts of P
+    // 8-bit tiles as TMA writes them: KB8 blocks of 128 head-dim columns.
+    static constexpr int TILE8_BYTES = KV8 ? T * D : 0;
+    static constexpr int KB8 = D / 128;
+    static constexpr int NSC = 4;                // row-scale slots (KV8)
+    static constexpr int SC_BYTES = KV8 ? NSC * 2 * T * 4 : 0;
     // Stage counts: three V stages (a V stage is held until P V of its tile is
     // done, so the V ring needs the depth), K stages as the budget allows.
-    static constexpr int VST = D == 256 ? 3 : (D == 128 ? 6 : 8);
+    // KV8: few f16 stages (a converted tile waits there only for its MMAs):
+    // two for V, whose next tile is converted while the softmax runs; two
+    // for K, or at head_dim 256 one (the next K tile is converted once S of
+    // the current one is done, well within a tile's softmax), which leaves
+    // the room for three 8-bit stages a tensor. The 8-bit rings hold the
+    // loads in flight and are as deep as the rest allows.
+    static constexpr int VST = KV8 ? 2 : (D == 256 ? 3 : (D == 128 ? 6 : 8));
     static constexpr int BUDGET = 224 * 1024 - Q_BYTES - VST * TILE_BYTES;
     static constexpr int KST_FIT = BUDGET / TILE_BYTES;
-    static constexpr int KST = KST_FIT > 8 ? 8 : KST_FIT;
+    static constexpr int KST = KV8 ? (D == 256 ? 1 : 2) : (KST_FIT > 8 ? 8 : KST_FIT);
+    static constexpr int BUDGET8 = 224 * 1024 - Q_BYTES - (KST + VST) * TILE_BYTES - SC_BYTES;
+    static constexpr int ST8_FIT = KV8 ? BUDGET8 / (2 * (TILE8_BYTES > 0 ? TILE8_BYTES : 1)) : 0;
+    static constexpr int K8ST = ST8_FIT > 6 ? 6 : ST8_FIT, V8ST = K8ST;
     static constexpr int OFF_Q = 0;
     static constexpr int OFF_K = OFF_Q + Q_BYTES;
     static constexpr int OFF_V = OFF_K + KST * TILE_BYTES;
-    static constexpr int OFF_BAR = OFF_V + VST * TILE_BYTES;
+    static constexpr int OFF_K8 = OFF_V + VST * TILE_BYTES;
+    static constexpr int OFF_V8 = OFF_K8 + K8ST * TILE8_BYTES;
+    static constexpr int OFF_SC = OFF_V8 + V8ST * TILE8_BYTES;
+    static constexpr int OFF_BAR = OFF_SC + SC_BYTES;
     // barriers: k_full, k_empty [KST]; v_full, v_empty [VST]; q_full, q_empty [NQ];
-    // s_full, s_free; p_full, o_fin [2]; mma_done
-    static constexpr int NBAR = 2 * KST + 2 * VST + 2 * NQ + 2 + 4 + 1;
+    // s_full, s_free; p_full, o_fin [2]; mma_done; KV8: k8_full, k8_empty
+    // [K8ST]; v8_full, v8_empty [V8ST]; q_conv [NQ]; sc_full, sc_empty [NSC]
+    static constexpr int NBAR = 2 * KST + 2 * VST + 2 * NQ + 2 + 4 + 1 +
+                                (KV8 ? 2 * K8ST + 2 * V8ST + NQ + 2 * NSC : 0);
     static constexpr int OFF_MISC = OFF_BAR + NBAR * 8;  // tmem base, abort flag
     static constexpr int SMEM_BYTES = OFF_MISC + 16;
     static constexpr int STATIC_SMEM = 1024;  // block scans (checked by ptxas -v)
@@ -95,11 +125,14 @@ struct TcShape {
     static constexpr int TMEM_O = 256;           // O at columns [256, 256 + D)
     static constexpr int TMEM_COLS = 512;
     // producers 0 (K) and 2 (V), S issuers 1 and 7, O issuer 8, Q loader 9, softmax 3..6
-    // (and at MR = 128, 10..13 for the quarters' second group of 16 rows)
+    // (and at MR = 128, 10..13 for the quarters' second group of 16 rows; KV8:
+    // converters 10 .. 10 + NCW - 1 for K and the next NCW for V)
     static constexpr int NSW = 4 * NG;           // softmax warps
-    static constexpr int NWARPS = 6 + NSW;
+    static constexpr int NCW = KV8 ? 4 : 0;      // converter warps per tensor
+    static constexpr int NWARPS = 6 + NSW + 2 * NCW;
     static constexpr int THREADS = NWARPS * 32;
-    static_assert(KST >= 2, "need at least two K stages");
+    static_assert(KST >= 2 || KV8, "need at least two K stages");
+    static_assert(!KV8 || (K8ST >= 3 && MR == 64 && D >= 128), "8-bit rings");
     static_assert(SMEM_BYTES + STATIC_SMEM <= 227 * 1024, "shared memory budget");
     static_assert(QR % 8 == 0 && QR <= MR && (MR == 64 || MR == 128), "Q rows per block");
     static_assert(TMEM_P + 2 * PCOLS <= TMEM_O && TMEM_O + D <= TMEM_COLS, "TMEM columns");
@@ -111,10 +144,12 @@ struct TcMaps {
     CUtensorMap v;
 };
 
-template <int D, bool F32OUT, int QR, int MR>
-__global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
+template <int D, bool F32OUT, int QR, int MR, bool KV8 = false, bool FP8 = false>
+__global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR, KV8>::THREADS, 1)
     split_kv_chunk_tc_kernel(const DecodeParams p, const __grid_constant__ TcMaps maps) {
-    using Sh = TcShape<D, F32OUT, QR, MR>;
+    using Sh = TcShape<D, F32OUT, QR, MR, KV8>;
+    static_assert(!FP8 || KV8, "fp8 codes are an 8-bit cache");
+    constexpr float OSC = FP8 ? 256.f : 1.f;  // output scale: E4M3 value rows arrive divided by 256
     constexpr int T = Sh::T, KB = Sh::KB, KST = Sh::KST, VST = Sh::VST, NW = Sh::NWARPS,
                   SEG_COST = Sh::SEG_COST;
     constexpr long long kBudget = 4000000000LL;  // ~2 s of clock cycles per wait
@@ -127,7 +162,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
     uint8_t* smem = smem_raw;  // 1024-byte aligned (128-byte swizzle atoms need it)
     const uint32_t sbase = smem_u32(smem);
     const uint32_t sQ = sbase + Sh::OFF_Q, sK = sbase + Sh::OFF_K, sV = sbase + Sh::OFF_V,
-                   sBar = sbase + Sh::OFF_BAR;
+                   sK8 = sbase + Sh::OFF_K8, sV8 = sbase + Sh::OFF_V8, sBar = sbase + Sh::OFF_BAR;
     auto k_full = [&](int s) { return sBar + 8u * s; };
     auto k_empty = [&](int s) { return sBar + 8u * (KST + s); };
     auto v_full = [&](int s) { return sBar + 8u * (2 * KST + s); };
@@ -146,6 +181,18 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
     // waits for, so parity waits are unambiguous.
     auto o_fin = [&](int b) { return sBar2 + 8u * (4 + b); };
     const uint32_t mma_done = sBar2 + 8u * 6;
+    // KV8: the 8-bit rings (filled by TMA, emptied by the converters), the
+    // f16 copy of each pair's Q, and the row-scale slots (filled by the
+    // converters, read by the softmax).
+    constexpr int K8ST = Sh::K8ST, V8ST = Sh::V8ST, NSC = Sh::NSC;
+    const uint32_t sBar3 = sBar2 + 8u * 7;
+    auto k8_full = [&](int s) { return sBar3 + 8u * s; };
+    auto k8_empty = [&](int s) { return sBar3 + 8u * (K8ST + s); };
+    auto v8_full = [&](int s) { return sBar3 + 8u * (2 * K8ST + s); };
+    auto v8_empty = [&](int s) { return sBar3 + 8u * (2 * K8ST + V8ST + s); };
+    auto q_conv = [&](int s) { return sBar3 + 8u * (2 * K8ST + 2 * V8ST + s); };
+    auto sc_full = [&](int s) { return sBar3 + 8u * (2 * K8ST + 2 * V8ST + NQ + s); };
+    auto sc_empty = [&](int s) { return sBar3 + 8u * (2 * K8ST + 2 * V8ST + NQ + NSC + s); };
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + Sh::OFF_MISC);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + Sh::OFF_MISC + 8);
 
@@ -160,13 +207,29 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
         asm volatile("prefetch.tensormap [%0];\n" ::"l"(reinterpret_cast<uint64_t>(&maps.v)) : "memory");
     }
     if (tid == 0) {
+        // (KV8: the converter warps of each tensor fill the f16 stages)
         for (int s = 0; s < KST; ++s) {
-            tc::mbar_init(k_full(s), 1);
+            tc::mbar_init(k_full(s), KV8 ? Sh::NCW : 1);
             tc::mbar_init(k_empty(s), 2);  // both S issuers
         }
         for (int s = 0; s < VST; ++s) {
-            tc::mbar_init(v_full(s), 1);
+            tc::mbar_init(v_full(s), KV8 ? Sh::NCW : 1);
             tc::mbar_init(v_empty(s), 1);
+        }
+        if constexpr (KV8) {
+            for (int s = 0; s < K8ST; ++s) {
+                tc::mbar_init(k8_full(s), 1);
+                tc::mbar_init(k8_empty(s), Sh::NCW);
+            }
+            for (int s = 0; s < V8ST; ++s) {
+                tc::mbar_init(v8_full(s), 1);
+                tc::mbar_init(v8_empty(s), Sh::NCW);
+            }
+            for (int s = 0; s < NQ; ++s) tc::mbar_init(q_conv(s), 1);
+            for (int s = 0; s < NSC; ++s) {
+                tc::mbar_init(sc_full(s), 2 * Sh::NCW);  // the converter warps
+                tc::mbar_init(sc_empty(s), Sh::NSW);  // the softmax warps
+            }
         }
         for (int s = 0; s < NQ; ++s) {
             tc::mbar_init(q_full(s), 1);
@@ -327,8 +390,16 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
             const uint64_t pol_kv = l2_evict_first_policy();
             Tile t;
             int j = 0;
-            const int NS = is_k ? KST : VST;
+            // KV8: the 8-bit rings (128-column boxes of one-byte codes).
+            const int NS = KV8 ? (is_k ? K8ST : V8ST) : (is_k ? KST : VST);
             const CUtensorMap* map = is_k ? &maps.k : &maps.v;
+            constexpr int NBOX = KV8 ? Sh::KB8 : KB, BOXC = KV8 ? 128 : 64;
+            constexpr uint32_t STAGE = KV8 ? Sh::TILE8_BYTES : Sh::TILE_BYTES;
+            auto full_of = [&](int s2) { return KV8 ? (is_k ? k8_full(s2) : v8_full(s2)) : (is_k ? k_full(s2) : v_full(s2)); };
+            auto empty_of = [&](int s2) {
+                return KV8 ? (is_k ? k8_empty(s2) : v8_empty(s2)) : (is_k ? k_empty(s2) : v_empty(s2));
+            };
+            const uint32_t ring = KV8 ? (is_k ? sK8 : sV8) : (is_k ? sK : sV);
             // Early mode: only tiles holding a pair's appended rows (those from
             // pos on) wait for the append's grid; tiles before them stream
             // meanwhile. pos is an input (complete at launch), read once per
@@ -354,16 +425,15 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
                     }
                 }
                 const int s = j % NS;
-                const uint32_t full = is_k ? k_full(s) : v_full(s);
-                const uint32_t empty = is_k ? k_empty(s) : v_empty(s);
-                if (!tc::mbar_wait(empty, ((j / NS) & 1) ^ 1, abort_flag, kBudget)) break;
-                tc::mbar_arrive_expect_tx(full, (uint32_t)Sh::TILE_BYTES);
-                const uint32_t dst = (is_k ? sK : sV) + (uint32_t)(s * Sh::TILE_BYTES);
+                const uint32_t full = full_of(s);
+                if (!tc::mbar_wait(empty_of(s), ((j / NS) & 1) ^ 1, abort_flag, kBudget)) break;
+                tc::mbar_arrive_expect_tx(full, STAGE);
+                const uint32_t dst = ring + (uint32_t)s * STAGE;
                 if (!paged) {
                     const int row = (t.b / vt) * p.S_max + t.tok_lo;
 #pragma unroll
-                    for (int kb = 0; kb < KB; ++kb)
-                        tc::tma_load_3d(dst + kb * Sh::KB_BYTES, map, kb * 64, t.h, row, full, pol_kv);
+                    for (int kb = 0; kb < NBOX; ++kb)
+                        tc::tma_load_3d(dst + kb * Sh::KB_BYTES, map, kb * BOXC, t.h, row, full, pol_kv);
                 } else {
                     // Paged cache: the tile is fetched as boxes of box_rows
                     // tokens (the page size, up to the tile), each from its
@@ -385,8 +455,8 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
                                 atomicOr(p.status, KVD_STATUS_BAD_PAGE);
                         }
 #pragma unroll
-                        for (int kb = 0; kb < KB; ++kb)
-                            tc::tma_load_3d(dst + kb * Sh::KB_BYTES + r0 * 128, map, kb * 64, t.h, row, full, pol_kv);
+                        for (int kb = 0; kb < NBOX; ++kb)
+                            tc::tma_load_3d(dst + kb * Sh::KB_BYTES + r0 * 128, map, kb * BOXC, t.h, row, full, pol_kv);
                     }
                 }
                 ++j;
@@ -394,7 +464,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
             // Do not leave with copies in flight: wait for the last loads to land.
             for (int jj = (j > NS ? j - NS : 0); jj < j; ++jj) {
                 const int s = jj % NS;
-                tc::mbar_wait(is_k ? k_full(s) : v_full(s), (jj / NS) & 1, abort_flag, kBudget / 4);
+                tc::mbar_wait(full_of(s), (jj / NS) & 1, abort_flag, kBudget / 4);
             }
         }
     } else if (warp == 9) {
@@ -403,40 +473,97 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
         // pair's last S is done) never holds up the K stream. When the run goes
         // on into a next pair, that pair's Q rows are also prefetched into L2,
         // so its load is short when its turn comes.
-        if (lane == 0) {
+        if constexpr (!KV8) {
+            if (lane == 0) {
+                const uint64_t pol_q = tc::l2_evict_last_policy();
+                // q staged by the preceding append (host-input step): wait for it.
+                if (p.early && p.q_wait) pdl_wait();
+                Tile t;
+                int qn = 0;
+                while (walker.next(t, NoOp{})) {
+                    if (!t.seg_start) continue;
+                    const int qs = qn % NQ;
+                    if (!tc::mbar_wait(q_empty(qs), ((qn / NQ) & 1) ^ 1, abort_flag, kBudget)) break;
+                    // The pair's query rows: its G heads, or at M = 128 the G heads
+                    // of each of the sequence's TQ query tokens, token i at rows
+                    // i * G8 (8-row aligned, as the swizzled layout needs).
+                    const int TQ = (MR == 128) ? p.T : 1, G8 = (G + 7) & ~7;
+                    tc::mbar_arrive_expect_tx(q_full(qs), (uint32_t)(KB * 128 * G * TQ));
+                    for (int i2 = 0; i2 < TQ; ++i2) {
+                        const int qrow = (t.b * TQ + i2) * p.Hq + t.h * G;
+#pragma unroll
+                        for (int kb = 0; kb < KB; ++kb)
+                            tc::tma_load_2d(sQ + qs * Sh::QS_BYTES + kb * Sh::QB_BYTES + i2 * G8 * 128, &maps.q, kb * 64,
+                                            qrow, q_full(qs), pol_q);
+                    }
+                    ++qn;
+                    if (walker.pstart + walker.ext() < walker.E) {
+                        const int nh = (t.h + 1 < p.Hkv) ? t.h + 1 : 0;
+                        const int nb = (t.h + 1 < p.Hkv) ? t.b : t.b + 1;
+                        if (nb < p.B)
+                            for (int i2 = 0; i2 < TQ; ++i2)
+                                tc::prefetch_l2(reinterpret_cast<const uint8_t*>(p.q) +
+                                                    (((size_t)nb * TQ + i2) * p.Hq + (size_t)nh * G) * D * 2,
+                                                (uint32_t)(G * D * 2));
+                    }
+                }
+                if (qn > 0) tc::mbar_wait(q_full((qn - 1) % NQ), ((qn - 1) / NQ) & 1, abort_flag, kBudget / 4);
+            }
+        } else {
+            // KV8: the whole warp then converts the pair's rows to f16 in place
+            // (the MMAs take f16 operands against the f16 K and V tiles) and
+            // signals q_conv, which the S issuers wait for.
             const uint64_t pol_q = tc::l2_evict_last_policy();
-            // q staged by the preceding append (host-input step): wait for it.
             if (p.early && p.q_wait) pdl_wait();
             Tile t;
             int qn = 0;
-            while (walker.next(t, NoOp{})) {
+            bool ok = true;
+            while (ok && walker.next(t, NoOp{})) {
                 if (!t.seg_start) continue;
                 const int qs = qn % NQ;
-                if (!tc::mbar_wait(q_empty(qs), ((qn / NQ) & 1) ^ 1, abort_flag, kBudget)) break;
-                // The pair's query rows: its G heads, or at M = 128 the G heads
-                // of each of the sequence's TQ query tokens, token i at rows
-                // i * G8 (8-row aligned, as the swizzled layout needs).
-                const int TQ = (MR == 128) ? p.T : 1, G8 = (G + 7) & ~7;
-                tc::mbar_arrive_expect_tx(q_full(qs), (uint32_t)(KB * 128 * G * TQ));
-                for (int i2 = 0; i2 < TQ; ++i2) {
-                    const int qrow = (t.b * TQ + i2) * p.Hq + t.h * G;
+                if (lane == 0) {
+                    ok = tc::mbar_wait(q_empty(qs), ((qn / NQ) & 1) ^ 1, abort_flag, kBudget);
+                    if (ok) {
+                        tc::mbar_arrive_expect_tx(q_full(qs), (uint32_t)(KB * 128 * G));
+                        const int qrow = t.b * p.Hq + t.h * G;
 #pragma unroll
-                    for (int kb = 0; kb < KB; ++kb)
-                        tc::tma_load_2d(sQ + qs * Sh::QS_BYTES + kb * Sh::QB_BYTES + i2 * G8 * 128, &maps.q, kb * 64,
-                                        qrow, q_full(qs), pol_q);
+                        for (int kb = 0; kb < KB; ++kb)
+                            tc::tma_load_2d(sQ + qs * Sh::QS_BYTES + kb * Sh::QB_BYTES, &maps.q, kb * 64, qrow,
+                                            q_full(qs), pol_q);
+                    }
                 }
+                ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+                if (!ok) break;
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(q_full(qs), (qn / NQ) & 1, abort_flag, kBudget));
+                if (!ok) break;
+                // Each block's G rows are contiguous (128 bytes a row); the
+                // conversion is elementwise, so the swizzle does not matter.
+                const int n16 = G * 8;
+#pragma unroll 1
+                for (int kb = 0; kb < KB; ++kb) {
+                    uint4* q4 = reinterpret_cast<uint4*>(smem + Sh::OFF_Q + qs * Sh::QS_BYTES + kb * Sh::QB_BYTES);
+#pragma unroll 4
+                    for (int idx = lane; idx < n16; idx += 32) {
+                        uint4 v = q4[idx];
+                        v.x = bf16x2_to_f16x2(v.x);
+                        v.y = bf16x2_to_f16x2(v.y);
+                        v.z = bf16x2_to_f16x2(v.z);
+                        v.w = bf16x2_to_f16x2(v.w);
+                        q4[idx] = v;
+                    }
+                }
+                tc::fence_proxy_async_smem();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(q_conv(qs));
                 ++qn;
-                if (walker.pstart + walker.ext() < walker.E) {
+                if (lane == 0 && walker.pstart + walker.ext() < walker.E) {
                     const int nh = (t.h + 1 < p.Hkv) ? t.h + 1 : 0;
                     const int nb = (t.h + 1 < p.Hkv) ? t.b : t.b + 1;
                     if (nb < p.B)
-                        for (int i2 = 0; i2 < TQ; ++i2)
-                            tc::prefetch_l2(reinterpret_cast<const uint8_t*>(p.q) +
-                                                (((size_t)nb * TQ + i2) * p.Hq + (size_t)nh * G) * D * 2,
-                                            (uint32_t)(G * D * 2));
+                        tc::prefetch_l2(reinterpret_cast<const uint8_t*>(p.q) + ((size_t)nb * p.Hq + (size_t)nh * G) * D * 2,
+                                        (uint32_t)(G * D * 2));
                 }
             }
-            if (qn > 0) tc::mbar_wait(q_full((qn - 1) % NQ), ((qn - 1) / NQ) & 1, abort_flag, kBudget / 4);
         }
     } else if (warp == 1 || warp == 7) {
         // ===================== S issuers (one thread each) =====================
@@ -450,14 +577,15 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
         if (lane == 0) {
             const int kh = (warp == 7) ? 1 : 0;
             constexpr int KH = D / 32;  // k-steps per half
-            constexpr uint32_t idesc_s = tc::idesc_bf16_f32(MR, T, false, false);
+            constexpr uint32_t idesc_s = tc::idesc_f32acc(MR, T, false, false, KV8);  // f16 operands for KV8
             const uint32_t s_base = tmem + (kh ? Sh::TMEM_S2 : Sh::TMEM_S);
             Tile t;
             int i = 0, qn = 0;
             while (walker.next(t, NoOp{})) {
                 const int sk = i % KST;
                 if (t.seg_start) {
-                    if (!tc::mbar_wait(q_full(qn % NQ), (qn / NQ) & 1, abort_flag, kBudget)) break;
+                    if (!tc::mbar_wait(KV8 ? q_conv(qn % NQ) : q_full(qn % NQ), (qn / NQ) & 1, abort_flag, kBudget))
+                        break;
                     ++qn;
                 }
                 const int qs = (qn - 1) % NQ;
@@ -487,7 +615,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
         // O += P(i) V(i): A = P from TMEM buffer i & 1 (the hi part, then the
         // lo part for fp32 output), B = the V stage in MN-major layout.
         if (lane == 0) {
-            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(MR, D, false, true);
+            constexpr uint32_t idesc_o = tc::idesc_f32acc(MR, D, false, true, KV8);
             Tile t;
             int i = 0;
             while (walker.next(t, NoOp{})) {
@@ -511,6 +639,124 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
             }
             tc::mma_commit(mma_done);
             tc::mbar_wait(mma_done, 0, abort_flag, kBudget);
+        }
+    } else if (KV8 && warp >= 10) {
+        static_assert(!KV8 || Sh::NCW == 2 || Sh::NCW == 4, "converter warps per tensor");
+        // ===================== converters (KV8: warps 10 .. 10 + NCW - 1 for K, the next NCW for V) =====================
+        // Each tensor's NCW warps turn its 8-bit tiles into f16 tiles in the
+        // layout TMA would have written for bf16 rows (128-byte swizzle,
+        // 64-column blocks), and read the tile's row scales from global
+        // memory into a scale slot for the softmax (zero past the tile's
+        // last token, so those rows weigh nothing). Chunk g of the 4 D 16-byte
+        // chunks of a tile goes to thread g % NCT of the tensor's NCT
+        // threads; the low bits of g pick column chunk c = 4 h + (g & 3) of
+        // row rho or rho ^ 5 of an 8-row group, so that the 8 threads of each
+        // quarter-warp read 8 distinct 16-byte bank groups of the 8-bit tile
+        // and write 8 distinct ones of the f16 tile; the higher bits pick the
+        // 8-row group and the 128-column block.
+        constexpr int NCW = Sh::NCW > 0 ? Sh::NCW : 1, NCT = NCW * 32;  // (NCW = 0 without KV8: unused)
+        const bool is_k = warp < 10 + NCW;
+        const int cth = (warp - 10 - (is_k ? 0 : NCW)) * 32 + lane;  // 0 .. NCT - 1 within the tensor
+        const int N8 = is_k ? K8ST : V8ST, NF = is_k ? KST : VST;
+        const uint32_t r8 = is_k ? sK8 : sV8, rf = is_k ? sK : sV;
+        const float* gsc = is_k ? p.k_scale : p.v_scale;
+        const float scmul = (FP8 && is_k) ? 256.f : 1.f;  // E4M3 key rows arrive divided by 256
+        const int r = cth;                                 // the tile row whose scale this thread reads (r < T)
+        // This thread's chunk: the bits of g % 64 give its row rlo within an
+        // 8-row group and its column chunk c8; the swizzle depends on the row
+        // only through rlo, so the offsets step evenly from chunk to chunk.
+        const int clo = cth & 3, sel = (cth >> 2) & 1, h = (cth >> 3) & 1, rho = (cth >> 4) & 3;
+        const int rlo = sel ? (rho ^ 5) : rho, c8 = 4 * h + clo;
+        const uint32_t rg0 = (uint32_t)(cth >> 6);  // first 8-row group (NCT = 128: 0 or 1)
+        const uint32_t src_off = rg0 * 1024 + rlo * 128 + ((c8 ^ rlo) * 16);
+        const uint32_t dst_off = h * Sh::KB_BYTES + rg0 * 1024 + rlo * 128;
+        const uint32_t d0 = ((2 * clo) ^ rlo) * 16, d1 = ((2 * clo + 1) ^ rlo) * 16;
+        // The row scales are loaded two tiles ahead (a second walker runs in
+        // front), so their latency hides behind the conversions in between.
+        // Early mode: as the producers, the append is waited for before a
+        // tile holding rows it writes.
+        bool waited = !p.early;
+        int pos_pair = -1, pos_b = -1;
+        auto load_scale = [&](const Tile& ta) -> float {
+            if (!waited) {
+                const int pair = ta.b * p.Hkv + ta.h;
+                if (pair != pos_pair) {
+                    pos_pair = pair;
+                    pos_b = __ldg(p.pos + ta.b / vt);
+                }
+                if (ta.tok_hi > pos_b) {
+                    pdl_wait();
+                    waited = true;
+                }
+            }
+            // The row's scale: cache row b * S_max + token, or in a paged
+            // cache its row in the pool (a table entry naming no page gives
+            // zero codes, read past the pool's end, and a zero scale); zero
+            // past the tile's last token.
+            float v = 0.f;
+            if (r < ta.tok_hi - ta.tok_lo && r < T) {
+                const int tok = ta.tok_lo + r;
+                long long row = (long long)(ta.b / vt) * p.S_max + tok;
+                if (p.block_table) {
+                    const int page = __ldg(p.block_table + (size_t)(ta.b / vt) * p.max_blocks + (tok >> p.page_shift));
+                    row = ((unsigned)page < (unsigned)p.num_pages)
+                              ? ((long long)page << p.page_shift) + (tok & ((1 << p.page_shift) - 1))
+                              : -1;
+                }
+                if (row >= 0) v = __ldg(gsc + (size_t)row * p.Hkv + ta.h);  // (not used until two tiles on)
+            }
+            return v;
+        };
+        WalkerT ahead = walker;
+        Tile t, ta;
+        float sc_next[2];
+#pragma unroll
+        for (int k = 0; k < 2; ++k) sc_next[k] = ahead.next(ta, NoOp{}) ? load_scale(ta) : 0.f;
+        int j = 0;
+        bool ok = true;
+        while (ok && walker.next(t, NoOp{})) {
+            const float sc = sc_next[0];
+            sc_next[0] = sc_next[1];
+            sc_next[1] = ahead.next(ta, NoOp{}) ? load_scale(ta) : 0.f;
+            const int s8 = j % N8, sf = j % NF, ss = j % NSC;
+            ok = __all_sync(0xffffffffu, tc::mbar_wait(is_k ? k8_full(s8) : v8_full(s8), (j / N8) & 1, abort_flag,
+                                                       kBudget));
+            if (!ok) break;
+            ok = __all_sync(0xffffffffu, tc::mbar_wait(is_k ? k_empty(sf) : v_empty(sf), ((j / NF) & 1) ^ 1,
+                                                       abort_flag, kBudget));
+            if (!ok) break;
+            ok = __all_sync(0xffffffffu, tc::mbar_wait(sc_empty(ss), ((j / NSC) & 1) ^ 1, abort_flag, kBudget));
+            if (!ok) break;
+            const uint8_t* src = smem + (r8 - sbase) + (size_t)s8 * Sh::TILE8_BYTES + src_off;
+            uint8_t* dst = smem + (rf - sbase) + (size_t)sf * Sh::TILE_BYTES + dst_off;
+            // Step it of this thread: 8-bit rows NCT / 64 groups on (NCT / 64 KB
+            // a step), f16 rows likewise, 128-column blocks every 8 groups.
+            constexpr int GPS = NCT / 64;  // 8-row groups a step
+#pragma unroll 4
+            for (int it = 0; it < D * 4 / NCT; ++it) {
+                const uint4 w = *reinterpret_cast<const uint4*>(src + it * GPS * 1024);
+                uint32_t f[8];
+                const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const uint32_t u = FP8 ? wv[q] : (wv[q] ^ 0x80808080u);
+                    f[2 * q] = codes_to_f16x2<FP8, 0x4140, 0x9180>(u);
+                    f[2 * q + 1] = codes_to_f16x2<FP8, 0x4342, 0xb3a2>(u);
+                }
+                const int grp = it * GPS;  // first 8-row group of the step (of 8 per 128-column block)
+                uint8_t* drow = dst + (grp >> 3) * 2 * Sh::KB_BYTES + (grp & 7) * 1024;
+                *reinterpret_cast<uint4*>(drow + d0) = make_uint4(f[0], f[1], f[2], f[3]);
+                *reinterpret_cast<uint4*>(drow + d1) = make_uint4(f[4], f[5], f[6], f[7]);
+            }
+            if (r < T) reinterpret_cast<float*>(smem + Sh::OFF_SC + ss * 2 * T * 4)[(is_k ? 0 : T) + r] = sc * scmul;
+            tc::fence_proxy_async_smem();  // the f16 tile, for the tensor core
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(is_k ? k8_empty(s8) : v8_empty(s8));
+                tc::mbar_arrive(is_k ? k_full(sf) : v_full(sf));
+                tc::mbar_arrive(sc_full(ss));
+            }
+            ++j;
         }
     } else if ((warp >= 3 && warp <= 6) || warp >= 10) {
         // ===================== softmax / epilogue (warps 3..6, 10..13) =====================
@@ -578,6 +824,15 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
         while (ok && walker.next(t, write_empty)) {
             ok = __all_sync(0xffffffffu, tc::mbar_wait(s_full, i & 1, abort_flag, kBudget));
             if (!ok) break;
+            // KV8: the tile's key and value row scales (zero past its last token).
+            const float* ksc = nullptr;
+            const float* vsc = nullptr;
+            if constexpr (KV8) {
+                ok = __all_sync(0xffffffffu, tc::mbar_wait(sc_full(i % NSC), (i / NSC) & 1, abort_flag, kBudget));
+                if (!ok) break;
+                ksc = reinterpret_cast<const float*>(smem + Sh::OFF_SC + (i % NSC) * 2 * T * 4) + hl * HT;
+                vsc = ksc + T;
+            }
             tc::fence_after_sync();
             __syncwarp();
             const int nvalid = t.tok_hi - t.tok_lo;
@@ -611,9 +866,12 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
                     if (MR == 128) vis = min(vis, t.L - (TQ - 1 - tok_[rg]) - t.tok_lo);
                     const int nv = vis - hl * HT;  // valid columns of this thread (may be <= 0)
 #pragma unroll
-                    for (int e = 0; e < HT; ++e)
-                        s[e] = (e < nv) ? (__uint_as_float(sa[e]) + __uint_as_float(sb[e])) * scale_log2
-                                        : -CUDART_INF_F;
+                    for (int e = 0; e < HT; ++e) {
+                        // (KV8: times the key row's scale; E4M3 key rows, which arrive
+                        // divided by 256, have it times 256)
+                        const float sc = KV8 ? scale_log2 * ksc[e] : scale_log2;
+                        s[e] = (e < nv) ? (__uint_as_float(sa[e]) + __uint_as_float(sb[e])) * sc : -CUDART_INF_F;
+                    }
                 }
                 float mx = s[0];
 #pragma unroll
@@ -623,7 +881,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
                 alpha[rg] = 1.f;
                 if (t.seg_start) {
                     m[rg] = mx;
-                    if (p.umax) {
+                    if (!KV8 && p.umax) {
                         // Unified maximum (FlashDecoding++'s asynchronized softmax):
                         // a row whose first tile's maximum lies within [phi - 64,
                         // phi + 8] (base 2) takes m = phi, shared by all partials of
@@ -640,7 +898,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
                     need_any = true;
                     alpha[rg] = (m[rg] == -CUDART_INF_F) ? 0.f : exp2f(m[rg] - mx);
                     m[rg] = mx;
-                    if (p.umax && active && p.status) atomicOr(p.status, KVD_STATUS_UMAX_FALLBACK);
+                    if (!KV8 && p.umax && active && p.status) atomicOr(p.status, KVD_STATUS_UMAX_FALLBACK);
                 }
                 // P = 2^(s - m), packed in pairs of adjacent tokens (bf16 hi part;
                 // lo part for fp32 output). A row that has seen no column yet
@@ -652,6 +910,16 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
                 for (int g = 0; g < HT / 2; ++g) {
                     const float e0 = live ? tc::ex2_approx(s[2 * g] - m[rg]) : 0.f;
                     const float e1 = live ? tc::ex2_approx(s[2 * g + 1] - m[rg]) : 0.f;
+                    if constexpr (KV8) {
+                        // Weights times the value rows' scales, in f16 (the V
+                        // tiles hold the codes' values); the sums take the
+                        // weights themselves.
+                        const float w0 = e0 * vsc[2 * g], w1 = e1 * vsc[2 * g + 1];
+                        hi[g] = pack_f16x2(w0, w1);
+                        if constexpr (F32OUT) lo[g] = pack_f16x2(w0 - f16_lo(hi[g]), w1 - f16_hi(hi[g]));
+                        ls += e0 + e1;
+                        continue;
+                    }
                     hi[g] = pack_bf16x2(e0, e1);
                     if constexpr (F32OUT) {
                         lo[g] = pack_bf16x2(e0 - bf16_lo(hi[g]), e1 - bf16_hi(hi[g]));
@@ -690,7 +958,14 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
                 }
             }
             tc::tmem_wait_st();
-            if (nvalid < T) {
+            if constexpr (KV8) {
+                // This tile's scales are read: free their slot.
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(sc_empty(i % NSC));
+            }
+            // (KV8 tiles need no zeroing: every code converts to a finite value,
+            // and the rows past the tile's end have zero scales.)
+            if (!KV8 && nvalid < T) {
                 // Rows past the sequence's end came from the cache's padding (or the
                 // next sequence): zero them so that 0-weights never meet NaN.
                 const int sv = i % VST;
@@ -724,7 +999,7 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR>::THREADS, 1)
                     // Partial slots hold the pair's T * G rows, token-major.
                     const size_t prow = slot * (size_t)(TQ * G) + (size_t)tok_[rg] * G + hd_[rg];
                     // Each thread writes 32 contiguous columns of its row per step.
-                    const float inv = t.full ? ((ltot > 0.f) ? 1.f / ltot : 0.f) : 1.f;
+                    const float inv = t.full ? ((ltot > 0.f) ? OSC / ltot : 0.f) : OSC;
                     const size_t grow = t.full ? qrow : prow;  // output (or partial) row
 #pragma unroll 1
                     for (int cc = 0; cc < HD / 32; ++cc) {

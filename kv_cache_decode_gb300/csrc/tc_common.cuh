@@ -148,15 +148,19 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo, ui
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma kind::f16: bf16 x bf16 -> fp32.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+// Instruction descriptor of tcgen05.mma kind::f16 with fp32 accumulators: A and B
+// both bf16, or both f16.
+__host__ __device__ constexpr uint32_t idesc_f32acc(int M, int N, bool a_mn_major, bool b_mn_major, bool f16) {
     return (1u << 4)                       // D format: f32
-           | (1u << 7)                     // A format: bf16
-           | (1u << 10)                    // B format: bf16
+           | ((f16 ? 0u : 1u) << 7)        // A format: f16 (0) or bf16 (1)
+           | ((f16 ? 0u : 1u) << 10)       // B format: the same
            | ((a_mn_major ? 1u : 0u) << 15)
            | ((b_mn_major ? 1u : 0u) << 16)
            | ((uint32_t)(N >> 3) << 17)
            | ((uint32_t)(M >> 4) << 24);
+}
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn_major, bool b_mn_major) {
+    return idesc_f32acc(M, N, a_mn_major, b_mn_major, false);
 }
 
 __device__ __forceinline__ void mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,

@@ -23,6 +23,7 @@ CASES = [
     ("mha64", 5, 6, 6, 64, 400, 1, 400, 122),
     ("g8d256", 4, 16, 2, 256, 300, 1, 300, 123),
     ("mqa48", 4, 48, 1, 256, 700, 1, 700, 124),
+    ("g64d128", 3, 64, 1, 128, 500, 1, 500, 126),
 ]
 
 

@@ -2,8 +2,9 @@
 quantizing append against the oracle's quantizer (bit for bit: every code and
 scale), and attention over the int8 cache against the oracle's attention over
 the rows read back (the usual tolerances). Shapes cover the head dimensions
-and groups from MHA to MQA (above 16 query heads per KV head, in several CTAs
-of 16 per token run), ragged and empty sequences; rows past each
+and groups from MHA to MQA (above 16 query heads per KV head on the tensor-core
+kernel's converting variant, or in several mma.sync CTAs of 16 per token run),
+ragged and empty sequences; rows past each
 sequence's end hold an invalid code and NaN scales, so any over-read fails.
 """
 import numpy as np
@@ -22,10 +23,15 @@ CASES = [
     ("mha64", 5, 6, 6, 64, 400, 1, 400, 52),
     ("g8d256", 4, 16, 2, 256, 300, 1, 300, 53),
     ("g16", 3, 16, 1, 128, 1100, 1, 1100, 54),
-    # groups above 16: several CTAs of 16 query heads per token run
+    # groups above 16: the tensor-core kernel's converting variant at head_dim
+    # 128 and 256 (Q blocks of 48 and, for g64d128, 64 rows); at head_dim 64,
+    # and for groups above 48 at 256, several mma.sync CTAs of 16 query heads
+    # per token run
     ("mqa48", 4, 48, 1, 256, 700, 1, 700, 56),
     ("g32d128", 5, 64, 2, 128, 600, 0, 600, 57),
     ("g20d64", 3, 20, 1, 64, 520, 1, 520, 58),
+    ("g64d128", 3, 64, 1, 128, 500, 1, 500, 59),
+    ("g56d256", 2, 56, 1, 256, 300, 1, 300, 60),
 ]
 
 
