@@ -273,8 +273,11 @@ kvd_status kvd_decode_step_paged(void* k_pages, void* v_pages, const void* k_new
  * read back: q stays bf16, the cache rows are exact small integers times
  * their scale, and the kernels compute in f16 MMAs with fp32 accumulation,
  * with each score multiplied by its key row's scale and each weight by its
- * value row's scale. Every supported group (the mma.sync kernel, one CTA per
- * 16 query heads of a group and token run); head_dim 64, 128 or 256. The
+ * value row's scale. Every supported group: groups of 17 to 64 query heads
+ * at head_dim 128, or 17 to 48 at 256, on the tcgen05 kernel's converting
+ * variant (the codes converted exactly to f16 in shared memory), others on
+ * the mma.sync kernel (one CTA per 16 query heads of a group and token run);
+ * head_dim 64, 128 or 256. The
  * split count and workspace are kvd_decode_plan's. A paged int8 cache (code
  * pools [num_pages, page_size, n_heads_kv, head_dim] and scale pools
  * [num_pages, page_size, n_heads_kv], one block table for both) is appended
@@ -349,8 +352,10 @@ kvd_status kvd_decode_step_q8(void* k_codes, void* v_codes, float* k_scales, flo
  * A query token that sees no token (L_b < T - i) gets a zero row and lse -inf.
  * T from 1 to KVD_MAX_TOKENS (above: KVD_ERR_UNSUPPORTED), any supported
  * group. Groups of up to 16 run on the mma.sync kernel, one CTA per 16 of a
- * pair's T * G rows and token run; wider groups on the tcgen05 kernel, each
- * query token as a sequence of its own over the shared cache rows. T = 1 is
+ * pair's T * G rows and token run; wider groups on the tcgen05 kernel, with
+ * the T tokens' rows stacked in one 128-row tile when T times the group
+ * (rounded up to 8) is at most 128 (bf16 caches), else each query token as a
+ * sequence of its own over the shared cache rows. T = 1 is
  * exactly the single-token call. The split count is the single-token plan's,
  * and the workspace holds T times the rows: size it with
  * kvd_decode_plan_multi. Rows of the append outside [0, s_max) are skipped
