@@ -732,8 +732,8 @@ def run_ours(args):
                        "write the result into pinned host memory)" if host_steps is not None else
                        "torch copies in, the step call, a copy back, per step")}
         if host_steps is not None:
-            # Where the time goes: the packet's copy in alone, the device step
-            # alone (ms_per_step above), and the same host step captured once
+            # Where the time goes: the packet's copy in alone, the result's copy
+            # out alone, the device step alone (ms_per_step above), and the same host step captured once
             # per cache copy in a CUDA graph (copy-in node, kernels writing the
             # result to host memory) and replayed: no per-step launch cost.
             hs = [torch.cuda.Event(enable_timing=True) for _ in range(2 * 20)]
@@ -744,6 +744,17 @@ def run_ours(args):
                 hs[2 * i + 1].record()
             torch.cuda.synchronize()
             h2d_us = statistics.median(hs[2 * i].elapsed_time(hs[2 * i + 1]) * 1e3 for i in range(20))
+            # and the result's copy out alone (the kernels write it to host
+            # memory themselves in the step; this is what a separate copy costs)
+            od = torch.empty(out_h.shape, dtype=out_h.dtype, device=dev)
+            for i in range(20):
+                torch.cuda.synchronize()
+                hs[2 * i].record()
+                out_h.copy_(od, non_blocking=True)
+                hs[2 * i + 1].record()
+            torch.cuda.synchronize()
+            d2h_us = statistics.median(hs[2 * i].elapsed_time(hs[2 * i + 1]) * 1e3 for i in range(20))
+            del od
             # the steps bound to a capture stream (HostStep takes its stream when built)
             cs = torch.cuda.Stream(device=dev)
             host_steps_g = [kvd.HostStep(pq, pkn, pvn, ppos, plens, kcs[r], vcs[r], staging, max_len, w.scale,
@@ -757,7 +768,8 @@ def run_ours(args):
                 host_graphs.append(g)
             g_ms = time_replays(host_graphs, args.steps, args.warmup)
             g_ms, = max_over_ranks([g_ms], device=dev)
-            e2e["breakdown"] = {"h2d_copy_us": round(h2d_us, 2), "device_step_us": round(ms_per_step * 1e3, 2),
+            e2e["breakdown"] = {"h2d_copy_us": round(h2d_us, 2), "d2h_copy_us": round(d2h_us, 2),
+                                "device_step_us": round(ms_per_step * 1e3, 2),
                                 "api_call_us": round(e2e_ms * 1e3, 2),
                                 "graph_replay_us": round(g_ms * 1e3, 2),
                                 "graph_replay_gbs": round(job_rate_gbs(world, step_bytes, g_ms), 2)}
