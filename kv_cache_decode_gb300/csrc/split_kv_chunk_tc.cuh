@@ -413,6 +413,18 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR, KV8>::THREADS, 1)
                 pos_b = __ldg(p.pos + walker.b / vt);
             }
             while (walker.next(t, NoOp{})) {
+                // Paged cache: the tile's block-table entries (one per box of
+                // box_rows tokens, at most T / 16), loaded together before the
+                // wait for the stage, so that their latency overlaps it.
+                int entry[T / 16];
+                if (paged) {
+                    const int32_t* table = p.block_table + (size_t)(t.b / vt) * p.max_blocks;
+#pragma unroll
+                    for (int q = 0; q < T / 16; ++q) {
+                        const int tok = t.tok_lo + q * box_rows;
+                        entry[q] = (q * box_rows < T && tok < t.tok_hi) ? __ldg(table + (tok >> p.page_shift)) : -1;
+                    }
+                }
                 if (!waited) {
                     const int pair = t.b * p.Hkv + t.h;
                     if (pair != pos_pair) {
@@ -442,13 +454,15 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR, KV8>::THREADS, 1)
                     // 16 tokens), so no box crosses a page. A box past the
                     // tile's tokens, or whose table entry names no page, is
                     // read from past the pool's end: zeros.
-                    const int32_t* table = p.block_table + (size_t)(t.b / vt) * p.max_blocks;
                     const int oob = p.num_pages << p.page_shift;
-                    for (int r0 = 0; r0 < T; r0 += box_rows) {
+#pragma unroll
+                    for (int q = 0; q < T / 16; ++q) {
+                        const int r0 = q * box_rows;
+                        if (r0 >= T) break;
                         const int tok = t.tok_lo + r0;
                         int row = oob;
                         if (tok < t.tok_hi) {
-                            const int page = __ldg(table + (tok >> p.page_shift));
+                            const int page = entry[q];
                             if ((unsigned)page < (unsigned)p.num_pages)
                                 row = (page << p.page_shift) + (tok & ((1 << p.page_shift) - 1));
                             else if (is_k && p.status)
