@@ -41,8 +41,13 @@ from kv_cache_decode_gb300 import roofline  # noqa: E402
 METRIC = "decode-attention KV GB/s and % of GB300 HBM peak; decode tokens/s per shape"
 UNIT = "GB/s"
 # Every source of the attention kernels: a profile taken on other sources is stale.
-CHUNK_SOURCES = ["split_kv_chunk.cuh", "split_kv_chunk_variants.cuh", "split_kv_chunk_tc.cuh",
-                 "split_kv_chunk_tc_launch.cuh", "tc_common.cuh", "common.cuh", "schedule.cuh"]
+# The sources each chunk-kernel engine is compiled from (the tcgen05 kernel
+# also takes shared helpers from the mma.sync kernel's header).
+CHUNK_SOURCES = {
+    "mma": ["split_kv_chunk.cuh", "split_kv_chunk_variants.cuh", "common.cuh", "schedule.cuh", "params.h"],
+    "tc": ["split_kv_chunk_tc.cuh", "split_kv_chunk_tc_launch.cuh", "tc_common.cuh", "split_kv_chunk.cuh",
+           "common.cuh", "schedule.cuh", "params.h"],
+}
 
 
 def parse_args():
@@ -114,9 +119,9 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
-def chunk_source_hash() -> str:
+def chunk_source_hash(engine: str) -> str:
     h = hashlib.sha256()
-    for name in CHUNK_SOURCES:
+    for name in CHUNK_SOURCES[engine]:
         with open(os.path.join(ROOT, "kv_cache_decode_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -128,12 +133,12 @@ def ncu_traffic(config: str):
     path = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(path):
         return None
-    want = chunk_source_hash()
     for line in open(path):
         if line.startswith("#") or not line.strip():
             continue
         kv = dict(x.split("=", 1) for x in line.split())
-        if kv.get("config") == config and kv.get("src_sha") == want:
+        engine = "tc" if kv.get("kernel", "").startswith("split_kv_chunk_tc") else "mma"
+        if kv.get("config") == config and kv.get("src_sha") == chunk_source_hash(engine):
             return int(float(kv["dram_bytes_per_launch"]))
     return None
 
