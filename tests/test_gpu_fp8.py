@@ -24,6 +24,7 @@ CASES = [
     ("g8d256", 4, 16, 2, 256, 300, 1, 300, 123),
     ("mqa48", 4, 48, 1, 256, 700, 1, 700, 124),
     ("g64d128", 3, 64, 1, 128, 500, 1, 500, 126),
+    ("g24d128kv3", 3, 72, 3, 128, 400, 0, 400, 127),
 ]
 
 

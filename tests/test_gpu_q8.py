@@ -32,6 +32,9 @@ CASES = [
     ("g20d64", 3, 20, 1, 64, 520, 1, 520, 58),
     ("g64d128", 3, 64, 1, 128, 500, 1, 500, 59),
     ("g56d256", 2, 56, 1, 256, 300, 1, 300, 60),
+    # groups that are not a multiple of 8 (padded Q rows), several KV heads
+    ("g20d256", 3, 20, 1, 256, 300, 1, 300, 61),
+    ("g24d128kv3", 3, 72, 3, 128, 400, 0, 400, 62),
 ]
 
 
