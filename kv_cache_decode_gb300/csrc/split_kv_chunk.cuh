@@ -332,16 +332,24 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
             static_assert(NT % CH8 == 0 && TT % RSTEP8 == 0 && NT >= 2 * TT, "int8 row split");
             const int shift = p.page_shift, in_page = (1 << shift) - 1;
             const int first = t.tok_lo >> shift;
-            const int c8 = tid % CH8, q0 = tid / CH8;
+            // Each thread copies RPT8 consecutive rows (at most two pages), as
+            // the bf16 paged rows below.
+            static_assert(RPT8 <= 16, "a thread's rows span at most two pages");
+            const int c8 = tid % CH8, rq = (tid / CH8) * RPT8;
+            const int tok0 = t.tok_lo + rq;
+            const int kb1 = min(RPT8, (((tok0 >> shift) + 1) << shift) - tok0);  // rows on the first page
+            const long long po0 = (rq < nvalid) ? s_pages[ps][(tok0 >> shift) - first] : -1;
+            const long long po1 = (kb1 < RPT8 && rq + kb1 < nvalid) ? s_pages[ps][(tok0 >> shift) + 1 - first] : -1;
+            const long long base0 = po0 + (long long)(tok0 & in_page) * (long long)row_stride;
+            const long long base1 = po1 - (long long)kb1 * (long long)row_stride;
             const int8_t* kb = reinterpret_cast<const int8_t*>(p.k) + (size_t)t.h * D + c8 * 16;
             const int8_t* vb = reinterpret_cast<const int8_t*>(p.v) + (size_t)t.h * D + c8 * 16;
 #pragma unroll
             for (int k = 0; k < RPT8; ++k) {
-                const int r = q0 + k * RSTEP8;
-                const int tok = t.tok_lo + r;
-                const long long po = (r < nvalid) ? s_pages[ps][(tok >> shift) - first] : -1;
-                const bool ok = po >= 0;
-                const size_t off = ok ? (size_t)po + (size_t)(tok & in_page) * row_stride : 0;
+                const int r = rq + k;
+                const bool second = k >= kb1;
+                const bool ok = r < nvalid && (second ? po1 : po0) >= 0;
+                const size_t off = ok ? (size_t)((second ? base1 : base0) + (long long)k * (long long)row_stride) : 0;
                 const uint32_t dst = sbase + (uint32_t)(r * D + swz8<D>(r, c8) * 16);
                 cp_async_16(dst, kb + off, ok ? 16 : 0, policy);
                 cp_async_16(dst + TILE_ELEMS, vb + off, ok ? 16 : 0, policy);
@@ -393,17 +401,29 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
                 cp_async_16(dst + TILE_ELEMS * 2, vb + off, ok ? 16 : 0, policy);
             }
         } else {
+            // Paged: each thread copies RPT consecutive rows, which lie on at
+            // most two pages (a page holds at least 16 tokens, RPT <= 16): a
+            // row's offset is its page's base plus a multiple of the row
+            // stride, with the two page entries read once per tile.
+            static_assert(RPT <= 16, "a thread's rows span at most two pages");
             const int shift = p.page_shift, in_page = (1 << shift) - 1;
             const int first = t.tok_lo >> shift;
+            const int rq = r0 * RPT;        // this thread's first row
+            const int tok0 = t.tok_lo + rq;
+            const int kb1 = min(RPT, (((tok0 >> shift) + 1) << shift) - tok0);  // rows on the first page
+            const long long po0 = (rq < nvalid) ? s_pages[ps][(tok0 >> shift) - first] : -1;
+            const long long po1 = (kb1 < RPT && rq + kb1 < nvalid) ? s_pages[ps][(tok0 >> shift) + 1 - first] : -1;
+            // row k: base + k * row_stride, base chosen by page
+            const long long base0 = po0 + (long long)(tok0 & in_page) * (long long)row_stride;
+            const long long base1 = po1 - (long long)kb1 * (long long)row_stride;
             const __nv_bfloat16* kb = Kg + (size_t)t.h * D + ch * 8;
             const __nv_bfloat16* vb = Vg + (size_t)t.h * D + ch * 8;
 #pragma unroll(RUNROLL)
             for (int k = 0; k < RPT; ++k) {
-                const int r = r0 + k * RSTEP;
-                const int tok = t.tok_lo + r;
-                const long long po = (r < nvalid) ? s_pages[ps][(tok >> shift) - first] : -1;
-                const bool ok = po >= 0;
-                const size_t off = ok ? (size_t)po + (size_t)(tok & in_page) * row_stride : 0;
+                const int r = rq + k;
+                const bool second = k >= kb1;
+                const bool ok = r < nvalid && (second ? po1 : po0) >= 0;
+                const size_t off = ok ? (size_t)((second ? base1 : base0) + (long long)k * (long long)row_stride) : 0;
                 const uint32_t dst = sbase + (uint32_t)((r * D + ((ch ^ (r & 7)) * 8)) * 2);
                 cp_async_16(dst, kb + off, ok ? 16 : 0, policy);
                 cp_async_16(dst + TILE_ELEMS * 2, vb + off, ok ? 16 : 0, policy);
