@@ -23,6 +23,7 @@ CASES = [
     ("gqa4", 9, 32, 8, 128, 900, 0, 900, 91),
     ("mqa48", 4, 48, 1, 256, 700, 1, 700, 92),
     ("mha64", 5, 6, 6, 64, 400, 1, 400, 93),
+    ("g8d256", 4, 16, 2, 256, 300, 1, 300, 94),  # mma.sync, 16 consecutive rows a thread
 ]
 
 
