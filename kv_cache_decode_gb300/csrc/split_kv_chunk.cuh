@@ -519,6 +519,18 @@ __global__ void __launch_bounds__(HT* TS * 32, MINB) split_kv_chunk_kernel(const
 
         if (ct.seg_start) {
             const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(p.q);
+            // When the run goes on into another pair, that pair's query rows are
+            // brought into L2 now, so that its first loads are short.
+            if (tid == 0 && cw.pstart + cw.ext() < cw.E) {
+                const int nh = (ct.h + 1 < p.Hkv) ? ct.h + 1 : 0;
+                const int nb = (ct.h + 1 < p.Hkv) ? ct.b : ct.b + 1;
+                if (nb < p.B)
+                    for (int i = 0; i < T; ++i)
+                        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;\n" ::"l"(
+                                         reinterpret_cast<uint64_t>(qb + (((size_t)nb * T + i) * p.Hq + (size_t)nh * G) * D)),
+                                     "r"((uint32_t)(G * D * 2))
+                                     : "memory");
+            }
             const bool v0 = r0 < TG, v1 = r1 < TG;
             const uint32_t* q0 = reinterpret_cast<const uint32_t*>(qb + (v0 ? out_row(ct.b, ct.h, r0) : 0) * D);
             const uint32_t* q1 = reinterpret_cast<const uint32_t*>(qb + (v1 ? out_row(ct.b, ct.h, r1) : 0) * D);
