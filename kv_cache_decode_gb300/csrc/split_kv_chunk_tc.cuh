@@ -1012,15 +1012,12 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR, KV8>::THREADS, 1)
                     const size_t qrow = out_row(t.b, t.h, tok_[rg], hd_[rg]);
                     // Partial slots hold the pair's T * G rows, token-major.
                     const size_t prow = slot * (size_t)(TQ * G) + (size_t)tok_[rg] * G + hd_[rg];
-                    // Each thread writes 32 contiguous columns of its row per step.
+                    // Each thread writes 32 contiguous columns of its row per chunk;
+                    // two chunks' TMEM loads share one wait.
                     const float inv = t.full ? ((ltot > 0.f) ? OSC / ltot : 0.f) : OSC;
                     const size_t grow = t.full ? qrow : prow;  // output (or partial) row
-#pragma unroll 1
-                    for (int cc = 0; cc < HD / 32; ++cc) {
+                    auto put = [&](int cc, const uint32_t (&r)[32]) {
                         const int col0 = hl * HD + cc * 32;
-                        uint32_t r[32];
-                        tc::tmem_ld_16x32bx2_x32<HD>(tmem + lanes(rg) + Sh::TMEM_O + cc * 32, r);
-                        tc::tmem_wait_ld();
                         if (active && t.full && !F32OUT) {
                             uint4* o = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.out) + grow * D + col0);
 #pragma unroll
@@ -1036,6 +1033,25 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR, KV8>::THREADS, 1)
                                 o[k] = make_float4(__uint_as_float(r[4 * k]) * inv, __uint_as_float(r[4 * k + 1]) * inv,
                                                    __uint_as_float(r[4 * k + 2]) * inv, __uint_as_float(r[4 * k + 3]) * inv);
                         }
+                    };
+                    constexpr int NCH = HD / 32;  // 32-column chunks per thread
+                    // (the 14- and 18-warp variants have no registers for two chunks)
+                    constexpr bool PAIRS = (MR == 64 && !KV8);
+#pragma unroll 1
+                    for (int cc = 0; PAIRS && cc + 1 < NCH; cc += 2) {
+                        uint32_t r0[32], r1[32];
+                        tc::tmem_ld_16x32bx2_x32<HD>(tmem + lanes(rg) + Sh::TMEM_O + cc * 32, r0);
+                        tc::tmem_ld_16x32bx2_x32<HD>(tmem + lanes(rg) + Sh::TMEM_O + (cc + 1) * 32, r1);
+                        tc::tmem_wait_ld();
+                        put(cc, r0);
+                        put(cc + 1, r1);
+                    }
+#pragma unroll 1
+                    for (int cc = PAIRS ? NCH - NCH % 2 : 0; cc < NCH; ++cc) {
+                        uint32_t r0[32];
+                        tc::tmem_ld_16x32bx2_x32<HD>(tmem + lanes(rg) + Sh::TMEM_O + cc * 32, r0);
+                        tc::tmem_wait_ld();
+                        put(cc, r0);
                     }
                     if (active && hl == 0) {
                         if (t.full) {
