@@ -286,20 +286,32 @@ def rotation_count(kv_bytes: int, cache_bytes: int, l2: int) -> int:
     return max(1, min(R, int(40e9 // max(cache_bytes, 1)), 16))
 
 
-def time_replays(graphs, steps: int, warmup: int) -> float:
-    """Milliseconds per step of `steps` graph replays (round-robin over
-    `graphs`), queued behind a spin kernel so the GPU never waits for the host,
-    between CUDA events on the replay stream."""
+def time_replays(graphs, steps: int, warmup: int, round_graph=None) -> float:
+    """Milliseconds per step of `steps` steps run as graph replays, queued
+    behind a spin kernel so the GPU never waits for the host, between CUDA
+    events on the replay stream. `graphs` hold one step each (round-robin over
+    the cache copies); `round_graph`, if given, holds round_steps(R) steps, one
+    on each copy in turn (as a model's graph holds many layers' steps), and is
+    replayed for whole rounds, the single-step graphs for the rest."""
     import torch
-    for i in range(warmup):
-        graphs[i % len(graphs)].replay()
+    R = len(graphs)
+    RS = round_steps(R)
+    def run(n):
+        if round_graph is not None:
+            for _ in range(n // RS):
+                round_graph.replay()
+            for i in range(n % RS):
+                graphs[i % R].replay()
+        else:
+            for i in range(n):
+                graphs[i % R].replay()
+    run(warmup)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda._sleep(int(2e6 + 2e5 * steps))
     e0.record()
-    for i in range(steps):
-        graphs[i % len(graphs)].replay()
+    run(steps)
     e1.record()
     e1.synchronize()
     return e0.elapsed_time(e1) / steps
@@ -320,6 +332,19 @@ def isolated_replay_us(graph, reps: int) -> float:
         b.synchronize()
         times.append(a.elapsed_time(b) * 1e3)
     return statistics.median(times)
+
+
+def round_steps(R: int) -> int:
+    """Steps in a round graph: whole passes over the R cache copies, about 16."""
+    return R * max(1, 16 // R)
+
+
+def capture_round(step, R: int, dev):
+    """One CUDA graph holding round_steps(R) steps, on copies 0, 1, ..., R - 1, 0, ..."""
+    def all_steps():
+        for i in range(round_steps(R)):
+            step(i % R)
+    return capture(all_steps, dev)
 
 
 def capture(fn, dev):
@@ -388,18 +413,21 @@ def measure_shape(kvd, dev, w, steps: int, warmup: int, l2: int, peak: float, la
         step(i % R)
     torch.cuda.synchronize()
     graphs = [capture(lambda r=r: step(r), dev) for r in range(R)]
+    round_graph = capture_round(step, R, dev)
     res = {"batch": B, "n_heads_q": Hq, "n_heads_kv": Hkv, "head_dim": D,
            "context": [int(lens_np.min()), int(lens_np.max())], "n_split": n_split, "step_bytes": int(step_bytes)}
     if latency:
         res["latency_us"] = round(isolated_replay_us(graphs[0], 50), 3)
-    ms = time_replays(graphs, steps, warmup)
+    ms = time_replays(graphs, steps, warmup, round_graph)
+    ms_one = time_replays(graphs, steps, warmup)
     chunk_ms = time_chunk(kvd, lambda r: (kcs[r], vcs[r]), R, steps, q, kn, vn, pos, lens, S, w.scale, out, ws)
     gbs = step_bytes / (ms * 1e-3) / 1e9
     achieved = step_bytes / (chunk_ms * 1e-3) / 1e9
     res.update({"ms_per_step": round(ms, 5), "gbs": round(gbs, 1), "hbm_frac_of_step": round(gbs / peak, 4),
                 "tokens_per_s": round(B / (ms * 1e-3), 1), "kernel_ms": round(chunk_ms, 5),
-                "roofline_frac": round(achieved / peak, 4), "copies_rotated": R})
-    del kcs, vcs, graphs
+                "roofline_frac": round(achieved / peak, 4), "copies_rotated": R,
+                "ms_per_step_one_step_graphs": round(ms_one, 5)})
+    del kcs, vcs, graphs, round_graph
     torch.cuda.empty_cache()
     return res
 
@@ -456,12 +484,13 @@ def measure_long_trials(kvd, dev, steps: int, warmup: int, l2: int, peak: float)
                 step(j % R)
             torch.cuda.synchronize()
             graphs = [capture(lambda r=r: step(r), dev) for r in range(R)]
-        ms = time_replays(graphs, steps, warmup)
+            round_graph = capture_round(step, R, dev)
+        ms = time_replays(graphs, steps, warmup, round_graph)
         nbytes = roofline.attention_step_bytes(L, Hq, Hkv, D)
         gbs = nbytes / (ms * 1e-3) / 1e9
         trials.append({"trial": i, "tokens": int(L.sum()), "ms_per_step": round(ms, 5), "gbs": round(gbs, 1),
                        "hbm_frac_of_step": round(gbs / peak, 4)})
-    del kcs, vcs, graphs
+    del kcs, vcs, graphs, round_graph
     torch.cuda.empty_cache()
     fr = [t["hbm_frac_of_step"] for t in trials]
     return {"n_split": n_split, "trials": trials, "hbm_frac_of_step_median": round(statistics.median(fr), 4),
@@ -589,7 +618,9 @@ def run_ours(args):
         step(i % R)
     torch.cuda.synchronize()
 
-    # CUDA graphs: one per cache copy, replayed round-robin in the timed region.
+    # CUDA graphs: one per cache copy, and one round graph holding a step on
+    # every copy in turn (as a model's graph holds many layers' steps), replayed
+    # back to back in the timed region (single-step graphs for a partial round).
     graphs = []
     cap_stream = torch.cuda.Stream(device=dev)
     for r in range(R):
@@ -597,9 +628,21 @@ def run_ours(args):
         with torch.cuda.graph(g, stream=cap_stream):
             step(r)
         graphs.append(g)
+    RS = round_steps(R)
+    round_graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(round_graph, stream=cap_stream):
+        for i in range(RS):
+            step(i % R)
     for g in graphs:
         g.replay()
+    round_graph.replay()
     torch.cuda.synchronize()
+
+    def run_steps(n):
+        for _ in range(n // RS):
+            round_graph.replay()
+        for i in range(n % RS):
+            graphs[i % R].replay()
 
     def barrier():
         if world > 1:
@@ -610,21 +653,29 @@ def run_ours(args):
     sampler = ClockSampler(local_rank)
     ev0 = torch.cuda.Event(enable_timing=True)
     ev1 = torch.cuda.Event(enable_timing=True)
-    for i in range(args.warmup):
-        graphs[i % R].replay()
+    run_steps(args.warmup)
     barrier()
     torch.cuda.synchronize()
     # Queue the timed replays behind a spin kernel, so that the GPU never waits
     # for the host to launch the next step inside the timed region.
     torch.cuda._sleep(int(2e6 + 2e5 * args.steps))
     ev0.record()
-    for i in range(args.steps):
-        graphs[i % R].replay()
+    run_steps(args.steps)
     ev1.record()
     ev1.synchronize()
     torch.cuda.synchronize()
     barrier()
     total_ms = ev0.elapsed_time(ev1)
+    # For comparison: the same steps as one graph launch each (adds the gap
+    # between graph launches to every step).
+    e_a, e_b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(int(2e6 + 2e5 * args.steps))
+    e_a.record()
+    for i in range(args.steps):
+        graphs[i % R].replay()
+    e_b.record()
+    e_b.synchronize()
+    one_step_graphs_ms = e_a.elapsed_time(e_b) / args.steps
 
     # ---- chunk-kernel durations: events around each launch on its stream ----
     stream = torch.cuda.current_stream()
@@ -815,7 +866,10 @@ def run_ours(args):
         "config": bench_config(w, B, Hq, Hkv, D, lens_np, args),
         "n_split": n_split,
         "l2_detail": f"{R} rotating KV-cache copies ({R * kv_bytes / 1e6:.0f} MB of K/V rows vs {l2 / 1e6:.0f} MB L2)",
-        "timing": "CUDA graph per step, CUDA events on the replay stream",
+        "timing": (f"CUDA graphs of {round_steps(R)} steps, one on each rotating cache copy in turn "
+                   "(as a model's graph holds many layers' steps), replayed back to back; single-step "
+                   "graphs for a partial round; CUDA events on the replay stream"),
+        "ms_per_step_one_step_graphs": round(one_step_graphs_ms, 5),
         "tokens_per_s": round(tokens_per_s, 1),
         "hbm_frac_of_step": round(value / world / peak, 4),
         "step_bytes": int(step_bytes), "append_bytes": int(append_bytes), "flops": int(flops),
