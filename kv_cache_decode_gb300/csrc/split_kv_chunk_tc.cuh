@@ -743,8 +743,10 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR, KV8>::THREADS, 1)
             if (!ok) break;
             const uint8_t* src = smem + (r8 - sbase) + (size_t)s8 * Sh::TILE8_BYTES + src_off;
             uint8_t* dst = smem + (rf - sbase) + (size_t)sf * Sh::TILE_BYTES + dst_off;
-            // Step it of this thread: 8-bit rows NCT / 64 groups on (NCT / 64 KB
-            // a step), f16 rows likewise, 128-column blocks every 8 groups.
+            // Each step moves this thread NCT / 64 8-row groups further down the
+            // tile (1 KB of 8-bit rows a group); every 8 groups the 8-bit
+            // tile's next 128-column block starts, which in f16 is the next
+            // pair of 64-column blocks.
             constexpr int GPS = NCT / 64;  // 8-row groups a step
 #pragma unroll 4
             for (int it = 0; it < D * 4 / NCT; ++it) {
