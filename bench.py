@@ -589,14 +589,10 @@ def run_ours(args):
     else:
         n_split, ws_bytes = kvd.decode_plan(B, Hq, Hkv, D, max_len, 0, args.n_split, args.out_dtype)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
-    # The step's launches: the attention (which appends the new rows itself for a
-    # bf16 cache on the tensor-core kernel, groups of 17-64), else an append and
-    # the attention; then the merge when the context is split.
-    appends_inside = (not int8) and 17 <= Hq // Hkv <= 64
-    launches_per_step = (1 if appends_inside else 2) + (1 if n_split > 1 else 0)
+    launches_per_step = 2 + (1 if n_split > 1 else 0)
 
     def step(r, stream=None):
-        # append the new token's K/V rows, then attend (one call)
+        # append the new token's K/V rows, then attend (one call, three launches)
         if multi:
             kvd.decode_step_multi(q, kcs[r], vcs[r], kn, vn, pos, lens, max_len, w.scale, out, workspace=ws,
                                   n_split=args.n_split, stream=stream)
