@@ -168,11 +168,7 @@ kvd_status kvd_decode_attention(const void* q, const void* k_cache, const void* 
  * has finished, and waits for the append only before loading cache rows. So
  * q, seq_lens and pos must be complete when this call's work starts on the
  * stream (as for any stream-ordered input), and only the cache rows may be
- * produced by the append. For a bf16 cache on the tensor-core kernel (groups
- * of 17 to 64 query heads per KV head) there is no separate append launch:
- * the attention kernel writes each new row just before the tile that holds
- * it is loaded (rows no tile reads, by then or at all, are written too), with
- * the same cache contents and status bits as the two calls.
+ * produced by the append.
  */
 kvd_status kvd_decode_step(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
                            const int32_t* pos, const void* q, const int32_t* seq_lens, int batch,

@@ -293,15 +293,7 @@ kvd_status decode(int phase, const void* q, const void* k_cache, const void* v_c
     }
     cudaStream_t s = static_cast<cudaStream_t>(stream);
 
-    // bf16 cache on the tcgen05 kernel, inputs on the device: the attention
-    // launch appends the new rows itself (no separate append launch before it).
-    const bool fused = app && !q8 && k->tensor_core && app->copy_bytes == 0 && (phase & kChunk);
-    if (fused) {
-        p.fused = 1;
-        p.k_new = app->k_new;
-        p.v_new = app->v_new;
-        p.pos = app->pos;
-    } else if (app) {
+    if (app) {
         int copy_sms = 0;
         if (app->copy_bytes > 0 && device_sms(&copy_sms) != KVD_OK) return KVD_ERR_CUDA;
         // The append, then the chunk kernel in early mode: it starts (and works

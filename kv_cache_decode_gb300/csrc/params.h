@@ -49,14 +49,6 @@ struct DecodeParams {
     // first seq_lens[b] - T + 1 + i tokens, and the workspace holds T * G rows
     // per slot.
     int T;
-    // Append inside the attention (tcgen05 bf16 kernel, kvd_decode_step): the
-    // new rows k_new / v_new [B, T, Hkv, D] of each sequence go to pos[b] ..
-    // pos[b] + T - 1 (T the query tokens per real sequence), written by the CTA
-    // whose tile holds them just before that tile's loads, or, for rows no
-    // tile reads, by the CTA of their pair's index modulo the grid. 0 otherwise.
-    int fused;
-    const void* k_new;
-    const void* v_new;
     // mma.sync kernel: blocks of 16 of a pair's T * G rows, one CTA each per
     // token run (n_split * row_blocks CTAs); 1 for the tcgen05 kernel.
     int row_blocks;

@@ -381,178 +381,106 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR, KV8>::THREADS, 1)
     memcpy(&walker, s_walker, sizeof(WalkerT));
     const bool has_work = s_has_work != 0;
 
-    // Append inside the attention (p.fused, bf16 cache): row i of k_new (or
-    // v_new) for real sequence b and KV head h goes to the cache row of token
-    // r, copied in 16-byte pieces by the calling warp's lanes. As the append
-    // kernel: a block-table entry naming no page skips the row and flags it.
-    auto append_row = [&](bool to_k, int b, int i, int TA, int h, int r) {
-        size_t row;
-        if (p.block_table) {
-            const int page = __ldg(p.block_table + (size_t)b * p.max_blocks + (r >> p.page_shift));
-            if ((unsigned)page >= (unsigned)p.num_pages) {
-                if (to_k && lane == 0 && p.status) atomicOr(p.status, KVD_STATUS_BAD_PAGE);
-                return;
-            }
-            row = ((size_t)page << p.page_shift) + (size_t)(r & ((1 << p.page_shift) - 1));
-        } else {
-            row = (size_t)b * p.S_max + r;
-        }
-        const uint4* src = reinterpret_cast<const uint4*>(to_k ? p.k_new : p.v_new) +
-                           (((size_t)b * TA + i) * p.Hkv + h) * (D / 8);
-        uint4* dst = reinterpret_cast<uint4*>(const_cast<void*>(to_k ? p.k : p.v)) + (row * p.Hkv + h) * (D / 8);
-        for (int c2 = lane; c2 < D / 8; c2 += 32) dst[c2] = __ldg(src + c2);
-    };
-    if (!KV8 && p.fused && warp == 3) {
-        // The new rows no tile of this launch reads (tokens at or past the
-        // pair's clamped length; positions outside the cache are flagged and
-        // skipped, as the append kernel does), for the pairs whose index is
-        // this CTA's modulo the grid, K and V, by the first softmax warp (idle
-        // until the first scores arrive). Rows a tile reads are appended by
-        // the producer that loads that tile, just before its loads.
-        const int TA = (MR == 128) ? p.T : vt;
-        const int Breal = p.B / vt;
-        for (int pr = c; pr < Breal * p.Hkv; pr += (int)gridDim.x) {
-            const int b = pr / p.Hkv, h = pr - b * p.Hkv;
-            const int pos0 = __ldg(p.pos + b);
-            const int L = clamp_len(__ldg(p.seq_lens + b), p.len_cap);
-            for (int i = 0; i < TA; ++i) {
-                const int r = pos0 + i;
-                if (r < 0 || r >= p.S_max) {
-                    if (h == 0 && lane == 0 && p.status) atomicOr(p.status, KVD_STATUS_POS_OUT_OF_RANGE);
-                } else if (r >= L) {
-                    append_row(true, b, i, TA, h, r);
-                    append_row(false, b, i, TA, h, r);
-                }
-            }
-        }
-    }
-
     if (!has_work) {
         // no tokens for this CTA: fall through to the common exit (TMEM release)
     } else if (warp == 0 || warp == 2) {
         // ===================== TMA producers =====================
-        // Lane 0 waits for the stages and issues the loads; with the append
-        // fused in (p.fused), the whole warp first copies the new rows a tile
-        // holds into the cache (K by warp 0, V by warp 2), and a proxy fence
-        // orders those stores before the tile's TMA reads.
-        const bool is_k = (warp == 0);
-        const uint64_t pol_kv = l2_evict_first_policy();
-        Tile t;
-        int j = 0;
-        // KV8: the 8-bit rings (128-column boxes of one-byte codes).
-        const int NS = KV8 ? (is_k ? K8ST : V8ST) : (is_k ? KST : VST);
-        const CUtensorMap* map = is_k ? &maps.k : &maps.v;
-        constexpr int NBOX = KV8 ? Sh::KB8 : KB, BOXC = KV8 ? 128 : 64;
-        constexpr uint32_t STAGE = KV8 ? Sh::TILE8_BYTES : Sh::TILE_BYTES;
-        auto full_of = [&](int s2) { return KV8 ? (is_k ? k8_full(s2) : v8_full(s2)) : (is_k ? k_full(s2) : v_full(s2)); };
-        auto empty_of = [&](int s2) {
-            return KV8 ? (is_k ? k8_empty(s2) : v8_empty(s2)) : (is_k ? k_empty(s2) : v_empty(s2));
-        };
-        const uint32_t ring = KV8 ? (is_k ? sK8 : sV8) : (is_k ? sK : sV);
-        // Early mode: only tiles holding a pair's appended rows (those from
-        // pos on) wait for the append's grid; tiles before them stream
-        // meanwhile. pos is an input (complete at launch), read once per
-        // pair until the first wait.
-        bool waited = !p.early;
-        int pos_pair = -1, pos_b = -1;
-        const bool paged = p.block_table != nullptr;
-        const int box_rows = paged ? min(1 << p.page_shift, T) : T;
-        const bool fused = !KV8 && p.fused;
-        if ((!waited || fused) && walker.b < p.B) {  // issued now, first used at the first tile
-            pos_pair = walker.b * p.Hkv + walker.h;
-            pos_b = __ldg(p.pos + walker.b / vt);
-        }
-        while (walker.next(t, NoOp{})) {
-            // Paged cache: the tile's block-table entries (one per box of
-            // box_rows tokens, at most T / 16), loaded together before the
-            // wait for the stage, so that their latency overlaps it.
-            int entry[T / 16];
-            if (paged && lane == 0) {
-                const int32_t* table = p.block_table + (size_t)(t.b / vt) * p.max_blocks;
+        if (lane == 0) {
+            const bool is_k = (warp == 0);
+            const uint64_t pol_kv = l2_evict_first_policy();
+            Tile t;
+            int j = 0;
+            // KV8: the 8-bit rings (128-column boxes of one-byte codes).
+            const int NS = KV8 ? (is_k ? K8ST : V8ST) : (is_k ? KST : VST);
+            const CUtensorMap* map = is_k ? &maps.k : &maps.v;
+            constexpr int NBOX = KV8 ? Sh::KB8 : KB, BOXC = KV8 ? 128 : 64;
+            constexpr uint32_t STAGE = KV8 ? Sh::TILE8_BYTES : Sh::TILE_BYTES;
+            auto full_of = [&](int s2) { return KV8 ? (is_k ? k8_full(s2) : v8_full(s2)) : (is_k ? k_full(s2) : v_full(s2)); };
+            auto empty_of = [&](int s2) {
+                return KV8 ? (is_k ? k8_empty(s2) : v8_empty(s2)) : (is_k ? k_empty(s2) : v_empty(s2));
+            };
+            const uint32_t ring = KV8 ? (is_k ? sK8 : sV8) : (is_k ? sK : sV);
+            // Early mode: only tiles holding a pair's appended rows (those from
+            // pos on) wait for the append's grid; tiles before them stream
+            // meanwhile. pos is an input (complete at launch), read once per
+            // pair until the first wait.
+            bool waited = !p.early;
+            int pos_pair = -1, pos_b = -1;
+            const bool paged = p.block_table != nullptr;
+            const int box_rows = paged ? min(1 << p.page_shift, T) : T;
+            if (!waited && walker.b < p.B) {  // issued now, first used at the first tile
+                pos_pair = walker.b * p.Hkv + walker.h;
+                pos_b = __ldg(p.pos + walker.b / vt);
+            }
+            while (walker.next(t, NoOp{})) {
+                // Paged cache: the tile's block-table entries (one per box of
+                // box_rows tokens, at most T / 16), loaded together before the
+                // wait for the stage, so that their latency overlaps it.
+                int entry[T / 16];
+                if (paged) {
+                    const int32_t* table = p.block_table + (size_t)(t.b / vt) * p.max_blocks;
 #pragma unroll
-                for (int q = 0; q < T / 16; ++q) {
-                    const int tok = t.tok_lo + q * box_rows;
-                    entry[q] = (q * box_rows < T && tok < t.tok_hi) ? __ldg(table + (tok >> p.page_shift)) : -1;
-                }
-            }
-            if (!waited || fused) {
-                const int pair = t.b * p.Hkv + t.h;
-                if (pair != pos_pair) {
-                    pos_pair = pair;
-                    pos_b = __ldg(p.pos + t.b / vt);
-                }
-                if (!waited && t.tok_hi > pos_b && lane == 0) {
-                    pdl_wait();
-                    waited = true;
-                }
-            }
-            if (fused) {
-                // The new rows this tile holds: tokens pos .. pos + TA - 1 of
-                // the real sequence that lie in [tok_lo, tok_hi).
-                const int TA = (MR == 128) ? p.T : vt;
-                bool wrote = false;
-                for (int i = 0; i < TA; ++i) {
-                    const int r = pos_b + i;
-                    if (r >= t.tok_lo && r < t.tok_hi) {
-                        append_row(is_k, t.b / vt, i, TA, t.h, r);
-                        wrote = true;
+                    for (int q = 0; q < T / 16; ++q) {
+                        const int tok = t.tok_lo + q * box_rows;
+                        entry[q] = (q * box_rows < T && tok < t.tok_hi) ? __ldg(table + (tok >> p.page_shift)) : -1;
                     }
                 }
-                if (wrote) asm volatile("fence.proxy.async.global;\n" ::: "memory");
-                __syncwarp();
-            }
-            bool ok = true;
-            if (lane == 0) {
+                if (!waited) {
+                    const int pair = t.b * p.Hkv + t.h;
+                    if (pair != pos_pair) {
+                        pos_pair = pair;
+                        pos_b = __ldg(p.pos + t.b / vt);
+                    }
+                    if (t.tok_hi > pos_b) {
+                        pdl_wait();
+                        waited = true;
+                    }
+                }
                 const int s = j % NS;
                 const uint32_t full = full_of(s);
-                ok = tc::mbar_wait(empty_of(s), ((j / NS) & 1) ^ 1, abort_flag, kBudget);
-                if (ok) {
-                    tc::mbar_arrive_expect_tx(full, STAGE);
-                    const uint32_t dst = ring + (uint32_t)s * STAGE;
-                    if (!paged) {
-                        const int row = (t.b / vt) * p.S_max + t.tok_lo;
+                if (!tc::mbar_wait(empty_of(s), ((j / NS) & 1) ^ 1, abort_flag, kBudget)) break;
+                tc::mbar_arrive_expect_tx(full, STAGE);
+                const uint32_t dst = ring + (uint32_t)s * STAGE;
+                if (!paged) {
+                    const int row = (t.b / vt) * p.S_max + t.tok_lo;
+#pragma unroll
+                    for (int kb = 0; kb < NBOX; ++kb)
+                        tc::tma_load_3d(dst + kb * Sh::KB_BYTES, map, kb * BOXC, t.h, row, full, pol_kv);
+                } else {
+                    // Paged cache: the tile is fetched as boxes of box_rows
+                    // tokens (the page size, up to the tile), each from its
+                    // block's page. Tile rows are page-aligned (tiles start at
+                    // multiples of T within a sequence, and a page is at least
+                    // 16 tokens), so no box crosses a page. A box past the
+                    // tile's tokens, or whose table entry names no page, is
+                    // read from past the pool's end: zeros.
+                    const int oob = p.num_pages << p.page_shift;
+#pragma unroll
+                    for (int q = 0; q < T / 16; ++q) {
+                        const int r0 = q * box_rows;
+                        if (r0 >= T) break;
+                        const int tok = t.tok_lo + r0;
+                        int row = oob;
+                        if (tok < t.tok_hi) {
+                            const int page = entry[q];
+                            if ((unsigned)page < (unsigned)p.num_pages)
+                                row = (page << p.page_shift) + (tok & ((1 << p.page_shift) - 1));
+                            else if (is_k && p.status)
+                                atomicOr(p.status, KVD_STATUS_BAD_PAGE);
+                        }
 #pragma unroll
                         for (int kb = 0; kb < NBOX; ++kb)
-                            tc::tma_load_3d(dst + kb * Sh::KB_BYTES, map, kb * BOXC, t.h, row, full, pol_kv);
-                    } else {
-                        // Paged cache: the tile is fetched as boxes of box_rows
-                        // tokens (the page size, up to the tile), each from its
-                        // block's page. Tile rows are page-aligned (tiles start at
-                        // multiples of T within a sequence, and a page is at least
-                        // 16 tokens), so no box crosses a page. A box past the
-                        // tile's tokens, or whose table entry names no page, is
-                        // read from past the pool's end: zeros.
-                        const int oob = p.num_pages << p.page_shift;
-#pragma unroll
-                        for (int q = 0; q < T / 16; ++q) {
-                            const int r0 = q * box_rows;
-                            if (r0 >= T) break;
-                            const int tok = t.tok_lo + r0;
-                            int row = oob;
-                            if (tok < t.tok_hi) {
-                                const int page = entry[q];
-                                if ((unsigned)page < (unsigned)p.num_pages)
-                                    row = (page << p.page_shift) + (tok & ((1 << p.page_shift) - 1));
-                                else if (is_k && p.status)
-                                    atomicOr(p.status, KVD_STATUS_BAD_PAGE);
-                            }
-#pragma unroll
-                            for (int kb = 0; kb < NBOX; ++kb)
-                                tc::tma_load_3d(dst + kb * Sh::KB_BYTES + r0 * 128, map, kb * BOXC, t.h, row, full,
-                                                pol_kv);
-                        }
+                            tc::tma_load_3d(dst + kb * Sh::KB_BYTES + r0 * 128, map, kb * BOXC, t.h, row, full, pol_kv);
                     }
                 }
+                ++j;
             }
-            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
-            ++j;
-        }
-        // Do not leave with copies in flight: wait for the last loads to land.
-        if (lane == 0)
+            // Do not leave with copies in flight: wait for the last loads to land.
             for (int jj = (j > NS ? j - NS : 0); jj < j; ++jj) {
                 const int s = jj % NS;
                 tc::mbar_wait(full_of(s), (jj / NS) & 1, abort_flag, kBudget / 4);
             }
+        }
     } else if (warp == 9) {
         // ===================== Q loader =====================
         // Its own thread, so that waiting for the Q slot (free once the previous
