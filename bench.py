@@ -295,16 +295,9 @@ def time_replays(graphs, steps: int, warmup: int, round_graph=None) -> float:
     replayed for whole rounds, the single-step graphs for the rest."""
     import torch
     R = len(graphs)
-    RS = round_steps(R)
     def run(n):
-        if round_graph is not None:
-            for _ in range(n // RS):
-                round_graph.replay()
-            for i in range(n % RS):
-                graphs[i % R].replay()
-        else:
-            for i in range(n):
-                graphs[i % R].replay()
+        for g in replay_plan(n, R, round_graph is not None):
+            (round_graph if g == "round" else graphs[g]).replay()
     run(warmup)
     torch.cuda.synchronize()
     e0 = torch.cuda.Event(enable_timing=True)
@@ -337,6 +330,17 @@ def isolated_replay_us(graph, reps: int) -> float:
 def round_steps(R: int) -> int:
     """Steps in a round graph: whole passes over the R cache copies, about 16."""
     return R * max(1, 16 // R)
+
+
+def replay_plan(n: int, R: int, use_round: bool = True):
+    """The graphs replayed for n steps, in order: "round" for a round graph
+    (round_steps(R) steps, copies 0, 1, ..., R - 1, 0, ...), an int r for the
+    single-step graph on copy r. The steps add up to exactly n, and the cache
+    copies follow each other round-robin from copy 0."""
+    RS = round_steps(R) if use_round else 1
+    if not use_round:
+        return [i % R for i in range(n)]
+    return ["round"] * (n // RS) + [i % R for i in range(n % RS)]
 
 
 def capture_round(step, R: int, dev):
@@ -639,10 +643,8 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     def run_steps(n):
-        for _ in range(n // RS):
-            round_graph.replay()
-        for i in range(n % RS):
-            graphs[i % R].replay()
+        for g in replay_plan(n, R):
+            (round_graph if g == "round" else graphs[g]).replay()
 
     def barrier():
         if world > 1:
