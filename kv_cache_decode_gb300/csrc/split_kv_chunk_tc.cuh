@@ -144,6 +144,40 @@ struct TcMaps {
     CUtensorMap v;
 };
 
+// A paged tile's TMA loads: boxes of box_rows tokens (the page size, up to the
+// tile), each from its block's page (entries e0..e3 of the block table, one
+// per box). Tile rows are page-aligned (tiles start at multiples of T within a
+// sequence, and a page is at least 16 tokens), so no box crosses a page. A
+// box past the tile's tokens, or whose entry names no page, is read from past
+// the pool's end: zeros (and flagged in *status when status is given). Kept
+// out of line: a contiguous cache never calls it, so its code stays out of
+// the kernel's instruction stream.
+template <int NBOX, int BOXC, int KB_BYTES, int T>
+__device__ __noinline__ void tma_paged_tile(uint32_t dst, const CUtensorMap* map, int h, int tok_lo, int tok_hi,
+                                            int e0, int e1, int e2, int e3, int box_rows, int page_shift,
+                                            int num_pages, uint32_t full, uint64_t pol, int32_t* status) {
+    static_assert(T / 16 == 4, "four boxes at most");
+    const int entry[4] = {e0, e1, e2, e3};
+    const int oob = num_pages << page_shift;
+#pragma unroll
+    for (int q = 0; q < T / 16; ++q) {
+        const int r0 = q * box_rows;
+        if (r0 >= T) break;
+        const int tok = tok_lo + r0;
+        int row = oob;
+        if (tok < tok_hi) {
+            const int page = entry[q];
+            if ((unsigned)page < (unsigned)num_pages)
+                row = (page << page_shift) + (tok & ((1 << page_shift) - 1));
+            else if (status)
+                atomicOr(status, KVD_STATUS_BAD_PAGE);
+        }
+#pragma unroll
+        for (int kb = 0; kb < NBOX; ++kb)
+            tc::tma_load_3d(dst + kb * KB_BYTES + r0 * 128, map, kb * BOXC, h, row, full, pol);
+    }
+}
+
 template <int D, bool F32OUT, int QR, int MR, bool KV8 = false, bool FP8 = false>
 __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR, KV8>::THREADS, 1)
     split_kv_chunk_tc_kernel(const DecodeParams p, const __grid_constant__ TcMaps maps) {
@@ -447,31 +481,9 @@ __global__ void __launch_bounds__(TcShape<D, F32OUT, QR, MR, KV8>::THREADS, 1)
                     for (int kb = 0; kb < NBOX; ++kb)
                         tc::tma_load_3d(dst + kb * Sh::KB_BYTES, map, kb * BOXC, t.h, row, full, pol_kv);
                 } else {
-                    // Paged cache: the tile is fetched as boxes of box_rows
-                    // tokens (the page size, up to the tile), each from its
-                    // block's page. Tile rows are page-aligned (tiles start at
-                    // multiples of T within a sequence, and a page is at least
-                    // 16 tokens), so no box crosses a page. A box past the
-                    // tile's tokens, or whose table entry names no page, is
-                    // read from past the pool's end: zeros.
-                    const int oob = p.num_pages << p.page_shift;
-#pragma unroll
-                    for (int q = 0; q < T / 16; ++q) {
-                        const int r0 = q * box_rows;
-                        if (r0 >= T) break;
-                        const int tok = t.tok_lo + r0;
-                        int row = oob;
-                        if (tok < t.tok_hi) {
-                            const int page = entry[q];
-                            if ((unsigned)page < (unsigned)p.num_pages)
-                                row = (page << p.page_shift) + (tok & ((1 << p.page_shift) - 1));
-                            else if (is_k && p.status)
-                                atomicOr(p.status, KVD_STATUS_BAD_PAGE);
-                        }
-#pragma unroll
-                        for (int kb = 0; kb < NBOX; ++kb)
-                            tc::tma_load_3d(dst + kb * Sh::KB_BYTES + r0 * 128, map, kb * BOXC, t.h, row, full, pol_kv);
-                    }
+                    tma_paged_tile<NBOX, BOXC, Sh::KB_BYTES, T>(dst, map, t.h, t.tok_lo, t.tok_hi, entry[0], entry[1],
+                                                                entry[2], entry[3], box_rows, p.page_shift,
+                                                                p.num_pages, full, pol_kv, is_k ? p.status : nullptr);
                 }
                 ++j;
             }
